@@ -1,0 +1,308 @@
+"""Pins for the CPU oracle: each check ties a function of oracle/nosa_oracle.py to
+something other than itself -- hand-computed values from the pages' rules, closed
+forms, invariants (Theorem 2), brute force on tiny inputs, or a library routine
+(torch's bf16 conversion and scaled-dot-product attention) in a special case."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import nosa_oracle as O
+from synth import inputs as syn
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load_rows(name):
+    rows = []
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line)
+    return rows
+
+
+# ----------------------------------------------------------------------------- bf16
+def test_bf16_round_hand_values():
+    # ulp of bf16 at 1.0 is 2^-7; halfway cases go to the even mantissa
+    cases = {1 + 2 ** -8: 1.0, 1 + 3 * 2 ** -8: 1 + 2 ** -6, 1 + 2 ** -9: 1.0,
+             -(1 + 2 ** -8): -1.0, 1 + 2 ** -8 + 2 ** -20: 1 + 2 ** -7,
+             3 * 2 ** -135: 2 ** -133, 0.0: 0.0, 255.5: 256.0, 254.5: 254.0}
+    for x, want in cases.items():
+        assert O.bf16_round(x) == want, (x, O.bf16_round(x), want)
+
+
+def test_bf16_round_matches_torch_on_float32_inputs():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.bf16_round(x.astype(np.float64)), want)
+
+
+# ----------------------------------------------------------------------------- CompressK
+def test_compress_keys_ramp_fixture():
+    want = [float(v) for v in _load_rows("compress_ramp.txt")[0].split()]
+    K = np.repeat(np.arange(96, dtype=np.float64)[:, None], 128, axis=1)
+    Kt = O.compress_keys(K)
+    assert Kt.shape == (5, 128)
+    assert np.array_equal(Kt[:, 0], want) and np.all(Kt == Kt[:, :1])
+    # the eviction score is mean-pooled over the same windows (eq. 5)
+    assert np.array_equal(O.window_means(np.arange(96, dtype=np.float64)), want)
+
+
+def test_compress_keys_rounds_exact_mean_to_even():
+    # 31 ones and one 1.125: mean 1 + 2^-8, halfway -> 1.0 ; with 1.375: 1 + 3*2^-8 -> 1 + 2^-6
+    for extra, want in [(1.125, 1.0), (1.375, 1 + 2 ** -6), (1.0078125, 1.0)]:
+        K = np.ones((32, 4))
+        K[7] = extra
+        assert O.compress_keys(K)[0, 0] == want
+
+
+def test_compressed_keys_are_one_sixteenth_of_K():
+    c = json.load(open(os.path.join(GOLD, "page_constants.json")))
+    for T in (4096, 16384, 65536):
+        assert O.num_windows(T) == (T - 32) // 16 + 1
+        assert abs(O.num_windows(T) / T - c["compressed_key_fraction"]) < 32 / T
+    assert O.num_windows(31) == 0 and O.num_windows(32) == 1 and O.num_windows(47) == 1
+    assert O.num_windows(48) == 2
+
+
+# ----------------------------------------------------------------------------- eviction head
+def test_eviction_score_closed_forms():
+    d, h = 8, 6
+    rng = np.random.default_rng(2)
+    W1 = rng.standard_normal((d, h))
+    W2 = rng.standard_normal(h)
+    # one-hot v picks one row of W1
+    for c in range(d):
+        v = np.zeros((1, d)); v[0, c] = 1.0
+        want = sum(W2[m] * math.log1p(math.exp(W1[c, m])) for m in range(h))
+        assert abs(O.eviction_scores(v, W1, W2)[0] - want) < 1e-12
+    # softplus(0) = ln 2
+    assert abs(O.eviction_scores(np.ones((1, d)), np.zeros((d, h)), W2)[0] - math.log(2) * W2.sum()) < 1e-12
+
+
+def test_eviction_score_hand_case_catches_transpose():
+    W1 = np.array([[1.0, -1.0], [0.0, 2.0]])
+    W2 = np.array([1.0, 0.5])
+    # v W1 = [1, 1]; softplus(1) = ln(1 + e) = 1.3132616875182228; times (1 + 0.5)
+    assert abs(O.eviction_scores(np.array([[1.0, 1.0]]), W1, W2)[0] - 1.9698925312773342) < 1e-14
+    # large arguments do not overflow: softplus(x) -> x
+    assert abs(O.softplus(800.0) - 800.0) < 1e-12 and O.softplus(-800.0) >= 0.0
+
+
+# ----------------------------------------------------------------------------- pooling
+def test_window_block_overlap_fixture():
+    m = O.window_block_overlap(16, O.num_windows(1024))
+    for row in _load_rows("pool_windows.txt"):
+        b, ws = row.split(":")
+        assert list(np.nonzero(m[int(b)])[0]) == [int(w) for w in ws.split()]
+    # closed form 4b-1 .. 4b+3 for every interior block
+    for b in range(1, 15):
+        assert list(np.nonzero(m[b])[0]) == list(range(4 * b - 1, 4 * b + 4))
+
+
+def test_block_pool_is_max_over_overlapping_windows():
+    s = np.arange(63, dtype=np.float64)[::-1] * 0.5  # decreasing: max is the first window
+    pooled = O.block_pool(s, 16)
+    assert pooled[0] == s[0] and pooled[1] == s[3] and pooled[5] == s[19] and pooled[15] == s[59]
+    # a block past the last complete window pools nothing
+    assert O.block_pool(np.array([1.0]), 2)[1] == -np.inf
+
+
+# ----------------------------------------------------------------------------- query score
+def test_query_scores_group_softmax_invariants():
+    rng = np.random.default_rng(3)
+    Kt = rng.standard_normal((40, 16))
+    Q = rng.standard_normal((4, 16))
+    s = O.query_scores(Q, Kt, 0.25)
+    assert abs(s.sum() - 4.0) < 1e-12          # each head's softmax sums to one
+    assert np.all(s > 0)
+    # G = 1: the softmax is monotone, so the ranking is the ranking of raw dot products
+    s1 = O.query_scores(Q[:1], Kt, 0.25)
+    assert np.array_equal(np.argsort(-s1, kind="stable"), np.argsort(-(Kt @ Q[0]), kind="stable"))
+
+
+def test_query_score_on_mean_key_equals_mean_of_token_scores():
+    # The explainer's form pools token scores q.k_j; with unrounded mean keys it is the same number.
+    rng = np.random.default_rng(4)
+    K = rng.standard_normal((160, 16))
+    q = rng.standard_normal(16)
+    nc = O.num_windows(160)
+    kbar = np.stack([K[16 * i:16 * i + 32].mean(0) for i in range(nc)])
+    token_form = np.array([(K[16 * i:16 * i + 32] @ q).mean() for i in range(nc)])
+    assert np.max(np.abs(kbar @ q - token_form)) < 1e-12
+
+
+# ----------------------------------------------------------------------------- selection
+def _best_subset_by_sum(scores, eligible, k):
+    """Brute force: with distinct scores the top-k set is the k-subset of largest sum."""
+    k = min(k, len(eligible))
+    best, arg = -np.inf, None
+    for sub in itertools.combinations(eligible, k):
+        v = sum(float(scores[b]) for b in sub)
+        if v > best:
+            best, arg = v, sorted(sub)
+    return arg if arg is not None else []
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_selection_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    nb = int(rng.integers(6, 13))
+    nw = int(rng.integers(1, 3))
+    k_q, k_e = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+    sq = rng.permutation(nb).astype(np.float64) + 0.5    # distinct, exact in float32
+    se = rng.permutation(nb).astype(np.float64) - 3.0
+    _, C, _ = O.partition(nb * 64, nw)
+    evicted = {b for b in C if rng.random() < 0.3}
+    Q = O.select_query_aware(sq, C, k_q)
+    assert Q == _best_subset_by_sum(sq, C, k_q)
+    E = O.select_query_agnostic(se, C, Q, evicted, k_e)
+    eligible = [b for b in C if b not in Q and b not in evicted]
+    assert E == _best_subset_by_sum(se, eligible, k_e)
+    assert not (set(E) & evicted) and not (set(E) & set(Q))
+
+
+def test_selection_ties_go_to_lower_block():
+    sq = np.zeros(10)
+    assert O.select_query_aware(sq, list(range(1, 8)), 3) == [1, 2, 3]
+    se = np.array([0, 5, 5, 1, 5, 5, 0, 0, 0, 0], dtype=np.float64)
+    assert O.select_query_agnostic(se, list(range(1, 8)), [2], set(), 2) == [1, 4]
+
+
+def test_selection_decided_in_float32():
+    # two scores that differ only below float32 resolution tie, so the lower block wins
+    sq = np.array([0.0, 1.0 + 1e-12, 1.0, 0.0])
+    assert O.select_query_aware(sq, [1, 2], 1) == [1]
+    sq = np.array([0.0, 1.0, 1.0 + 1e-12, 0.0])
+    assert O.select_query_aware(sq, [1, 2], 1) == [1]
+
+
+def test_partition_sink_window_candidates():
+    sink, C, win = O.partition(4097, 4)          # 65 blocks, last one partial
+    assert sink == [0] and win == [61, 62, 63, 64] and C == list(range(1, 61))
+    assert O.partition(64 * 3, 4) == ([0], [], [1, 2])
+    assert O.partition(1, 4) == ([0], [], [])
+
+
+# ----------------------------------------------------------------------------- a unit over many steps
+def _run_unit(T0, steps, k_q, k_e, window, sigma, seed, G=2, d=32, kernel=32):
+    w = syn.Workload("t", 1, 1, G, 1, T0, k_q, k_e, window, steps, sigma=sigma, head_dim=d,
+                     evict_hidden=16, seed=seed)
+    x = w.unit_inputs(0, 0, 0)
+    u = O.UnitOracle(head_dim=d, k_q=k_q, k_e=k_e, window_tokens=window,
+                     max_context=T0 + steps, W1=x["W1"], W2=x["W2"])
+    u.append(x["K"][:T0], x["V"][:T0])
+    res = []
+    for t in range(steps):
+        p = T0 + t
+        res.append(u.step(x["Q"][t], x["K"][p:p + 1], x["V"][p:p + 1]))
+    return u, x, res
+
+
+@pytest.mark.parametrize("sigma,seed", [(0.3, 0), (1.0, 1), (3.0, 2)])
+def test_theorem2_locality_bound(sigma, seed):
+    k_q, k_e = 4, 12
+    _, _, res = _run_unit(2048, 70, k_q, k_e, 256, sigma, seed)
+    gammas = [r["gamma"] for r in res[1:]]
+    assert min(gammas) >= k_e / (k_q + k_e) - 1e-12
+    c = json.load(open(os.path.join(GOLD, "page_constants.json")))
+    k, kq = c["budget_tokens"] // 64, c["k_q_tokens"] // 64
+    assert (k - kq) / k == c["gamma_lower_bound"]
+
+
+def test_eviction_is_sticky_and_fetches_follow_the_set_difference():
+    k_q, k_e = 3, 6
+    u, x, res = _run_unit(1500, 90, k_q, k_e, 128, 1.0, 5)
+    dropped = set()
+    S_prev = []
+    for t, r in enumerate(res):
+        assert not (set(r["E"]) & dropped)                       # never re-selected by E
+        fetched = [b for b, _ in r["fetch"]]
+        assert fetched == sorted(set(r["S"]) - set(S_prev))      # exactly the new blocks
+        if t > 0:
+            assert len(set(r["D"]) - set(S_prev)) <= k_q         # only Q can bring new dynamic blocks
+        slots = r["slot_of"]
+        assert len(set(slots)) == len(slots) and max(slots) < u.cap
+        _, C, _ = O.partition(1500 + t + 1, 2)
+        dropped |= {b for b in C if b not in set(r["D"])}
+        S_prev = r["S"]
+    assert len(res[0]["fetch"]) == len(res[0]["S"])              # cold first step fetches all of S_1
+
+
+def test_budget_accounting_and_transfer_unit():
+    c = json.load(open(os.path.join(GOLD, "page_constants.json")))
+    bb = c["budget_blocks"]
+    assert bb["sink"] + bb["window"] + bb["dynamic"] == bb["total"] == c["budget_tokens"] // c["block_tokens"]
+    assert c["block_tokens"] * c["head_dim"] * 2 == c["block_transfer_bytes"]
+    _, _, res = _run_unit(3000, 10, 4, 8, 256, 0.3, 3)
+    # the query-agnostic part comes up short only when Q takes blocks it could have kept
+    assert res[0]["short"] == 0
+    for r in res:
+        assert len(r["S"]) == 1 + 4 + 4 + 8 - r["short"] and len(r["Q"]) == 4
+
+
+def test_k_e_zero_is_plain_top_k():
+    u, x, res = _run_unit(2000, 5, 6, 0, 128, 0.3, 4)
+    for r in res:
+        assert r["E"] == [] and r["D"] == r["Q"]
+        _, C, _ = O.partition(u.T, 2)
+        order = sorted(C, key=lambda b: (-np.float32(r["sq_blk"][b]), b))
+        assert r["Q"] == sorted(order[:6])
+
+
+# ----------------------------------------------------------------------------- attention
+def _sdpa(Q, K, V, scale, mask=None):
+    q = torch.from_numpy(Q)[None, :, None, :]
+    k = torch.from_numpy(K)[None, None].expand(1, Q.shape[0], -1, -1)
+    v = torch.from_numpy(V)[None, None].expand(1, Q.shape[0], -1, -1)
+    m = None if mask is None else torch.from_numpy(mask)[None, None, None, :]
+    return torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, scale=scale)[0, :, 0].numpy()
+
+
+def test_covering_budget_equals_dense_attention():
+    # k covers every candidate: S is every block and the output is dense decode attention
+    T0, d = 1000, 32
+    u, x, res = _run_unit(T0, 4, 20, 20, 128, 0.3, 6, d=d)
+    for t, r in enumerate(res):
+        T = T0 + t + 1
+        assert r["S"] == list(range(O.num_blocks(T)))
+        Qg = O.bf16_bits_to_f64(x["Q"][t])
+        K = O.bf16_bits_to_f64(x["K"][:T]); V = O.bf16_bits_to_f64(x["V"][:T])
+        assert np.max(np.abs(r["out"] - _sdpa(Qg, K, V, 1 / math.sqrt(d)))) < 1e-6
+
+
+def test_sparse_attention_equals_masked_dense():
+    rng = np.random.default_rng(7)
+    T, d = 700, 16
+    K, V = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    Q = rng.standard_normal((3, d))
+    S = [0, 2, 5, 10]
+    mask = np.zeros(T, bool)
+    for b in S:
+        mask[64 * b: min(64 * b + 64, T)] = True
+    got = O.sparse_attention(Q, K, V, S, T, 0.3)
+    assert np.max(np.abs(got - _sdpa(Q, K, V, 0.3, mask))) < 1e-12
+
+
+def test_assign_slots_pairs_ascending():
+    fetch, m, where = O.assign_slots([0, 3, 4, 9], [3, -1, 7, 0, 8])
+    # slot 2 (block 7) and 4 (block 8) are freed; free slots 1, 2, 4; new blocks 4, 9
+    assert fetch == [(4, 1), (9, 2)] and m == [3, 4, 9, 0, -1] and where == [3, 0, 1, 2]
+
+
+# ----------------------------------------------------------------------------- inputs
+def test_synthetic_inputs_are_counter_based():
+    a = syn.normals(0, syn.T_K, 1, 2, 3, 1001, 77)
+    b = syn.normals(0, syn.T_K, 1, 2, 3, 1000, 100)[1:78]
+    assert np.array_equal(a, b)
+    z = syn.normals(0, syn.T_V, 0, 0, 0, 0, 1 << 18)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1) < 0.01
+    q = O.bf16_bits_to_f64(syn.query_walk(0, 0, 0, 0, 4, 128, 0.3))
+    assert np.allclose(np.linalg.norm(q, axis=1), math.sqrt(128), rtol=1e-2)
