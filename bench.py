@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Decode throughput of the NOSA attention path on GB300.
+
+A step is one decode step of the whole attention stack: for every layer,
+append the new token (host store + cache slot, eviction score, compressed
+key), score and select blocks, gather the newly selected blocks from pinned
+host memory, and attend over the selection -- all in libnosa.so kernels.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
+
+N > 1 runs under torchrun with one process per GPU; every rank serves its own
+batch (independent sequences, no collective on the data path: weak scaling).
+Inputs are synthetic (seeded), shaped like the workload; the full K/V context
+lives in pinned host memory before timing starts.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s (attn path, 1 GB300) + % HBM roofline and % PCIe H2D BW for fetch"
+BLOCK_BYTES = 32768
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="nosa1b_16k_b8")
+    ap.add_argument("--sigma", type=float, default=None)
+    ap.add_argument("--k-q", type=int, default=None)
+    ap.add_argument("--gather-ctas", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers (only for host-memory limits)")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="timed graph leg only (profiling runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- helpers
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def h2d_peak(torch, nbytes=1 << 30, reps=6):
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        d.copy_(h, non_blocking=True)
+        e.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (s.elapsed_time(e) * 1e-3) / 1e9)
+    del h, d
+    return best
+
+
+def oracle_baseline(wl, seconds, total_units):
+    """Time the CPU oracle on a bounded sample of the workload (a few units' decode steps)."""
+    from oracle import nosa_oracle as O
+    from synth import inputs as syn
+    samples = []
+    lbg = [(0, 0, 0), (wl.layers - 1, wl.batch - 1, wl.kv_heads - 1)]
+    for (l, b, g) in lbg:
+        x = wl.unit_inputs(l, b, g)
+        o = O.UnitOracle(head_dim=wl.head_dim, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
+                         window_tokens=wl.window_tokens, max_context=wl.max_context, W1=x["W1"], W2=x["W2"])
+        o.append(x["K"][:wl.context], x["V"][:wl.context])
+        samples.append((o, x))
+    n = 0
+    t0 = time.perf_counter()
+    t = 0
+    while time.perf_counter() - t0 < seconds and t < wl.steps:
+        for o, x in samples:
+            p = wl.context + t
+            o.step(x["Q"][t], x["K"][p:p + 1], x["V"][p:p + 1])
+            n += 1
+        t += 1
+    dt = time.perf_counter() - t0
+    per_unit = dt / max(n, 1)
+    value = wl.batch / (per_unit * total_units)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} unit-steps ({len(samples)} units x {t} decode steps) of {total_units} units/step, "
+                      f"{dt:.1f} s; numpy float64 with its default BLAS threading"}
+
+
+# ---------------------------------------------------------------------------- native arm
+def run_native(args, rank, world, local_rank):
+    import torch
+    from offloadable_block_sparse_gb300 import nosa as N
+    from synth import inputs as syn
+    torch.cuda.set_device(local_rank)
+    dev = "cuda"
+    over = {}
+    if args.sigma is not None:
+        over["sigma"] = args.sigma
+    if args.k_q is not None:
+        over["k_q"], over["k_e"] = args.k_q, 64 - args.k_q
+    wl = syn.workload(args.workload, **over)
+    L = args.layers or wl.layers
+    B, Hq, Hkv, d = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
+    U = B * Hkv
+    K, W = args.steps, args.warmup
+    n_time_leg = 0 if args.quick else min(K, 8)
+    n_e2e = 0 if args.quick else min(K, 8)
+    total_steps = 1 + W + K + n_time_leg + n_e2e
+    cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
+                        window_tokens=wl.window_tokens, max_context=wl.context + total_steps,
+                        sink_blocks=wl.sink_blocks, evict_hidden=wl.evict_hidden, gather_ctas=args.gather_ctas)
+    stream = torch.cuda.current_stream()
+    ctx = N.nosa_create(cfg, stream.cuda_stream)
+    sizes = N.nosa_query_sizes(cfg)
+    gen = torch.Generator(device=dev).manual_seed(1000 * rank + 7)
+    cgen = torch.Generator().manual_seed(1000 * rank + 11)
+    for l in range(L):
+        W1 = (torch.randn((Hkv, d, wl.evict_hidden), generator=cgen) / math.sqrt(d)).float().contiguous()
+        W2 = (torch.randn((Hkv, wl.evict_hidden), generator=cgen) / math.sqrt(wl.evict_hidden)).float().contiguous()
+        N.nosa_set_eviction_head(ctx, l, W1.numpy(), W2.numpy())
+        Kc = torch.randn((B, Hkv, wl.context, d), generator=gen, device=dev).to(torch.bfloat16)
+        Vc = torch.randn((B, Hkv, wl.context, d), generator=gen, device=dev).to(torch.bfloat16)
+        N.nosa_append_kv(ctx, l, Kc.view(torch.int16), Vc.view(torch.int16), wl.context)
+        del Kc, Vc
+    torch.cuda.synchronize()
+    # per-step inputs: random-walk queries (normalised, sqrt(d) norm), fresh N(0,1) keys/values
+    qs = torch.randn((L, B, Hq, d), generator=gen, device=dev)
+    qs = qs / qs.norm(dim=-1, keepdim=True) * math.sqrt(d)
+    Qall = torch.empty((total_steps, L, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    for t in range(total_steps):
+        qs = qs + wl.sigma * torch.randn(qs.shape, generator=gen, device=dev)
+        qs = qs / qs.norm(dim=-1, keepdim=True) * math.sqrt(d)
+        Qall[t] = qs.to(torch.bfloat16)
+    KVall = torch.randn((total_steps, 2, L, B, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    cur_q = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
+    cur_kv = torch.empty((2, L, B, Hkv, d), dtype=torch.bfloat16, device=dev)
+    i16 = torch.int16
+    step_i = [0]
+
+    def eager_step(t):
+        for l in range(L):
+            N.nosa_step(ctx, l, Qall[t, l].view(i16), KVall[t, 0, l].view(i16), KVall[t, 1, l].view(i16),
+                        out[l].view(i16))
+
+    # step 1 (cold fetch of every selected block) is not timed
+    eager_step(0)
+    step_i[0] = 1
+    use_graph = not args.no_graph
+    graph = None
+    if use_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        N.nosa_set_stream(ctx, side.cuda_stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for l in range(L):
+                N.nosa_step(ctx, l, cur_q[l].view(i16), cur_kv[0, l].view(i16), cur_kv[1, l].view(i16),
+                            out[l].view(i16))
+        N.nosa_set_stream(ctx, stream.cuda_stream)
+        assert N.nosa_sync(ctx) == N.NOSA_OK
+
+    def run_step(t):
+        if use_graph:
+            cur_q.copy_(Qall[t], non_blocking=True)
+            cur_kv.copy_(KVall[t], non_blocking=True)
+            graph.replay()
+        else:
+            eager_step(t)
+
+    for _ in range(W):
+        run_step(step_i[0])
+        step_i[0] += 1
+    N.nosa_reset_stats(ctx)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        run_step(step_i[0])
+        step_i[0] += 1
+    e1.record()
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = e0.elapsed_time(e1) / K
+    st = N.nosa_sync(ctx)
+    if st != N.NOSA_OK:
+        raise RuntimeError(f"device error {N.STATUS_NAMES[st]}")
+    stats = N.nosa_get_stats(ctx)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * B / (ms * 1e-3)
+    fetched_per_step = stats.blocks_fetched / K
+
+    result = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
+              "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+              "dtype": "bf16", "data": "synthetic",
+              "config": {"workload": wl.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": Hkv,
+                         "head_dim": d, "context": wl.context, "k_q": wl.k_q, "k_e": wl.k_e,
+                         "sink_blocks": wl.sink_blocks, "window_tokens": wl.window_tokens, "sigma": wl.sigma,
+                         "parallelism": f"replicas x{world} (independent sequences per GPU)",
+                         "cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
+                         "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache "
+                               "(L2 is 129 MB)"},
+              "gpu_launches": 4 * L * K,
+              "clocks": ck,
+              "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min, "bound": wl.k_e / (wl.k_q + wl.k_e)},
+              "fetch_blocks_per_step": fetched_per_step,
+              "short_selections": stats.short_selections}
+    if args.quick or rank != 0:
+        N.nosa_destroy(ctx)
+        return result
+
+    # ---------------- per-kernel leg: one event pair around each launch, on the launching stream
+    ev = {k: [] for k in ("append", "select", "fetch", "attend")}
+    N.nosa_reset_stats(ctx)
+    for _ in range(n_time_leg):
+        t = step_i[0]
+        step_i[0] += 1
+        for l in range(L):
+            pairs = []
+            calls = [("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16), KVall[t, 1, l].view(i16), 1)),
+                     ("select", lambda: N.nosa_select(ctx, l, Qall[t, l].view(i16))),
+                     ("fetch", lambda: N.nosa_fetch(ctx, l)),
+                     ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16)))]
+            for name, fn in calls:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                pairs.append((name, a, b))
+            torch.cuda.synchronize()
+            for name, a, b in pairs:
+                ev[name].append(a.elapsed_time(b) * 1e3)
+    st2 = N.nosa_get_stats(ctx)
+    us = {k: statistics.mean(v) for k, v in ev.items()}
+    n_sel = np.zeros(U, np.int32)
+    N.nosa_export_state(ctx, 0, n_sel=n_sel)
+    T_now = N.nosa_context_length(ctx, 0)
+    valid_tail = T_now - 64 * ((T_now + 63) // 64 - 1)
+    G = Hq // Hkv
+    attend_bytes = float(np.sum((n_sel.astype(np.int64) * 64 - (64 - valid_tail)) * d * 2 * 2)) + 2 * U * G * d * 2
+    nc = (T_now - 32) // 16 + 1
+    nb = (T_now + 63) // 64
+    select_bytes = U * (nc * d * 2 + nb * 4 + G * d * 2)
+    fetch_bytes_launch = st2.blocks_fetched / max(n_time_leg * L, 1) * BLOCK_BYTES
+    hbm, src = measured_peaks()
+    h2d = h2d_peak(torch)
+    hbm_kernels = {"attend": attend_bytes, "select": select_bytes}
+    dominant = max(hbm_kernels, key=lambda k: us[k])
+    ach = hbm_kernels[dominant] / (us[dominant] * 1e-6) / 1e9
+    result["roofline"] = {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
+                          "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
+                          "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                          "algorithmic_bytes_per_launch": hbm_kernels[dominant],
+                          "avg_launch_us": us[dominant]}
+    fach = fetch_bytes_launch / (us["fetch"] * 1e-6) / 1e9
+    result["fetch_roofline"] = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach,
+                                "peak": h2d, "unit": "GB/s", "frac": fach / h2d,
+                                "peak_source": "best pinned 1 GiB cudaMemcpyAsync H2D measured in this run",
+                                "bytes_per_launch": fetch_bytes_launch, "avg_launch_us": us["fetch"]}
+    result["stages_us_per_layer"] = us
+    result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / ((us["attend"] + us["select"]) * 1e-6) / 1e9 / hbm
+
+    # ---------------- e2e: the public host-pointer API, copies inside the timed region
+    qh = torch.empty((n_e2e, L, B, Hq, d), dtype=torch.bfloat16).pin_memory()
+    kvh = torch.empty((n_e2e, 2, L, B, Hkv, d), dtype=torch.bfloat16).pin_memory()
+    oh = torch.empty((n_e2e, L, B, Hq, d), dtype=torch.bfloat16).pin_memory()
+    t_base = step_i[0]
+    qh.copy_(Qall[t_base:t_base + n_e2e])
+    kvh.copy_(KVall[t_base:t_base + n_e2e])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    a.record(stream)
+    for j in range(n_e2e):
+        for l in range(L):
+            N.nosa_step_host(ctx, l, qh[j, l].view(i16), kvh[j, 0, l].view(i16), kvh[j, 1, l].view(i16),
+                             oh[j, l].view(i16))
+    b.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    step_i[0] += n_e2e
+    e2e_ms = max(a.elapsed_time(b), wall * 1e3) / n_e2e
+    result["e2e"] = {"value": B / (e2e_ms * 1e-3), "unit": "tok/s", "ms_per_step": e2e_ms,
+                     "h2d_bytes_per_step": L * (B * Hq * d * 2 + 2 * U * d * 2),
+                     "d2h_bytes_per_step": L * B * Hq * d * 2,
+                     "how": "nosa_step_host per layer from pinned host q/k/v, output read back to pinned host; "
+                            "no CUDA graph; max of device-event and host wall time"}
+    assert N.nosa_sync(ctx) == N.NOSA_OK
+    N.nosa_destroy(ctx)
+    del Qall, KVall
+    torch.cuda.empty_cache()
+    if world == 1:
+        result["cpu_baseline"] = oracle_baseline(syn.workload(args.workload, **over), args.cpu_seconds, L * U)
+    result["host_store_gb"] = sizes.host_store_bytes / 1e9
+    return result
+
+
+def run_reference(args):
+    """The oracle, as it stands, on host cores: each step is a bounded sample of the workload."""
+    from synth import inputs as syn
+    wl = syn.workload(args.workload)
+    U = wl.layers * wl.batch * wl.kv_heads
+    per_step = max(2.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
+    base = oracle_baseline(wl, per_step * (args.steps + args.warmup), U)
+    return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "layers": wl.layers, "batch": wl.batch, "context": wl.context},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_native(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * nosa.h -- C ABI of the NOSA decode-step hot path on one GB300 (sm_103a).
+ *
+ * NOSA (Native and Offloadable Sparse Attention) keeps the full bf16 K/V cache
+ * in pinned host memory.  The GPU keeps only compressed keys, pooled eviction
+ * scores and a small per-sequence block cache.  One decode step per layer is
+ *
+ *   append  -> new K/V to the host store (and to its cache slot), eviction
+ *              score s^e = softplus(v W1) W2, new compressed key when a
+ *              16-token stride completes                        (a1)
+ *   select  -> query-aware score over all compressed keys, mean->max pooling
+ *              onto 64-token blocks, top-k_q query-aware blocks, then k_e
+ *              blocks by pooled s^e among never-dropped candidates, plus the
+ *              sink and sliding-window blocks; set difference against the
+ *              cache; list of blocks to fetch                  (a2-a4)
+ *   fetch   -> persistent UVA gather of the newly needed 16 KiB K and V
+ *              chunks from pinned host memory into cache slots  (a5)
+ *   attend  -> split-K flash-decode over the selected blocks    (a6)
+ *
+ * Sources: the NOSA wiki page (aiwiki.ai), sections "How NOSA works",
+ * "Main-experiment configuration" and "NOSI: the inference system"; the
+ * NOSA-1B blog (wmrh.cn), sections on the key compressor, the CIS pooling
+ * kernel and the two-stage top-k; the NOSA explainer (l189.com), section 2.1
+ * (eq. 4-8); the SparDA summary (developer.aliyun.com), section on the KV
+ * prefetch runtime (persistent UVA kernel, CTA-count rule).
+ *
+ * Conventions for every entry point
+ *   * Every call returns nosa_status; no exception or abort crosses the ABI.
+ *   * Argument errors are reported synchronously and change no state.
+ *   * Device work is asynchronous on the context's stream.  Errors detected on
+ *     the device (bounds, timeouts, capacity) are latched in a device error
+ *     word and reported by nosa_sync() (and by later calls, which then fail
+ *     with NOSA_ERR_STATE until nosa_reset_state()).
+ *   * Pointers marked "device" must be device (or managed) memory and must stay
+ *     valid until the stream reaches the call; "host" pointers are read or
+ *     written before the call returns unless stated otherwise.
+ *   * bf16 tensors are passed as uint16_t bit patterns.
+ *   * Units: a unit is one (sequence b, kv head g) of one layer; within a layer
+ *     units are ordered u = b * num_kv_heads + g.  GQA: q head h uses kv head
+ *     h / (num_q_heads / num_kv_heads).
+ *   * All sequences of a context share one length T per layer.
+ *   * The library allocates in nosa_create only; the step calls allocate
+ *     nothing and can be captured in a CUDA graph (per-step values such as the
+ *     context length live in device memory).
+ */
+#ifndef NOSA_H_
+#define NOSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NOSA_OK = 0,
+  NOSA_ERR_INVALID_ARG = 1, /* bad pointer, layer, size or config field */
+  NOSA_ERR_OOM = 2,         /* device allocation failed */
+  NOSA_ERR_HOST_ALLOC = 3,  /* pinned host allocation failed */
+  NOSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (e.g. no GPU) */
+  NOSA_ERR_CAPACITY = 5,    /* append past max_context */
+  NOSA_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up */
+  NOSA_ERR_BOUNDS = 7,      /* a device-side index check failed */
+  NOSA_ERR_STATE = 8        /* call out of order, or the context is in a failed state */
+} nosa_status;
+
+/* Flags for nosa_config.flags (none defined yet; must be 0). */
+
+typedef struct {
+  uint32_t struct_size;   /* sizeof(nosa_config) */
+  int32_t num_layers;     /* L >= 1 */
+  int32_t batch;          /* B >= 1 sequences */
+  int32_t num_q_heads;    /* Hq; Hq % Hkv == 0 and 1 <= Hq/Hkv <= 8 */
+  int32_t num_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;       /* d; must be 128 */
+  int32_t block_size;     /* n_b; must be 64 (wiki: block size 64 tokens) */
+  int32_t cmp_kernel;     /* CompressK window; must be 32 */
+  int32_t cmp_stride;     /* CompressK stride; must be 16 */
+  int32_t k_q;            /* query-aware blocks per step (>= 0) */
+  int32_t k_e;            /* query-agnostic blocks per step (>= 0); sink/window not counted */
+  int32_t sink_blocks;    /* leading blocks always selected (>= 0) */
+  int32_t window_tokens;  /* sliding window, a multiple of block_size (>= 0) */
+  int32_t max_context;    /* capacity per sequence in tokens, 1 .. 262144 */
+  int32_t evict_hidden;   /* eviction-head hidden size h: multiple of 32, 32..256 */
+  int32_t gather_ctas;    /* CTAs of the persistent fetch kernel; 0 = rule 16 if B<32 else 32 */
+  float softmax_scale;    /* 0 => 1/sqrt(head_dim) */
+  uint32_t flags;         /* must be 0 */
+} nosa_config;
+
+/* Derived sizes; filled by nosa_query_sizes (host only, no GPU needed). */
+typedef struct {
+  int32_t units_per_layer; /* B * Hkv */
+  int32_t group;           /* Hq / Hkv */
+  int32_t cache_slots;     /* blocks per unit in the GPU cache = sink + window/64 + k_q + k_e */
+  int32_t max_blocks;      /* ceil(max_context / 64) */
+  int32_t max_windows;     /* complete CompressK windows at max_context */
+  int32_t evict_words;     /* 32-bit words of the per-unit eviction bitmap */
+  uint64_t host_store_bytes;   /* pinned K/V store: L*U*max_blocks*2*64*d*2 */
+  uint64_t device_state_bytes; /* everything nosa_create allocates on the device */
+} nosa_sizes;
+
+typedef struct nosa_ctx nosa_ctx;
+
+/* Per-context counters, accumulated on the device by nosa_select. */
+typedef struct {
+  uint64_t selections;      /* unit-selections made */
+  uint64_t gamma_samples;   /* unit-selections that had a previous selection */
+  double gamma_mean;        /* mean over those of |D_t & S_{t-1}| / |D_t| */
+  double gamma_min;         /* minimum of the same (1.0 if no sample) */
+  uint64_t blocks_fetched;  /* blocks copied host -> device (each 2 x 16 KiB) */
+  uint64_t bytes_fetched;   /* blocks_fetched * 32 KiB */
+  uint64_t short_selections;/* unit-selections whose query-agnostic part came up short */
+} nosa_stats;
+
+/* Host-side view for nosa_export_state: every pointer is host memory or NULL
+ * (skipped).  Shapes are per layer; U = units_per_layer, cap = cache_slots. */
+typedef struct {
+  int32_t* sel;       /* [U][cap] selected blocks S, ascending, -1 padded */
+  int32_t* sel_kind;  /* [U][cap] 0 sink, 1 window, 2 query-aware, 3 query-agnostic, -1 pad */
+  int32_t* sel_slot;  /* [U][cap] cache slot of each selected block, -1 pad */
+  int32_t* n_sel;     /* [U] */
+  int32_t* fetch;     /* [U][cap][2] (block, slot) fetched by the last selection, ascending */
+  int32_t* n_fetch;   /* [U] */
+  int32_t* slot_blk;  /* [U][cap] block held by each slot, -1 free */
+  uint32_t* evicted;  /* [U][evict_words] sticky eviction bitmap, bit b%32 of word b/32 */
+  uint16_t* kt;       /* [U][max_windows][d] compressed keys (bf16 bits) */
+  float* se_win;      /* [U][max_windows] window means of the eviction score */
+  float* se_blk;      /* [U][max_blocks] pooled eviction score (-inf before any window) */
+  int32_t* gamma;     /* [U][2] |D_t & S_{t-1}| and |D_t| of the last selection */
+} nosa_state_view;
+
+/* Validate a config without touching the GPU.  NOSA_OK or NOSA_ERR_INVALID_ARG. */
+nosa_status nosa_validate_config(const nosa_config* cfg);
+
+/* Sizes derived from a valid config (host only). */
+nosa_status nosa_query_sizes(const nosa_config* cfg, nosa_sizes* out);
+
+/* Create a context on the current CUDA device.  `stream` is a cudaStream_t
+ * (NULL = legacy default stream) owned by the caller; every later call of the
+ * context is queued on it.  Allocates the pinned, mapped host K/V store and
+ * all device state; eviction heads start at zero.  On failure *out is NULL. */
+nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out);
+
+/* Drain the stream and free everything.  NULL is accepted. */
+nosa_status nosa_destroy(nosa_ctx* ctx);
+
+/* Change the stream later calls are queued on (e.g. a capture stream). */
+nosa_status nosa_set_stream(nosa_ctx* ctx, void* stream);
+
+/* Eviction head of one layer (eq. 4): host float32 W1 [Hkv][d][h] and
+ * W2 [Hkv][h], copied before return. */
+nosa_status nosa_set_eviction_head(nosa_ctx* ctx, int layer, const float* W1, const float* W2);
+
+/* Append n_tokens >= 1 tokens to every sequence of `layer`.
+ * k, v: bf16 [B][Hkv][n_tokens][d]; device memory, or pinned/pageable host
+ * memory when src_is_host != 0 (then copied before the kernels run).
+ * n_tokens == 1 is the decode-step append; n_tokens > 1 is a bulk context load
+ * (host store, eviction scores, compressed keys; cached blocks are kept in step).
+ * Returns NOSA_ERR_CAPACITY (no state change) if T + n_tokens > max_context. */
+nosa_status nosa_append_kv(nosa_ctx* ctx, int layer, const uint16_t* k, const uint16_t* v,
+                           int n_tokens, int src_is_host);
+
+/* Score and select the blocks of every unit of `layer` for query q
+ * (device bf16 [B][Hq][d]), update the eviction bitmap and the slot map, and
+ * build the fetch list.  Optional device outputs: sel_out [B][Hkv][cache_slots]
+ * (S ascending, -1 padded) and nfetch_out [B][Hkv] (blocks to fetch). */
+nosa_status nosa_select(nosa_ctx* ctx, int layer, const uint16_t* q, int32_t* sel_out,
+                        int32_t* nfetch_out);
+
+/* Copy the blocks listed by the last nosa_select of `layer` from the pinned
+ * host store into their cache slots (persistent UVA gather kernel). */
+nosa_status nosa_fetch(nosa_ctx* ctx, int layer);
+
+/* Attention of q (device bf16 [B][Hq][d]) over the selected blocks; writes
+ * out (device bf16 [B][Hq][d]).  Needs a select + fetch for the current T. */
+nosa_status nosa_attend(nosa_ctx* ctx, int layer, const uint16_t* q, uint16_t* out);
+
+/* append(1 token) + select + fetch + attend.  k_new, v_new: device bf16
+ * [B][Hkv][d]; q, out: device bf16 [B][Hq][d]. */
+nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
+                      const uint16_t* v_new, uint16_t* out);
+
+/* nosa_step with host (pinned) q, k_new, v_new and out: the inputs are copied
+ * to context-owned device buffers and the output back, on the stream.  out is
+ * written when the stream reaches the end of the step. */
+nosa_status nosa_step_host(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
+                           const uint16_t* v_new, uint16_t* out);
+
+/* Wait for the stream; report and latch any device-side error. */
+nosa_status nosa_sync(nosa_ctx* ctx);
+
+/* Clear a latched error (the device state may be inconsistent afterwards). */
+nosa_status nosa_reset_state(nosa_ctx* ctx);
+
+/* Current context length of `layer` (synchronises the stream). */
+nosa_status nosa_context_length(nosa_ctx* ctx, int layer, int32_t* T_out);
+
+/* Counters (synchronises the stream); nosa_reset_stats zeroes them. */
+nosa_status nosa_get_stats(nosa_ctx* ctx, nosa_stats* out);
+nosa_status nosa_reset_stats(nosa_ctx* ctx);
+
+/* Pooled block scores of the last selection of `layer`, host float
+ * [U][max_blocks] each (sq_blk: query-aware, se_blk: query-agnostic); either may
+ * be NULL.  Valid until the next nosa_select of any layer.  Synchronises. */
+nosa_status nosa_debug_scores(nosa_ctx* ctx, int layer, float* sq_blk, float* se_blk);
+
+/* Copy selection / cache / compression state of `layer` to host memory. Synchronises. */
+nosa_status nosa_export_state(nosa_ctx* ctx, int layer, const nosa_state_view* view);
+
+const char* nosa_status_string(nosa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NOSA_H_ */

@@ -1,0 +1,257 @@
+// a6 attend: split-K flash-decode over the selected blocks (NOSA explainer
+// eq. 8: attention of q over K[selected], V[selected]; NOSA-1B blog,
+// sparse_forward: attention over the top-k block indices only).
+//
+// grid (attend_chunks, U), 128 threads.  CTA (chunk, u) owns entries
+// [chunk*bpc, chunk*bpc + bpc) of unit u's ascending selection.  One elected
+// thread streams each 32 KiB block (K and V, two 16 KiB boxes with the 128-byte
+// swizzle) from the block cache into a 3-stage shared-memory ring with TMA
+// (cp.async.bulk.tensor) and an mbarrier per stage.  Warp w handles tokens
+// [16w, 16w+16) of every block on the tensor cores (mma.sync m16n8k16, bf16 in,
+// fp32 accumulate):
+//   S^T (16 tokens x 8 heads) = K (ldmatrix) . q^T           (8 MMAs)
+//   online softmax per head in registers (exp2, warp shuffles)
+//   P^T fragments by movmatrix.trans of the bf16-packed S^T fragments
+//   O^T (128 dims x 8 heads) += V^T (ldmatrix.trans) . P^T   (8 MMAs)
+// The four warps' (m, l, O) are merged in shared memory into one partial per
+// CTA; the last CTA of the unit (atomic ticket) merges the partials and writes
+// the bf16 output.
+#include "nosa_internal.cuh"
+#include "ptx.cuh"
+
+namespace nosa {
+
+constexpr int kStageBytes = kBlockBytes;            // 32 KiB: [d half][K,V][64 tokens][64 dims]
+static_assert(4 * kMaxGroup * kHeadDim * 4 <= kAttendStages * kStageBytes, "warp partials alias the stages");
+constexpr long long kWaitLimit = 2000000000LL;      // ~1 s of SM clocks
+
+__device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int token, int chunk) {
+  return stage + dhalf * 16384 + kv * 8192 + token * 128 + (((chunk ^ (token & 7)) & 7) << 4);
+}
+
+__global__ void __launch_bounds__(kAttendThreads, 2)
+    attend_kernel(const __grid_constant__ CUtensorMap tmap, LayerState s, const uint16_t* __restrict__ q,
+                  uint16_t* __restrict__ out) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kAttendStages];
+  __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
+  __shared__ int last, bad_any;
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
+  float* wo = reinterpret_cast<float*>(smem);
+
+  const int chunk = blockIdx.x, u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gr = lane >> 2, t4 = lane & 3;
+  const Geometry geo = geometry(*s.T, s.nw, s.sink);
+  const int G = s.G;
+  const int nsel = s.n_sel[u];
+  const int e0 = chunk * s.attend_blocks_per_cta;
+  const int nblk = max(0, min(e0 + s.attend_blocks_per_cta, nsel) - e0);
+  const int32_t* sel = s.sel + (size_t)u * s.cap;
+  const int32_t* sslot = s.sel_slot + (size_t)u * s.cap;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (tid == 0) {
+    prefetch_tmap(&tmap);
+    for (int i = 0; i < kAttendStages; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    bad_any = 0;
+  }
+  __syncthreads();
+  auto issue = [&](int i) {  // entry e0+i into stage i % kAttendStages (thread 0 only)
+    int slot = sslot[e0 + i];
+    if (slot < 0 || slot >= s.cap) {
+      atomicOr(s.err, kErrBounds);
+      slot = 0;  // keep the copy in bounds; the result is flagged as invalid
+    }
+    const int flat = (s.unit_base + u) * s.cap + slot;
+    const int st = i % kAttendStages;
+    mbar_arrive_expect_tx(&bars[st], kStageBytes);
+    tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
+    tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    for (; issued < min(nblk, kAttendStages); ++issued) issue(issued);
+  }
+
+  // q^T as the B operand: b0 = q[head gr][16ks + 2t4 .. +1], b1 = the same +8
+  uint32_t qb[8][2];
+  {
+    const uint16_t* qh = q + ((size_t)u * G + min(gr, G - 1)) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qb[ks][0] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4) : 0u;
+      qb[ks][1] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4 + 8) : 0u;
+    }
+  }
+  const float sl2 = s.scale * 1.4426950408889634f;  // softmax in base 2
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+  const int tok0 = warp * 16;
+  // ldmatrix row addresses of this lane (token, 16-byte chunk) before swizzling
+  const int tk_k = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);  // K: matrices (rows 0-7|8-15) x (k lo|hi)
+  const int ch_k = lane >> 4;
+  const int tk_v = tok0 + (lane & 7) + ((lane >> 4) << 3);        // V^T: (d lo|hi) x (tokens 0-7|8-15)
+  const int ch_v = (lane >> 3) & 1;
+
+  int consumed = 0;
+  for (int i = 0; i < nblk; ++i) {
+    const int st = i % kAttendStages;
+    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((i / kAttendStages) & 1), kWaitLimit);
+    if (__syncthreads_or(!okw)) {
+      if (tid == 0) atomicOr(s.err, kErrTimeout);
+      bad_any = 1;
+      break;
+    }
+    consumed = i + 1;
+    const int blk = sel[e0 + i];
+    const int valid = (blk == geo.nb - 1) ? geo.valid_tail : kBlock;
+    const uint32_t stg = sbase + st * kStageBytes;
+    if (tok0 < valid) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int dch = 2 * ks + ch_k;
+        uint32_t a[4];
+        ldsm_x4(a, swz(stg, dch >> 3, 0, tk_k, dch & 7));
+        mma_16816(acc, a, qb[ks][0], qb[ks][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j] *= sl2;
+      if (tok0 + gr >= valid) acc[0] = acc[1] = -INFINITY;
+      if (tok0 + gr + 8 >= valid) acc[2] = acc[3] = -INFINITY;
+      float mx0 = fmaxf(acc[0], acc[2]), mx1 = fmaxf(acc[1], acc[3]);
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: token tok0 is valid
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float p0 = exp2f(acc[0] - mn0), p1 = exp2f(acc[1] - mn1);
+      const float p2 = exp2f(acc[2] - mn0), p3 = exp2f(acc[3] - mn1);
+      l0 = l0 * al0 + p0 + p2;
+      l1 = l1 * al1 + p1 + p3;
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0-7 of the tile
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8-15
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int dch = 2 * mt + ch_v;
+        uint32_t a[4];
+        ldsm_x4_trans(a, swz(stg, dch >> 3, 1, tk_v, dch & 7));
+        mma_16816(o[mt], a, pb0, pb1);
+      }
+    }
+    __syncthreads();  // every warp is done with this stage
+    if (tid == 0 && issued < nblk) {
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (bad_any && tid == 0) {  // drain copies still in flight before the shared memory is reused
+    for (int i = consumed; i < issued; ++i)
+      mbar_wait_bounded(&bars[i % kAttendStages], (uint32_t)((i / kAttendStages) & 1), kWaitLimit);
+  }
+  __syncthreads();
+  // warp partials -> shared memory
+#pragma unroll
+  for (int o2 = 4; o2 < 32; o2 <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+  }
+  if (gr == 0) {
+    wm[warp][2 * t4] = m0;
+    wm[warp][2 * t4 + 1] = m1;
+    wl[warp][2 * t4] = l0;
+    wl[warp][2 * t4 + 1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    float* w0 = wo + ((warp * kMaxGroup + 2 * t4) * kHeadDim);
+    float* w1 = wo + ((warp * kMaxGroup + 2 * t4 + 1) * kHeadDim);
+    w0[16 * mt + gr] = o[mt][0];
+    w1[16 * mt + gr] = o[mt][1];
+    w0[16 * mt + gr + 8] = o[mt][2];
+    w1[16 * mt + gr + 8] = o[mt][3];
+  }
+  __syncthreads();
+  // CTA partial (base-2 max, sum, unnormalised output) for each head
+  const int x = tid;  // head dimension
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w][h]);
+    float L = 0.f, O = 0.f;
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float f = exp2f(wm[w][h] - M);
+        L += wl[w][h] * f;
+        O += wo[(w * kMaxGroup + h) * kHeadDim + x] * f;
+      }
+    }
+    float* part = s.apart + (((size_t)u * s.attend_chunks + chunk) * kMaxGroup + h) * kPartStride;
+    if (x == 0) {
+      part[0] = M;
+      part[1] = L;
+    }
+    part[2 + x] = O;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned int t = atomicAdd(&s.tickets[s.U + u], 1u);
+    last = (t == (unsigned int)s.attend_chunks - 1);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid == 0) s.tickets[s.U + u] = 0;
+  for (int h = 0; h < G; ++h) {
+    const float* pb = s.apart + ((size_t)u * s.attend_chunks * kMaxGroup + h) * kPartStride;
+    float M = -INFINITY;
+    for (int j = 0; j < s.attend_chunks; ++j) M = fmaxf(M, __ldcg(pb + (size_t)j * kMaxGroup * kPartStride));
+    float L = 0.f, O = 0.f;
+    if (M > -INFINITY) {
+      for (int j = 0; j < s.attend_chunks; ++j) {
+        const float* p = pb + (size_t)j * kMaxGroup * kPartStride;
+        const float mj = __ldcg(p);
+        if (mj > -INFINITY) {
+          const float f = exp2f(mj - M);
+          L += __ldcg(p + 1) * f;
+          O += __ldcg(p + 2 + x) * f;
+        }
+      }
+    }
+    const float r = L > 0.f ? O / L : 0.f;
+    out[((size_t)u * G + h) * kHeadDim + x] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+  }
+}
+
+size_t attend_smem_bytes() { return 1024 + kAttendStages * kStageBytes; }
+
+cudaError_t init_attend() {
+  return cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attend_smem_bytes());
+}
+
+cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
+                          cudaStream_t st) {
+  const size_t smem = attend_smem_bytes();
+  attend_kernel<<<dim3(s.attend_chunks, s.U), kAttendThreads, smem, st>>>(*tmap, s, q, out);
+  return cudaGetLastError();
+}
+
+}  // namespace nosa

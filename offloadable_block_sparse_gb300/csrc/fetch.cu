@@ -1,0 +1,70 @@
+// a5 fetch: persistent UVA gather of newly selected blocks from the pinned host
+// store into their cache slots (wiki "NOSI": a host-to-device kernel that reads
+// CPU memory directly through Unified Virtual Addressing, block-wise 16 KiB
+// transfers; SparDA summary, KV prefetch runtime: a small resident set of CTAs
+// handles all copy work, CTA count traded against compute SMs).
+//
+// One work item is one block: its K and V chunks (2 x 16 KiB) are contiguous in
+// both the host store and the slot.  Each thread keeps 4 x 16 bytes in flight
+// per item; the CTA walks items item = blockIdx.x, += gridDim.x.  Rows past the
+// end of the partial tail block are written as zeros.
+#include "nosa_internal.cuh"
+#include "ptx.cuh"
+
+namespace nosa {
+
+constexpr int kMaxGatherUnits = 4096;
+
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s) {
+  __shared__ int pref[kMaxGatherUnits + 1];
+  __shared__ int scan_tmp[32];
+  const int tid = threadIdx.x;
+  const Geometry geo = geometry(*s.T, s.nw, s.sink);
+  // exclusive prefix of the per-unit fetch counts
+  int carry = 0;
+  for (int base = 0; base < s.U; base += blockDim.x) {
+    const int uu = base + tid;
+    const int v = uu < s.U ? s.n_fetch[uu] : 0;
+    int tot;
+    const int ex = block_scan_excl(v, scan_tmp, &tot);
+    if (uu < s.U) pref[uu] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) pref[s.U] = carry;
+  __syncthreads();
+  const int total = carry;
+  constexpr int kVec = kBlockBytes / 16 / kGatherThreads;  // 16-byte vectors per thread per block (4)
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
+    int lo = 0, hi = s.U - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pref[mid] <= item) lo = mid;
+      else hi = mid - 1;
+    }
+    const int u = lo, j = item - pref[u];
+    const int b = s.fetch[((size_t)u * s.cap + j) * 2], slot = s.fetch[((size_t)u * s.cap + j) * 2 + 1];
+    if (b < 0 || b >= geo.nb || slot < 0 || slot >= s.cap) {
+      if (tid == 0) atomicOr(s.err, kErrBounds);
+      continue;
+    }
+    const int rows = (b == geo.nb - 1) ? geo.valid_tail : kBlock;
+    const uint4* src = reinterpret_cast<const uint4*>(s.host_kv + ((size_t)u * s.nb_max + b) * 2 * kBlockElems);
+    uint4* dst = reinterpret_cast<uint4*>(s.cache + ((size_t)u * s.cap + slot) * 2 * kBlockElems);
+    uint4 v[kVec];
+#pragma unroll
+    for (int r = 0; r < kVec; ++r) {
+      const int idx = tid + r * kGatherThreads;
+      const int row = (idx >> 4) & (kBlock - 1);  // 16 vectors per 256-byte row; K rows then V rows
+      v[r] = row < rows ? ld_stream_v4(src + idx) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int r = 0; r < kVec; ++r) dst[tid + r * kGatherThreads] = v[r];
+  }
+}
+
+cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st) {
+  gather_kernel<<<ctas, kGatherThreads, 0, st>>>(s);
+  return cudaGetLastError();
+}
+
+}  // namespace nosa

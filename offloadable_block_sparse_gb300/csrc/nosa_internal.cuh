@@ -1,0 +1,162 @@
+// Internal definitions shared by the translation units of libnosa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/nosa.h"
+
+namespace nosa {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlock = 64;
+constexpr int kCmpKernel = 32;
+constexpr int kCmpStride = 16;
+constexpr int kMaxGroup = 8;               // q heads per kv head handled by one MMA column tile
+constexpr int kBlockElems = kBlock * kHeadDim;      // one K (or V) block: 8192 bf16 = 16 KiB
+constexpr int kBlockBytes = 2 * kBlockElems * 2;    // K + V of one block: 32 KiB
+
+// device error word bits
+constexpr int kErrBounds = 1;
+constexpr int kErrTimeout = 2;
+constexpr int kErrCapacity = 4;
+
+// one launch of the score/select kernel covers kScoreWarps * kScoreTiles * 16 windows per CTA
+constexpr int kScoreThreads = 256;
+constexpr int kScoreWarps = kScoreThreads / 32;
+constexpr int kScoreTiles = 2;
+constexpr int kWindowsPerCta = kScoreWarps * kScoreTiles * 16;
+
+constexpr int kAttendThreads = 128;        // 4 warps, 16 tokens of every 64-token block each
+constexpr int kAttendStages = 3;           // 32 KiB TMA stages per CTA
+constexpr int kPartStride = 2 + kHeadDim;  // (m, l, o[128]) per head in a split-K partial
+
+constexpr int kGatherThreads = 512;
+
+// Per-layer derived quantities from the context length T (same formulas on host and device).
+struct Geometry {
+  int T, nb, nc, valid_tail, ws, ns;
+};
+
+__host__ __device__ inline Geometry geometry(int T, int nw, int sink) {
+  Geometry g;
+  g.T = T;
+  g.nb = (T + kBlock - 1) / kBlock;
+  g.nc = T < kCmpKernel ? 0 : (T - kCmpKernel) / kCmpStride + 1;
+  g.valid_tail = T - kBlock * (g.nb - 1);
+  g.ns = sink < g.nb ? sink : g.nb;
+  int ws = g.nb - nw;
+  g.ws = ws > g.ns ? ws : g.ns;
+  return g;
+}
+
+// Device counters behind nosa_get_stats.
+struct DevStats {
+  unsigned long long selections;
+  unsigned long long gamma_samples;
+  unsigned long long gamma_num;   // sum of |D & S_prev|
+  unsigned long long gamma_den;   // sum of |D|
+  unsigned long long blocks_fetched;
+  unsigned long long short_selections;
+  unsigned int gamma_min_bits;    // float bits of the minimum gamma (non-negative floats order as ints)
+  unsigned int pad;
+};
+
+// Pointers of one layer's state, offset by the host before each launch.
+struct LayerState {
+  int layer;
+  int U;            // units of this layer
+  int G;            // q heads per kv head
+  int Hkv;
+  int cap, nb_max, nc_max, T_max, ev_words, nw, sink, k_q, k_e, h;
+  int unit_base;    // layer * U: first unit of this layer in context-wide arrays
+  float scale;
+  int* T;                 // device context length of this layer
+  uint16_t* host_kv;      // device alias of the pinned store [U][nb_max][2][64][d]
+  uint16_t* cache;        // [U][cap][2][64][d]
+  uint16_t* kt;           // [U][nc_max][d]
+  uint16_t* kring;        // [U][32][d]
+  float* se_tok;          // [U][T_max]
+  float* se_win;          // [U][nc_max]
+  float* se_blk;          // [U][nb_max]
+  int32_t* slot_blk;      // [U][cap]
+  int32_t* blk2slot;      // [U][nb_max]
+  uint32_t* evicted;      // [U][ev_words]
+  int32_t* sel;           // [U][cap]
+  int32_t* sel_kind;      // [U][cap]
+  int32_t* sel_slot;      // [U][cap]
+  int32_t* n_sel;         // [U]
+  int32_t* fetch;         // [U][cap][2]
+  int32_t* n_fetch;       // [U]
+  int32_t* gamma;         // [U][2]
+  const float* W1;        // [Hkv][d][h]
+  const float* W2;        // [Hkv][h]
+  // scratch shared by all layers (stream ordered)
+  float* zbuf;            // [U][G][nc_max]
+  float* spart;           // [U][score_chunks][kMaxGroup][2]
+  float* sq_blk;          // [U][nb_max]
+  float* apart;           // [U][attend_chunks][kMaxGroup][kPartStride]
+  unsigned int* tickets;  // [3][U]: append, score, attend
+  DevStats* stats;
+  int* err;
+  int score_chunks;
+  int attend_chunks;
+  int attend_blocks_per_cta;
+};
+
+}  // namespace nosa
+
+struct nosa_ctx {
+  nosa_config cfg;
+  nosa_sizes sz;
+  int L, B, Hq, Hkv, G, d, U, h, nw, cap;
+  cudaStream_t stream;
+  int device;
+  int num_sms;
+  // pinned host store and its device alias
+  uint16_t* host_kv;
+  uint16_t* host_kv_dev;
+  size_t host_layer_elems;
+  // device state (all layers)
+  void* dev_block;  // one allocation holding everything below
+  uint16_t *cache, *kt, *kring;
+  float *se_tok, *se_win, *se_blk, *W1, *W2;
+  int32_t *slot_blk, *blk2slot, *sel, *sel_kind, *sel_slot, *n_sel, *fetch, *n_fetch, *gamma;
+  uint32_t* evicted;
+  int *T, *err;
+  nosa::DevStats* stats;
+  // scratch
+  float *zbuf, *spart, *sq_blk, *apart;
+  unsigned int* tickets;
+  int score_chunks, attend_chunks, attend_blocks_per_cta, gather_ctas;
+  // staging buffers for host-pointer calls
+  uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
+  size_t stage_tok_cap;   // tokens per unit the bulk staging buffers hold
+  uint16_t *bulk_k, *bulk_v;
+  // TMA descriptor of the block cache (4-D: d, token, K/V, flat slot)
+  CUtensorMap tmap_cache;
+  // host mirrors
+  std::vector<int> T_host;
+  std::vector<int> sel_T;   // T at the last selection (-1: none), host view
+  int failed;               // latched nosa_status of a device-side error
+};
+
+namespace nosa {
+LayerState layer_state(nosa_ctx* c, int layer);
+cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, cudaStream_t st);
+cudaError_t launch_append_bulk(const LayerState& s, const uint16_t* k, const uint16_t* v, int T_old,
+                               int n, cudaStream_t st);
+cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, cudaStream_t st);
+cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st);
+cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
+                          cudaStream_t st);
+size_t score_select_smem(const LayerState& s);
+// one-time kernel attributes (dynamic shared memory limits), called by nosa_create
+cudaError_t init_append(const LayerState& s);
+cudaError_t init_score_select(const LayerState& s);
+cudaError_t init_attend();
+}  // namespace nosa

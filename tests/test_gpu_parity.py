@@ -1,0 +1,133 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Selections, fetch lists, slots, eviction bitmaps and
+compressed keys bit-exact (near ties logged and adopted, see nosa_harness);
+pooled scores within 1e-4 relative; outputs within 2e-2 max-abs / 2e-3 mean-abs."""
+import math
+
+import numpy as np
+import pytest
+
+from synth import inputs as syn
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # collected on CPU machines too; every test here is marked gpu
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from tests.nosa_harness import Parity  # noqa: E402
+from offloadable_block_sparse_gb300 import nosa as N  # noqa: E402
+
+
+def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0):
+    p = Parity(wl, sample_units=samples, layers=layers, gather_ctas=gather_ctas)
+    try:
+        p.load_context()
+        for _ in range(steps):
+            p.run_step(split_calls=split_calls)
+        assert N.nosa_sync(p.ctx) == N.NOSA_OK
+        stats = N.nosa_get_stats(p.ctx)
+        return p.log, stats
+    finally:
+        p.close()
+
+
+def _report(name, log, stats=None):
+    print(f"[{name}] steps={log.steps} unit_steps={log.unit_steps} near_ties={len(log.near_ties)} "
+          f"max_out_abs={log.max_out_abs:.2e} max_mean_abs={log.max_out_mean_abs:.2e} "
+          f"max_score_rel={log.max_score_rel:.2e} gamma_min={min(log.gammas) if log.gammas else None}")
+
+
+def test_tiny_every_step_every_unit():
+    wl = syn.workload("tiny")
+    log, stats = run(wl, wl.steps)
+    _report("tiny", log, stats)
+    assert log.unit_steps == wl.steps * 2
+    assert min(log.gammas) >= wl.k_e / (wl.k_q + wl.k_e) - 1e-12   # Theorem 2 on the GPU path
+    assert stats.gamma_min >= wl.k_e / (wl.k_q + wl.k_e) - 1e-6
+
+
+def test_tiny_through_separate_calls():
+    wl = syn.workload("tiny", steps=12)
+    log, _ = run(wl, wl.steps, split_calls=True)
+    assert log.unit_steps == 24
+
+
+def test_ragged_context_group4_small_window():
+    # T_0 not a multiple of 64 or 16: the tail block is partial and is fetched on the first step;
+    # 8 q heads over 2 kv heads (G = 4)
+    wl = syn.Workload("ragged", layers=2, batch=3, q_heads=8, kv_heads=2, context=1001, k_q=3, k_e=5,
+                      window_tokens=128, steps=70, sigma=1.0)
+    log, _ = run(wl, wl.steps)
+    _report("ragged", log)
+    assert log.unit_steps == 70 * 12
+
+
+def test_short_context_everything_selected():
+    # fewer blocks than the budget: every block is selected, so attention is dense
+    wl = syn.Workload("short", layers=1, batch=2, q_heads=16, kv_heads=2, context=40, k_q=4, k_e=12,
+                      window_tokens=256, steps=30)
+    log, _ = run(wl, wl.steps)
+    assert log.unit_steps == 60
+
+
+def test_no_sink_no_window_query_aware_only():
+    wl = syn.Workload("kq_only", layers=1, batch=2, q_heads=4, kv_heads=1, context=3000, k_q=8, k_e=0,
+                      window_tokens=0, sink_blocks=0, steps=20, sigma=1.0)
+    log, _ = run(wl, wl.steps)
+    assert log.unit_steps == 40
+
+
+def test_gather_cta_counts_agree():
+    wl = syn.Workload("ctas", layers=1, batch=4, q_heads=16, kv_heads=2, context=4096, k_q=4, k_e=12,
+                      window_tokens=256, steps=6, sigma=1.0)
+    for ctas in (1, 8, 64):
+        log, _ = run(wl, wl.steps, gather_ctas=ctas)
+        assert log.unit_steps == 6 * 8
+
+
+def test_capacity_error_leaves_state_unchanged():
+    wl = syn.Workload("cap", layers=1, batch=1, q_heads=16, kv_heads=2, context=100, k_q=2, k_e=2,
+                      window_tokens=128, steps=2)
+    p = Parity(wl)
+    try:
+        p.load_context()
+        p.run_step()
+        p.run_step()
+        k = torch.zeros((1, 2, 128), dtype=torch.int16, device="cuda")
+        with pytest.raises(N.NosaError) as e:
+            N.nosa_append_kv(p.ctx, 0, k, k, 1)
+        assert e.value.status == N.NOSA_ERR_CAPACITY
+        assert N.nosa_context_length(p.ctx, 0) == 102
+        assert N.nosa_sync(p.ctx) == N.NOSA_OK
+    finally:
+        p.close()
+
+
+def test_out_of_order_calls_are_rejected():
+    wl = syn.Workload("order", layers=1, batch=1, q_heads=16, kv_heads=2, context=300, k_q=2, k_e=2,
+                      window_tokens=128, steps=2)
+    p = Parity(wl)
+    try:
+        p.load_context()
+        q = torch.zeros((1, 16, 128), dtype=torch.int16, device="cuda")
+        with pytest.raises(N.NosaError) as e:
+            N.nosa_attend(p.ctx, 0, q, q)   # no selection for this length yet
+        assert e.value.status == N.NOSA_ERR_STATE
+        with pytest.raises(N.NosaError):
+            N.nosa_fetch(p.ctx, 0)
+        with pytest.raises(N.NosaError):
+            N.nosa_step(p.ctx, 5, q, q, q, q)
+    finally:
+        p.close()
+
+
+@pytest.mark.parametrize("name,steps,samples,layers", [
+    ("nosa1b_16k_b8", 256, [(0, 0, 0), (5, 3, 1), (17, 7, 0), (27, 6, 1)], None),
+])
+def test_full_size_sampled(name, steps, samples, layers):
+    wl = syn.workload(name)
+    log, stats = run(wl, steps, samples=samples, layers=layers)
+    _report(name, log, stats)
+    assert log.unit_steps == steps * len(samples)
+    assert stats.gamma_min >= wl.k_e / (wl.k_q + wl.k_e) - 1e-6
