@@ -36,8 +36,8 @@ BLOCK_BYTES = 32768
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="nosa1b_16k_b8")
     ap.add_argument("--sigma", type=float, default=None)
@@ -127,7 +127,8 @@ def oracle_baseline(wl, seconds, total_units):
     from oracle import nosa_oracle as O
     from synth import inputs as syn
     samples = []
-    lbg = [(0, 0, 0), (wl.layers - 1, wl.batch - 1, wl.kv_heads - 1)]
+    lbg = [(0, 0, 0), (wl.layers - 1, wl.batch - 1, wl.kv_heads - 1), (wl.layers // 2, wl.batch // 2, 0),
+           (1 % wl.layers, wl.batch - 1, 0)]
     for (l, b, g) in lbg:
         x = wl.unit_inputs(l, b, g)
         o = O.UnitOracle(head_dim=wl.head_dim, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
@@ -243,6 +244,7 @@ def run_native(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading before the timed region
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(K):
@@ -292,6 +294,9 @@ def run_native(args, rank, world, local_rank):
         step_i[0] += 1
         for l in range(L):
             pairs = []
+            # hold the stream while the four launches and their events are queued, so that the
+            # events time the kernels back to back rather than the host's launch latency
+            torch.cuda._sleep(400000)
             calls = [("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16), KVall[t, 1, l].view(i16), 1)),
                      ("select", lambda: N.nosa_select(ctx, l, Qall[t, l].view(i16))),
                      ("fetch", lambda: N.nosa_fetch(ctx, l)),

@@ -11,10 +11,15 @@
 namespace nosa {
 
 // ---------------------------------------------------------------- one token per unit
-// grid: U CTAs (one per unit), 128 threads (one per head dimension).
-__global__ void __launch_bounds__(128) append_one_kernel(LayerState s, const uint16_t* __restrict__ knew,
-                                                         const uint16_t* __restrict__ vnew) {
+// grid: U CTAs (one per unit), 256 threads.  The eviction-head matvec splits the
+// 128 input dims in two halves per hidden unit so that each thread issues its 64
+// W1 loads back to back (one memory round trip rather than a dependent chain).
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads) append_one_kernel(LayerState s, const uint16_t* __restrict__ knew,
+                                                                    const uint16_t* __restrict__ vnew) {
   __shared__ float vf[kHeadDim];
+  __shared__ float half_acc[2][kHeadDim];
   __shared__ float red[4];
   const int u = blockIdx.x, tid = threadIdx.x;
   const int p = *s.T;  // position of the new token (all CTAs read it before any ticket)
@@ -39,37 +44,44 @@ __global__ void __launch_bounds__(128) append_one_kernel(LayerState s, const uin
       *reinterpret_cast<uint4*>(s.cache + coff) = val;
     }
   }
-  const uint16_t kb = krow[tid];
-  s.kring[((size_t)u * 32 + (p & 31)) * kHeadDim + tid] = kb;
-  vf[tid] = bf16_to_float(vrow[tid]);
+  if (tid < kHeadDim) {
+    s.kring[((size_t)u * 32 + (p & 31)) * kHeadDim + tid] = krow[tid];
+    vf[tid] = bf16_to_float(vrow[tid]);
+  }
   __syncthreads();
 
-  // eviction head of kv head g: hidden unit m per thread, dot product over c in order
+  // eviction head of kv head g: s^e = sum_m W2[m] softplus(sum_c v[c] W1[c][m])
   const int g = u % s.Hkv;
   const float* W1 = s.W1 + (size_t)g * kHeadDim * s.h;
   const float* W2 = s.W2 + (size_t)g * s.h;
+  const int mi = tid & (kHeadDim - 1), hf = tid >> 7;
   float part = 0.f;
-  for (int m = tid; m < s.h; m += blockDim.x) {
+  for (int m0 = 0; m0 < s.h; m0 += kHeadDim) {
+    const int m = m0 + mi;
+    const float* w = W1 + (size_t)(hf * 64) * s.h + m;
     float acc = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < kHeadDim; ++c) acc = fmaf(vf[c], W1[c * s.h + m], acc);
-    part = fmaf(softplus(acc), W2[m], part);
+#pragma unroll
+    for (int c = 0; c < 64; ++c) acc = fmaf(vf[hf * 64 + c], w[(size_t)c * s.h], acc);
+    half_acc[hf][mi] = acc;
+    __syncthreads();
+    if (tid < kHeadDim) part = fmaf(softplus(half_acc[0][mi] + half_acc[1][mi]), W2[m], part);
+    __syncthreads();
   }
-  part = warp_sum(part);
-  if ((tid & 31) == 0) red[tid >> 5] = part;
+  if (tid < kHeadDim) {
+    part = warp_sum(part);
+    if ((tid & 31) == 0) red[tid >> 5] = part;
+  }
   __syncthreads();
   if (tid == 0) s.se_tok[(size_t)u * s.T_max + p] = (red[0] + red[1]) + (red[2] + red[3]);
   __syncthreads();
 
   const int T = p + 1;
-  if (T >= kCmpKernel && (T - kCmpKernel) % kCmpStride == 0) {
+  if (T >= kCmpKernel && (T - kCmpKernel) % kCmpStride == 0 && tid < kHeadDim) {
     const int i = (T - kCmpKernel) / kCmpStride;  // window [16i, 16i+32) just completed
     double acc = 0.0;                              // exact: 32 bf16 values fit a double's fraction
-#pragma unroll 8
-    for (int r = 0; r < kCmpKernel; ++r) {
-      const int j = kCmpStride * i + r;
-      acc += bf16_to_double(s.kring[((size_t)u * 32 + (j & 31)) * kHeadDim + tid]);
-    }
+    const uint16_t* ring = s.kring + (size_t)u * 32 * kHeadDim + tid;
+#pragma unroll
+    for (int r = 0; r < kCmpKernel; ++r) acc += bf16_to_double(ring[((kCmpStride * i + r) & 31) * kHeadDim]);
     s.kt[((size_t)u * s.nc_max + i) * kHeadDim + tid] = double_to_bf16_rne(acc / kCmpKernel);
     if (tid < 32) {
       double e = (double)s.se_tok[(size_t)u * s.T_max + kCmpStride * i + tid];
@@ -187,7 +199,7 @@ __global__ void __launch_bounds__(128) append_bulk_finish_kernel(LayerState s, c
 }
 
 cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, cudaStream_t st) {
-  append_one_kernel<<<s.U, 128, 0, st>>>(s, k, v);
+  append_one_kernel<<<s.U, kAppendThreads, 0, st>>>(s, k, v);
   return cudaGetLastError();
 }
 

@@ -237,9 +237,10 @@ class Parity:
             ev = st["evicted"][u]
             ev_gpu = {bb for bb in range(nb) if (ev[bb >> 5] >> (bb & 31)) & 1}
             assert ev_gpu == o.evicted, "eviction bitmap mismatch"
-            if r["gamma"] is not None:
-                num, den = st["gamma"][u]
-                assert den == len(r["D"]) and abs(num / max(den, 1) - r["gamma"]) < 1e-12
+            num, den = st["gamma"][u]
+            assert den == len(r["D"])
+            if r["gamma"] is not None and den > 0:   # gamma is undefined for an empty dynamic set
+                assert abs(num / den - r["gamma"]) < 1e-12
                 self.log.gammas.append(r["gamma"])
             self.log.fetched += len(r["fetch"])
             ref = o.attend(qb, r["S"])
