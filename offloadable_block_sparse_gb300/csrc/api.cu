@@ -243,8 +243,8 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   const size_t nc = std::max(d.nc_max, 1);
   c->score_chunks = cdiv(nc, kWindowsPerCta);
   int bpc = cdiv((long long)c->U * d.cap, 2ll * std::max(c->num_sms, 1));
-  bpc = std::min(std::max(bpc, 1), 16);
-  if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), d.cap);
+  bpc = std::min(std::max(bpc, 1), kMaxBlocksPerCta);
+  if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), kMaxBlocksPerCta);
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kAttendStages];
   __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
+  __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta];
   __shared__ int last, bad_any;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
@@ -42,39 +43,8 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
 
   const int chunk = blockIdx.x, u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = lane >> 2, t4 = lane & 3;
-  const Geometry geo = geometry(*s.T, s.nw, s.sink);
   const int G = s.G;
-  const int nsel = s.n_sel[u];
-  const int e0 = chunk * s.attend_blocks_per_cta;
-  const int nblk = max(0, min(e0 + s.attend_blocks_per_cta, nsel) - e0);
-  const int32_t* sel = s.sel + (size_t)u * s.cap;
-  const int32_t* sslot = s.sel_slot + (size_t)u * s.cap;
-  const uint32_t sbase = smem_u32(smem);
-
-  if (tid == 0) {
-    prefetch_tmap(&tmap);
-    for (int i = 0; i < kAttendStages; ++i) mbar_init(&bars[i], 1);
-    fence_mbar_init();
-    bad_any = 0;
-  }
-  __syncthreads();
-  auto issue = [&](int i) {  // entry e0+i into stage i % kAttendStages (thread 0 only)
-    int slot = sslot[e0 + i];
-    if (slot < 0 || slot >= s.cap) {
-      atomicOr(s.err, kErrBounds);
-      slot = 0;  // keep the copy in bounds; the result is flagged as invalid
-    }
-    const int flat = (s.unit_base + u) * s.cap + slot;
-    const int st = i % kAttendStages;
-    mbar_arrive_expect_tx(&bars[st], kStageBytes);
-    tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
-    tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
-  };
-  int issued = 0;
-  if (tid == 0) {
-    for (; issued < min(nblk, kAttendStages); ++issued) issue(issued);
-  }
-
+  // independent loads first: q fragments, the context length, the unit's selection size
   // q^T as the B operand: b0 = q[head gr][16ks + 2t4 .. +1], b1 = the same +8
   uint32_t qb[8][2];
   {
@@ -85,6 +55,40 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
       qb[ks][1] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4 + 8) : 0u;
     }
   }
+  const Geometry geo = geometry(*s.T, s.nw, s.sink);
+  const int nsel = s.n_sel[u];
+  const int e0 = chunk * s.attend_blocks_per_cta;
+  const int nblk = max(0, min(e0 + s.attend_blocks_per_cta, nsel) - e0);
+  const uint32_t sbase = smem_u32(smem);
+
+  if (tid < nblk) {  // this CTA's block ids and cache slots, in one round trip
+    s_blk[tid] = s.sel[(size_t)u * s.cap + e0 + tid];
+    int slot = s.sel_slot[(size_t)u * s.cap + e0 + tid];
+    if (slot < 0 || slot >= s.cap) {
+      atomicOr(s.err, kErrBounds);
+      slot = 0;  // keep the copy in bounds; the result is flagged as invalid
+    }
+    s_slot[tid] = slot;
+  }
+  if (tid == 0) {
+    prefetch_tmap(&tmap);
+    for (int i = 0; i < kAttendStages; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    bad_any = 0;
+  }
+  __syncthreads();
+  auto issue = [&](int i) {  // entry e0+i into stage i % kAttendStages (thread 0 only)
+    const int flat = (s.unit_base + u) * s.cap + s_slot[i];
+    const int st = i % kAttendStages;
+    mbar_arrive_expect_tx(&bars[st], kStageBytes);
+    tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
+    tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    for (; issued < min(nblk, kAttendStages); ++issued) issue(issued);
+  }
+
   const float sl2 = s.scale * 1.4426950408889634f;  // softmax in base 2
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float o[8][4];
@@ -108,8 +112,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
       break;
     }
     consumed = i + 1;
-    const int blk = sel[e0 + i];
-    const int valid = (blk == geo.nb - 1) ? geo.valid_tail : kBlock;
+    const int valid = (s_blk[i] == geo.nb - 1) ? geo.valid_tail : kBlock;
     const uint32_t stg = sbase + st * kStageBytes;
     if (tok0 < valid) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   __syncthreads();
   // CTA partial (base-2 max, sum, unnormalised output) for each head
   const int x = tid;  // head dimension
+  float* part0 = s.apart + ((size_t)u * s.attend_chunks + chunk) * kMaxGroup * kPartStride;
   for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
 #pragma unroll
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
         O += wo[(w * kMaxGroup + h) * kHeadDim + x] * f;
       }
     }
-    float* part = s.apart + (((size_t)u * s.attend_chunks + chunk) * kMaxGroup + h) * kPartStride;
+    float* part = part0 + h * kPartStride;
     if (x == 0) {
       part[0] = M;
       part[1] = L;
@@ -220,23 +224,42 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   if (!last) return;
   __threadfence();
   if (tid == 0) s.tickets[s.U + u] = 0;
-  for (int h = 0; h < G; ++h) {
-    const float* pb = s.apart + ((size_t)u * s.attend_chunks * kMaxGroup + h) * kPartStride;
+  // merge the unit's partials: all (m, l) pairs in one round trip, then every o value in flight at once
+  const int nch = s.attend_chunks;
+  const float* pu = s.apart + (size_t)u * nch * kMaxGroup * kPartStride;
+  float* pm = reinterpret_cast<float*>(smem);        // [nch][8] scale factors
+  float* pl = pm + nch * kMaxGroup;                  // [nch][8] sums
+  __shared__ float Mh[kMaxGroup], Lh[kMaxGroup];
+  for (int idx = tid; idx < nch * G; idx += blockDim.x) {
+    const int j = idx / G, h = idx % G;
+    const float* p = pu + ((size_t)j * kMaxGroup + h) * kPartStride;
+    pm[j * kMaxGroup + h] = __ldcg(p);
+    pl[j * kMaxGroup + h] = __ldcg(p + 1);
+  }
+  __syncthreads();
+  if (tid < G) {
     float M = -INFINITY;
-    for (int j = 0; j < s.attend_chunks; ++j) M = fmaxf(M, __ldcg(pb + (size_t)j * kMaxGroup * kPartStride));
-    float L = 0.f, O = 0.f;
-    if (M > -INFINITY) {
-      for (int j = 0; j < s.attend_chunks; ++j) {
-        const float* p = pb + (size_t)j * kMaxGroup * kPartStride;
-        const float mj = __ldcg(p);
-        if (mj > -INFINITY) {
-          const float f = exp2f(mj - M);
-          L += __ldcg(p + 1) * f;
-          O += __ldcg(p + 2 + x) * f;
-        }
-      }
+    for (int j = 0; j < nch; ++j) M = fmaxf(M, pm[j * kMaxGroup + tid]);
+    float L = 0.f;
+    for (int j = 0; j < nch; ++j) {
+      const float mj = pm[j * kMaxGroup + tid];
+      const float f = (mj > -INFINITY) ? exp2f(mj - M) : 0.f;
+      pm[j * kMaxGroup + tid] = f;
+      L += pl[j * kMaxGroup + tid] * f;
     }
-    const float r = L > 0.f ? O / L : 0.f;
+    Mh[tid] = M;
+    Lh[tid] = L;
+  }
+  __syncthreads();
+  for (int h = 0; h < G; ++h) {
+    float O = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < nch; ++j) {
+      const float f = pm[j * kMaxGroup + h];
+      const float ov = __ldcg(pu + ((size_t)j * kMaxGroup + h) * kPartStride + 2 + x);
+      O = fmaf(ov, f, O);
+    }
+    const float r = Lh[h] > 0.f ? O / Lh[h] : 0.f;
     out[((size_t)u * G + h) * kHeadDim + x] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
   }
 }

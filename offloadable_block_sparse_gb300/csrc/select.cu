@@ -89,8 +89,8 @@ __device__ void block_topk(const uint32_t* keys, uint8_t* flags, int lo, int hi,
 
 }  // namespace
 
-// grid (score_chunks, U), 256 threads.  Dynamic shared memory (phase 2):
-// sqw[nc_max] floats, keys[nb_max] uint32, flags[nb_max] bytes.
+// grid (score_chunks, U), 256 threads.  Dynamic shared memory (phase 2): window
+// scores, pooled s^e, block->slot map, radix keys, chunk stats, eviction words, flags.
 __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState s, const uint16_t* __restrict__ q) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ SelShared sh;
@@ -215,57 +215,89 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   if (tid == 0) s.tickets[u] = 0;
 
   // ---------------- phase 2: selection for unit u
-  float* sqw = reinterpret_cast<float*>(dsm);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(dsm + sizeof(float) * s.nc_max);
-  uint8_t* flags = reinterpret_cast<uint8_t*>(keys + s.nb_max);
+  // Every global value the selection needs is requested up front (one memory
+  // round trip); the rest runs from shared memory.
+  const int nb = geo.nb, ws = geo.ws;
+  const int nch = s.score_chunks;
+  float* sqw = reinterpret_cast<float*>(dsm);                   // [nc_max] window scores
+  float* sek = sqw + s.nc_max;                                  // [nb_max] pooled s^e
+  int32_t* b2s = reinterpret_cast<int32_t*>(sek + s.nb_max);    // [nb_max] block -> slot
+  uint32_t* keys = reinterpret_cast<uint32_t*>(b2s + s.nb_max); // [nb_max]
+  float* sp = reinterpret_cast<float*>(keys + s.nb_max);        // [nch][G][2] chunk stats
+  uint32_t* evw = reinterpret_cast<uint32_t*>(sp + nch * kMaxGroup * 2);  // [ev_words]
+  uint8_t* flags = reinterpret_cast<uint8_t*>(evw + s.ev_words);          // [nb_max]
+  const int per = (nb + blockDim.x - 1) / blockDim.x;
+  const int lo = min(tid * per, nb), hi = min(lo + per, nb);
+  const int words = (nb + 31) / 32;
+  for (int idx = tid; idx < nch * G; idx += blockDim.x) {
+    const int j = idx / G, h = idx % G;
+    const float* p = s.spart + (((size_t)u * nch + j) * kMaxGroup + h) * 2;
+    sp[(j * kMaxGroup + h) * 2] = __ldcg(p);
+    sp[(j * kMaxGroup + h) * 2 + 1] = __ldcg(p + 1);
+  }
+  for (int b = lo; b < hi; ++b) {
+    sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
+    b2s[b] = s.blk2slot[(size_t)u * s.nb_max + b];
+  }
+  for (int w = tid; w < words; w += blockDim.x) evw[w] = s.evicted[(size_t)u * s.ev_words + w];
+  int32_t* sblk = s.slot_blk + (size_t)u * s.cap;
+  const int my_slot_blk = tid < s.cap ? sblk[tid] : -1;
+  __syncthreads();
   if (tid < G) {
     float M = -INFINITY;
-    for (int j = 0; j < s.score_chunks; ++j)
-      M = fmaxf(M, __ldcg(s.spart + (((size_t)u * s.score_chunks + j) * kMaxGroup + tid) * 2));
+    for (int j = 0; j < nch; ++j) M = fmaxf(M, sp[(j * kMaxGroup + tid) * 2]);
     float S = 0.f;
-    for (int j = 0; j < s.score_chunks; ++j) {
-      const float* sp = s.spart + (((size_t)u * s.score_chunks + j) * kMaxGroup + tid) * 2;
-      const float mj = __ldcg(sp);
-      if (mj > -INFINITY) S += __ldcg(sp + 1) * expf(mj - M);
+    for (int j = 0; j < nch; ++j) {
+      const float mj = sp[(j * kMaxGroup + tid) * 2];
+      if (mj > -INFINITY) S += sp[(j * kMaxGroup + tid) * 2 + 1] * expf(mj - M);
     }
     sh.Mh[tid] = M;
     sh.invS[tid] = 1.f / S;
   }
   __syncthreads();
-  for (int i = tid; i < nc; i += blockDim.x) {
-    float acc = 0.f;
-    for (int h = 0; h < G; ++h)
-      acc += expf(__ldcg(s.zbuf + ((size_t)u * G + h) * s.nc_max + i) - sh.Mh[h]) * sh.invS[h];
-    sqw[i] = acc;
+  // s^q per window: the group's softmax probabilities summed over heads
+  for (int i0 = tid; i0 < nc; i0 += 4 * blockDim.x) {
+    float zv[4][kMaxGroup];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + r * blockDim.x;
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h)
+        zv[r][h] = (h < G && i < nc) ? __ldcg(s.zbuf + ((size_t)u * G + h) * s.nc_max + i) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = i0 + r * blockDim.x;
+      if (i >= nc) continue;
+      float acc = 0.f;
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h)
+        if (h < G) acc += expf(zv[r][h] - sh.Mh[h]) * sh.invS[h];
+      sqw[i] = acc;
+    }
   }
   __syncthreads();
-  const int nb = geo.nb, ws = geo.ws;
-  const int per = (nb + blockDim.x - 1) / blockDim.x;
-  const int lo = min(tid * per, nb), hi = min(lo + per, nb);
-  const uint32_t* ev = s.evicted + (size_t)u * s.ev_words;
+  // max-pool onto blocks; candidates lie strictly between the sink and the window
   for (int b = lo; b < hi; ++b) {
     const int wl = max(4 * b - 1, 0), wh = min(4 * b + 3, nc - 1);
     float m = -INFINITY;
     for (int i = wl; i <= wh; ++i) m = fmaxf(m, sqw[i]);
     s.sq_blk[(size_t)u * s.nb_max + b] = m;
     keys[b] = orderable(m);
-    const bool cand = b >= s.sink && b < ws;
-    flags[b] = cand ? F_CAND : 0;
+    flags[b] = (b >= s.sink && b < ws) ? F_CAND : 0;
   }
   __syncthreads();
   block_topk(keys, flags, lo, hi, s.k_q, F_CAND, F_Q, sh);
-  const float* seb = s.se_blk + (size_t)u * s.nb_max;
   for (int b = lo; b < hi; ++b) {
-    keys[b] = orderable(seb[b]);
-    const bool evb = (ev[b >> 5] >> (b & 31)) & 1u;
+    keys[b] = orderable(sek[b]);
+    const bool evb = (evw[b >> 5] >> (b & 31)) & 1u;
     if ((flags[b] & F_CAND) && !(flags[b] & F_Q) && !evb) flags[b] |= F_ELIG;
   }
   __syncthreads();
   block_topk(keys, flags, lo, hi, s.k_e, F_ELIG, F_E, sh);
 
-  // selection S, sticky eviction, new (non-resident) blocks
+  // selection S, blocks without a slot
   int nD = 0, nE = 0, nDnew = 0, nS = 0, nNew = 0;
-  const int32_t* b2s = s.blk2slot + (size_t)u * s.nb_max;
   for (int b = lo; b < hi; ++b) {
     uint8_t f = flags[b];
     const bool inS = b < geo.ns || b >= ws || (f & (F_Q | F_E));
@@ -285,32 +317,17 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     flags[b] = f;
   }
   __syncthreads();
-  {
-    const int words = (nb + 31) / 32;
-    uint32_t* evw = s.evicted + (size_t)u * s.ev_words;
-    for (int w = tid; w < words; w += blockDim.x) {
-      uint32_t bits = 0;
-      for (int j = 0; j < 32; ++j) {
-        const int b = 32 * w + j;
-        if (b < nb && (flags[b] & F_CAND) && !(flags[b] & (F_Q | F_E))) bits |= 1u << j;
-      }
-      if (bits) evw[w] |= bits;
+  // sticky eviction: candidates outside D are dropped for good
+  for (int w = tid; w < words; w += blockDim.x) {
+    uint32_t bits = 0;
+    for (int j = 0; j < 32; ++j) {
+      const int b = 32 * w + j;
+      if (b < nb && (flags[b] & F_CAND) && !(flags[b] & (F_Q | F_E))) bits |= 1u << j;
     }
+    if (bits & ~evw[w]) s.evicted[(size_t)u * s.ev_words + w] = evw[w] | bits;
   }
   // free slots: empty, or holding a block that left the selection (ascending)
-  int32_t* sblk = s.slot_blk + (size_t)u * s.cap;
-  int my_slot_blk = -1, is_free = 0;
-  if (tid < s.cap) {
-    my_slot_blk = sblk[tid];
-    is_free = !(my_slot_blk >= 0 && my_slot_blk < nb && (flags[my_slot_blk] & F_S));
-  }
-  int had_prev = 0;
-  {
-    int tot;
-    had_prev = (tid < s.cap && my_slot_blk >= 0) ? 1 : 0;
-    block_scan_excl(had_prev, sh.scan, &tot);
-    had_prev = tot > 0;
-  }
+  const int is_free = tid < s.cap && !(my_slot_blk >= 0 && my_slot_blk < nb && (flags[my_slot_blk] & F_S));
   int n_free;
   const int free_rank = block_scan_excl(is_free, sh.scan, &n_free);
   if (is_free) sh.free_by_rank[free_rank] = tid;
@@ -320,18 +337,19 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     if (tid == 0) atomicOr(s.err, kErrBounds);
     n_new = n_free;
   }
-  int32_t* b2s_w = s.blk2slot + (size_t)u * s.nb_max;
+  int32_t* b2s_g = s.blk2slot + (size_t)u * s.nb_max;
   if (is_free && my_slot_blk >= 0) {
-    if (my_slot_blk < s.nb_max) b2s_w[my_slot_blk] = -1;
+    if (my_slot_blk < s.nb_max) b2s_g[my_slot_blk] = -1;
     else atomicOr(s.err, kErrBounds);
   }
-  __syncthreads();
+  __syncthreads();  // free_by_rank complete
   int32_t* fl = s.fetch + (size_t)u * s.cap * 2;
   for (int b = lo; b < hi; ++b) {
     if (!(flags[b] & F_NEW)) continue;
     if (new_rank < n_new) {
       const int slot = sh.free_by_rank[new_rank];
-      b2s_w[b] = slot;
+      b2s[b] = slot;
+      b2s_g[b] = slot;
       sblk[slot] = b;
       fl[2 * new_rank] = b;
       fl[2 * new_rank + 1] = slot;
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     if (pos < s.cap) {
       sel[pos] = b;
       kind[pos] = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
-      sslot[pos] = b2s_w[b];
+      sslot[pos] = b2s[b];
     } else {
       atomicOr(s.err, kErrBounds);
     }
@@ -363,11 +381,27 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     kind[i] = -1;
     sslot[i] = -1;
   }
-  int sumD, sumDnew, sumE;
-  block_scan_excl(nD, sh.scan, &sumD);
-  block_scan_excl(nDnew, sh.scan, &sumDnew);
-  block_scan_excl(nE, sh.scan, &sumE);
+  // unit totals: |D|, |D \ S_prev|, |E|, whether any block was resident before
+  int4 v = make_int4(nD, nDnew, nE, (tid < s.cap && my_slot_blk >= 0) ? 1 : 0);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
+    v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
+  }
+  __shared__ int4 wsum[kScoreWarps];
+  if (lane == 0) wsum[warp] = v;
+  __syncthreads();
   if (tid == 0) {
+    int4 t = wsum[0];
+    for (int w = 1; w < kScoreWarps; ++w) {
+      t.x += wsum[w].x;
+      t.y += wsum[w].y;
+      t.z += wsum[w].z;
+      t.w += wsum[w].w;
+    }
+    const int sumD = t.x, sumDnew = t.y, sumE = t.z, had_prev = t.w > 0;
     s.n_sel[u] = min(total_S, s.cap);
     s.n_fetch[u] = n_new;
     s.gamma[2 * u] = sumD - sumDnew;
@@ -386,7 +420,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
 }
 
 size_t score_select_smem(const LayerState& s) {
-  return sizeof(float) * s.nc_max + sizeof(uint32_t) * s.nb_max + s.nb_max + 16;
+  return sizeof(float) * s.nc_max + 3 * sizeof(uint32_t) * s.nb_max +
+         sizeof(float) * s.score_chunks * kMaxGroup * 2 + sizeof(uint32_t) * s.ev_words + s.nb_max + 16;
 }
 
 cudaError_t init_score_select(const LayerState& s) {

@@ -68,7 +68,7 @@ def test_short_context_everything_selected():
     wl = syn.Workload("short", layers=1, batch=2, q_heads=16, kv_heads=2, context=40, k_q=4, k_e=12,
                       window_tokens=256, steps=30)
     log, _ = run(wl, wl.steps)
-    assert log.unit_steps == 60
+    assert log.unit_steps == 30 * 4
 
 
 def test_no_sink_no_window_query_aware_only():
