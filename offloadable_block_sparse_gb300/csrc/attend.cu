@@ -251,15 +251,28 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
     Lh[tid] = L;
   }
   __syncthreads();
-  for (int h = 0; h < G; ++h) {
-    float O = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < nch; ++j) {
-      const float f = pm[j * kMaxGroup + h];
-      const float ov = __ldcg(pu + ((size_t)j * kMaxGroup + h) * kPartStride + 2 + x);
-      O = fmaf(ov, f, O);
-    }
-    const float r = Lh[h] > 0.f ? O / Lh[h] : 0.f;
+  // o partials: 8 chunks x 8 heads of loads in flight per batch
+  float O[kMaxGroup];
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) O[h] = 0.f;
+  for (int j0 = 0; j0 < nch; j0 += 8) {
+    float ov[8][kMaxGroup];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h)
+        ov[r][h] = (j0 + r < nch && h < G) ? __ldcg(pu + ((size_t)(j0 + r) * kMaxGroup + h) * kPartStride + 2 + x)
+                                           : 0.f;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int h = 0; h < kMaxGroup; ++h)
+        if (j0 + r < nch && h < G) O[h] = fmaf(ov[r][h], pm[(j0 + r) * kMaxGroup + h], O[h]);
+  }
+#pragma unroll
+  for (int h = 0; h < kMaxGroup; ++h) {
+    if (h >= G) break;
+    const float r = Lh[h] > 0.f ? O[h] / Lh[h] : 0.f;
     out[((size_t)u * G + h) * kHeadDim + x] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
   }
 }
