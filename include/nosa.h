@@ -210,6 +210,37 @@ nosa_status nosa_export_state(nosa_ctx* ctx, int layer, const nosa_state_view* v
 
 const char* nosa_status_string(nosa_status s);
 
+/* Sparse attention over a caller-owned block cache that allocates nothing.
+ * The paper has no counterpart: this exists for callers that must not call
+ * cudaMalloc (a memory pool they do not own, an allocator under capture or
+ * audit, a path that may not grow the device footprint after start-up).
+ * It runs the same split-K kernel as nosa_attend without a context; its
+ * scratch (split-K partials, merge tickets, context length) is one fixed
+ * file-scope device array of about 8.5 MB that every GPU loading this library
+ * keeps until the process exits.
+ *   q        device bf16 [units][group][128]
+ *   cache    device bf16 [units][cache_slots][2][64][128] (K then V of each
+ *            slot's block, 16-byte aligned), the layout of a context's cache
+ *   sel      device int32 [units][cache_slots] selected block ids, ascending
+ *   sel_slot device int32 [units][cache_slots] slot of each selected block
+ *   n_sel    device int32 [units] number of selected blocks per unit
+ *   context_len  tokens per sequence; block ceil(context_len/64)-1 is the
+ *            partial tail and only its first tokens are attended
+ *   softmax_scale 0 => 1/sqrt(128);  out device bf16 [units][group][128]
+ * Limits: units <= 1024 and units * ceil(cache_slots / chunk) <= 2048 split-K
+ * partials (chunk <= 16 blocks); larger requests return NOSA_ERR_CAPACITY
+ * before anything is queued.  Calls never allocate, so their scratch is shared:
+ * calls that overlap on the GPU (other streams, other threads) race and must be
+ * serialised by the caller; each call clears the tickets it uses.  The first
+ * call on a device does a one-time set-up (looks up the scratch address and
+ * sets the kernel's shared-memory limit); make that first call before any
+ * stream capture.  Asynchronous on `stream`; out-of-range slots are clamped and
+ * make that unit's output meaningless. */
+nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* cache, const int32_t* sel,
+                                const int32_t* sel_slot, const int32_t* n_sel, int units, int group,
+                                int cache_slots, int context_len, float softmax_scale, uint16_t* out,
+                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ globals().update({n: i for i, n in enumerate(STATUS_NAMES)})
 EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_destroy", "nosa_set_stream",
            "nosa_set_eviction_head", "nosa_append_kv", "nosa_select", "nosa_fetch", "nosa_attend", "nosa_step",
            "nosa_step_host", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
-           "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string"]
+           "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string",
+           "nosa_attend_noalloc"]
 
 
 class nosa_config(ctypes.Structure):
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
             "nosa_reset_stats": [vp],
             "nosa_debug_scores": [vp, i32, p, p],
             "nosa_export_state": [vp, i32, ctypes.POINTER(nosa_state_view)],
+            "nosa_attend_noalloc": [p, p, p, p, p, i32, i32, i32, i32, ctypes.c_float, p, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -224,3 +226,11 @@ def nosa_export_state(ctx, layer, **arrays) -> None:
     """Keyword arrays (host numpy) named as the fields of nosa_state_view."""
     view = nosa_state_view(**{k: _ptr(v) for k, v in arrays.items()})
     _check(lib().nosa_export_state(ctx, layer, ctypes.byref(view)), "nosa_export_state")
+
+
+def nosa_attend_noalloc(q, cache, sel, sel_slot, n_sel, units, group, cache_slots, context_len, out,
+                        softmax_scale=0.0, stream=0) -> None:
+    """Attention over a caller-owned block cache without any device allocation (see include/nosa.h)."""
+    _check(lib().nosa_attend_noalloc(_ptr(q), _ptr(cache), _ptr(sel), _ptr(sel_slot), _ptr(n_sel), units, group,
+                                     cache_slots, context_len, softmax_scale, _ptr(out), stream or None),
+           "nosa_attend_noalloc")

@@ -1,0 +1,90 @@
+"""nosa_attend_noalloc against nosa_attend.
+
+The no-allocation entry point serves callers that must not call cudaMalloc
+(they run inside a memory pool they do not own, under an allocator that is
+being captured or audited, or on a path that may not grow the device footprint
+after start-up).  It runs the split-K attention with its scratch in a fixed
+device array.  This test drives a context for a few decode steps, rebuilds that
+context's block cache from the known K/V, and checks that two no-allocation
+calls in a row reproduce the context's attention output within the parity
+tolerance used for the oracle comparison (max-abs 2e-2, mean-abs 2e-3).
+The file name sorts last so that a run stopping at the first failure has
+already run every other test.
+"""
+import math
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from offloadable_block_sparse_gb300 import nosa as N  # noqa: E402
+
+
+def test_noalloc_attend_matches_context_attend_twice():
+    torch.cuda.set_device(0)
+    B, Hq, Hkv, d, T0, steps = 3, 16, 2, 128, 2000, 3
+    G, U = Hq // Hkv, B * Hkv
+    cfg = N.make_config(num_layers=1, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=4, k_e=12,
+                        window_tokens=256, max_context=T0 + steps)
+    stream = torch.cuda.current_stream()
+    ctx = N.nosa_create(cfg, stream.cuda_stream)
+    try:
+        cap = N.nosa_query_sizes(cfg).cache_slots
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        Kall = torch.randn((B, Hkv, T0 + steps, d), generator=gen, device="cuda").to(torch.bfloat16)
+        Vall = torch.randn((B, Hkv, T0 + steps, d), generator=gen, device="cuda").to(torch.bfloat16)
+        W1 = (torch.randn((Hkv, d, 128)) / math.sqrt(d)).float().contiguous()
+        W2 = (torch.randn((Hkv, 128)) / math.sqrt(128)).float().contiguous()
+        N.nosa_set_eviction_head(ctx, 0, W1.numpy(), W2.numpy())
+        N.nosa_append_kv(ctx, 0, Kall[:, :, :T0].contiguous().view(torch.int16),
+                         Vall[:, :, :T0].contiguous().view(torch.int16), T0)
+        out_ctx = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+        for t in range(steps):
+            q = torch.randn((B, Hq, d), generator=gen, device="cuda")
+            q = (q / q.norm(dim=-1, keepdim=True) * math.sqrt(d)).to(torch.bfloat16)
+            k = Kall[:, :, T0 + t].contiguous()
+            v = Vall[:, :, T0 + t].contiguous()
+            N.nosa_step(ctx, 0, q.view(torch.int16), k.view(torch.int16), v.view(torch.int16),
+                        out_ctx.view(torch.int16))
+        assert N.nosa_sync(ctx) == N.NOSA_OK
+        T = T0 + steps
+        sel = np.zeros((U, cap), np.int32)
+        sel_slot = np.zeros((U, cap), np.int32)
+        n_sel = np.zeros(U, np.int32)
+        N.nosa_export_state(ctx, 0, sel=sel, sel_slot=sel_slot, n_sel=n_sel)
+
+        # the context's block cache, rebuilt from the known K/V: slot s of unit u holds
+        # block sel[u][i] (K then V, rows past the context zero)
+        cache = torch.zeros((U, cap, 2, 64, d), dtype=torch.bfloat16, device="cuda")
+        Ku = Kall.reshape(U, T, d)
+        Vu = Vall.reshape(U, T, d)
+        for u in range(U):
+            for i in range(n_sel[u]):
+                b, sl = int(sel[u, i]), int(sel_slot[u, i])
+                e = min(64 * b + 64, T)
+                cache[u, sl, 0, :e - 64 * b] = Ku[u, 64 * b:e]
+                cache[u, sl, 1, :e - 64 * b] = Vu[u, 64 * b:e]
+        sel_d = torch.from_numpy(sel).cuda()
+        slot_d = torch.from_numpy(sel_slot).cuda()
+        nsel_d = torch.from_numpy(n_sel).cuda()
+        ref = out_ctx.float()
+        for _ in range(2):  # two calls in a row share the fixed scratch
+            out = torch.full((B, Hq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+            N.nosa_attend_noalloc(q.view(torch.int16), cache.view(torch.int16), sel_d, slot_d, nsel_d, U, G, cap,
+                                  T, out.view(torch.int16), stream=stream.cuda_stream)
+            torch.cuda.synchronize()
+            err = (out.float() - ref).abs()
+            assert torch.isfinite(out.float()).all()
+            assert err.max().item() <= 2e-2 and err.mean().item() <= 2e-3, (err.max().item(), err.mean().item())
+        # sizes beyond the fixed scratch are refused before anything is queued
+        with pytest.raises(N.NosaError) as e:
+            N.nosa_attend_noalloc(q.view(torch.int16), cache.view(torch.int16), sel_d, slot_d, nsel_d, 5000, G, cap,
+                                  T, out.view(torch.int16), stream=stream.cuda_stream)
+        assert e.value.status == N.NOSA_ERR_CAPACITY
+    finally:
+        N.nosa_destroy(ctx)
