@@ -173,11 +173,14 @@ nosa_status nosa_select(nosa_ctx* ctx, int layer, const uint16_t* q, int32_t* se
 nosa_status nosa_fetch(nosa_ctx* ctx, int layer);
 
 /* Attention of q (device bf16 [B][Hq][d]) over the selected blocks; writes
- * out (device bf16 [B][Hq][d]).  Needs a select + fetch for the current T. */
+ * out (device bf16 [B][Hq][d]).  Needs a selection for the current T.  If
+ * nosa_fetch has not run since that selection, the attention CTAs copy the
+ * newly selected blocks from the pinned host store themselves (and write them
+ * to their cache slots), so no separate gather pass is needed. */
 nosa_status nosa_attend(nosa_ctx* ctx, int layer, const uint16_t* q, uint16_t* out);
 
-/* append(1 token) + select + fetch + attend.  k_new, v_new: device bf16
- * [B][Hkv][d]; q, out: device bf16 [B][Hq][d]. */
+/* append(1 token) + select + attend with the fetch fused into attend (three
+ * kernels).  k_new, v_new: device bf16 [B][Hkv][d]; q, out: device bf16 [B][Hq][d]. */
 nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                       const uint16_t* v_new, uint16_t* out);
 

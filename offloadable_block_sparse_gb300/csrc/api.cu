@@ -79,7 +79,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 void free_ctx(nosa_ctx* c) {
   void* dev[] = {c->cache, c->kt, c->kring, c->se_tok, c->se_win, c->se_blk, c->W1, c->W2, c->slot_blk,
-                 c->blk2slot, c->sel, c->sel_kind, c->sel_slot, c->n_sel, c->fetch, c->n_fetch, c->gamma,
+                 c->blk2slot, c->sel, c->sel_kind, c->sel_slot, c->sel_new, c->n_sel, c->fetch, c->n_fetch, c->gamma,
                  c->evicted, c->T, c->err, c->stats, c->zbuf, c->spart, c->sq_blk, c->apart, c->tickets,
                  c->stage_q, c->stage_k, c->stage_v, c->stage_out, c->bulk_k, c->bulk_v};
   for (void* p : dev)
@@ -126,6 +126,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.sel = c->sel + lu * d.cap;
   s.sel_kind = c->sel_kind + lu * d.cap;
   s.sel_slot = c->sel_slot + lu * d.cap;
+  s.sel_new = c->sel_new + lu * d.cap;
   s.n_sel = c->n_sel + lu;
   s.fetch = c->fetch + lu * d.cap * 2;
   s.n_fetch = c->n_fetch + lu;
@@ -238,6 +239,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   c->T_host.assign(c->L, 0);
   c->sel_T.assign(c->L, -1);
+  c->fetch_T.assign(c->L, -1);
 
   const size_t LU = (size_t)c->L * c->U;
   const size_t nc = std::max(d.nc_max, 1);
@@ -285,6 +287,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   dalloc(&c->sel, LU * d.cap * 4);
   dalloc(&c->sel_kind, LU * d.cap * 4);
   dalloc(&c->sel_slot, LU * d.cap * 4);
+  dalloc(&c->sel_new, LU * d.cap * 4);
   dalloc(&c->n_sel, LU * 4);
   dalloc(&c->fetch, LU * d.cap * 8);
   dalloc(&c->n_fetch, LU * 4);
@@ -321,6 +324,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   ok = ok && cudaMemset(c->sel, 0xFF, LU * d.cap * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->sel_kind, 0xFF, LU * d.cap * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->sel_slot, 0xFF, LU * d.cap * 4) == cudaSuccess;
+  ok = ok && cudaMemset(c->sel_new, 0, LU * d.cap * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->n_sel, 0, LU * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->fetch, 0xFF, LU * d.cap * 8) == cudaSuccess;
   ok = ok && cudaMemset(c->n_fetch, 0, LU * 4) == cudaSuccess;
@@ -455,6 +459,7 @@ nosa_status nosa_fetch(nosa_ctx* c, int layer) {
   if (st != NOSA_OK) return st;
   if (c->sel_T[layer] != c->T_host[layer]) return NOSA_ERR_STATE;
   CK(launch_gather(layer_state(c, layer), c->gather_ctas, c->stream));
+  c->fetch_T[layer] = c->T_host[layer];
   return NOSA_OK;
 }
 
@@ -463,7 +468,9 @@ nosa_status nosa_attend(nosa_ctx* c, int layer, const uint16_t* q, uint16_t* out
   if (st != NOSA_OK) return st;
   if (!q || !out) return NOSA_ERR_INVALID_ARG;
   if (c->sel_T[layer] != c->T_host[layer]) return NOSA_ERR_STATE;
-  CK(launch_attend(layer_state(c, layer), &c->tmap_cache, q, out, c->stream));
+  // without a nosa_fetch since the selection, the attend CTAs fetch the new blocks themselves
+  const int fused = c->fetch_T[layer] != c->T_host[layer];
+  CK(launch_attend(layer_state(c, layer), &c->tmap_cache, q, out, fused, c->stream));
   return NOSA_OK;
 }
 
@@ -476,8 +483,7 @@ nosa_status nosa_step(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t*
   const LayerState s = layer_state(c, layer);
   CK(launch_append_one(s, k_new, v_new, c->stream));
   CK(launch_score_select(s, q, c->stream));
-  CK(launch_gather(s, c->gather_ctas, c->stream));
-  CK(launch_attend(s, &c->tmap_cache, q, out, c->stream));
+  CK(launch_attend(s, &c->tmap_cache, q, out, 1, c->stream));  // the fetch runs inside attend
   c->T_host[layer] += 1;
   c->sel_T[layer] = c->T_host[layer];
   return NOSA_OK;

@@ -31,11 +31,11 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int t
 
 __global__ void __launch_bounds__(kAttendThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap tmap, LayerState s, const uint16_t* __restrict__ q,
-                  uint16_t* __restrict__ out) {
+                  uint16_t* __restrict__ out, int fused_fetch) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kAttendStages];
   __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
-  __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta];
+  __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta], s_new[kMaxBlocksPerCta];
   __shared__ int last, bad_any;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
       slot = 0;  // keep the copy in bounds; the result is flagged as invalid
     }
     s_slot[tid] = slot;
+    s_new[tid] = fused_fetch ? s.sel_new[(size_t)u * s.cap + e0 + tid] : 0;
   }
   if (tid == 0) {
     prefetch_tmap(&tmap);
@@ -77,17 +78,39 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
     bad_any = 0;
   }
   __syncthreads();
-  auto issue = [&](int i) {  // entry e0+i into stage i % kAttendStages (thread 0 only)
-    const int flat = (s.unit_base + u) * s.cap + s_slot[i];
+  // Stage i % kAttendStages receives entry e0+i: a cached block by TMA (thread 0),
+  // or -- when the fetch is fused in -- a block without a slot straight from the
+  // pinned host store by cp.async of all threads (rows past the context zero-filled).
+  // One cp.async group is committed per entry (empty for TMA entries).
+  auto issue = [&](int i) {
     const int st = i % kAttendStages;
-    mbar_arrive_expect_tx(&bars[st], kStageBytes);
-    tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
-    tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
+    const bool fresh = i < nblk && s_new[i];
+    if (tid == 0 && i < nblk) {
+      if (fresh) {
+        mbar_arrive(&bars[st]);
+      } else {
+        const int flat = (s.unit_base + u) * s.cap + s_slot[i];
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[st], kStageBytes);
+        tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
+        tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
+      }
+    }
+    if (fresh) {
+      const int rows = (s_blk[i] == geo.nb - 1) ? geo.valid_tail : kBlock;
+      const uint16_t* src = s.host_kv + ((size_t)u * s.nb_max + s_blk[i]) * 2 * kBlockElems;
+#pragma unroll 4
+      for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
+        const int idx = tid + j * kAttendThreads;  // 16-byte chunk: K|V, row, chunk of the 256-byte row
+        const int kv = idx >> 10, r = (idx >> 4) & 63, cc = idx & 15;
+        cp_async_16(swz(sbase + st * kStageBytes, cc >> 3, kv, r, cc & 7),
+                    src + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8, r < rows ? 16u : 0u);
+      }
+    }
+    cp_async_commit();
   };
-  int issued = 0;
-  if (tid == 0) {
-    for (; issued < min(nblk, kAttendStages); ++issued) issue(issued);
-  }
+  for (int i = 0; i < kAttendStages; ++i) issue(i);
+  int issued = kAttendStages;
 
   const float sl2 = s.scale * 1.4426950408889634f;  // softmax in base 2
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -106,6 +129,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   for (int i = 0; i < nblk; ++i) {
     const int st = i % kAttendStages;
     const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((i / kAttendStages) & 1), kWaitLimit);
+    cp_async_wait<kAttendStages - 1>();  // this entry's cp.async group (if any) has landed
     if (__syncthreads_or(!okw)) {
       if (tid == 0) atomicOr(s.err, kErrTimeout);
       bad_any = 1;
@@ -158,14 +182,26 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
         mma_16816(o[mt], a, pb0, pb1);
       }
     }
-    __syncthreads();  // every warp is done with this stage
-    if (tid == 0 && issued < nblk) {
-      issue(issued);
-      ++issued;
+    if (s_new[i]) {  // a fetched block also goes to its cache slot for later steps
+      uint16_t* dst = s.cache + ((size_t)u * s.cap + s_slot[i]) * 2 * kBlockElems;
+#pragma unroll 4
+      for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
+        const int idx = tid + j * kAttendThreads;
+        const int kv = idx >> 10, r = (idx >> 4) & 63, cc = idx & 15;
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "r"(swz(stg, cc >> 3, kv, r, cc & 7)));
+        *reinterpret_cast<uint4*>(dst + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8) = v;
+      }
     }
+    __syncthreads();  // every warp is done with this stage
+    issue(issued);
+    ++issued;
   }
+  cp_async_wait_all();
   if (bad_any && tid == 0) {  // drain copies still in flight before the shared memory is reused
-    for (int i = consumed; i < issued; ++i)
+    for (int i = consumed; i < min(issued, nblk); ++i)
       mbar_wait_bounded(&bars[i % kAttendStages], (uint32_t)((i / kAttendStages) & 1), kWaitLimit);
   }
   __syncthreads();
@@ -284,9 +320,9 @@ cudaError_t init_attend() {
 }
 
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
-                          cudaStream_t st) {
+                          int fused_fetch, cudaStream_t st) {
   const size_t smem = attend_smem_bytes();
-  attend_kernel<<<dim3(s.attend_chunks, s.U), kAttendThreads, smem, st>>>(*tmap, s, q, out);
+  attend_kernel<<<dim3(s.attend_chunks, s.U), kAttendThreads, smem, st>>>(*tmap, s, q, out, fused_fetch);
   return cudaGetLastError();
 }
 

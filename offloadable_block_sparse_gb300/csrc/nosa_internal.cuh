@@ -90,6 +90,7 @@ struct LayerState {
   int32_t* sel;           // [U][cap]
   int32_t* sel_kind;      // [U][cap]
   int32_t* sel_slot;      // [U][cap]
+  int32_t* sel_new;       // [U][cap] 1: the block had no slot before this selection (fetched)
   int32_t* n_sel;         // [U]
   int32_t* fetch;         // [U][cap][2]
   int32_t* n_fetch;       // [U]
@@ -126,7 +127,7 @@ struct nosa_ctx {
   void* dev_block;  // one allocation holding everything below
   uint16_t *cache, *kt, *kring;
   float *se_tok, *se_win, *se_blk, *W1, *W2;
-  int32_t *slot_blk, *blk2slot, *sel, *sel_kind, *sel_slot, *n_sel, *fetch, *n_fetch, *gamma;
+  int32_t *slot_blk, *blk2slot, *sel, *sel_kind, *sel_slot, *sel_new, *n_sel, *fetch, *n_fetch, *gamma;
   uint32_t* evicted;
   int *T, *err;
   nosa::DevStats* stats;
@@ -143,6 +144,7 @@ struct nosa_ctx {
   // host mirrors
   std::vector<int> T_host;
   std::vector<int> sel_T;   // T at the last selection (-1: none), host view
+  std::vector<int> fetch_T; // T at the last nosa_fetch (-1: none): attend fetches itself otherwise
   int failed;               // latched nosa_status of a device-side error
 };
 
@@ -153,8 +155,11 @@ cudaError_t launch_append_bulk(const LayerState& s, const uint16_t* k, const uin
                                int n, cudaStream_t st);
 cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, cudaStream_t st);
 cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st);
+// fused_fetch != 0: blocks marked in sel_new are copied from the pinned host
+// store by the attend CTAs themselves (and written back to their slots), so no
+// separate gather launch is needed.
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
-                          cudaStream_t st);
+                          int fused_fetch, cudaStream_t st);
 size_t score_select_smem(const LayerState& s);
 // one-time kernel attributes (dynamic shared memory limits), called by nosa_create
 cudaError_t init_append(const LayerState& s);

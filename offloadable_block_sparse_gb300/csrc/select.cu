@@ -31,60 +31,74 @@ struct SelShared {
   float Mh[kMaxGroup], invS[kMaxGroup];
 };
 
-// Top-k over the blocks whose flag has `valid` set: sets `mark` on the k largest
-// keys, ties to the lower block index.  Radix select on the 32-bit keys
-// (4 passes of 8 bits), then the tied keys are taken in block order.
-// Blocks are split into contiguous per-thread ranges [lo, hi).
-__device__ void block_topk(const uint32_t* keys, uint8_t* flags, int lo, int hi, int k, uint8_t valid, uint8_t mark,
-                           SelShared& sh) {
-  const int tid = threadIdx.x;
-  int cnt = 0;
-  for (int b = lo; b < hi; ++b) cnt += (flags[b] & valid) ? 1 : 0;
-  int total;
-  block_scan_excl(cnt, sh.scan, &total);
+// Top-k over the blocks whose flag has `valid` set, run by one warp: sets `mark`
+// on the k largest keys, ties to the lower block index.  Radix select on the
+// 32-bit keys (4 passes of 8 bits; histogram in shared memory, bins scanned
+// with warp shuffles), then the keys equal to the k-th largest are taken in
+// ascending block order with ballots.  No block-wide barrier.
+__device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, uint8_t valid, uint8_t mark,
+                          int* hist) {
+  const int lane = threadIdx.x & 31;
   if (k <= 0) return;
-  if (total <= k) {
-    for (int b = lo; b < hi; ++b)
+  int cnt = 0;
+  for (int b = lane; b < n; b += 32) cnt += (flags[b] & valid) ? 1 : 0;
+  cnt = warp_sum(cnt);
+  if (cnt <= k) {
+    for (int b = lane; b < n; b += 32)
       if (flags[b] & valid) flags[b] |= mark;
-    __syncthreads();
+    __syncwarp();
     return;
   }
   uint32_t prefix = 0, pmask = 0;
   int need = k;
   for (int shift = 24; shift >= 0; shift -= 8) {
-    sh.hist[tid] = 0;
-    __syncthreads();
-    for (int b = lo; b < hi; ++b)
-      if ((flags[b] & valid) && (keys[b] & pmask) == prefix) atomicAdd(&sh.hist[(keys[b] >> shift) & 255], 1);
-    __syncthreads();
-    const int v = sh.hist[255 - tid];  // digits from the top
-    int tot;
-    const int excl = block_scan_excl(v, sh.scan, &tot);
-    if (excl < need && excl + v >= need) {
-      sh.digit = 255 - tid;
-      sh.above = excl;
+    for (int i = lane; i < 256; i += 32) hist[i] = 0;
+    __syncwarp();
+    for (int b = lane; b < n; b += 32)
+      if ((flags[b] & valid) && (keys[b] & pmask) == prefix) atomicAdd(&hist[(keys[b] >> shift) & 255], 1);
+    __syncwarp();
+    int c[8], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // lane owns 8 bins counted down from the top digit
+      c[j] = hist[255 - (8 * lane + j)];
+      tot += c[j];
     }
-    __syncthreads();
-    need -= sh.above;
-    prefix |= (uint32_t)sh.digit << shift;
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - tot, fd = -1, fa = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (fd < 0 && run < need && run + c[j] >= need) {
+        fd = 255 - (8 * lane + j);
+        fa = run;
+      }
+      run += c[j];
+    }
+    const unsigned int m = __ballot_sync(0xffffffffu, fd >= 0);
+    const int src = __ffs(m) - 1;
+    const int digit = __shfl_sync(0xffffffffu, fd, src);
+    need -= __shfl_sync(0xffffffffu, fa, src);
+    prefix |= (uint32_t)digit << shift;
     pmask |= 255u << shift;
-    __syncthreads();
+    __syncwarp();
   }
   // prefix is the k-th largest key; `need` keys equal to it are taken, lowest blocks first
-  int ties = 0;
-  for (int b = lo; b < hi; ++b) ties += ((flags[b] & valid) && keys[b] == prefix) ? 1 : 0;
-  int tt;
-  int rank = block_scan_excl(ties, sh.scan, &tt);
-  for (int b = lo; b < hi; ++b) {
-    if (!(flags[b] & valid)) continue;
-    if (keys[b] > prefix) {
-      flags[b] |= mark;
-    } else if (keys[b] == prefix) {
-      if (rank < need) flags[b] |= mark;
-      ++rank;
-    }
+  int taken = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int b = base + lane;
+    const bool v = b < n && (flags[b] & valid);
+    const uint32_t key = v ? keys[b] : 0u;
+    const bool tie = v && key == prefix;
+    const unsigned int tm = __ballot_sync(0xffffffffu, tie);
+    const int rank = taken + __popc(tm & ((1u << lane) - 1u));
+    if ((v && key > prefix) || (tie && rank < need)) flags[b] |= mark;
+    taken += __popc(tm);
   }
-  __syncthreads();
+  __syncwarp();
 }
 
 }  // namespace
@@ -287,14 +301,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     flags[b] = (b >= s.sink && b < ws) ? F_CAND : 0;
   }
   __syncthreads();
-  block_topk(keys, flags, lo, hi, s.k_q, F_CAND, F_Q, sh);
+  if (warp == 0) warp_topk(keys, flags, nb, s.k_q, F_CAND, F_Q, sh.hist);
+  __syncthreads();
   for (int b = lo; b < hi; ++b) {
     keys[b] = orderable(sek[b]);
     const bool evb = (evw[b >> 5] >> (b & 31)) & 1u;
     if ((flags[b] & F_CAND) && !(flags[b] & F_Q) && !evb) flags[b] |= F_ELIG;
   }
   __syncthreads();
-  block_topk(keys, flags, lo, hi, s.k_e, F_ELIG, F_E, sh);
+  if (warp == 0) warp_topk(keys, flags, nb, s.k_e, F_ELIG, F_E, sh.hist);
+  __syncthreads();
 
   // selection S, blocks without a slot
   int nD = 0, nE = 0, nDnew = 0, nS = 0, nNew = 0;
@@ -364,6 +380,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   int32_t* sel = s.sel + (size_t)u * s.cap;
   int32_t* kind = s.sel_kind + (size_t)u * s.cap;
   int32_t* sslot = s.sel_slot + (size_t)u * s.cap;
+  int32_t* snew = s.sel_new + (size_t)u * s.cap;
   for (int b = lo; b < hi; ++b) {
     const uint8_t f = flags[b];
     if (!(f & F_S)) continue;
@@ -371,6 +388,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
       sel[pos] = b;
       kind[pos] = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
       sslot[pos] = b2s[b];
+      snew[pos] = (f & F_NEW) ? 1 : 0;
     } else {
       atomicOr(s.err, kErrBounds);
     }
@@ -380,6 +398,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     sel[i] = -1;
     kind[i] = -1;
     sslot[i] = -1;
+    snew[i] = 0;
   }
   // unit totals: |D|, |D \ S_prev|, |E|, whether any block was resident before
   int4 v = make_int4(nD, nDnew, nE, (tid < s.cap && my_slot_blk >= 0) ? 1 : 0);

@@ -148,7 +148,7 @@ class Parity:
             v[b, g] = torch.from_numpy(x["V"][pos].view(np.int16)).view(torch.bfloat16).to(self.dev)
         return q, k, v
 
-    def run_step(self, check=True, split_calls=False):
+    def run_step(self, check=True, split_calls=False, separate_fetch=True):
         torch, N = self.torch, self.N
         for l in range(self.L):
             q, k, v = self.step_inputs(l)
@@ -156,7 +156,8 @@ class Parity:
             if split_calls:
                 N.nosa_append_kv(self.ctx, l, k.view(torch.int16), v.view(torch.int16), 1)
                 N.nosa_select(self.ctx, l, q.view(torch.int16))
-                N.nosa_fetch(self.ctx, l)
+                if separate_fetch:
+                    N.nosa_fetch(self.ctx, l)
                 N.nosa_attend(self.ctx, l, q.view(torch.int16), out.view(torch.int16))
             else:
                 N.nosa_step(self.ctx, l, q.view(torch.int16), k.view(torch.int16), v.view(torch.int16),

@@ -19,12 +19,12 @@ from tests.nosa_harness import Parity  # noqa: E402
 from offloadable_block_sparse_gb300 import nosa as N  # noqa: E402
 
 
-def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0):
+def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0, separate_fetch=True):
     p = Parity(wl, sample_units=samples, layers=layers, gather_ctas=gather_ctas)
     try:
         p.load_context()
         for _ in range(steps):
-            p.run_step(split_calls=split_calls)
+            p.run_step(split_calls=split_calls, separate_fetch=separate_fetch)
         assert N.nosa_sync(p.ctx) == N.NOSA_OK
         stats = N.nosa_get_stats(p.ctx)
         return p.log, stats
@@ -51,6 +51,14 @@ def test_tiny_through_separate_calls():
     wl = syn.workload("tiny", steps=12)
     log, _ = run(wl, wl.steps, split_calls=True)
     assert log.unit_steps == 24
+
+
+def test_separate_calls_attend_fetches_itself():
+    # select then attend without nosa_fetch: the attention kernel copies the new blocks itself
+    wl = syn.Workload("fused", layers=2, batch=2, q_heads=16, kv_heads=2, context=3001, k_q=4, k_e=8,
+                      window_tokens=256, steps=40, sigma=1.0)
+    log, _ = run(wl, wl.steps, split_calls=True, separate_fetch=False)
+    assert log.unit_steps == 40 * 8
 
 
 def test_ragged_context_group4_small_window():
