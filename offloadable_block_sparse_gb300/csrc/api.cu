@@ -80,7 +80,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 void free_ctx(nosa_ctx* c) {
   void* dev[] = {c->cache, c->kt, c->kring, c->se_tok, c->se_win, c->se_blk, c->W1, c->W2, c->slot_blk,
                  c->blk2slot, c->sel, c->sel_kind, c->sel_slot, c->sel_new, c->n_sel, c->fetch, c->n_fetch, c->gamma,
-                 c->evicted, c->T, c->err, c->stats, c->zbuf, c->spart, c->sq_blk, c->apart, c->tickets,
+                 c->evicted, c->T, c->err, c->stats, c->sq_blk, c->apart, c->tickets,
                  c->stage_q, c->stage_k, c->stage_v, c->stage_out, c->bulk_k, c->bulk_v};
   for (void* p : dev)
     if (p) cudaFree(p);
@@ -133,16 +133,16 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.gamma = c->gamma + lu * 2;
   s.W1 = c->W1 + (size_t)l * c->Hkv * kHeadDim * d.h;
   s.W2 = c->W2 + (size_t)l * c->Hkv * d.h;
-  s.zbuf = c->zbuf;
-  s.spart = c->spart;
   s.sq_blk = c->sq_blk;
   s.apart = c->apart;
   s.tickets = c->tickets;
   s.stats = c->stats;
   s.err = c->err;
   s.score_chunks = c->score_chunks;
+  s.score_wpc = c->score_wpc;
   s.attend_chunks = c->attend_chunks;
   s.attend_blocks_per_cta = c->attend_blocks_per_cta;
+  s.attend_cluster = c->attend_cluster;
   return s;
 }
 }  // namespace nosa
@@ -243,10 +243,26 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
 
   const size_t LU = (size_t)c->L * c->U;
   const size_t nc = std::max(d.nc_max, 1);
-  c->score_chunks = cdiv(nc, kWindowsPerCta);
+  // selector: one cluster of up to 8 CTAs per unit, each scoring a multiple of 128 windows
+  c->score_chunks = std::min(8, cdiv(nc, kWindowsPerCta));
+  c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
+  // attend: about two CTAs per SM in total, at most kMaxBlocksPerCta blocks each; the unit's
+  // CTAs form one cluster when the device can schedule clusters of that size
   int bpc = cdiv((long long)c->U * d.cap, 2ll * std::max(c->num_sms, 1));
   bpc = std::min(std::max(bpc, 1), kMaxBlocksPerCta);
   if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), kMaxBlocksPerCta);
+  if (init_attend() != cudaSuccess) {  // the cluster query below needs the kernel's smem limit set
+    (void)cudaGetLastError();
+    delete c;
+    return NOSA_ERR_CUDA;
+  }
+  const int max_cluster = attend_max_cluster();
+  c->attend_cluster = 1;
+  if (const char* e = getenv("NOSA_ATTEND_CLUSTER")) c->attend_cluster = atoi(e) != 0;
+  if (c->attend_cluster) {
+    while (cdiv(d.cap, bpc) > max_cluster && bpc < kMaxBlocksPerCta) ++bpc;
+    if (cdiv(d.cap, bpc) > max_cluster) c->attend_cluster = 0;
+  }
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
@@ -296,8 +312,6 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   dalloc(&c->T, c->L * sizeof(int));
   dalloc(&c->err, sizeof(int));
   dalloc(&c->stats, sizeof(DevStats));
-  dalloc(&c->zbuf, (size_t)c->U * d.G * nc * 4);
-  dalloc(&c->spart, (size_t)c->U * c->score_chunks * kMaxGroup * 2 * 4);
   dalloc(&c->sq_blk, (size_t)c->U * d.nb_max * 4);
   dalloc(&c->apart, (size_t)c->U * c->attend_chunks * kMaxGroup * kPartStride * 4);
   dalloc(&c->tickets, (3 * (size_t)c->U + 1) * 4);
@@ -367,7 +381,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   }
   {
     const LayerState s0 = layer_state(c, 0);
-    if (init_append(s0) != cudaSuccess || init_score_select(s0) != cudaSuccess || init_attend() != cudaSuccess) {
+    if (init_append(s0) != cudaSuccess || init_score_select(s0) != cudaSuccess) {
       (void)cudaGetLastError();
       free_ctx(c);
       return NOSA_ERR_CUDA;

@@ -16,8 +16,12 @@
 // The four warps' (m, l, O) are merged in shared memory into one partial per
 // CTA; the last CTA of the unit (atomic ticket) merges the partials and writes
 // the bf16 output.
+#include <cooperative_groups.h>
+
 #include "nosa_internal.cuh"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace nosa {
 
@@ -29,6 +33,10 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int t
   return stage + dhalf * 16384 + kv * 8192 + token * 128 + (((chunk ^ (token & 7)) & 7) << 4);
 }
 
+// kCluster: the unit's CTAs form one thread-block cluster and merge their
+// partials through distributed shared memory; otherwise they merge through
+// global scratch with an atomic ticket (the last CTA of the unit merges).
+template <bool kCluster>
 __global__ void __launch_bounds__(kAttendThreads, 2)
     attend_kernel(const __grid_constant__ CUtensorMap tmap, LayerState s, const uint16_t* __restrict__ q,
                   uint16_t* __restrict__ out, int fused_fetch) {
@@ -229,6 +237,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   __syncthreads();
   // CTA partial (base-2 max, sum, unnormalised output) for each head
   const int x = tid;  // head dimension
+  __shared__ float cp_m[kMaxGroup], cp_l[kMaxGroup], cp_o[kMaxGroup][kHeadDim];
   float* part0 = s.apart + ((size_t)u * s.attend_chunks + chunk) * kMaxGroup * kPartStride;
   for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
@@ -243,12 +252,47 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
         O += wo[(w * kMaxGroup + h) * kHeadDim + x] * f;
       }
     }
-    float* part = part0 + h * kPartStride;
-    if (x == 0) {
-      part[0] = M;
-      part[1] = L;
+    if constexpr (kCluster) {
+      if (x == 0) {
+        cp_m[h] = M;
+        cp_l[h] = L;
+      }
+      cp_o[h][x] = O;
+    } else {
+      float* part = part0 + h * kPartStride;
+      if (x == 0) {
+        part[0] = M;
+        part[1] = L;
+      }
+      part[2 + x] = O;
     }
-    part[2 + x] = O;
+  }
+  if constexpr (kCluster) {
+    // every CTA of the unit merges the heads h = rank, rank + CS, ... from all CTAs' partials
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank(), CS = (int)cluster.num_blocks();
+    cluster.sync();
+    for (int h = rank; h < G; h += CS) {
+      float mr[16], M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        mr[r] = r < CS ? *cluster.map_shared_rank(&cp_m[h], r) : -INFINITY;
+        M = fmaxf(M, mr[r]);
+      }
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        if (r < CS && mr[r] > -INFINITY) {
+          const float f = exp2f(mr[r] - M);
+          L += *cluster.map_shared_rank(&cp_l[h], r) * f;
+          O += *cluster.map_shared_rank(&cp_o[h][x], r) * f;
+        }
+      }
+      const float res = L > 0.f ? O / L : 0.f;
+      out[((size_t)u * G + h) * kHeadDim + x] = __bfloat16_as_ushort(__float2bfloat16_rn(res));
+    }
+    cluster.sync();  // keep every CTA's partial alive until all remote reads are done
+    return;
   }
   __threadfence();
   __syncthreads();
@@ -316,14 +360,60 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
 size_t attend_smem_bytes() { return 1024 + kAttendStages * kStageBytes; }
 
 cudaError_t init_attend() {
-  return cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attend_smem_bytes());
+  cudaError_t e = cudaFuncSetAttribute(attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)attend_smem_bytes());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)attend_smem_bytes());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                           int fused_fetch, cudaStream_t st) {
   const size_t smem = attend_smem_bytes();
-  attend_kernel<<<dim3(s.attend_chunks, s.U), kAttendThreads, smem, st>>>(*tmap, s, q, out, fused_fetch);
-  return cudaGetLastError();
+  if (!s.attend_cluster) {
+    attend_kernel<false><<<dim3(s.attend_chunks, s.U), kAttendThreads, smem, st>>>(*tmap, s, q, out, fused_fetch);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.attend_chunks, s.U);
+  cfg.blockDim = dim3(kAttendThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = s.attend_chunks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_kernel<true>, *tmap, s, q, out, fused_fetch);
+}
+
+// Largest cluster of attend CTAs (with this kernel's shared memory) the device can schedule.
+int attend_max_cluster() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kAttendThreads);
+  cfg.dynamicSmemBytes = attend_smem_bytes();
+  int best = 1;
+  for (int c : {16, 8, 4, 2}) {
+    cfg.gridDim = dim3(c, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = c;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<true>, &cfg) == cudaSuccess && n > 0) {
+      best = c;
+      break;
+    }
+    (void)cudaGetLastError();
+  }
+  return best;
 }
 
 }  // namespace nosa

@@ -98,16 +98,16 @@ struct LayerState {
   const float* W1;        // [Hkv][d][h]
   const float* W2;        // [Hkv][h]
   // scratch shared by all layers (stream ordered)
-  float* zbuf;            // [U][G][nc_max]
-  float* spart;           // [U][score_chunks][kMaxGroup][2]
-  float* sq_blk;          // [U][nb_max]
+  float* sq_blk;          // [U][nb_max] pooled query-aware scores of the last selection
   float* apart;           // [U][attend_chunks][kMaxGroup][kPartStride]
   unsigned int* tickets;  // [3][U]: append, score, attend
   DevStats* stats;
   int* err;
-  int score_chunks;
-  int attend_chunks;
+  int score_chunks;        // CTAs (one cluster) per unit in the selector
+  int score_wpc;           // compressed windows per selector CTA (multiple of 128)
+  int attend_chunks;       // split-K CTAs per unit in attend
   int attend_blocks_per_cta;
+  int attend_cluster;      // 1: attend CTAs of a unit form a cluster and merge through DSMEM
 };
 
 }  // namespace nosa
@@ -132,9 +132,9 @@ struct nosa_ctx {
   int *T, *err;
   nosa::DevStats* stats;
   // scratch
-  float *zbuf, *spart, *sq_blk, *apart;
+  float *sq_blk, *apart;
   unsigned int* tickets;
-  int score_chunks, attend_chunks, attend_blocks_per_cta, gather_ctas;
+  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_cluster, gather_ctas;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   size_t stage_tok_cap;   // tokens per unit the bulk staging buffers hold
@@ -165,4 +165,5 @@ size_t score_select_smem(const LayerState& s);
 cudaError_t init_append(const LayerState& s);
 cudaError_t init_score_select(const LayerState& s);
 cudaError_t init_attend();
+int attend_max_cluster();
 }  // namespace nosa

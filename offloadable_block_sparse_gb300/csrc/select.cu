@@ -1,41 +1,60 @@
 // a2-a4: fused scorer, two-part selector, set difference and fetch list.
 //
-// Phase 1 (every CTA): z_{h,i} = q_h . K~_i * scale for a chunk of compressed
-// windows, on the tensor cores (mma.sync m16n8k16, windows as M, the GQA
-// group's heads as N), plus the chunk's per-head softmax statistics.
-// Phase 2 (last CTA of each unit, by atomic ticket): per-head softmax over all
-// windows summed over the group (SparDA summary, "lightweight design": the
-// block selector aggregates the group's heads through a softmax), max-pooled
-// onto the 64-token blocks (NOSA explainer eq. 5-6); top-k_q query-aware
-// blocks, then k_e blocks by the pooled eviction score among candidates never
-// dropped before (wiki "How NOSA works": query-aware picks set to +inf, the
-// rest filled by the query-agnostic score, never-reselect constraint); sink
-// and window blocks; sticky eviction update; set difference against the
-// block cache with ascending free-slot assignment (wiki "NOSI": set-difference
-// kernel, only changed blocks are swapped).
+// One thread-block cluster per unit: CTA r of the cluster scores compressed
+// windows [r*wpc, (r+1)*wpc).
+//   1. z_{h,i} = q_h . K~_i * scale on the tensor cores (mma.sync m16n8k16,
+//      16 windows as M, the GQA group's heads as N = 8), kept in shared memory,
+//      with this CTA's per-head softmax statistics (max, sum of exp).
+//   2. cluster barrier; every CTA reads all CTAs' statistics through
+//      distributed shared memory, forms the group softmax over all windows
+//      summed over the heads (SparDA summary, "lightweight design": the block
+//      selector aggregates the group's heads through a softmax) and max-pools
+//      its windows onto the 64-token blocks they overlap (NOSA explainer
+//      eq. 5-6), combining into the leader CTA's block scores with remote
+//      atomic max.
+//   3. cluster barrier; the leader selects: top-k_q query-aware blocks, then
+//      k_e blocks by the pooled eviction score among candidates never dropped
+//      before (wiki "How NOSA works": query-aware picks set to +inf, the rest
+//      filled by the query-agnostic score, never-reselect constraint); sink and
+//      window blocks; sticky eviction update; set difference against the block
+//      cache with ascending free-slot assignment (wiki "NOSI": set-difference
+//      kernel, only changed blocks are swapped); fetch list.
+// The leader's inputs for step 3 (pooled s^e, slot tables, eviction bitmap) are
+// requested at kernel start and arrive while step 1 runs.
+#include <cooperative_groups.h>
+
 #include "nosa_internal.cuh"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace nosa {
 
 namespace {
 
 constexpr uint8_t F_CAND = 1, F_ELIG = 2, F_Q = 4, F_E = 8, F_S = 16, F_NEW = 32;
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // orderable(-inf)
 
 struct SelShared {
   int scan[32];
   int hist[256];
   int free_by_rank[256];
-  int digit, above, total, last;
   float cmax[kScoreWarps][kMaxGroup];
-  float Mh[kMaxGroup], invS[kMaxGroup];
+  float Mloc[kMaxGroup], Sloc[kMaxGroup];  // this CTA's softmax statistics (read remotely)
+  float Mh[kMaxGroup], invS[kMaxGroup];    // the unit's statistics
+  int4 wsum[kScoreWarps];
 };
+
+__device__ __forceinline__ float from_orderable(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 // Top-k over the blocks whose flag has `valid` set, run by one warp: sets `mark`
 // on the k largest keys, ties to the lower block index.  Radix select on the
-// 32-bit keys (4 passes of 8 bits; histogram in shared memory, bins scanned
-// with warp shuffles), then the keys equal to the k-th largest are taken in
-// ascending block order with ballots.  No block-wide barrier.
+// 32-bit keys (4 passes of 8 bits).  Pooled scores share their high bits, so
+// lanes with equal digits are merged with __match_any_sync before one shared
+// atomic per distinct digit; the bins are scanned with warp shuffles.  The keys
+// equal to the k-th largest are then taken in ascending block order by ballot.
 __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, uint8_t valid, uint8_t mark,
                           int* hist) {
   const int lane = threadIdx.x & 31;
@@ -54,8 +73,13 @@ __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, ui
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
-    for (int b = lane; b < n; b += 32)
-      if ((flags[b] & valid) && (keys[b] & pmask) == prefix) atomicAdd(&hist[(keys[b] >> shift) & 255], 1);
+    for (int base = 0; base < n; base += 32) {
+      const int b = base + lane;
+      const bool act = b < n && (flags[b] & valid) && (keys[b] & pmask) == prefix;
+      const int dg = act ? (int)((keys[b] >> shift) & 255u) : -1;
+      const unsigned int peers = __match_any_sync(0xffffffffu, dg);
+      if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+    }
     __syncwarp();
     int c[8], tot = 0;
 #pragma unroll
@@ -103,47 +127,71 @@ __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, ui
 
 }  // namespace
 
-// grid (score_chunks, U), 256 threads.  Dynamic shared memory (phase 2): window
-// scores, pooled s^e, block->slot map, radix keys, chunk stats, eviction words, flags.
+// grid (cluster size, U) with clusters (cluster size, 1, 1); 256 threads.
+// Dynamic shared memory: z[kMaxGroup][wpc] and sq[wpc] floats (every CTA), then
+// for the leader keys[nb_max], se[nb_max], b2s[nb_max], eviction words, flags[nb_max].
 __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState s, const uint16_t* __restrict__ q) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ SelShared sh;
-  const int chunk = blockIdx.x, u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank(), CS = (int)cluster.num_blocks();
+  const int u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = lane >> 2, t4 = lane & 3;
-  const Geometry geo = geometry(*s.T, s.nw, s.sink);
-  const int G = s.G, nc = geo.nc;
+  const int G = s.G, wpc = s.score_wpc;
+  float* zs = reinterpret_cast<float*>(dsm);                      // [kMaxGroup][wpc]
+  float* sqs = zs + kMaxGroup * wpc;                              // [wpc]
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sqs + wpc);        // leader: [nb_max]
+  float* sek = reinterpret_cast<float*>(keys + s.nb_max);         // leader: [nb_max] pooled s^e
+  int32_t* b2s = reinterpret_cast<int32_t*>(sek + s.nb_max);      // leader: [nb_max] block -> slot
+  uint32_t* evw = reinterpret_cast<uint32_t*>(b2s + s.nb_max);    // leader: [ev_words]
+  uint8_t* flags = reinterpret_cast<uint8_t*>(evw + s.ev_words);  // leader: [nb_max]
 
-  // ---------------- phase 1: z for this chunk of windows
-  // k order inside each 32-dim chunk is permuted identically for A (K~ rows) and
-  // B (q), so each thread loads 16 contiguous bytes per row: lanes t4 of a row
-  // cover 64 contiguous bytes and a warp load touches whole 32-byte sectors.
+  // q fragments first: they do not depend on the context length.  The k order in
+  // each 32-dim chunk is permuted identically for A (K~ rows) and B (q), so a
+  // thread loads 16 contiguous bytes per row and a warp load covers whole sectors.
   uint4 qf[4];
   {
-    const uint16_t* qh = q + ((size_t)u * G + gr) * kHeadDim;
+    const uint16_t* qh = q + ((size_t)u * G + min(gr, G - 1)) * kHeadDim;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
       qf[c] = gr < G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
   }
+  const Geometry geo = geometry(*s.T, s.nw, s.sink);
+  const int nc = geo.nc, nb = geo.nb;
+  const int i0 = rank * wpc;  // first window of this CTA
+
+  // leader: request the selection's inputs now; they arrive during the scoring
+  int my_slot_blk = -1;
+  if (rank == 0) {
+    for (int b = tid; b < nb; b += blockDim.x) {
+      keys[b] = kKeyNegInf;
+      sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
+      b2s[b] = s.blk2slot[(size_t)u * s.nb_max + b];
+    }
+    for (int w = tid; w < (nb + 31) / 32; w += blockDim.x) evw[w] = s.evicted[(size_t)u * s.ev_words + w];
+    if (tid < s.cap) my_slot_blk = s.slot_blk[(size_t)u * s.cap + tid];
+  }
+
+  // ---------------- 1. z for this CTA's windows, per-head max
   const float scale = s.scale;
-  float z[kScoreTiles][4];
-  int rowi[kScoreTiles][2];
-  {
-    uint4 a[kScoreTiles][2][4];
+  float mx[2] = {-INFINITY, -INFINITY};
+  const int tiles = wpc / (16 * kScoreWarps);
+  for (int t0 = 0; t0 < tiles; t0 += 2) {
+    uint4 a[2][2][4];
 #pragma unroll
-    for (int tl = 0; tl < kScoreTiles; ++tl) {
-      const int base = chunk * kWindowsPerCta + (warp * kScoreTiles + tl) * 16;
+    for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr) {
-        const int r = base + gr + 8 * hr;
-        rowi[tl][hr] = r;
-        const uint16_t* kr = s.kt + ((size_t)u * s.nc_max + min(r, s.nc_max - 1)) * kHeadDim;
+        const int r = i0 + (warp * tiles + t0 + tl) * 16 + gr + 8 * hr;
+        const bool ok = t0 + tl < tiles && r < nc;
+        const uint16_t* kr = s.kt + ((size_t)u * s.nc_max + (ok ? r : 0)) * kHeadDim;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          a[tl][hr][c] = r < nc ? *reinterpret_cast<const uint4*>(kr + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
+          a[tl][hr][c] = ok ? *reinterpret_cast<const uint4*>(kr + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
       }
-    }
 #pragma unroll
-    for (int tl = 0; tl < kScoreTiles; ++tl) {
+    for (int tl = 0; tl < 2; ++tl) {
+      if (t0 + tl >= tiles) break;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -156,23 +204,16 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
           mma_16816(acc, af, qq[2 * hh], qq[2 * hh + 1]);
         }
       }
+      const int wl0 = (warp * tiles + t0 + tl) * 16 + gr;  // local window of acc[0..1]
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int r = rowi[tl][j >> 1];
-        z[tl][j] = r < nc ? acc[j] * scale : -INFINITY;
+        const int wl = wl0 + 8 * (j >> 1), h = 2 * t4 + (j & 1);
+        const float z = (i0 + wl < nc) ? acc[j] * scale : -INFINITY;
+        zs[h * wpc + wl] = z;
+        mx[j & 1] = fmaxf(mx[j & 1], z);
       }
     }
   }
-  // store z and the chunk's per-head max
-  float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-  for (int tl = 0; tl < kScoreTiles; ++tl)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int h = 2 * t4 + (j & 1), r = rowi[tl][j >> 1];
-      if (h < G && r < nc) s.zbuf[((size_t)u * G + h) * s.nc_max + r] = z[tl][j];
-      mx[j & 1] = fmaxf(mx[j & 1], z[tl][j]);
-    }
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
@@ -187,123 +228,63 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   if (tid < kMaxGroup) {
     float m = -INFINITY;
     for (int w = 0; w < kScoreWarps; ++w) m = fmaxf(m, sh.cmax[w][tid]);
-    sh.Mh[tid] = m;
+    sh.Mloc[tid] = m;
   }
   __syncthreads();
-  float se[2] = {0.f, 0.f};
-#pragma unroll
-  for (int tl = 0; tl < kScoreTiles; ++tl)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float M = sh.Mh[2 * t4 + (j & 1)];
-      if (z[tl][j] > -INFINITY) se[j & 1] += expf(z[tl][j] - M);
-    }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    se[j] += __shfl_xor_sync(0xffffffffu, se[j], 4);
-    se[j] += __shfl_xor_sync(0xffffffffu, se[j], 8);
-    se[j] += __shfl_xor_sync(0xffffffffu, se[j], 16);
+  // sum of exp per head over this CTA's windows: warp w handles head w
+  if (warp < G) {
+    const float M = sh.Mloc[warp];
+    float e = 0.f;
+    if (M > -INFINITY)
+      for (int wl = lane; wl < wpc; wl += 32) e += expf(zs[warp * wpc + wl] - M);  // exp(-inf) = 0
+    e = warp_sum(e);
+    if (lane == 0) sh.Sloc[warp] = e;
   }
-  __syncthreads();
-  if (gr == 0) {
-    sh.cmax[warp][2 * t4] = se[0];
-    sh.cmax[warp][2 * t4 + 1] = se[1];
-  }
-  __syncthreads();
-  if (tid < G) {
-    float ssum = 0.f;
-    for (int w = 0; w < kScoreWarps; ++w) ssum += sh.cmax[w][tid];
-    float* sp = s.spart + (((size_t)u * s.score_chunks + chunk) * kMaxGroup + tid) * 2;
-    sp[0] = sh.Mh[tid];
-    sp[1] = ssum;
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned int t = atomicAdd(&s.tickets[u], 1u);
-    sh.last = (t == (unsigned int)s.score_chunks - 1);
-  }
-  __syncthreads();
-  if (!sh.last) return;
-  __threadfence();
-  if (tid == 0) s.tickets[u] = 0;
+  cluster.sync();  // every CTA's statistics (and the leader's key init) are visible
 
-  // ---------------- phase 2: selection for unit u
-  // Every global value the selection needs is requested up front (one memory
-  // round trip); the rest runs from shared memory.
-  const int nb = geo.nb, ws = geo.ws;
-  const int nch = s.score_chunks;
-  float* sqw = reinterpret_cast<float*>(dsm);                   // [nc_max] window scores
-  float* sek = sqw + s.nc_max;                                  // [nb_max] pooled s^e
-  int32_t* b2s = reinterpret_cast<int32_t*>(sek + s.nb_max);    // [nb_max] block -> slot
-  uint32_t* keys = reinterpret_cast<uint32_t*>(b2s + s.nb_max); // [nb_max]
-  float* sp = reinterpret_cast<float*>(keys + s.nb_max);        // [nch][G][2] chunk stats
-  uint32_t* evw = reinterpret_cast<uint32_t*>(sp + nch * kMaxGroup * 2);  // [ev_words]
-  uint8_t* flags = reinterpret_cast<uint8_t*>(evw + s.ev_words);          // [nb_max]
-  const int per = (nb + blockDim.x - 1) / blockDim.x;
-  const int lo = min(tid * per, nb), hi = min(lo + per, nb);
-  const int words = (nb + 31) / 32;
-  for (int idx = tid; idx < nch * G; idx += blockDim.x) {
-    const int j = idx / G, h = idx % G;
-    const float* p = s.spart + (((size_t)u * nch + j) * kMaxGroup + h) * 2;
-    sp[(j * kMaxGroup + h) * 2] = __ldcg(p);
-    sp[(j * kMaxGroup + h) * 2 + 1] = __ldcg(p + 1);
-  }
-  for (int b = lo; b < hi; ++b) {
-    sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
-    b2s[b] = s.blk2slot[(size_t)u * s.nb_max + b];
-  }
-  for (int w = tid; w < words; w += blockDim.x) evw[w] = s.evicted[(size_t)u * s.ev_words + w];
-  int32_t* sblk = s.slot_blk + (size_t)u * s.cap;
-  const int my_slot_blk = tid < s.cap ? sblk[tid] : -1;
-  __syncthreads();
+  // ---------------- 2. unit statistics, window scores, pooled block maxima -> leader
   if (tid < G) {
     float M = -INFINITY;
-    for (int j = 0; j < nch; ++j) M = fmaxf(M, sp[(j * kMaxGroup + tid) * 2]);
+    for (int r = 0; r < CS; ++r) M = fmaxf(M, *cluster.map_shared_rank(&sh.Mloc[tid], r));
     float S = 0.f;
-    for (int j = 0; j < nch; ++j) {
-      const float mj = sp[(j * kMaxGroup + tid) * 2];
-      if (mj > -INFINITY) S += sp[(j * kMaxGroup + tid) * 2 + 1] * expf(mj - M);
+    for (int r = 0; r < CS; ++r) {
+      const float mr = *cluster.map_shared_rank(&sh.Mloc[tid], r);
+      if (mr > -INFINITY) S += *cluster.map_shared_rank(&sh.Sloc[tid], r) * expf(mr - M);
     }
     sh.Mh[tid] = M;
     sh.invS[tid] = 1.f / S;
   }
   __syncthreads();
-  // s^q per window: the group's softmax probabilities summed over heads
-  for (int i0 = tid; i0 < nc; i0 += 4 * blockDim.x) {
-    float zv[4][kMaxGroup];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r * blockDim.x;
-#pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h)
-        zv[r][h] = (h < G && i < nc) ? __ldcg(s.zbuf + ((size_t)u * G + h) * s.nc_max + i) : 0.f;
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = i0 + r * blockDim.x;
-      if (i >= nc) continue;
-      float acc = 0.f;
-#pragma unroll
-      for (int h = 0; h < kMaxGroup; ++h)
-        if (h < G) acc += expf(zv[r][h] - sh.Mh[h]) * sh.invS[h];
-      sqw[i] = acc;
-    }
+  const int i1 = min(i0 + wpc, nc);
+  for (int wl = tid; wl < i1 - i0; wl += blockDim.x) {
+    float acc = 0.f;
+    for (int h = 0; h < G; ++h) acc += expf(zs[h * wpc + wl] - sh.Mh[h]) * sh.invS[h];
+    sqs[wl] = acc;
   }
   __syncthreads();
-  // max-pool onto blocks; candidates lie strictly between the sink and the window
-  for (int b = lo; b < hi; ++b) {
-    const int wl = max(4 * b - 1, 0), wh = min(4 * b + 3, nc - 1);
-    float m = -INFINITY;
-    for (int i = wl; i <= wh; ++i) m = fmaxf(m, sqw[i]);
-    s.sq_blk[(size_t)u * s.nb_max + b] = m;
-    keys[b] = orderable(m);
+  if (i1 > i0) {
+    uint32_t* lkeys = cluster.map_shared_rank(keys, 0);
+    const int b_lo = (kCmpStride * i0) / kBlock, b_hi = (kCmpStride * (i1 - 1) + kCmpKernel - 1) / kBlock;
+    for (int b = b_lo + tid; b <= b_hi; b += blockDim.x) {
+      const int wlo = max(4 * b - 1, i0), whi = min(4 * b + 3, i1 - 1);
+      float m = -INFINITY;
+      for (int i = wlo; i <= whi; ++i) m = fmaxf(m, sqs[i - i0]);
+      if (wlo <= whi) atomicMax(lkeys + b, orderable(m));
+    }
+  }
+  cluster.sync();  // block maxima have landed in the leader; remote reads are done
+  if (rank != 0) return;
+
+  // ---------------- 3. selection by the leader
+  const int ws = geo.ws;
+  for (int b = tid; b < nb; b += blockDim.x) {
+    s.sq_blk[(size_t)u * s.nb_max + b] = from_orderable(keys[b]);
     flags[b] = (b >= s.sink && b < ws) ? F_CAND : 0;
   }
   __syncthreads();
   if (warp == 0) warp_topk(keys, flags, nb, s.k_q, F_CAND, F_Q, sh.hist);
   __syncthreads();
-  for (int b = lo; b < hi; ++b) {
+  for (int b = tid; b < nb; b += blockDim.x) {
     keys[b] = orderable(sek[b]);
     const bool evb = (evw[b >> 5] >> (b & 31)) & 1u;
     if ((flags[b] & F_CAND) && !(flags[b] & F_Q) && !evb) flags[b] |= F_ELIG;
@@ -312,7 +293,9 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   if (warp == 0) warp_topk(keys, flags, nb, s.k_e, F_ELIG, F_E, sh.hist);
   __syncthreads();
 
-  // selection S, blocks without a slot
+  // selection S and the blocks without a slot; contiguous per-thread ranges keep block order
+  const int per = (nb + blockDim.x - 1) / blockDim.x;
+  const int lo = min(tid * per, nb), hi = min(lo + per, nb);
   int nD = 0, nE = 0, nDnew = 0, nS = 0, nNew = 0;
   for (int b = lo; b < hi; ++b) {
     uint8_t f = flags[b];
@@ -334,7 +317,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   }
   __syncthreads();
   // sticky eviction: candidates outside D are dropped for good
-  for (int w = tid; w < words; w += blockDim.x) {
+  for (int w = tid; w < (nb + 31) / 32; w += blockDim.x) {
     uint32_t bits = 0;
     for (int j = 0; j < 32; ++j) {
       const int b = 32 * w + j;
@@ -343,6 +326,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     if (bits & ~evw[w]) s.evicted[(size_t)u * s.ev_words + w] = evw[w] | bits;
   }
   // free slots: empty, or holding a block that left the selection (ascending)
+  int32_t* sblk = s.slot_blk + (size_t)u * s.cap;
   const int is_free = tid < s.cap && !(my_slot_blk >= 0 && my_slot_blk < nb && (flags[my_slot_blk] & F_S));
   int n_free;
   const int free_rank = block_scan_excl(is_free, sh.scan, &n_free);
@@ -374,7 +358,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   }
   if (is_free && free_rank >= n_new) sblk[tid] = -1;
   __syncthreads();
-  // ascending selection list with kinds and slots
+  // ascending selection list with kinds, slots and the fetched marks
   int total_S;
   int pos = block_scan_excl(nS, sh.scan, &total_S);
   int32_t* sel = s.sel + (size_t)u * s.cap;
@@ -409,16 +393,15 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     v.z += __shfl_xor_sync(0xffffffffu, v.z, o);
     v.w += __shfl_xor_sync(0xffffffffu, v.w, o);
   }
-  __shared__ int4 wsum[kScoreWarps];
-  if (lane == 0) wsum[warp] = v;
+  if (lane == 0) sh.wsum[warp] = v;
   __syncthreads();
   if (tid == 0) {
-    int4 t = wsum[0];
+    int4 t = sh.wsum[0];
     for (int w = 1; w < kScoreWarps; ++w) {
-      t.x += wsum[w].x;
-      t.y += wsum[w].y;
-      t.z += wsum[w].z;
-      t.w += wsum[w].w;
+      t.x += sh.wsum[w].x;
+      t.y += sh.wsum[w].y;
+      t.z += sh.wsum[w].z;
+      t.w += sh.wsum[w].w;
     }
     const int sumD = t.x, sumDnew = t.y, sumE = t.z, had_prev = t.w > 0;
     s.n_sel[u] = min(total_S, s.cap);
@@ -439,8 +422,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
 }
 
 size_t score_select_smem(const LayerState& s) {
-  return sizeof(float) * s.nc_max + 3 * sizeof(uint32_t) * s.nb_max +
-         sizeof(float) * s.score_chunks * kMaxGroup * 2 + sizeof(uint32_t) * s.ev_words + s.nb_max + 16;
+  return sizeof(float) * (kMaxGroup + 1) * s.score_wpc + 3 * sizeof(uint32_t) * s.nb_max +
+         sizeof(uint32_t) * s.ev_words + s.nb_max + 16;
 }
 
 cudaError_t init_score_select(const LayerState& s) {
@@ -449,9 +432,19 @@ cudaError_t init_score_select(const LayerState& s) {
 }
 
 cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, cudaStream_t st) {
-  const size_t smem = score_select_smem(s);
-  score_select_kernel<<<dim3(s.score_chunks, s.U), kScoreThreads, smem, st>>>(s, q);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s.score_chunks, s.U);
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = score_select_smem(s);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = s.score_chunks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, score_select_kernel, s, q);
 }
 
 }  // namespace nosa
