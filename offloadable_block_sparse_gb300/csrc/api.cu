@@ -143,6 +143,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.attend_chunks = c->attend_chunks;
   s.attend_blocks_per_cta = c->attend_blocks_per_cta;
   s.attend_cluster = c->attend_cluster;
+  s.attend_deep = c->attend_deep;
   return s;
 }
 }  // namespace nosa
@@ -256,7 +257,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     delete c;
     return NOSA_ERR_CUDA;
   }
-  const int max_cluster = attend_max_cluster();
+  const int max_cluster = attend_max_cluster(false);
   c->attend_cluster = 1;
   if (const char* e = getenv("NOSA_ATTEND_CLUSTER")) c->attend_cluster = atoi(e) != 0;
   if (c->attend_cluster) {
@@ -265,6 +266,8 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   }
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
+  c->attend_deep = c->attend_cluster && (long long)c->attend_chunks * c->U <= c->num_sms &&
+                   attend_max_cluster(true) >= c->attend_chunks;
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
   c->stage_tok_cap = 512;
 
@@ -431,7 +434,7 @@ nosa_status nosa_append_kv(nosa_ctx* c, int layer, const uint16_t* k, const uint
       kd = c->stage_k;
       vd = c->stage_v;
     }
-    CK(launch_append_one(s, kd, vd, c->stream));
+    CK(launch_append_one(s, kd, vd, true, c->stream));
   } else if (!src_is_host) {
     CK(launch_append_bulk(s, k, v, c->T_host[layer], n, c->stream));
   } else {
@@ -455,7 +458,7 @@ nosa_status nosa_select(nosa_ctx* c, int layer, const uint16_t* q, int32_t* sel_
   if (!q) return NOSA_ERR_INVALID_ARG;
   if (c->T_host[layer] < 1) return NOSA_ERR_STATE;
   const LayerState s = layer_state(c, layer);
-  CK(launch_score_select(s, q, c->stream));
+  CK(launch_score_select(s, q, true, c->stream));
   if (sel_out) {
     copy_i32<<<cdiv((size_t)c->U * c->cap, 256), 256, 0, c->stream>>>(sel_out, s.sel, (size_t)c->U * c->cap);
     CK(cudaGetLastError());
@@ -484,7 +487,7 @@ nosa_status nosa_attend(nosa_ctx* c, int layer, const uint16_t* q, uint16_t* out
   if (c->sel_T[layer] != c->T_host[layer]) return NOSA_ERR_STATE;
   // without a nosa_fetch since the selection, the attend CTAs fetch the new blocks themselves
   const int fused = c->fetch_T[layer] != c->T_host[layer];
-  CK(launch_attend(layer_state(c, layer), &c->tmap_cache, q, out, fused, c->stream));
+  CK(launch_attend(layer_state(c, layer), &c->tmap_cache, q, out, fused, true, c->stream));
   return NOSA_OK;
 }
 
@@ -495,9 +498,9 @@ nosa_status nosa_step(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t*
   if (!q || !k_new || !v_new || !out) return NOSA_ERR_INVALID_ARG;
   if (c->T_host[layer] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
   const LayerState s = layer_state(c, layer);
-  CK(launch_append_one(s, k_new, v_new, c->stream));
-  CK(launch_score_select(s, q, c->stream));
-  CK(launch_attend(s, &c->tmap_cache, q, out, 1, c->stream));  // the fetch runs inside attend
+  CK(launch_append_one(s, k_new, v_new, true, c->stream));
+  CK(launch_score_select(s, q, true, c->stream));
+  CK(launch_attend(s, &c->tmap_cache, q, out, 1, true, c->stream));  // the fetch runs inside attend
   c->T_host[layer] += 1;
   c->sel_T[layer] = c->T_host[layer];
   return NOSA_OK;

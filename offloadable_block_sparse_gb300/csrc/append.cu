@@ -22,9 +22,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_one_kernel(LayerState s
   __shared__ float half_acc[2][kHeadDim];
   __shared__ float red[4];
   const int u = blockIdx.x, tid = threadIdx.x;
+  // Nothing here reads the previous kernel's results (that is the previous
+  // layer's attention): let the selector launch now, and wait for the previous
+  // kernel only before exiting, so that completions stay ordered.
+  pdl_launch_dependents();
   const int p = *s.T;  // position of the new token (all CTAs read it before any ticket)
   if (p >= s.T_max) {
     if (tid == 0 && u == 0) atomicOr(s.err, kErrCapacity);
+    pdl_wait();
     return;  // every CTA sees the same p: nobody takes a ticket, T is unchanged
   }
   const int blk = p / kBlock, row = p % kBlock;
@@ -148,6 +153,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_one_kernel(LayerState s
       *s.T = T;
     }
   }
+  pdl_wait();
 }
 
 // ---------------------------------------------------------------- bulk context load
@@ -240,9 +246,8 @@ __global__ void __launch_bounds__(128) append_bulk_finish_kernel(LayerState s, c
   if (u == 0 && tid == 0) *s.T = T_new;
 }
 
-cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, cudaStream_t st) {
-  append_one_kernel<<<s.U, kAppendThreads, 0, st>>>(s, k, v);
-  return cudaGetLastError();
+cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, bool pdl, cudaStream_t st) {
+  return launch_ex(append_one_kernel, dim3(s.U), dim3(kAppendThreads), 0, st, pdl, 0, s, k, v);
 }
 
 static size_t bulk_tokens_smem(const LayerState& s) {

@@ -26,7 +26,8 @@ namespace cg = cooperative_groups;
 namespace nosa {
 
 constexpr int kStageBytes = kBlockBytes;            // 32 KiB: [d half][K,V][64 tokens][64 dims]
-static_assert(4 * kMaxGroup * kHeadDim * 4 <= kAttendStages * kStageBytes, "warp partials alias the stages");
+static_assert(4 * kMaxGroup * kHeadDim * 4 <= 3 * kStageBytes, "warp partials alias the stages");
+constexpr int kDeepStages = 6;  // when a unit's CTAs get an SM each
 constexpr long long kWaitLimit = 2000000000LL;      // ~1 s of SM clocks
 
 __device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int token, int chunk) {
@@ -36,14 +37,15 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int t
 // kCluster: the unit's CTAs form one thread-block cluster and merge their
 // partials through distributed shared memory; otherwise they merge through
 // global scratch with an atomic ticket (the last CTA of the unit merges).
-template <bool kCluster>
-__global__ void __launch_bounds__(kAttendThreads, 2)
+template <bool kCluster, int kStages>
+__global__ void __launch_bounds__(kAttendThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap tmap, LayerState s, const uint16_t* __restrict__ q,
                   uint16_t* __restrict__ out, int fused_fetch) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kAttendStages];
+  __shared__ __align__(8) uint64_t bars[kStages];
   __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
   __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta], s_new[kMaxBlocksPerCta];
+  __shared__ int s_ord[kMaxBlocksPerCta];
   __shared__ int last, bad_any;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
@@ -63,7 +65,9 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
       qb[ks][1] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4 + 8) : 0u;
     }
   }
-  const Geometry geo = geometry(*s.T, s.nw, s.sink);
+  const Geometry geo = geometry(*s.T, s.nw, s.sink);  // written two kernels back (append)
+  pdl_wait();               // the selection (previous kernel) is needed from here
+  pdl_launch_dependents();  // the next layer's append may start
   const int nsel = s.n_sel[u];
   const int e0 = chunk * s.attend_blocks_per_cta;
   const int nblk = max(0, min(e0 + s.attend_blocks_per_cta, nsel) - e0);
@@ -79,11 +83,18 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
     s_slot[tid] = slot;
     s_new[tid] = fused_fetch ? s.sel_new[(size_t)u * s.cap + e0 + tid] : 0;
   }
+  __syncthreads();
   if (tid == 0) {
     prefetch_tmap(&tmap);
-    for (int i = 0; i < kAttendStages; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     bad_any = 0;
+    // blocks coming over the host link first, so their latency overlaps the cached blocks' loads
+    int n = 0;
+    for (int i = 0; i < nblk; ++i)
+      if (s_new[i]) s_ord[n++] = i;
+    for (int i = 0; i < nblk; ++i)
+      if (!s_new[i]) s_ord[n++] = i;
   }
   __syncthreads();
   // Stage i % kAttendStages receives entry e0+i: a cached block by TMA (thread 0),
@@ -91,13 +102,14 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   // pinned host store by cp.async of all threads (rows past the context zero-filled).
   // One cp.async group is committed per entry (empty for TMA entries).
   auto issue = [&](int i) {
-    const int st = i % kAttendStages;
-    const bool fresh = i < nblk && s_new[i];
+    const int st = i % kStages;
+    const int e = i < nblk ? s_ord[i] : 0;
+    const bool fresh = i < nblk && s_new[e];
     if (tid == 0 && i < nblk) {
       if (fresh) {
         mbar_arrive(&bars[st]);
       } else {
-        const int flat = (s.unit_base + u) * s.cap + s_slot[i];
+        const int flat = (s.unit_base + u) * s.cap + s_slot[e];
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[st], kStageBytes);
         tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
@@ -105,8 +117,8 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
       }
     }
     if (fresh) {
-      const int rows = (s_blk[i] == geo.nb - 1) ? geo.valid_tail : kBlock;
-      const uint16_t* src = s.host_kv + ((size_t)u * s.nb_max + s_blk[i]) * 2 * kBlockElems;
+      const int rows = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
+      const uint16_t* src = s.host_kv + ((size_t)u * s.nb_max + s_blk[e]) * 2 * kBlockElems;
 #pragma unroll 4
       for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
         const int idx = tid + j * kAttendThreads;  // 16-byte chunk: K|V, row, chunk of the 256-byte row
@@ -117,8 +129,8 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
     }
     cp_async_commit();
   };
-  for (int i = 0; i < kAttendStages; ++i) issue(i);
-  int issued = kAttendStages;
+  for (int i = 0; i < kStages; ++i) issue(i);
+  int issued = kStages;
 
   const float sl2 = s.scale * 1.4426950408889634f;  // softmax in base 2
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -135,16 +147,17 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
 
   int consumed = 0;
   for (int i = 0; i < nblk; ++i) {
-    const int st = i % kAttendStages;
-    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((i / kAttendStages) & 1), kWaitLimit);
-    cp_async_wait<kAttendStages - 1>();  // this entry's cp.async group (if any) has landed
+    const int st = i % kStages;
+    const int e = s_ord[i];
+    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((i / kStages) & 1), kWaitLimit);
+    cp_async_wait<kStages - 1>();  // this entry's cp.async group (if any) has landed
     if (__syncthreads_or(!okw)) {
       if (tid == 0) atomicOr(s.err, kErrTimeout);
       bad_any = 1;
       break;
     }
     consumed = i + 1;
-    const int valid = (s_blk[i] == geo.nb - 1) ? geo.valid_tail : kBlock;
+    const int valid = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
     const uint32_t stg = sbase + st * kStageBytes;
     if (tok0 < valid) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -190,8 +203,8 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
         mma_16816(o[mt], a, pb0, pb1);
       }
     }
-    if (s_new[i]) {  // a fetched block also goes to its cache slot for later steps
-      uint16_t* dst = s.cache + ((size_t)u * s.cap + s_slot[i]) * 2 * kBlockElems;
+    if (s_new[e]) {  // a fetched block also goes to its cache slot for later steps
+      uint16_t* dst = s.cache + ((size_t)u * s.cap + s_slot[e]) * 2 * kBlockElems;
 #pragma unroll 4
       for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
         const int idx = tid + j * kAttendThreads;
@@ -210,7 +223,7 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   cp_async_wait_all();
   if (bad_any && tid == 0) {  // drain copies still in flight before the shared memory is reused
     for (int i = consumed; i < min(issued, nblk); ++i)
-      mbar_wait_bounded(&bars[i % kAttendStages], (uint32_t)((i / kAttendStages) & 1), kWaitLimit);
+      mbar_wait_bounded(&bars[i % kStages], (uint32_t)((i / kStages) & 1), kWaitLimit);
   }
   __syncthreads();
   // warp partials -> shared memory
@@ -357,47 +370,44 @@ __global__ void __launch_bounds__(kAttendThreads, 2)
   }
 }
 
-size_t attend_smem_bytes() { return 1024 + kAttendStages * kStageBytes; }
+size_t attend_smem_bytes(int stages) { return 1024 + (size_t)stages * kStageBytes; }
+
+template <bool C, int S>
+static cudaError_t set_attend_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(attend_kernel<C, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)attend_smem_bytes(S));
+  if (e != cudaSuccess || !C) return e;
+  return cudaFuncSetAttribute(attend_kernel<C, S>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
 
 cudaError_t init_attend() {
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)attend_smem_bytes());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)attend_smem_bytes());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attend_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = set_attend_attrs<false, kAttendStages>();
+  if (e == cudaSuccess) e = set_attend_attrs<true, kAttendStages>();
+  if (e == cudaSuccess) e = set_attend_attrs<true, kDeepStages>();
+  return e;
+}
+
+template <bool C, int S>
+static cudaError_t launch_attend_t(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
+                                   int fused_fetch, bool pdl, cudaStream_t st) {
+  return launch_ex(attend_kernel<C, S>, dim3(s.attend_chunks, s.U), dim3(kAttendThreads), attend_smem_bytes(S), st,
+                   pdl, C ? s.attend_chunks : 0, *tmap, s, q, out, fused_fetch);
 }
 
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
-                          int fused_fetch, cudaStream_t st) {
-  const size_t smem = attend_smem_bytes();
-  if (!s.attend_cluster) {
-    attend_kernel<false><<<dim3(s.attend_chunks, s.U), kAttendThreads, smem, st>>>(*tmap, s, q, out, fused_fetch);
-    return cudaGetLastError();
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(s.attend_chunks, s.U);
-  cfg.blockDim = dim3(kAttendThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = s.attend_chunks;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_kernel<true>, *tmap, s, q, out, fused_fetch);
+                          int fused_fetch, bool pdl, cudaStream_t st) {
+  if (!s.attend_cluster) return launch_attend_t<false, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
+  if (s.attend_deep) return launch_attend_t<true, kDeepStages>(s, tmap, q, out, fused_fetch, pdl, st);
+  return launch_attend_t<true, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
 }
 
 // Largest cluster of attend CTAs (with this kernel's shared memory) the device can schedule.
-int attend_max_cluster() {
+int attend_max_cluster(bool deep) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kAttendThreads);
-  cfg.dynamicSmemBytes = attend_smem_bytes();
+  cfg.dynamicSmemBytes = attend_smem_bytes(deep ? kDeepStages : kAttendStages);
   int best = 1;
-  for (int c : {16, 8, 4, 2}) {
+  for (int c : {8, 4, 2}) {
     cfg.gridDim = dim3(c, 1);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -407,7 +417,9 @@ int attend_max_cluster() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_kernel<true>, &cfg) == cudaSuccess && n > 0) {
+    const cudaError_t e = deep ? cudaOccupancyMaxActiveClusters(&n, attend_kernel<true, kDeepStages>, &cfg)
+                               : cudaOccupancyMaxActiveClusters(&n, attend_kernel<true, kAttendStages>, &cfg);
+    if (e == cudaSuccess && n > 0) {
       best = c;
       break;
     }

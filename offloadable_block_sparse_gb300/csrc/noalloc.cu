@@ -144,7 +144,7 @@ extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* ca
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   noalloc_prepare_kernel<<<(2 * units + 255) / 256, 256, 0, cs>>>(scratch, context_len, units);
   if (cudaGetLastError() != cudaSuccess) return NOSA_ERR_CUDA;
-  if (launch_attend(s, &tmap, q, out, 0, cs) != cudaSuccess) {
+  if (launch_attend(s, &tmap, q, out, 0, false, cs) != cudaSuccess) {
     (void)cudaGetLastError();
     return NOSA_ERR_CUDA;
   }

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
 #include <vector>
 
 #include "../../include/nosa.h"
@@ -108,6 +109,7 @@ struct LayerState {
   int attend_chunks;       // split-K CTAs per unit in attend
   int attend_blocks_per_cta;
   int attend_cluster;      // 1: attend CTAs of a unit form a cluster and merge through DSMEM
+  int attend_deep;         // 1: one attend CTA per SM, with a deeper TMA pipeline
 };
 
 }  // namespace nosa
@@ -134,7 +136,7 @@ struct nosa_ctx {
   // scratch
   float *sq_blk, *apart;
   unsigned int* tickets;
-  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_cluster, gather_ctas;
+  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_cluster, attend_deep, gather_ctas;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   size_t stage_tok_cap;   // tokens per unit the bulk staging buffers hold
@@ -149,21 +151,53 @@ struct nosa_ctx {
 };
 
 namespace nosa {
+// Launch through cudaLaunchKernelEx: optional programmatic dependent launch
+// (the kernel overlaps its independent prologue with the previous kernel's
+// tail; it calls griddepcontrol.wait before touching that kernel's results)
+// and an optional cluster of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 LayerState layer_state(nosa_ctx* c, int layer);
-cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, cudaStream_t st);
+// pdl: launch as a programmatic dependent of the previous kernel in the stream
+cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, bool pdl, cudaStream_t st);
 cudaError_t launch_append_bulk(const LayerState& s, const uint16_t* k, const uint16_t* v, int T_old,
                                int n, cudaStream_t st);
-cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, cudaStream_t st);
+cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, bool pdl, cudaStream_t st);
 cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st);
 // fused_fetch != 0: blocks marked in sel_new are copied from the pinned host
 // store by the attend CTAs themselves (and written back to their slots), so no
 // separate gather launch is needed.
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
-                          int fused_fetch, cudaStream_t st);
+                          int fused_fetch, bool pdl, cudaStream_t st);
 size_t score_select_smem(const LayerState& s);
 // one-time kernel attributes (dynamic shared memory limits), called by nosa_create
 cudaError_t init_append(const LayerState& s);
 cudaError_t init_score_select(const LayerState& s);
 cudaError_t init_attend();
-int attend_max_cluster();
+int attend_max_cluster(bool deep);
 }  // namespace nosa

@@ -51,16 +51,23 @@ __device__ __forceinline__ float from_orderable(uint32_t k) {
 
 // Top-k over the blocks whose flag has `valid` set, run by one warp: sets `mark`
 // on the k largest keys, ties to the lower block index.  Radix select on the
-// 32-bit keys (4 passes of 8 bits).  Pooled scores share their high bits, so
-// lanes with equal digits are merged with __match_any_sync before one shared
-// atomic per distinct digit; the bins are scanned with warp shuffles.  The keys
+// keys' offsets from the smallest valid key: the passes start at the highest
+// bit of (max - min), so the 8-bit digits spread over the actual range of the
+// scores (pooled scores share their high bits) and the shared-memory histogram
+// atomics rarely collide; the bins are scanned with warp shuffles.  The keys
 // equal to the k-th largest are then taken in ascending block order by ballot.
 __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, uint8_t valid, uint8_t mark,
                           int* hist) {
   const int lane = threadIdx.x & 31;
   if (k <= 0) return;
   int cnt = 0;
-  for (int b = lane; b < n; b += 32) cnt += (flags[b] & valid) ? 1 : 0;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int b = lane; b < n; b += 32)
+    if (flags[b] & valid) {
+      ++cnt;
+      kmin = min(kmin, keys[b]);
+      kmax = max(kmax, keys[b]);
+    }
   cnt = warp_sum(cnt);
   if (cnt <= k) {
     for (int b = lane; b < n; b += 32)
@@ -68,17 +75,20 @@ __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, ui
     __syncwarp();
     return;
   }
-  uint32_t prefix = 0, pmask = 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  }
+  const int bits = 32 - __clz(kmax - kmin);  // offsets lie in [0, 2^bits)
+  uint32_t prefix = 0, pmask = 0;            // over offsets
   int need = k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = ((bits + 7) / 8 - 1) * 8; shift >= 0; shift -= 8) {
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
-    for (int base = 0; base < n; base += 32) {
-      const int b = base + lane;
-      const bool act = b < n && (flags[b] & valid) && (keys[b] & pmask) == prefix;
-      const int dg = act ? (int)((keys[b] >> shift) & 255u) : -1;
-      const unsigned int peers = __match_any_sync(0xffffffffu, dg);
-      if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[dg], __popc(peers));
+    for (int b = lane; b < n; b += 32) {
+      const uint32_t off = keys[b] - kmin;
+      if ((flags[b] & valid) && (off & pmask) == prefix) atomicAdd(&hist[(off >> shift) & 255u], 1);
     }
     __syncwarp();
     int c[8], tot = 0;
@@ -110,16 +120,17 @@ __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, ui
     pmask |= 255u << shift;
     __syncwarp();
   }
-  // prefix is the k-th largest key; `need` keys equal to it are taken, lowest blocks first
+  // kmin + prefix is the k-th largest key; `need` keys equal to it are taken, lowest blocks first
+  const uint32_t thr = kmin + prefix;
   int taken = 0;
   for (int base = 0; base < n; base += 32) {
     const int b = base + lane;
     const bool v = b < n && (flags[b] & valid);
     const uint32_t key = v ? keys[b] : 0u;
-    const bool tie = v && key == prefix;
+    const bool tie = v && key == thr;
     const unsigned int tm = __ballot_sync(0xffffffffu, tie);
     const int rank = taken + __popc(tm & ((1u << lane) - 1u));
-    if ((v && key > prefix) || (tie && rank < need)) flags[b] |= mark;
+    if ((v && key > thr) || (tie && rank < need)) flags[b] |= mark;
     taken += __popc(tm);
   }
   __syncwarp();
@@ -156,6 +167,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     for (int c = 0; c < 4; ++c)
       qf[c] = gr < G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
   }
+  pdl_wait();               // the append kernel's context length, keys and scores are needed from here
+  pdl_launch_dependents();  // the attention kernel may start its own prologue
   const Geometry geo = geometry(*s.T, s.nw, s.sink);
   const int nc = geo.nc, nb = geo.nb;
   const int i0 = rank * wpc;  // first window of this CTA
@@ -431,20 +444,9 @@ cudaError_t init_score_select(const LayerState& s) {
                               (int)score_select_smem(s));
 }
 
-cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(s.score_chunks, s.U);
-  cfg.blockDim = dim3(kScoreThreads);
-  cfg.dynamicSmemBytes = score_select_smem(s);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = s.score_chunks;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, score_select_kernel, s, q);
+cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, bool pdl, cudaStream_t st) {
+  return launch_ex(score_select_kernel, dim3(s.score_chunks, s.U), dim3(kScoreThreads), score_select_smem(s), st,
+                   pdl, s.score_chunks, s, q);
 }
 
 }  // namespace nosa
