@@ -268,6 +268,11 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->attend_chunks = cdiv(d.cap, bpc);
   c->attend_deep = c->attend_cluster && (long long)c->attend_chunks * c->U <= c->num_sms &&
                    attend_max_cluster(true) >= c->attend_chunks;
+  // measured: clusters of single-CTA-per-SM attends do not co-schedule well, so off unless asked for
+  {
+    const char* e = getenv("NOSA_ATTEND_DEEP");
+    c->attend_deep = c->attend_deep && e && atoi(e) != 0;
+  }
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
   c->stage_tok_cap = 512;
 

@@ -2,8 +2,8 @@
 // eq. 8: attention of q over K[selected], V[selected]; NOSA-1B blog,
 // sparse_forward: attention over the top-k block indices only).
 //
-// grid (attend_chunks, U), 128 threads.  CTA (chunk, u) owns entries
-// [chunk*bpc, chunk*bpc + bpc) of unit u's ascending selection.  One elected
+// grid (attend_chunks, U), 128 threads.  CTA (chunk, u) owns every
+// attend_chunks-th entry of unit u's selection (blocks still on the host first).  One elected
 // thread streams each 32 KiB block (K and V, two 16 KiB boxes with the 128-byte
 // swizzle) from the block cache into a 3-stage shared-memory ring with TMA
 // (cp.async.bulk.tensor) and an mbarrier per stage.  Warp w handles tokens
@@ -45,7 +45,6 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   __shared__ __align__(8) uint64_t bars[kStages];
   __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
   __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta], s_new[kMaxBlocksPerCta];
-  __shared__ int s_ord[kMaxBlocksPerCta];
   __shared__ int last, bad_any;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
@@ -69,41 +68,57 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   pdl_wait();               // the selection (previous kernel) is needed from here
   pdl_launch_dependents();  // the next layer's append may start
   const int nsel = s.n_sel[u];
-  const int e0 = chunk * s.attend_blocks_per_cta;
-  const int nblk = max(0, min(e0 + s.attend_blocks_per_cta, nsel) - e0);
   const uint32_t sbase = smem_u32(smem);
-
-  if (tid < nblk) {  // this CTA's block ids and cache slots, in one round trip
-    s_blk[tid] = s.sel[(size_t)u * s.cap + e0 + tid];
-    int slot = s.sel_slot[(size_t)u * s.cap + e0 + tid];
-    if (slot < 0 || slot >= s.cap) {
-      atomicOr(s.err, kErrBounds);
-      slot = 0;  // keep the copy in bounds; the result is flagged as invalid
+  // Work split: the unit's selected blocks are dealt round-robin to its CTAs in an
+  // order that puts the blocks still to be copied from the host first, so those
+  // few spread one per CTA and their copies start before anything else.
+  const int CS = gridDim.x;
+  const int nblk = chunk < nsel ? (nsel - chunk + CS - 1) / CS : 0;
+  if (warp == 0) {
+    int n_new = 0;
+    for (int base = 0; base < nsel; base += 32) {
+      const int e = base + lane;
+      const bool nw = e < nsel && fused_fetch && s.sel_new[(size_t)u * s.cap + e];
+      n_new += __popc(__ballot_sync(0xffffffffu, nw));
     }
-    s_slot[tid] = slot;
-    s_new[tid] = fused_fetch ? s.sel_new[(size_t)u * s.cap + e0 + tid] : 0;
+    int seen_new = 0, seen_old = 0;
+    for (int base = 0; base < nsel; base += 32) {
+      const int e = base + lane;
+      const bool in = e < nsel;
+      const bool nw = in && fused_fetch && s.sel_new[(size_t)u * s.cap + e];
+      const unsigned int bn = __ballot_sync(0xffffffffu, nw), bo = __ballot_sync(0xffffffffu, in && !nw);
+      const unsigned int below = (1u << lane) - 1u;
+      const int pos = nw ? seen_new + __popc(bn & below) : n_new + seen_old + __popc(bo & below);
+      seen_new += __popc(bn);
+      seen_old += __popc(bo);
+      if (in && pos % CS == chunk) {
+        const int i = pos / CS;
+        s_blk[i] = s.sel[(size_t)u * s.cap + e];
+        int slot = s.sel_slot[(size_t)u * s.cap + e];
+        if (slot < 0 || slot >= s.cap) {
+          atomicOr(s.err, kErrBounds);
+          slot = 0;  // keep the copy in bounds; the result is flagged as invalid
+        }
+        s_slot[i] = slot;
+        s_new[i] = nw ? 1 : 0;
+      }
+    }
   }
-  __syncthreads();
   if (tid == 0) {
     prefetch_tmap(&tmap);
     for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
     bad_any = 0;
-    // blocks coming over the host link first, so their latency overlaps the cached blocks' loads
-    int n = 0;
-    for (int i = 0; i < nblk; ++i)
-      if (s_new[i]) s_ord[n++] = i;
-    for (int i = 0; i < nblk; ++i)
-      if (!s_new[i]) s_ord[n++] = i;
   }
   __syncthreads();
-  // Stage i % kAttendStages receives entry e0+i: a cached block by TMA (thread 0),
+
+  // Stage i % kStages receives this CTA's i-th block: a cached block by TMA (thread 0),
   // or -- when the fetch is fused in -- a block without a slot straight from the
   // pinned host store by cp.async of all threads (rows past the context zero-filled).
   // One cp.async group is committed per entry (empty for TMA entries).
   auto issue = [&](int i) {
     const int st = i % kStages;
-    const int e = i < nblk ? s_ord[i] : 0;
+    const int e = i < nblk ? i : 0;
     const bool fresh = i < nblk && s_new[e];
     if (tid == 0 && i < nblk) {
       if (fresh) {
@@ -148,7 +163,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   int consumed = 0;
   for (int i = 0; i < nblk; ++i) {
     const int st = i % kStages;
-    const int e = s_ord[i];
+    const int e = i;
     const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((i / kStages) & 1), kWaitLimit);
     cp_async_wait<kStages - 1>();  // this entry's cp.async group (if any) has landed
     if (__syncthreads_or(!okw)) {

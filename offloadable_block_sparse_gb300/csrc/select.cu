@@ -51,10 +51,10 @@ __device__ __forceinline__ float from_orderable(uint32_t k) {
 
 // Top-k over the blocks whose flag has `valid` set, run by one warp: sets `mark`
 // on the k largest keys, ties to the lower block index.  Radix select on the
-// keys' offsets from the smallest valid key: the passes start at the highest
-// bit of (max - min), so the 8-bit digits spread over the actual range of the
-// scores (pooled scores share their high bits) and the shared-memory histogram
-// atomics rarely collide; the bins are scanned with warp shuffles.  The keys
+// keys' offsets from the smallest valid key, 8-bit digits taken from the
+// highest bit of (max - min) down, so the digits spread over the actual range
+// of the scores (pooled scores share their high bits) and the shared-memory
+// histogram atomics rarely collide; the bins are scanned with warp shuffles.  The keys
 // equal to the k-th largest are then taken in ascending block order by ballot.
 __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, uint8_t valid, uint8_t mark,
                           int* hist) {
@@ -83,12 +83,15 @@ __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, ui
   const int bits = 32 - __clz(kmax - kmin);  // offsets lie in [0, 2^bits)
   uint32_t prefix = 0, pmask = 0;            // over offsets
   int need = k;
-  for (int shift = ((bits + 7) / 8 - 1) * 8; shift >= 0; shift -= 8) {
+  // digits of 8 bits from the top of the offset range down; the last one may be narrower
+  for (int top = bits; top > 0; top -= 8) {
+    const int shift = max(top - 8, 0);
+    const uint32_t dmask = (1u << (top - shift)) - 1u;
     for (int i = lane; i < 256; i += 32) hist[i] = 0;
     __syncwarp();
     for (int b = lane; b < n; b += 32) {
       const uint32_t off = keys[b] - kmin;
-      if ((flags[b] & valid) && (off & pmask) == prefix) atomicAdd(&hist[(off >> shift) & 255u], 1);
+      if ((flags[b] & valid) && (off & pmask) == prefix) atomicAdd(&hist[(off >> shift) & dmask], 1);
     }
     __syncwarp();
     int c[8], tot = 0;
@@ -117,7 +120,7 @@ __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, int k, ui
     const int digit = __shfl_sync(0xffffffffu, fd, src);
     need -= __shfl_sync(0xffffffffu, fa, src);
     prefix |= (uint32_t)digit << shift;
-    pmask |= 255u << shift;
+    pmask |= dmask << shift;
     __syncwarp();
   }
   // kmin + prefix is the k-th largest key; `need` keys equal to it are taken, lowest blocks first
