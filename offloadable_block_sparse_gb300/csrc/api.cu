@@ -142,7 +142,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.score_wpc = c->score_wpc;
   s.attend_chunks = c->attend_chunks;
   s.attend_blocks_per_cta = c->attend_blocks_per_cta;
-  s.attend_cluster = c->attend_cluster;
+  s.attend_mode = c->attend_mode;
   s.attend_deep = c->attend_deep;
   return s;
 }
@@ -247,8 +247,9 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   // selector: one cluster of up to 8 CTAs per unit, each scoring a multiple of 128 windows
   c->score_chunks = std::min(8, cdiv(nc, kWindowsPerCta));
   c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
-  // attend: about two CTAs per SM in total, at most kMaxBlocksPerCta blocks each; the unit's
-  // CTAs form one cluster when the device can schedule clusters of that size
+  // attend: about two CTAs per SM in total, at most kMaxBlocksPerCta blocks each.  Merge of the
+  // split-K partials: by a small follow-up kernel (default), or inside one thread-block cluster
+  // per unit (needs clusters of the unit's CTA count to be schedulable), or by an atomic ticket.
   int bpc = cdiv((long long)c->U * d.cap, 2ll * std::max(c->num_sms, 1));
   bpc = std::min(std::max(bpc, 1), kMaxBlocksPerCta);
   if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), kMaxBlocksPerCta);
@@ -257,22 +258,18 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     delete c;
     return NOSA_ERR_CUDA;
   }
-  const int max_cluster = attend_max_cluster(false);
-  c->attend_cluster = 1;
-  if (const char* e = getenv("NOSA_ATTEND_CLUSTER")) c->attend_cluster = atoi(e) != 0;
-  if (c->attend_cluster) {
+  c->attend_mode = 2;
+  if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
+  if (c->attend_mode == 1) {
+    const int max_cluster = attend_max_cluster(false);
     while (cdiv(d.cap, bpc) > max_cluster && bpc < kMaxBlocksPerCta) ++bpc;
-    if (cdiv(d.cap, bpc) > max_cluster) c->attend_cluster = 0;
+    if (cdiv(d.cap, bpc) > max_cluster) c->attend_mode = 2;
   }
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
-  c->attend_deep = c->attend_cluster && (long long)c->attend_chunks * c->U <= c->num_sms &&
-                   attend_max_cluster(true) >= c->attend_chunks;
-  // measured: clusters of single-CTA-per-SM attends do not co-schedule well, so off unless asked for
-  {
-    const char* e = getenv("NOSA_ATTEND_DEEP");
-    c->attend_deep = c->attend_deep && e && atoi(e) != 0;
-  }
+  c->attend_deep = 0;
+  if (const char* e = getenv("NOSA_ATTEND_DEEP"))
+    c->attend_deep = c->attend_mode == 1 && atoi(e) != 0 && attend_max_cluster(true) >= c->attend_chunks;
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
   c->stage_tok_cap = 512;
 

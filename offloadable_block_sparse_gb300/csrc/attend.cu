@@ -34,10 +34,13 @@ __device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int t
   return stage + dhalf * 16384 + kv * 8192 + token * 128 + (((chunk ^ (token & 7)) & 7) << 4);
 }
 
-// kCluster: the unit's CTAs form one thread-block cluster and merge their
-// partials through distributed shared memory; otherwise they merge through
-// global scratch with an atomic ticket (the last CTA of the unit merges).
-template <bool kCluster, int kStages>
+// How a unit's split-K partials are merged:
+//   kMerge == kMergeTicket : through global scratch; the last CTA of the unit (atomic ticket) merges;
+//   kMerge == kMergeCluster: the unit's CTAs form one cluster and merge through distributed shared memory;
+//   kMerge == kMergeKernel : CTAs write their partials and exit; attend_merge_kernel merges.
+constexpr int kMergeTicket = 0, kMergeCluster = 1, kMergeKernel = 2;
+
+template <int kMerge, int kStages>
 __global__ void __launch_bounds__(kAttendThreads, 1)
     attend_kernel(const __grid_constant__ CUtensorMap tmap, LayerState s, const uint16_t* __restrict__ q,
                   uint16_t* __restrict__ out, int fused_fetch) {
@@ -280,7 +283,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
         O += wo[(w * kMaxGroup + h) * kHeadDim + x] * f;
       }
     }
-    if constexpr (kCluster) {
+    if constexpr (kMerge == kMergeCluster) {
       if (x == 0) {
         cp_m[h] = M;
         cp_l[h] = L;
@@ -295,7 +298,8 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
       part[2 + x] = O;
     }
   }
-  if constexpr (kCluster) {
+  if constexpr (kMerge == kMergeKernel) return;
+  if constexpr (kMerge == kMergeCluster) {
     // every CTA of the unit merges the heads h = rank, rank + CS, ... from all CTAs' partials
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank(), CS = (int)cluster.num_blocks();
@@ -387,33 +391,81 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
 
 size_t attend_smem_bytes(int stages) { return 1024 + (size_t)stages * kStageBytes; }
 
-template <bool C, int S>
+// Merges the split-K partials of one (head, unit): grid (group, U), 128 threads
+// (one per head dimension).  Launched as a programmatic dependent of the
+// attention kernel; every (m, l) pair and o value is requested at once.
+__global__ void __launch_bounds__(kHeadDim) attend_merge_kernel(LayerState s, uint16_t* __restrict__ out) {
+  __shared__ float fm[256], fl[256];
+  pdl_wait();  // the partials are written by the previous kernel
+  pdl_launch_dependents();
+  const int h = blockIdx.x, u = blockIdx.y, x = threadIdx.x;
+  const int nch = s.attend_chunks;
+  const float* pb = s.apart + ((size_t)u * nch * kMaxGroup + h) * kPartStride;
+  for (int j = x; j < nch; j += blockDim.x) {
+    fm[j] = pb[(size_t)j * kMaxGroup * kPartStride];
+    fl[j] = pb[(size_t)j * kMaxGroup * kPartStride + 1];
+  }
+  float ov[16];
+  const int first = min(nch, 16);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) ov[j] = j < first ? pb[(size_t)j * kMaxGroup * kPartStride + 2 + x] : 0.f;
+  __syncthreads();
+  float M = -INFINITY;
+  for (int j = 0; j < nch; ++j) M = fmaxf(M, fm[j]);
+  float L = 0.f, O = 0.f;
+  if (M > -INFINITY) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < first && fm[j] > -INFINITY) {
+        const float f = exp2f(fm[j] - M);
+        L += fl[j] * f;
+        O = fmaf(ov[j], f, O);
+      }
+    for (int j = 16; j < nch; ++j)
+      if (fm[j] > -INFINITY) {
+        const float f = exp2f(fm[j] - M);
+        L += fl[j] * f;
+        O = fmaf(pb[(size_t)j * kMaxGroup * kPartStride + 2 + x], f, O);
+      }
+  }
+  const float r = L > 0.f ? O / L : 0.f;
+  out[((size_t)u * s.G + h) * kHeadDim + x] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
+}
+
+template <int M, int S>
 static cudaError_t set_attend_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(attend_kernel<C, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(attend_kernel<M, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)attend_smem_bytes(S));
-  if (e != cudaSuccess || !C) return e;
-  return cudaFuncSetAttribute(attend_kernel<C, S>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess || M != kMergeCluster) return e;
+  return cudaFuncSetAttribute(attend_kernel<M, S>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 cudaError_t init_attend() {
-  cudaError_t e = set_attend_attrs<false, kAttendStages>();
-  if (e == cudaSuccess) e = set_attend_attrs<true, kAttendStages>();
-  if (e == cudaSuccess) e = set_attend_attrs<true, kDeepStages>();
+  cudaError_t e = set_attend_attrs<kMergeTicket, kAttendStages>();
+  if (e == cudaSuccess) e = set_attend_attrs<kMergeCluster, kAttendStages>();
+  if (e == cudaSuccess) e = set_attend_attrs<kMergeCluster, kDeepStages>();
+  if (e == cudaSuccess) e = set_attend_attrs<kMergeKernel, kAttendStages>();
   return e;
 }
 
-template <bool C, int S>
+template <int M, int S>
 static cudaError_t launch_attend_t(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                                    int fused_fetch, bool pdl, cudaStream_t st) {
-  return launch_ex(attend_kernel<C, S>, dim3(s.attend_chunks, s.U), dim3(kAttendThreads), attend_smem_bytes(S), st,
-                   pdl, C ? s.attend_chunks : 0, *tmap, s, q, out, fused_fetch);
+  return launch_ex(attend_kernel<M, S>, dim3(s.attend_chunks, s.U), dim3(kAttendThreads), attend_smem_bytes(S), st,
+                   pdl, M == kMergeCluster ? s.attend_chunks : 0, *tmap, s, q, out, fused_fetch);
 }
 
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                           int fused_fetch, bool pdl, cudaStream_t st) {
-  if (!s.attend_cluster) return launch_attend_t<false, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
-  if (s.attend_deep) return launch_attend_t<true, kDeepStages>(s, tmap, q, out, fused_fetch, pdl, st);
-  return launch_attend_t<true, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
+  if (s.attend_mode == kMergeKernel) {
+    cudaError_t e = launch_attend_t<kMergeKernel, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
+    if (e != cudaSuccess) return e;
+    return launch_ex(attend_merge_kernel, dim3(s.G, s.U), dim3(kHeadDim), 0, st, true, 0, s, out);
+  }
+  if (s.attend_mode == kMergeTicket)
+    return launch_attend_t<kMergeTicket, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
+  if (s.attend_deep) return launch_attend_t<kMergeCluster, kDeepStages>(s, tmap, q, out, fused_fetch, pdl, st);
+  return launch_attend_t<kMergeCluster, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
 }
 
 // Largest cluster of attend CTAs (with this kernel's shared memory) the device can schedule.
@@ -432,8 +484,9 @@ int attend_max_cluster(bool deep) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = deep ? cudaOccupancyMaxActiveClusters(&n, attend_kernel<true, kDeepStages>, &cfg)
-                               : cudaOccupancyMaxActiveClusters(&n, attend_kernel<true, kAttendStages>, &cfg);
+    const cudaError_t e =
+        deep ? cudaOccupancyMaxActiveClusters(&n, attend_kernel<kMergeCluster, kDeepStages>, &cfg)
+             : cudaOccupancyMaxActiveClusters(&n, attend_kernel<kMergeCluster, kAttendStages>, &cfg);
     if (e == cudaSuccess && n > 0) {
       best = c;
       break;

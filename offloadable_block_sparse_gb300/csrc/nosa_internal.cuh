@@ -108,7 +108,7 @@ struct LayerState {
   int score_wpc;           // compressed windows per selector CTA (multiple of 128)
   int attend_chunks;       // split-K CTAs per unit in attend
   int attend_blocks_per_cta;
-  int attend_cluster;      // 1: attend CTAs of a unit form a cluster and merge through DSMEM
+  int attend_mode;         // split-K merge: 0 ticket (global), 1 cluster (DSMEM), 2 merge kernel
   int attend_deep;         // 1: one attend CTA per SM, with a deeper TMA pipeline
 };
 
@@ -136,7 +136,7 @@ struct nosa_ctx {
   // scratch
   float *sq_blk, *apart;
   unsigned int* tickets;
-  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_cluster, attend_deep, gather_ctas;
+  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_mode, attend_deep, gather_ctas;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   size_t stage_tok_cap;   // tokens per unit the bulk staging buffers hold

@@ -12,7 +12,9 @@
 //      its windows onto the 64-token blocks they overlap (NOSA explainer
 //      eq. 5-6), combining into the leader CTA's block scores with remote
 //      atomic max.
-//   3. cluster barrier; the leader selects: top-k_q query-aware blocks, then
+//   3. every CTA ranks the candidate blocks it owns and sends its k_q best to
+//      the leader; after a third barrier the leader selects: the top-k_q of
+//      those query-aware candidates, then
 //      k_e blocks by the pooled eviction score among candidates never dropped
 //      before (wiki "How NOSA works": query-aware picks set to +inf, the rest
 //      filled by the query-agnostic score, never-reselect constraint); sink and
@@ -34,8 +36,10 @@ namespace {
 
 constexpr uint8_t F_CAND = 1, F_ELIG = 2, F_Q = 4, F_E = 8, F_S = 16, F_NEW = 32;
 constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // orderable(-inf)
+constexpr int kMaxScoreCluster = 8;
 
 struct SelShared {
+  int cand_n[kMaxScoreCluster];  // leader: local winners per cluster CTA
   int scan[32];
   int hist[256];
   int free_by_rank[256];
@@ -158,7 +162,10 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   float* sek = reinterpret_cast<float*>(keys + s.nb_max);         // leader: [nb_max] pooled s^e
   int32_t* b2s = reinterpret_cast<int32_t*>(sek + s.nb_max);      // leader: [nb_max] block -> slot
   uint32_t* evw = reinterpret_cast<uint32_t*>(b2s + s.nb_max);    // leader: [ev_words]
-  uint8_t* flags = reinterpret_cast<uint8_t*>(evw + s.ev_words);  // leader: [nb_max]
+  uint32_t* cand_key = evw + s.ev_words;                          // leader: [8][k_q] local winners' keys
+  int32_t* cand_blk = reinterpret_cast<int32_t*>(cand_key + kMaxScoreCluster * s.k_q);  // [8][k_q]
+  int32_t* eblk = cand_blk + kMaxScoreCluster * s.k_q;             // leader: [nb_max] eligible blocks
+  uint8_t* flags = reinterpret_cast<uint8_t*>(eblk + s.nb_max);   // leader: [nb_max]
 
   // q fragments first: they do not depend on the context length.  The k order in
   // each 32-dim chunk is permuted identically for A (K~ rows) and B (q), so a
@@ -289,29 +296,100 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     }
   }
   cluster.sync();  // block maxima have landed in the leader; remote reads are done
+
+  // ---------------- 2b. each CTA ranks the candidate blocks it owns (a contiguous range);
+  // its k_q best go to the leader, which then ranks only those (at most 8 * k_q)
+  const int ws = geo.ws, kq = s.k_q;
+  {
+    const int nbpc = (nb + CS - 1) / CS;
+    const int ob0 = min(rank * nbpc, nb), ob1 = min(ob0 + nbpc, nb);
+    const int cb0 = max(ob0, s.sink), cb1 = min(ob1, ws);
+    const int nown = max(cb1 - cb0, 0);
+    uint32_t* lk = reinterpret_cast<uint32_t*>(sqs);  // wpc >= 128 and >= owned blocks
+    const uint32_t* lkeys = cluster.map_shared_rank(keys, 0);
+    for (int i = tid; i < nown; i += blockDim.x) lk[i] = lkeys[cb0 + i];
+    __syncthreads();
+    uint32_t* ckey = cluster.map_shared_rank(cand_key, 0);
+    int32_t* cblk = cluster.map_shared_rank(cand_blk, 0);
+    for (int i = tid; i < nown && kq > 0; i += blockDim.x) {
+      const uint32_t ki = lk[i];
+      int r = 0;  // higher score first, then lower block
+      for (int j = 0; j < nown; ++j) {
+        const uint32_t kj = lk[j];
+        r += (kj > ki) || (kj == ki && j < i);
+      }
+      if (r < kq) {
+        ckey[rank * kq + r] = ki;
+        cblk[rank * kq + r] = cb0 + i;
+      }
+    }
+    if (tid == 0) *cluster.map_shared_rank(&sh.cand_n[rank], 0) = min(nown, max(kq, 0));
+  }
+  cluster.sync();  // the local winners have landed in the leader
   if (rank != 0) return;
 
   // ---------------- 3. selection by the leader
-  const int ws = geo.ws;
   for (int b = tid; b < nb; b += blockDim.x) {
     s.sq_blk[(size_t)u * s.nb_max + b] = from_orderable(keys[b]);
     flags[b] = (b >= s.sink && b < ws) ? F_CAND : 0;
   }
   __syncthreads();
-  if (warp == 0) warp_topk(keys, flags, nb, s.k_q, F_CAND, F_Q, sh.hist);
-  __syncthreads();
-  for (int b = tid; b < nb; b += blockDim.x) {
-    keys[b] = orderable(sek[b]);
-    const bool evb = (evw[b >> 5] >> (b & 31)) & 1u;
-    if ((flags[b] & F_CAND) && !(flags[b] & F_Q) && !evb) flags[b] |= F_ELIG;
+  // query-aware: rank among the gathered local winners
+  for (int idx = tid; idx < CS * kq; idx += blockDim.x) {
+    const int ri = idx / kq;
+    if (idx % kq >= sh.cand_n[ri]) continue;
+    const uint32_t ki = cand_key[idx];
+    const int bi = cand_blk[idx];
+    int r = 0;
+    for (int rj = 0; rj < CS; ++rj)
+      for (int j = 0; j < sh.cand_n[rj]; ++j) {
+        const uint32_t kj = cand_key[rj * kq + j];
+        r += (kj > ki) || (kj == ki && cand_blk[rj * kq + j] < bi);
+      }
+    if (r < kq) flags[bi] |= F_Q;
   }
   __syncthreads();
-  if (warp == 0) warp_topk(keys, flags, nb, s.k_e, F_ELIG, F_E, sh.hist);
+  // query-agnostic: candidates outside Q never dropped before, ranked by pooled s^e
+  const int per = (nb + blockDim.x - 1) / blockDim.x;
+  const int lo = min(tid * per, nb), hi = min(lo + per, nb);
+  int nel = 0;
+  for (int b = lo; b < hi; ++b) {
+    const bool evb = (evw[b >> 5] >> (b & 31)) & 1u;
+    if ((flags[b] & F_CAND) && !(flags[b] & F_Q) && !evb) {
+      flags[b] |= F_ELIG;
+      ++nel;
+    }
+  }
+  int n_elig;
+  int epos = block_scan_excl(nel, sh.scan, &n_elig);
+  if (n_elig <= s.k_e) {
+    for (int b = lo; b < hi; ++b)
+      if (flags[b] & F_ELIG) flags[b] |= F_E;
+  } else if (n_elig <= 1024) {
+    for (int b = lo; b < hi; ++b)
+      if (flags[b] & F_ELIG) {
+        keys[epos] = orderable(sek[b]);
+        eblk[epos] = b;
+        ++epos;
+      }
+    __syncthreads();
+    for (int i = tid; i < n_elig; i += blockDim.x) {
+      const uint32_t ki = keys[i];
+      int r = 0;  // eligible blocks are in ascending order: ties go to the lower index
+      for (int j = 0; j < n_elig; ++j) {
+        const uint32_t kj = keys[j];
+        r += (kj > ki) || (kj == ki && j < i);
+      }
+      if (r < s.k_e) flags[eblk[i]] |= F_E;
+    }
+  } else {  // many eligible blocks (a first selection over a long context): radix select
+    for (int b = tid; b < nb; b += blockDim.x) keys[b] = orderable(sek[b]);
+    __syncthreads();
+    if (warp == 0) warp_topk(keys, flags, nb, s.k_e, F_ELIG, F_E, sh.hist);
+  }
   __syncthreads();
 
   // selection S and the blocks without a slot; contiguous per-thread ranges keep block order
-  const int per = (nb + blockDim.x - 1) / blockDim.x;
-  const int lo = min(tid * per, nb), hi = min(lo + per, nb);
   int nD = 0, nE = 0, nDnew = 0, nS = 0, nNew = 0;
   for (int b = lo; b < hi; ++b) {
     uint8_t f = flags[b];
@@ -438,8 +516,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
 }
 
 size_t score_select_smem(const LayerState& s) {
-  return sizeof(float) * (kMaxGroup + 1) * s.score_wpc + 3 * sizeof(uint32_t) * s.nb_max +
-         sizeof(uint32_t) * s.ev_words + s.nb_max + 16;
+  return sizeof(float) * (kMaxGroup + 1) * s.score_wpc + 4 * sizeof(uint32_t) * s.nb_max +
+         sizeof(uint32_t) * s.ev_words + 2 * sizeof(uint32_t) * kMaxScoreCluster * s.k_q + s.nb_max + 16;
 }
 
 cudaError_t init_score_select(const LayerState& s) {
