@@ -115,40 +115,47 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   }
   __syncthreads();
 
-  // Stage i % kStages receives this CTA's i-th block: a cached block by TMA (thread 0),
-  // or -- when the fetch is fused in -- a block without a slot straight from the
-  // pinned host store by cp.async of all threads (rows past the context zero-filled).
-  // One cp.async group is committed per entry (empty for TMA entries).
-  auto issue = [&](int i) {
-    const int st = i % kStages;
-    const int e = i < nblk ? i : 0;
-    const bool fresh = i < nblk && s_new[e];
-    if (tid == 0 && i < nblk) {
-      if (fresh) {
-        mbar_arrive(&bars[st]);
-      } else {
-        const int flat = (s.unit_base + u) * s.cap + s_slot[e];
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[st], kStageBytes);
-        tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
-        tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
-      }
-    }
-    if (fresh) {
-      const int rows = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
-      const uint16_t* src = s.host_kv + ((size_t)u * s.nb_max + s_blk[e]) * 2 * kBlockElems;
+  // Pipeline.  Blocks without a cache slot (first in this CTA's list) are copied
+  // straight from the pinned host store by cp.async of all threads into
+  // dedicated stages right away (rows past the context zero-filled) and consumed
+  // last, so the host-link latency overlaps the cached blocks.  Cached blocks
+  // stream through the remaining stages as a ring, each loaded by one TMA
+  // (thread 0) completing on the stage's mbarrier.  Host blocks beyond the
+  // dedicated stages (rare) pass through the ring as well.
+  int nnew = 0;
+  while (nnew < nblk && s_new[nnew]) ++nnew;
+  const int ded = min(nnew, kStages - 1);  // dedicated stages 0 .. ded-1
+  const int ring = kStages - ded;          // ring stages ded .. kStages-1
+  const int nr = nblk - ded;               // ring entries: local entries ded .. nblk-1
+  auto host_copy = [&](int e, int st) {    // all threads
+    const int rows = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
+    const uint16_t* src = s.host_kv + ((size_t)u * s.nb_max + s_blk[e]) * 2 * kBlockElems;
 #pragma unroll 4
-      for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
-        const int idx = tid + j * kAttendThreads;  // 16-byte chunk: K|V, row, chunk of the 256-byte row
-        const int kv = idx >> 10, r = (idx >> 4) & 63, cc = idx & 15;
-        cp_async_16(swz(sbase + st * kStageBytes, cc >> 3, kv, r, cc & 7),
-                    src + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8, r < rows ? 16u : 0u);
-      }
+    for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
+      const int idx = tid + j * kAttendThreads;  // 16-byte chunk: K|V, row, chunk of the 256-byte row
+      const int kv = idx >> 10, r = (idx >> 4) & 63, cc = idx & 15;
+      cp_async_16(swz(sbase + st * kStageBytes, cc >> 3, kv, r, cc & 7),
+                  src + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8, r < rows ? 16u : 0u);
     }
     cp_async_commit();
   };
-  for (int i = 0; i < kStages; ++i) issue(i);
-  int issued = kStages;
+  auto issue_ring = [&](int p) {  // ring entry p into stage ded + p % ring
+    if (p >= nr) return;
+    const int st = ded + p % ring, e = ded + p;
+    if (s_new[e]) {
+      if (tid == 0) mbar_arrive(&bars[st]);
+      host_copy(e, st);
+    } else if (tid == 0) {
+      const int flat = (s.unit_base + u) * s.cap + s_slot[e];
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bars[st], kStageBytes);
+      tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
+      tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
+    }
+  };
+  for (int d = 0; d < ded; ++d) host_copy(d, d);
+  for (int p = 0; p < ring; ++p) issue_ring(p);
+  int issued = ring;
 
   const float sl2 = s.scale * 1.4426950408889634f;  // softmax in base 2
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -163,20 +170,10 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   const int tk_v = tok0 + (lane & 7) + ((lane >> 4) << 3);        // V^T: (d lo|hi) x (tokens 0-7|8-15)
   const int ch_v = (lane >> 3) & 1;
 
-  int consumed = 0;
-  for (int i = 0; i < nblk; ++i) {
-    const int st = i % kStages;
-    const int e = i;
-    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((i / kStages) & 1), kWaitLimit);
-    cp_async_wait<kStages - 1>();  // this entry's cp.async group (if any) has landed
-    if (__syncthreads_or(!okw)) {
-      if (tid == 0) atomicOr(s.err, kErrTimeout);
-      bad_any = 1;
-      break;
-    }
-    consumed = i + 1;
+  // one 64-token block in stage memory stg: warp's 16 tokens, online softmax, PV; fetched
+  // blocks are also written to their cache slot for later steps
+  auto process = [&](uint32_t stg, int e) {
     const int valid = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
-    const uint32_t stg = sbase + st * kStageBytes;
     if (tok0 < valid) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -221,7 +218,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
         mma_16816(o[mt], a, pb0, pb1);
       }
     }
-    if (s_new[e]) {  // a fetched block also goes to its cache slot for later steps
+    if (s_new[e]) {
       uint16_t* dst = s.cache + ((size_t)u * s.cap + s_slot[e]) * 2 * kBlockElems;
 #pragma unroll 4
       for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
@@ -234,14 +231,31 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
         *reinterpret_cast<uint4*>(dst + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8) = v;
       }
     }
+  };
+
+  int consumed = 0;
+  for (int p = 0; p < nr; ++p) {
+    const int st = ded + p % ring, e = ded + p;
+    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((p / ring) & 1), kWaitLimit);
+    if (s_new[e]) cp_async_wait_all();  // a host block that passed through the ring
+    if (__syncthreads_or(!okw)) {
+      if (tid == 0) atomicOr(s.err, kErrTimeout);
+      bad_any = 1;
+      break;
+    }
+    consumed = p + 1;
+    process(sbase + st * kStageBytes, e);
     __syncthreads();  // every warp is done with this stage
-    issue(issued);
+    issue_ring(issued);
     ++issued;
   }
   cp_async_wait_all();
+  __syncthreads();  // the dedicated host blocks have landed
+  if (!bad_any)
+    for (int d = 0; d < ded; ++d) process(sbase + d * kStageBytes, d);
   if (bad_any && tid == 0) {  // drain copies still in flight before the shared memory is reused
-    for (int i = consumed; i < min(issued, nblk); ++i)
-      mbar_wait_bounded(&bars[i % kStages], (uint32_t)((i / kStages) & 1), kWaitLimit);
+    for (int p = consumed; p < min(issued, nr); ++p)
+      mbar_wait_bounded(&bars[ded + p % ring], (uint32_t)((p / ring) & 1), kWaitLimit);
   }
   __syncthreads();
   // warp partials -> shared memory

@@ -266,14 +266,20 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   cluster.sync();  // every CTA's statistics (and the leader's key init) are visible
 
   // ---------------- 2. unit statistics, window scores, pooled block maxima -> leader
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int r = 0; r < CS; ++r) M = fmaxf(M, *cluster.map_shared_rank(&sh.Mloc[tid], r));
-    float S = 0.f;
-    for (int r = 0; r < CS; ++r) {
-      const float mr = *cluster.map_shared_rank(&sh.Mloc[tid], r);
-      if (mr > -INFINITY) S += *cluster.map_shared_rank(&sh.Sloc[tid], r) * expf(mr - M);
+  if (tid < G) {  // all CTAs' statistics for head tid, requested at once
+    float mr[kMaxScoreCluster], sr[kMaxScoreCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxScoreCluster; ++r) {
+      mr[r] = r < CS ? *cluster.map_shared_rank(&sh.Mloc[tid], r) : -INFINITY;
+      sr[r] = r < CS ? *cluster.map_shared_rank(&sh.Sloc[tid], r) : 0.f;
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int r = 0; r < kMaxScoreCluster; ++r) M = fmaxf(M, mr[r]);
+    float S = 0.f;
+#pragma unroll
+    for (int r = 0; r < kMaxScoreCluster; ++r)
+      if (mr[r] > -INFINITY) S += sr[r] * expf(mr[r] - M);
     sh.Mh[tid] = M;
     sh.invS[tid] = 1.f / S;
   }
@@ -314,6 +320,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     for (int i = tid; i < nown && kq > 0; i += blockDim.x) {
       const uint32_t ki = lk[i];
       int r = 0;  // higher score first, then lower block
+#pragma unroll 8
       for (int j = 0; j < nown; ++j) {
         const uint32_t kj = lk[j];
         r += (kj > ki) || (kj == ki && j < i);
@@ -334,18 +341,37 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     flags[b] = (b >= s.sink && b < ws) ? F_CAND : 0;
   }
   __syncthreads();
-  // query-aware: rank among the gathered local winners
+  // query-aware: compact the gathered local winners, then rank them
+  __shared__ int cofs[kMaxScoreCluster + 1];
+  if (tid == 0) {
+    int o = 0;
+    for (int r = 0; r < CS; ++r) {
+      cofs[r] = o;
+      o += sh.cand_n[r];
+    }
+    cofs[CS] = o;
+  }
+  __syncthreads();
+  const int ncand = cofs[CS];
+  uint32_t* qk = keys;                           // compact winners' keys (the block keys are no longer needed)
+  int32_t* qb = eblk;                            // and their blocks
   for (int idx = tid; idx < CS * kq; idx += blockDim.x) {
-    const int ri = idx / kq;
-    if (idx % kq >= sh.cand_n[ri]) continue;
-    const uint32_t ki = cand_key[idx];
-    const int bi = cand_blk[idx];
+    const int ri = idx / kq, j = idx % kq;
+    if (j < sh.cand_n[ri]) {
+      qk[cofs[ri] + j] = cand_key[idx];
+      qb[cofs[ri] + j] = cand_blk[idx];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < ncand; i += blockDim.x) {
+    const uint32_t ki = qk[i];
+    const int bi = qb[i];
     int r = 0;
-    for (int rj = 0; rj < CS; ++rj)
-      for (int j = 0; j < sh.cand_n[rj]; ++j) {
-        const uint32_t kj = cand_key[rj * kq + j];
-        r += (kj > ki) || (kj == ki && cand_blk[rj * kq + j] < bi);
-      }
+#pragma unroll 8
+    for (int j = 0; j < ncand; ++j) {
+      const uint32_t kj = qk[j];
+      r += (kj > ki) || (kj == ki && qb[j] < bi);
+    }
     if (r < kq) flags[bi] |= F_Q;
   }
   __syncthreads();
@@ -376,6 +402,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     for (int i = tid; i < n_elig; i += blockDim.x) {
       const uint32_t ki = keys[i];
       int r = 0;  // eligible blocks are in ascending order: ties go to the lower index
+#pragma unroll 8
       for (int j = 0; j < n_elig; ++j) {
         const uint32_t kj = keys[j];
         r += (kj > ki) || (kj == ki && j < i);
