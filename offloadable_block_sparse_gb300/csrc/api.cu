@@ -248,8 +248,9 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->score_chunks = std::min(8, cdiv(nc, kWindowsPerCta));
   c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
   // attend: about two CTAs per SM in total, at most kMaxBlocksPerCta blocks each.  Merge of the
-  // split-K partials: by a small follow-up kernel (default), or inside one thread-block cluster
-  // per unit (needs clusters of the unit's CTA count to be schedulable), or by an atomic ticket.
+  // split-K partials: inside one thread-block cluster per unit (default, when clusters of the
+  // unit's CTA count can be scheduled), else by a small follow-up kernel; an atomic ticket merge
+  // is kept for the context-free entry point.
   int bpc = cdiv((long long)c->U * d.cap, 2ll * std::max(c->num_sms, 1));
   bpc = std::min(std::max(bpc, 1), kMaxBlocksPerCta);
   if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), kMaxBlocksPerCta);
@@ -258,7 +259,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     delete c;
     return NOSA_ERR_CUDA;
   }
-  c->attend_mode = 2;
+  c->attend_mode = 1;
   if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
   if (c->attend_mode == 1) {
     const int max_cluster = attend_max_cluster(false);

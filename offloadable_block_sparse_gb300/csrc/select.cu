@@ -49,6 +49,27 @@ struct SelShared {
   int4 wsum[kScoreWarps];
 };
 
+// Composite ranking key: higher score first, then lower block.  Distinct blocks give
+// distinct keys, so a rank is one branch-free count of larger keys.
+__device__ __forceinline__ unsigned long long rank_key(uint32_t score_key, int blk) {
+  return ((unsigned long long)score_key << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)blk);
+}
+
+// Rank of key ki among list[0..n): the number of larger keys (loads pipelined, no branches).
+__device__ __forceinline__ int count_larger(const unsigned long long* list, int n, unsigned long long ki) {
+  int r = 0;
+#pragma unroll 8
+  for (int j = 0; j < n; ++j) r += list[j] > ki ? 1 : 0;
+  return r;
+}
+
+// Floats of the first shared-memory region: the window logits, later reused for
+// 64-bit ranking keys (up to 8 * k_q gathered winners, or one per block).
+__host__ __device__ inline int zs_floats(const LayerState& s) {
+  const int keys64 = 2 * (kMaxScoreCluster * s.k_q > s.nb_max ? kMaxScoreCluster * s.k_q : s.nb_max);
+  return kMaxGroup * s.score_wpc > keys64 ? kMaxGroup * s.score_wpc : keys64;
+}
+
 __device__ __forceinline__ float from_orderable(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
@@ -156,8 +177,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   const int u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gr = lane >> 2, t4 = lane & 3;
   const int G = s.G, wpc = s.score_wpc;
-  float* zs = reinterpret_cast<float*>(dsm);                      // [kMaxGroup][wpc]
-  float* sqs = zs + kMaxGroup * wpc;                              // [wpc]
+  float* zs = reinterpret_cast<float*>(dsm);                      // [kMaxGroup][wpc], later ranking keys
+  float* sqs = zs + zs_floats(s);                                 // [wpc]
   uint32_t* keys = reinterpret_cast<uint32_t*>(sqs + wpc);        // leader: [nb_max]
   float* sek = reinterpret_cast<float*>(keys + s.nb_max);         // leader: [nb_max] pooled s^e
   int32_t* b2s = reinterpret_cast<int32_t*>(sek + s.nb_max);      // leader: [nb_max] block -> slot
@@ -311,22 +332,17 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     const int ob0 = min(rank * nbpc, nb), ob1 = min(ob0 + nbpc, nb);
     const int cb0 = max(ob0, s.sink), cb1 = min(ob1, ws);
     const int nown = max(cb1 - cb0, 0);
-    uint32_t* lk = reinterpret_cast<uint32_t*>(sqs);  // wpc >= 128 and >= owned blocks
+    unsigned long long* lk = reinterpret_cast<unsigned long long*>(zs);  // z is no longer needed
     const uint32_t* lkeys = cluster.map_shared_rank(keys, 0);
-    for (int i = tid; i < nown; i += blockDim.x) lk[i] = lkeys[cb0 + i];
+    for (int i = tid; i < nown; i += blockDim.x) lk[i] = rank_key(lkeys[cb0 + i], cb0 + i);
     __syncthreads();
     uint32_t* ckey = cluster.map_shared_rank(cand_key, 0);
     int32_t* cblk = cluster.map_shared_rank(cand_blk, 0);
     for (int i = tid; i < nown && kq > 0; i += blockDim.x) {
-      const uint32_t ki = lk[i];
-      int r = 0;  // higher score first, then lower block
-#pragma unroll 8
-      for (int j = 0; j < nown; ++j) {
-        const uint32_t kj = lk[j];
-        r += (kj > ki) || (kj == ki && j < i);
-      }
+      const unsigned long long ki = lk[i];
+      const int r = count_larger(lk, nown, ki);
       if (r < kq) {
-        ckey[rank * kq + r] = ki;
+        ckey[rank * kq + r] = (uint32_t)(ki >> 32);
         cblk[rank * kq + r] = cb0 + i;
       }
     }
@@ -341,7 +357,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     flags[b] = (b >= s.sink && b < ws) ? F_CAND : 0;
   }
   __syncthreads();
-  // query-aware: compact the gathered local winners, then rank them
+  // query-aware: gather the CTAs' winners into one list of composite keys and rank them
+  unsigned long long* ck = reinterpret_cast<unsigned long long*>(zs);
   __shared__ int cofs[kMaxScoreCluster + 1];
   if (tid == 0) {
     int o = 0;
@@ -353,26 +370,14 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   }
   __syncthreads();
   const int ncand = cofs[CS];
-  uint32_t* qk = keys;                           // compact winners' keys (the block keys are no longer needed)
-  int32_t* qb = eblk;                            // and their blocks
   for (int idx = tid; idx < CS * kq; idx += blockDim.x) {
     const int ri = idx / kq, j = idx % kq;
-    if (j < sh.cand_n[ri]) {
-      qk[cofs[ri] + j] = cand_key[idx];
-      qb[cofs[ri] + j] = cand_blk[idx];
-    }
+    if (j < sh.cand_n[ri]) ck[cofs[ri] + j] = rank_key(cand_key[idx], cand_blk[idx]);
   }
   __syncthreads();
   for (int i = tid; i < ncand; i += blockDim.x) {
-    const uint32_t ki = qk[i];
-    const int bi = qb[i];
-    int r = 0;
-#pragma unroll 8
-    for (int j = 0; j < ncand; ++j) {
-      const uint32_t kj = qk[j];
-      r += (kj > ki) || (kj == ki && qb[j] < bi);
-    }
-    if (r < kq) flags[bi] |= F_Q;
+    const unsigned long long ki = ck[i];
+    if (count_larger(ck, ncand, ki) < kq) flags[0xFFFFFFFFu - (uint32_t)ki] |= F_Q;
   }
   __syncthreads();
   // query-agnostic: candidates outside Q never dropped before, ranked by pooled s^e
@@ -392,22 +397,13 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     for (int b = lo; b < hi; ++b)
       if (flags[b] & F_ELIG) flags[b] |= F_E;
   } else if (n_elig <= 1024) {
+    unsigned long long* ek = reinterpret_cast<unsigned long long*>(zs);
     for (int b = lo; b < hi; ++b)
-      if (flags[b] & F_ELIG) {
-        keys[epos] = orderable(sek[b]);
-        eblk[epos] = b;
-        ++epos;
-      }
+      if (flags[b] & F_ELIG) ek[epos++] = rank_key(orderable(sek[b]), b);
     __syncthreads();
     for (int i = tid; i < n_elig; i += blockDim.x) {
-      const uint32_t ki = keys[i];
-      int r = 0;  // eligible blocks are in ascending order: ties go to the lower index
-#pragma unroll 8
-      for (int j = 0; j < n_elig; ++j) {
-        const uint32_t kj = keys[j];
-        r += (kj > ki) || (kj == ki && j < i);
-      }
-      if (r < s.k_e) flags[eblk[i]] |= F_E;
+      const unsigned long long ki = ek[i];
+      if (count_larger(ek, n_elig, ki) < s.k_e) flags[0xFFFFFFFFu - (uint32_t)ki] |= F_E;
     }
   } else {  // many eligible blocks (a first selection over a long context): radix select
     for (int b = tid; b < nb; b += blockDim.x) keys[b] = orderable(sek[b]);
@@ -543,7 +539,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
 }
 
 size_t score_select_smem(const LayerState& s) {
-  return sizeof(float) * (kMaxGroup + 1) * s.score_wpc + 4 * sizeof(uint32_t) * s.nb_max +
+  return sizeof(float) * ((size_t)zs_floats(s) + s.score_wpc) + 4 * sizeof(uint32_t) * s.nb_max +
          sizeof(uint32_t) * s.ev_words + 2 * sizeof(uint32_t) * kMaxScoreCluster * s.k_q + s.nb_max + 16;
 }
 
