@@ -182,7 +182,7 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
   const long long cap = (long long)c->sink_blocks + c->window_tokens / kBlock + c->k_q + c->k_e;
-  if (cap < 1 || cap > 256) return NOSA_ERR_INVALID_ARG;
+  if (cap < 1 || cap > kMaxCacheSlots) return NOSA_ERR_INVALID_ARG;
   if ((long long)c->num_layers * U * cap >= (1ll << 31)) return NOSA_ERR_INVALID_ARG;
   return NOSA_OK;
 }
@@ -269,8 +269,15 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
   c->attend_deep = 0;
-  if (const char* e = getenv("NOSA_ATTEND_DEEP"))
-    c->attend_deep = c->attend_mode == 1 && atoi(e) != 0 && attend_max_cluster(true) >= c->attend_chunks;
+  if (const char* e = getenv("NOSA_ATTEND_DEEP")) {
+    c->attend_deep = atoi(e) != 0 && (c->attend_mode == 2 || attend_max_cluster(true) >= c->attend_chunks);
+    if (c->attend_deep && c->attend_mode == 2 && !getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) {
+      // one CTA per SM: chunks such that units x chunks is about the SM count
+      bpc = std::min(std::max(cdiv((long long)c->U * d.cap, std::max(c->num_sms, 1)), 1), kMaxBlocksPerCta);
+      c->attend_blocks_per_cta = bpc;
+      c->attend_chunks = cdiv(d.cap, bpc);
+    }
+  }
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
   c->stage_tok_cap = 512;
 

@@ -78,17 +78,29 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   const int CS = gridDim.x;
   const int nblk = chunk < nsel ? (nsel - chunk + CS - 1) / CS : 0;
   if (warp == 0) {
+    // one round trip: every entry's block, slot and fetched mark, requested with the count
+    int ev[kMaxCacheSlots / 32][3];
+#pragma unroll
+    for (int it = 0; it < kMaxCacheSlots / 32; ++it) {
+      const int e = it * 32 + lane;
+      const bool in = e < s.cap;
+      const size_t o = (size_t)u * s.cap + (in ? e : 0);
+      ev[it][0] = in ? s.sel[o] : -1;
+      ev[it][1] = in ? s.sel_slot[o] : 0;
+      ev[it][2] = (in && fused_fetch) ? s.sel_new[o] : 0;
+    }
     int n_new = 0;
-    for (int base = 0; base < nsel; base += 32) {
-      const int e = base + lane;
-      const bool nw = e < nsel && fused_fetch && s.sel_new[(size_t)u * s.cap + e];
-      n_new += __popc(__ballot_sync(0xffffffffu, nw));
+#pragma unroll
+    for (int it = 0; it < kMaxCacheSlots / 32; ++it) {
+      const int e = it * 32 + lane;
+      n_new += __popc(__ballot_sync(0xffffffffu, e < nsel && ev[it][2]));
     }
     int seen_new = 0, seen_old = 0;
-    for (int base = 0; base < nsel; base += 32) {
-      const int e = base + lane;
+#pragma unroll
+    for (int it = 0; it < kMaxCacheSlots / 32; ++it) {
+      const int e = it * 32 + lane;
       const bool in = e < nsel;
-      const bool nw = in && fused_fetch && s.sel_new[(size_t)u * s.cap + e];
+      const bool nw = in && ev[it][2];
       const unsigned int bn = __ballot_sync(0xffffffffu, nw), bo = __ballot_sync(0xffffffffu, in && !nw);
       const unsigned int below = (1u << lane) - 1u;
       const int pos = nw ? seen_new + __popc(bn & below) : n_new + seen_old + __popc(bo & below);
@@ -96,12 +108,12 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
       seen_old += __popc(bo);
       if (in && pos % CS == chunk) {
         const int i = pos / CS;
-        s_blk[i] = s.sel[(size_t)u * s.cap + e];
-        int slot = s.sel_slot[(size_t)u * s.cap + e];
+        int slot = ev[it][1];
         if (slot < 0 || slot >= s.cap) {
           atomicOr(s.err, kErrBounds);
           slot = 0;  // keep the copy in bounds; the result is flagged as invalid
         }
+        s_blk[i] = ev[it][0];
         s_slot[i] = slot;
         s_new[i] = nw ? 1 : 0;
       }
@@ -459,6 +471,7 @@ cudaError_t init_attend() {
   if (e == cudaSuccess) e = set_attend_attrs<kMergeCluster, kAttendStages>();
   if (e == cudaSuccess) e = set_attend_attrs<kMergeCluster, kDeepStages>();
   if (e == cudaSuccess) e = set_attend_attrs<kMergeKernel, kAttendStages>();
+  if (e == cudaSuccess) e = set_attend_attrs<kMergeKernel, kDeepStages>();
   return e;
 }
 
@@ -472,7 +485,8 @@ static cudaError_t launch_attend_t(const LayerState& s, const CUtensorMap* tmap,
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                           int fused_fetch, bool pdl, cudaStream_t st) {
   if (s.attend_mode == kMergeKernel) {
-    cudaError_t e = launch_attend_t<kMergeKernel, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
+    cudaError_t e = s.attend_deep ? launch_attend_t<kMergeKernel, kDeepStages>(s, tmap, q, out, fused_fetch, pdl, st)
+                                  : launch_attend_t<kMergeKernel, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
     if (e != cudaSuccess) return e;
     return launch_ex(attend_merge_kernel, dim3(s.G, s.U), dim3(kHeadDim), 0, st, true, 0, s, out);
   }

@@ -204,15 +204,20 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   const int nc = geo.nc, nb = geo.nb;
   const int i0 = rank * wpc;  // first window of this CTA
 
-  // leader: request the selection's inputs now; they arrive during the scoring
+  // leader: request the selection's inputs now as asynchronous copies into shared
+  // memory; they land while the scoring runs (waited for before the selection)
   int my_slot_blk = -1;
   if (rank == 0) {
+    const float* seg = s.se_blk + (size_t)u * s.nb_max;
+    const int32_t* b2g = s.blk2slot + (size_t)u * s.nb_max;
+    const uint32_t* evg = s.evicted + (size_t)u * s.ev_words;
     for (int b = tid; b < nb; b += blockDim.x) {
       keys[b] = kKeyNegInf;
-      sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
-      b2s[b] = s.blk2slot[(size_t)u * s.nb_max + b];
+      cp_async_4(smem_u32(sek + b), seg + b);
+      cp_async_4(smem_u32(b2s + b), b2g + b);
     }
-    for (int w = tid; w < (nb + 31) / 32; w += blockDim.x) evw[w] = s.evicted[(size_t)u * s.ev_words + w];
+    for (int w = tid; w < (nb + 31) / 32; w += blockDim.x) cp_async_4(smem_u32(evw + w), evg + w);
+    cp_async_commit();
     if (tid < s.cap) my_slot_blk = s.slot_blk[(size_t)u * s.cap + tid];
   }
 
@@ -350,6 +355,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   }
   cluster.sync();  // the local winners have landed in the leader
   if (rank != 0) return;
+  cp_async_wait_all();  // the leader's early copies (pooled s^e, slot map, eviction words)
 
   // ---------------- 3. selection by the leader
   for (int b = tid; b < nb; b += blockDim.x) {

@@ -130,11 +130,24 @@ def test_out_of_order_calls_are_rejected():
         p.close()
 
 
-@pytest.mark.parametrize("name,steps,samples,layers", [
-    ("nosa1b_16k_b8", 256, [(0, 0, 0), (5, 3, 1), (17, 7, 0), (27, 6, 1)], None),
-])
-def test_full_size_sampled(name, steps, samples, layers):
-    wl = syn.workload(name)
+# Full-size workloads, every unit run on the GPU, sampled units checked against the oracle at every
+# step.  The 8B-shaped workload keeps its per-layer sizes (32 sequences x 8 kv heads x 32K tokens)
+# but runs 8 of its 32 layers: its full host store (138 GB pinned) exceeds the test machine's RAM.
+FULL = [
+    ("nosa1b_16k_b8", 256, [(0, 0, 0), (5, 3, 1), (17, 7, 0), (27, 6, 1)], None, {}),
+    ("nosa1b_16k_b128", 128, [(0, 0, 0), (13, 77, 1), (27, 127, 0)], None, {}),
+    ("nosa1b_16k_b128", 64, [(3, 5, 0), (20, 100, 1)], None, {"sigma": 1.0}),
+    ("nosa8b_32k_b32", 128, [(0, 0, 0), (4, 17, 5), (7, 31, 7)], 8, {}),
+    ("nosa1b_64k_b32", 64, [(0, 0, 0), (14, 9, 1), (27, 31, 0)], None, {}),
+    ("nosa1b_64k_b32", 32, [(1, 2, 1), (26, 30, 0)], None, {"k_q": 32, "k_e": 32}),
+]
+
+
+@pytest.mark.parametrize("name,steps,samples,layers,over", FULL,
+                         ids=[f"{n}-{s}steps-{'-'.join(f'{k}{v}' for k, v in o.items()) or 'base'}"
+                              for n, s, _, _, o in FULL])
+def test_full_size_sampled(name, steps, samples, layers, over):
+    wl = syn.workload(name, **over)
     log, stats = run(wl, steps, samples=samples, layers=layers)
     _report(name, log, stats)
     assert log.unit_steps == steps * len(samples)
