@@ -153,6 +153,21 @@ def oracle_baseline(wl, seconds, total_units):
                       f"{dt:.1f} s; numpy float64 with its default BLAS threading"}
 
 
+def slowest_rank_ms(ms: float, world: int, device: str = "cpu") -> float:
+    """Per-step time of the slowest rank (max over ranks; every rank must call it)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(batch_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job decode tokens/s: every rank serves its own batch (weak scaling)."""
+    return world * batch_per_rank / (ms_per_step * 1e-3)
+
+
 # ---------------------------------------------------------------------------- native arm
 def run_native(args, rank, world, local_rank):
     import torch
@@ -171,7 +186,7 @@ def run_native(args, rank, world, local_rank):
     U = B * Hkv
     K, W = args.steps, args.warmup
     n_time_leg = 0 if args.quick else min(K, 8)
-    n_e2e = 0 if args.quick else min(K, 8)
+    n_e2e = 0 if args.quick else min(K, 16)
     total_steps = 1 + W + K + n_time_leg + n_e2e
     cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=wl.context + total_steps,
@@ -260,11 +275,8 @@ def run_native(args, rank, world, local_rank):
     if st != N.NOSA_OK:
         raise RuntimeError(f"device error {N.STATUS_NAMES[st]}")
     stats = N.nosa_get_stats(ctx)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * B / (ms * 1e-3)
+    ms = slowest_rank_ms(ms, world, dev)
+    value = job_throughput(B, world, ms)
     fetched_per_step = stats.blocks_fetched / K
 
     result = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -346,31 +358,68 @@ def run_native(args, rank, world, local_rank):
     result["stages_us_per_layer"] = us
     result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / ((us["attend"] + us["select"]) * 1e-6) / 1e9 / hbm
 
-    # ---------------- e2e: the public host-pointer API, copies inside the timed region
-    qh = torch.empty((n_e2e, L, B, Hq, d), dtype=torch.bfloat16).pin_memory()
-    kvh = torch.empty((n_e2e, 2, L, B, Hkv, d), dtype=torch.bfloat16).pin_memory()
-    oh = torch.empty((n_e2e, L, B, Hq, d), dtype=torch.bfloat16).pin_memory()
-    t_base = step_i[0]
-    qh.copy_(Qall[t_base:t_base + n_e2e])
-    kvh.copy_(KVall[t_base:t_base + n_e2e])
+    # ---------------- e2e: the public host-pointer API (nosa_step_host), copies inside the timed region.
+    # Two CUDA graphs, each capturing the 28 layers' nosa_step_host calls on its own set of pinned
+    # host buffers, alternate: while one replays, the host writes the next step's inputs into the
+    # other set (after that set's previous replay has finished) and reads the step's outputs back.
+    e2e_graph = use_graph
+    sets = [dict(q=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory(),
+                 kv=torch.empty((2, L, B, Hkv, d), dtype=torch.bfloat16).pin_memory(),
+                 out=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
+    q_src = Qall[step_i[0]:step_i[0] + n_e2e].cpu()
+    kv_src = KVall[step_i[0]:step_i[0] + n_e2e].cpu()
+    outs_host = torch.empty((n_e2e, L, B, Hq, d), dtype=torch.bfloat16)
+
+    def host_step(bs):
+        for l in range(L):
+            N.nosa_step_host(ctx, l, bs["q"][l].view(i16), bs["kv"][0, l].view(i16), bs["kv"][1, l].view(i16),
+                             bs["out"][l].view(i16))
+
+    graphs_e2e = []
+    if e2e_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        N.nosa_set_stream(ctx, side.cuda_stream)
+        for bs in sets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                host_step(bs)
+            graphs_e2e.append(g)
+        N.nosa_set_stream(ctx, stream.cuda_stream)
+        assert N.nosa_sync(ctx) == N.NOSA_OK
     torch.cuda.synchronize()
+    done = [None, None]
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     a.record(stream)
     for j in range(n_e2e):
-        for l in range(L):
-            N.nosa_step_host(ctx, l, qh[j, l].view(i16), kvh[j, 0, l].view(i16), kvh[j, 1, l].view(i16),
-                             oh[j, l].view(i16))
+        k = j % 2
+        bs = sets[k]
+        if done[k] is not None:
+            done[k].synchronize()                   # that set's previous step has finished
+            outs_host[j - 2].copy_(bs["out"])       # read its result back on the host
+        bs["q"].copy_(q_src[j])
+        bs["kv"].copy_(kv_src[j])
+        if e2e_graph:
+            graphs_e2e[k].replay()
+        else:
+            host_step(bs)
+        done[k] = torch.cuda.Event()
+        done[k].record(stream)
     b.record(stream)
     torch.cuda.synchronize()
+    for j in range(max(0, n_e2e - 2), n_e2e):
+        outs_host[j].copy_(sets[j % 2]["out"])
     wall = time.perf_counter() - t0
     step_i[0] += n_e2e
     e2e_ms = max(a.elapsed_time(b), wall * 1e3) / n_e2e
     result["e2e"] = {"value": B / (e2e_ms * 1e-3), "unit": "tok/s", "ms_per_step": e2e_ms,
                      "h2d_bytes_per_step": L * (B * Hq * d * 2 + 2 * U * d * 2),
                      "d2h_bytes_per_step": L * B * Hq * d * 2,
-                     "how": "nosa_step_host per layer from pinned host q/k/v, output read back to pinned host; "
-                            "no CUDA graph; max of device-event and host wall time"}
+                     "how": "nosa_step_host for every layer from pinned host q/k/v, outputs copied back to pinned "
+                            "host and read on the host; " + ("two alternating CUDA graphs of those calls"
+                                                            if e2e_graph else "eager calls") +
+                            "; max of device-event and host wall time"}
     assert N.nosa_sync(ctx) == N.NOSA_OK
     N.nosa_destroy(ctx)
     del Qall, KVall

@@ -65,7 +65,16 @@ typedef enum {
   NOSA_ERR_STATE = 8        /* call out of order, or the context is in a failed state */
 } nosa_status;
 
-/* Flags for nosa_config.flags (none defined yet; must be 0). */
+/* Flags for nosa_config.flags.  Both are test hooks that fault and hang nothing:
+ * NOSA_F_TEST_ZERO_WAIT  the attention kernel's waits for its staged blocks give
+ *                        up at once, so the timeout path runs (copies already in
+ *                        flight are still drained with the normal bound) and
+ *                        NOSA_ERR_TIMEOUT is latched;
+ * NOSA_F_TEST_BAD_SLOT   the selector publishes an out-of-range cache slot for the
+ *                        first selected block of unit 0; the attention kernel clamps
+ *                        it and NOSA_ERR_BOUNDS is latched. */
+#define NOSA_F_TEST_ZERO_WAIT 1u
+#define NOSA_F_TEST_BAD_SLOT 2u
 
 typedef struct {
   uint32_t struct_size;   /* sizeof(nosa_config) */
@@ -85,7 +94,7 @@ typedef struct {
   int32_t evict_hidden;   /* eviction-head hidden size h: multiple of 32, 32..256 */
   int32_t gather_ctas;    /* CTAs of the persistent fetch kernel; 0 = rule 16 if B<32 else 32 */
   float softmax_scale;    /* 0 => 1/sqrt(head_dim) */
-  uint32_t flags;         /* must be 0 */
+  uint32_t flags;         /* 0, or NOSA_F_TEST_* hooks */
 } nosa_config;
 
 /* Derived sizes; filled by nosa_query_sizes (host only, no GPU needed). */

@@ -144,6 +144,8 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.attend_blocks_per_cta = c->attend_blocks_per_cta;
   s.attend_mode = c->attend_mode;
   s.attend_deep = c->attend_deep;
+  s.wait_limit = (c->cfg.flags & NOSA_F_TEST_ZERO_WAIT) ? 0 : kWaitCycles;
+  s.test_bad_slot = (c->cfg.flags & NOSA_F_TEST_BAD_SLOT) ? 1 : 0;
   return s;
 }
 }  // namespace nosa
@@ -178,7 +180,8 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->max_context < 1 || c->max_context > 262144) return NOSA_ERR_INVALID_ARG;
   if (c->evict_hidden < 32 || c->evict_hidden > 256 || c->evict_hidden % 32) return NOSA_ERR_INVALID_ARG;
   if (c->gather_ctas < 0 || c->gather_ctas > 4096) return NOSA_ERR_INVALID_ARG;
-  if (!(c->softmax_scale >= 0.f) || c->flags != 0) return NOSA_ERR_INVALID_ARG;
+  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT)))
+    return NOSA_ERR_INVALID_ARG;
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
   const long long cap = (long long)c->sink_blocks + c->window_tokens / kBlock + c->k_q + c->k_e;

@@ -28,7 +28,7 @@ namespace nosa {
 constexpr int kStageBytes = kBlockBytes;            // 32 KiB: [d half][K,V][64 tokens][64 dims]
 static_assert(4 * kMaxGroup * kHeadDim * 4 <= 3 * kStageBytes, "warp partials alias the stages");
 constexpr int kDeepStages = 6;  // when a unit's CTAs get an SM each
-constexpr long long kWaitLimit = 2000000000LL;      // ~1 s of SM clocks
+constexpr long long kWaitLimit = kWaitCycles;  // bound of the drain waits after a timeout
 
 __device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int token, int chunk) {
   return stage + dhalf * 16384 + kv * 8192 + token * 128 + (((chunk ^ (token & 7)) & 7) << 4);
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   int consumed = 0;
   for (int p = 0; p < nr; ++p) {
     const int st = ded + p % ring, e = ded + p;
-    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((p / ring) & 1), kWaitLimit);
+    const bool okw = mbar_wait_bounded(&bars[st], (uint32_t)((p / ring) & 1), s.wait_limit);
     if (s_new[e]) cp_async_wait_all();  // a host block that passed through the ring
     if (__syncthreads_or(!okw)) {
       if (tid == 0) atomicOr(s.err, kErrTimeout);

@@ -39,6 +39,7 @@ constexpr int kMaxCacheSlots = 256;        // cache slots per unit (sink + windo
 constexpr int kPartStride = 2 + kHeadDim;  // (m, l, o[128]) per head in a split-K partial
 
 constexpr int kGatherThreads = 512;
+constexpr long long kWaitCycles = 2000000000LL;  // bounded device waits: about a second of SM clocks
 
 // Per-layer derived quantities from the context length T (same formulas on host and device).
 struct Geometry {
@@ -111,6 +112,8 @@ struct LayerState {
   int attend_blocks_per_cta;
   int attend_mode;         // split-K merge: 0 ticket (global), 1 cluster (DSMEM), 2 merge kernel
   int attend_deep;         // 1: one attend CTA per SM, with a deeper TMA pipeline
+  long long wait_limit;    // SM cycles a staged-block wait may take before it reports a timeout
+  int test_bad_slot;       // test hook: publish one out-of-range slot (unit 0, first entry)
 };
 
 }  // namespace nosa

@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
     if (pos < s.cap) {
       sel[pos] = b;
       kind[pos] = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
-      sslot[pos] = b2s[b];
+      sslot[pos] = (s.test_bad_slot && u == 0 && pos == 0) ? s.cap : b2s[b];  // test hook
       snew[pos] = (f & F_NEW) ? 1 : 0;
     } else {
       atomicOr(s.err, kErrBounds);

@@ -18,6 +18,8 @@ NOSA_OK = 0
 STATUS_NAMES = ["NOSA_OK", "NOSA_ERR_INVALID_ARG", "NOSA_ERR_OOM", "NOSA_ERR_HOST_ALLOC", "NOSA_ERR_CUDA",
                 "NOSA_ERR_CAPACITY", "NOSA_ERR_TIMEOUT", "NOSA_ERR_BOUNDS", "NOSA_ERR_STATE"]
 globals().update({n: i for i, n in enumerate(STATUS_NAMES)})
+NOSA_F_TEST_ZERO_WAIT = 1
+NOSA_F_TEST_BAD_SLOT = 2
 
 # every entry point declared in include/nosa.h
 EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_destroy", "nosa_set_stream",

@@ -130,6 +130,33 @@ def test_out_of_order_calls_are_rejected():
         p.close()
 
 
+def _one_step(p):
+    q, k, v = p.step_inputs(0)
+    out = torch.empty_like(q)
+    N.nosa_step(p.ctx, 0, q.view(torch.int16), k.view(torch.int16), v.view(torch.int16), out.view(torch.int16))
+
+
+@pytest.mark.parametrize("flag,status", [(N.NOSA_F_TEST_ZERO_WAIT, N.NOSA_ERR_TIMEOUT),
+                                         (N.NOSA_F_TEST_BAD_SLOT, N.NOSA_ERR_BOUNDS)])
+def test_device_errors_are_latched_and_recoverable(flag, status):
+    # Failure detection without a fault or a hang: a test hook makes the attention kernel's
+    # bounded waits give up at once, or publishes an out-of-range slot that the kernel clamps.
+    wl = syn.Workload("hook", layers=1, batch=2, q_heads=16, kv_heads=2, context=2048, k_q=4, k_e=12,
+                      window_tokens=256, steps=4)
+    p = Parity(wl, sample_units=[], flags=flag)
+    try:
+        p.load_context()
+        _one_step(p)
+        assert N.nosa_sync(p.ctx) == status
+        with pytest.raises(N.NosaError) as e:     # the context stays failed ...
+            _one_step(p)
+        assert e.value.status == N.NOSA_ERR_STATE
+        N.nosa_reset_state(p.ctx)                 # ... until the error is cleared
+        assert N.nosa_sync(p.ctx) == N.NOSA_OK
+    finally:
+        p.close()
+
+
 # Full-size workloads, every unit run on the GPU, sampled units checked against the oracle at every
 # step.  The 8B-shaped workload keeps its per-layer sizes (32 sequences x 8 kv heads x 32K tokens)
 # but runs 8 of its 32 layers: its full host store (138 GB pinned) exceeds the test machine's RAM.
