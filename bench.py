@@ -416,8 +416,9 @@ def run_native(args, rank, world, local_rank):
     result["e2e"] = {"value": B / (e2e_ms * 1e-3), "unit": "tok/s", "ms_per_step": e2e_ms,
                      "h2d_bytes_per_step": L * (B * Hq * d * 2 + 2 * U * d * 2),
                      "d2h_bytes_per_step": L * B * Hq * d * 2,
-                     "how": "nosa_step_host for every layer from pinned host q/k/v, outputs copied back to pinned "
-                            "host and read on the host; " + ("two alternating CUDA graphs of those calls"
+                     "how": "nosa_step_host for every layer on pinned host q/k/v/out (the kernels read the inputs "
+                            "and write the outputs in place over the host link), outputs then copied out of the "
+                            "pinned buffers on the host; " + ("two alternating CUDA graphs of those calls"
                                                             if e2e_graph else "eager calls") +
                             "; max of device-event and host wall time"}
     assert N.nosa_sync(ctx) == N.NOSA_OK

@@ -66,10 +66,13 @@ typedef enum {
 } nosa_status;
 
 /* Flags for nosa_config.flags.  Both are test hooks that fault and hang nothing:
- * NOSA_F_TEST_ZERO_WAIT  the attention kernel's waits for its staged blocks give
- *                        up at once, so the timeout path runs (copies already in
- *                        flight are still drained with the normal bound) and
- *                        NOSA_ERR_TIMEOUT is latched;
+ * NOSA_F_TEST_ZERO_WAIT  the attention kernel's waits for blocks staged through its
+ *                        copy ring give up without waiting, so the timeout path
+ *                        runs (copies already in flight are still drained with the
+ *                        normal bound) and NOSA_ERR_TIMEOUT is latched.  A step whose
+ *                        blocks all come from host memory into dedicated stages (the
+ *                        first step after a cold start, small batches) has no such
+ *                        wait; the first step that reads a cached block latches it;
  * NOSA_F_TEST_BAD_SLOT   the selector publishes an out-of-range cache slot for the
  *                        first selected block of unit 0; the attention kernel clamps
  *                        it and NOSA_ERR_BOUNDS is latched. */
@@ -193,9 +196,12 @@ nosa_status nosa_attend(nosa_ctx* ctx, int layer, const uint16_t* q, uint16_t* o
 nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                       const uint16_t* v_new, uint16_t* out);
 
-/* nosa_step with host (pinned) q, k_new, v_new and out: the inputs are copied
- * to context-owned device buffers and the output back, on the stream.  out is
- * written when the stream reaches the end of the step. */
+/* nosa_step with host q, k_new, v_new and out.  When all four are page-locked
+ * (cudaHostAlloc / cudaHostRegister) the kernels read the inputs and write the
+ * output in place over the host link; otherwise the inputs are copied to
+ * context-owned device buffers and the output back, on the stream.  Either way
+ * the buffers must stay untouched until the stream reaches the end of the step,
+ * when out is written. */
 nosa_status nosa_step_host(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, uint16_t* out);
 

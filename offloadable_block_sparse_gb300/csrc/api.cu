@@ -144,7 +144,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.attend_blocks_per_cta = c->attend_blocks_per_cta;
   s.attend_mode = c->attend_mode;
   s.attend_deep = c->attend_deep;
-  s.wait_limit = (c->cfg.flags & NOSA_F_TEST_ZERO_WAIT) ? 0 : kWaitCycles;
+  s.wait_limit = (c->cfg.flags & NOSA_F_TEST_ZERO_WAIT) ? -1 : kWaitCycles;
   s.test_bad_slot = (c->cfg.flags & NOSA_F_TEST_BAD_SLOT) ? 1 : 0;
   return s;
 }
@@ -519,11 +519,29 @@ nosa_status nosa_step(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t*
   return NOSA_OK;
 }
 
+// The device address of page-locked host memory (cudaHostAlloc / cudaHostRegister), or
+// nullptr for memory the device cannot address (pageable allocations).
+static void* pinned_device_view(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 nosa_status nosa_step_host(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                            uint16_t* out) {
   nosa_status st = check_ctx(c, layer);
   if (st != NOSA_OK) return st;
   if (!q || !k_new || !v_new || !out) return NOSA_ERR_INVALID_ARG;
+  // Page-locked buffers are read and written by the kernels in place over the host link:
+  // no copy operations between the three kernels, so they stay chained.
+  void *dq = pinned_device_view(q), *dk = pinned_device_view(k_new), *dv = pinned_device_view(v_new),
+       *dout = pinned_device_view(out);
+  if (dq && dk && dv && dout)
+    return nosa_step(c, layer, static_cast<const uint16_t*>(dq), static_cast<const uint16_t*>(dk),
+                     static_cast<const uint16_t*>(dv), static_cast<uint16_t*>(dout));
   const size_t qbytes = (size_t)c->B * c->Hq * kHeadDim * 2, kvbytes = (size_t)c->U * kHeadDim * 2;
   CK(cudaMemcpyAsync(c->stage_q, q, qbytes, cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->stage_k, k_new, kvbytes, cudaMemcpyHostToDevice, c->stream));

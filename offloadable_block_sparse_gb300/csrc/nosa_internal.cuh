@@ -112,7 +112,7 @@ struct LayerState {
   int attend_blocks_per_cta;
   int attend_mode;         // split-K merge: 0 ticket (global), 1 cluster (DSMEM), 2 merge kernel
   int attend_deep;         // 1: one attend CTA per SM, with a deeper TMA pipeline
-  long long wait_limit;    // SM cycles a staged-block wait may take before it reports a timeout
+  long long wait_limit;    // SM cycles a staged-block wait may take before it reports a timeout (<0: none)
   int test_bad_slot;       // test hook: publish one out-of-range slot (unit 0, first entry)
 };
 

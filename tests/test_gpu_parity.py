@@ -146,8 +146,13 @@ def test_device_errors_are_latched_and_recoverable(flag, status):
     p = Parity(wl, sample_units=[], flags=flag)
     try:
         p.load_context()
-        _one_step(p)
-        assert N.nosa_sync(p.ctx) == status
+        got = N.NOSA_OK
+        for _ in range(2):  # the first step after a cold start may read every block from host memory
+            _one_step(p)
+            got = N.nosa_sync(p.ctx)
+            if got != N.NOSA_OK:
+                break
+        assert got == status
         with pytest.raises(N.NosaError) as e:     # the context stays failed ...
             _one_step(p)
         assert e.value.status == N.NOSA_ERR_STATE
@@ -155,6 +160,45 @@ def test_device_errors_are_latched_and_recoverable(flag, status):
         assert N.nosa_sync(p.ctx) == N.NOSA_OK
     finally:
         p.close()
+
+
+def test_host_pointer_step_matches_device_step():
+    # nosa_step_host reads page-locked inputs in place and copies pageable ones; both must give
+    # exactly the device-pointer step's outputs (same kernels, same inputs, deterministic merges).
+    wl = syn.Workload("host", layers=2, batch=3, q_heads=16, kv_heads=2, context=1500, k_q=4, k_e=12,
+                      window_tokens=256, steps=6)
+    ps = [Parity(wl, sample_units=[]) for _ in range(3)]
+    try:
+        for p in ps:
+            p.load_context()
+        gen = torch.Generator(device="cuda").manual_seed(77)
+        for t in range(wl.steps):
+            for l in range(wl.layers):
+                q = torch.randn((wl.batch, wl.q_heads, 128), generator=gen, device="cuda")
+                q = (q / q.norm(dim=-1, keepdim=True) * math.sqrt(128)).to(torch.bfloat16)
+                k = torch.randn((wl.batch, wl.kv_heads, 128), generator=gen, device="cuda").to(torch.bfloat16)
+                v = torch.randn((wl.batch, wl.kv_heads, 128), generator=gen, device="cuda").to(torch.bfloat16)
+                outs = []
+                out_d = torch.empty_like(q)
+                N.nosa_step(ps[0].ctx, l, q.view(torch.int16), k.view(torch.int16), v.view(torch.int16),
+                            out_d.view(torch.int16))
+                outs.append(out_d)
+                for p, pin in ((ps[1], True), (ps[2], False)):
+                    hq, hk, hv = (x.cpu() for x in (q, k, v))
+                    ho = torch.empty_like(hq)
+                    if pin:
+                        hq, hk, hv, ho = hq.pin_memory(), hk.pin_memory(), hv.pin_memory(), ho.pin_memory()
+                    N.nosa_step_host(p.ctx, l, hq.view(torch.int16), hk.view(torch.int16), hv.view(torch.int16),
+                                     ho.view(torch.int16))
+                    assert N.nosa_sync(p.ctx) == N.NOSA_OK
+                    outs.append(ho)
+                assert N.nosa_sync(ps[0].ctx) == N.NOSA_OK
+                ref = outs[0].cpu().view(torch.int16)
+                for o in outs[1:]:
+                    assert torch.equal(o.view(torch.int16), ref), (t, l)
+    finally:
+        for p in ps:
+            p.close()
 
 
 # Full-size workloads, every unit run on the GPU, sampled units checked against the oracle at every
