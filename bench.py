@@ -185,7 +185,7 @@ def run_native(args, rank, world, local_rank):
     B, Hq, Hkv, d = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
     U = B * Hkv
     K, W = args.steps, args.warmup
-    n_time_leg = 0 if args.quick else min(K, 8)
+    n_time_leg = 0 if args.quick else 2 * min(K, 8)
     n_e2e = 0 if args.quick else min(K, 16)
     total_steps = 1 + W + K + n_time_leg + n_e2e
     cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
@@ -194,6 +194,7 @@ def run_native(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     sizes = N.nosa_query_sizes(cfg)
+    step_kernels, decode_cluster = N.nosa_step_plan(ctx)
     gen = torch.Generator(device=dev).manual_seed(1000 * rank + 7)
     cgen = torch.Generator().manual_seed(1000 * rank + 11)
     for l in range(L):
@@ -287,9 +288,10 @@ def run_native(args, rank, world, local_rank):
                          "sink_blocks": wl.sink_blocks, "window_tokens": wl.window_tokens, "sigma": wl.sigma,
                          "parallelism": f"replicas x{world} (independent sequences per GPU)",
                          "cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
+                         "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster,
                          "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache "
                                "(L2 is 129 MB)"},
-              "gpu_launches": 3 * L * K,
+              "gpu_launches": step_kernels * L * K,
               "clocks": ck,
               "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min, "bound": wl.k_e / (wl.k_q + wl.k_e)},
               "fetch_blocks_per_step": fetched_per_step,
@@ -299,22 +301,30 @@ def run_native(args, rank, world, local_rank):
         return result
 
     # ---------------- per-kernel leg: one event pair around each launch, on the launching stream.
-    # The step's kernels are append, select and attend (which fetches the new blocks itself);
-    # the standalone gather kernel (nosa_fetch) is then re-run on the same fetch list to time it.
-    ev = {k: [] for k in ("append", "select", "attend", "gather")}
-    N.nosa_reset_stats(ctx)
-    for _ in range(n_time_leg):
+    # Even steps time nosa_step per layer (the fused decode kernel, or its three kernels); odd
+    # steps time the separate calls: append, select and attend (which fetches the new blocks
+    # itself), then the standalone gather kernel (nosa_fetch) re-run on the same fetch list.
+    ev = {k: [] for k in ("decode", "append", "select", "attend", "gather")}
+    fetched_split = 0
+    for it in range(n_time_leg):
         t = step_i[0]
         step_i[0] += 1
+        if it % 2:
+            s0 = N.nosa_get_stats(ctx).blocks_fetched
         for l in range(L):
             pairs = []
             # hold the stream while the launches and their events are queued, so that the
             # events time the kernels back to back rather than the host's launch latency
             torch.cuda._sleep(400000)
-            calls = [("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16), KVall[t, 1, l].view(i16), 1)),
-                     ("select", lambda: N.nosa_select(ctx, l, Qall[t, l].view(i16))),
-                     ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16))),
-                     ("gather", lambda: N.nosa_fetch(ctx, l))]
+            if it % 2 == 0:
+                calls = [("decode", lambda: N.nosa_step(ctx, l, Qall[t, l].view(i16), KVall[t, 0, l].view(i16),
+                                                        KVall[t, 1, l].view(i16), out[l].view(i16)))]
+            else:
+                calls = [("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16),
+                                                             KVall[t, 1, l].view(i16), 1)),
+                         ("select", lambda: N.nosa_select(ctx, l, Qall[t, l].view(i16))),
+                         ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16))),
+                         ("gather", lambda: N.nosa_fetch(ctx, l))]
             for name, fn in calls:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -324,7 +334,8 @@ def run_native(args, rank, world, local_rank):
             torch.cuda.synchronize()
             for name, a, b in pairs:
                 ev[name].append(a.elapsed_time(b) * 1e3)
-    st2 = N.nosa_get_stats(ctx)
+        if it % 2:
+            fetched_split += N.nosa_get_stats(ctx).blocks_fetched - s0
     us = {k: statistics.mean(v) for k, v in ev.items()}
     n_sel = np.zeros(U, np.int32)
     N.nosa_export_state(ctx, 0, n_sel=n_sel)
@@ -335,19 +346,25 @@ def run_native(args, rank, world, local_rank):
     nc = (T_now - 32) // 16 + 1
     nb = (T_now + 63) // 64
     select_bytes = U * (nc * d * 2 + nb * 4 + G * d * 2)
-    fetch_bytes_launch = st2.blocks_fetched / max(n_time_leg * L, 1) * BLOCK_BYTES
+    fetch_bytes_launch = fetched_split / max(n_time_leg // 2 * L, 1) * BLOCK_BYTES
     hbm, src = measured_peaks()
     h2d = h2d_peak(torch)
-    hbm_kernels = {"attend": attend_bytes, "select": select_bytes}
-    dominant = max(hbm_kernels, key=lambda k: us[k])
-    ach = hbm_kernels[dominant] / (us[dominant] * 1e-6) / 1e9
+    peak_src = f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"
+    if step_kernels == 1:
+        dominant, dom_bytes = "decode", attend_bytes + select_bytes
+        note = ("fused decode kernel (append + score + select + fetch + attend); bytes = compressed keys, "
+                "pooled scores and q read by the scorer plus K+V of every selected token read by the attention "
+                "and its output; the newly selected blocks among them arrive over the host link inside the kernel")
+    else:
+        hbm_kernels = {"attend": attend_bytes, "select": select_bytes}
+        dominant = max(hbm_kernels, key=lambda k: us[k])
+        dom_bytes = hbm_kernels[dominant]
+        note = ("attend bytes = K+V of every selected token; the newly selected blocks among them arrive over "
+                "the host link inside the same kernel")
+    ach = dom_bytes / (us[dominant] * 1e-6) / 1e9
     result["roofline"] = {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
-                          "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
-                          "unit": "GB/s", "frac": ach / hbm, "traffic": None,
-                          "algorithmic_bytes_per_launch": hbm_kernels[dominant],
-                          "avg_launch_us": us[dominant],
-                          "note": "attend bytes = K+V of every selected token; the newly selected blocks among "
-                                  "them arrive over the host link inside the same kernel"}
+                          "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                          "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": us[dominant], "note": note}
     fach = fetch_bytes_launch / (us["gather"] * 1e-6) / 1e9
     result["fetch_roofline"] = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach,
                                 "peak": h2d, "unit": "GB/s", "frac": fach / h2d,
@@ -356,7 +373,8 @@ def run_native(args, rank, world, local_rank):
                                 "note": "standalone nosa_fetch on the step's fetch list; the timed step fetches "
                                         "inside attend instead"}
     result["stages_us_per_layer"] = us
-    result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / ((us["attend"] + us["select"]) * 1e-6) / 1e9 / hbm
+    sel_att_us = us["decode"] if step_kernels == 1 else us["attend"] + us["select"]
+    result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / (sel_att_us * 1e-6) / 1e9 / hbm
 
     # ---------------- e2e: the public host-pointer API (nosa_step_host), copies inside the timed region.
     # Two CUDA graphs, each capturing the 28 layers' nosa_step_host calls on its own set of pinned

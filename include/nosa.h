@@ -78,6 +78,12 @@ typedef enum {
  *                        it and NOSA_ERR_BOUNDS is latched. */
 #define NOSA_F_TEST_ZERO_WAIT 1u
 #define NOSA_F_TEST_BAD_SLOT 2u
+/* NOSA_F_UNFUSED_STEP: nosa_step launches three kernels (append, select, attend
+ * with the fetch inside) instead of the fused one-kernel decode step.  Same
+ * selections; the attention's split-K partition differs, so outputs may differ
+ * in the last bits.  The fused kernel is also skipped when the device cannot
+ * schedule its thread-block clusters. */
+#define NOSA_F_UNFUSED_STEP 4u
 
 typedef struct {
   uint32_t struct_size;   /* sizeof(nosa_config) */
@@ -204,6 +210,11 @@ nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_
  * when out is written. */
 nosa_status nosa_step_host(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, uint16_t* out);
+
+/* How nosa_step runs on this context: *kernels_per_layer = 1 (the fused decode
+ * kernel, one thread-block cluster of *cluster_size CTAs per unit) or 3 (append,
+ * select and attend kernels; *cluster_size = 0).  Either pointer may be NULL. */
+nosa_status nosa_step_plan(nosa_ctx* ctx, int32_t* kernels_per_layer, int32_t* cluster_size);
 
 /* Wait for the stream; report and latch any device-side error. */
 nosa_status nosa_sync(nosa_ctx* ctx);

@@ -148,6 +148,13 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.test_bad_slot = (c->cfg.flags & NOSA_F_TEST_BAD_SLOT) ? 1 : 0;
   return s;
 }
+
+LayerState decode_state(nosa_ctx* c, int layer) {
+  LayerState s = layer_state(c, layer);
+  s.score_chunks = c->dec_cs;
+  s.score_wpc = c->dec_wpc;
+  return s;
+}
 }  // namespace nosa
 
 extern "C" {
@@ -180,7 +187,7 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->max_context < 1 || c->max_context > 262144) return NOSA_ERR_INVALID_ARG;
   if (c->evict_hidden < 32 || c->evict_hidden > 256 || c->evict_hidden % 32) return NOSA_ERR_INVALID_ARG;
   if (c->gather_ctas < 0 || c->gather_ctas > 4096) return NOSA_ERR_INVALID_ARG;
-  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT)))
+  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT | NOSA_F_UNFUSED_STEP)))
     return NOSA_ERR_INVALID_ARG;
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
@@ -282,7 +289,38 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     }
   }
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
-  c->stage_tok_cap = 512;
+  // Fused decode kernel: one cluster of dec_cs CTAs per unit, each CTA dec_teams attention
+  // workers of four warps.  It pays off while all units' clusters are resident at once (the
+  // small batches where the step is latency bound): the largest cluster of 8, 4 or 2 CTAs for
+  // which that holds is taken, else the step runs as three kernels, as it does when the cache
+  // has more slots than a CTA has threads.  NOSA_FUSED=0 turns it off; NOSA_DECODE_CLUSTER,
+  // NOSA_DECODE_TEAMS and NOSA_DECODE_STAGES override the choices.
+  c->dec_cs = 0;
+  c->dec_teams = 2;
+  c->dec_nst = 3;
+  if (const char* e = getenv("NOSA_DECODE_TEAMS")) c->dec_teams = atoi(e) == 1 ? 1 : 2;
+  if (const char* e = getenv("NOSA_DECODE_STAGES")) c->dec_nst = std::min(std::max(atoi(e), 2), 6);
+  const char* fused_env = getenv("NOSA_FUSED");
+  if (!(cfg->flags & NOSA_F_UNFUSED_STEP) && (!fused_env || atoi(fused_env) != 0) &&
+      d.cap <= 128 * c->dec_teams) {
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    std::vector<int> sizes = {8, 4, 2};
+    const char* force = getenv("NOSA_DECODE_CLUSTER");
+    if (force) sizes = {std::min(std::max(atoi(force), 1), 8)};
+    const int warps = 4 * c->dec_teams;
+    for (int cs : sizes) {
+      c->dec_cs = cs;
+      c->dec_wpc = cdiv(cdiv(nc, cs), 16 * warps) * 16 * warps;
+      const LayerState sd = decode_state(c, 0);
+      const bool ok = decode_smem_bytes(sd, c->dec_teams, c->dec_nst) + 24 * 1024 <= (size_t)optin &&
+                      init_decode(sd, c->dec_teams, c->dec_nst) == cudaSuccess;
+      const int active = ok ? decode_active_clusters(sd, c->dec_teams, c->dec_nst, cs) : 0;
+      (void)cudaGetLastError();
+      if (active >= 1 && (force || active >= c->U)) break;
+      c->dec_cs = 0;
+    }
+  }
 
   // pinned, mapped host store
   const size_t host_bytes = c->sz.host_store_bytes;
@@ -510,10 +548,15 @@ nosa_status nosa_step(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t*
   if (st != NOSA_OK) return st;
   if (!q || !k_new || !v_new || !out) return NOSA_ERR_INVALID_ARG;
   if (c->T_host[layer] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
-  const LayerState s = layer_state(c, layer);
-  CK(launch_append_one(s, k_new, v_new, true, c->stream));
-  CK(launch_score_select(s, q, true, c->stream));
-  CK(launch_attend(s, &c->tmap_cache, q, out, 1, true, c->stream));  // the fetch runs inside attend
+  if (c->dec_cs > 0) {  // one fused kernel
+    CK(launch_decode(decode_state(c, layer), &c->tmap_cache, q, k_new, v_new, out, c->dec_teams, c->dec_nst, true,
+                     c->stream));
+  } else {
+    const LayerState s = layer_state(c, layer);
+    CK(launch_append_one(s, k_new, v_new, true, c->stream));
+    CK(launch_score_select(s, q, true, c->stream));
+    CK(launch_attend(s, &c->tmap_cache, q, out, 1, true, c->stream));  // the fetch runs inside attend
+  }
   c->T_host[layer] += 1;
   c->sel_T[layer] = c->T_host[layer];
   return NOSA_OK;
@@ -549,6 +592,13 @@ nosa_status nosa_step_host(nosa_ctx* c, int layer, const uint16_t* q, const uint
   st = nosa_step(c, layer, c->stage_q, c->stage_k, c->stage_v, c->stage_out);
   if (st != NOSA_OK) return st;
   CK(cudaMemcpyAsync(out, c->stage_out, qbytes, cudaMemcpyDeviceToHost, c->stream));
+  return NOSA_OK;
+}
+
+nosa_status nosa_step_plan(nosa_ctx* c, int32_t* kernels_per_layer, int32_t* cluster_size) {
+  if (!c) return NOSA_ERR_INVALID_ARG;
+  if (kernels_per_layer) *kernels_per_layer = c->dec_cs > 0 ? 1 : 3;
+  if (cluster_size) *cluster_size = c->dec_cs;
   return NOSA_OK;
 }
 

@@ -5,155 +5,35 @@
 // compressed key K~_i = bf16(mean of 32 keys) (NOSA-1B blog, key compressor:
 // kernel 32, stride 16) and the window mean of s^e, max-pooled onto the
 // 64-token blocks the window overlaps (explainer eq. 5-6).
-#include "nosa_internal.cuh"
-#include "ptx.cuh"
+#include "append_core.cuh"
 
 namespace nosa {
 
 // ---------------------------------------------------------------- one token per unit
-// grid: U CTAs (one per unit), 256 threads.  The eviction-head matvec splits the
-// 128 input dims in two halves per hidden unit so that each thread issues its 64
-// W1 loads back to back (one memory round trip rather than a dependent chain).
+// grid: U CTAs (one per unit), 256 threads.
 constexpr int kAppendThreads = 256;
 
 __global__ void __launch_bounds__(kAppendThreads) append_one_kernel(LayerState s, const uint16_t* __restrict__ knew,
                                                                     const uint16_t* __restrict__ vnew) {
-  __shared__ float vf[kHeadDim];
-  __shared__ float half_acc[2][kHeadDim];
-  __shared__ float red[4];
   const int u = blockIdx.x, tid = threadIdx.x;
-  // Nothing here reads the previous kernel's results (that is the previous
-  // layer's attention): let the selector launch now, and wait for the previous
-  // kernel only before exiting, so that completions stay ordered.
-  pdl_launch_dependents();
+  // k_new and v_new may come from the previous kernel: wait before reading them
+  pdl_wait();
+  pdl_launch_dependents();  // the selector may start its own prologue
   const int p = *s.T;  // position of the new token (all CTAs read it before any ticket)
   if (p >= s.T_max) {
     if (tid == 0 && u == 0) atomicOr(s.err, kErrCapacity);
-    pdl_wait();
     return;  // every CTA sees the same p: nobody takes a ticket, T is unchanged
   }
-  const int blk = p / kBlock, row = p % kBlock;
-  const int T = p + 1;
-  const bool window_done = T >= kCmpKernel && (T - kCmpKernel) % kCmpStride == 0;
-  const int wi = window_done ? (T - kCmpKernel) / kCmpStride : 0;  // window [16wi, 16wi+32) completes now
-  const uint16_t* krow = knew + (size_t)u * kHeadDim;
-  const uint16_t* vrow = vnew + (size_t)u * kHeadDim;
-  const int g = u % s.Hkv;
-  const float* W1 = s.W1 + (size_t)g * kHeadDim * s.h;
-  const float* W2 = s.W2 + (size_t)g * s.h;
-  const int mi = tid & (kHeadDim - 1), hf = tid >> 7;
-
-  // ---- every load the step needs, issued together (one memory round trip)
-  uint4 rowv = make_uint4(0, 0, 0, 0);
-  int slot = -1;
-  if (tid < 32) {
-    rowv = *reinterpret_cast<const uint4*>(((tid >> 4) ? vrow : krow) + (tid & 15) * 8);
-    slot = s.blk2slot[(size_t)u * s.nb_max + blk];
-  }
-  uint16_t kb = 0, vb = 0;
-  float w2 = 0.f;
-  if (tid < kHeadDim) {
-    kb = krow[tid];
-    vb = vrow[tid];
-    w2 = W2[mi];
-  }
-  float w[64];
-  {
-    const float* wp = W1 + (size_t)(hf * 64) * s.h + mi;
-#pragma unroll
-    for (int c = 0; c < 64; ++c) w[c] = wp[(size_t)c * s.h];
-  }
-  uint16_t ring[kCmpKernel - 1];
-  float se_prev = 0.f, sb1 = 0.f, sb2 = 0.f;
-  if (window_done) {
-    if (tid < kHeadDim) {
-      const uint16_t* rp = s.kring + (size_t)u * 32 * kHeadDim + tid;
-#pragma unroll
-      for (int r = 0; r < kCmpKernel - 1; ++r) ring[r] = rp[((p - (kCmpKernel - 1) + r) & 31) * kHeadDim];
-    }
-    if (tid < kCmpKernel - 1) se_prev = s.se_tok[(size_t)u * s.T_max + p - (kCmpKernel - 1) + tid];
-    if (tid == 0) {
-      const float* sb = s.se_blk + (size_t)u * s.nb_max;
-      sb1 = sb[(kCmpStride * wi) / kBlock];
-      sb2 = sb[(kCmpStride * wi + kCmpKernel - 1) / kBlock];
-    }
-  }
-
-  // ---- stores of the new token: host store (UVA), resident cache slot, key ring
-  if (tid < 32) {
-    const int half = tid >> 4, c8 = (tid & 15) * 8;
-    const size_t hoff = (((size_t)u * s.nb_max + blk) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
-    *reinterpret_cast<uint4*>(s.host_kv + hoff) = rowv;  // store through the UVA alias of pinned memory
-    if (slot >= s.cap) {
-      atomicOr(s.err, kErrBounds);
-    } else if (slot >= 0) {
-      const size_t coff = (((size_t)u * s.cap + slot) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
-      *reinterpret_cast<uint4*>(s.cache + coff) = rowv;
-    }
-  }
-  if (tid < kHeadDim) {
-    s.kring[((size_t)u * 32 + (p & 31)) * kHeadDim + tid] = kb;
-    vf[tid] = bf16_to_float(vb);
-  }
-  __syncthreads();
-
-  // ---- eviction head: s^e = sum_m W2[m] softplus(sum_c v[c] W1[c][m]); two halves of c per m
-  float part = 0.f;
-  for (int m0 = 0; m0 < s.h; m0 += kHeadDim) {
-    if (m0 > 0) {  // hidden sizes above 128: further column blocks
-      const float* wp = W1 + (size_t)(hf * 64) * s.h + m0 + mi;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) w[c] = wp[(size_t)c * s.h];
-      if (tid < kHeadDim) w2 = W2[m0 + mi];
-    }
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 64; ++c) acc = fmaf(vf[hf * 64 + c], w[c], acc);
-    half_acc[hf][mi] = acc;
-    __syncthreads();
-    if (tid < kHeadDim) part = fmaf(softplus(half_acc[0][mi] + half_acc[1][mi]), w2, part);
-    __syncthreads();
-  }
-  if (tid < kHeadDim) {
-    part = warp_sum(part);
-    if ((tid & 31) == 0) red[tid >> 5] = part;
-  }
-  __syncthreads();
-  const float se = (red[0] + red[1]) + (red[2] + red[3]);
-  if (tid == 0) s.se_tok[(size_t)u * s.T_max + p] = se;
-
-  // ---- a completed window: compressed key (exact mean in float64) and pooled eviction score
-  if (window_done) {
-    if (tid < kHeadDim) {
-      double acc = bf16_to_double(kb);
-#pragma unroll
-      for (int r = 0; r < kCmpKernel - 1; ++r) acc += bf16_to_double(ring[r]);
-      s.kt[((size_t)u * s.nc_max + wi) * kHeadDim + tid] = double_to_bf16_rne(acc / kCmpKernel);
-    }
-    if (tid < 32) {
-      double e = (double)(tid < kCmpKernel - 1 ? se_prev : se);
-      e = warp_sum(e);
-      if (tid == 0) {
-        const float mean = (float)(e / kCmpKernel);
-        s.se_win[(size_t)u * s.nc_max + wi] = mean;
-        const int b1 = (kCmpStride * wi) / kBlock, b2 = (kCmpStride * wi + kCmpKernel - 1) / kBlock;
-        float* sb = s.se_blk + (size_t)u * s.nb_max;
-        sb[b1] = fmaxf(sb1, mean);
-        if (b2 != b1) sb[b2] = fmaxf(sb2, mean);
-      }
-    }
-  }
+  append_token<kAppendThreads>(s, u, p, knew, vnew, true);
   // the last CTA to finish advances the layer's context length
-  __syncthreads();
   if (tid == 0) {
     unsigned int* tk = s.tickets + 3 * s.U;
     const unsigned int t = atomicAdd(tk, 1u);
     if (t == gridDim.x - 1) {
       *tk = 0;
-      *s.T = T;
+      *s.T = p + 1;
     }
   }
-  pdl_wait();
 }
 
 // ---------------------------------------------------------------- bulk context load

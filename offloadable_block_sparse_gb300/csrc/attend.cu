@@ -2,37 +2,23 @@
 // eq. 8: attention of q over K[selected], V[selected]; NOSA-1B blog,
 // sparse_forward: attention over the top-k block indices only).
 //
-// grid (attend_chunks, U), 128 threads.  CTA (chunk, u) owns every
-// attend_chunks-th entry of unit u's selection (blocks still on the host first).  One elected
-// thread streams each 32 KiB block (K and V, two 16 KiB boxes with the 128-byte
-// swizzle) from the block cache into a 3-stage shared-memory ring with TMA
-// (cp.async.bulk.tensor) and an mbarrier per stage.  Warp w handles tokens
-// [16w, 16w+16) of every block on the tensor cores (mma.sync m16n8k16, bf16 in,
-// fp32 accumulate):
-//   S^T (16 tokens x 8 heads) = K (ldmatrix) . q^T           (8 MMAs)
-//   online softmax per head in registers (exp2, warp shuffles)
-//   P^T fragments by movmatrix.trans of the bf16-packed S^T fragments
-//   O^T (128 dims x 8 heads) += V^T (ldmatrix.trans) . P^T   (8 MMAs)
-// The four warps' (m, l, O) are merged in shared memory into one partial per
-// CTA; the last CTA of the unit (atomic ticket) merges the partials and writes
-// the bf16 output.
+// grid (attend_chunks, U), 128 threads: one worker of the shared core (a team
+// of four warps, TMA ring over the block cache, host blocks by cp.async) per
+// CTA.  CTA (chunk, u) owns every attend_chunks-th entry of unit u's selection
+// (blocks still on the host first).  The four warps' (m, l, O) are merged in
+// shared memory into one partial per CTA; the unit's partials are then merged
+// through the cluster's distributed shared memory, by a merge kernel, or by the
+// last CTA of the unit (atomic ticket), which writes the bf16 output.
 #include <cooperative_groups.h>
 
-#include "nosa_internal.cuh"
-#include "ptx.cuh"
+#include "attend_core.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace nosa {
 
-constexpr int kStageBytes = kBlockBytes;            // 32 KiB: [d half][K,V][64 tokens][64 dims]
 static_assert(4 * kMaxGroup * kHeadDim * 4 <= 3 * kStageBytes, "warp partials alias the stages");
 constexpr int kDeepStages = 6;  // when a unit's CTAs get an SM each
-constexpr long long kWaitLimit = kWaitCycles;  // bound of the drain waits after a timeout
-
-__device__ __forceinline__ uint32_t swz(uint32_t stage, int dhalf, int kv, int token, int chunk) {
-  return stage + dhalf * 16384 + kv * 8192 + token * 128 + (((chunk ^ (token & 7)) & 7) << 4);
-}
 
 // How a unit's split-K partials are merged:
 //   kMerge == kMergeTicket : through global scratch; the last CTA of the unit (atomic ticket) merges;
@@ -48,25 +34,16 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   __shared__ __align__(8) uint64_t bars[kStages];
   __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
   __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta], s_new[kMaxBlocksPerCta];
-  __shared__ int last, bad_any;
+  __shared__ int last;
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
   float* wo = reinterpret_cast<float*>(smem);
 
   const int chunk = blockIdx.x, u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gr = lane >> 2, t4 = lane & 3;
   const int G = s.G;
   // independent loads first: q fragments, the context length, the unit's selection size
-  // q^T as the B operand: b0 = q[head gr][16ks + 2t4 .. +1], b1 = the same +8
   uint32_t qb[8][2];
-  {
-    const uint16_t* qh = q + ((size_t)u * G + min(gr, G - 1)) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qb[ks][0] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4) : 0u;
-      qb[ks][1] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4 + 8) : 0u;
-    }
-  }
+  load_q_frags(qb, q, u, G, lane);
   const Geometry geo = geometry(*s.T, s.nw, s.sink);  // written two kernels back (append)
   pdl_wait();               // the selection (previous kernel) is needed from here
   pdl_launch_dependents();  // the next layer's append may start
@@ -123,193 +100,19 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
     prefetch_tmap(&tmap);
     for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
-    bad_any = 0;
   }
   __syncthreads();
 
-  // Pipeline.  Blocks without a cache slot (first in this CTA's list) are copied
-  // straight from the pinned host store by cp.async of all threads into
-  // dedicated stages right away (rows past the context zero-filled) and consumed
-  // last, so the host-link latency overlaps the cached blocks.  Cached blocks
-  // stream through the remaining stages as a ring, each loaded by one TMA
-  // (thread 0) completing on the stage's mbarrier.  Host blocks beyond the
-  // dedicated stages (rare) pass through the ring as well.
-  int nnew = 0;
-  while (nnew < nblk && s_new[nnew]) ++nnew;
-  const int ded = min(nnew, kStages - 1);  // dedicated stages 0 .. ded-1
-  const int ring = kStages - ded;          // ring stages ded .. kStages-1
-  const int nr = nblk - ded;               // ring entries: local entries ded .. nblk-1
-  auto host_copy = [&](int e, int st) {    // all threads
-    const int rows = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
-    const uint16_t* src = s.host_kv + ((size_t)u * s.nb_max + s_blk[e]) * 2 * kBlockElems;
-#pragma unroll 4
-    for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
-      const int idx = tid + j * kAttendThreads;  // 16-byte chunk: K|V, row, chunk of the 256-byte row
-      const int kv = idx >> 10, r = (idx >> 4) & 63, cc = idx & 15;
-      cp_async_16(swz(sbase + st * kStageBytes, cc >> 3, kv, r, cc & 7),
-                  src + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8, r < rows ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
-  auto issue_ring = [&](int p) {  // ring entry p into stage ded + p % ring
-    if (p >= nr) return;
-    const int st = ded + p % ring, e = ded + p;
-    if (s_new[e]) {
-      if (tid == 0) mbar_arrive(&bars[st]);
-      host_copy(e, st);
-    } else if (tid == 0) {
-      const int flat = (s.unit_base + u) * s.cap + s_slot[e];
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[st], kStageBytes);
-      tma_load_4d(sbase + st * kStageBytes, &tmap, 0, 0, 0, flat, &bars[st]);
-      tma_load_4d(sbase + st * kStageBytes + 16384, &tmap, 64, 0, 0, flat, &bars[st]);
-    }
-  };
-  for (int d = 0; d < ded; ++d) host_copy(d, d);
-  for (int p = 0; p < ring; ++p) issue_ring(p);
-  int issued = ring;
+  WarpAcc A;
+  A.init();
+  attend_worker(&tmap, s, geo, u, qb, s_blk, s_slot, s_new, nblk, sbase, bars, kStages, Team{0}, tid, A);
+  __syncthreads();  // every copy has landed (or was drained): the stages can hold the warp partials
 
-  const float sl2 = s.scale * 1.4426950408889634f;  // softmax in base 2
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[8][4];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-  const int tok0 = warp * 16;
-  // ldmatrix row addresses of this lane (token, 16-byte chunk) before swizzling
-  const int tk_k = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);  // K: matrices (rows 0-7|8-15) x (k lo|hi)
-  const int ch_k = lane >> 4;
-  const int tk_v = tok0 + (lane & 7) + ((lane >> 4) << 3);        // V^T: (d lo|hi) x (tokens 0-7|8-15)
-  const int ch_v = (lane >> 3) & 1;
-
-  // one 64-token block in stage memory stg: warp's 16 tokens, online softmax, PV; fetched
-  // blocks are also written to their cache slot for later steps
-  auto process = [&](uint32_t stg, int e) {
-    const int valid = (s_blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
-    if (tok0 < valid) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int dch = 2 * ks + ch_k;
-        uint32_t a[4];
-        ldsm_x4(a, swz(stg, dch >> 3, 0, tk_k, dch & 7));
-        mma_16816(acc, a, qb[ks][0], qb[ks][1]);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j] *= sl2;
-      if (tok0 + gr >= valid) acc[0] = acc[1] = -INFINITY;
-      if (tok0 + gr + 8 >= valid) acc[2] = acc[3] = -INFINITY;
-      float mx0 = fmaxf(acc[0], acc[2]), mx1 = fmaxf(acc[1], acc[3]);
-#pragma unroll
-      for (int o2 = 4; o2 < 32; o2 <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: token tok0 is valid
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-      const float p0 = exp2f(acc[0] - mn0), p1 = exp2f(acc[1] - mn1);
-      const float p2 = exp2f(acc[2] - mn0), p3 = exp2f(acc[3] - mn1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
-      }
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0-7 of the tile
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8-15
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int dch = 2 * mt + ch_v;
-        uint32_t a[4];
-        ldsm_x4_trans(a, swz(stg, dch >> 3, 1, tk_v, dch & 7));
-        mma_16816(o[mt], a, pb0, pb1);
-      }
-    }
-    if (s_new[e]) {
-      uint16_t* dst = s.cache + ((size_t)u * s.cap + s_slot[e]) * 2 * kBlockElems;
-#pragma unroll 4
-      for (int j = 0; j < kStageBytes / 16 / kAttendThreads; ++j) {
-        const int idx = tid + j * kAttendThreads;
-        const int kv = idx >> 10, r = (idx >> 4) & 63, cc = idx & 15;
-        uint4 v;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
-                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                     : "r"(swz(stg, cc >> 3, kv, r, cc & 7)));
-        *reinterpret_cast<uint4*>(dst + (size_t)kv * kBlockElems + r * kHeadDim + cc * 8) = v;
-      }
-    }
-  };
-
-  int consumed = 0;
-  for (int p = 0; p < nr; ++p) {
-    const int st = ded + p % ring, e = ded + p;
-    // a negative limit (a test hook) gives up without waiting, so the timeout path runs every time
-    const bool okw = s.wait_limit >= 0 && mbar_wait_bounded(&bars[st], (uint32_t)((p / ring) & 1), s.wait_limit);
-    if (s_new[e]) cp_async_wait_all();  // a host block that passed through the ring
-    if (__syncthreads_or(!okw)) {
-      if (tid == 0) atomicOr(s.err, kErrTimeout);
-      bad_any = 1;
-      break;
-    }
-    consumed = p + 1;
-    process(sbase + st * kStageBytes, e);
-    __syncthreads();  // every warp is done with this stage
-    issue_ring(issued);
-    ++issued;
-  }
-  cp_async_wait_all();
-  __syncthreads();  // the dedicated host blocks have landed
-  if (!bad_any)
-    for (int d = 0; d < ded; ++d) process(sbase + d * kStageBytes, d);
-  if (bad_any && tid == 0) {  // drain copies still in flight before the shared memory is reused
-    for (int p = consumed; p < min(issued, nr); ++p)
-      mbar_wait_bounded(&bars[ded + p % ring], (uint32_t)((p / ring) & 1), kWaitLimit);
-  }
-  __syncthreads();
-  // warp partials -> shared memory
-#pragma unroll
-  for (int o2 = 4; o2 < 32; o2 <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
-  }
-  if (gr == 0) {
-    wm[warp][2 * t4] = m0;
-    wm[warp][2 * t4 + 1] = m1;
-    wl[warp][2 * t4] = l0;
-    wl[warp][2 * t4 + 1] = l1;
-  }
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    float* w0 = wo + ((warp * kMaxGroup + 2 * t4) * kHeadDim);
-    float* w1 = wo + ((warp * kMaxGroup + 2 * t4 + 1) * kHeadDim);
-    w0[16 * mt + gr] = o[mt][0];
-    w1[16 * mt + gr] = o[mt][1];
-    w0[16 * mt + gr + 8] = o[mt][2];
-    w1[16 * mt + gr + 8] = o[mt][3];
-  }
-  __syncthreads();
   // CTA partial (base-2 max, sum, unnormalised output) for each head
-  const int x = tid;  // head dimension
   __shared__ float cp_m[kMaxGroup], cp_l[kMaxGroup], cp_o[kMaxGroup][kHeadDim];
   float* part0 = s.apart + ((size_t)u * s.attend_chunks + chunk) * kMaxGroup * kPartStride;
-  for (int h = 0; h < G; ++h) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w][h]);
-    float L = 0.f, O = 0.f;
-    if (M > -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float f = exp2f(wm[w][h] - M);
-        L += wl[w][h] * f;
-        O += wo[(w * kMaxGroup + h) * kHeadDim + x] * f;
-      }
-    }
+  cta_partial<4>(A, wm, wl, wo, G, [&](int h, float M, float L, float O) {
+    const int x = tid;
     if constexpr (kMerge == kMergeCluster) {
       if (x == 0) {
         cp_m[h] = M;
@@ -324,7 +127,8 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
       }
       part[2 + x] = O;
     }
-  }
+  });
+  const int x = tid;  // head dimension
   if constexpr (kMerge == kMergeKernel) return;
   if constexpr (kMerge == kMergeCluster) {
     // every CTA of the unit merges the heads h = rank, rank + CS, ... from all CTAs' partials

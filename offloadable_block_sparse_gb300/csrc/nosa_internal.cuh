@@ -141,6 +141,9 @@ struct nosa_ctx {
   float *sq_blk, *apart;
   unsigned int* tickets;
   int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_mode, attend_deep, gather_ctas;
+  // fused decode kernel (nosa_step): cluster size (0: off, three kernels instead), windows per
+  // scoring CTA, attention stages per team
+  int dec_cs, dec_wpc, dec_nst, dec_teams;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   size_t stage_tok_cap;   // tokens per unit the bulk staging buffers hold
@@ -204,4 +207,13 @@ cudaError_t init_append(const LayerState& s);
 cudaError_t init_score_select(const LayerState& s);
 cudaError_t init_attend();
 int attend_max_cluster(bool deep);
+// fused decode step of one layer (append + select + fetch + attend); s carries the fused
+// kernel's cluster size and windows per CTA in score_chunks / score_wpc
+LayerState decode_state(nosa_ctx* c, int layer);
+// teams: attention workers (four warps each) per CTA, 1 or 2; nst: stages per worker
+size_t decode_smem_bytes(const LayerState& s, int teams, int nst);
+cudaError_t init_decode(const LayerState& s, int teams, int nst);
+int decode_active_clusters(const LayerState& s, int teams, int nst, int cs);
+cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, uint16_t* out, int teams, int nst, bool pdl, cudaStream_t st);
 }  // namespace nosa

@@ -20,13 +20,14 @@ STATUS_NAMES = ["NOSA_OK", "NOSA_ERR_INVALID_ARG", "NOSA_ERR_OOM", "NOSA_ERR_HOS
 globals().update({n: i for i, n in enumerate(STATUS_NAMES)})
 NOSA_F_TEST_ZERO_WAIT = 1
 NOSA_F_TEST_BAD_SLOT = 2
+NOSA_F_UNFUSED_STEP = 4
 
 # every entry point declared in include/nosa.h
 EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_destroy", "nosa_set_stream",
            "nosa_set_eviction_head", "nosa_append_kv", "nosa_select", "nosa_fetch", "nosa_attend", "nosa_step",
            "nosa_step_host", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
            "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string",
-           "nosa_attend_noalloc"]
+           "nosa_attend_noalloc", "nosa_step_plan"]
 
 
 class nosa_config(ctypes.Structure):
@@ -88,6 +89,7 @@ def lib() -> ctypes.CDLL:
             "nosa_step": [vp, i32, p, p, p, p],
             "nosa_step_host": [vp, i32, p, p, p, p],
             "nosa_sync": [vp],
+            "nosa_step_plan": [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
             "nosa_reset_state": [vp],
             "nosa_context_length": [vp, i32, ctypes.POINTER(ctypes.c_int32)],
             "nosa_get_stats": [vp, ctypes.POINTER(nosa_stats)],
@@ -193,6 +195,13 @@ def nosa_step(ctx, layer, q, k_new, v_new, out) -> None:
 
 def nosa_step_host(ctx, layer, q, k_new, v_new, out) -> None:
     _check(lib().nosa_step_host(ctx, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)), "nosa_step_host")
+
+
+def nosa_step_plan(ctx):
+    """(kernels per layer of nosa_step: 1 fused or 3, cluster size of the fused kernel or 0)."""
+    k, c = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().nosa_step_plan(ctx, ctypes.byref(k), ctypes.byref(c)), "nosa_step_plan")
+    return k.value, c.value
 
 
 def nosa_sync(ctx) -> int:

@@ -19,8 +19,12 @@ from tests.nosa_harness import Parity  # noqa: E402
 from offloadable_block_sparse_gb300 import nosa as N  # noqa: E402
 
 
-def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0, separate_fetch=True):
-    p = Parity(wl, sample_units=samples, layers=layers, gather_ctas=gather_ctas)
+FUSED, UNFUSED = 0, N.NOSA_F_UNFUSED_STEP
+STEP_MODES = pytest.mark.parametrize("mode", [FUSED, UNFUSED], ids=["fused", "three-kernels"])
+
+
+def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0, separate_fetch=True, flags=0):
+    p = Parity(wl, sample_units=samples, layers=layers, gather_ctas=gather_ctas, flags=flags)
     try:
         p.load_context()
         for _ in range(steps):
@@ -38,9 +42,10 @@ def _report(name, log, stats=None):
           f"max_score_rel={log.max_score_rel:.2e} gamma_min={min(log.gammas) if log.gammas else None}")
 
 
-def test_tiny_every_step_every_unit():
+@STEP_MODES
+def test_tiny_every_step_every_unit(mode):
     wl = syn.workload("tiny")
-    log, stats = run(wl, wl.steps)
+    log, stats = run(wl, wl.steps, flags=mode)
     _report("tiny", log, stats)
     assert log.unit_steps == wl.steps * 2
     assert min(log.gammas) >= wl.k_e / (wl.k_q + wl.k_e) - 1e-12   # Theorem 2 on the GPU path
@@ -61,28 +66,31 @@ def test_separate_calls_attend_fetches_itself():
     assert log.unit_steps == 40 * 8
 
 
-def test_ragged_context_group4_small_window():
+@STEP_MODES
+def test_ragged_context_group4_small_window(mode):
     # T_0 not a multiple of 64 or 16: the tail block is partial and is fetched on the first step;
     # 8 q heads over 2 kv heads (G = 4)
     wl = syn.Workload("ragged", layers=2, batch=3, q_heads=8, kv_heads=2, context=1001, k_q=3, k_e=5,
                       window_tokens=128, steps=70, sigma=1.0)
-    log, _ = run(wl, wl.steps)
+    log, _ = run(wl, wl.steps, flags=mode)
     _report("ragged", log)
     assert log.unit_steps == 70 * 12
 
 
-def test_short_context_everything_selected():
+@STEP_MODES
+def test_short_context_everything_selected(mode):
     # fewer blocks than the budget: every block is selected, so attention is dense
     wl = syn.Workload("short", layers=1, batch=2, q_heads=16, kv_heads=2, context=40, k_q=4, k_e=12,
                       window_tokens=256, steps=30)
-    log, _ = run(wl, wl.steps)
+    log, _ = run(wl, wl.steps, flags=mode)
     assert log.unit_steps == 30 * 4
 
 
-def test_no_sink_no_window_query_aware_only():
+@STEP_MODES
+def test_no_sink_no_window_query_aware_only(mode):
     wl = syn.Workload("kq_only", layers=1, batch=2, q_heads=4, kv_heads=1, context=3000, k_q=8, k_e=0,
                       window_tokens=0, sink_blocks=0, steps=20, sigma=1.0)
-    log, _ = run(wl, wl.steps)
+    log, _ = run(wl, wl.steps, flags=mode)
     assert log.unit_steps == 40
 
 
@@ -110,6 +118,17 @@ def test_capacity_error_leaves_state_unchanged():
         assert N.nosa_sync(p.ctx) == N.NOSA_OK
     finally:
         p.close()
+
+
+def test_step_plan_follows_the_flag():
+    wl = syn.workload("tiny")
+    for flags, kernels in ((FUSED, 1), (UNFUSED, 3)):
+        p = Parity(wl, flags=flags)
+        try:
+            k, cs = N.nosa_step_plan(p.ctx)
+            assert k == kernels and (cs > 0) == (kernels == 1)
+        finally:
+            p.close()
 
 
 def test_out_of_order_calls_are_rejected():
@@ -206,6 +225,7 @@ def test_host_pointer_step_matches_device_step():
 # but runs 8 of its 32 layers: its full host store (138 GB pinned) exceeds the test machine's RAM.
 FULL = [
     ("nosa1b_16k_b8", 256, [(0, 0, 0), (5, 3, 1), (17, 7, 0), (27, 6, 1)], None, {}),
+    ("nosa1b_16k_b8", 96, [(2, 1, 0), (26, 4, 1)], None, {"flags": UNFUSED}),
     ("nosa1b_16k_b128", 128, [(0, 0, 0), (13, 77, 1), (27, 127, 0)], None, {}),
     ("nosa1b_16k_b128", 64, [(3, 5, 0), (20, 100, 1)], None, {"sigma": 1.0}),
     ("nosa8b_32k_b32", 128, [(0, 0, 0), (4, 17, 5), (7, 31, 7)], 8, {}),
@@ -218,8 +238,10 @@ FULL = [
                          ids=[f"{n}-{s}steps-{'-'.join(f'{k}{v}' for k, v in o.items()) or 'base'}"
                               for n, s, _, _, o in FULL])
 def test_full_size_sampled(name, steps, samples, layers, over):
+    over = dict(over)
+    flags = over.pop("flags", 0)
     wl = syn.workload(name, **over)
-    log, stats = run(wl, steps, samples=samples, layers=layers)
+    log, stats = run(wl, steps, samples=samples, layers=layers, flags=flags)
     _report(name, log, stats)
     assert log.unit_steps == steps * len(samples)
     assert stats.gamma_min >= wl.k_e / (wl.k_q + wl.k_e) - 1e-6
