@@ -37,7 +37,10 @@ Readings taken where the pages leave a step open (each is listed in the design doc):
     without a slot is fetched (this includes a newly started tail block and, on
     the first step after a bulk context load, every selected block); freed and
     free slots are handed out in ascending order to new blocks in ascending order.
-  * no DMA attention bias in the attention step (eq. 8 prints none).
+  * by default no DMA attention bias in the attention step (eq. 8 prints none);
+    as an option (UnitOracle(dma_bias=True)) each token's eviction score s^e_j
+    is added to its scaled logit q.k_j / sqrt(d), the additive bias of DMA that
+    the eviction head comes from (wiki "How NOSA works").
 
 Parity pins for every function live in tests/test_oracle.py.
 """
@@ -192,13 +195,20 @@ def assign_slots(S, slot_blk):
     return fetch, new_map, [where[b] for b in S]
 
 
-def sparse_attention(Qg, K, V, S, T, scale, block=64):
-    """Eq. 8: softmax attention of each head over the tokens of the selected blocks."""
+def sparse_attention(Qg, K, V, S, T, scale, block=64, bias=None):
+    """Eq. 8: softmax attention of each head over the tokens of the selected blocks.
+
+    bias (one value per token, natural-log units) is the DMA-style additive attention
+    bias (wiki "How NOSA works": the eviction head is adapted from DMA, which adds its
+    per-token score to the attention logits): token j's logit is q.k_j * scale + bias[j].
+    """
     idx = np.concatenate([np.arange(block * b, min(block * (b + 1), T)) for b in S]) if S else np.zeros(0, int)
     Qg = np.asarray(Qg, np.float64)
     Ks = np.asarray(K, np.float64)[idx]
     Vs = np.asarray(V, np.float64)[idx]
     z = (Qg @ Ks.T) * scale
+    if bias is not None:
+        z = z + np.asarray(bias, np.float64)[idx][None, :]
     z = z - z.max(axis=1, keepdims=True)
     p = np.exp(z)
     p = p / p.sum(axis=1, keepdims=True)
@@ -217,12 +227,13 @@ class UnitOracle:
     """State and steps of one (layer, batch, kv-head) unit, computed from its raw inputs."""
 
     def __init__(self, *, head_dim=128, block=64, kernel=32, stride=16, k_q, k_e,
-                 sink_blocks=1, window_tokens, max_context, W1, W2, scale=None):
+                 sink_blocks=1, window_tokens, max_context, W1, W2, scale=None, dma_bias=False):
         self.d, self.block, self.kernel, self.stride = head_dim, block, kernel, stride
         self.k_q, self.k_e, self.sink = k_q, k_e, sink_blocks
         self.nw = window_tokens // block
         self.cap = sink_blocks + self.nw + k_q + k_e
         self.scale = 1.0 / math.sqrt(head_dim) if not scale else scale
+        self.dma_bias = dma_bias  # attention logits get each token's eviction score added
         self.W1 = np.asarray(W1, np.float64)
         self.W2 = np.asarray(W2, np.float64)
         self.K = np.zeros((max_context, head_dim))
@@ -298,7 +309,8 @@ class UnitOracle:
     # -- a6: attention over the selection
     def attend(self, q_bits, S):
         Qg = bf16_bits_to_f64(q_bits).reshape(-1, self.d)
-        return sparse_attention(Qg, self.K[:self.T], self.V[:self.T], S, self.T, self.scale, self.block)
+        bias = self.se_tok[:self.T] if self.dma_bias else None
+        return sparse_attention(Qg, self.K[:self.T], self.V[:self.T], S, self.T, self.scale, self.block, bias)
 
     def step(self, q_bits, k_bits, v_bits):
         """One decode step: append, score, select, diff, attend."""

@@ -291,6 +291,71 @@ def test_sparse_attention_equals_masked_dense():
     assert np.max(np.abs(got - _sdpa(Q, K, V, 0.3, mask))) < 1e-12
 
 
+# DMA-style additive attention bias (wiki "How NOSA works": the eviction head comes from DMA,
+# which adds its per-token score to the attention logits).
+def test_dma_bias_equals_sdpa_with_an_additive_float_mask():
+    rng = np.random.default_rng(11)
+    T, d = 700, 16
+    K, V = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    Q = rng.standard_normal((3, d))
+    bias = rng.standard_normal(T) * 2.0
+    S = [0, 2, 5, 10]
+    mask = np.full(T, -np.inf)
+    for b in S:
+        mask[64 * b: min(64 * b + 64, T)] = bias[64 * b: min(64 * b + 64, T)]
+    got = O.sparse_attention(Q, K, V, S, T, 0.3, bias=bias)
+    assert np.max(np.abs(got - _sdpa(Q, K, V, 0.3, mask))) < 1e-12
+
+
+def test_dma_bias_constant_shift_changes_nothing_and_two_tokens_match_the_closed_form():
+    rng = np.random.default_rng(12)
+    T, d = 130, 8
+    K, V = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    Q = rng.standard_normal((2, d))
+    S = [0, 2]
+    plain = O.sparse_attention(Q, K, V, S, T, 0.5)
+    shifted = O.sparse_attention(Q, K, V, S, T, 0.5, bias=np.full(T, 7.25))
+    assert np.max(np.abs(plain - shifted)) < 1e-12
+    # two tokens (block 2 holds tokens 128, 129 only): softmax of z + b written out
+    q = Q[0]
+    z = np.array([q @ K[128], q @ K[129]]) * 0.5
+    b = np.array([0.7, -1.9])
+    w = np.exp(z + b)
+    want = (w[0] * V[128] + w[1] * V[129]) / w.sum()
+    bias = np.zeros(T)
+    bias[128:130] = b
+    got = O.sparse_attention(Q[:1], K, V, [2], T, 0.5, bias=bias)[0]
+    assert np.max(np.abs(got - want)) < 1e-12
+
+
+def test_unit_dma_bias_is_the_eviction_score_of_each_token():
+    # One hidden unit: s^e_j = -100 * softplus(v_j[0]).  Block 3's tokens get v[0] = 20 (bias about
+    # -2000: masked out), every other token v[0] = -20 (bias about -2e-7: no effect), so with the
+    # bias the output is attention over the selection without block 3; with W2 = 0 it is unbiased.
+    rng = np.random.default_rng(13)
+    T, d = 600, 16
+    K = O.bf16_round(rng.standard_normal((T, d)))
+    V = O.bf16_round(rng.standard_normal((T, d)))
+    V[:, 0] = -20.0
+    V[192:256, 0] = 20.0
+    W1 = np.zeros((d, 1)); W1[0, 0] = 1.0
+    Q = O.f64_to_bf16_bits(rng.standard_normal((2, d)))
+    S = [0, 1, 3, 5, 9]
+
+    def unit(W2, dma):
+        u = O.UnitOracle(head_dim=d, k_q=2, k_e=2, window_tokens=128, max_context=T, W1=W1, W2=W2,
+                         dma_bias=dma)
+        u.append(O.f64_to_bf16_bits(K), O.f64_to_bf16_bits(V))
+        return u.attend(Q, S)
+
+    Qg = O.bf16_bits_to_f64(Q)
+    without3 = O.sparse_attention(Qg, K, V, [0, 1, 5, 9], T, 1 / math.sqrt(d))
+    plain = O.sparse_attention(Qg, K, V, S, T, 1 / math.sqrt(d))
+    assert np.max(np.abs(unit(np.array([-100.0]), True) - without3)) < 1e-5
+    assert np.max(np.abs(unit(np.array([0.0]), True) - plain)) < 1e-12
+    assert np.max(np.abs(unit(np.array([-100.0]), False) - plain)) < 1e-12
+
+
 def test_assign_slots_pairs_ascending():
     fetch, m, where = O.assign_slots([0, 3, 4, 9], [3, -1, 7, 0, 8])
     # slot 2 (block 7) and 4 (block 8) are freed; free slots 1, 2, 4; new blocks 4, 9
