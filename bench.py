@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--gather-ctas", type=int, default=0)
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (only for host-memory limits)")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--dma-bias", action="store_true", help="attention adds each token's eviction score (DMA bias)")
     ap.add_argument("--quick", action="store_true", help="timed graph leg only (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -190,7 +191,8 @@ def run_native(args, rank, world, local_rank):
     total_steps = 1 + W + K + n_time_leg + n_e2e
     cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=wl.context + total_steps,
-                        sink_blocks=wl.sink_blocks, evict_hidden=wl.evict_hidden, gather_ctas=args.gather_ctas)
+                        sink_blocks=wl.sink_blocks, evict_hidden=wl.evict_hidden, gather_ctas=args.gather_ctas,
+                        flags=N.NOSA_F_DMA_BIAS if args.dma_bias else 0)
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     sizes = N.nosa_query_sizes(cfg)
@@ -289,6 +291,7 @@ def run_native(args, rank, world, local_rank):
                          "parallelism": f"replicas x{world} (independent sequences per GPU)",
                          "cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
                          "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster,
+                         "dma_bias": bool(args.dma_bias),
                          "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache "
                                "(L2 is 129 MB)"},
               "gpu_launches": step_kernels * L * K,

@@ -84,6 +84,12 @@ typedef enum {
  * in the last bits.  The fused kernel is also skipped when the device cannot
  * schedule its thread-block clusters. */
 #define NOSA_F_UNFUSED_STEP 4u
+/* NOSA_F_DMA_BIAS: the attention adds each attended token's eviction score s^e_j
+ * to its scaled logit, softmax_j(q.k_j / sqrt(d) + s^e_j): the additive attention
+ * bias of DMA, from which the eviction head is adapted (NOSA wiki, "How NOSA
+ * works"; the NOSA-1B blog names the score CIS).  Off: plain attention (NOSA
+ * explainer eq. 8). */
+#define NOSA_F_DMA_BIAS 8u
 
 typedef struct {
   uint32_t struct_size;   /* sizeof(nosa_config) */

@@ -117,7 +117,8 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.cache = c->cache + lu * d.cap * 2 * kBlockElems;
   s.kt = c->kt + lu * s.nc_max * kHeadDim;
   s.kring = c->kring + lu * 32 * kHeadDim;
-  s.se_tok = c->se_tok + lu * s.T_max;
+  s.se_stride = d.nb_max * kBlock;
+  s.se_tok = c->se_tok + lu * s.se_stride;
   s.se_win = c->se_win + lu * s.nc_max;
   s.se_blk = c->se_blk + lu * d.nb_max;
   s.slot_blk = c->slot_blk + lu * d.cap;
@@ -146,6 +147,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.attend_deep = c->attend_deep;
   s.wait_limit = (c->cfg.flags & NOSA_F_TEST_ZERO_WAIT) ? -1 : kWaitCycles;
   s.test_bad_slot = (c->cfg.flags & NOSA_F_TEST_BAD_SLOT) ? 1 : 0;
+  s.dma_bias = (c->cfg.flags & NOSA_F_DMA_BIAS) ? 1 : 0;
   return s;
 }
 
@@ -187,7 +189,7 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->max_context < 1 || c->max_context > 262144) return NOSA_ERR_INVALID_ARG;
   if (c->evict_hidden < 32 || c->evict_hidden > 256 || c->evict_hidden % 32) return NOSA_ERR_INVALID_ARG;
   if (c->gather_ctas < 0 || c->gather_ctas > 4096) return NOSA_ERR_INVALID_ARG;
-  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT | NOSA_F_UNFUSED_STEP)))
+  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT | NOSA_F_UNFUSED_STEP | NOSA_F_DMA_BIAS)))
     return NOSA_ERR_INVALID_ARG;
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
@@ -211,7 +213,7 @@ nosa_status nosa_query_sizes(const nosa_config* c, nosa_sizes* out) {
   out->evict_words = d.ev_words;
   out->host_store_bytes = L * U * d.nb_max * (uint64_t)kBlockBytes;
   const uint64_t per_unit = (uint64_t)d.cap * kBlockBytes + nc * kHeadDim * 2 + 32 * kHeadDim * 2 +
-                            (uint64_t)c->max_context * 4 + nc * 4 + (uint64_t)d.nb_max * 8 + d.ev_words * 4ull +
+                            (uint64_t)d.nb_max * kBlock * 4 + nc * 4 + (uint64_t)d.nb_max * 8 + d.ev_words * 4ull +
                             (uint64_t)d.cap * 4 * 5 + 4 * 4;
   const int score_chunks = cdiv(nc, kWindowsPerCta);
   const uint64_t scratch = U * d.G * nc * 4 + U * score_chunks * kMaxGroup * 8 + U * d.nb_max * 4 +
@@ -347,7 +349,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   dalloc(&c->cache, LU * d.cap * (size_t)kBlockBytes);
   dalloc(&c->kt, LU * nc * kHeadDim * 2);
   dalloc(&c->kring, LU * 32 * kHeadDim * 2);
-  dalloc(&c->se_tok, LU * (size_t)cfg->max_context * 4);
+  dalloc(&c->se_tok, LU * (size_t)d.nb_max * kBlock * 4);
   dalloc(&c->se_win, LU * nc * 4);
   dalloc(&c->se_blk, LU * d.nb_max * 4);
   dalloc(&c->W1, (size_t)c->L * c->Hkv * kHeadDim * d.h * 4);
@@ -383,7 +385,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   bool ok = cudaMemset(c->cache, 0, LU * d.cap * (size_t)kBlockBytes) == cudaSuccess;
   ok = ok && cudaMemset(c->kt, 0, LU * nc * kHeadDim * 2) == cudaSuccess;
   ok = ok && cudaMemset(c->kring, 0, LU * 32 * kHeadDim * 2) == cudaSuccess;
-  ok = ok && cudaMemset(c->se_tok, 0, LU * (size_t)cfg->max_context * 4) == cudaSuccess;
+  ok = ok && cudaMemset(c->se_tok, 0, LU * (size_t)d.nb_max * kBlock * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->se_win, 0, LU * nc * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->W1, 0, (size_t)c->L * c->Hkv * kHeadDim * d.h * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->W2, 0, (size_t)c->L * c->Hkv * d.h * 4) == cudaSuccess;

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(256) append_bulk_tokens_kernel(LayerState s, c
   part += __shfl_xor_sync(0xffffffffu, part, 1);
   part += __shfl_xor_sync(0xffffffffu, part, 2);
   part += __shfl_xor_sync(0xffffffffu, part, 4);
-  if (sub == 0 && t < ntok) s.se_tok[(size_t)u * s.T_max + T_old + tok0 + t] = part;
+  if (sub == 0 && t < ntok) s.se_tok[(size_t)u * s.se_stride + T_old + tok0 + t] = part;
 }
 
 // B2: per (new window, unit): compressed key and window mean of s^e.  Keys of
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(128) append_bulk_windows_kernel(LayerState s, 
   }
   s.kt[((size_t)u * s.nc_max + i) * kHeadDim + tid] = double_to_bf16_rne(acc / kCmpKernel);
   if (tid < 32) {
-    double e = (double)s.se_tok[(size_t)u * s.T_max + kCmpStride * i + tid];
+    double e = (double)s.se_tok[(size_t)u * s.se_stride + kCmpStride * i + tid];
     e = warp_sum(e);
     if (tid == 0) s.se_win[(size_t)u * s.nc_max + i] = (float)(e / kCmpKernel);
   }

@@ -75,7 +75,7 @@ __device__ __forceinline__ void append_token(const LayerState& s, int u, int p, 
   }
   float se_prev = 0.f, sb1 = 0.f, sb2 = 0.f;
   if (window_done) {
-    if (tid < kCmpKernel - 1) se_prev = s.se_tok[(size_t)u * s.T_max + p - (kCmpKernel - 1) + tid];
+    if (tid < kCmpKernel - 1) se_prev = s.se_tok[(size_t)u * s.se_stride + p - (kCmpKernel - 1) + tid];
     if (tid == 0) {
       const float* sb = s.se_blk + (size_t)u * s.nb_max;
       sb1 = sb[(kCmpStride * wi) / kBlock];
@@ -130,7 +130,7 @@ __device__ __forceinline__ void append_token(const LayerState& s, int u, int p, 
   }
   __syncthreads();
   const float se = (red[0] + red[1]) + (red[2] + red[3]);
-  if (tid == 0) s.se_tok[(size_t)u * s.T_max + p] = se;
+  if (tid == 0) s.se_tok[(size_t)u * s.se_stride + p] = se;
 
   // ---- a completed window: window mean of s^e, pooled onto the blocks it overlaps
   if (window_done && tid < 32) {

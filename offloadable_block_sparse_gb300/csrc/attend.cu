@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
   __shared__ int s_blk[kMaxBlocksPerCta], s_slot[kMaxBlocksPerCta], s_new[kMaxBlocksPerCta];
   __shared__ int last;
+  __shared__ __align__(16) float sebuf[kStages][kBlock];  // per-token eviction scores of the staged blocks
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
   float* wo = reinterpret_cast<float*>(smem);
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
 
   WarpAcc A;
   A.init();
-  attend_worker(&tmap, s, geo, u, qb, s_blk, s_slot, s_new, nblk, sbase, bars, kStages, Team{0}, tid, A);
+  attend_worker(&tmap, s, geo, u, qb, s_blk, s_slot, s_new, nblk, sbase, bars, kStages, &sebuf[0][0], Team{0}, tid, A);
   __syncthreads();  // every copy has landed (or was drained): the stages can hold the warp partials
 
   // CTA partial (base-2 max, sum, unnormalised output) for each head

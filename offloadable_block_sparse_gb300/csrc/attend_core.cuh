@@ -91,12 +91,13 @@ struct WarpAcc {
 
 // Runs one worker over its list (blk, slot, isnew; n entries, blocks without a slot
 // first) with `nst` stages at sbase and their mbarriers `bars` (initialised, count 1).
-// Returns false if a staged-block wait gave up (the error word has the
+// With s.dma_bias, sebuf (nst x 64 floats, 16-byte aligned) receives each staged
+// block's per-token eviction scores, added to the logits.  Returns false if a staged-block wait gave up (the error word has the
 // timeout bit; copies in flight have been drained).  ttid: thread index within the team.
 __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const LayerState& s, const Geometry& geo,
                                               int u, const uint32_t (&qb)[8][2], const int* blk, const int* slot,
                                               const int* isnew, int n, uint32_t sbase, uint64_t* bars, int nst,
-                                              Team team, int ttid, WarpAcc& A) {
+                                              float* sebuf, Team team, int ttid, WarpAcc& A) {
   const int lane = ttid & 31, warp = ttid >> 5;
   const int gr = lane >> 2, t4 = lane & 3;
   int nnew = 0;
@@ -104,7 +105,16 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
   const int ded = min(nnew, nst - 1);  // dedicated stages 0 .. ded-1
   const int ring = nst - ded;          // ring stages ded .. nst-1
   const int nr = n - ded;              // ring entries: local entries ded .. n-1
-  auto host_copy = [&](int e, int st) { host_block_copy(s, geo, u, blk[e], sbase + st * kStageBytes, ttid); };
+  const bool dma = s.dma_bias != 0;
+  // the block's 64 per-token eviction scores (256 bytes, 256-byte aligned rows)
+  auto se_src = [&](int e) { return s.se_tok + (size_t)u * s.se_stride + (size_t)kBlock * blk[e]; };
+  auto host_copy = [&](int e, int st) {
+    host_block_copy(s, geo, u, blk[e], sbase + st * kStageBytes, ttid);
+    if (dma) {
+      if (ttid < kBlock / 4) cp_async_16(smem_u32(sebuf + st * kBlock) + 16 * ttid, se_src(e) + 4 * ttid, 16);
+      cp_async_commit();
+    }
+  };
   auto issue_ring = [&](int p) {  // ring entry p into stage ded + p % ring
     if (p >= nr) return;
     const int st = ded + p % ring, e = ded + p;
@@ -114,9 +124,10 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
     } else if (ttid == 0) {
       const int flat = (s.unit_base + u) * s.cap + slot[e];
       fence_proxy_async_smem();
-      mbar_arrive_expect_tx(&bars[st], kStageBytes);
+      mbar_arrive_expect_tx(&bars[st], kStageBytes + (dma ? kBlock * 4 : 0));
       tma_load_4d(sbase + st * kStageBytes, tmap, 0, 0, 0, flat, &bars[st]);
       tma_load_4d(sbase + st * kStageBytes + 16384, tmap, 64, 0, 0, flat, &bars[st]);
+      if (dma) bulk_copy_g2s(smem_u32(sebuf + st * kBlock), se_src(e), kBlock * 4, &bars[st]);
     }
   };
   for (int d = 0; d < ded; ++d) host_copy(d, d);
@@ -131,7 +142,8 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
   const int tk_v = tok0 + (lane & 7) + ((lane >> 4) << 3);        // V^T: (d lo|hi) x (tokens 0-7|8-15)
   const int ch_v = (lane >> 3) & 1;
 
-  auto process = [&](uint32_t stg, int e) {
+  auto process = [&](int st, int e) {
+    const uint32_t stg = sbase + st * kStageBytes;
     const int valid = (blk[e] == geo.nb - 1) ? geo.valid_tail : kBlock;
     if (tok0 < valid) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -144,6 +156,14 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[j] *= sl2;
+      if (dma) {  // natural-log bias in base-2 units
+        const float b0 = sebuf[st * kBlock + tok0 + gr] * 1.4426950408889634f;
+        const float b1 = sebuf[st * kBlock + tok0 + gr + 8] * 1.4426950408889634f;
+        acc[0] += b0;
+        acc[1] += b0;
+        acc[2] += b1;
+        acc[3] += b1;
+      }
       if (tok0 + gr >= valid) acc[0] = acc[1] = -INFINITY;
       if (tok0 + gr + 8 >= valid) acc[2] = acc[3] = -INFINITY;
       float mx0 = fmaxf(acc[0], acc[2]), mx1 = fmaxf(acc[1], acc[3]);
@@ -205,7 +225,7 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
       break;
     }
     consumed = p + 1;
-    process(sbase + st * kStageBytes, e);
+    process(st, e);
     team.sync();  // every warp is done with this stage
     issue_ring(issued);
     ++issued;
@@ -213,7 +233,7 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
   cp_async_wait_all();
   team.sync();  // the dedicated host blocks have landed
   if (!bad)
-    for (int d = 0; d < ded; ++d) process(sbase + d * kStageBytes, d);
+    for (int d = 0; d < ded; ++d) process(d, d);
   if (bad && ttid == 0) {  // drain copies still in flight before the shared memory is reused
     for (int p = consumed; p < min(issued, nr); ++p)
       mbar_wait_bounded(&bars[ded + p % ring], (uint32_t)((p / ring) & 1), kWaitCycles);

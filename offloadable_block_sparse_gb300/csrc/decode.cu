@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   __shared__ int w_blk[kTeams][kSlots], w_slot[kTeams][kSlots], w_new[kTeams][kSlots], w_n[kTeams];
   __shared__ float wm[4 * kTeams][kMaxGroup], wl[4 * kTeams][kMaxGroup];
   __shared__ float cp_m[kMaxGroup], cp_l[kMaxGroup], cp_o[kMaxGroup][kHeadDim];
+  __shared__ __align__(16) float sebuf[kTeams][kDecodeMaxStages][kBlock];  // staged blocks' eviction scores
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank(), CS = (int)cluster.num_blocks();
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   A.init();
   const uint32_t sbase = smem_u32(smem) + (uint32_t)(team * nst * kStageBytes);
   attend_worker(&tmap, s, geo, u, qb, w_blk[team], w_slot[team], w_new[team], w_n[team], sbase, bars[team], nst,
-                Team{kTeams == 1 ? 0u : 1u + (uint32_t)team}, ttid, A);
+                &sebuf[team][0][0], Team{kTeams == 1 ? 0u : 1u + (uint32_t)team}, ttid, A);
   __syncthreads();  // every copy has landed (or was drained): the stages can hold the warp partials
 
   float* wo = reinterpret_cast<float*>(smem);  // [warps][8 heads][128]

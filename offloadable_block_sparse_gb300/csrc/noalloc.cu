@@ -142,6 +142,7 @@ extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* ca
   s.attend_chunks = chunks;
   s.attend_mode = 0;  // merge by ticket in the fixed scratch
   s.wait_limit = kWaitCycles;
+  s.dma_bias = 0;  // no eviction scores here: plain attention
   s.attend_blocks_per_cta = bpc;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   noalloc_prepare_kernel<<<(2 * units + 255) / 256, 256, 0, cs>>>(scratch, context_len, units);

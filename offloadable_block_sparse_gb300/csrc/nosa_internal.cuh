@@ -77,6 +77,8 @@ struct LayerState {
   int G;            // q heads per kv head
   int Hkv;
   int cap, nb_max, nc_max, T_max, ev_words, nw, sink, k_q, k_e, h;
+  int se_stride;          // row stride of se_tok: nb_max * 64, so each block's scores start 256-byte aligned
+  int dma_bias;           // attention logits get each token's eviction score added
   int unit_base;    // layer * U: first unit of this layer in context-wide arrays
   float scale;
   int* T;                 // device context length of this layer
@@ -84,7 +86,7 @@ struct LayerState {
   uint16_t* cache;        // [U][cap][2][64][d]
   uint16_t* kt;           // [U][nc_max][d]
   uint16_t* kring;        // [U][32][d]
-  float* se_tok;          // [U][T_max]
+  float* se_tok;          // [U][se_stride]
   float* se_win;          // [U][nc_max]
   float* se_blk;          // [U][nb_max]
   int32_t* slot_blk;      // [U][cap]

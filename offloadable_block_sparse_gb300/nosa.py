@@ -21,6 +21,7 @@ globals().update({n: i for i, n in enumerate(STATUS_NAMES)})
 NOSA_F_TEST_ZERO_WAIT = 1
 NOSA_F_TEST_BAD_SLOT = 2
 NOSA_F_UNFUSED_STEP = 4
+NOSA_F_DMA_BIAS = 8
 
 # every entry point declared in include/nosa.h
 EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_destroy", "nosa_set_stream",

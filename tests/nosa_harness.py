@@ -82,6 +82,7 @@ class Parity:
         self.d = wl.head_dim
         self.dev = device
         self.check_scores = check_scores
+        self.flags = flags
         self.cfg = N.make_config(num_layers=self.L, batch=wl.batch, num_q_heads=wl.q_heads,
                                  num_kv_heads=wl.kv_heads, k_q=wl.k_q, k_e=wl.k_e,
                                  window_tokens=wl.window_tokens, max_context=wl.max_context,
@@ -121,7 +122,7 @@ class Parity:
                 V[b, g] = torch.from_numpy(x["V"][:T0].view(np.int16)).view(torch.bfloat16).to(self.dev)
                 o = O.UnitOracle(head_dim=d, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
                                  window_tokens=wl.window_tokens, max_context=wl.max_context,
-                                 W1=W1[g], W2=W2[g])
+                                 W1=W1[g], W2=W2[g], dma_bias=bool(self.flags & N.NOSA_F_DMA_BIAS))
                 o.append(x["K"][:T0], x["V"][:T0])
                 self.oracles[(l, b, g)] = o
             N.nosa_append_kv(self.ctx, l, K.view(torch.int16), V.view(torch.int16), T0)

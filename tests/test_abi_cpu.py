@@ -45,7 +45,7 @@ def test_validate_config():
     assert N.nosa_validate_config(_cfg()) == N.NOSA_OK
     bad = [dict(head_dim=64), dict(block_size=32), dict(cmp_kernel=16), dict(cmp_stride=8),
            dict(num_q_heads=15), dict(num_q_heads=32, num_kv_heads=2), dict(k_q=-1), dict(window_tokens=100),
-           dict(max_context=0), dict(max_context=1 << 20), dict(evict_hidden=100), dict(flags=8),
+           dict(max_context=0), dict(max_context=1 << 20), dict(evict_hidden=100), dict(flags=16),
            dict(k_q=200, k_e=100), dict(batch=4097, num_kv_heads=1, num_q_heads=8), dict(softmax_scale=-1.0)]
     for b in bad:
         assert N.nosa_validate_config(_cfg(**b)) == N.NOSA_ERR_INVALID_ARG, b
@@ -58,6 +58,7 @@ def test_test_hook_flags_are_accepted():
     assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_TEST_ZERO_WAIT)) == N.NOSA_OK
     assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_TEST_BAD_SLOT | N.NOSA_F_TEST_ZERO_WAIT)) == N.NOSA_OK
     assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_UNFUSED_STEP)) == N.NOSA_OK
+    assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_DMA_BIAS | N.NOSA_F_UNFUSED_STEP)) == N.NOSA_OK
 
 
 def test_query_sizes_closed_forms():

@@ -67,6 +67,27 @@ def test_separate_calls_attend_fetches_itself():
 
 
 @STEP_MODES
+def test_tiny_with_dma_attention_bias(mode):
+    # attention logits get each token's eviction score added; sigma 1.0 moves the selection
+    wl = syn.workload("tiny", steps=24, sigma=1.0)
+    log, _ = run(wl, wl.steps, flags=mode | N.NOSA_F_DMA_BIAS)
+    _report("tiny-dma", log)
+    assert log.unit_steps == 48
+
+
+def test_dma_bias_through_separate_calls():
+    wl = syn.workload("tiny", steps=10)
+    p = Parity(wl, flags=N.NOSA_F_DMA_BIAS)
+    try:
+        p.load_context()
+        for _ in range(wl.steps):
+            p.run_step(split_calls=True, separate_fetch=False)
+        assert N.nosa_sync(p.ctx) == N.NOSA_OK
+    finally:
+        p.close()
+
+
+@STEP_MODES
 def test_ragged_context_group4_small_window(mode):
     # T_0 not a multiple of 64 or 16: the tail block is partial and is fetched on the first step;
     # 8 q heads over 2 kv heads (G = 4)
@@ -226,6 +247,7 @@ def test_host_pointer_step_matches_device_step():
 FULL = [
     ("nosa1b_16k_b8", 256, [(0, 0, 0), (5, 3, 1), (17, 7, 0), (27, 6, 1)], None, {}),
     ("nosa1b_16k_b8", 96, [(2, 1, 0), (26, 4, 1)], None, {"flags": UNFUSED}),
+    ("nosa1b_16k_b8", 64, [(1, 2, 1), (27, 7, 0)], None, {"flags": N.NOSA_F_DMA_BIAS}),
     ("nosa1b_16k_b128", 128, [(0, 0, 0), (13, 77, 1), (27, 127, 0)], None, {}),
     ("nosa1b_16k_b128", 64, [(3, 5, 0), (20, 100, 1)], None, {"sigma": 1.0}),
     ("nosa8b_32k_b32", 128, [(0, 0, 0), (4, 17, 5), (7, 31, 7)], 8, {}),
