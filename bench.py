@@ -108,6 +108,36 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ["append_core.cuh", "select_core.cuh", "attend_core.cuh", "ptx.cuh", "nosa_internal.cuh",
+                  "decode.cu", "attend.cu", "select.cu", "append.cu", "fetch.cu"]
+
+
+def kernel_source_hash():
+    """sha256 over the kernel sources, to tell whether stored ncu counters still describe them."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, "offloadable_block_sparse_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel, key):
+    """DRAM bytes per launch of `kernel` on workload `key` from a stored ncu capture, or (None, why)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None, "no capture"
+    if data.get("source_hash") != kernel_source_hash():
+        return None, "kernel changed since the capture"
+    e = data.get("entries", {}).get(f"{kernel}|{key}")
+    if not e:
+        return None, "no capture of this kernel and workload"
+    return e["dram_bytes_per_launch"], e["capture"]
+
+
 def h2d_peak(torch, nbytes=1 << 30, reps=6):
     h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
@@ -365,9 +395,12 @@ def run_native(args, rank, world, local_rank):
         note = ("attend bytes = K+V of every selected token; the newly selected blocks among them arrive over "
                 "the host link inside the same kernel")
     ach = dom_bytes / (us[dominant] * 1e-6) / 1e9
+    traffic, traffic_src = captured_traffic(f"{dominant}_kernel",
+                                            f"{wl.name}|sigma{wl.sigma}|kq{wl.k_q}|dma{int(args.dma_bias)}")
     result["roofline"] = {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
-                          "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
-                          "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_us": us[dominant], "note": note}
+                          "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
+                          "traffic_source": traffic_src, "algorithmic_bytes_per_launch": dom_bytes,
+                          "avg_launch_us": us[dominant], "note": note}
     fach = fetch_bytes_launch / (us["gather"] * 1e-6) / 1e9
     result["fetch_roofline"] = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach,
                                 "peak": h2d, "unit": "GB/s", "frac": fach / h2d,

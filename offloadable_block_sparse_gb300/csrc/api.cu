@@ -293,7 +293,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
   // Fused decode kernel: one cluster of dec_cs CTAs per unit, each CTA dec_teams attention
   // workers of four warps.  It pays off while all units' clusters are resident at once (the
-  // small batches where the step is latency bound): the largest cluster of 8, 4 or 2 CTAs for
+  // small batches where the step is latency bound): the largest cluster of 8 or 4 CTAs for
   // which that holds is taken, else the step runs as three kernels, as it does when the cache
   // has more slots than a CTA has threads.  NOSA_FUSED=0 turns it off; NOSA_DECODE_CLUSTER,
   // NOSA_DECODE_TEAMS and NOSA_DECODE_STAGES override the choices.
@@ -307,7 +307,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
       d.cap <= 128 * c->dec_teams) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    std::vector<int> sizes = {8, 4, 2};
+    std::vector<int> sizes = {8, 4};  // with clusters of 2 the selector and attention are too narrow
     const char* force = getenv("NOSA_DECODE_CLUSTER");
     if (force) sizes = {std::min(std::max(atoi(force), 1), 8)};
     const int warps = 4 * c->dec_teams;
