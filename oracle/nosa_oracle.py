@@ -292,9 +292,10 @@ class UnitOracle:
         E = select_query_agnostic(se_blk, C, Q, self.evicted, self.k_e)
         return Q, E
 
-    # -- a3/a4: commit a selection: eviction update, set difference, slots
-    def commit(self, Q, E):
-        sink, C, win = self.partition()
+    # -- a3/a4: commit a selection: eviction update, set difference, slots (for a context of T tokens,
+    # by default the current one)
+    def commit(self, Q, E, T=None):
+        sink, C, win = partition(self.T if T is None else T, self.nw, self.sink, self.block)
         D = sorted(set(Q) | set(E))
         S = sorted(set(sink) | set(D) | set(win))
         Dset = set(D)
@@ -311,6 +312,29 @@ class UnitOracle:
         Qg = bf16_bits_to_f64(q_bits).reshape(-1, self.d)
         bias = self.se_tok[:self.T] if self.dma_bias else None
         return sparse_attention(Qg, self.K[:self.T], self.V[:self.T], S, self.T, self.scale, self.block, bias)
+
+    # -- SparDA-style selection one layer ahead (SparDA summary: a forecast vector of layer l
+    # picks layer l+1's blocks before layer l+1 runs; one forecast head per kv head, no softmax
+    # aggregation over a group; sink and local blocks by position).  It is made before the token
+    # it serves is appended: scores over the windows complete now, blocks and candidates of T+1.
+    def forecast_scores(self, f_bits):
+        F = bf16_bits_to_f64(f_bits).reshape(1, self.d)
+        sq_win = query_scores(F, self.compressed_keys(), self.scale)
+        se_win = window_means(self.se_tok[:self.T], self.kernel, self.stride)
+        nb1 = num_blocks(self.T + 1, self.block)
+        return (block_pool(sq_win, nb1, self.block, self.kernel, self.stride),
+                block_pool(se_win, nb1, self.block, self.kernel, self.stride))
+
+    def forecast_step(self, f_bits, q_bits, k_bits, v_bits):
+        """Forecast selection for T+1, diff and slots; then append the token and attend with q."""
+        sq, se = self.forecast_scores(f_bits)
+        _, C, _ = partition(self.T + 1, self.nw, self.sink, self.block)
+        Q = select_query_aware(sq, C, self.k_q)
+        E = select_query_agnostic(se, C, Q, self.evicted, self.k_e)
+        r = self.commit(Q, E, T=self.T + 1)
+        self.append(k_bits, v_bits)
+        r.update(Q=Q, E=E, sq_blk=sq, se_blk=se, out=self.attend(q_bits, r["S"]))
+        return r
 
     def step(self, q_bits, k_bits, v_bits):
         """One decode step: append, score, select, diff, attend."""

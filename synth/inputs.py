@@ -34,7 +34,7 @@ from __future__ import annotations
 import numpy as np
 
 # tensor ids (part of the stream key)
-T_K, T_V, T_W1, T_W2, T_Q0, T_QN = 1, 2, 3, 4, 5, 6
+T_K, T_V, T_W1, T_W2, T_Q0, T_QN, T_F0, T_FN = 1, 2, 3, 4, 5, 6, 7, 8
 
 _M64 = np.uint64(0xFFFFFFFFFFFFFFFF)
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
@@ -113,12 +113,12 @@ def eviction_head(seed: int, layer: int, kv_head: int, d: int, h: int):
 
 
 def query_walk(seed: int, layer: int, batch: int, q_head: int, steps: int, d: int,
-               sigma: float) -> np.ndarray:
+               sigma: float, tensors=(T_Q0, T_QN)) -> np.ndarray:
     """bf16 bits [steps][d]: row t-1 is the query of decode step t (t = 1..steps)."""
-    q = normals(seed, T_Q0, layer, batch, q_head, 0, d)
+    q = normals(seed, tensors[0], layer, batch, q_head, 0, d)
     q = q / np.linalg.norm(q) * np.sqrt(d)
     out = np.empty((steps, d), dtype=np.uint16)
-    noise = normals(seed, T_QN, layer, batch, q_head, 0, steps * d).reshape(steps, d)
+    noise = normals(seed, tensors[1], layer, batch, q_head, 0, steps * d).reshape(steps, d)
     for t in range(steps):
         q = q + sigma * noise[t]
         q = q / np.linalg.norm(q) * np.sqrt(d)
@@ -157,7 +157,9 @@ class Workload:
         W1, W2 = eviction_head(self.seed, layer, kv_head, d, self.evict_hidden)
         Q = np.stack([query_walk(self.seed, layer, batch, kv_head * G + j, self.steps, d, self.sigma)
                       for j in range(G)], axis=1)  # [steps][G][d]
-        return dict(K=K, V=V, W1=W1, W2=W2, Q=Q)
+        # forecast vectors (one per kv head, the same random walk on their own streams)
+        F = query_walk(self.seed, layer, batch, kv_head, self.steps, d, self.sigma, (T_F0, T_FN))  # [steps][d]
+        return dict(K=K, V=V, W1=W1, W2=W2, Q=Q, F=F)
 
 
 # The five benchmark shapes (synthetic stand-ins for the pages' PG19 / NOSA-1B / NOSA-8B runs).

@@ -257,6 +257,52 @@ def test_k_e_zero_is_plain_top_k():
         assert r["Q"] == sorted(order[:6])
 
 
+# ----------------------------------------------------------------------------- forecast (SparDA)
+def _pair(T0, steps, k_q, k_e, window, sigma, seed, G, d=32):
+    w = syn.Workload("f", 1, 1, G, 1, T0, k_q, k_e, window, steps, sigma=sigma, head_dim=d,
+                     evict_hidden=16, seed=seed)
+    x = w.unit_inputs(0, 0, 0)
+
+    def unit():
+        u = O.UnitOracle(head_dim=d, k_q=k_q, k_e=k_e, window_tokens=window, max_context=T0 + steps,
+                         W1=x["W1"], W2=x["W2"])
+        u.append(x["K"][:T0], x["V"][:T0])
+        return u
+    return unit(), unit(), x
+
+
+def test_forecast_with_the_query_as_forecast_selects_what_the_plain_step_selects():
+    # One q head per kv head and the forecast equal to the query: selecting before the append
+    # (windows complete now, blocks of T+1) and after it differ only by the window the new token
+    # completes, which overlaps window blocks only and rescales every candidate's softmax score
+    # by one factor -- the same blocks are chosen, slots, fetches and outputs agree.
+    T0, steps = 2000, 70                  # a new block starts at T = 2049 (step 49)
+    a, b, x = _pair(T0, steps, 4, 8, 256, 1.0, 3, G=1)
+    for t in range(steps):
+        p = T0 + t
+        ra = a.step(x["Q"][t], x["K"][p:p + 1], x["V"][p:p + 1])
+        rb = b.forecast_step(x["Q"][t][0], x["Q"][t], x["K"][p:p + 1], x["V"][p:p + 1])
+        for key in ("S", "D", "fetch", "slot_of"):
+            assert ra[key] == rb[key], (t, key)
+        assert a.evicted == b.evicted
+        assert np.max(np.abs(ra["out"] - rb["out"])) < 1e-12
+
+
+def test_forecast_selection_keeps_the_locality_bound_and_fetches_a_new_tail_block():
+    T0, steps, k_q, k_e = 2048, 60, 4, 12  # the first forecast already serves a new block
+    _, u, x = _pair(T0, steps, k_q, k_e, 256, 1.0, 4, G=2)
+    gammas = []
+    for t in range(steps):
+        p = T0 + t
+        r = u.forecast_step(x["F"][t], x["Q"][t], x["K"][p:p + 1], x["V"][p:p + 1])
+        if t == 0:
+            assert 32 in r["S"] and 32 in [b for b, _ in r["fetch"]]   # block 32 starts at token 2048
+        if r["gamma"] is not None:
+            gammas.append(r["gamma"])
+        assert all(b < O.num_blocks(T0 + t + 1) for b in r["S"])
+    assert min(gammas) >= k_e / (k_q + k_e) - 1e-12
+
+
 # ----------------------------------------------------------------------------- attention
 def _sdpa(Q, K, V, scale, mask=None):
     q = torch.from_numpy(Q)[None, :, None, :]
