@@ -217,6 +217,31 @@ nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_
 nosa_status nosa_step_host(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, uint16_t* out);
 
+/* SparDA-style forecast selection (SparDA summary: a forecast vector of layer l picks
+ * layer l+1's blocks one layer ahead, so the copy of those blocks overlaps layer l's
+ * work; one forecast head per kv head; sink and local blocks by position).  Selects
+ * the blocks of `layer` for its context after the NEXT append (T+1): candidates, sink
+ * and window of T+1, query-aware scores from the forecast f (device bf16 [B][Hkv][d])
+ * over the windows complete at T, query-agnostic part, eviction, slots and fetch list
+ * as in nosa_select.  Then nosa_fetch (optional), nosa_append_kv of the token and
+ * nosa_attend use it.  NOSA_ERR_STATE if a forecast for T+1 was already made. */
+nosa_status nosa_forecast_select(nosa_ctx* ctx, int layer, const uint16_t* f);
+
+/* Pipelined forecast step of `layer` (needs a forecast selection for this token, from
+ * nosa_forecast_select or an earlier nosa_step_forecast).  If f_next is not NULL it
+ * first starts, on the context's own prefetch stream, the forecast selection of
+ * next_layer (!= layer) with f_next and the copy of its new blocks; then, on the
+ * context's stream, waits for this layer's prefetch (if one was started by an earlier
+ * call), appends k_new/v_new and attends with q.  The prefetch stream forks from and
+ * joins the context's stream through events, so a CUDA graph capture of a sequence of
+ * calls stays one graph; call nosa_forecast_join before ending a capture.  Pointers as
+ * in nosa_step; f_next: device bf16 [B][Hkv][d]. */
+nosa_status nosa_step_forecast(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
+                               const uint16_t* v_new, uint16_t* out, const uint16_t* f_next, int next_layer);
+
+/* Makes the context's stream wait for every prefetch started by nosa_step_forecast. */
+nosa_status nosa_forecast_join(nosa_ctx* ctx);
+
 /* How nosa_step runs on this context: *kernels_per_layer = 1 (the fused decode
  * kernel, one thread-block cluster of *cluster_size CTAs per unit) or 3 (append,
  * select and attend kernels; *cluster_size = 0).  Either pointer may be NULL. */

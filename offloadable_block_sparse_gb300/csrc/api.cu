@@ -85,6 +85,10 @@ void free_ctx(nosa_ctx* c) {
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_kv) cudaFreeHost(c->host_kv);
+  for (cudaEvent_t e : c->ev_pref)
+    if (e) cudaEventDestroy(e);
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+  if (c->pref_stream) cudaStreamDestroy(c->pref_stream);
   delete c;
 }
 
@@ -252,6 +256,8 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
   c->T_host.assign(c->L, 0);
   c->sel_T.assign(c->L, -1);
+  c->ev_pref.assign(c->L, nullptr);
+  c->pref_pending.assign(c->L, 0);
   c->fetch_T.assign(c->L, -1);
 
   const size_t LU = (size_t)c->L * c->U;
@@ -443,12 +449,23 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
       return NOSA_ERR_CUDA;
     }
   }
+  // forecast pipeline: a prefetch stream and its events
+  bool ev_ok = cudaStreamCreateWithFlags(&c->pref_stream, cudaStreamNonBlocking) == cudaSuccess &&
+               cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+  for (int l = 0; l < c->L && ev_ok; ++l)
+    ev_ok = cudaEventCreateWithFlags(&c->ev_pref[l], cudaEventDisableTiming) == cudaSuccess;
+  if (!ev_ok) {
+    (void)cudaGetLastError();
+    free_ctx(c);
+    return NOSA_ERR_CUDA;
+  }
   *out = c;
   return NOSA_OK;
 }
 
 nosa_status nosa_destroy(nosa_ctx* c) {
   if (!c) return NOSA_OK;
+  if (c->pref_stream) cudaStreamSynchronize(c->pref_stream);
   cudaStreamSynchronize(c->stream);
   (void)cudaGetLastError();
   free_ctx(c);
@@ -527,9 +544,71 @@ nosa_status nosa_select(nosa_ctx* c, int layer, const uint16_t* q, int32_t* sel_
 nosa_status nosa_fetch(nosa_ctx* c, int layer) {
   nosa_status st = check_ctx(c, layer);
   if (st != NOSA_OK) return st;
-  if (c->sel_T[layer] != c->T_host[layer]) return NOSA_ERR_STATE;
-  CK(launch_gather(layer_state(c, layer), c->gather_ctas, c->stream));
-  c->fetch_T[layer] = c->T_host[layer];
+  const int ahead = c->sel_T[layer] - c->T_host[layer];  // 1 after a forecast selection
+  if (ahead != 0 && ahead != 1) return NOSA_ERR_STATE;
+  CK(launch_gather(layer_state(c, layer), c->gather_ctas, c->stream, ahead));
+  c->fetch_T[layer] = c->sel_T[layer];
+  return NOSA_OK;
+}
+
+// Forecast selection of `layer` for its context after the next append, on `stream`.
+static nosa_status forecast_select_on(nosa_ctx* c, int layer, const uint16_t* f, cudaStream_t stream) {
+  if (c->T_host[layer] < 1) return NOSA_ERR_STATE;
+  if (c->T_host[layer] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
+  if (c->sel_T[layer] == c->T_host[layer] + 1) return NOSA_ERR_STATE;  // one forecast per token
+  LayerState s = layer_state(c, layer);
+  s.G = 1;  // one forecast head per kv head
+  CK(launch_score_select(s, f, true, stream, 1));
+  c->sel_T[layer] = c->T_host[layer] + 1;
+  return NOSA_OK;
+}
+
+nosa_status nosa_forecast_select(nosa_ctx* c, int layer, const uint16_t* f) {
+  nosa_status st = check_ctx(c, layer);
+  if (st != NOSA_OK) return st;
+  if (!f) return NOSA_ERR_INVALID_ARG;
+  return forecast_select_on(c, layer, f, c->stream);
+}
+
+nosa_status nosa_step_forecast(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t* k_new,
+                               const uint16_t* v_new, uint16_t* out, const uint16_t* f_next, int next_layer) {
+  nosa_status st = check_ctx(c, layer);
+  if (st != NOSA_OK) return st;
+  if (!q || !k_new || !v_new || !out) return NOSA_ERR_INVALID_ARG;
+  if (c->sel_T[layer] != c->T_host[layer] + 1) return NOSA_ERR_STATE;  // no forecast for this token
+  if (f_next) {
+    if (next_layer < 0 || next_layer >= c->L || next_layer == layer) return NOSA_ERR_INVALID_ARG;
+    if (c->sel_T[next_layer] == c->T_host[next_layer] + 1) return NOSA_ERR_STATE;
+    if (c->T_host[next_layer] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
+    // the next layer's state was last written by work already queued on the step stream
+    CK(cudaEventRecord(c->ev_fork, c->stream));
+    CK(cudaStreamWaitEvent(c->pref_stream, c->ev_fork, 0));
+    st = forecast_select_on(c, next_layer, f_next, c->pref_stream);
+    if (st != NOSA_OK) return st;
+    CK(launch_gather(layer_state(c, next_layer), c->gather_ctas, c->pref_stream, 1));
+    c->fetch_T[next_layer] = c->sel_T[next_layer];
+    CK(cudaEventRecord(c->ev_pref[next_layer], c->pref_stream));
+    c->pref_pending[next_layer] = 1;
+  }
+  if (c->pref_pending[layer]) {
+    CK(cudaStreamWaitEvent(c->stream, c->ev_pref[layer], 0));
+    c->pref_pending[layer] = 0;
+  }
+  const LayerState s = layer_state(c, layer);
+  CK(launch_append_one(s, k_new, v_new, true, c->stream));
+  c->T_host[layer] += 1;
+  const int fused = c->fetch_T[layer] != c->T_host[layer];  // no prefetch ran: attend copies itself
+  CK(launch_attend(s, &c->tmap_cache, q, out, fused, true, c->stream));
+  return NOSA_OK;
+}
+
+nosa_status nosa_forecast_join(nosa_ctx* c) {
+  if (!c) return NOSA_ERR_INVALID_ARG;
+  for (int l = 0; l < c->L; ++l) {
+    if (!c->pref_pending[l]) continue;
+    CK(cudaStreamWaitEvent(c->stream, c->ev_pref[l], 0));
+    c->pref_pending[l] = 0;
+  }
   return NOSA_OK;
 }
 
@@ -606,13 +685,18 @@ nosa_status nosa_step_plan(nosa_ctx* c, int32_t* kernels_per_layer, int32_t* clu
 
 nosa_status nosa_sync(nosa_ctx* c) {
   if (!c) return NOSA_ERR_INVALID_ARG;
+  CK(cudaStreamSynchronize(c->pref_stream));
   CK(cudaStreamSynchronize(c->stream));
   int e = 0;
   CK(cudaMemcpy(&e, c->err, sizeof(int), cudaMemcpyDeviceToHost));
   std::vector<int> T(c->L);
   CK(cudaMemcpy(T.data(), c->T, c->L * sizeof(int), cudaMemcpyDeviceToHost));
   for (int l = 0; l < c->L; ++l) {  // graph replays advance the device lengths only
-    if (T[l] != c->T_host[l] && c->sel_T[l] == c->T_host[l]) c->sel_T[l] = T[l];
+    if (T[l] != c->T_host[l]) {   // keep the selection (and fetch) a forecast ahead, or not, as captured
+      const int ds = c->sel_T[l] - c->T_host[l], df = c->fetch_T[l] - c->T_host[l];
+      if (ds == 0 || ds == 1) c->sel_T[l] = T[l] + ds;
+      if (df == 0 || df == 1) c->fetch_T[l] = T[l] + df;
+    }
     c->T_host[l] = T[l];
   }
   if (e && !c->failed) c->failed = err_to_status(e);

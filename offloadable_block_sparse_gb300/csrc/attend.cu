@@ -42,13 +42,16 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
 
   const int chunk = blockIdx.x, u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = s.G;
-  // independent loads first: q fragments, the context length, the unit's selection size
+  // Everything is read after the wait (q, the context length, the selection): the previous
+  // kernel may be the append that sets T, or the kernel that wrote q.  These loads and the
+  // selection entries below go out together, one round trip.
+  pdl_wait();
+  pdl_launch_dependents();  // the next layer's append may start
   uint32_t qb[8][2];
   load_q_frags(qb, q, u, G, lane);
-  const Geometry geo = geometry(*s.T, s.nw, s.sink);  // written two kernels back (append)
-  pdl_wait();               // the selection (previous kernel) is needed from here
-  pdl_launch_dependents();  // the next layer's append may start
+  const int T = *s.T;
   const int nsel = s.n_sel[u];
+  const Geometry geo = geometry(T, s.nw, s.sink);
   const uint32_t sbase = smem_u32(smem);
   // Work split: the unit's selected blocks are dealt round-robin to its CTAs in an
   // order that puts the blocks still to be copied from the host first, so those

@@ -7,7 +7,9 @@
 // One work item is one block: its K and V chunks (2 x 16 KiB) are contiguous in
 // both the host store and the slot.  Each thread keeps 4 x 16 bytes in flight
 // per item; the CTA walks items item = blockIdx.x, += gridDim.x.  Rows past the
-// end of the partial tail block are written as zeros.
+// end of the partial tail block are written as zeros.  ahead = 1: the list comes from a
+// forecast selection for T + 1 and may name the block the next token starts, which has no
+// rows yet (all zeros here; the append writes its first row into the slot).
 #include "nosa_internal.cuh"
 #include "ptx.cuh"
 
@@ -15,11 +17,12 @@ namespace nosa {
 
 constexpr int kMaxGatherUnits = 4096;
 
-__global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s) {
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s, int ahead) {
   __shared__ int pref[kMaxGatherUnits + 1];
   __shared__ int scan_tmp[32];
   const int tid = threadIdx.x;
   const Geometry geo = geometry(*s.T, s.nw, s.sink);
+  const int nb_sel = geometry(*s.T + ahead, s.nw, s.sink).nb;  // blocks of the selection's context
   // exclusive prefix of the per-unit fetch counts
   int carry = 0;
   for (int base = 0; base < s.U; base += blockDim.x) {
@@ -43,11 +46,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s) {
     }
     const int u = lo, j = item - pref[u];
     const int b = s.fetch[((size_t)u * s.cap + j) * 2], slot = s.fetch[((size_t)u * s.cap + j) * 2 + 1];
-    if (b < 0 || b >= geo.nb || slot < 0 || slot >= s.cap) {
+    if (b < 0 || b >= nb_sel || slot < 0 || slot >= s.cap) {
       if (tid == 0) atomicOr(s.err, kErrBounds);
       continue;
     }
-    const int rows = (b == geo.nb - 1) ? geo.valid_tail : kBlock;
+    const int rows = b < geo.nb - 1 ? kBlock : (b == geo.nb - 1 ? geo.valid_tail : 0);
     const uint4* src = reinterpret_cast<const uint4*>(s.host_kv + ((size_t)u * s.nb_max + b) * 2 * kBlockElems);
     uint4* dst = reinterpret_cast<uint4*>(s.cache + ((size_t)u * s.cap + slot) * 2 * kBlockElems);
     uint4 v[kVec];
@@ -62,8 +65,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s) {
   }
 }
 
-cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st) {
-  gather_kernel<<<ctas, kGatherThreads, 0, st>>>(s);
+cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st, int ahead) {
+  gather_kernel<<<ctas, kGatherThreads, 0, st>>>(s, ahead);
   return cudaGetLastError();
 }
 

@@ -157,6 +157,12 @@ struct nosa_ctx {
   std::vector<int> sel_T;   // T at the last selection (-1: none), host view
   std::vector<int> fetch_T; // T at the last nosa_fetch (-1: none): attend fetches itself otherwise
   int failed;               // latched nosa_status of a device-side error
+  // forecast pipeline: prefetch stream, fork event, one "prefetched" event per layer and whether
+  // the layer's stream still has to wait for it
+  cudaStream_t pref_stream;
+  cudaEvent_t ev_fork;
+  std::vector<cudaEvent_t> ev_pref;
+  std::vector<char> pref_pending;
 };
 
 namespace nosa {
@@ -196,8 +202,9 @@ LayerState layer_state(nosa_ctx* c, int layer);
 cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint16_t* v, bool pdl, cudaStream_t st);
 cudaError_t launch_append_bulk(const LayerState& s, const uint16_t* k, const uint16_t* v, int T_old,
                                int n, cudaStream_t st);
-cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, bool pdl, cudaStream_t st);
-cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st);
+// ahead = 1: forecast selection / its gather, made before the next token is appended
+cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, bool pdl, cudaStream_t st, int ahead = 0);
+cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st, int ahead = 0);
 // fused_fetch != 0: blocks marked in sel_new are copied from the pinned host
 // store by the attend CTAs themselves (and written back to their slots), so no
 // separate gather launch is needed.

@@ -28,7 +28,8 @@ EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_dest
            "nosa_set_eviction_head", "nosa_append_kv", "nosa_select", "nosa_fetch", "nosa_attend", "nosa_step",
            "nosa_step_host", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
            "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string",
-           "nosa_attend_noalloc", "nosa_step_plan"]
+           "nosa_attend_noalloc", "nosa_step_plan", "nosa_forecast_select", "nosa_step_forecast",
+           "nosa_forecast_join"]
 
 
 class nosa_config(ctypes.Structure):
@@ -90,6 +91,9 @@ def lib() -> ctypes.CDLL:
             "nosa_step": [vp, i32, p, p, p, p],
             "nosa_step_host": [vp, i32, p, p, p, p],
             "nosa_sync": [vp],
+            "nosa_forecast_select": [vp, i32, p],
+            "nosa_step_forecast": [vp, i32, p, p, p, p, p, i32],
+            "nosa_forecast_join": [vp],
             "nosa_step_plan": [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
             "nosa_reset_state": [vp],
             "nosa_context_length": [vp, i32, ctypes.POINTER(ctypes.c_int32)],
@@ -196,6 +200,20 @@ def nosa_step(ctx, layer, q, k_new, v_new, out) -> None:
 
 def nosa_step_host(ctx, layer, q, k_new, v_new, out) -> None:
     _check(lib().nosa_step_host(ctx, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)), "nosa_step_host")
+
+
+def nosa_forecast_select(ctx, layer, f) -> None:
+    _check(lib().nosa_forecast_select(ctx, layer, _ptr(f)), "nosa_forecast_select")
+
+
+def nosa_step_forecast(ctx, layer, q, k_new, v_new, out, f_next=None, next_layer=0) -> None:
+    _check(lib().nosa_step_forecast(ctx, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                    _ptr(f_next) if f_next is not None else None, next_layer),
+           "nosa_step_forecast")
+
+
+def nosa_forecast_join(ctx) -> None:
+    _check(lib().nosa_forecast_join(ctx), "nosa_forecast_join")
 
 
 def nosa_step_plan(ctx):

@@ -149,6 +149,80 @@ class Parity:
             v[b, g] = torch.from_numpy(x["V"][pos].view(np.int16)).view(torch.bfloat16).to(self.dev)
         return q, k, v
 
+    def forecast_inputs(self, l, t):
+        """f [B][Hkv][d] on the device: the forecast vectors for the token of decode step t+1 of layer l."""
+        torch, wl = self.torch, self.wl
+        f = torch.randn((wl.batch, wl.kv_heads, self.d), generator=self._filler, device=self.dev)
+        f = (f / f.norm(dim=-1, keepdim=True) * math.sqrt(self.d)).to(torch.bfloat16)
+        for (sl, b, g) in self.samples:
+            if sl == l:
+                f[b, g] = torch.from_numpy(self.inputs[(l, b, g)]["F"][t].view(np.int16)).view(
+                    torch.bfloat16).to(self.dev)
+        return f
+
+    def run_forecast_step(self, check=True, separate_fetch=True):
+        """One decode step with forecast selections made by separate calls, every layer checked."""
+        torch, N = self.torch, self.N
+        for l in range(self.L):
+            q, k, v = self.step_inputs(l)
+            f = self.forecast_inputs(l, self.t)
+            out = torch.empty_like(q)
+            N.nosa_forecast_select(self.ctx, l, f.view(torch.int16))
+            if separate_fetch:
+                N.nosa_fetch(self.ctx, l)
+            N.nosa_append_kv(self.ctx, l, k.view(torch.int16), v.view(torch.int16), 1)
+            N.nosa_attend(self.ctx, l, q.view(torch.int16), out.view(torch.int16))
+            if check and any(sl == l for (sl, _, _) in self.samples):
+                st = N.nosa_sync(self.ctx)
+                assert st == 0, f"device error {N.STATUS_NAMES[st]}"
+                self._check_layer(l, q, out, f)
+        self.t += 1
+        self.log.steps += 1
+
+    def run_forecast_pipeline(self, steps):
+        """Steps through nosa_step_forecast: each layer's call starts the next layer's forecast and
+        prefetch on the context's prefetch stream (the last layer forecasts layer 0 of the next
+        step).  Outputs of the sampled units are checked against the oracle's forecast step."""
+        torch, N = self.torch, self.N
+        assert self.L >= 2
+        fs = [[self.forecast_inputs(l, t) for l in range(self.L)] for t in range(steps)]
+        N.nosa_forecast_select(self.ctx, 0, fs[0][0].view(torch.int16))
+        for t in range(steps):
+            done = []
+            for l in range(self.L):
+                q, k, v = self.step_inputs(l)
+                out = torch.empty_like(q)
+                if l + 1 < self.L:
+                    fn, nxt = fs[t][l + 1], l + 1
+                else:
+                    fn, nxt = (fs[t + 1][0], 0) if t + 1 < steps else (None, 0)
+                N.nosa_step_forecast(self.ctx, l, q.view(torch.int16), k.view(torch.int16), v.view(torch.int16),
+                                     out.view(torch.int16), None if fn is None else fn.view(torch.int16), nxt)
+                done.append((l, q, k, v, out))
+            N.nosa_forecast_join(self.ctx)
+            st = N.nosa_sync(self.ctx)
+            assert st == 0, f"device error {N.STATUS_NAMES[st]}"
+            for (l, q, k, v, out) in done:
+                f_h = fs[t][l].view(torch.int16).cpu().numpy().view(np.uint16)
+                q_h = q.view(torch.int16).cpu().numpy().view(np.uint16)
+                out_h = out.float().cpu().numpy()
+                for (sl, b, g) in self.samples:
+                    if sl != l:
+                        continue
+                    o, x = self.oracles[(l, b, g)], self.inputs[(l, b, g)]
+                    pos = self.wl.context + self.t
+                    r = o.forecast_step(f_h[b, g], q_h[b, g * self.G:(g + 1) * self.G], x["K"][pos:pos + 1],
+                                        x["V"][pos:pos + 1])
+                    err = np.abs(out_h[b, g * self.G:(g + 1) * self.G] - r["out"])
+                    self.log.max_out_abs = max(self.log.max_out_abs, float(err.max()))
+                    self.log.max_out_mean_abs = max(self.log.max_out_mean_abs, float(err.mean()))
+                    assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS, f"output error {err.max():.3e}"
+                    if r["gamma"] is not None:
+                        self.log.gammas.append(r["gamma"])
+                    self.log.unit_steps += 1
+            self.t += 1
+            self.log.steps += 1
+
     def run_step(self, check=True, split_calls=False, separate_fetch=True):
         torch, N = self.torch, self.N
         for l in range(self.L):
@@ -186,11 +260,14 @@ class Parity:
         st["sq_blk"] = sq
         return st
 
-    def _check_layer(self, l, q, out):
+    def _check_layer(self, l, q, out, f=None):
+        """Compares layer l's selection, state and output with the oracle.  With f (the forecast
+        vectors of this step) the oracle selects before the append, as the forecast path does."""
         wl = self.wl
         st = self._export(l)
         out_h = out.float().cpu().numpy()
         q_h = q.view(self.torch.int16).cpu().numpy().view(np.uint16)
+        f_h = None if f is None else f.view(self.torch.int16).cpu().numpy().view(np.uint16)
         for (sl, b, g) in self.samples:
             if sl != l:
                 continue
@@ -198,17 +275,25 @@ class Parity:
             o = self.oracles[(l, b, g)]
             x = self.inputs[(l, b, g)]
             pos = wl.context + self.t
-            o.append(x["K"][pos:pos + 1], x["V"][pos:pos + 1])
             qb = q_h[b, g * self.G:(g + 1) * self.G]
             assert np.array_equal(qb, x["Q"][self.t])
-            nb, nc = o.nb, o.nc
-            # compressed keys: bit-exact
-            kt_or = O.f64_to_bf16_bits(o.compressed_keys())
-            assert np.array_equal(st["kt"][u, :nc], kt_or), f"K~ mismatch unit {(l, b, g)} step {self.t}"
-            sq, se = o.scores(qb)
+            if f is None:
+                o.append(x["K"][pos:pos + 1], x["V"][pos:pos + 1])
+                sq, se = o.scores(qb)
+                T_sel = o.T
+            else:
+                fb = f_h[b, g]
+                assert np.array_equal(fb, x["F"][self.t])
+                sq, se = o.forecast_scores(fb)
+                T_sel = o.T + 1
+            _, C, _ = O.partition(T_sel, o.nw, o.sink, o.block)
+            nb = O.num_blocks(T_sel, o.block)
             if self.check_scores:
                 e1 = rel_err(st["sq_blk"][u, :nb], sq)
-                e2 = rel_err(st["se_blk"][u, :nb], se)
+                # the forecast path appends after it selects: the token's window may move the pooled
+                # s^e of window blocks, so only the candidates' scores are compared there
+                cmp = slice(0, nb) if f is None else C
+                e2 = rel_err(st["se_blk"][u, :nb][cmp], np.asarray(se)[cmp]) if (f is None or C) else 0.0
                 self.log.max_score_rel = max(self.log.max_score_rel, e1, e2)
                 assert e1 <= SCORE_REL and e2 <= SCORE_REL, f"pooled scores {e1:.2e} {e2:.2e} unit {(l, b, g)}"
             n = st["n_sel"][u]
@@ -216,8 +301,7 @@ class Parity:
             kinds = st["sel_kind"][u, :n]
             Q_gpu = sorted(int(bb) for bb, kk in zip(S_gpu, kinds) if kk == 2)
             E_gpu = sorted(int(bb) for bb, kk in zip(S_gpu, kinds) if kk == 3)
-            _, C, _ = o.partition()
-            Q = o.select(sq, se)[0]
+            Q = O.select_query_aware(sq, C, wl.k_q)
             if Q != Q_gpu:
                 ok = _near_tie_ok(np.asarray(sq).astype(np.float32), Q_gpu, Q, C, wl.k_q)
                 assert ok, f"query-aware pick differs beyond a near tie: unit {(l, b, g)} step {self.t}: {Q} vs {Q_gpu}"
@@ -230,7 +314,13 @@ class Parity:
                 assert ok, f"query-agnostic pick differs beyond a near tie: unit {(l, b, g)} step {self.t}"
                 self.log.near_ties.append(("e", (l, b, g), self.t, sorted(set(E) ^ set(E_gpu))))
                 E = E_gpu
-            r = o.commit(Q, E)
+            r = o.commit(Q, E, T=T_sel)
+            if f is not None:
+                o.append(x["K"][pos:pos + 1], x["V"][pos:pos + 1])
+            nb, nc = o.nb, o.nc
+            # compressed keys after the step's append: bit-exact
+            kt_or = O.f64_to_bf16_bits(o.compressed_keys())
+            assert np.array_equal(st["kt"][u, :nc], kt_or), f"K~ mismatch unit {(l, b, g)} step {self.t}"
             assert S_gpu == r["S"], f"selection mismatch unit {(l, b, g)} step {self.t}"
             assert list(st["sel_slot"][u, :n]) == r["slot_of"], "slot mismatch"
             nf = st["n_fetch"][u]
@@ -250,8 +340,9 @@ class Parity:
             err = np.abs(got - ref)
             self.log.max_out_abs = max(self.log.max_out_abs, float(err.max()))
             self.log.max_out_mean_abs = max(self.log.max_out_mean_abs, float(err.mean()))
-            assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS, f"output error {err.max():.3e}"
-            assert err.max() <= 2 ** -7 * np.abs(ref).max() + 1e-4, f"output error {err.max():.3e} (tight)"
+            where = f"unit {(l, b, g)} step {self.t} T {o.T} max|ref| {np.abs(ref).max():.3e}"
+            assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS, f"output error {err.max():.3e} {where}"
+            assert err.max() <= 2 ** -7 * np.abs(ref).max() + 1e-4, f"output error {err.max():.3e} (tight) {where}"
             self.log.unit_steps += 1
 
     def close(self):

@@ -241,6 +241,94 @@ def test_host_pointer_step_matches_device_step():
             p.close()
 
 
+# ----------------------------------------------------------------------------- forecast (SparDA)
+@pytest.mark.parametrize("separate_fetch", [True, False], ids=["prefetch", "attend-fetches"])
+def test_forecast_selection_every_step(separate_fetch):
+    # selection one layer ahead with a forecast vector per kv head; the fetch either runs before
+    # the append (as a prefetch would) or is left to the attention after it
+    wl = syn.workload("tiny", steps=40, sigma=1.0)
+    p = Parity(wl)
+    try:
+        p.load_context()
+        for _ in range(wl.steps):
+            p.run_forecast_step(separate_fetch=separate_fetch)
+        assert N.nosa_sync(p.ctx) == N.NOSA_OK
+        _report("forecast", p.log)
+        assert p.log.unit_steps == 80
+        assert min(p.log.gammas) >= wl.k_e / (wl.k_q + wl.k_e) - 1e-12
+    finally:
+        p.close()
+
+
+def test_forecast_new_tail_block_is_prefetched():
+    # T0 a multiple of 64: the first forecast serves the token that starts a new block
+    wl = syn.Workload("fc_tail", layers=1, batch=2, q_heads=16, kv_heads=2, context=2048, k_q=4, k_e=12,
+                      window_tokens=256, steps=70, sigma=1.0)
+    p = Parity(wl)
+    try:
+        p.load_context()
+        for _ in range(wl.steps):
+            p.run_forecast_step()
+        assert p.log.unit_steps == 70 * 4
+    finally:
+        p.close()
+
+
+def test_forecast_pipeline_overlaps_the_next_layer():
+    wl = syn.Workload("fc_pipe", layers=3, batch=3, q_heads=16, kv_heads=2, context=3000, k_q=4, k_e=12,
+                      window_tokens=256, steps=30, sigma=1.0)
+    p = Parity(wl)
+    try:
+        p.load_context()
+        p.run_forecast_pipeline(wl.steps)
+        _report("forecast-pipeline", p.log)
+        assert p.log.unit_steps == 30 * 3 * 3 * 2
+        assert min(p.log.gammas) >= wl.k_e / (wl.k_q + wl.k_e) - 1e-12
+    finally:
+        p.close()
+
+
+def test_forecast_call_order_is_checked():
+    wl = syn.Workload("fc_order", layers=2, batch=1, q_heads=16, kv_heads=2, context=500, k_q=2, k_e=2,
+                      window_tokens=128, steps=2)
+    p = Parity(wl)
+    try:
+        p.load_context()
+        q = torch.zeros((1, 16, 128), dtype=torch.int16, device="cuda")
+        kv = torch.zeros((1, 2, 128), dtype=torch.int16, device="cuda")
+        f = torch.zeros((1, 2, 128), dtype=torch.int16, device="cuda")
+        with pytest.raises(N.NosaError) as e:     # no forecast for this token yet
+            N.nosa_step_forecast(p.ctx, 0, q, kv, kv, q)
+        assert e.value.status == N.NOSA_ERR_STATE
+        N.nosa_forecast_select(p.ctx, 0, f)
+        with pytest.raises(N.NosaError) as e:     # one forecast per token
+            N.nosa_forecast_select(p.ctx, 0, f)
+        assert e.value.status == N.NOSA_ERR_STATE
+        with pytest.raises(N.NosaError) as e:     # the next layer must differ
+            N.nosa_step_forecast(p.ctx, 0, q, kv, kv, q, f, 0)
+        assert e.value.status == N.NOSA_ERR_INVALID_ARG
+        N.nosa_step_forecast(p.ctx, 0, q, kv, kv, q, f, 1)
+        N.nosa_step_forecast(p.ctx, 1, q, kv, kv, q)
+        N.nosa_forecast_join(p.ctx)
+        assert N.nosa_sync(p.ctx) == N.NOSA_OK
+        assert N.nosa_context_length(p.ctx, 0) == 501 and N.nosa_context_length(p.ctx, 1) == 501
+    finally:
+        p.close()
+
+
+def test_forecast_pipeline_full_size_sampled():
+    # the 1B, 16K, batch-8 workload's per-layer shape, all 28 layers pipelined, sampled units checked
+    wl = syn.workload("nosa1b_16k_b8")
+    p = Parity(wl, sample_units=[(0, 0, 0), (13, 5, 1), (27, 7, 0)])
+    try:
+        p.load_context()
+        p.run_forecast_pipeline(24)
+        _report("forecast-c2", p.log)
+        assert p.log.unit_steps == 24 * 3
+    finally:
+        p.close()
+
+
 # Full-size workloads, every unit run on the GPU, sampled units checked against the oracle at every
 # step.  The 8B-shaped workload keeps its per-layer sizes (32 sequences x 8 kv heads x 32K tokens)
 # but runs 8 of its 32 layers: its full host store (138 GB pinned) exceeds the test machine's RAM.
