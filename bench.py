@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (only for host-memory limits)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--dma-bias", action="store_true", help="attention adds each token's eviction score (DMA bias)")
+    ap.add_argument("--dense", action="store_true",
+                    help="full-attention comparator: dense decode attention over a device-resident KV cache")
+    ap.add_argument("--forecast", action="store_true",
+                    help="SparDA-style selection one layer ahead from forecast vectors, the next layer's "
+                         "selection and prefetch overlapping the current layer (timed leg only)")
     ap.add_argument("--quick", action="store_true", help="timed graph leg only (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -247,18 +252,43 @@ def run_native(args, rank, world, local_rank):
         qs = qs / qs.norm(dim=-1, keepdim=True) * math.sqrt(d)
         Qall[t] = qs.to(torch.bfloat16)
     KVall = torch.randn((total_steps, 2, L, B, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    fc = args.forecast
+    if fc:  # forecast vectors: one random walk per (layer, sequence, kv head), like the queries
+        fs = torch.randn((L, B, Hkv, d), generator=gen, device=dev)
+        fs = fs / fs.norm(dim=-1, keepdim=True) * math.sqrt(d)
+        Fall = torch.empty((total_steps + 1, L, B, Hkv, d), dtype=torch.bfloat16, device=dev)
+        for t in range(total_steps + 1):
+            fs = fs + wl.sigma * torch.randn(fs.shape, generator=gen, device=dev)
+            fs = fs / fs.norm(dim=-1, keepdim=True) * math.sqrt(d)
+            Fall[t] = fs.to(torch.bfloat16)
+        cur_f = torch.empty((L, B, Hkv, d), dtype=torch.bfloat16, device=dev)
+        cur_f0n = torch.empty((B, Hkv, d), dtype=torch.bfloat16, device=dev)  # layer 0, next step
     out = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
     cur_q = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
     cur_kv = torch.empty((2, L, B, Hkv, d), dtype=torch.bfloat16, device=dev)
     i16 = torch.int16
     step_i = [0]
 
+    def forecast_calls(q, kv, f, f0n):
+        # layer l's call starts layer l+1's forecast and prefetch; the last layer forecasts layer 0
+        # of the next step; the step ends joined to the prefetch stream
+        for l in range(L):
+            fn, nxt = (f[l + 1], l + 1) if l + 1 < L else (f0n, 0)
+            N.nosa_step_forecast(ctx, l, q[l].view(i16), kv[0, l].view(i16), kv[1, l].view(i16), out[l].view(i16),
+                                 fn.view(i16), nxt)
+        N.nosa_forecast_join(ctx)
+
     def eager_step(t):
+        if fc:
+            forecast_calls(Qall[t], KVall[t], Fall[t], Fall[t + 1, 0])
+            return
         for l in range(L):
             N.nosa_step(ctx, l, Qall[t, l].view(i16), KVall[t, 0, l].view(i16), KVall[t, 1, l].view(i16),
                         out[l].view(i16))
 
     # step 1 (cold fetch of every selected block) is not timed
+    if fc:
+        N.nosa_forecast_select(ctx, 0, Fall[0, 0].view(i16))
     eager_step(0)
     step_i[0] = 1
     use_graph = not args.no_graph
@@ -269,9 +299,12 @@ def run_native(args, rank, world, local_rank):
         N.nosa_set_stream(ctx, side.cuda_stream)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
-            for l in range(L):
-                N.nosa_step(ctx, l, cur_q[l].view(i16), cur_kv[0, l].view(i16), cur_kv[1, l].view(i16),
-                            out[l].view(i16))
+            if fc:
+                forecast_calls(cur_q, cur_kv, cur_f, cur_f0n)
+            else:
+                for l in range(L):
+                    N.nosa_step(ctx, l, cur_q[l].view(i16), cur_kv[0, l].view(i16), cur_kv[1, l].view(i16),
+                                out[l].view(i16))
         N.nosa_set_stream(ctx, stream.cuda_stream)
         assert N.nosa_sync(ctx) == N.NOSA_OK
 
@@ -279,6 +312,9 @@ def run_native(args, rank, world, local_rank):
         if use_graph:
             cur_q.copy_(Qall[t], non_blocking=True)
             cur_kv.copy_(KVall[t], non_blocking=True)
+            if fc:
+                cur_f.copy_(Fall[t], non_blocking=True)
+                cur_f0n.copy_(Fall[t + 1, 0], non_blocking=True)
             graph.replay()
         else:
             eager_step(t)
@@ -322,14 +358,20 @@ def run_native(args, rank, world, local_rank):
                          "cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
                          "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster,
                          "dma_bias": bool(args.dma_bias),
+                         "selection": "forecast one layer ahead, overlapped prefetch" if fc else "query (per step)",
                          "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache "
                                "(L2 is 129 MB)"},
-              "gpu_launches": step_kernels * L * K,
+              "gpu_launches": (4 if fc else step_kernels) * L * K,
               "clocks": ck,
               "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min, "bound": wl.k_e / (wl.k_q + wl.k_e)},
               "fetch_blocks_per_step": fetched_per_step,
               "short_selections": stats.short_selections}
-    if args.quick or rank != 0:
+    if args.quick or fc or rank != 0:
+        if fc:
+            result["roofline"] = None
+            result["e2e"] = None
+            result["note"] = ("forecast mode: timed graph leg only (4 kernels per layer: forecast select and "
+                              "gather on the prefetch stream, append and attend on the step stream)")
         N.nosa_destroy(ctx)
         return result
 
@@ -485,6 +527,95 @@ def run_native(args, rank, world, local_rank):
     return result
 
 
+def run_dense(args, rank, world, local_rank):
+    """Full-attention comparator (the pages' FullAttn rows): every layer's attention reads the whole
+    context from a device-resident KV cache; no selection, no host memory.  Same workload shapes."""
+    import torch
+    from offloadable_block_sparse_gb300 import nosa as N
+    from synth import inputs as syn
+    torch.cuda.set_device(local_rank)
+    dev = "cuda"
+    over = {"sigma": args.sigma} if args.sigma is not None else {}
+    wl = syn.workload(args.workload, **over)
+    L = args.layers or wl.layers
+    B, Hq, Hkv, d = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
+    U, G, T = B * Hkv, Hq // Hkv, wl.context
+    nb = -(-T // 64)
+    K, W = args.steps, args.warmup
+    gen = torch.Generator(device=dev).manual_seed(1000 * rank + 17)
+    kv = torch.empty((L, U, nb, 2, 64, d), dtype=torch.bfloat16, device=dev)
+    for l in range(L):
+        for u0 in range(0, U, 16):
+            u1 = min(U, u0 + 16)
+            kv[l, u0:u1] = torch.randn((u1 - u0, nb, 2, 64, d), generator=gen, device=dev).to(torch.bfloat16)
+    qs = torch.randn((K + W + 1, L, U, G, d), generator=gen, device=dev)
+    Qall = (qs / qs.norm(dim=-1, keepdim=True) * math.sqrt(d)).to(torch.bfloat16)
+    del qs
+    out = torch.empty((L, U, G, d), dtype=torch.bfloat16, device=dev)
+    cur_q = torch.empty((L, U, G, d), dtype=torch.bfloat16, device=dev)
+    nbytes = N.nosa_dense_scratch_bytes(U, T)
+    scratch = torch.zeros(nbytes // 4 + 64, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    i16 = torch.int16
+
+    def calls(q, st):
+        for l in range(L):
+            N.nosa_dense_attend(q[l].view(i16), kv[l].view(i16), U, G, nb, T, out[l].view(i16), scratch, nbytes,
+                                stream=st)
+
+    calls(Qall[0], stream.cuda_stream)  # first call sets the kernel attributes outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        calls(cur_q, side.cuda_stream)
+    for t in range(W):
+        cur_q.copy_(Qall[1 + t], non_blocking=True)
+        graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(K):
+        cur_q.copy_(Qall[1 + W + t], non_blocking=True)
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    assert int(scratch[0].item()) == 0, "device-side error in the dense attention"
+    ms = slowest_rank_ms(e0.elapsed_time(e1) / K, world, dev)
+    # per-launch time of one layer's dense attention (kernel + merge), stream held while queueing
+    per = []
+    for _ in range(5):
+        torch.cuda._sleep(400000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        N.nosa_dense_attend(Qall[0, 0].view(i16), kv[0].view(i16), U, G, nb, T, out[0].view(i16), scratch, nbytes,
+                            stream=stream.cuda_stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(b) * 1e3)
+    us = statistics.median(per)
+    bytes_launch = U * T * 2 * d * 2 + 2 * U * G * d * 2
+    hbm, src = measured_peaks()
+    return {"metric": METRIC, "value": job_throughput(B, world, ms), "unit": "tok/s", "n_gpus": world, "steps": K,
+            "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": Hkv,
+                       "head_dim": d, "context": T, "selection": "dense (full-attention comparator, KV in HBM)",
+                       "parallelism": f"replicas x{world}", "cuda_graph": True},
+            "gpu_launches": 2 * L * K, "clocks": ck,
+            "roofline": {"kernel": "dense_attend_kernel + merge", "bound": "hbm",
+                         "achieved": bytes_launch / (us * 1e-6) / 1e9, "peak": hbm,
+                         "peak_source": f"{src} hbm_gbs (MEASURED_PEAKS.json)", "unit": "GB/s",
+                         "frac": bytes_launch / (us * 1e-6) / 1e9 / hbm, "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_launch, "avg_launch_us": us},
+            "kv_resident_gb": kv.numel() * 2 / 1e9}
+
+
 def run_reference(args):
     """The oracle, as it stands, on host cores: each step is a bounded sample of the workload."""
     from synth import inputs as syn
@@ -513,7 +644,7 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    res = run_native(args, rank, world, local_rank)
+    res = run_dense(args, rank, world, local_rank) if args.dense else run_native(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

@@ -242,6 +242,26 @@ nosa_status nosa_step_forecast(nosa_ctx* ctx, int layer, const uint16_t* q, cons
 /* Makes the context's stream wait for every prefetch started by nosa_step_forecast. */
 nosa_status nosa_forecast_join(nosa_ctx* ctx);
 
+/* Dense GQA decode attention over a device-resident KV store: the full-attention
+ * comparator of the NOSA wiki's decode-throughput table (every token attended; no
+ * selection, no host memory).  Context-free; allocates nothing.
+ *   q        device bf16 [units][group][d]
+ *   kv       device bf16 [units][max_blocks][2][64][d]: block b of unit u holds keys
+ *            then values of tokens 64b .. 64b+63 (the layout of the host store and
+ *            of the block cache); 16-byte aligned
+ *   context_len  tokens attended (<= max_blocks * 64 and <= 1,048,576)
+ *   out      device bf16 [units][group][d]
+ *   scratch  device memory of at least nosa_dense_scratch_bytes(units, context_len)
+ *            bytes, 256-byte aligned; its first 4 bytes receive device-side error bits
+ *            (zero them before the call to read them after it)
+ * Asynchronous on `stream`.  NOSA_ERR_CAPACITY if the scratch is too small. */
+nosa_status nosa_dense_attend(const uint16_t* q, const uint16_t* kv, int units, int group, int max_blocks,
+                              int context_len, float softmax_scale, uint16_t* out, void* scratch,
+                              size_t scratch_bytes, void* stream);
+
+/* Scratch bytes nosa_dense_attend needs (0 on a bad argument or without a device). */
+size_t nosa_dense_scratch_bytes(int units, int context_len);
+
 /* How nosa_step runs on this context: *kernels_per_layer = 1 (the fused decode
  * kernel, one thread-block cluster of *cluster_size CTAs per unit) or 3 (append,
  * select and attend kernels; *cluster_size = 0).  Either pointer may be NULL. */

@@ -267,6 +267,10 @@ __global__ void __launch_bounds__(kHeadDim) attend_merge_kernel(LayerState s, ui
   out[((size_t)u * s.G + h) * kHeadDim + x] = __bfloat16_as_ushort(__float2bfloat16_rn(r));
 }
 
+cudaError_t launch_attend_merge(const LayerState& s, uint16_t* out, cudaStream_t st) {
+  return launch_ex(attend_merge_kernel, dim3(s.G, s.U), dim3(kHeadDim), 0, st, true, 0, s, out);
+}
+
 template <int M, int S>
 static cudaError_t set_attend_attrs() {
   cudaError_t e = cudaFuncSetAttribute(attend_kernel<M, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,

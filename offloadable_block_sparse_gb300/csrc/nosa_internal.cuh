@@ -210,6 +210,8 @@ cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st, int ah
 // separate gather launch is needed.
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                           int fused_fetch, bool pdl, cudaStream_t st);
+// merges s.attend_chunks split-K partials per unit from s.apart into out (at most 256 chunks)
+cudaError_t launch_attend_merge(const LayerState& s, uint16_t* out, cudaStream_t st);
 size_t score_select_smem(const LayerState& s);
 // one-time kernel attributes (dynamic shared memory limits), called by nosa_create
 cudaError_t init_append(const LayerState& s);

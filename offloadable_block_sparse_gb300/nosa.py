@@ -29,7 +29,7 @@ EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_dest
            "nosa_step_host", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
            "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string",
            "nosa_attend_noalloc", "nosa_step_plan", "nosa_forecast_select", "nosa_step_forecast",
-           "nosa_forecast_join"]
+           "nosa_forecast_join", "nosa_dense_attend", "nosa_dense_scratch_bytes"]
 
 
 class nosa_config(ctypes.Structure):
@@ -94,6 +94,8 @@ def lib() -> ctypes.CDLL:
             "nosa_forecast_select": [vp, i32, p],
             "nosa_step_forecast": [vp, i32, p, p, p, p, p, i32],
             "nosa_forecast_join": [vp],
+            "nosa_dense_attend": [p, p, i32, i32, i32, i32, ctypes.c_float, p, p, ctypes.c_size_t, vp],
+            "nosa_dense_scratch_bytes": [i32, i32],
             "nosa_step_plan": [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
             "nosa_reset_state": [vp],
             "nosa_context_length": [vp, i32, ctypes.POINTER(ctypes.c_int32)],
@@ -109,6 +111,7 @@ def lib() -> ctypes.CDLL:
             f.restype = ctypes.c_int
         L.nosa_status_string.argtypes = [ctypes.c_int]
         L.nosa_status_string.restype = ctypes.c_char_p
+        L.nosa_dense_scratch_bytes.restype = ctypes.c_size_t
         _lib = L
     return _lib
 
@@ -214,6 +217,17 @@ def nosa_step_forecast(ctx, layer, q, k_new, v_new, out, f_next=None, next_layer
 
 def nosa_forecast_join(ctx) -> None:
     _check(lib().nosa_forecast_join(ctx), "nosa_forecast_join")
+
+
+def nosa_dense_scratch_bytes(units, context_len) -> int:
+    return int(lib().nosa_dense_scratch_bytes(units, context_len))
+
+
+def nosa_dense_attend(q, kv, units, group, max_blocks, context_len, out, scratch, scratch_bytes,
+                      softmax_scale=0.0, stream=0) -> None:
+    """Dense decode attention over a device KV store [units][max_blocks][2][64][d] (see include/nosa.h)."""
+    _check(lib().nosa_dense_attend(_ptr(q), _ptr(kv), units, group, max_blocks, context_len, softmax_scale,
+                                   _ptr(out), _ptr(scratch), scratch_bytes, stream), "nosa_dense_attend")
 
 
 def nosa_step_plan(ctx):
