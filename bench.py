@@ -113,15 +113,19 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ["append_core.cuh", "select_core.cuh", "attend_core.cuh", "ptx.cuh", "nosa_internal.cuh",
-                  "decode.cu", "attend.cu", "select.cu", "append.cu", "fetch.cu"]
+# the sources each measured kernel is compiled from
+KERNEL_SOURCES = {
+    "decode_kernel": ["decode.cu", "append_core.cuh", "select_core.cuh", "attend_core.cuh", "ptx.cuh",
+                      "nosa_internal.cuh"],
+    "attend_kernel": ["attend.cu", "attend_core.cuh", "ptx.cuh", "nosa_internal.cuh"],
+}
 
 
-def kernel_source_hash():
-    """sha256 over the kernel sources, to tell whether stored ncu counters still describe them."""
+def kernel_source_hash(kernel):
+    """sha256 over a kernel's sources, to tell whether stored ncu counters still describe it."""
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES.get(kernel, []):
         h.update(f.encode())
         with open(os.path.join(ROOT, "offloadable_block_sparse_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
@@ -135,11 +139,11 @@ def captured_traffic(kernel, key):
             data = json.load(f)
     except (OSError, ValueError):
         return None, "no capture"
-    if data.get("source_hash") != kernel_source_hash():
-        return None, "kernel changed since the capture"
     e = data.get("entries", {}).get(f"{kernel}|{key}")
     if not e:
         return None, "no capture of this kernel and workload"
+    if e.get("source_hash") != kernel_source_hash(kernel):
+        return None, "kernel changed since the capture"
     return e["dram_bytes_per_launch"], e["capture"]
 
 
