@@ -265,24 +265,33 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   // selector: one cluster of up to 8 CTAs per unit, each scoring a multiple of 128 windows
   c->score_chunks = std::min(8, cdiv(nc, kWindowsPerCta));
   c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
-  // attend: about two CTAs per SM in total, at most kMaxBlocksPerCta blocks each.  Merge of the
-  // split-K partials: inside one thread-block cluster per unit (default, when clusters of the
-  // unit's CTA count can be scheduled), else by a small follow-up kernel; an atomic ticket merge
-  // is kept for the context-free entry point.
-  int bpc = cdiv((long long)c->U * d.cap, 2ll * std::max(c->num_sms, 1));
-  bpc = std::min(std::max(bpc, 1), kMaxBlocksPerCta);
+  // attend: 8 to 16 selected blocks per CTA, about four CTAs' worth per SM in total (measured
+  // best at the batch-128/256 and 64K-context workloads: fewer, longer CTAs starve the host
+  // copies of parallelism, more CTAs spend their time in set-up and merging).  Merge of the
+  // split-K partials: inside one thread-block cluster per unit when all the attention's CTAs
+  // fit in one wave (latency-bound sizes), else by a small merge kernel -- a cluster's CTAs hold
+  // their SMs until the slowest one is done, which costs 10-17 % at multi-wave sizes.  An atomic
+  // ticket merge is kept for the context-free entry point.
+  const int sms = std::max(c->num_sms, 1);
+  int bpc = cdiv((long long)c->U * d.cap, 4ll * sms);
+  bpc = std::min(std::max(bpc, 8), 16);
   if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), kMaxBlocksPerCta);
   if (init_attend() != cudaSuccess) {  // the cluster query below needs the kernel's smem limit set
     (void)cudaGetLastError();
     delete c;
     return NOSA_ERR_CUDA;
   }
-  c->attend_mode = 1;
-  if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
-  if (c->attend_mode == 1) {
+  {
     const int max_cluster = attend_max_cluster(false);
-    while (cdiv(d.cap, bpc) > max_cluster && bpc < kMaxBlocksPerCta) ++bpc;
-    if (cdiv(d.cap, bpc) > max_cluster) c->attend_mode = 2;
+    int cbpc = bpc;  // blocks per CTA if the unit's CTAs are to form one cluster
+    while (cdiv(d.cap, cbpc) > max_cluster && cbpc < kMaxBlocksPerCta) ++cbpc;
+    const bool one_wave = (long long)c->U * cdiv(d.cap, cbpc) <= 2ll * sms;
+    c->attend_mode = (one_wave && cdiv(d.cap, cbpc) <= max_cluster) ? 1 : 2;
+    if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
+    if (c->attend_mode == 1) {
+      if (cdiv(d.cap, cbpc) <= max_cluster) bpc = cbpc;
+      else c->attend_mode = 2;
+    }
   }
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
@@ -291,7 +300,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     c->attend_deep = atoi(e) != 0 && (c->attend_mode == 2 || attend_max_cluster(true) >= c->attend_chunks);
     if (c->attend_deep && c->attend_mode == 2 && !getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) {
       // one CTA per SM: chunks such that units x chunks is about the SM count
-      bpc = std::min(std::max(cdiv((long long)c->U * d.cap, std::max(c->num_sms, 1)), 1), kMaxBlocksPerCta);
+      bpc = std::min(std::max(cdiv((long long)c->U * d.cap, sms), 1), kMaxBlocksPerCta);
       c->attend_blocks_per_cta = bpc;
       c->attend_chunks = cdiv(d.cap, bpc);
     }

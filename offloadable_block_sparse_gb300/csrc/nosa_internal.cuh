@@ -34,7 +34,7 @@ constexpr int kWindowsPerCta = kScoreWarps * kScoreTiles * 16;
 
 constexpr int kAttendThreads = 128;        // 4 warps, 16 tokens of every 64-token block each
 constexpr int kAttendStages = 3;           // 32 KiB TMA stages per CTA
-constexpr int kMaxBlocksPerCta = 16;       // split-K chunk: selected blocks per attend CTA
+constexpr int kMaxBlocksPerCta = 64;       // split-K chunk: selected blocks per attend CTA
 constexpr int kMaxCacheSlots = 256;        // cache slots per unit (sink + window + k_q + k_e)
 constexpr int kPartStride = 2 + kHeadDim;  // (m, l, o[128]) per head in a split-K partial
 
