@@ -262,9 +262,17 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
 
   const size_t LU = (size_t)c->L * c->U;
   const size_t nc = std::max(d.nc_max, 1);
-  // selector: one cluster of up to 8 CTAs per unit, each scoring a multiple of 128 windows
-  c->score_chunks = std::min(8, cdiv(nc, kWindowsPerCta));
-  c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
+  // selector: one cluster of up to 8 CTAs per unit, each scoring a multiple of 128 windows, and
+  // about two CTAs per SM in total: a unit's cluster lives mostly in its leader's serial phase,
+  // so at large batch more units in flight beat more CTAs per unit (measured: one CTA per unit
+  // at 256 units, four at 64 units with 64K contexts)
+  c->score_chunks = std::max(1, std::min({8, cdiv(nc, kWindowsPerCta), 2 * std::max(c->num_sms, 1) / c->U}));
+  if (const char* e = getenv("NOSA_SCORE_CHUNKS")) c->score_chunks = std::min(std::max(atoi(e), 1), 8);
+  for (;;) {  // more CTAs per unit while one CTA's logits would not fit its shared memory
+    c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
+    if (c->score_chunks >= 8 || score_select_smem(layer_state(c, 0)) <= 200 * 1024) break;
+    ++c->score_chunks;
+  }
   // attend: 8 to 16 selected blocks per CTA, about four CTAs' worth per SM in total (measured
   // best at the batch-128/256 and 64K-context workloads: fewer, longer CTAs starve the host
   // copies of parallelism, more CTAs spend their time in set-up and merging).  Merge of the
