@@ -275,11 +275,11 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   }
   // attend: 8 to 16 selected blocks per CTA, about four CTAs' worth per SM in total (measured
   // best at the batch-128/256 and 64K-context workloads: fewer, longer CTAs starve the host
-  // copies of parallelism, more CTAs spend their time in set-up and merging).  Merge of the
-  // split-K partials: inside one thread-block cluster per unit when all the attention's CTAs
-  // fit in one wave (latency-bound sizes), else by a small merge kernel -- a cluster's CTAs hold
-  // their SMs until the slowest one is done, which costs 10-17 % at multi-wave sizes.  An atomic
-  // ticket merge is kept for the context-free entry point.
+  // copies of parallelism, more CTAs spend their time in set-up and merging).  The split-K
+  // partials are merged by a small merge kernel: merging inside a thread-block cluster per unit
+  // (NOSA_ATTEND_MODE=1) makes a cluster's CTAs hold their SMs until the slowest one is done and
+  // measured 5-17 % slower at every workload, batch 8 included.  An atomic ticket merge is kept
+  // for the context-free entry point.
   const int sms = std::max(c->num_sms, 1);
   int bpc = cdiv((long long)c->U * d.cap, 4ll * sms);
   bpc = std::min(std::max(bpc, 8), 16);
@@ -289,17 +289,12 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     delete c;
     return NOSA_ERR_CUDA;
   }
-  {
+  c->attend_mode = 2;
+  if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
+  if (c->attend_mode == 1) {  // the unit's CTAs must form one cluster
     const int max_cluster = attend_max_cluster(false);
-    int cbpc = bpc;  // blocks per CTA if the unit's CTAs are to form one cluster
-    while (cdiv(d.cap, cbpc) > max_cluster && cbpc < kMaxBlocksPerCta) ++cbpc;
-    const bool one_wave = (long long)c->U * cdiv(d.cap, cbpc) <= 2ll * sms;
-    c->attend_mode = (one_wave && cdiv(d.cap, cbpc) <= max_cluster) ? 1 : 2;
-    if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
-    if (c->attend_mode == 1) {
-      if (cdiv(d.cap, cbpc) <= max_cluster) bpc = cbpc;
-      else c->attend_mode = 2;
-    }
+    while (cdiv(d.cap, bpc) > max_cluster && bpc < kMaxBlocksPerCta) ++bpc;
+    if (cdiv(d.cap, bpc) > max_cluster) c->attend_mode = 2;
   }
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
