@@ -115,8 +115,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   // CTA partial (base-2 max, sum, unnormalised output) for each head
   __shared__ float cp_m[kMaxGroup], cp_l[kMaxGroup], cp_o[kMaxGroup][kHeadDim];
   float* part0 = s.apart + ((size_t)u * s.attend_chunks + chunk) * kMaxGroup * kPartStride;
-  cta_partial<4>(A, wm, wl, wo, G, [&](int h, float M, float L, float O) {
-    const int x = tid;
+  cta_partial<4>(A, wm, wl, wo, G, [&](int h, int x, float M, float L, float O) {
     if constexpr (kMerge == kMergeCluster) {
       if (x == 0) {
         cp_m[h] = M;

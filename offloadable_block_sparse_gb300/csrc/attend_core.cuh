@@ -244,9 +244,11 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
 }
 
 // Reduces the warps' softmax state to one (m, l, o) per head: warp partials go to
-// shared memory (wm, wl [nwarps][8], wo [nwarps][8][128]) and thread x (< 128) of the
-// CTA combines dimension x.  Call with every thread of the CTA; contains __syncthreads.
-// emit(h, M, L, O) is called by threads x < 128 for every head h < G.
+// shared memory (wm, wl [nwarps][8], wo [nwarps][8][128]); one thread per head forms
+// the head's maximum, sum and per-warp scale factors (written over wm), then every
+// thread of the CTA combines output elements.  Call with every thread of the CTA;
+// contains __syncthreads.  emit(h, x, M, L, O) is called once per head h < G and
+// dimension x < 128.
 template <int kWarps, typename Emit>
 __device__ __forceinline__ void cta_partial(const WarpAcc& A, float (*wm)[kMaxGroup], float (*wl)[kMaxGroup],
                                             float* wo, int G, Emit emit) {
@@ -273,24 +275,30 @@ __device__ __forceinline__ void cta_partial(const WarpAcc& A, float (*wm)[kMaxGr
     w0[16 * mt + gr + 8] = A.o[mt][2];
     w1[16 * mt + gr + 8] = A.o[mt][3];
   }
+  __shared__ float head_m[kMaxGroup], head_l[kMaxGroup];
   __syncthreads();
-  if (tid < kHeadDim) {
-    const int x = tid;  // head dimension
-    for (int h = 0; h < G; ++h) {
-      float M = -INFINITY;
+  if (tid < G) {
+    const int h = tid;
+    float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h]);
-      float L = 0.f, O = 0.f;
-      if (M > -INFINITY) {
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][h]);
+    float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float f = exp2f(wm[w][h] - M);
-          L += wl[w][h] * f;
-          O += wo[(w * kMaxGroup + h) * kHeadDim + x] * f;
-        }
-      }
-      emit(h, M, L, O);
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = M > -INFINITY ? exp2f(wm[w][h] - M) : 0.f;
+      L += wl[w][h] * f;
+      wm[w][h] = f;  // the warp's scale factor from here on
     }
+    head_m[h] = M;
+    head_l[h] = L;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * kHeadDim; idx += blockDim.x) {
+    const int h = idx >> 7, x = idx & (kHeadDim - 1);
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) O = fmaf(wo[(w * kMaxGroup + h) * kHeadDim + x], wm[w][h], O);
+    emit(h, x, head_m[h], head_l[h], O);
   }
 }
 

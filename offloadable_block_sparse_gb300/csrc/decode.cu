@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   __syncthreads();  // the window key written above is read by this CTA's scorer
 
   // ---------------- a2-a4: selector phases
-  score_windows<(kTeams == 1 ? 4 : 2)>(s, u, geo.nc, rank, m, sh, qf);
+  score_windows<4>(s, u, geo.nc, rank, m, sh, qf);
   if (rank == CS - 1) __threadfence_system();  // the token's host-store row, copied by other CTAs below
   cluster.sync();  // every CTA's statistics are visible
   pool_blocks(s, u, geo, rank, CS, m, sh);
@@ -179,18 +179,20 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   __syncthreads();  // every copy has landed (or was drained): the stages can hold the warp partials
 
   float* wo = reinterpret_cast<float*>(smem);  // [warps][8 heads][128]
-  cta_partial<4 * kTeams>(A, wm, wl, wo, G, [&](int h, float M, float L, float O) {
-    if (tid == 0) {
+  cta_partial<4 * kTeams>(A, wm, wl, wo, G, [&](int h, int x, float M, float L, float O) {
+    if (x == 0) {
       cp_m[h] = M;
       cp_l[h] = L;
     }
-    cp_o[h][tid] = O;
+    cp_o[h][x] = O;
   });
-  // every CTA of the unit merges the heads h = rank, rank + CS, ... from all CTAs' partials
+  // every CTA of the unit merges the heads h = rank, rank + CS, ... from all CTAs' partials,
+  // one output element per thread
   cluster.sync();
-  if (tid < kHeadDim) {
-    const int x = tid;
-    for (int h = rank; h < G; h += CS) {
+  {
+    const int nh = (G - rank + CS - 1) / CS;
+    for (int idx = tid; idx < nh * kHeadDim; idx += blockDim.x) {
+      const int h = rank + CS * (idx >> 7), x = idx & (kHeadDim - 1);
       float mr[8], M = -INFINITY;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {

@@ -52,13 +52,13 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
   __syncthreads();  // every copy has landed (or was drained): the stages can hold the warp partials
   float* wo = reinterpret_cast<float*>(smem);
   float* part0 = s.apart + ((size_t)u * s.attend_chunks + chunk) * kMaxGroup * kPartStride;
-  cta_partial<4>(A, wm, wl, wo, s.G, [&](int h, float M, float L, float O) {
+  cta_partial<4>(A, wm, wl, wo, s.G, [&](int h, int x, float M, float L, float O) {
     float* part = part0 + h * kPartStride;
-    if (tid == 0) {
+    if (x == 0) {
       part[0] = M;
       part[1] = L;
     }
-    part[2 + tid] = O;
+    part[2 + x] = O;
   });
 }
 
