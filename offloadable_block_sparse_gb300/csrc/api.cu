@@ -148,7 +148,6 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.attend_chunks = c->attend_chunks;
   s.attend_blocks_per_cta = c->attend_blocks_per_cta;
   s.attend_mode = c->attend_mode;
-  s.attend_deep = c->attend_deep;
   s.wait_limit = (c->cfg.flags & NOSA_F_TEST_ZERO_WAIT) ? -1 : kWaitCycles;
   s.test_bad_slot = (c->cfg.flags & NOSA_F_TEST_BAD_SLOT) ? 1 : 0;
   s.dma_bias = (c->cfg.flags & NOSA_F_DMA_BIAS) ? 1 : 0;
@@ -292,22 +291,12 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->attend_mode = 2;
   if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
   if (c->attend_mode == 1) {  // the unit's CTAs must form one cluster
-    const int max_cluster = attend_max_cluster(false);
+    const int max_cluster = attend_max_cluster();
     while (cdiv(d.cap, bpc) > max_cluster && bpc < kMaxBlocksPerCta) ++bpc;
     if (cdiv(d.cap, bpc) > max_cluster) c->attend_mode = 2;
   }
   c->attend_blocks_per_cta = bpc;
   c->attend_chunks = cdiv(d.cap, bpc);
-  c->attend_deep = 0;
-  if (const char* e = getenv("NOSA_ATTEND_DEEP")) {
-    c->attend_deep = atoi(e) != 0 && (c->attend_mode == 2 || attend_max_cluster(true) >= c->attend_chunks);
-    if (c->attend_deep && c->attend_mode == 2 && !getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) {
-      // one CTA per SM: chunks such that units x chunks is about the SM count
-      bpc = std::min(std::max(cdiv((long long)c->U * d.cap, sms), 1), kMaxBlocksPerCta);
-      c->attend_blocks_per_cta = bpc;
-      c->attend_chunks = cdiv(d.cap, bpc);
-    }
-  }
   c->gather_ctas = cfg->gather_ctas > 0 ? cfg->gather_ctas : (cfg->batch < 32 ? 16 : 32);
   // Fused decode kernel: one cluster of dec_cs CTAs per unit, each CTA dec_teams attention
   // workers of four warps.  It pays off while all units' clusters are resident at once (the

@@ -18,7 +18,6 @@ namespace cg = cooperative_groups;
 namespace nosa {
 
 static_assert(4 * kMaxGroup * kHeadDim * 4 <= 3 * kStageBytes, "warp partials alias the stages");
-constexpr int kDeepStages = 6;  // when a unit's CTAs get an SM each
 
 // How a unit's split-K partials are merged:
 //   kMerge == kMergeTicket : through global scratch; the last CTA of the unit (atomic ticket) merges;
@@ -281,9 +280,7 @@ static cudaError_t set_attend_attrs() {
 cudaError_t init_attend() {
   cudaError_t e = set_attend_attrs<kMergeTicket, kAttendStages>();
   if (e == cudaSuccess) e = set_attend_attrs<kMergeCluster, kAttendStages>();
-  if (e == cudaSuccess) e = set_attend_attrs<kMergeCluster, kDeepStages>();
   if (e == cudaSuccess) e = set_attend_attrs<kMergeKernel, kAttendStages>();
-  if (e == cudaSuccess) e = set_attend_attrs<kMergeKernel, kDeepStages>();
   return e;
 }
 
@@ -297,22 +294,20 @@ static cudaError_t launch_attend_t(const LayerState& s, const CUtensorMap* tmap,
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                           int fused_fetch, bool pdl, cudaStream_t st) {
   if (s.attend_mode == kMergeKernel) {
-    cudaError_t e = s.attend_deep ? launch_attend_t<kMergeKernel, kDeepStages>(s, tmap, q, out, fused_fetch, pdl, st)
-                                  : launch_attend_t<kMergeKernel, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
+    cudaError_t e = launch_attend_t<kMergeKernel, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
     if (e != cudaSuccess) return e;
-    return launch_ex(attend_merge_kernel, dim3(s.G, s.U), dim3(kHeadDim), 0, st, true, 0, s, out);
+    return launch_attend_merge(s, out, st);
   }
   if (s.attend_mode == kMergeTicket)
     return launch_attend_t<kMergeTicket, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
-  if (s.attend_deep) return launch_attend_t<kMergeCluster, kDeepStages>(s, tmap, q, out, fused_fetch, pdl, st);
   return launch_attend_t<kMergeCluster, kAttendStages>(s, tmap, q, out, fused_fetch, pdl, st);
 }
 
 // Largest cluster of attend CTAs (with this kernel's shared memory) the device can schedule.
-int attend_max_cluster(bool deep) {
+int attend_max_cluster() {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kAttendThreads);
-  cfg.dynamicSmemBytes = attend_smem_bytes(deep ? kDeepStages : kAttendStages);
+  cfg.dynamicSmemBytes = attend_smem_bytes(kAttendStages);
   int best = 1;
   for (int c : {8, 4, 2}) {
     cfg.gridDim = dim3(c, 1);
@@ -324,9 +319,7 @@ int attend_max_cluster(bool deep) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e =
-        deep ? cudaOccupancyMaxActiveClusters(&n, attend_kernel<kMergeCluster, kDeepStages>, &cfg)
-             : cudaOccupancyMaxActiveClusters(&n, attend_kernel<kMergeCluster, kAttendStages>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, attend_kernel<kMergeCluster, kAttendStages>, &cfg);
     if (e == cudaSuccess && n > 0) {
       best = c;
       break;

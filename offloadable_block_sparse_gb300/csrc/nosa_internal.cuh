@@ -113,7 +113,6 @@ struct LayerState {
   int attend_chunks;       // split-K CTAs per unit in attend
   int attend_blocks_per_cta;
   int attend_mode;         // split-K merge: 0 ticket (global), 1 cluster (DSMEM), 2 merge kernel
-  int attend_deep;         // 1: one attend CTA per SM, with a deeper TMA pipeline
   long long wait_limit;    // SM cycles a staged-block wait may take before it reports a timeout (<0: none)
   int test_bad_slot;       // test hook: publish one out-of-range slot (unit 0, first entry)
 };
@@ -142,7 +141,7 @@ struct nosa_ctx {
   // scratch
   float *sq_blk, *apart;
   unsigned int* tickets;
-  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_mode, attend_deep, gather_ctas;
+  int score_chunks, score_wpc, attend_chunks, attend_blocks_per_cta, attend_mode, gather_ctas;
   // fused decode kernel (nosa_step): cluster size (0: off, three kernels instead), windows per
   // scoring CTA, attention stages per team
   int dec_cs, dec_wpc, dec_nst, dec_teams;
@@ -217,7 +216,7 @@ size_t score_select_smem(const LayerState& s);
 cudaError_t init_append(const LayerState& s);
 cudaError_t init_score_select(const LayerState& s);
 cudaError_t init_attend();
-int attend_max_cluster(bool deep);
+int attend_max_cluster();
 // fused decode step of one layer (append + select + fetch + attend); s carries the fused
 // kernel's cluster size and windows per CTA in score_chunks / score_wpc
 LayerState decode_state(nosa_ctx* c, int layer);
