@@ -12,16 +12,19 @@
 //             CTA waits for the append before scoring.
 //   a2-a4     the selector phases with cluster barriers between them (scores and
 //             statistics through distributed shared memory, local top-k_q per
-//             CTA, selection by the leader CTA, which also leaves the selection
-//             list in its shared memory).
+//             CTA, pushed to every CTA).  Every CTA then runs the selection on
+//             the same inputs and reaches the same result; rank 0 alone stores
+//             the unit's selection state, and each CTA keeps its own workers'
+//             shares of the list, so no list crosses the cluster.
 //   a5-a6     every team is one split-K worker (the attention core: TMA ring
 //             over the block cache, blocks still on the host copied by cp.async
 //             and written to their new cache slot); the unit's selected blocks
 //             are dealt round-robin to the kTeams*CS workers, blocks without a
 //             slot first; the warps' partials are merged in shared memory and
 //             the CTAs' partials through distributed shared memory.
-// The selector's shared memory and the attention stages alias: the selection is
-// complete (cluster barrier) before any stage is loaded.
+// The selector's shared memory and the attention stages alias: a CTA's own selection
+// is complete (CTA barrier) before its stages are loaded, and no CTA reads another's
+// selector memory after the second cluster barrier.
 #include <algorithm>
 
 #include "append_core.cuh"
@@ -44,8 +47,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   extern __shared__ unsigned char smem_raw[];
   __shared__ SelShared sh;
   __shared__ __align__(8) uint64_t bars[kTeams][kDecodeMaxStages];
-  __shared__ int l_sel[kSlots], l_slot[kSlots], l_new[kSlots], l_n;  // leader's list
-  __shared__ int w_blk[kTeams][kSlots], w_slot[kTeams][kSlots], w_new[kTeams][kSlots], w_n[kTeams];
+  __shared__ int w_blk[kTeams][kSlots], w_slot[kTeams][kSlots], w_new[kTeams][kSlots];
   __shared__ float wm[4 * kTeams][kMaxGroup], wl[4 * kTeams][kMaxGroup];
   __shared__ float cp_m[kMaxGroup], cp_l[kMaxGroup], cp_o[kMaxGroup][kHeadDim];
   __shared__ __align__(16) float sebuf[kTeams][kDecodeMaxStages][kBlock];  // staged blocks' eviction scores
@@ -91,8 +93,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   // pooled s^e of the last two blocks may change in this step (a completed window overlaps
   // only them); the leader reads those after the append, the rest now
   const int nb_se = max(min(geo.ws, geo.nb - 2), 0);
-  int my_slot_blk = -1;
-  if (rank == 0) my_slot_blk = leader_prefetch(s, u, geo.nb, nb_se, m);
+  const int my_slot_blk = leader_prefetch(s, u, geo.nb, nb_se, m);  // every CTA selects
   // the window's scorer, and the next CTA, which scores it as the window before its range,
   // both compute its key (the same bits) before they read it
   if (window_done && (wi / s.score_wpc == rank || wi == rank * s.score_wpc - 1)) window_key(s, u, p, wi, knew);
@@ -107,74 +108,41 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   if (rank == CS - 1) __threadfence_system();  // the token's host-store row, copied by other CTAs below
   cluster.sync();  // every CTA's statistics are visible
   pool_blocks(s, u, geo, rank, CS, m, sh);
-  rank_local(s, geo, rank, CS, m, sh);
-  cluster.sync();  // the local winners (and the append's pooled s^e) are visible to the leader
+  rank_local(s, geo, rank, CS, m, sh, true);
+  cluster.sync();  // every CTA holds all local winners; the append's pooled s^e are visible
 
-  if (rank == 0) {
-    cp_async_wait_all();  // the leader's early copies (pooled s^e, slot map, eviction words)
-    if (tid < 2) {
-      const int b = nb_se + tid;
-      if (b < geo.ws) m.sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
-    }
-    __syncthreads();
-    leader_select(s, u, geo, CS, m, sh, my_slot_blk, LeaderLists{l_sel, l_slot, l_new, &l_n});
-  }
-  cluster.sync();  // the selection list is in the leader's shared memory
-
-  // ---------------- a5-a6: deal the selection to the workers round-robin, blocks without a
-  // slot first
-  const int NW = kTeams * CS, wkr = kTeams * rank + team;  // workers of the unit, this one
-  if ((ttid >> 5) == 0) {  // warp 0 of each team
-    const int* rsel = cluster.map_shared_rank(l_sel, 0);
-    const int* rslot = cluster.map_shared_rank(l_slot, 0);
-    const int* rnew = cluster.map_shared_rank(l_new, 0);
-    const int nsel = min(*cluster.map_shared_rank(&l_n, 0), s.cap);
-    int ev[kSlots / 32][3];
-#pragma unroll
-    for (int it = 0; it < kSlots / 32; ++it) {
-      const int e = it * 32 + lane;
-      const bool in = e < nsel;
-      ev[it][0] = in ? rsel[e] : -1;
-      ev[it][1] = in ? rslot[e] : 0;
-      ev[it][2] = in ? rnew[e] : 0;
-    }
-    int n_new = 0;
-#pragma unroll
-    for (int it = 0; it < kSlots / 32; ++it) {
-      const int e = it * 32 + lane;
-      n_new += __popc(__ballot_sync(0xffffffffu, e < nsel && ev[it][2]));
-    }
-    int seen_new = 0, seen_old = 0;
-#pragma unroll
-    for (int it = 0; it < kSlots / 32; ++it) {
-      const int e = it * 32 + lane;
-      const bool in = e < nsel;
-      const bool nw = in && ev[it][2];
-      const unsigned int bn = __ballot_sync(0xffffffffu, nw), bo = __ballot_sync(0xffffffffu, in && !nw);
-      const unsigned int below = (1u << lane) - 1u;
-      const int pos = nw ? seen_new + __popc(bn & below) : n_new + seen_old + __popc(bo & below);
-      seen_new += __popc(bn);
-      seen_old += __popc(bo);
-      if (in && pos % NW == wkr) {
-        const int i = pos / NW;
-        int slot = ev[it][1];
-        if (slot < 0 || slot >= s.cap) {
-          atomicOr(s.err, kErrBounds);
-          slot = 0;  // keep the copy in bounds; the result is flagged as invalid
-        }
-        w_blk[team][i] = ev[it][0];
-        w_slot[team][i] = slot;
-        w_new[team][i] = nw ? 1 : 0;
-      }
-    }
-    if (lane == 0) w_n[team] = wkr < nsel ? (nsel - wkr + NW - 1) / NW : 0;
+  // ---------------- a5-a6: every CTA selects (rank 0 also stores the unit's selection state)
+  // and keeps its workers' shares: position dp of the dealing order (blocks without a slot
+  // first) goes to worker dp % NW
+  cp_async_wait_all();  // the early copies (pooled s^e, slot map, eviction words)
+  if (tid < 2) {
+    const int b = nb_se + tid;
+    if (b < geo.ws) m.sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
   }
   __syncthreads();
+  const int NW = kTeams * CS, wkr = kTeams * rank + team;  // workers of the unit, this one
+  const int total_S = leader_select(s, u, geo, CS, m, sh, my_slot_blk, rank == 0,
+                                    [&](int pos, int b, int slot, bool isnew, int dp) {
+                                      const int w = dp % NW;
+                                      if (w / kTeams != rank || dp >= s.cap) return;
+                                      if (slot < 0 || slot >= s.cap) {
+                                        atomicOr(s.err, kErrBounds);
+                                        slot = 0;  // keep the copy in bounds; the result is flagged
+                                      }
+                                      const int t = w % kTeams, i = dp / NW;
+                                      w_blk[t][i] = b;
+                                      w_slot[t][i] = slot;
+                                      w_new[t][i] = isnew ? 1 : 0;
+                                    });
+  // a selection larger than the cache is an error (flagged by the selection): attend nothing
+  const int nsel = total_S <= s.cap ? total_S : 0;
+  const int my_n = wkr < nsel ? (nsel - wkr + NW - 1) / NW : 0;
+  __syncthreads();  // the workers' lists are complete
 
   WarpAcc A;
   A.init();
   const uint32_t sbase = smem_u32(smem) + (uint32_t)(team * nst * kStageBytes);
-  attend_worker(&tmap, s, geo, u, qb, w_blk[team], w_slot[team], w_new[team], w_n[team], sbase, bars[team], nst,
+  attend_worker(&tmap, s, geo, u, qb, w_blk[team], w_slot[team], w_new[team], my_n, sbase, bars[team], nst,
                 &sebuf[team][0][0], Team{kTeams == 1 ? 0u : 1u + (uint32_t)team}, ttid, A);
   __syncthreads();  // every copy has landed (or was drained): the stages can hold the warp partials
 

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_select_kernel(LayerState 
   cluster.sync();  // the local winners have landed in the leader; remote reads are done
   if (rank != 0) return;
   cp_async_wait_all();  // the leader's early copies (pooled s^e, slot map, eviction words)
-  leader_select(s, u, geo, CS, m, sh, my_slot_blk, LeaderLists{nullptr, nullptr, nullptr, nullptr});
+  leader_select(s, u, geo, CS, m, sh, my_slot_blk, true, NoDeal{});
 }
 
 size_t score_select_smem(const LayerState& s) { return region_bytes(s); }

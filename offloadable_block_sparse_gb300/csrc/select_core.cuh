@@ -204,13 +204,9 @@ __device__ __forceinline__ Smem layout(unsigned char* dsm, const LayerState& s) 
   return m;
 }
 
-// Where the leader also leaves the selection list for the CTAs of its cluster
-// (nullptr members: global memory only).
-struct LeaderLists {
-  int32_t* sel;
-  int32_t* slot;
-  int32_t* isnew;  // 1: to be copied from the host
-  int32_t* n;
+// A selection's consumer that takes nothing (the selection goes to global memory only).
+struct NoDeal {
+  __device__ __forceinline__ void operator()(int, int, int, bool, int) const {}
 };
 
 // q fragments for the scorer.  The k order in each 32-dim chunk is permuted
@@ -233,8 +229,8 @@ __device__ __forceinline__ int leader_prefetch(const LayerState& s, int u, int n
   float* sek = m.sek;
   int32_t* b2s = m.b2s;
   uint32_t* evw = m.evw;
-  // leader: request the selection's inputs now as asynchronous copies into shared
-  // memory; they land while the scoring runs (waited for before the selection)
+  // a selecting CTA requests the selection's inputs now as asynchronous copies into
+  // shared memory; they land while the scoring runs (waited for before the selection)
   const float* seg = s.se_blk + (size_t)u * s.nb_max;
   const int32_t* b2g = s.blk2slot + (size_t)u * s.nb_max;
   const uint32_t* evg = s.evicted + (size_t)u * s.ev_words;
@@ -430,9 +426,10 @@ __device__ __forceinline__ void pool_blocks(const LayerState& s, int u, const Ge
   __syncthreads();
 }
 
-// Phase 2b (right after phase 2): this CTA's k_q best candidate blocks to the leader.
+// Phase 2b (right after phase 2): this CTA's k_q best candidate blocks to the leader, or
+// with to_all to every CTA of the cluster (each then selects on its own).
 __device__ __forceinline__ void rank_local(const LayerState& s, const Geometry& geo, int rank, int CS,
-                                           const Smem& m, SelShared& sh) {
+                                           const Smem& m, SelShared& sh, bool to_all = false) {
   cg::cluster_group cluster = cg::this_cluster();
   const int tid = threadIdx.x;
   const int nb = geo.nb;
@@ -451,22 +448,22 @@ __device__ __forceinline__ void rank_local(const LayerState& s, const Geometry& 
     unsigned long long* lk = reinterpret_cast<unsigned long long*>(zs);  // z is no longer needed
     for (int i = tid; i < nown; i += blockDim.x) lk[i] = rank_key(keys[cb0 + i], cb0 + i);
     __syncthreads();
-    uint32_t* ckey = cluster.map_shared_rank(cand_key, 0);
-    int32_t* cblk = cluster.map_shared_rank(cand_blk, 0);
+    const int ndst = to_all ? CS : 1;
     for (int i = tid; i < nown && kq > 0; i += blockDim.x) {
       const unsigned long long ki = lk[i];
       const int r = count_larger(lk, nown, ki);
-      if (r < kq) {
-        ckey[rank * kq + r] = (uint32_t)(ki >> 32);
-        cblk[rank * kq + r] = cb0 + i;
-      }
+      if (r < kq)
+        for (int d = 0; d < ndst; ++d) {
+          cluster.map_shared_rank(cand_key, d)[rank * kq + r] = (uint32_t)(ki >> 32);
+          cluster.map_shared_rank(cand_blk, d)[rank * kq + r] = cb0 + i;
+        }
     }
-    if (tid == 0) *cluster.map_shared_rank(&sh.cand_n[rank], 0) = min(nown, max(kq, 0));
+    if (tid < ndst) *cluster.map_shared_rank(&sh.cand_n[rank], tid) = min(nown, max(kq, 0));
   }
 }
 
-// Phase 3a, leader only (after a cluster barrier and cp_async_wait_all): candidate
-// flags and the query-aware picks Q (flags F_Q).
+// Phase 3a, in a CTA holding every CTA's local winners (after a cluster barrier and
+// cp_async_wait_all): candidate flags and the query-aware picks Q (flags F_Q).
 __device__ __forceinline__ void leader_query(const LayerState& s, int u, const Geometry& geo, int CS,
                                              const Smem& m, SelShared& sh) {
   const int tid = threadIdx.x;
@@ -503,10 +500,15 @@ __device__ __forceinline__ void leader_query(const LayerState& s, int u, const G
   __syncthreads();
 }
 
-// Phase 3b, leader only: the query-agnostic picks E, the selection S, the eviction
-// update, slot assignment, fetch list, selection lists and statistics.
-__device__ __forceinline__ void leader_rest(const LayerState& s, int u, const Geometry& geo, const Smem& m,
-                                            SelShared& sh, int my_slot_blk, const LeaderLists& out) {
+// Phase 3b: the query-agnostic picks E, the selection S and the slots of its new blocks.
+// The writer (one CTA per unit) also stores the eviction update, slot tables, fetch list,
+// selection lists and statistics; every CTA that runs it on the same inputs reaches the
+// same selection.  deal(pos, b, slot, isnew, dp) is called for each selected block b at
+// list position pos < cap, with its slot (as published) and its dealing position dp: the
+// blocks without a slot first, then the rest, each in block order.  Returns |S|.
+template <typename Deal>
+__device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geometry& geo, const Smem& m,
+                                           SelShared& sh, int my_slot_blk, bool writer, Deal deal) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nb = geo.nb, ws = geo.ws;
   float* zs = m.zs;
@@ -573,7 +575,7 @@ __device__ __forceinline__ void leader_rest(const LayerState& s, int u, const Ge
     const int b = 32 * w + lane;
     const uint32_t bits =
         __ballot_sync(0xffffffffu, b < nb && (flags[b] & F_CAND) && !(flags[b] & (F_Q | F_E)));
-    if (lane == 0 && (bits & ~evw[w])) s.evicted[(size_t)u * s.ev_words + w] = evw[w] | bits;
+    if (writer && lane == 0 && (bits & ~evw[w])) s.evicted[(size_t)u * s.ev_words + w] = evw[w] | bits;
   }
   // one scan of three counts (each at most 256, 10 bits apiece): free slots (empty, or holding a
   // block that left the selection; ascending), blocks without a slot, and selected blocks
@@ -582,16 +584,17 @@ __device__ __forceinline__ void leader_rest(const LayerState& s, int u, const Ge
   int packed_total;
   const int packed = block_scan_excl(is_free | (nNew << 10) | (nS << 20), sh.scan, &packed_total);
   const int free_rank = packed & 1023, n_free = packed_total & 1023;
-  int new_rank = (packed >> 10) & 1023, n_new = (packed_total >> 10) & 1023;
+  const int new_before = (packed >> 10) & 1023, n_new_all = (packed_total >> 10) & 1023;
+  int new_rank = new_before, n_new = n_new_all;
   int pos = packed >> 20;
   const int total_S = packed_total >> 20;
   if (is_free) sh.free_by_rank[free_rank] = tid;
   if (n_new > n_free) {  // cannot happen when cap >= |S|; guard the slot table anyway
-    if (tid == 0) atomicOr(s.err, kErrBounds);
+    if (writer && tid == 0) atomicOr(s.err, kErrBounds);
     n_new = n_free;
   }
   int32_t* b2s_g = s.blk2slot + (size_t)u * s.nb_max;
-  if (is_free && my_slot_blk >= 0) {
+  if (writer && is_free && my_slot_blk >= 0) {
     if (my_slot_blk < s.nb_max) b2s_g[my_slot_blk] = -1;
     else atomicOr(s.err, kErrBounds);
   }
@@ -602,38 +605,43 @@ __device__ __forceinline__ void leader_rest(const LayerState& s, int u, const Ge
     if (new_rank < n_new) {
       const int slot = sh.free_by_rank[new_rank];
       b2s[b] = slot;
-      b2s_g[b] = slot;
-      sblk[slot] = b;
-      fl[2 * new_rank] = b;
-      fl[2 * new_rank + 1] = slot;
+      if (writer) {
+        b2s_g[b] = slot;
+        sblk[slot] = b;
+        fl[2 * new_rank] = b;
+        fl[2 * new_rank + 1] = slot;
+      }
     }
     ++new_rank;
   }
-  if (is_free && free_rank >= n_new) sblk[tid] = -1;
+  if (writer && is_free && free_rank >= n_new) sblk[tid] = -1;
   // ascending selection list with kinds, slots and the fetched marks (a thread's own blocks:
   // their slots were assigned just above by the same thread)
   int32_t* sel = s.sel + (size_t)u * s.cap;
   int32_t* kind = s.sel_kind + (size_t)u * s.cap;
   int32_t* sslot = s.sel_slot + (size_t)u * s.cap;
   int32_t* snew = s.sel_new + (size_t)u * s.cap;
+  int nw_before = new_before;  // blocks without a slot ahead of b in block order
   for (int b = lo; b < hi; ++b) {
     const uint8_t f = flags[b];
     if (!(f & F_S)) continue;
+    const bool isnew = f & F_NEW;
     if (pos < s.cap) {
-      sel[pos] = b;
-      kind[pos] = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
-      sslot[pos] = (s.test_bad_slot && u == 0 && pos == 0) ? s.cap : b2s[b];  // test hook
-      snew[pos] = (f & F_NEW) ? 1 : 0;
-      if (out.sel) {
-        out.sel[pos] = b;
-        out.slot[pos] = sslot[pos];
-        out.isnew[pos] = snew[pos];
+      const int slot = (s.test_bad_slot && u == 0 && pos == 0) ? s.cap : b2s[b];  // test hook
+      if (writer) {
+        sel[pos] = b;
+        kind[pos] = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
+        sslot[pos] = slot;
+        snew[pos] = isnew ? 1 : 0;
       }
-    } else {
+      deal(pos, b, slot, isnew, isnew ? nw_before : n_new_all + pos - nw_before);
+    } else if (writer) {
       atomicOr(s.err, kErrBounds);
     }
+    if (isnew) ++nw_before;
     ++pos;
   }
+  if (!writer) return total_S;
   for (int i = total_S + tid; i < s.cap; i += blockDim.x) {
     sel[i] = -1;
     kind[i] = -1;
@@ -661,7 +669,6 @@ __device__ __forceinline__ void leader_rest(const LayerState& s, int u, const Ge
     }
     const int sumD = t.x, sumDnew = t.y, sumE = t.z, had_prev = t.w > 0;
     s.n_sel[u] = min(total_S, s.cap);
-    if (out.sel) *out.n = min(total_S, s.cap);
     s.n_fetch[u] = n_new;
     s.gamma[2 * u] = sumD - sumDnew;
     s.gamma[2 * u + 1] = sumD;
@@ -676,15 +683,17 @@ __device__ __forceinline__ void leader_rest(const LayerState& s, int u, const Ge
       atomicMin(&s.stats->gamma_min_bits, __float_as_uint(gmm));
     }
   }
+  return total_S;
 }
 
-// Phase 3, leader only (after a cluster barrier and cp_async_wait_all): the selection,
-// eviction update, slot assignment, fetch list, selection lists and statistics.
-__device__ __forceinline__ void leader_select(const LayerState& s, int u, const Geometry& geo, int CS,
-                                              const Smem& m, SelShared& sh, int my_slot_blk,
-                                              const LeaderLists& out) {
+// Phase 3 (after a cluster barrier and cp_async_wait_all), in a CTA that holds every CTA's
+// local winners: the selection; the writer also stores its global state (leader_rest).
+template <typename Deal>
+__device__ __forceinline__ int leader_select(const LayerState& s, int u, const Geometry& geo, int CS,
+                                             const Smem& m, SelShared& sh, int my_slot_blk, bool writer,
+                                             Deal deal) {
   leader_query(s, u, geo, CS, m, sh);
-  leader_rest(s, u, geo, m, sh, my_slot_blk, out);
+  return leader_rest(s, u, geo, m, sh, my_slot_blk, writer, deal);
 }
 
 }  // namespace selcore
