@@ -2,9 +2,12 @@
 // eq. 8: attention of q over K[selected], V[selected]; NOSA-1B blog,
 // sparse_forward: attention over the top-k block indices only).
 //
-// grid (attend_chunks, U), 128 threads: one worker of the shared core (a team
-// of four warps, TMA ring over the block cache, host blocks by cp.async) per
-// CTA.  CTA (chunk, u) owns every attend_chunks-th entry of unit u's selection
+// grid (U, attend_chunks) — (attend_chunks, U) when a unit's CTAs form one cluster —
+// 128 threads: one worker of the shared core (a team of four warps, TMA ring over the
+// block cache, host blocks by cp.async) per CTA.  CTAs start in the order of their
+// linear index, so with chunks along y every unit's chunk 0 (which holds its first block
+// still on the host) starts in the first wave, then chunk 1, ...: the host-link copies of
+// all units are under way from the start rather than a wave at a time.  CTA (chunk, u) owns every attend_chunks-th entry of unit u's selection
 // (blocks still on the host first).  The four warps' (m, l, O) are merged in
 // shared memory into one partial per CTA; the unit's partials are then merged
 // through the cluster's distributed shared memory, by a merge kernel, or by the
@@ -39,7 +42,9 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   // [4 warps][8 heads][128] warp partials, aliasing the stages once every copy has landed
   float* wo = reinterpret_cast<float*>(smem);
 
-  const int chunk = blockIdx.x, u = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr bool kChunksAlongX = kMerge == kMergeCluster;
+  const int chunk = kChunksAlongX ? blockIdx.x : blockIdx.y, u = kChunksAlongX ? blockIdx.y : blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = s.G;
   // Everything is read after the wait (q, the context length, the selection): the previous
   // kernel may be the append that sets T, or the kernel that wrote q.  These loads and the
@@ -55,7 +60,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   // Work split: the unit's selected blocks are dealt round-robin to its CTAs in an
   // order that puts the blocks still to be copied from the host first, so those
   // few spread one per CTA and their copies start before anything else.
-  const int CS = gridDim.x;
+  const int CS = kChunksAlongX ? gridDim.x : gridDim.y;  // the unit's CTAs
   const int nblk = chunk < nsel ? (nsel - chunk + CS - 1) / CS : 0;
   if (warp == 0) {
     // one round trip: every entry's block, slot and fetched mark, requested with the count
@@ -287,8 +292,9 @@ cudaError_t init_attend() {
 template <int M, int S>
 static cudaError_t launch_attend_t(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,
                                    int fused_fetch, bool pdl, cudaStream_t st) {
-  return launch_ex(attend_kernel<M, S>, dim3(s.attend_chunks, s.U), dim3(kAttendThreads), attend_smem_bytes(S), st,
-                   pdl, M == kMergeCluster ? s.attend_chunks : 0, *tmap, s, q, out, fused_fetch);
+  const dim3 grid = M == kMergeCluster ? dim3(s.attend_chunks, s.U) : dim3(s.U, s.attend_chunks);
+  return launch_ex(attend_kernel<M, S>, grid, dim3(kAttendThreads), attend_smem_bytes(S), st, pdl,
+                   M == kMergeCluster ? s.attend_chunks : 0, *tmap, s, q, out, fused_fetch);
 }
 
 cudaError_t launch_attend(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, uint16_t* out,

@@ -115,6 +115,21 @@ def test_no_sink_no_window_query_aware_only(mode):
     assert log.unit_steps == 40
 
 
+@STEP_MODES
+def test_sparse_prefill_by_steps_from_one_token(mode):
+    # NOSA_S prefill: the eviction constraint is defined per step, so the selection for prompt
+    # position t is the decode selection at t; the prompt is fed one token at a time from a
+    # one-token context.  With k = 3 the selection turns sparse once the prompt passes 6 blocks
+    # (sink 1 + window 2 + k 3): the first complete windows, the first evictions and the window
+    # sliding over the budget all happen inside the prompt.
+    wl = syn.Workload("prefill", layers=1, batch=2, q_heads=16, kv_heads=2, context=1, k_q=1, k_e=2,
+                      window_tokens=128, steps=640)
+    log, stats = run(wl, wl.steps, flags=mode)
+    assert log.unit_steps == 640 * 4
+    assert log.gammas and min(log.gammas) >= 2 / 3 - 1e-6  # Theorem 2: gamma >= k_e / k
+    assert min(log.gammas) < 1.0  # the selection moved: blocks were dropped during the prompt
+
+
 def test_gather_cta_counts_agree():
     wl = syn.Workload("ctas", layers=1, batch=4, q_heads=16, kv_heads=2, context=4096, k_q=4, k_e=12,
                       window_tokens=256, steps=6, sigma=1.0)
