@@ -107,6 +107,10 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   score_windows<4>(s, u, geo.nc, rank, m, sh, qf);
   if (rank == CS - 1) __threadfence_system();  // the token's host-store row, copied by other CTAs below
   cluster.sync();  // every CTA's statistics are visible
+  // pooled s^e of the last two blocks (written by the append before the barrier above): loaded
+  // now, so that the load lands while the CTAs pool and rank
+  const int b_se = nb_se + tid;
+  const float se_patch = (tid < 2 && b_se < geo.ws) ? s.se_blk[(size_t)u * s.nb_max + b_se] : 0.f;
   pool_blocks(s, u, geo, rank, CS, m, sh);
   rank_local(s, geo, rank, CS, m, sh, true);
   cluster.sync();  // every CTA holds all local winners; the append's pooled s^e are visible
@@ -115,11 +119,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   // and keeps its workers' shares: position dp of the dealing order (blocks without a slot
   // first) goes to worker dp % NW
   cp_async_wait_all();  // the early copies (pooled s^e, slot map, eviction words)
-  if (tid < 2) {
-    const int b = nb_se + tid;
-    if (b < geo.ws) m.sek[b] = s.se_blk[(size_t)u * s.nb_max + b];
-  }
-  __syncthreads();
+  if (tid < 2 && b_se < geo.ws) m.sek[b_se] = se_patch;  // read by the selection after its first barrier
   const int NW = kTeams * CS, wkr = kTeams * rank + team;  // workers of the unit, this one
   const int total_S = leader_select(s, u, geo, CS, m, sh, my_slot_blk, rank == 0,
                                     [&](int pos, int b, int slot, bool isnew, int dp) {
