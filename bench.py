@@ -226,8 +226,9 @@ def run_native(args, rank, world, local_rank):
     U = B * Hkv
     K, W = args.steps, args.warmup
     n_time_leg = 0 if args.quick else 2 * min(K, 8)
-    n_e2e = 0 if args.quick else min(K, 16)
-    total_steps = 1 + W + K + n_time_leg + n_e2e
+    n_e2e = 0 if args.quick else min(K, 64)
+    n_e2e_warm = 6 if n_e2e else 0  # two untimed replays of each e2e graph (the first uploads it)
+    total_steps = 1 + W + K + n_time_leg + n_e2e_warm + n_e2e
     cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=wl.context + total_steps,
                         sink_blocks=wl.sink_blocks, evict_hidden=wl.evict_hidden, gather_ctas=args.gather_ctas,
@@ -427,7 +428,6 @@ def run_native(args, rank, world, local_rank):
     select_bytes = U * (nc * d * 2 + nb * 4 + G * d * 2)
     fetch_bytes_launch = fetched_split / max(n_time_leg // 2 * L, 1) * BLOCK_BYTES
     hbm, src = measured_peaks()
-    h2d = h2d_peak(torch)
     peak_src = f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"
     if step_kernels == 1:
         dominant, dom_bytes = "decode", attend_bytes + select_bytes
@@ -447,33 +447,28 @@ def run_native(args, rank, world, local_rank):
                           "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
                           "traffic_source": traffic_src, "algorithmic_bytes_per_launch": dom_bytes,
                           "avg_launch_us": us[dominant], "note": note}
-    fach = fetch_bytes_launch / (us["gather"] * 1e-6) / 1e9
-    result["fetch_roofline"] = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach,
-                                "peak": h2d, "unit": "GB/s", "frac": fach / h2d,
-                                "peak_source": "best pinned 1 GiB cudaMemcpyAsync H2D measured in this run",
-                                "bytes_per_launch": fetch_bytes_launch, "avg_launch_us": us["gather"],
-                                "note": "standalone nosa_fetch on the step's fetch list; the timed step fetches "
-                                        "inside attend instead"}
+    fach = fetch_bytes_launch / (us["gather"] * 1e-6) / 1e9  # its peak is measured after the e2e leg
     result["stages_us_per_layer"] = us
     sel_att_us = us["decode"] if step_kernels == 1 else us["attend"] + us["select"]
     result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / (sel_att_us * 1e-6) / 1e9 / hbm
 
-    # ---------------- e2e: the public host-pointer API (nosa_step_host), copies inside the timed region.
-    # Two CUDA graphs, each capturing the 28 layers' nosa_step_host calls on its own set of pinned
-    # host buffers, alternate: while one replays, the host writes the next step's inputs into the
-    # other set (after that set's previous replay has finished) and reads the step's outputs back.
+    # ---------------- e2e: the public host-pointer API (nosa_step_host_all: one copy of every layer's
+    # q, k, v to the device, the layers' steps, one copy of the outputs back), copies inside the timed
+    # region.  Three CUDA graphs, each capturing that call on its own set of pinned host buffers, take
+    # turns: while one replays, the host reads the outputs of the set that finished and writes the
+    # next step's inputs into it, up to two steps ahead of the device.
     e2e_graph = use_graph
+    n_sets = 3
     sets = [dict(q=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory(),
                  kv=torch.empty((2, L, B, Hkv, d), dtype=torch.bfloat16).pin_memory(),
-                 out=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
-    q_src = Qall[step_i[0]:step_i[0] + n_e2e].cpu()
-    kv_src = KVall[step_i[0]:step_i[0] + n_e2e].cpu()
-    outs_host = torch.empty((n_e2e, L, B, Hq, d), dtype=torch.bfloat16)
+                 out=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory()) for _ in range(n_sets)]
+    q_src = Qall[step_i[0]:step_i[0] + n_e2e_warm + n_e2e].cpu()
+    kv_src = KVall[step_i[0]:step_i[0] + n_e2e_warm + n_e2e].cpu()
+    outs_host = torch.zeros((n_e2e, L, B, Hq, d), dtype=torch.bfloat16)  # pages touched before the timing
 
     def host_step(bs):
-        for l in range(L):
-            N.nosa_step_host(ctx, l, bs["q"][l].view(i16), bs["kv"][0, l].view(i16), bs["kv"][1, l].view(i16),
-                             bs["out"][l].view(i16))
+        N.nosa_step_host_all(ctx, bs["q"].view(i16), bs["kv"][0].view(i16), bs["kv"][1].view(i16),
+                             bs["out"].view(i16))
 
     graphs_e2e = []
     if e2e_graph:
@@ -487,17 +482,31 @@ def run_native(args, rank, world, local_rank):
             graphs_e2e.append(g)
         N.nosa_set_stream(ctx, stream.cuda_stream)
         assert N.nosa_sync(ctx) == N.NOSA_OK
+    # untimed: two replays of each graph (its first launch uploads it), on real steps of the sequence
+    for j in range(n_e2e_warm):
+        bs = sets[j % n_sets]
+        bs["q"].copy_(q_src[j])
+        bs["kv"].copy_(kv_src[j])
+        if e2e_graph:
+            graphs_e2e[j % n_sets].replay()
+        else:
+            host_step(bs)
     torch.cuda.synchronize()
-    done = [None, None]
+    q_src, kv_src = q_src[n_e2e_warm:], kv_src[n_e2e_warm:]
+    step_i[0] += n_e2e_warm
+    done = [None] * n_sets
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     a.record(stream)
+    busy = 0.0  # host time outside the waits: copies and graph launches
     for j in range(n_e2e):
-        k = j % 2
+        k = j % n_sets
         bs = sets[k]
         if done[k] is not None:
             done[k].synchronize()                   # that set's previous step has finished
-            outs_host[j - 2].copy_(bs["out"])       # read its result back on the host
+        tb = time.perf_counter()
+        if done[k] is not None:
+            outs_host[j - n_sets].copy_(bs["out"])  # read its result back on the host
         bs["q"].copy_(q_src[j])
         bs["kv"].copy_(kv_src[j])
         if e2e_graph:
@@ -506,22 +515,35 @@ def run_native(args, rank, world, local_rank):
             host_step(bs)
         done[k] = torch.cuda.Event()
         done[k].record(stream)
+        busy += time.perf_counter() - tb
     b.record(stream)
     torch.cuda.synchronize()
-    for j in range(max(0, n_e2e - 2), n_e2e):
-        outs_host[j].copy_(sets[j % 2]["out"])
+    for j in range(max(0, n_e2e - n_sets), n_e2e):
+        outs_host[j].copy_(sets[j % n_sets]["out"])
     wall = time.perf_counter() - t0
     step_i[0] += n_e2e
-    e2e_ms = max(a.elapsed_time(b), wall * 1e3) / n_e2e
+    dev_ms, wall_ms = a.elapsed_time(b) / n_e2e, wall * 1e3 / n_e2e
+    e2e_ms = max(dev_ms, wall_ms)
     result["e2e"] = {"value": B / (e2e_ms * 1e-3), "unit": "tok/s", "ms_per_step": e2e_ms,
+                     "device_ms_per_step": dev_ms, "host_wall_ms_per_step": wall_ms,
+                     "host_busy_ms_per_step": busy * 1e3 / n_e2e, "steps": n_e2e,
                      "h2d_bytes_per_step": L * (B * Hq * d * 2 + 2 * U * d * 2),
                      "d2h_bytes_per_step": L * B * Hq * d * 2,
-                     "how": "nosa_step_host for every layer on pinned host q/k/v/out (the kernels read the inputs "
-                            "and write the outputs in place over the host link), outputs then copied out of the "
-                            "pinned buffers on the host; " + ("two alternating CUDA graphs of those calls"
+                     "how": "nosa_step_host_all on pinned host q/k/v/out (one host-to-device copy of every layer's "
+                            "inputs, the layers' steps, one device-to-host copy of the outputs), outputs then "
+                            "copied out of the pinned buffers on the host; " + ("three CUDA graphs of those calls "
+                                                                                "taking turns"
                                                             if e2e_graph else "eager calls") +
                             "; max of device-event and host wall time"}
     assert N.nosa_sync(ctx) == N.NOSA_OK
+    # the link's peak: a 1 GiB pinned copy, after the e2e leg (whose pinned buffers it would share)
+    h2d = h2d_peak(torch)
+    result["fetch_roofline"] = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach,
+                                "peak": h2d, "unit": "GB/s", "frac": fach / h2d,
+                                "peak_source": "best pinned 1 GiB cudaMemcpyAsync H2D measured in this run",
+                                "bytes_per_launch": fetch_bytes_launch, "avg_launch_us": us["gather"],
+                                "note": "standalone nosa_fetch on the step's fetch list; the timed step fetches "
+                                        "inside attend instead"}
     N.nosa_destroy(ctx)
     del Qall, KVall
     torch.cuda.empty_cache()

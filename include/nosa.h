@@ -217,6 +217,20 @@ nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_
 nosa_status nosa_step_host(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, uint16_t* out);
 
+/* One decode step of every layer from host buffers: q and out [L][B][Hq][d], k_new and
+ * v_new [L][B][Hkv][d], bf16, layer-major.  Copies q, k_new and v_new to
+ * context-owned device buffers (one cudaMemcpyAsync each), runs nosa_step for layers
+ * 0 .. L-1 in order on those, and copies every layer's output back (one
+ * cudaMemcpyAsync), all on the context's stream, so that the layers' kernels stay
+ * chained and no layer waits on the host link for its inputs.  Every layer is checked
+ * before anything is queued: on an error nothing runs and no state changes
+ * (NOSA_ERR_CAPACITY if any layer is full).  Page-locked buffers (cudaHostAlloc /
+ * cudaHostRegister) let the copies run asynchronously and be captured in a CUDA
+ * graph; pageable ones work outside a capture.  The buffers must stay untouched until
+ * the stream reaches the end of the step, when out is written. */
+nosa_status nosa_step_host_all(nosa_ctx* ctx, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                               uint16_t* out);
+
 /* SparDA-style forecast selection (SparDA summary: a forecast vector of layer l picks
  * layer l+1's blocks one layer ahead, so the copy of those blocks overlaps layer l's
  * work; one forecast head per kv head; sink and local blocks by position).  Selects

@@ -81,7 +81,8 @@ void free_ctx(nosa_ctx* c) {
   void* dev[] = {c->cache, c->kt, c->kring, c->se_tok, c->se_win, c->se_blk, c->W1, c->W2, c->slot_blk,
                  c->blk2slot, c->sel, c->sel_kind, c->sel_slot, c->sel_new, c->n_sel, c->fetch, c->n_fetch, c->gamma,
                  c->evicted, c->T, c->err, c->stats, c->sq_blk, c->apart, c->tickets,
-                 c->stage_q, c->stage_k, c->stage_v, c->stage_out, c->bulk_k, c->bulk_v};
+                 c->stage_q, c->stage_k, c->stage_v, c->stage_out, c->bulk_k, c->bulk_v,
+                 c->step_q, c->step_k, c->step_v, c->step_out};
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_kv) cudaFreeHost(c->host_kv);
@@ -379,6 +380,10 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   dalloc(&c->apart, (size_t)c->U * c->attend_chunks * kMaxGroup * kPartStride * 4);
   dalloc(&c->tickets, (3 * (size_t)c->U + 1) * 4);
   dalloc(&c->stage_q, (size_t)c->B * c->Hq * kHeadDim * 2);
+  dalloc(&c->step_q, (size_t)c->L * c->B * c->Hq * kHeadDim * 2);
+  dalloc(&c->step_out, (size_t)c->L * c->B * c->Hq * kHeadDim * 2);
+  dalloc(&c->step_k, (size_t)c->L * c->U * kHeadDim * 2);
+  dalloc(&c->step_v, (size_t)c->L * c->U * kHeadDim * 2);
   dalloc(&c->stage_out, (size_t)c->B * c->Hq * kHeadDim * 2);
   dalloc(&c->stage_k, (size_t)c->U * kHeadDim * 2);
   dalloc(&c->stage_v, (size_t)c->U * kHeadDim * 2);
@@ -674,6 +679,27 @@ nosa_status nosa_step_host(nosa_ctx* c, int layer, const uint16_t* q, const uint
   st = nosa_step(c, layer, c->stage_q, c->stage_k, c->stage_v, c->stage_out);
   if (st != NOSA_OK) return st;
   CK(cudaMemcpyAsync(out, c->stage_out, qbytes, cudaMemcpyDeviceToHost, c->stream));
+  return NOSA_OK;
+}
+
+nosa_status nosa_step_host_all(nosa_ctx* c, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                               uint16_t* out) {
+  if (!c || !q || !k_new || !v_new || !out) return NOSA_ERR_INVALID_ARG;
+  for (int l = 0; l < c->L; ++l) {  // everything nosa_step checks, for every layer, before anything runs
+    const nosa_status st = check_ctx(c, l);
+    if (st != NOSA_OK) return st;
+    if (c->T_host[l] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
+  }
+  const size_t qL = (size_t)c->B * c->Hq * kHeadDim, kvL = (size_t)c->U * kHeadDim;  // elements per layer
+  CK(cudaMemcpyAsync(c->step_q, q, c->L * qL * 2, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->step_k, k_new, c->L * kvL * 2, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->step_v, v_new, c->L * kvL * 2, cudaMemcpyHostToDevice, c->stream));
+  for (int l = 0; l < c->L; ++l) {
+    const nosa_status st = nosa_step(c, l, c->step_q + l * qL, c->step_k + l * kvL, c->step_v + l * kvL,
+                                     c->step_out + l * qL);
+    if (st != NOSA_OK) return st;
+  }
+  CK(cudaMemcpyAsync(out, c->step_out, c->L * qL * 2, cudaMemcpyDeviceToHost, c->stream));
   return NOSA_OK;
 }
 

@@ -147,6 +147,7 @@ struct nosa_ctx {
   int dec_cs, dec_wpc, dec_nst, dec_teams;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
+  uint16_t *step_q, *step_k, *step_v, *step_out;  // every layer's inputs and outputs (nosa_step_host_all)
   size_t stage_tok_cap;   // tokens per unit the bulk staging buffers hold
   uint16_t *bulk_k, *bulk_v;
   // TMA descriptor of the block cache (4-D: d, token, K/V, flat slot)

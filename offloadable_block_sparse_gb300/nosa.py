@@ -26,7 +26,7 @@ NOSA_F_DMA_BIAS = 8
 # every entry point declared in include/nosa.h
 EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_destroy", "nosa_set_stream",
            "nosa_set_eviction_head", "nosa_append_kv", "nosa_select", "nosa_fetch", "nosa_attend", "nosa_step",
-           "nosa_step_host", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
+           "nosa_step_host", "nosa_step_host_all", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
            "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string",
            "nosa_attend_noalloc", "nosa_step_plan", "nosa_forecast_select", "nosa_step_forecast",
            "nosa_forecast_join", "nosa_dense_attend", "nosa_dense_scratch_bytes"]
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "nosa_attend": [vp, i32, p, p],
             "nosa_step": [vp, i32, p, p, p, p],
             "nosa_step_host": [vp, i32, p, p, p, p],
+            "nosa_step_host_all": [vp, p, p, p, p],
             "nosa_sync": [vp],
             "nosa_forecast_select": [vp, i32, p],
             "nosa_step_forecast": [vp, i32, p, p, p, p, p, i32],
@@ -203,6 +204,11 @@ def nosa_step(ctx, layer, q, k_new, v_new, out) -> None:
 
 def nosa_step_host(ctx, layer, q, k_new, v_new, out) -> None:
     _check(lib().nosa_step_host(ctx, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)), "nosa_step_host")
+
+
+def nosa_step_host_all(ctx, q, k_new, v_new, out) -> None:
+    """Every layer's step from host buffers: q/out [L][B][Hq][d], k_new/v_new [L][B][Hkv][d]."""
+    _check(lib().nosa_step_host_all(ctx, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out)), "nosa_step_host_all")
 
 
 def nosa_forecast_select(ctx, layer, f) -> None:

@@ -256,6 +256,55 @@ def test_host_pointer_step_matches_device_step():
             p.close()
 
 
+@pytest.mark.parametrize("pin", [True, False], ids=["page-locked", "pageable"])
+def test_whole_step_host_call_matches_per_layer_steps(pin):
+    # nosa_step_host_all copies every layer's inputs at once, runs the layers and copies the
+    # outputs back: the same outputs and state as nosa_step per layer on device inputs.  The
+    # workload's capacity is context + steps, so the call after the last step is refused.
+    wl = syn.Workload("host_all", layers=3, batch=3, q_heads=16, kv_heads=2, context=1500, k_q=4, k_e=12,
+                      window_tokens=256, steps=5)
+    ps = [Parity(wl, sample_units=[]) for _ in range(2)]
+    try:
+        for p in ps:
+            p.load_context()
+        gen = torch.Generator(device="cuda").manual_seed(78)
+        L, B, Hq, Hkv = wl.layers, wl.batch, wl.q_heads, wl.kv_heads
+        for t in range(wl.steps):
+            q = torch.randn((L, B, Hq, 128), generator=gen, device="cuda")
+            q = (q / q.norm(dim=-1, keepdim=True) * math.sqrt(128)).to(torch.bfloat16)
+            k = torch.randn((L, B, Hkv, 128), generator=gen, device="cuda").to(torch.bfloat16)
+            v = torch.randn((L, B, Hkv, 128), generator=gen, device="cuda").to(torch.bfloat16)
+            out_d = torch.empty_like(q)
+            for l in range(L):
+                N.nosa_step(ps[0].ctx, l, q[l].view(torch.int16), k[l].view(torch.int16), v[l].view(torch.int16),
+                            out_d[l].view(torch.int16))
+            hq, hk, hv = (x.cpu() for x in (q, k, v))
+            ho = torch.full_like(hq, float("nan"))
+            if pin:
+                hq, hk, hv, ho = hq.pin_memory(), hk.pin_memory(), hv.pin_memory(), ho.pin_memory()
+            N.nosa_step_host_all(ps[1].ctx, hq.view(torch.int16), hk.view(torch.int16), hv.view(torch.int16),
+                                 ho.view(torch.int16))
+            for p in ps:
+                assert N.nosa_sync(p.ctx) == N.NOSA_OK
+            assert torch.equal(ho.view(torch.int16), out_d.cpu().view(torch.int16)), f"step {t}"
+        for l in range(L):
+            a, b = ps[0]._export(l), ps[1]._export(l)
+            for key in ("sel", "sel_slot", "slot_blk", "evicted", "n_sel"):
+                assert np.array_equal(a[key], b[key]), (l, key)
+        T_before = [N.nosa_context_length(ps[1].ctx, l) for l in range(L)]
+        hq = torch.zeros((L, B, Hq, 128), dtype=torch.bfloat16)
+        hk = torch.zeros((L, B, Hkv, 128), dtype=torch.bfloat16)
+        ho = torch.zeros_like(hq)
+        with pytest.raises(N.NosaError) as e:
+            N.nosa_step_host_all(ps[1].ctx, hq.view(torch.int16), hk.view(torch.int16), hk.view(torch.int16),
+                                 ho.view(torch.int16))
+        assert e.value.status == N.NOSA_ERR_CAPACITY
+        assert [N.nosa_context_length(ps[1].ctx, l) for l in range(L)] == T_before
+    finally:
+        for p in ps:
+            p.close()
+
+
 # ----------------------------------------------------------------------------- forecast (SparDA)
 @pytest.mark.parametrize("separate_fetch", [True, False], ids=["prefetch", "attend-fetches"])
 def test_forecast_selection_every_step(separate_fetch):
