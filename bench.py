@@ -366,7 +366,8 @@ def run_native(args, rank, world, local_rank):
                          "selection": "forecast one layer ahead, overlapped prefetch" if fc else "query (per step)",
                          "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache "
                                "(L2 is 129 MB)"},
-              "gpu_launches": (4 if fc else step_kernels) * L * K,
+              # forecast: forecast select and gather (prefetch stream), append, attention, merge
+              "gpu_launches": (5 if fc else step_kernels) * L * K,
               "clocks": ck,
               "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min, "bound": wl.k_e / (wl.k_q + wl.k_e)},
               "fetch_blocks_per_step": fetched_per_step,
@@ -375,8 +376,8 @@ def run_native(args, rank, world, local_rank):
         if fc:
             result["roofline"] = None
             result["e2e"] = None
-            result["note"] = ("forecast mode: timed graph leg only (4 kernels per layer: forecast select and "
-                              "gather on the prefetch stream, append and attend on the step stream)")
+            result["note"] = ("forecast mode: timed graph leg only (5 kernels per layer: forecast select and "
+                              "gather on the prefetch stream, append, attention and its merge on the step stream)")
         N.nosa_destroy(ctx)
         return result
 

@@ -276,9 +276,12 @@ nosa_status nosa_dense_attend(const uint16_t* q, const uint16_t* kv, int units, 
 /* Scratch bytes nosa_dense_attend needs (0 on a bad argument or without a device). */
 size_t nosa_dense_scratch_bytes(int units, int context_len);
 
-/* How nosa_step runs on this context: *kernels_per_layer = 1 (the fused decode
- * kernel, one thread-block cluster of *cluster_size CTAs per unit) or 3 (append,
- * select and attend kernels; *cluster_size = 0).  Either pointer may be NULL. */
+/* How nosa_step runs on this context: *kernels_per_layer = the kernel launches of
+ * one layer's step: 1 (the fused decode kernel, one thread-block cluster of
+ * *cluster_size CTAs per unit), or 3 (the selector kernel, which also appends the
+ * token, the attention kernel and the kernel merging its split-K partials;
+ * *cluster_size = 0) — 2 when the attention merges its partials itself.  Either
+ * pointer may be NULL. */
 nosa_status nosa_step_plan(nosa_ctx* ctx, int32_t* kernels_per_layer, int32_t* cluster_size);
 
 /* Wait for the stream; report and latch any device-side error. */

@@ -640,8 +640,7 @@ nosa_status nosa_step(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t*
                      c->stream));
   } else {
     const LayerState s = layer_state(c, layer);
-    CK(launch_append_one(s, k_new, v_new, true, c->stream));
-    CK(launch_score_select(s, q, true, c->stream));
+    CK(launch_score_select(s, q, true, c->stream, 0, k_new, v_new));  // appends the token first
     CK(launch_attend(s, &c->tmap_cache, q, out, 1, true, c->stream));  // the fetch runs inside attend
   }
   c->T_host[layer] += 1;
@@ -705,7 +704,8 @@ nosa_status nosa_step_host_all(nosa_ctx* c, const uint16_t* q, const uint16_t* k
 
 nosa_status nosa_step_plan(nosa_ctx* c, int32_t* kernels_per_layer, int32_t* cluster_size) {
   if (!c) return NOSA_ERR_INVALID_ARG;
-  if (kernels_per_layer) *kernels_per_layer = c->dec_cs > 0 ? 1 : 3;
+  // fused: one kernel; else the selector (which appends) and the attention, plus the merge kernel
+  if (kernels_per_layer) *kernels_per_layer = c->dec_cs > 0 ? 1 : (c->attend_mode == 2 ? 3 : 2);
   if (cluster_size) *cluster_size = c->dec_cs;
   return NOSA_OK;
 }

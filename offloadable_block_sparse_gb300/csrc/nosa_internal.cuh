@@ -203,7 +203,9 @@ cudaError_t launch_append_one(const LayerState& s, const uint16_t* k, const uint
 cudaError_t launch_append_bulk(const LayerState& s, const uint16_t* k, const uint16_t* v, int T_old,
                                int n, cudaStream_t st);
 // ahead = 1: forecast selection / its gather, made before the next token is appended
-cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, bool pdl, cudaStream_t st, int ahead = 0);
+// knew/vnew (ahead 0 only): the kernel also appends the step's token (the step path).
+cudaError_t launch_score_select(const LayerState& s, const uint16_t* q, bool pdl, cudaStream_t st, int ahead = 0,
+                                const uint16_t* knew = nullptr, const uint16_t* vnew = nullptr);
 cudaError_t launch_gather(const LayerState& s, int ctas, cudaStream_t st, int ahead = 0);
 // fused_fetch != 0: blocks marked in sel_new are copied from the pinned host
 // store by the attend CTAs themselves (and written back to their slots), so no
