@@ -8,7 +8,7 @@
 #include <algorithm>
 #include <new>
 
-#include "nosa_internal.cuh"
+#include "host.h"
 
 using namespace nosa;
 

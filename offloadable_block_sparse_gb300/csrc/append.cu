@@ -6,6 +6,7 @@
 // kernel 32, stride 16) and the window mean of s^e, max-pooled onto the
 // 64-token blocks the window overlaps (explainer eq. 5-6).
 #include "append_core.cuh"
+#include "host.h"
 
 namespace nosa {
 

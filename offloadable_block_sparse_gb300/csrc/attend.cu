@@ -15,6 +15,7 @@
 #include <cooperative_groups.h>
 
 #include "attend_core.cuh"
+#include "host.h"
 
 namespace cg = cooperative_groups;
 

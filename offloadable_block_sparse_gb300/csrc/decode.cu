@@ -29,6 +29,7 @@
 
 #include "append_core.cuh"
 #include "attend_core.cuh"
+#include "host.h"
 #include "select_core.cuh"
 
 namespace nosa {

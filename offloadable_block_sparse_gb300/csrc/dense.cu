@@ -12,6 +12,7 @@
 #include <algorithm>
 
 #include "attend_core.cuh"
+#include "host.h"
 
 namespace nosa {
 

@@ -10,7 +10,7 @@
 // end of the partial tail block are written as zeros.  ahead = 1: the list comes from a
 // forecast selection for T + 1 and may name the block the next token starts, which has no
 // rows yet (all zeros here; the append writes its first row into the slot).
-#include "nosa_internal.cuh"
+#include "host.h"
 #include "ptx.cuh"
 
 namespace nosa {

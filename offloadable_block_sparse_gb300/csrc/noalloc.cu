@@ -14,7 +14,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "nosa_internal.cuh"
+#include "host.h"
 
 namespace {
 

@@ -2,6 +2,7 @@
 // the fused decode kernel) composed with cluster barriers between them; in a step
 // (nosa_step) it also runs a1, the append of the token, as the fused kernel does.
 #include "append_core.cuh"
+#include "host.h"
 #include "select_core.cuh"
 
 namespace nosa {
