@@ -78,11 +78,13 @@ typedef enum {
  *                        it and NOSA_ERR_BOUNDS is latched. */
 #define NOSA_F_TEST_ZERO_WAIT 1u
 #define NOSA_F_TEST_BAD_SLOT 2u
-/* NOSA_F_UNFUSED_STEP: nosa_step launches three kernels (append, select, attend
- * with the fetch inside) instead of the fused one-kernel decode step.  Same
- * selections; the attention's split-K partition differs, so outputs may differ
- * in the last bits.  The fused kernel is also skipped when the device cannot
- * schedule its thread-block clusters. */
+/* NOSA_F_UNFUSED_STEP: nosa_step launches the selector (which appends the token
+ * first), the attention (with the fetch inside) and the merge of its split-K
+ * partials instead of the fused one-kernel decode step.  Same selections; the
+ * attention's split-K partition differs, so outputs may differ in the last bits.
+ * The fused kernel is also skipped when the device cannot schedule all units'
+ * thread-block clusters at once or the cache has more slots than a CTA has
+ * threads. */
 #define NOSA_F_UNFUSED_STEP 4u
 /* NOSA_F_DMA_BIAS: the attention adds each attended token's eviction score s^e_j
  * to its scaled logit, softmax_j(q.k_j / sqrt(d) + s^e_j): the additive attention
@@ -203,8 +205,12 @@ nosa_status nosa_fetch(nosa_ctx* ctx, int layer);
  * to their cache slots), so no separate gather pass is needed. */
 nosa_status nosa_attend(nosa_ctx* ctx, int layer, const uint16_t* q, uint16_t* out);
 
-/* append(1 token) + select + attend with the fetch fused into attend (three
- * kernels).  k_new, v_new: device bf16 [B][Hkv][d]; q, out: device bf16 [B][Hq][d]. */
+/* One decode step of `layer`: append the token (k_new, v_new), score and select,
+ * fetch the new blocks and attend with q, as one fused kernel or a short kernel
+ * chain (nosa_step_plan says which); the same selections and state as
+ * nosa_append_kv + nosa_select + nosa_attend.  k_new, v_new: device bf16
+ * [B][Hkv][d]; q, out: device bf16 [B][Hq][d].  NOSA_ERR_CAPACITY (nothing queued)
+ * when the layer's context is full. */
 nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                       const uint16_t* v_new, uint16_t* out);
 
