@@ -249,13 +249,15 @@ nosa_status nosa_forecast_select(nosa_ctx* ctx, int layer, const uint16_t* f);
 
 /* Pipelined forecast step of `layer` (needs a forecast selection for this token, from
  * nosa_forecast_select or an earlier nosa_step_forecast).  If f_next is not NULL it
- * first starts, on the context's own prefetch stream, the forecast selection of
- * next_layer (!= layer) with f_next and the copy of its new blocks; then, on the
- * context's stream, waits for this layer's prefetch (if one was started by an earlier
- * call), appends k_new/v_new and attends with q.  The prefetch stream forks from and
- * joins the context's stream through events, so a CUDA graph capture of a sequence of
- * calls stays one graph; call nosa_forecast_join before ending a capture.  Pointers as
- * in nosa_step; f_next: device bf16 [B][Hkv][d]. */
+ * first starts, on the context's own streams, the forecast selection of next_layer
+ * (!= layer) with f_next and, after it, the copy of its new blocks (the selection on
+ * a selection stream, the copy on a prefetch stream, so that one layer's selection
+ * overlaps the previous layer's copy); then, on the context's stream, waits for this
+ * layer's prefetch (if one was started by an earlier call), appends k_new/v_new and
+ * attends with q.  Those streams fork from and join the context's stream through
+ * events, so a CUDA graph capture of a sequence of calls stays one graph; call
+ * nosa_forecast_join before ending a capture.  Pointers as in nosa_step; f_next:
+ * device bf16 [B][Hkv][d]. */
 nosa_status nosa_step_forecast(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                                const uint16_t* v_new, uint16_t* out, const uint16_t* f_next, int next_layer);
 

@@ -86,10 +86,13 @@ void free_ctx(nosa_ctx* c) {
   for (void* p : dev)
     if (p) cudaFree(p);
   if (c->host_kv) cudaFreeHost(c->host_kv);
+  for (cudaEvent_t e : c->ev_sel)
+    if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : c->ev_pref)
     if (e) cudaEventDestroy(e);
   if (c->ev_fork) cudaEventDestroy(c->ev_fork);
   if (c->pref_stream) cudaStreamDestroy(c->pref_stream);
+  if (c->sel_stream) cudaStreamDestroy(c->sel_stream);
   delete c;
 }
 
@@ -257,6 +260,11 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->T_host.assign(c->L, 0);
   c->sel_T.assign(c->L, -1);
   c->ev_pref.assign(c->L, nullptr);
+  c->ev_sel.assign(c->L, nullptr);
+  // forecast pipeline: the selections on their own stream (NOSA_FORECAST_STREAMS=1: one prefetch
+  // stream for selections and gathers, in order)
+  c->forecast_split = 1;
+  if (const char* e = getenv("NOSA_FORECAST_STREAMS")) c->forecast_split = atoi(e) != 1;
   c->pref_pending.assign(c->L, 0);
   c->fetch_T.assign(c->L, -1);
 
@@ -457,9 +465,11 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   }
   // forecast pipeline: a prefetch stream and its events
   bool ev_ok = cudaStreamCreateWithFlags(&c->pref_stream, cudaStreamNonBlocking) == cudaSuccess &&
+               cudaStreamCreateWithFlags(&c->sel_stream, cudaStreamNonBlocking) == cudaSuccess &&
                cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
   for (int l = 0; l < c->L && ev_ok; ++l)
-    ev_ok = cudaEventCreateWithFlags(&c->ev_pref[l], cudaEventDisableTiming) == cudaSuccess;
+    ev_ok = cudaEventCreateWithFlags(&c->ev_pref[l], cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&c->ev_sel[l], cudaEventDisableTiming) == cudaSuccess;
   if (!ev_ok) {
     (void)cudaGetLastError();
     free_ctx(c);
@@ -472,6 +482,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
 nosa_status nosa_destroy(nosa_ctx* c) {
   if (!c) return NOSA_OK;
   if (c->pref_stream) cudaStreamSynchronize(c->pref_stream);
+  if (c->sel_stream) cudaStreamSynchronize(c->sel_stream);
   cudaStreamSynchronize(c->stream);
   (void)cudaGetLastError();
   free_ctx(c);
@@ -587,10 +598,17 @@ nosa_status nosa_step_forecast(nosa_ctx* c, int layer, const uint16_t* q, const 
     if (c->sel_T[next_layer] == c->T_host[next_layer] + 1) return NOSA_ERR_STATE;
     if (c->T_host[next_layer] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
     // the next layer's state was last written by work already queued on the step stream
+    // the selection on its own stream, the gather after it on the prefetch stream: the next
+    // call's selection (another layer) need not wait for this gather
+    cudaStream_t ss = c->forecast_split ? c->sel_stream : c->pref_stream;
     CK(cudaEventRecord(c->ev_fork, c->stream));
-    CK(cudaStreamWaitEvent(c->pref_stream, c->ev_fork, 0));
-    st = forecast_select_on(c, next_layer, f_next, c->pref_stream);
+    CK(cudaStreamWaitEvent(ss, c->ev_fork, 0));
+    st = forecast_select_on(c, next_layer, f_next, ss);
     if (st != NOSA_OK) return st;
+    if (c->forecast_split) {
+      CK(cudaEventRecord(c->ev_sel[next_layer], c->sel_stream));
+      CK(cudaStreamWaitEvent(c->pref_stream, c->ev_sel[next_layer], 0));
+    }
     CK(launch_gather(layer_state(c, next_layer), c->gather_ctas, c->pref_stream, 1));
     c->fetch_T[next_layer] = c->sel_T[next_layer];
     CK(cudaEventRecord(c->ev_pref[next_layer], c->pref_stream));
@@ -712,6 +730,7 @@ nosa_status nosa_step_plan(nosa_ctx* c, int32_t* kernels_per_layer, int32_t* clu
 
 nosa_status nosa_sync(nosa_ctx* c) {
   if (!c) return NOSA_ERR_INVALID_ARG;
+  CK(cudaStreamSynchronize(c->sel_stream));
   CK(cudaStreamSynchronize(c->pref_stream));
   CK(cudaStreamSynchronize(c->stream));
   int e = 0;

@@ -43,9 +43,12 @@ struct nosa_ctx {
   int failed;               // latched nosa_status of a device-side error
   // forecast pipeline: prefetch stream, fork event, one "prefetched" event per layer and whether
   // the layer's stream still has to wait for it
-  cudaStream_t pref_stream;
+  cudaStream_t pref_stream;  // the forecast gathers
+  cudaStream_t sel_stream;   // the forecast selections (a layer's overlaps the previous layer's gather)
+  int forecast_split;        // 1: selections on sel_stream; 0: selections and gathers in order on pref_stream
   cudaEvent_t ev_fork;
-  std::vector<cudaEvent_t> ev_pref;
+  std::vector<cudaEvent_t> ev_pref;  // per layer: its forecast gather is done
+  std::vector<cudaEvent_t> ev_sel;   // per layer: its forecast selection is done
   std::vector<char> pref_pending;
 };
 
