@@ -34,6 +34,9 @@
  *   * Pointers marked "device" must be device (or managed) memory and must stay
  *     valid until the stream reaches the call; "host" pointers are read or
  *     written before the call returns unless stated otherwise.
+ *   * A context is not thread-safe: its calls come from one host thread at a
+ *     time (or are serialised by the caller).  Different contexts are
+ *     independent, except the file-scope scratch of nosa_attend_noalloc.
  *   * bf16 tensors are passed as uint16_t bit patterns.
  *   * Units: a unit is one (sequence b, kv head g) of one layer; within a layer
  *     units are ordered u = b * num_kv_heads + g.  GQA: q head h uses kv head
