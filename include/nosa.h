@@ -264,7 +264,10 @@ nosa_status nosa_forecast_select(nosa_ctx* ctx, int layer, const uint16_t* f);
 nosa_status nosa_step_forecast(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                                const uint16_t* v_new, uint16_t* out, const uint16_t* f_next, int next_layer);
 
-/* Makes the context's stream wait for every prefetch started by nosa_step_forecast. */
+/* Makes the context's stream wait for every prefetch started by nosa_step_forecast.
+ * (Every entry point that works on a layer also waits for that layer's pending
+ * prefetch first, and the calls that read or reset state wait for all of the
+ * context's streams, so the forecast and plain entry points may be mixed.) */
 nosa_status nosa_forecast_join(nosa_ctx* ctx);
 
 /* Dense GQA decode attention over a device-resident KV store: the full-attention

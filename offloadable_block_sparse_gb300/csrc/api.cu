@@ -495,12 +495,31 @@ nosa_status nosa_set_stream(nosa_ctx* c, void* stream) {
   return NOSA_OK;
 }
 
+// A forecast gather started for `layer` on the prefetch stream finishes before the context's
+// stream touches that layer's state again (calls may mix the forecast and plain entry points).
+static nosa_status join_layer(nosa_ctx* c, int layer) {
+  if (c->pref_pending[layer]) {
+    CK(cudaStreamWaitEvent(c->stream, c->ev_pref[layer], 0));
+    c->pref_pending[layer] = 0;
+  }
+  return NOSA_OK;
+}
+
+// Everything queued on the context's streams (step, forecast selections, forecast gathers) is done.
+static nosa_status sync_all(nosa_ctx* c) {
+  CK(cudaStreamSynchronize(c->sel_stream));
+  CK(cudaStreamSynchronize(c->pref_stream));
+  CK(cudaStreamSynchronize(c->stream));
+  return NOSA_OK;
+}
+
 nosa_status nosa_set_eviction_head(nosa_ctx* c, int layer, const float* W1, const float* W2) {
   nosa_status st = check_ctx(c, layer);
   if (st != NOSA_OK) return st;
   if (!W1 || !W2) return NOSA_ERR_INVALID_ARG;
   const size_t n1 = (size_t)c->Hkv * kHeadDim * c->h, n2 = (size_t)c->Hkv * c->h;
-  CK(cudaStreamSynchronize(c->stream));
+  st = sync_all(c);
+  if (st != NOSA_OK) return st;
   CK(cudaMemcpy(c->W1 + layer * n1, W1, n1 * 4, cudaMemcpyHostToDevice));
   CK(cudaMemcpy(c->W2 + layer * n2, W2, n2 * 4, cudaMemcpyHostToDevice));
   return NOSA_OK;
@@ -511,6 +530,8 @@ nosa_status nosa_append_kv(nosa_ctx* c, int layer, const uint16_t* k, const uint
   if (st != NOSA_OK) return st;
   if (!k || !v || n < 1) return NOSA_ERR_INVALID_ARG;
   if ((long long)c->T_host[layer] + n > c->cfg.max_context) return NOSA_ERR_CAPACITY;
+  st = join_layer(c, layer);
+  if (st != NOSA_OK) return st;
   const LayerState s = layer_state(c, layer);
   const size_t row = kHeadDim * 2;
   if (n == 1) {
@@ -544,6 +565,8 @@ nosa_status nosa_select(nosa_ctx* c, int layer, const uint16_t* q, int32_t* sel_
   if (st != NOSA_OK) return st;
   if (!q) return NOSA_ERR_INVALID_ARG;
   if (c->T_host[layer] < 1) return NOSA_ERR_STATE;
+  st = join_layer(c, layer);
+  if (st != NOSA_OK) return st;
   const LayerState s = layer_state(c, layer);
   CK(launch_score_select(s, q, true, c->stream));
   if (sel_out) {
@@ -563,6 +586,8 @@ nosa_status nosa_fetch(nosa_ctx* c, int layer) {
   if (st != NOSA_OK) return st;
   const int ahead = c->sel_T[layer] - c->T_host[layer];  // 1 after a forecast selection
   if (ahead != 0 && ahead != 1) return NOSA_ERR_STATE;
+  st = join_layer(c, layer);
+  if (st != NOSA_OK) return st;
   CK(launch_gather(layer_state(c, layer), c->gather_ctas, c->stream, ahead));
   c->fetch_T[layer] = c->sel_T[layer];
   return NOSA_OK;
@@ -641,6 +666,8 @@ nosa_status nosa_attend(nosa_ctx* c, int layer, const uint16_t* q, uint16_t* out
   if (st != NOSA_OK) return st;
   if (!q || !out) return NOSA_ERR_INVALID_ARG;
   if (c->sel_T[layer] != c->T_host[layer]) return NOSA_ERR_STATE;
+  st = join_layer(c, layer);
+  if (st != NOSA_OK) return st;
   // without a nosa_fetch since the selection, the attend CTAs fetch the new blocks themselves
   const int fused = c->fetch_T[layer] != c->T_host[layer];
   CK(launch_attend(layer_state(c, layer), &c->tmap_cache, q, out, fused, true, c->stream));
@@ -653,6 +680,8 @@ nosa_status nosa_step(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t*
   if (st != NOSA_OK) return st;
   if (!q || !k_new || !v_new || !out) return NOSA_ERR_INVALID_ARG;
   if (c->T_host[layer] + 1 > c->cfg.max_context) return NOSA_ERR_CAPACITY;
+  st = join_layer(c, layer);
+  if (st != NOSA_OK) return st;
   if (c->dec_cs > 0) {  // one fused kernel
     CK(launch_decode(decode_state(c, layer), &c->tmap_cache, q, k_new, v_new, out, c->dec_teams, c->dec_nst, true,
                      c->stream));
@@ -730,9 +759,8 @@ nosa_status nosa_step_plan(nosa_ctx* c, int32_t* kernels_per_layer, int32_t* clu
 
 nosa_status nosa_sync(nosa_ctx* c) {
   if (!c) return NOSA_ERR_INVALID_ARG;
-  CK(cudaStreamSynchronize(c->sel_stream));
-  CK(cudaStreamSynchronize(c->pref_stream));
-  CK(cudaStreamSynchronize(c->stream));
+  const nosa_status ss = sync_all(c);
+  if (ss != NOSA_OK) return ss;
   int e = 0;
   CK(cudaMemcpy(&e, c->err, sizeof(int), cudaMemcpyDeviceToHost));
   std::vector<int> T(c->L);
@@ -751,7 +779,8 @@ nosa_status nosa_sync(nosa_ctx* c) {
 
 nosa_status nosa_reset_state(nosa_ctx* c) {
   if (!c) return NOSA_ERR_INVALID_ARG;
-  CK(cudaStreamSynchronize(c->stream));
+  const nosa_status ss = sync_all(c);
+  if (ss != NOSA_OK) return ss;
   CK(cudaMemset(c->err, 0, sizeof(int)));
   c->failed = 0;
   return NOSA_OK;
@@ -766,7 +795,8 @@ nosa_status nosa_context_length(nosa_ctx* c, int layer, int32_t* T_out) {
 
 nosa_status nosa_get_stats(nosa_ctx* c, nosa_stats* out) {
   if (!c || !out) return NOSA_ERR_INVALID_ARG;
-  CK(cudaStreamSynchronize(c->stream));
+  const nosa_status ss = sync_all(c);
+  if (ss != NOSA_OK) return ss;
   DevStats d;
   CK(cudaMemcpy(&d, c->stats, sizeof(d), cudaMemcpyDeviceToHost));
   out->selections = d.selections;
@@ -783,7 +813,8 @@ nosa_status nosa_get_stats(nosa_ctx* c, nosa_stats* out) {
 
 nosa_status nosa_reset_stats(nosa_ctx* c) {
   if (!c) return NOSA_ERR_INVALID_ARG;
-  CK(cudaStreamSynchronize(c->stream));
+  const nosa_status ss = sync_all(c);
+  if (ss != NOSA_OK) return ss;
   DevStats z{};
   z.gamma_min_bits = 0x3F800000u;
   CK(cudaMemcpy(c->stats, &z, sizeof(z), cudaMemcpyHostToDevice));
@@ -792,7 +823,8 @@ nosa_status nosa_reset_stats(nosa_ctx* c) {
 
 nosa_status nosa_debug_scores(nosa_ctx* c, int layer, float* sq, float* se) {
   if (!c || layer < 0 || layer >= c->L) return NOSA_ERR_INVALID_ARG;
-  CK(cudaStreamSynchronize(c->stream));
+  const nosa_status ss = sync_all(c);
+  if (ss != NOSA_OK) return ss;
   const LayerState s = layer_state(c, layer);
   const size_t n = (size_t)c->U * s.nb_max * 4;
   if (sq) CK(cudaMemcpy(sq, s.sq_blk, n, cudaMemcpyDeviceToHost));
@@ -802,7 +834,8 @@ nosa_status nosa_debug_scores(nosa_ctx* c, int layer, float* sq, float* se) {
 
 nosa_status nosa_export_state(nosa_ctx* c, int layer, const nosa_state_view* v) {
   if (!c || !v || layer < 0 || layer >= c->L) return NOSA_ERR_INVALID_ARG;
-  CK(cudaStreamSynchronize(c->stream));
+  const nosa_status ss = sync_all(c);
+  if (ss != NOSA_OK) return ss;
   const LayerState s = layer_state(c, layer);
   const size_t U = c->U, cap = c->cap;
   auto cp = [&](void* dst, const void* src, size_t bytes) {
