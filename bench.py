@@ -12,6 +12,25 @@ N > 1 runs under torchrun with one process per GPU; every rank serves its own
 batch (independent sequences, no collective on the data path: weak scaling).
 Inputs are synthetic (seeded), shaped like the workload; the full K/V context
 lives in pinned host memory before timing starts.
+
+Rank 0 prints one JSON line.  Beside the contract's keys (value = tok/s of the
+whole stack from CUDA events around K graph-replayed steps, max over ranks):
+  roofline            the dominant kernel's algorithmic bytes / its mean launch
+                      time (per-kernel leg) against MEASURED_PEAKS' HBM copy
+                      bandwidth; traffic = stored ncu DRAM bytes per launch while
+                      the kernel's sources still hash to the capture's
+  fetch_roofline      the standalone gather on the step's fetch list against the
+                      best pinned 1 GiB host-to-device copy of the same run
+  hbm_frac_score_select_attend, stages_us_per_layer (per-kernel leg), gamma,
+  fetch_blocks_per_step, short_selections, clocks (nvidia-smi samples taken
+  during the timed region), gpu_launches (this library's kernels in the timed
+  region)
+  e2e                 the same metric through nosa_step_host_all on pinned host
+                      buffers, copies inside the timed region (device, host wall
+                      and host busy time per step reported)
+  cpu_baseline        the oracle on a bounded sample on the host cores (rank 0)
+--impl reference times the oracle alone (this path has no other reference
+implementation); --quick keeps only the timed leg (profiling runs).
 """
 from __future__ import annotations
 
