@@ -17,7 +17,7 @@ NOSA computes, in float64 numpy, in the order the pages describe it:
   7. attention        exact softmax attention over the selected tokens (eq. 8)
   8. locality         gamma(t) = |D_t intersect S_{t-1}| / |D_t|     (Theorem 2)
 
-Readings taken where the pages leave a step open (each is listed in the design doc):
+Readings taken where the pages leave a step open:
   * kernel 32 / stride 16 for CompressK (the wiki table prints "32 / 16" with a
     note that SparDA and InfLLM-V2 give kernel 32, stride 16; the NOSA-1B blog
     gives kernel_size=32, stride 16).

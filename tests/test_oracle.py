@@ -128,15 +128,58 @@ def test_query_scores_group_softmax_invariants():
     assert np.array_equal(np.argsort(-s1, kind="stable"), np.argsort(-(Kt @ Q[0]), kind="stable"))
 
 
-def test_query_score_on_mean_key_equals_mean_of_token_scores():
-    # The explainer's form pools token scores q.k_j; with unrounded mean keys it is the same number.
+def test_query_scores_hand_case_two_heads_three_windows():
+    # d = 4, so the temperature is 1/sqrt(4) = 1/2.  Windows K~ = 2 e0, 2 e1, 0; heads q = e0, e1.
+    # Logits z = (q . K~) / 2: head 0 -> (1, 0, 0), head 1 -> (0, 1, 0).  Each head's softmax runs
+    # over the windows; the group score is the sum over the heads:
+    #   s = ((e + 1) / (e + 2), (e + 1) / (e + 2), 2 / (e + 2)).
+    # A temperature of 1/d, a softmax over the heads instead of the windows, or a mean over the
+    # heads instead of the sum gives other numbers.
+    e = math.e
+    Kt = np.array([[2.0, 0, 0, 0], [0, 2.0, 0, 0], [0, 0, 0, 0]])
+    Q = np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0]])
+    want = np.array([(e + 1) / (e + 2), (e + 1) / (e + 2), 2 / (e + 2)])
+    assert np.max(np.abs(O.query_scores(Q, Kt, 1 / math.sqrt(4)) - want)) < 1e-15
+
+
+def test_unit_scores_use_inverse_sqrt_d_temperature_hand_case():
+    # One unit with head_dim 4 and 80 tokens: four complete windows, two blocks.  Keys come in
+    # groups of 16 tokens g0..g4 = 2e0, 2e0, 2e1, 2e1, 0, so K~_i = (g_i + g_{i+1}) / 2 =
+    # 2e0, e0 + e1, 2e1, e1.  Heads q0 = 2e0, q1 = 2e1 at the default temperature 1/sqrt(4):
+    #   z0 = (2, 1, 0, 0), z1 = (0, 1, 2, 1)
+    #   s_i = exp(z0_i) / (e^2 + e + 2) + exp(z1_i) / (1 + e)^2.
+    # Block 0 (tokens 0..63) overlaps windows 0..3, block 1 (tokens 64..127) only window 3, so the
+    # pooled scores are max(s) = s_0 and s_3.
+    e = math.e
+    d, T = 4, 80
+    g = [[2, 0, 0, 0], [2, 0, 0, 0], [0, 2, 0, 0], [0, 2, 0, 0], [0, 0, 0, 0]]
+    K = np.repeat(np.array(g, np.float64), 16, axis=0)
+    u = O.UnitOracle(head_dim=d, k_q=1, k_e=1, window_tokens=0, max_context=T,
+                     W1=np.zeros((d, 2)), W2=np.zeros(2))
+    u.append(O.f64_to_bf16_bits(K), O.f64_to_bf16_bits(np.zeros((T, d))))
+    assert np.array_equal(u.compressed_keys(), [[2, 0, 0, 0], [1, 1, 0, 0], [0, 2, 0, 0], [0, 1, 0, 0]])
+    a, b = e ** 2 + e + 2, (1 + e) ** 2
+    s0 = e ** 2 / a + 1 / b
+    s3 = 1 / a + e / b
+    sq, se = u.scores(O.f64_to_bf16_bits(np.array([[2.0, 0, 0, 0], [0, 2.0, 0, 0]])))
+    assert abs(sq[0] - s0) < 1e-15 and abs(sq[1] - s3) < 1e-15
+    assert abs(s0 - 0.6826251735421364) < 1e-15 and abs(s3 - 0.2792064726850172) < 1e-15
+    # W2 = 0: every eviction score is zero, so both pooled query-agnostic scores are zero
+    assert np.array_equal(se, [0.0, 0.0])
+
+
+def test_single_head_query_score_is_softmax_of_mean_token_logits():
+    # The explainer writes the query-aware score through per-token logits q.k_j pooled by the mean
+    # over a window.  With one head and unrounded mean keys, query_scores must equal the softmax of
+    # those pooled token logits at the same temperature (computed here without query_scores).
     rng = np.random.default_rng(4)
     K = rng.standard_normal((160, 16))
     q = rng.standard_normal(16)
     nc = O.num_windows(160)
     kbar = np.stack([K[16 * i:16 * i + 32].mean(0) for i in range(nc)])
-    token_form = np.array([(K[16 * i:16 * i + 32] @ q).mean() for i in range(nc)])
-    assert np.max(np.abs(kbar @ q - token_form)) < 1e-12
+    token_form = np.array([(K[16 * i:16 * i + 32] @ q).mean() for i in range(nc)]) * 0.25
+    w = np.exp(token_form - token_form.max())
+    assert np.max(np.abs(O.query_scores(q[None, :], kbar, 0.25) - w / w.sum())) < 1e-12
 
 
 # ----------------------------------------------------------------------------- selection
@@ -215,6 +258,29 @@ def test_theorem2_locality_bound(sigma, seed):
     c = json.load(open(os.path.join(GOLD, "page_constants.json")))
     k, kq = c["budget_tokens"] // 64, c["k_q_tokens"] // 64
     assert (k - kq) / k == c["gamma_lower_bound"]
+
+
+def test_locality_hand_values():
+    # gamma = |D_t & S_{t-1}| / |D_t|: D = {3, 5, 8, 9}, S_prev = {0, 3, 8, 12, 13, 14} share {3, 8}
+    # -> 2 / 4.  Dividing by |S_prev| would give 2 / 6, intersecting S_t instead of D_t more.
+    assert O.locality([3, 5, 8, 9], [0, 3, 8, 12, 13, 14]) == 0.5
+    assert O.locality([3], [4]) == 0.0 and O.locality([], [1]) == 1.0
+
+
+def test_unit_locality_over_two_hand_selections():
+    # 10 blocks, window 2 blocks (8, 9), sink 0: candidates 1..7.  Selection 1: Q = {2}, E = {3, 4}
+    # -> S_1 = {0, 2, 3, 4, 8, 9}.  Selection 2: Q = {5}, E = {3, 4} -> D_2 = {3, 4, 5}, of which
+    # {3, 4} were in S_1: gamma = 2/3 (|S_2 & S_1| / |S_2| would be 5/6, / |S_1| would be 1/3).
+    u = O.UnitOracle(head_dim=4, k_q=1, k_e=2, window_tokens=128, max_context=640,
+                     W1=np.zeros((4, 2)), W2=np.zeros(2))
+    u.append(np.zeros((640, 4), np.uint16), np.zeros((640, 4), np.uint16))
+    r1 = u.commit([2], [3, 4])
+    assert r1["S"] == [0, 2, 3, 4, 8, 9] and r1["gamma"] is None
+    assert u.evicted == {1, 5, 6, 7}
+    r2 = u.commit([5], [3, 4])
+    assert r2["D"] == [3, 4, 5] and abs(r2["gamma"] - 2 / 3) < 1e-15
+    assert r2["fetch"] == [(5, 1)]              # block 2 left its slot 1, block 5 takes it
+    assert r2["gamma"] >= u.k_e / (u.k_q + u.k_e) - 1e-15
 
 
 def test_eviction_is_sticky_and_fetches_follow_the_set_difference():
