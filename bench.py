@@ -16,21 +16,27 @@ lives in pinned host memory before timing starts.
 Rank 0 prints one JSON line.  Beside the contract's keys (value = tok/s of the
 whole stack from CUDA events around K graph-replayed steps, max over ranks):
   roofline            the dominant kernel's algorithmic bytes / its mean launch
-                      time (per-kernel leg) against MEASURED_PEAKS' HBM copy
-                      bandwidth; traffic = stored ncu DRAM bytes per launch while
-                      the kernel's sources still hash to the capture's
-  fetch_roofline      the standalone gather on the step's fetch list against the
-                      best pinned 1 GiB host-to-device copy of the same run
+                      time (isolated launches of the per-kernel leg) against
+                      MEASURED_PEAKS' HBM copy bandwidth; in_step = the score,
+                      select and attend bytes of every layer / ms_per_step;
+                      traffic = stored ncu DRAM bytes per launch while the
+                      kernel's sources still hash to the capture's
+  fetch_roofline      the gather kernel on the step's fetch list against the
+                      best pinned 1 GiB host-to-device copy of the same run;
+                      in_attend = the new blocks' bytes / the attention launch
+                      that copies them; in_step = fetched bytes / ms_per_step
   hbm_frac_score_select_attend, stages_us_per_layer (per-kernel leg), gamma,
   fetch_blocks_per_step, short_selections, clocks (nvidia-smi samples taken
   during the timed region), gpu_launches (this library's kernels in the timed
-  region)
-  e2e                 the same metric through nosa_step_host_all on pinned host
+  region), plan (the kernels nosa_step runs)
+  e2e                 the same metric through the public API on pinned host
                       buffers, copies inside the timed region (device, host wall
                       and host busy time per step reported)
   cpu_baseline        the oracle on a bounded sample on the host cores (rank 0)
 --impl reference times the oracle alone (this path has no other reference
-implementation); --quick keeps only the timed leg (profiling runs).
+implementation); --quick keeps only the timed leg (profiling runs); --forecast
+runs the SparDA-style pipeline (every leg above, on its kernels); the sizing
+flags set nosa_config's kernel sizing fields.
 """
 from __future__ import annotations
 
@@ -58,7 +64,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="nosa1b_16k_b8")
+    ap.add_argument("--workload", default="nosa8b_32k_b32",
+                    help="default: the 8B-shaped stack (32 layers, 32/8 heads, 32K context, batch 32), the "
+                         "largest workload that fits one GPU and its host")
     ap.add_argument("--sigma", type=float, default=None)
     ap.add_argument("--k-q", type=int, default=None)
     ap.add_argument("--gather-ctas", type=int, default=0)
@@ -71,6 +79,11 @@ def parse():
                     help="SparDA-style selection one layer ahead from forecast vectors, the next layer's "
                          "selection and prefetch overlapping the current layer (timed leg only)")
     ap.add_argument("--quick", action="store_true", help="timed graph leg only (profiling runs)")
+    # kernel sizing overrides (nosa_config fields; 0 = the library's rule)
+    for f in ("score-ctas", "attend-blocks-per-cta", "attend-merge", "decode-cluster", "decode-teams",
+              "decode-stages", "forecast-streams"):
+        ap.add_argument(f"--{f}", type=int, default=0)
+    ap.add_argument("--unfused", action="store_true", help="three-kernel step even where the fused kernel fits")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -212,6 +225,27 @@ def oracle_baseline(wl, seconds, total_units):
                       f"{dt:.1f} s; numpy float64 with its default BLAS threading"}
 
 
+def sizing_overrides(args):
+    """nosa_config sizing fields set on the command line (0 = the library's rule)."""
+    return {k: getattr(args, k) for k in ("score_ctas", "attend_blocks_per_cta", "attend_merge", "decode_cluster",
+                                          "decode_teams", "decode_stages", "forecast_streams")}
+
+
+def workload_config(wl, args, layers, world):
+    """The `config` object of the JSON line: the workload, as both arms print it."""
+    cfg = {"workload": wl.name, "layers": layers, "batch_per_gpu": wl.batch, "q_heads": wl.q_heads,
+           "kv_heads": wl.kv_heads, "head_dim": wl.head_dim, "context": wl.context, "k_q": wl.k_q, "k_e": wl.k_e,
+           "sink_blocks": wl.sink_blocks, "window_tokens": wl.window_tokens, "sigma": wl.sigma,
+           "parallelism": f"replicas x{world} (independent sequences per GPU)",
+           "dma_bias": bool(args.dma_bias),
+           "selection": "forecast one layer ahead, overlapped prefetch" if args.forecast else "query (per step)",
+           "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache (L2 is 129 MB)"}
+    over = {k: v for k, v in sizing_overrides(args).items() if v}
+    if over:
+        cfg["sizing"] = over
+    return cfg
+
+
 def slowest_rank_ms(ms: float, world: int, device: str = "cpu") -> float:
     """Per-step time of the slowest rank (max over ranks; every rank must call it)."""
     if world <= 1:
@@ -248,10 +282,11 @@ def run_native(args, rank, world, local_rank):
     n_e2e = 0 if args.quick else min(K, 64)
     n_e2e_warm = 6 if n_e2e else 0  # two untimed replays of each e2e graph (the first uploads it)
     total_steps = 1 + W + K + n_time_leg + n_e2e_warm + n_e2e
+    flags = (N.NOSA_F_DMA_BIAS if args.dma_bias else 0) | (N.NOSA_F_UNFUSED_STEP if args.unfused else 0)
     cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=wl.context + total_steps,
                         sink_blocks=wl.sink_blocks, evict_hidden=wl.evict_hidden, gather_ctas=args.gather_ctas,
-                        flags=N.NOSA_F_DMA_BIAS if args.dma_bias else 0)
+                        flags=flags, **sizing_overrides(args))
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     sizes = N.nosa_query_sizes(cfg)
@@ -375,48 +410,48 @@ def run_native(args, rank, world, local_rank):
     result = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
               "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
               "dtype": "bf16", "data": "synthetic",
-              "config": {"workload": wl.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": Hkv,
-                         "head_dim": d, "context": wl.context, "k_q": wl.k_q, "k_e": wl.k_e,
-                         "sink_blocks": wl.sink_blocks, "window_tokens": wl.window_tokens, "sigma": wl.sigma,
-                         "parallelism": f"replicas x{world} (independent sequences per GPU)",
-                         "cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
-                         "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster,
-                         "dma_bias": bool(args.dma_bias),
-                         "selection": "forecast one layer ahead, overlapped prefetch" if fc else "query (per step)",
-                         "l2": "no flush: one step reads > 1 GB of distinct K/V, compressed keys and cache "
-                               "(L2 is 129 MB)"},
+              "config": workload_config(wl, args, L, world),
+              "plan": {"cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
+                       "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster},
               # forecast: forecast select and gather (prefetch stream), append, attention, merge
               "gpu_launches": (5 if fc else step_kernels) * L * K,
               "clocks": ck,
               "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min, "bound": wl.k_e / (wl.k_q + wl.k_e)},
               "fetch_blocks_per_step": fetched_per_step,
               "short_selections": stats.short_selections}
-    if args.quick or fc or rank != 0:
-        if fc:
-            result["roofline"] = None
-            result["e2e"] = None
-            result["note"] = ("forecast mode: timed graph leg only (5 kernels per layer: forecast select and "
-                              "gather on the prefetch stream, append, attention and its merge on the step stream)")
+    if args.quick or rank != 0:
         N.nosa_destroy(ctx)
         return result
 
     # ---------------- per-kernel leg: one event pair around each launch, on the launching stream.
-    # Even steps time nosa_step per layer (the fused decode kernel, or its three kernels); odd
-    # steps time the separate calls: append, select and attend (which fetches the new blocks
-    # itself), then the standalone gather kernel (nosa_fetch) re-run on the same fetch list.
-    ev = {k: [] for k in ("decode", "append", "select", "attend", "gather")}
-    fetched_split = 0
+    # Plain mode: even steps time nosa_step per layer (the fused decode kernel, or its three
+    # kernels); odd steps time the separate calls: append, select and attend (which fetches the
+    # new blocks itself), then the standalone gather kernel (nosa_fetch) re-run on the same fetch
+    # list.  Forecast mode: every step times the forecast path's kernels as separate calls on the
+    # step stream: forecast selection, the gather of its new blocks, append, attention.
+    ev = {k: [] for k in ("decode", "append", "select", "attend", "gather", "fselect")}
+    fetched_split, split_steps = 0, 0
     for it in range(n_time_leg):
         t = step_i[0]
         step_i[0] += 1
-        if it % 2:
+        split = fc or it % 2 == 1
+        if split:
             s0 = N.nosa_get_stats(ctx).blocks_fetched
+            split_steps += 1
         for l in range(L):
             pairs = []
             # hold the stream while the launches and their events are queued, so that the
             # events time the kernels back to back rather than the host's launch latency
             torch.cuda._sleep(400000)
-            if it % 2 == 0:
+            if fc:
+                # after the timed graphs layer 0 of this step already has its forecast selection
+                calls = [] if (it == 0 and l == 0) else [
+                    ("fselect", lambda: N.nosa_forecast_select(ctx, l, Fall[t, l].view(i16)))]
+                calls += [("gather", lambda: N.nosa_fetch(ctx, l)),
+                          ("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16),
+                                                              KVall[t, 1, l].view(i16), 1)),
+                          ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16)))]
+            elif not split:
                 calls = [("decode", lambda: N.nosa_step(ctx, l, Qall[t, l].view(i16), KVall[t, 0, l].view(i16),
                                                         KVall[t, 1, l].view(i16), out[l].view(i16)))]
             else:
@@ -434,62 +469,98 @@ def run_native(args, rank, world, local_rank):
             torch.cuda.synchronize()
             for name, a, b in pairs:
                 ev[name].append(a.elapsed_time(b) * 1e3)
-        if it % 2:
+        if split:
             fetched_split += N.nosa_get_stats(ctx).blocks_fetched - s0
-    us = {k: statistics.mean(v) for k, v in ev.items()}
-    n_sel = np.zeros(U, np.int32)
-    N.nosa_export_state(ctx, 0, n_sel=n_sel)
+    us = {k: statistics.mean(v) for k, v in ev.items() if v}
+    G = Hq // Hkv
     T_now = N.nosa_context_length(ctx, 0)
     valid_tail = T_now - 64 * ((T_now + 63) // 64 - 1)
-    G = Hq // Hkv
-    attend_bytes = float(np.sum((n_sel.astype(np.int64) * 64 - (64 - valid_tail)) * d * 2 * 2)) + 2 * U * G * d * 2
     nc = (T_now - 32) // 16 + 1
     nb = (T_now + 63) // 64
+    attend_layers = []
+    for l in range(L):  # every layer's selection sizes: algorithmic K+V bytes of its attention
+        n_sel = np.zeros(U, np.int32)
+        N.nosa_export_state(ctx, l, n_sel=n_sel)
+        attend_layers.append(float(np.sum((n_sel.astype(np.int64) * 64 - (64 - valid_tail)) * d * 2 * 2))
+                             + 2 * U * G * d * 2)
+    attend_bytes = statistics.mean(attend_layers)
     select_bytes = U * (nc * d * 2 + nb * 4 + G * d * 2)
-    fetch_bytes_launch = fetched_split / max(n_time_leg // 2 * L, 1) * BLOCK_BYTES
+    fetch_bytes_launch = fetched_split / max(split_steps * L, 1) * BLOCK_BYTES
     hbm, src = measured_peaks()
     peak_src = f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"
-    if step_kernels == 1:
+    if step_kernels == 1 and not fc:
         dominant, dom_bytes = "decode", attend_bytes + select_bytes
         note = ("fused decode kernel (append + score + select + fetch + attend); bytes = compressed keys, "
                 "pooled scores and q read by the scorer plus K+V of every selected token read by the attention "
                 "and its output; the newly selected blocks among them arrive over the host link inside the kernel")
     else:
-        hbm_kernels = {"attend": attend_bytes, "select": select_bytes}
+        hbm_kernels = {"attend": attend_bytes, "fselect" if fc else "select": select_bytes}
         dominant = max(hbm_kernels, key=lambda k: us[k])
         dom_bytes = hbm_kernels[dominant]
-        note = ("attend bytes = K+V of every selected token; the newly selected blocks among them arrive over "
-                "the host link inside the same kernel")
+        note = ("attend bytes = K+V of every selected token and the output; in plain mode the newly selected "
+                "blocks among them arrive over the host link inside the same kernel, in forecast mode the "
+                "gather copied them before")
     ach = dom_bytes / (us[dominant] * 1e-6) / 1e9
-    traffic, traffic_src = captured_traffic(f"{dominant}_kernel",
-                                            f"{wl.name}|sigma{wl.sigma}|kq{wl.k_q}|dma{int(args.dma_bias)}")
-    result["roofline"] = {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
+    kname = "score_select_kernel" if dominant in ("select", "fselect") else f"{dominant}_kernel"
+    traffic, traffic_src = captured_traffic(kname, f"{wl.name}|sigma{wl.sigma}|kq{wl.k_q}|dma{int(args.dma_bias)}")
+    step_bytes = float(sum(attend_layers)) + L * select_bytes
+    in_step = step_bytes / (ms * 1e-3) / 1e9
+    result["roofline"] = {"kernel": kname, "bound": "hbm", "achieved": ach, "peak": hbm,
                           "peak_source": peak_src, "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
                           "traffic_source": traffic_src, "algorithmic_bytes_per_launch": dom_bytes,
-                          "avg_launch_us": us[dominant], "note": note}
-    fach = fetch_bytes_launch / (us["gather"] * 1e-6) / 1e9  # its peak is measured after the e2e leg
+                          "avg_launch_us": us[dominant],
+                          "how": "events around each launch of the per-kernel leg (isolated launches)",
+                          "in_step": {"achieved": in_step, "frac": in_step / hbm, "unit": "GB/s",
+                                      "algorithmic_bytes_per_step": step_bytes,
+                                      "how": "score + select + attend bytes of every layer / ms_per_step of the "
+                                             "timed graph leg"},
+                          "note": note}
     result["stages_us_per_layer"] = us
-    sel_att_us = us["decode"] if step_kernels == 1 else us["attend"] + us["select"]
+    sel_att_us = us["decode"] if (step_kernels == 1 and not fc) else us["attend"] + us.get("select", us.get("fselect", 0))
     result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / (sel_att_us * 1e-6) / 1e9 / hbm
 
-    # ---------------- e2e: the public host-pointer API (nosa_step_host_all: one copy of every layer's
-    # q, k, v to the device, the layers' steps, one copy of the outputs back), copies inside the timed
-    # region.  Three CUDA graphs, each capturing that call on its own set of pinned host buffers, take
-    # turns: while one replays, the host reads the outputs of the set that finished and writes the
-    # next step's inputs into it, up to two steps ahead of the device.
+    # ---------------- e2e through the public API, copies inside the timed region.  Plain mode:
+    # nosa_step_host_all (one host-to-device copy of every layer's q, k, v, the layers' steps, one
+    # device-to-host copy of the outputs).  Forecast mode: host-to-device copies of q, k, v and the
+    # forecast vectors from pinned memory, the nosa_step_forecast calls, the device-to-host copy of
+    # the outputs.  Three CUDA graphs, each capturing one step on its own set of pinned host
+    # buffers, take turns: while one replays, the host reads the outputs of the set that finished
+    # and writes the next step's inputs into it, up to two steps ahead of the device.
     e2e_graph = use_graph
     n_sets = 3
     sets = [dict(q=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory(),
                  kv=torch.empty((2, L, B, Hkv, d), dtype=torch.bfloat16).pin_memory(),
                  out=torch.empty((L, B, Hq, d), dtype=torch.bfloat16).pin_memory()) for _ in range(n_sets)]
+    if fc:
+        for bs in sets:
+            bs["f"] = torch.empty((L + 1, B, Hkv, d), dtype=torch.bfloat16).pin_memory()  # layers, then next layer 0
     q_src = Qall[step_i[0]:step_i[0] + n_e2e_warm + n_e2e].cpu()
     kv_src = KVall[step_i[0]:step_i[0] + n_e2e_warm + n_e2e].cpu()
+    if fc:
+        f_src = torch.cat([Fall[step_i[0]:step_i[0] + n_e2e_warm + n_e2e],
+                           Fall[step_i[0] + 1:step_i[0] + n_e2e_warm + n_e2e + 1, :1]], dim=1).cpu()
     outs_host = torch.zeros((n_e2e, L, B, Hq, d), dtype=torch.bfloat16)  # pages touched before the timing
 
     def host_step(bs):
-        N.nosa_step_host_all(ctx, bs["q"].view(i16), bs["kv"][0].view(i16), bs["kv"][1].view(i16),
-                             bs["out"].view(i16))
+        if not fc:
+            N.nosa_step_host_all(ctx, bs["q"].view(i16), bs["kv"][0].view(i16), bs["kv"][1].view(i16),
+                                 bs["out"].view(i16))
+            return
+        cur_q.copy_(bs["q"], non_blocking=True)
+        cur_kv.copy_(bs["kv"], non_blocking=True)
+        cur_f.copy_(bs["f"][:L], non_blocking=True)
+        cur_f0n.copy_(bs["f"][L], non_blocking=True)
+        forecast_calls(cur_q, cur_kv, cur_f, cur_f0n)
+        bs["out"].copy_(out, non_blocking=True)
 
+    def fill(bs, j):
+        bs["q"].copy_(q_src[j])
+        bs["kv"].copy_(kv_src[j])
+        if fc:
+            bs["f"].copy_(f_src[j])
+
+    if fc:  # the pipeline expects layer 0's forecast for the next token to exist
+        N.nosa_forecast_select(ctx, 0, Fall[step_i[0], 0].view(i16))
     graphs_e2e = []
     if e2e_graph:
         side = torch.cuda.Stream()
@@ -505,14 +576,15 @@ def run_native(args, rank, world, local_rank):
     # untimed: two replays of each graph (its first launch uploads it), on real steps of the sequence
     for j in range(n_e2e_warm):
         bs = sets[j % n_sets]
-        bs["q"].copy_(q_src[j])
-        bs["kv"].copy_(kv_src[j])
+        fill(bs, j)
         if e2e_graph:
             graphs_e2e[j % n_sets].replay()
         else:
             host_step(bs)
     torch.cuda.synchronize()
     q_src, kv_src = q_src[n_e2e_warm:], kv_src[n_e2e_warm:]
+    if fc:
+        f_src = f_src[n_e2e_warm:]
     step_i[0] += n_e2e_warm
     done = [None] * n_sets
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -527,8 +599,7 @@ def run_native(args, rank, world, local_rank):
         tb = time.perf_counter()
         if done[k] is not None:
             outs_host[j - n_sets].copy_(bs["out"])  # read its result back on the host
-        bs["q"].copy_(q_src[j])
-        bs["kv"].copy_(kv_src[j])
+        fill(bs, j)
         if e2e_graph:
             graphs_e2e[k].replay()
         else:
@@ -544,26 +615,40 @@ def run_native(args, rank, world, local_rank):
     step_i[0] += n_e2e
     dev_ms, wall_ms = a.elapsed_time(b) / n_e2e, wall * 1e3 / n_e2e
     e2e_ms = max(dev_ms, wall_ms)
+    h2d_step = L * (B * Hq * d * 2 + 2 * U * d * 2) + ((L + 1) * U * d * 2 if fc else 0)
+    how = ("nosa_step_host_all on pinned host q/k/v/out (one host-to-device copy of every layer's inputs, the "
+           "layers' steps, one device-to-host copy of the outputs)" if not fc else
+           "host-to-device copies of q, k, v and the forecast vectors from pinned memory, nosa_step_forecast for "
+           "every layer, the device-to-host copy of the outputs")
     result["e2e"] = {"value": B / (e2e_ms * 1e-3), "unit": "tok/s", "ms_per_step": e2e_ms,
                      "device_ms_per_step": dev_ms, "host_wall_ms_per_step": wall_ms,
                      "host_busy_ms_per_step": busy * 1e3 / n_e2e, "steps": n_e2e,
-                     "h2d_bytes_per_step": L * (B * Hq * d * 2 + 2 * U * d * 2),
-                     "d2h_bytes_per_step": L * B * Hq * d * 2,
-                     "how": "nosa_step_host_all on pinned host q/k/v/out (one host-to-device copy of every layer's "
-                            "inputs, the layers' steps, one device-to-host copy of the outputs), outputs then "
-                            "copied out of the pinned buffers on the host; " + ("three CUDA graphs of those calls "
-                                                                                "taking turns"
-                                                            if e2e_graph else "eager calls") +
+                     "h2d_bytes_per_step": h2d_step, "d2h_bytes_per_step": L * B * Hq * d * 2,
+                     "how": how + ", outputs then copied out of the pinned buffers on the host; " +
+                            ("three CUDA graphs of those calls taking turns" if e2e_graph else "eager calls") +
                             "; max of device-event and host wall time"}
     assert N.nosa_sync(ctx) == N.NOSA_OK
     # the link's peak: a 1 GiB pinned copy, after the e2e leg (whose pinned buffers it would share)
     h2d = h2d_peak(torch)
-    result["fetch_roofline"] = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach,
-                                "peak": h2d, "unit": "GB/s", "frac": fach / h2d,
-                                "peak_source": "best pinned 1 GiB cudaMemcpyAsync H2D measured in this run",
-                                "bytes_per_launch": fetch_bytes_launch, "avg_launch_us": us["gather"],
-                                "note": "standalone nosa_fetch on the step's fetch list; the timed step fetches "
-                                        "inside attend instead"}
+    fach = fetch_bytes_launch / (us["gather"] * 1e-6) / 1e9
+    fetch_step = fetched_per_step * BLOCK_BYTES
+    fr = {"kernel": "gather_kernel", "bound": "host-to-device link", "achieved": fach, "peak": h2d, "unit": "GB/s",
+          "frac": fach / h2d, "peak_source": "best pinned 1 GiB cudaMemcpyAsync H2D measured in this run",
+          "bytes_per_launch": fetch_bytes_launch, "avg_launch_us": us["gather"],
+          "in_step": {"achieved": fetch_step / (ms * 1e-3) / 1e9, "frac": fetch_step / (ms * 1e-3) / 1e9 / h2d,
+                      "bytes_per_step": fetch_step,
+                      "how": "blocks the timed steps fetched x 32 KiB / ms_per_step: the link's use over the whole "
+                             "step (selections included)"}}
+    if fc:
+        fr["note"] = "the forecast path's gather (nosa_fetch after nosa_forecast_select), the kernel the timed step runs"
+    else:
+        attend_link = fetch_bytes_launch / (us["attend"] * 1e-6) / 1e9
+        fr["note"] = ("standalone nosa_fetch on the step's fetch list; in the timed step the attention kernel "
+                      "copies the new blocks itself")
+        fr["in_attend"] = {"achieved": attend_link, "frac": attend_link / h2d,
+                           "how": "new blocks' bytes / the attention launch that copies them (a lower bound on "
+                                  "the link's rate during that launch, which also reads the cached blocks)"}
+    result["fetch_roofline"] = fr
     N.nosa_destroy(ctx)
     del Qall, KVall
     torch.cuda.empty_cache()
@@ -665,14 +750,19 @@ def run_dense(args, rank, world, local_rank):
 def run_reference(args):
     """The oracle, as it stands, on host cores: each step is a bounded sample of the workload."""
     from synth import inputs as syn
-    wl = syn.workload(args.workload)
+    over = {}
+    if args.sigma is not None:
+        over["sigma"] = args.sigma
+    if args.k_q is not None:
+        over["k_q"], over["k_e"] = args.k_q, 64 - args.k_q
+    wl = syn.workload(args.workload, **over)
     U = wl.layers * wl.batch * wl.kv_heads
     per_step = max(2.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
     base = oracle_baseline(wl, per_step * (args.steps + args.warmup), U)
     return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "layers": wl.layers, "batch": wl.batch, "context": wl.context},
+            "config": workload_config(wl, args, args.layers or wl.layers, 1),
             "cpu_baseline": base,
             "e2e": {"value": base["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -95,6 +95,10 @@ typedef enum {
  * works"; the NOSA-1B blog names the score CIS).  Off: plain attention (NOSA
  * explainer eq. 8). */
 #define NOSA_F_DMA_BIAS 8u
+/* NOSA_F_TEST_RADIX_TOPK (test hook): the query-agnostic top-k_e always takes the warp radix
+ * select, which otherwise runs only when more than 1024 blocks are eligible (the first
+ * selection over a context of more than about 66K tokens).  Same selections either way. */
+#define NOSA_F_TEST_RADIX_TOPK 16u
 
 typedef struct {
   uint32_t struct_size;   /* sizeof(nosa_config) */
@@ -114,8 +118,32 @@ typedef struct {
   int32_t evict_hidden;   /* eviction-head hidden size h: multiple of 32, 32..256 */
   int32_t gather_ctas;    /* CTAs of the persistent fetch kernel; 0 = rule 16 if B<32 else 32 */
   float softmax_scale;    /* 0 => 1/sqrt(head_dim) */
-  uint32_t flags;         /* 0, or NOSA_F_TEST_* hooks */
+  uint32_t flags;         /* 0, or NOSA_F_* flags */
+  /* Kernel sizing.  0 takes the library's rule for each (set from measurements on
+   * GB300); a non-zero value overrides it, for sweeps and tests.  Selections, fetch
+   * lists and state do not depend on them; outputs may differ in the last bits (the
+   * order in which split-K partials are merged). */
+  int32_t score_ctas;            /* selector CTAs (one thread-block cluster) per unit, 1..8;
+                                    rule: about two CTAs per SM over a layer's units, more while
+                                    one CTA's window logits would not fit its shared memory */
+  int32_t attend_blocks_per_cta; /* selected blocks per attention CTA (split-K chunk), 1..64;
+                                    rule: 8..16 for about four CTAs per SM */
+  int32_t attend_merge;          /* how split-K partials are merged: NOSA_MERGE_* */
+  int32_t decode_cluster;        /* fused step: CTAs per unit cluster, 1..8 (rule: the largest of 8
+                                    and 4 whose clusters for all units are resident at once, else
+                                    the three-kernel chain); a forced size must be schedulable */
+  int32_t decode_teams;          /* fused step: attention workers of four warps per CTA, 1 or 2 */
+  int32_t decode_stages;         /* fused step: 32 KiB staging buffers per worker, 2..6 (rule: 3) */
+  int32_t forecast_streams;      /* forecast pipeline: 2 = selections and gathers on two streams
+                                    (a layer's selection overlaps the previous layer's gather),
+                                    1 = both in order on one stream */
 } nosa_config;
+
+/* Values of nosa_config.attend_merge. */
+#define NOSA_MERGE_AUTO 0    /* the rule: NOSA_MERGE_KERNEL */
+#define NOSA_MERGE_KERNEL 1  /* CTAs store partials; a dependent merge kernel combines them */
+#define NOSA_MERGE_TICKET 2  /* the unit's last CTA (atomic ticket) combines them */
+#define NOSA_MERGE_CLUSTER 3 /* the unit's CTAs form one cluster and combine through DSMEM */
 
 /* Derived sizes; filled by nosa_query_sizes (host only, no GPU needed). */
 typedef struct {
@@ -177,11 +205,16 @@ nosa_status nosa_destroy(nosa_ctx* ctx);
 /* Change the stream later calls are queued on (e.g. a capture stream). */
 nosa_status nosa_set_stream(nosa_ctx* ctx, void* stream);
 
-/* Eviction head of one layer (eq. 4): host float32 W1 [Hkv][d][h] and
- * W2 [Hkv][h], copied before return. */
+/* Eviction head of one layer: host float32 W1 [Hkv][d][h] and W2 [Hkv][h], copied before
+ * return.  Defined by: NOSA explainer, section 2.1, eq. 4 (s^e = softplus(v W1) W2); NOSA wiki,
+ * "How NOSA works" (the query-agnostic eviction head, one per kv head, ranked before any
+ * exponential as in ED-DMA). */
 nosa_status nosa_set_eviction_head(nosa_ctx* ctx, int layer, const float* W1, const float* W2);
 
-/* Append n_tokens >= 1 tokens to every sequence of `layer`.
+/* Append n_tokens >= 1 tokens to every sequence of `layer` (row a1).
+ * Defined by: NOSA explainer, section 2.1, eq. 4-6 (eviction score of each token, mean pooling
+ * of keys and scores over compression windows); NOSA-1B blog, key compressor (kernel 32,
+ * stride 16); NOSA wiki, "NOSI: the inference system" (the full K/V lives in host memory).
  * k, v: bf16 [B][Hkv][n_tokens][d]; device memory, or pinned/pageable host
  * memory when src_is_host != 0 (then copied before the kernels run).
  * n_tokens == 1 is the decode-step append; n_tokens > 1 is a bulk context load
@@ -192,17 +225,27 @@ nosa_status nosa_append_kv(nosa_ctx* ctx, int layer, const uint16_t* k, const ui
 
 /* Score and select the blocks of every unit of `layer` for query q
  * (device bf16 [B][Hq][d]), update the eviction bitmap and the slot map, and
- * build the fetch list.  Optional device outputs: sel_out [B][Hkv][cache_slots]
+ * build the fetch list (rows a2-a4).  Defined by: NOSA wiki, "How NOSA works" (query-aware
+ * top-k_q scores set to +inf, the rest filled from the query-agnostic score, a block dropped
+ * by that part never re-selected by it) and "Main-experiment configuration" (sink block,
+ * sliding-window blocks, 64-token blocks); NOSA explainer, section 2.1, eq. 5-6 (pooled block
+ * scores, the selection); SparDA summary, "lightweight design" (softmax aggregation over a GQA
+ * group); NOSA wiki, "NOSI" (set difference against the cached blocks).  Optional device outputs: sel_out [B][Hkv][cache_slots]
  * (S ascending, -1 padded) and nfetch_out [B][Hkv] (blocks to fetch). */
 nosa_status nosa_select(nosa_ctx* ctx, int layer, const uint16_t* q, int32_t* sel_out,
                         int32_t* nfetch_out);
 
 /* Copy the blocks listed by the last nosa_select of `layer` from the pinned
- * host store into their cache slots (persistent UVA gather kernel). */
+ * host store into their cache slots (persistent UVA gather kernel, row a5).  Defined by:
+ * NOSA wiki, "NOSI: the inference system" (a host-to-device kernel reading host memory
+ * through unified virtual addressing, block-wise 16 KiB transfers); SparDA summary, KV
+ * prefetch runtime (a resident set of copy CTAs, their count chosen by batch size). */
 nosa_status nosa_fetch(nosa_ctx* ctx, int layer);
 
 /* Attention of q (device bf16 [B][Hq][d]) over the selected blocks; writes
- * out (device bf16 [B][Hq][d]).  Needs a selection for the current T.  If
+ * out (device bf16 [B][Hq][d]) (row a6).  Defined by: NOSA explainer, section 2.1, eq. 8
+ * (softmax attention over the keys and values of the selected blocks); NOSA-1B blog, decode
+ * stage (attention over the top-k block indices only).  Needs a selection for the current T.  If
  * nosa_fetch has not run since that selection, the attention CTAs copy the
  * newly selected blocks from the pinned host store themselves (and write them
  * to their cache slots), so no separate gather pass is needed. */
@@ -210,14 +253,16 @@ nosa_status nosa_attend(nosa_ctx* ctx, int layer, const uint16_t* q, uint16_t* o
 
 /* One decode step of `layer`: append the token (k_new, v_new), score and select,
  * fetch the new blocks and attend with q, as one fused kernel or a short kernel
- * chain (nosa_step_plan says which); the same selections and state as
+ * chain (nosa_step_plan says which): rows a1-a6 as defined at nosa_append_kv,
+ * nosa_select, nosa_fetch and nosa_attend (NOSA wiki, "How NOSA works" and "NOSI";
+ * NOSA explainer, section 2.1, eq. 4-8); the same selections and state as
  * nosa_append_kv + nosa_select + nosa_attend.  k_new, v_new: device bf16
  * [B][Hkv][d]; q, out: device bf16 [B][Hq][d].  NOSA_ERR_CAPACITY (nothing queued)
  * when the layer's context is full. */
 nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                       const uint16_t* v_new, uint16_t* out);
 
-/* nosa_step with host q, k_new, v_new and out.  When all four are page-locked
+/* nosa_step with host q, k_new, v_new and out (the same step and sources as nosa_step).  When all four are page-locked
  * (cudaHostAlloc / cudaHostRegister) the kernels read the inputs and write the
  * output in place over the host link; otherwise the inputs are copied to
  * context-owned device buffers and the output back, on the stream.  Either way
@@ -226,7 +271,7 @@ nosa_status nosa_step(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_
 nosa_status nosa_step_host(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                            const uint16_t* v_new, uint16_t* out);
 
-/* One decode step of every layer from host buffers: q and out [L][B][Hq][d], k_new and
+/* One decode step of every layer from host buffers (nosa_step per layer, same sources): q and out [L][B][Hq][d], k_new and
  * v_new [L][B][Hkv][d], bf16, layer-major.  Copies q, k_new and v_new to
  * context-owned device buffers (one cudaMemcpyAsync each), runs nosa_step for layers
  * 0 .. L-1 in order on those, and copies every layer's output back (one
@@ -271,7 +316,7 @@ nosa_status nosa_step_forecast(nosa_ctx* ctx, int layer, const uint16_t* q, cons
 nosa_status nosa_forecast_join(nosa_ctx* ctx);
 
 /* Dense GQA decode attention over a device-resident KV store: the full-attention
- * comparator of the NOSA wiki's decode-throughput table (every token attended; no
+ * comparator of the NOSA wiki's decode-throughput table (section "Decoding throughput") (every token attended; no
  * selection, no host memory).  Context-free; allocates nothing.
  *   q        device bf16 [units][group][d]
  *   kv       device bf16 [units][max_blocks][2][64][d]: block b of unit u holds keys
@@ -311,9 +356,9 @@ nosa_status nosa_context_length(nosa_ctx* ctx, int layer, int32_t* T_out);
 nosa_status nosa_get_stats(nosa_ctx* ctx, nosa_stats* out);
 nosa_status nosa_reset_stats(nosa_ctx* ctx);
 
-/* Pooled block scores of the last selection of `layer`, host float
+/* Pooled block scores of the last selection of `layer` (plain or forecast), host float
  * [U][max_blocks] each (sq_blk: query-aware, se_blk: query-agnostic); either may
- * be NULL.  Valid until the next nosa_select of any layer.  Synchronises. */
+ * be NULL.  Each layer keeps its own.  Synchronises. */
 nosa_status nosa_debug_scores(nosa_ctx* ctx, int layer, float* sq_blk, float* se_blk);
 
 /* Copy selection / cache / compression state of `layer` to host memory. Synchronises. */
@@ -334,23 +379,29 @@ const char* nosa_status_string(nosa_status s);
  *            slot's block, 16-byte aligned), the layout of a context's cache
  *   sel      device int32 [units][cache_slots] selected block ids, ascending
  *   sel_slot device int32 [units][cache_slots] slot of each selected block
- *   n_sel    device int32 [units] number of selected blocks per unit
+ *   n_sel    device int32 [units] number of selected blocks per unit, at most
+ *            cache_slots
  *   context_len  tokens per sequence; block ceil(context_len/64)-1 is the
  *            partial tail and only its first tokens are attended
  *   softmax_scale 0 => 1/sqrt(128);  out device bf16 [units][group][128]
+ *   err_out  optional device int32 (4-byte aligned): cleared on the stream, then
+ *            receives the device-side error bits of this call: 1 = an n_sel above
+ *            cache_slots or a slot outside [0, cache_slots) was met (clamped into
+ *            range; that unit's output is meaningless), 2 = a bounded wait for a
+ *            staged block gave up (that unit's outputs are NaN).  NULL: the bits
+ *            go to the library's own scratch and are not reported.
  * Limits: units <= 1024 and units * ceil(cache_slots / chunk) <= 2048 split-K
- * partials (chunk <= 16 blocks); larger requests return NOSA_ERR_CAPACITY
- * before anything is queued.  Calls never allocate, so their scratch is shared:
- * calls that overlap on the GPU (other streams, other threads) race and must be
- * serialised by the caller; each call clears the tickets it uses.  The first
- * call on a device does a one-time set-up (looks up the scratch address and
- * sets the kernel's shared-memory limit); make that first call before any
- * stream capture.  Asynchronous on `stream`; out-of-range slots are clamped and
- * make that unit's output meaningless. */
+ * partials, where chunk (blocks per CTA) is widened up to 64 to fit; larger
+ * requests return NOSA_ERR_CAPACITY before anything is queued.  Calls never
+ * allocate, so their scratch is shared: calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller; each call
+ * clears the tickets it uses.  The first call on a device does a one-time set-up
+ * (looks up the scratch address and sets the kernel's shared-memory limit); make
+ * that first call before any stream capture.  Asynchronous on `stream`. */
 nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* cache, const int32_t* sel,
                                 const int32_t* sel_slot, const int32_t* n_sel, int units, int group,
                                 int cache_slots, int context_len, float softmax_scale, uint16_t* out,
-                                void* stream);
+                                int32_t* err_out, void* stream);
 
 #ifdef __cplusplus
 }

@@ -142,7 +142,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.gamma = c->gamma + lu * 2;
   s.W1 = c->W1 + (size_t)l * c->Hkv * kHeadDim * d.h;
   s.W2 = c->W2 + (size_t)l * c->Hkv * d.h;
-  s.sq_blk = c->sq_blk;
+  s.sq_blk = c->sq_blk + lu * d.nb_max;
   s.apart = c->apart;
   s.tickets = c->tickets;
   s.stats = c->stats;
@@ -154,6 +154,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.attend_mode = c->attend_mode;
   s.wait_limit = (c->cfg.flags & NOSA_F_TEST_ZERO_WAIT) ? -1 : kWaitCycles;
   s.test_bad_slot = (c->cfg.flags & NOSA_F_TEST_BAD_SLOT) ? 1 : 0;
+  s.test_radix = (c->cfg.flags & NOSA_F_TEST_RADIX_TOPK) ? 1 : 0;
   s.dma_bias = (c->cfg.flags & NOSA_F_DMA_BIAS) ? 1 : 0;
   return s;
 }
@@ -196,8 +197,16 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->max_context < 1 || c->max_context > 262144) return NOSA_ERR_INVALID_ARG;
   if (c->evict_hidden < 32 || c->evict_hidden > 256 || c->evict_hidden % 32) return NOSA_ERR_INVALID_ARG;
   if (c->gather_ctas < 0 || c->gather_ctas > 4096) return NOSA_ERR_INVALID_ARG;
-  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT | NOSA_F_UNFUSED_STEP | NOSA_F_DMA_BIAS)))
+  if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT | NOSA_F_UNFUSED_STEP | NOSA_F_DMA_BIAS |
+                                               NOSA_F_TEST_RADIX_TOPK)))
     return NOSA_ERR_INVALID_ARG;
+  if (c->score_ctas < 0 || c->score_ctas > 8) return NOSA_ERR_INVALID_ARG;
+  if (c->attend_blocks_per_cta < 0 || c->attend_blocks_per_cta > kMaxBlocksPerCta) return NOSA_ERR_INVALID_ARG;
+  if (c->attend_merge < NOSA_MERGE_AUTO || c->attend_merge > NOSA_MERGE_CLUSTER) return NOSA_ERR_INVALID_ARG;
+  if (c->decode_cluster < 0 || c->decode_cluster > 8) return NOSA_ERR_INVALID_ARG;
+  if (c->decode_teams < 0 || c->decode_teams > 2) return NOSA_ERR_INVALID_ARG;
+  if (c->decode_stages != 0 && (c->decode_stages < 2 || c->decode_stages > 6)) return NOSA_ERR_INVALID_ARG;
+  if (c->forecast_streams < 0 || c->forecast_streams > 2) return NOSA_ERR_INVALID_ARG;
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
   const long long cap = (long long)c->sink_blocks + c->window_tokens / kBlock + c->k_q + c->k_e;
@@ -220,10 +229,10 @@ nosa_status nosa_query_sizes(const nosa_config* c, nosa_sizes* out) {
   out->evict_words = d.ev_words;
   out->host_store_bytes = L * U * d.nb_max * (uint64_t)kBlockBytes;
   const uint64_t per_unit = (uint64_t)d.cap * kBlockBytes + nc * kHeadDim * 2 + 32 * kHeadDim * 2 +
-                            (uint64_t)d.nb_max * kBlock * 4 + nc * 4 + (uint64_t)d.nb_max * 8 + d.ev_words * 4ull +
+                            (uint64_t)d.nb_max * kBlock * 4 + nc * 4 + (uint64_t)d.nb_max * 12 + d.ev_words * 4ull +
                             (uint64_t)d.cap * 4 * 5 + 4 * 4;
   const int score_chunks = cdiv(nc, kWindowsPerCta);
-  const uint64_t scratch = U * d.G * nc * 4 + U * score_chunks * kMaxGroup * 8 + U * d.nb_max * 4 +
+  const uint64_t scratch = U * d.G * nc * 4 + U * score_chunks * kMaxGroup * 8 +
                            U * (uint64_t)d.cap * kMaxGroup * kPartStride * 4 + (3 * U + 1) * 4;
   out->device_state_bytes = L * U * per_unit + L * c->num_kv_heads * (uint64_t)kHeadDim * d.h * 4 + scratch;
   return NOSA_OK;
@@ -261,10 +270,9 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->sel_T.assign(c->L, -1);
   c->ev_pref.assign(c->L, nullptr);
   c->ev_sel.assign(c->L, nullptr);
-  // forecast pipeline: the selections on their own stream (NOSA_FORECAST_STREAMS=1: one prefetch
+  // forecast pipeline: the selections on their own stream (forecast_streams = 1: one prefetch
   // stream for selections and gathers, in order)
-  c->forecast_split = 1;
-  if (const char* e = getenv("NOSA_FORECAST_STREAMS")) c->forecast_split = atoi(e) != 1;
+  c->forecast_split = cfg->forecast_streams != 1;
   c->pref_pending.assign(c->L, 0);
   c->fetch_T.assign(c->L, -1);
 
@@ -275,7 +283,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   // so at large batch more units in flight beat more CTAs per unit (measured: one CTA per unit
   // at 256 units, four at 64 units with 64K contexts)
   c->score_chunks = std::max(1, std::min({8, cdiv(nc, kWindowsPerCta), 2 * std::max(c->num_sms, 1) / c->U}));
-  if (const char* e = getenv("NOSA_SCORE_CHUNKS")) c->score_chunks = std::min(std::max(atoi(e), 1), 8);
+  if (cfg->score_ctas > 0) c->score_chunks = cfg->score_ctas;
   for (;;) {  // more CTAs per unit while one CTA's logits would not fit its shared memory
     c->score_wpc = cdiv(cdiv(nc, c->score_chunks), 16 * kScoreWarps) * 16 * kScoreWarps;
     if (c->score_chunks >= 8 || score_select_smem(layer_state(c, 0)) <= 200 * 1024) break;
@@ -285,21 +293,21 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   // best at the batch-128/256 and 64K-context workloads: fewer, longer CTAs starve the host
   // copies of parallelism, more CTAs spend their time in set-up and merging).  The split-K
   // partials are merged by a small merge kernel: merging inside a thread-block cluster per unit
-  // (NOSA_ATTEND_MODE=1) makes a cluster's CTAs hold their SMs until the slowest one is done and
-  // measured 5-17 % slower at every workload, batch 8 included.  An atomic ticket merge is kept
-  // for the context-free entry point.
+  // (NOSA_MERGE_CLUSTER) makes a cluster's CTAs hold their SMs until the slowest one is done and
+  // measured 5-17 % slower at every workload, batch 8 included; merging in the unit's last CTA
+  // (NOSA_MERGE_TICKET, the context-free entry point's merge) 1-16 % slower.
   const int sms = std::max(c->num_sms, 1);
   int bpc = cdiv((long long)c->U * d.cap, 4ll * sms);
   bpc = std::min(std::max(bpc, 8), 16);
-  if (const char* e = getenv("NOSA_ATTEND_BLOCKS_PER_CTA")) bpc = std::min(std::max(atoi(e), 1), kMaxBlocksPerCta);
+  if (cfg->attend_blocks_per_cta > 0) bpc = cfg->attend_blocks_per_cta;
   if (init_attend() != cudaSuccess) {  // the cluster query below needs the kernel's smem limit set
     (void)cudaGetLastError();
     delete c;
     return NOSA_ERR_CUDA;
   }
-  c->attend_mode = 2;
-  if (const char* e = getenv("NOSA_ATTEND_MODE")) c->attend_mode = std::min(std::max(atoi(e), 0), 2);
-  if (c->attend_mode == 1) {  // the unit's CTAs must form one cluster
+  // internal modes: 0 ticket, 1 cluster, 2 merge kernel
+  c->attend_mode = cfg->attend_merge == NOSA_MERGE_TICKET ? 0 : cfg->attend_merge == NOSA_MERGE_CLUSTER ? 1 : 2;
+  if (c->attend_mode == 1) {  // the unit's CTAs must form one cluster: widen the chunks until they do
     const int max_cluster = attend_max_cluster();
     while (cdiv(d.cap, bpc) > max_cluster && bpc < kMaxBlocksPerCta) ++bpc;
     if (cdiv(d.cap, bpc) > max_cluster) c->attend_mode = 2;
@@ -311,21 +319,17 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   // workers of four warps.  It pays off while all units' clusters are resident at once (the
   // small batches where the step is latency bound): the largest cluster of 8 or 4 CTAs for
   // which that holds is taken, else the step runs as three kernels, as it does when the cache
-  // has more slots than a CTA has threads.  NOSA_FUSED=0 turns it off; NOSA_DECODE_CLUSTER,
-  // NOSA_DECODE_TEAMS and NOSA_DECODE_STAGES override the choices.
+  // has more slots than a CTA has threads.  NOSA_F_UNFUSED_STEP turns it off; decode_cluster,
+  // decode_teams and decode_stages override the choices.
   c->dec_cs = 0;
-  c->dec_teams = 2;
-  c->dec_nst = 3;
-  if (const char* e = getenv("NOSA_DECODE_TEAMS")) c->dec_teams = atoi(e) == 1 ? 1 : 2;
-  if (const char* e = getenv("NOSA_DECODE_STAGES")) c->dec_nst = std::min(std::max(atoi(e), 2), 6);
-  const char* fused_env = getenv("NOSA_FUSED");
-  if (!(cfg->flags & NOSA_F_UNFUSED_STEP) && (!fused_env || atoi(fused_env) != 0) &&
-      d.cap <= 128 * c->dec_teams) {
+  c->dec_teams = cfg->decode_teams > 0 ? cfg->decode_teams : 2;
+  c->dec_nst = cfg->decode_stages > 0 ? cfg->decode_stages : 3;
+  if (!(cfg->flags & NOSA_F_UNFUSED_STEP) && d.cap <= 128 * c->dec_teams) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     std::vector<int> sizes = {8, 4};  // with clusters of 2 the selector and attention are too narrow
-    const char* force = getenv("NOSA_DECODE_CLUSTER");
-    if (force) sizes = {std::min(std::max(atoi(force), 1), 8)};
+    const bool force = cfg->decode_cluster > 0;
+    if (force) sizes = {cfg->decode_cluster};
     const int warps = 4 * c->dec_teams;
     for (int cs : sizes) {
       c->dec_cs = cs;
@@ -384,7 +388,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   dalloc(&c->T, c->L * sizeof(int));
   dalloc(&c->err, sizeof(int));
   dalloc(&c->stats, sizeof(DevStats));
-  dalloc(&c->sq_blk, (size_t)c->U * d.nb_max * 4);
+  dalloc(&c->sq_blk, LU * d.nb_max * 4);
   dalloc(&c->apart, (size_t)c->U * c->attend_chunks * kMaxGroup * kPartStride * 4);
   dalloc(&c->tickets, (3 * (size_t)c->U + 1) * 4);
   dalloc(&c->stage_q, (size_t)c->B * c->Hq * kHeadDim * 2);
@@ -423,7 +427,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   ok = ok && cudaMemset(c->T, 0, c->L * sizeof(int)) == cudaSuccess;
   ok = ok && cudaMemset(c->err, 0, sizeof(int)) == cudaSuccess;
   ok = ok && cudaMemset(c->tickets, 0, (3 * (size_t)c->U + 1) * 4) == cudaSuccess;
-  ok = ok && cudaMemset(c->sq_blk, 0, (size_t)c->U * d.nb_max * 4) == cudaSuccess;
+  ok = ok && cudaMemset(c->sq_blk, 0, LU * d.nb_max * 4) == cudaSuccess;
   if (ok) {
     fill_f32<<<std::max(1, std::min(cdiv(LU * d.nb_max, 256), 4096)), 256>>>(c->se_blk, LU * d.nb_max, -INFINITY);
     ok = cudaGetLastError() == cudaSuccess;

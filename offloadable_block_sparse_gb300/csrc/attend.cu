@@ -55,7 +55,11 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   uint32_t qb[8][2];
   load_q_frags(qb, q, u, G, lane);
   const int T = *s.T;
-  const int nsel = s.n_sel[u];
+  const int nsel_in = s.n_sel[u];
+  // a count beyond the selection arrays (possible only for a caller-supplied selection) is
+  // clamped, so that no list index leaves the arrays, and flagged
+  const int nsel = min(max(nsel_in, 0), s.cap);
+  if (nsel != nsel_in && tid == 0 && chunk == 0) atomicOr(s.err, kErrBounds);
   const Geometry geo = geometry(T, s.nw, s.sink);
   const uint32_t sbase = smem_u32(smem);
   // Work split: the unit's selected blocks are dealt round-robin to its CTAs in an

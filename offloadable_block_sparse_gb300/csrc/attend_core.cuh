@@ -92,8 +92,10 @@ struct WarpAcc {
 // Runs one worker over its list (blk, slot, isnew; n entries, blocks without a slot
 // first) with `nst` stages at sbase and their mbarriers `bars` (initialised, count 1).
 // With s.dma_bias, sebuf (nst x 64 floats, 16-byte aligned) receives each staged
-// block's per-token eviction scores, added to the logits.  Returns false if a staged-block wait gave up (the error word has the
-// timeout bit; copies in flight have been drained).  ttid: thread index within the team.
+// block's per-token eviction scores, added to the logits.  Returns false if a staged-block wait
+// gave up: the error word has the timeout bit, copies in flight have been drained, and the
+// worker's softmax sums are NaN, so every output its partial reaches is NaN rather than a
+// plausible value.  ttid: thread index within the team.
 __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const LayerState& s, const Geometry& geo,
                                               int u, const uint32_t (&qb)[8][2], const int* blk, const int* slot,
                                               const int* isnew, int n, uint32_t sbase, uint64_t* bars, int nst,
@@ -238,6 +240,7 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
     for (int p = consumed; p < min(issued, nr); ++p)
       mbar_wait_bounded(&bars[ded + p % ring], (uint32_t)((p / ring) & 1), kWaitCycles);
   }
+  if (bad) A.l0 = A.l1 = __int_as_float(0x7fc00000);  // NaN: the merged outputs of this unit are NaN
   (void)gr;
   (void)t4;
   return !bad;

@@ -26,20 +26,21 @@ constexpr size_t kTicketsOff = 256;
 constexpr size_t kPartialsOff = kTicketsOff + 2 * kNoAllocMaxUnits * sizeof(unsigned int) + 256;
 constexpr size_t kScratchBytes = kPartialsOff + (size_t)kNoAllocMaxPartials * kMaxGroup * kPartStride * sizeof(float);
 
-// [0]: context length, [4]: device error word, [256...]: tickets, then partials.
+// [0]: context length, [4]: device error word (used when the caller passes none),
+// [256...]: tickets, then partials.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char* g_scratch_ptr[kMaxDevices] = {};
 
-__global__ void noalloc_prepare_kernel(unsigned char* scratch, int T, int units) {
+__global__ void noalloc_prepare_kernel(unsigned char* scratch, int* err, int T, int units) {
   int* hdr = reinterpret_cast<int*>(scratch);
   unsigned int* tickets = reinterpret_cast<unsigned int*>(scratch + kTicketsOff);
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i == 0) {
     hdr[0] = T;
-    hdr[1] = 0;
+    *err = 0;  // the error word this call reports into starts clear
   }
   if (i < 2 * units) tickets[i] = 0;  // merge tickets start at zero on every call
 }
@@ -87,7 +88,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* cache, const int32_t* sel,
                                            const int32_t* sel_slot, const int32_t* n_sel, int units, int group,
                                            int cache_slots, int context_len, float softmax_scale, uint16_t* out,
-                                           void* stream) {
+                                           int32_t* err_out, void* stream) {
   if (!q || !cache || !sel || !sel_slot || !n_sel || !out) return NOSA_ERR_INVALID_ARG;
   if (units < 1 || group < 1 || group > kMaxGroup || cache_slots < 1 || cache_slots > 256 || context_len < 1 ||
       !(softmax_scale >= 0.f))
@@ -100,6 +101,7 @@ extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* ca
     (void)cudaGetLastError();
     return NOSA_ERR_CUDA;
   }
+  if (reinterpret_cast<uintptr_t>(err_out) % 4) return NOSA_ERR_INVALID_ARG;
   // split-K chunking as in a context, widened until the partials fit the fixed scratch
   int bpc = (int)(((long long)units * cache_slots + 2ll * num_sms - 1) / (2ll * num_sms));
   bpc = std::min(std::max(bpc, 1), kMaxBlocksPerCta);
@@ -133,7 +135,7 @@ extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* ca
   s.unit_base = 0;
   s.scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)kHeadDim);
   s.T = reinterpret_cast<int*>(scratch);
-  s.err = reinterpret_cast<int*>(scratch) + 1;
+  s.err = err_out ? reinterpret_cast<int*>(err_out) : reinterpret_cast<int*>(scratch) + 1;
   s.tickets = reinterpret_cast<unsigned int*>(scratch + kTicketsOff);
   s.apart = reinterpret_cast<float*>(scratch + kPartialsOff);
   s.sel = const_cast<int32_t*>(sel);
@@ -145,7 +147,7 @@ extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* ca
   s.dma_bias = 0;  // no eviction scores here: plain attention
   s.attend_blocks_per_cta = bpc;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  noalloc_prepare_kernel<<<(2 * units + 255) / 256, 256, 0, cs>>>(scratch, context_len, units);
+  noalloc_prepare_kernel<<<(2 * units + 255) / 256, 256, 0, cs>>>(scratch, s.err, context_len, units);
   if (cudaGetLastError() != cudaSuccess) return NOSA_ERR_CUDA;
   if (launch_attend(s, &tmap, q, out, 0, false, cs) != cudaSuccess) {
     (void)cudaGetLastError();

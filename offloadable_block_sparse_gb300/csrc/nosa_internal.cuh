@@ -104,8 +104,8 @@ struct LayerState {
   int32_t* gamma;         // [U][2]
   const float* W1;        // [Hkv][d][h]
   const float* W2;        // [Hkv][h]
+  float* sq_blk;          // [U][nb_max] pooled query-aware scores of this layer's last selection
   // scratch shared by all layers (stream ordered)
-  float* sq_blk;          // [U][nb_max] pooled query-aware scores of the last selection
   float* apart;           // [U][attend_chunks][kMaxGroup][kPartStride]
   unsigned int* tickets;  // [3][U]: append, score, attend
   DevStats* stats;
@@ -117,6 +117,7 @@ struct LayerState {
   int attend_mode;         // split-K merge: 0 ticket (global), 1 cluster (DSMEM), 2 merge kernel
   long long wait_limit;    // SM cycles a staged-block wait may take before it reports a timeout (<0: none)
   int test_bad_slot;       // test hook: publish one out-of-range slot (unit 0, first entry)
+  int test_radix;          // test hook: the query-agnostic top-k always by warp radix select
 };
 
 }  // namespace nosa

@@ -533,7 +533,7 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
   if (n_elig <= s.k_e) {
     for (int b = lo; b < hi; ++b)
       if (flags[b] & F_ELIG) flags[b] |= F_E;
-  } else if (n_elig <= 1024) {
+  } else if (n_elig <= 1024 && !s.test_radix) {
     unsigned long long* ek = reinterpret_cast<unsigned long long*>(zs);
     for (int b = lo; b < hi; ++b)
       if (flags[b] & F_ELIG) ek[epos++] = rank_key(orderable(sek[b]), b);

@@ -22,6 +22,8 @@ NOSA_F_TEST_ZERO_WAIT = 1
 NOSA_F_TEST_BAD_SLOT = 2
 NOSA_F_UNFUSED_STEP = 4
 NOSA_F_DMA_BIAS = 8
+NOSA_F_TEST_RADIX_TOPK = 16
+NOSA_MERGE_AUTO, NOSA_MERGE_KERNEL, NOSA_MERGE_TICKET, NOSA_MERGE_CLUSTER = 0, 1, 2, 3
 
 # every entry point declared in include/nosa.h
 EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_destroy", "nosa_set_stream",
@@ -39,7 +41,11 @@ class nosa_config(ctypes.Structure):
                 ("k_q", ctypes.c_int32), ("k_e", ctypes.c_int32), ("sink_blocks", ctypes.c_int32),
                 ("window_tokens", ctypes.c_int32), ("max_context", ctypes.c_int32),
                 ("evict_hidden", ctypes.c_int32), ("gather_ctas", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float), ("flags", ctypes.c_uint32)]
+                ("softmax_scale", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("score_ctas", ctypes.c_int32), ("attend_blocks_per_cta", ctypes.c_int32),
+                ("attend_merge", ctypes.c_int32), ("decode_cluster", ctypes.c_int32),
+                ("decode_teams", ctypes.c_int32), ("decode_stages", ctypes.c_int32),
+                ("forecast_streams", ctypes.c_int32)]
 
 
 class nosa_sizes(ctypes.Structure):
@@ -104,7 +110,7 @@ def lib() -> ctypes.CDLL:
             "nosa_reset_stats": [vp],
             "nosa_debug_scores": [vp, i32, p, p],
             "nosa_export_state": [vp, i32, ctypes.POINTER(nosa_state_view)],
-            "nosa_attend_noalloc": [p, p, p, p, p, i32, i32, i32, i32, ctypes.c_float, p, vp],
+            "nosa_attend_noalloc": [p, p, p, p, p, i32, i32, i32, i32, ctypes.c_float, p, p, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -143,10 +149,13 @@ def _check(st: int, where: str):
 
 def make_config(*, num_layers, batch, num_q_heads, num_kv_heads, k_q, k_e, window_tokens, max_context,
                 head_dim=128, block_size=64, cmp_kernel=32, cmp_stride=16, sink_blocks=1, evict_hidden=128,
-                gather_ctas=0, softmax_scale=0.0, flags=0) -> nosa_config:
+                gather_ctas=0, softmax_scale=0.0, flags=0, score_ctas=0, attend_blocks_per_cta=0,
+                attend_merge=0, decode_cluster=0, decode_teams=0, decode_stages=0,
+                forecast_streams=0) -> nosa_config:
     return nosa_config(ctypes.sizeof(nosa_config), num_layers, batch, num_q_heads, num_kv_heads, head_dim,
                        block_size, cmp_kernel, cmp_stride, k_q, k_e, sink_blocks, window_tokens, max_context,
-                       evict_hidden, gather_ctas, softmax_scale, flags)
+                       evict_hidden, gather_ctas, softmax_scale, flags, score_ctas, attend_blocks_per_cta,
+                       attend_merge, decode_cluster, decode_teams, decode_stages, forecast_streams)
 
 
 # ------------------------------------------------------------------ entry points
@@ -279,8 +288,10 @@ def nosa_export_state(ctx, layer, **arrays) -> None:
 
 
 def nosa_attend_noalloc(q, cache, sel, sel_slot, n_sel, units, group, cache_slots, context_len, out,
-                        softmax_scale=0.0, stream=0) -> None:
-    """Attention over a caller-owned block cache without any device allocation (see include/nosa.h)."""
+                        softmax_scale=0.0, err_out=None, stream=0) -> None:
+    """Attention over a caller-owned block cache without any device allocation (see include/nosa.h).
+    err_out: optional device int32 that receives the call's device-side error bits."""
     _check(lib().nosa_attend_noalloc(_ptr(q), _ptr(cache), _ptr(sel), _ptr(sel_slot), _ptr(n_sel), units, group,
-                                     cache_slots, context_len, softmax_scale, _ptr(out), stream or None),
+                                     cache_slots, context_len, softmax_scale, _ptr(out), _ptr(err_out),
+                                     stream or None),
            "nosa_attend_noalloc")

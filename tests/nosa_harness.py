@@ -71,7 +71,7 @@ class Parity:
     """Drives one context through the C ABI and checks sampled units against the oracle."""
 
     def __init__(self, wl: syn.Workload, sample_units=None, layers=None, gather_ctas=0, device="cuda",
-                 check_scores=True, flags=0):
+                 check_scores=True, flags=0, **sizing):
         import torch
         from offloadable_block_sparse_gb300 import nosa as N
         self.torch, self.N = torch, N
@@ -87,7 +87,7 @@ class Parity:
                                  num_kv_heads=wl.kv_heads, k_q=wl.k_q, k_e=wl.k_e,
                                  window_tokens=wl.window_tokens, max_context=wl.max_context,
                                  sink_blocks=wl.sink_blocks, evict_hidden=wl.evict_hidden,
-                                 gather_ctas=gather_ctas, flags=flags)
+                                 gather_ctas=gather_ctas, flags=flags, **sizing)
         self.sizes = N.nosa_query_sizes(self.cfg)
         self.stream = torch.cuda.current_stream()
         self.ctx = N.nosa_create(self.cfg, self.stream.cuda_stream)

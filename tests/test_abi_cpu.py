@@ -45,13 +45,24 @@ def test_validate_config():
     assert N.nosa_validate_config(_cfg()) == N.NOSA_OK
     bad = [dict(head_dim=64), dict(block_size=32), dict(cmp_kernel=16), dict(cmp_stride=8),
            dict(num_q_heads=15), dict(num_q_heads=32, num_kv_heads=2), dict(k_q=-1), dict(window_tokens=100),
-           dict(max_context=0), dict(max_context=1 << 20), dict(evict_hidden=100), dict(flags=16),
-           dict(k_q=200, k_e=100), dict(batch=4097, num_kv_heads=1, num_q_heads=8), dict(softmax_scale=-1.0)]
+           dict(max_context=0), dict(max_context=1 << 20), dict(evict_hidden=100), dict(flags=32),
+           dict(k_q=200, k_e=100), dict(batch=4097, num_kv_heads=1, num_q_heads=8), dict(softmax_scale=-1.0),
+           dict(score_ctas=9), dict(score_ctas=-1), dict(attend_blocks_per_cta=65), dict(attend_merge=4),
+           dict(decode_cluster=9), dict(decode_teams=3), dict(decode_stages=1), dict(decode_stages=7),
+           dict(forecast_streams=3)]
     for b in bad:
         assert N.nosa_validate_config(_cfg(**b)) == N.NOSA_ERR_INVALID_ARG, b
     c = _cfg()
     c.struct_size = 4
     assert N.nosa_validate_config(c) == N.NOSA_ERR_INVALID_ARG
+
+
+def test_sizing_overrides_are_accepted():
+    good = [dict(score_ctas=1), dict(score_ctas=8), dict(attend_blocks_per_cta=1), dict(attend_blocks_per_cta=64),
+            dict(attend_merge=N.NOSA_MERGE_TICKET), dict(attend_merge=N.NOSA_MERGE_CLUSTER),
+            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1)]
+    for g in good:
+        assert N.nosa_validate_config(_cfg(**g)) == N.NOSA_OK, g
 
 
 def test_test_hook_flags_are_accepted():

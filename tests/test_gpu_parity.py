@@ -23,9 +23,12 @@ FUSED, UNFUSED = 0, N.NOSA_F_UNFUSED_STEP
 STEP_MODES = pytest.mark.parametrize("mode", [FUSED, UNFUSED], ids=["fused", "three-kernels"])
 
 
-def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0, separate_fetch=True, flags=0):
-    p = Parity(wl, sample_units=samples, layers=layers, gather_ctas=gather_ctas, flags=flags)
+def run(wl, steps, samples=None, layers=None, split_calls=False, gather_ctas=0, separate_fetch=True, flags=0,
+        plan=None, **sizing):
+    p = Parity(wl, sample_units=samples, layers=layers, gather_ctas=gather_ctas, flags=flags, **sizing)
     try:
+        if plan is not None:  # the step form the test is about is the one that runs
+            assert N.nosa_step_plan(p.ctx) == plan, N.nosa_step_plan(p.ctx)
         p.load_context()
         for _ in range(steps):
             p.run_step(split_calls=split_calls, separate_fetch=separate_fetch)
@@ -130,12 +133,75 @@ def test_sparse_prefill_by_steps_from_one_token(mode):
     assert min(log.gammas) < 1.0  # the selection moved: blocks were dropped during the prompt
 
 
-def test_gather_cta_counts_agree():
-    wl = syn.Workload("ctas", layers=1, batch=4, q_heads=16, kv_heads=2, context=4096, k_q=4, k_e=12,
-                      window_tokens=256, steps=6, sigma=1.0)
-    for ctas in (1, 8, 64):
-        log, _ = run(wl, wl.steps, gather_ctas=ctas)
-        assert log.unit_steps == 6 * 8
+@pytest.mark.parametrize("ctas", [1, 8, 64, 152])
+def test_gather_cta_counts_agree(ctas):
+    # the separate calls with nosa_fetch: the persistent gather kernel copies every new block
+    # (the cold first step's whole selection, then the query-aware picks) at each CTA count
+    wl = syn.Workload("ctas", layers=2, batch=4, q_heads=16, kv_heads=2, context=4096, k_q=4, k_e=12,
+                      window_tokens=256, steps=8, sigma=1.0)
+    log, stats = run(wl, wl.steps, gather_ctas=ctas, split_calls=True, separate_fetch=True)
+    assert log.unit_steps == 8 * 16
+    assert log.fetched > 16 * 21  # more than the cold step's blocks: later steps fetched too
+    assert stats.blocks_fetched == log.fetched
+
+
+# Kernel sizing overrides (nosa_config): every non-default choice against the oracle, with the
+# step form it belongs to checked through nosa_step_plan.  sigma 1.0 moves the selection.
+SIZING = [
+    (dict(score_ctas=1), UNFUSED, (3, 0)),
+    (dict(score_ctas=3), UNFUSED, (3, 0)),
+    (dict(score_ctas=8), UNFUSED, (3, 0)),
+    (dict(attend_blocks_per_cta=1), UNFUSED, (3, 0)),
+    (dict(attend_blocks_per_cta=64), UNFUSED, (3, 0)),
+    (dict(attend_merge=N.NOSA_MERGE_TICKET), UNFUSED, (2, 0)),
+    (dict(attend_merge=N.NOSA_MERGE_CLUSTER), UNFUSED, (2, 0)),
+    (dict(attend_merge=N.NOSA_MERGE_TICKET, attend_blocks_per_cta=3), UNFUSED, (2, 0)),
+    (dict(decode_cluster=1), FUSED, (1, 1)),
+    (dict(decode_cluster=2), FUSED, (1, 2)),
+    (dict(decode_cluster=8), FUSED, (1, 8)),
+    (dict(decode_teams=1), FUSED, None),
+    (dict(decode_stages=2), FUSED, None),
+    (dict(decode_teams=1, decode_stages=6), FUSED, None),
+]
+
+
+@pytest.mark.parametrize("sizing,mode,plan", SIZING,
+                         ids=["-".join(f"{k}{v}" for k, v in z.items()) for z, _, _ in SIZING])
+def test_sizing_overrides(sizing, mode, plan):
+    wl = syn.workload("tiny", steps=16, sigma=1.0)
+    log, _ = run(wl, wl.steps, flags=mode, plan=plan, **sizing)
+    assert log.unit_steps == 32
+    if mode == FUSED:  # the fused kernel, not the chain, ran
+        p = Parity(wl, sample_units=[], flags=mode, **sizing)
+        try:
+            assert N.nosa_step_plan(p.ctx)[0] == 1
+        finally:
+            p.close()
+    # the separate calls with the same sizing
+    log, _ = run(syn.workload("tiny", steps=6, sigma=1.0), 6, flags=mode, split_calls=True, **sizing)
+    assert log.unit_steps == 12
+
+
+@STEP_MODES
+def test_radix_topk_hook(mode):
+    # the warp radix select for the query-agnostic part at every step (normally only beyond 1024
+    # eligible blocks): the same selections as the oracle's
+    wl = syn.workload("tiny", steps=24, sigma=1.0)
+    log, _ = run(wl, wl.steps, flags=mode | N.NOSA_F_TEST_RADIX_TOPK)
+    assert log.unit_steps == 48
+
+
+@STEP_MODES
+def test_long_context_first_selection_takes_the_radix_select(mode):
+    # 70,000 tokens: 1094 blocks, so the first selection after the bulk load has more than 1024
+    # eligible blocks (every candidate outside the query-aware picks) and takes the warp radix
+    # select without any hook; later steps rank the few never-dropped candidates directly
+    wl = syn.Workload("long70k", layers=1, batch=2, q_heads=16, kv_heads=2, context=70000, k_q=16, k_e=48,
+                      window_tokens=1024, steps=3, sigma=0.3)
+    nb = -(-70001 // 64)
+    assert nb - 16 - 1 - 16 > 1024
+    log, _ = run(wl, wl.steps, flags=mode)
+    assert log.unit_steps == 3 * 4
 
 
 def test_capacity_error_leaves_state_unchanged():
@@ -338,10 +404,11 @@ def test_forecast_new_tail_block_is_prefetched():
         p.close()
 
 
-def test_forecast_pipeline_overlaps_the_next_layer():
+@pytest.mark.parametrize("streams", [0, 1], ids=["two-streams", "one-stream"])
+def test_forecast_pipeline_overlaps_the_next_layer(streams):
     wl = syn.Workload("fc_pipe", layers=3, batch=3, q_heads=16, kv_heads=2, context=3000, k_q=4, k_e=12,
                       window_tokens=256, steps=30, sigma=1.0)
-    p = Parity(wl)
+    p = Parity(wl, forecast_streams=streams)
     try:
         p.load_context()
         p.run_forecast_pipeline(wl.steps)
