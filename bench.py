@@ -84,6 +84,9 @@ def parse():
               "decode-stages", "forecast-streams"):
         ap.add_argument(f"--{f}", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="three-kernel step even where the fused kernel fits")
+    ap.add_argument("--prefill", action="store_true",
+                    help="NOSA_S sparse prefill of the workload's context length as one prompt, every layer, "
+                         "from empty layers (nosa_prefill); prints a prefill tok/s line")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -747,6 +750,74 @@ def run_dense(args, rank, world, local_rank):
             "kv_resident_gb": kv.numel() * 2 / 1e9}
 
 
+def run_prefill(args, rank, world, local_rank):
+    """NOSA_S sparse prefill: a prompt of the workload's context length through every layer (nosa_prefill),
+    each timed repetition on a fresh context (a prefill starts from empty layers)."""
+    import torch
+    from offloadable_block_sparse_gb300 import nosa as N
+    from synth import inputs as syn
+    torch.cuda.set_device(local_rank)
+    over = {"sigma": args.sigma} if args.sigma is not None else {}
+    wl = syn.workload(args.workload, **over)
+    L = args.layers or wl.layers
+    B, Hq, Hkv, d, n = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.context
+    U = B * Hkv
+    gen = torch.Generator(device="cuda").manual_seed(1000 * rank + 23)
+    q = torch.randn((B, Hq, n, d), generator=gen, device="cuda")
+    q = (q / q.norm(dim=-1, keepdim=True) * math.sqrt(d)).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, n, d), generator=gen, device="cuda").to(torch.bfloat16)
+    v = torch.randn((B, Hkv, n, d), generator=gen, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(q)
+    cgen = torch.Generator().manual_seed(1000 * rank + 29)
+    heads = [((torch.randn((Hkv, d, wl.evict_hidden), generator=cgen) / math.sqrt(d)).float().numpy(),
+              (torch.randn((Hkv, wl.evict_hidden), generator=cgen) / math.sqrt(wl.evict_hidden)).float().numpy())
+             for _ in range(L)]
+    flags = N.NOSA_F_DMA_BIAS if args.dma_bias else 0
+    cfg = N.make_config(num_layers=L, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
+                        window_tokens=wl.window_tokens, max_context=n + 1, sink_blocks=wl.sink_blocks,
+                        evict_hidden=wl.evict_hidden, flags=flags, **sizing_overrides(args))
+    stream = torch.cuda.current_stream()
+    times = []
+    K, W = max(args.steps, 1), max(args.warmup, 1)
+    scratch, nbytes = None, 0
+    clocks = ClockSampler(local_rank)
+    i16 = torch.int16
+    for rep in range(W + K):
+        ctx = N.nosa_create(cfg, stream.cuda_stream)
+        for l in range(L):
+            N.nosa_set_eviction_head(ctx, l, *heads[l])
+        if scratch is None:
+            nbytes = N.nosa_prefill_scratch_bytes(ctx, n)
+            scratch = torch.empty(nbytes // 2 + 64, dtype=torch.int16, device="cuda")
+        torch.cuda.synchronize()
+        if rep == W:
+            clocks.start()
+            time.sleep(0.3)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for l in range(L):
+            N.nosa_prefill(ctx, l, q.view(i16), k.view(i16), v.view(i16), n, out.view(i16), scratch, nbytes)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if N.nosa_sync(ctx) != N.NOSA_OK:
+            raise RuntimeError("device error in the prefill")
+        if rep >= W:
+            times.append(a.elapsed_time(b))
+        stats = N.nosa_get_stats(ctx)
+        N.nosa_destroy(ctx)
+    ck = clocks.stop()
+    ms = slowest_rank_ms(statistics.mean(times), world, "cuda")
+    return {"metric": "sparse prefill tok/s (NOSA_S, attn path, 1 GB300)", "value": job_throughput(B * n, world, ms),
+            "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(workload_config(wl, args, L, world), prompt_tokens=n,
+                           selection="NOSA_S: every prompt position selected as the decode step would, in order"),
+            "gpu_launches": 6 * L * K, "clocks": ck,
+            "step": "one prompt of context tokens per sequence through every layer (nosa_prefill per layer)",
+            "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min},
+            "blocks_selected_fetched": stats.blocks_fetched}
+
+
 def run_reference(args):
     """The oracle, as it stands, on host cores: each step is a bounded sample of the workload."""
     from synth import inputs as syn
@@ -780,7 +851,12 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    res = run_dense(args, rank, world, local_rank) if args.dense else run_native(args, rank, world, local_rank)
+    if args.dense:
+        res = run_dense(args, rank, world, local_rank)
+    elif args.prefill:
+        res = run_prefill(args, rank, world, local_rank)
+    else:
+        res = run_native(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

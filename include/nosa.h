@@ -335,6 +335,33 @@ nosa_status nosa_dense_attend(const uint16_t* q, const uint16_t* kv, int units, 
 /* Scratch bytes nosa_dense_attend needs (0 on a bad argument or without a device). */
 size_t nosa_dense_scratch_bytes(int units, int context_len);
 
+/* NOSA_S sparse prefill of an empty `layer` (T = 0): appends a prompt of n_tokens tokens to
+ * every sequence and attends every prompt position over its own block selection, in one call.
+ * Defined by: NOSA wiki, "Results" (NOSA_S: sparse attention in prefill as well as in
+ * decoding) and "How NOSA works" (a block the query-agnostic part drops at one step is never
+ * re-selected by it, so a position's selection depends on the earlier positions').  The
+ * selection for prompt position t is the one the decode step at T = t + 1 makes, with the
+ * eviction state carried from position t - 1: the positions are selected in order (one CTA per
+ * unit), then the attention of all positions runs in one launch, reading the prompt's K/V from
+ * k and v.  Afterwards the layer's state (host store, compressed keys, scores, eviction bitmap,
+ * cache slots and their contents, last selection, counters) is the state n_tokens calls of
+ * nosa_step with the same tokens would leave, and decoding continues with nosa_step.
+ *   q, out   device bf16 [B][Hq][n_tokens][d] (out[b][h][t] is position t's attention output)
+ *   k, v     device bf16 [B][Hkv][n_tokens][d], 16-byte aligned
+ *   scratch  device memory of at least nosa_prefill_scratch_bytes(ctx, n_tokens) bytes, 4-byte
+ *            aligned.  Afterwards it holds every position's selection: int16 [B][Hkv][n_tokens]
+ *            [cache_slots], ascending, -1 padded; entry bits 0-11 are the block, bits 12-13
+ *            its kind (0 sink, 1 window, 2 query-aware, 3 query-agnostic)
+ * NOSA_ERR_STATE if the layer is not empty; NOSA_ERR_CAPACITY if n_tokens exceeds max_context or
+ * the prompt length one selector CTA holds (nosa_prefill_scratch_bytes returns the scratch size
+ * for any length; 131,072 tokens at most, fewer when the selector state of the context's
+ * max_context would not fit one CTA's shared memory), or if the scratch is too small. */
+nosa_status nosa_prefill(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         int n_tokens, uint16_t* out, void* scratch, size_t scratch_bytes);
+
+/* Scratch bytes nosa_prefill needs for a prompt of n_tokens (0 on a bad argument). */
+size_t nosa_prefill_scratch_bytes(nosa_ctx* ctx, int n_tokens);
+
 /* How nosa_step runs on this context: *kernels_per_layer = the kernel launches of
  * one layer's step: 1 (the fused decode kernel, one thread-block cluster of
  * *cluster_size CTAs per unit), or 3 (the selector kernel, which also appends the

@@ -11,7 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnosa.so")
-SOURCES = ["api.cu", "append.cu", "select.cu", "fetch.cu", "attend.cu", "decode.cu", "dense.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "append.cu", "select.cu", "fetch.cu", "attend.cu", "decode.cu", "dense.cu", "noalloc.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]

@@ -466,11 +466,38 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
       free_ctx(c);
       return NOSA_ERR_CUDA;
     }
+    // sparse prefill: one selector CTA per unit holds the logits of every window of the prompt;
+    // the longest prompt (up to max_context) whose selector state fits the shared memory
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    LayerState sp = s0;
+    sp.score_chunks = 1;
+    c->pf_max_tokens = std::min(cfg->max_context, prefill_max_tokens());
+    for (;;) {
+      const int ncp = std::max(c->pf_max_tokens < kCmpKernel ? 0 : (c->pf_max_tokens - kCmpKernel) / kCmpStride + 1, 1);
+      sp.score_wpc = cdiv(ncp, 16 * kScoreWarps) * 16 * kScoreWarps;
+      if (prefill_select_smem(sp) + 8 * 1024 <= (size_t)optin || c->pf_max_tokens <= kBlock) break;
+      c->pf_max_tokens -= 16 * kScoreWarps * kCmpStride;  // one tile row of windows less
+    }
+    c->pf_wpc = sp.score_wpc;
+    if (init_prefill(sp) != cudaSuccess) {
+      (void)cudaGetLastError();
+      c->pf_max_tokens = 0;
+    }
   }
-  // forecast pipeline: a prefetch stream and its events
-  bool ev_ok = cudaStreamCreateWithFlags(&c->pref_stream, cudaStreamNonBlocking) == cudaSuccess &&
-               cudaStreamCreateWithFlags(&c->sel_stream, cudaStreamNonBlocking) == cudaSuccess &&
-               cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
+  // forecast pipeline: a selection and a prefetch stream and their events.  Both streams take the
+  // device's highest priority: their kernels (the next layer's selection and its host copies) are
+  // on the step's critical path, so their CTAs are scheduled ahead of the current layer's
+  // remaining attention CTAs as SMs free up.
+  int prio_least = 0, prio_greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest) != cudaSuccess) {
+    (void)cudaGetLastError();
+    prio_greatest = 0;
+  }
+  bool ev_ok =
+      cudaStreamCreateWithPriority(&c->pref_stream, cudaStreamNonBlocking, prio_greatest) == cudaSuccess &&
+      cudaStreamCreateWithPriority(&c->sel_stream, cudaStreamNonBlocking, prio_greatest) == cudaSuccess &&
+      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) == cudaSuccess;
   for (int l = 0; l < c->L && ev_ok; ++l)
     ev_ok = cudaEventCreateWithFlags(&c->ev_pref[l], cudaEventDisableTiming) == cudaSuccess &&
             cudaEventCreateWithFlags(&c->ev_sel[l], cudaEventDisableTiming) == cudaSuccess;
@@ -750,6 +777,47 @@ nosa_status nosa_step_host_all(nosa_ctx* c, const uint16_t* q, const uint16_t* k
     if (st != NOSA_OK) return st;
   }
   CK(cudaMemcpyAsync(out, c->step_out, c->L * qL * 2, cudaMemcpyDeviceToHost, c->stream));
+  return NOSA_OK;
+}
+
+size_t nosa_prefill_scratch_bytes(nosa_ctx* c, int n_tokens) {
+  if (!c || n_tokens < 1) return 0;
+  return (size_t)c->U * (size_t)n_tokens * (size_t)c->cap * sizeof(int16_t);
+}
+
+nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         int n_tokens, uint16_t* out, void* scratch, size_t scratch_bytes) {
+  nosa_status st = check_ctx(c, layer);
+  if (st != NOSA_OK) return st;
+  if (!q || !k || !v || !out || !scratch || n_tokens < 1) return NOSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16) return NOSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(scratch) % 4) return NOSA_ERR_INVALID_ARG;
+  if (c->T_host[layer] != 0) return NOSA_ERR_STATE;  // a prefill starts an empty layer
+  if (n_tokens > c->cfg.max_context || n_tokens > c->pf_max_tokens) return NOSA_ERR_CAPACITY;
+  if (scratch_bytes < nosa_prefill_scratch_bytes(c, n_tokens)) return NOSA_ERR_CAPACITY;
+  st = join_layer(c, layer);
+  if (st != NOSA_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return NOSA_ERR_CUDA;
+  // the prompt's K and V, [U][n][d] each: boxes of 64 dims x 64 tokens with the 128-byte swizzle
+  CUtensorMap tk, tv;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_tokens, (cuuint64_t)c->U};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)n_tokens * kHeadDim * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kBlock, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  for (int i = 0; i < 2; ++i)
+    if (enc(i ? &tv : &tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(i ? v : k), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return NOSA_ERR_INVALID_ARG;
+  LayerState s = layer_state(c, layer);
+  CK(launch_append_bulk(s, k, v, 0, n_tokens, c->stream));
+  s.score_chunks = 1;
+  s.score_wpc = c->pf_wpc;
+  CK(launch_prefill(s, &tk, &tv, q, k, v, out, static_cast<int16_t*>(scratch), n_tokens, c->stream));
+  c->T_host[layer] = n_tokens;
+  c->sel_T[layer] = n_tokens;
+  c->fetch_T[layer] = n_tokens;  // every cache slot holds its block
   return NOSA_OK;
 }
 

@@ -64,9 +64,14 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   // Work split: the unit's selected blocks are dealt round-robin to its CTAs in an
   // order that puts the blocks still to be copied from the host first, so those
-  // few spread one per CTA and their copies start before anything else.
+  // few spread one per CTA.  Each unit starts dealing at its own chunk (u mod CS), so
+  // neighbouring units' host blocks land on different chunks and every wave of CTAs
+  // carries about the same share of host copies: the link stays busy for the whole
+  // launch while the cached blocks stream from HBM, instead of the first waves waiting
+  // on the link and the last ones on HBM.
   const int CS = kChunksAlongX ? gridDim.x : gridDim.y;  // the unit's CTAs
-  const int nblk = chunk < nsel ? (nsel - chunk + CS - 1) / CS : 0;
+  const int c0 = (chunk - u % CS + CS) % CS;             // this CTA's dealing positions: c0, c0 + CS, ...
+  const int nblk = c0 < nsel ? (nsel - c0 + CS - 1) / CS : 0;
   if (warp == 0) {
     // one round trip: every entry's block, slot and fetched mark, requested with the count
     int ev[kMaxCacheSlots / 32][3];
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
       const int pos = nw ? seen_new + __popc(bn & below) : n_new + seen_old + __popc(bo & below);
       seen_new += __popc(bn);
       seen_old += __popc(bo);
-      if (in && pos % CS == chunk) {
+      if (in && pos % CS == c0) {
         const int i = pos / CS;
         int slot = ev[it][1];
         if (slot < 0 || slot >= s.cap) {

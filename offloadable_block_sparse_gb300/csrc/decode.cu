@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
   if (tid < 2 && b_se < geo.ws) m.sek[b_se] = se_patch;  // read by the selection after its first barrier
   const int NW = kTeams * CS, wkr = kTeams * rank + team;  // workers of the unit, this one
   const int total_S = leader_select(s, u, geo, CS, m, sh, my_slot_blk, rank == 0,
-                                    [&](int pos, int b, int slot, bool isnew, int dp) {
+                                    [&](int pos, int b, int slot, bool isnew, int dp, int) {
                                       const int w = dp % NW;
                                       if (w / kTeams != rank || dp >= s.cap) return;
                                       if (slot < 0 || slot >= s.cap) {

@@ -29,6 +29,9 @@ struct nosa_ctx {
   // fused decode kernel (nosa_step): cluster size (0: off, three kernels instead), windows per
   // scoring CTA, attention stages per team
   int dec_cs, dec_wpc, dec_nst, dec_teams;
+  // sparse prefill: windows per selector CTA for the longest prompt whose selector state fits
+  // shared memory, and that prompt length (0: the prefill kernels could not be set up)
+  int pf_wpc, pf_max_tokens;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   uint16_t *step_q, *step_k, *step_v, *step_out;  // every layer's inputs and outputs (nosa_step_host_all)
@@ -85,4 +88,13 @@ cudaError_t init_decode(const LayerState& s, int teams, int nst);
 int decode_active_clusters(const LayerState& s, int teams, int nst, int cs);
 cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, uint16_t* out, int teams, int nst, bool pdl, cudaStream_t st);
+// sparse prefill of an empty layer (after the bulk append of the prompt): selections of every
+// position in order into hist [U][n][cap], cache slots refreshed from the prompt, attention of
+// every position.  s.score_chunks = 1 and s.score_wpc covers the prompt's windows.
+size_t prefill_select_smem(const LayerState& s);
+cudaError_t init_prefill(const LayerState& s);
+int prefill_max_tokens();
+cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
+                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, int n,
+                           cudaStream_t st);
 }  // namespace nosa

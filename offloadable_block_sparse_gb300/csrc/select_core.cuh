@@ -206,7 +206,7 @@ __device__ __forceinline__ Smem layout(unsigned char* dsm, const LayerState& s) 
 
 // A selection's consumer that takes nothing (the selection goes to global memory only).
 struct NoDeal {
-  __device__ __forceinline__ void operator()(int, int, int, bool, int) const {}
+  __device__ __forceinline__ void operator()(int, int, int, bool, int, int) const {}
 };
 
 // q fragments for the scorer.  The k order in each 32-dim chunk is permuted
@@ -503,9 +503,10 @@ __device__ __forceinline__ void leader_query(const LayerState& s, int u, const G
 // Phase 3b: the query-agnostic picks E, the selection S and the slots of its new blocks.
 // The writer (one CTA per unit) also stores the eviction update, slot tables, fetch list,
 // selection lists and statistics; every CTA that runs it on the same inputs reaches the
-// same selection.  deal(pos, b, slot, isnew, dp) is called for each selected block b at
-// list position pos < cap, with its slot (as published) and its dealing position dp: the
-// blocks without a slot first, then the rest, each in block order.  Returns |S|.
+// same selection.  deal(pos, b, slot, isnew, dp, kind) is called for each selected block b at
+// list position pos < cap, with its slot (as published), its dealing position dp (the blocks
+// without a slot first, then the rest, each in block order) and its kind (0 sink, 1 window,
+// 2 query-aware, 3 query-agnostic).  Returns |S|.
 template <typename Deal>
 __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geometry& geo, const Smem& m,
                                            SelShared& sh, int my_slot_blk, bool writer, Deal deal) {
@@ -628,13 +629,14 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
     const bool isnew = f & F_NEW;
     if (pos < s.cap) {
       const int slot = (s.test_bad_slot && u == 0 && pos == 0) ? s.cap : b2s[b];  // test hook
+      const int kd = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
       if (writer) {
         sel[pos] = b;
-        kind[pos] = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
+        kind[pos] = kd;
         sslot[pos] = slot;
         snew[pos] = isnew ? 1 : 0;
       }
-      deal(pos, b, slot, isnew, isnew ? nw_before : n_new_all + pos - nw_before);
+      deal(pos, b, slot, isnew, isnew ? nw_before : n_new_all + pos - nw_before, kd);
     } else if (writer) {
       atomicOr(s.err, kErrBounds);
     }

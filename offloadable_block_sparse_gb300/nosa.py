@@ -31,7 +31,8 @@ EXPORTS = ["nosa_validate_config", "nosa_query_sizes", "nosa_create", "nosa_dest
            "nosa_step_host", "nosa_step_host_all", "nosa_sync", "nosa_reset_state", "nosa_context_length", "nosa_get_stats",
            "nosa_reset_stats", "nosa_debug_scores", "nosa_export_state", "nosa_status_string",
            "nosa_attend_noalloc", "nosa_step_plan", "nosa_forecast_select", "nosa_step_forecast",
-           "nosa_forecast_join", "nosa_dense_attend", "nosa_dense_scratch_bytes"]
+           "nosa_forecast_join", "nosa_dense_attend", "nosa_dense_scratch_bytes", "nosa_prefill",
+           "nosa_prefill_scratch_bytes"]
 
 
 class nosa_config(ctypes.Structure):
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
             "nosa_dense_attend": [p, p, i32, i32, i32, i32, ctypes.c_float, p, p, ctypes.c_size_t, vp],
             "nosa_dense_scratch_bytes": [i32, i32],
             "nosa_step_plan": [vp, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+            "nosa_prefill": [vp, i32, p, p, p, i32, p, p, ctypes.c_size_t],
+            "nosa_prefill_scratch_bytes": [vp, i32],
             "nosa_reset_state": [vp],
             "nosa_context_length": [vp, i32, ctypes.POINTER(ctypes.c_int32)],
             "nosa_get_stats": [vp, ctypes.POINTER(nosa_stats)],
@@ -119,6 +122,7 @@ def lib() -> ctypes.CDLL:
         L.nosa_status_string.argtypes = [ctypes.c_int]
         L.nosa_status_string.restype = ctypes.c_char_p
         L.nosa_dense_scratch_bytes.restype = ctypes.c_size_t
+        L.nosa_prefill_scratch_bytes.restype = ctypes.c_size_t
         _lib = L
     return _lib
 
@@ -243,6 +247,16 @@ def nosa_dense_attend(q, kv, units, group, max_blocks, context_len, out, scratch
     """Dense decode attention over a device KV store [units][max_blocks][2][64][d] (see include/nosa.h)."""
     _check(lib().nosa_dense_attend(_ptr(q), _ptr(kv), units, group, max_blocks, context_len, softmax_scale,
                                    _ptr(out), _ptr(scratch), scratch_bytes, stream), "nosa_dense_attend")
+
+
+def nosa_prefill_scratch_bytes(ctx, n_tokens) -> int:
+    return int(lib().nosa_prefill_scratch_bytes(ctx, n_tokens))
+
+
+def nosa_prefill(ctx, layer, q, k, v, n_tokens, out, scratch, scratch_bytes) -> None:
+    """NOSA_S sparse prefill of an empty layer: q/out [B][Hq][n][d], k/v [B][Hkv][n][d] (see include/nosa.h)."""
+    _check(lib().nosa_prefill(ctx, layer, _ptr(q), _ptr(k), _ptr(v), n_tokens, _ptr(out), _ptr(scratch),
+                              scratch_bytes), "nosa_prefill")
 
 
 def nosa_step_plan(ctx):

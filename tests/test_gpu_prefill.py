@@ -1,0 +1,224 @@
+"""NOSA_S sparse prefill (nosa_prefill) against the CPU oracle.
+
+The oracle runs its decode step over the prompt, one position at a time from an
+empty context (the reading of sparse prefill taken here: position t gets the
+selection the decode step at T = t + 1 makes, the eviction state carried from
+t - 1).  The GPU selects every position in order and attends all positions in
+one launch.  Compared: every checked position's selection (blocks and kinds)
+bit-exact, near ties logged and adopted as in the decode tests; outputs within
+max-abs 2e-2 / mean-abs 2e-3 and the tighter relative bound; the layer's state
+after the prompt (compressed keys, eviction bitmap, slot map, last selection and
+fetch list) bit-exact; then a few decode steps continue from that state, which
+checks the cache the prefill leaves behind.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import nosa_oracle as O
+from synth import inputs as syn
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from tests.nosa_harness import OUT_MAX_ABS, OUT_MEAN_ABS, _near_tie_ok  # noqa: E402
+from offloadable_block_sparse_gb300 import nosa as N  # noqa: E402
+
+FUSED, UNFUSED = 0, N.NOSA_F_UNFUSED_STEP
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def _check_out(got, ref, where):
+    err = np.abs(got - ref)
+    assert err.max() <= OUT_MAX_ABS and err.mean() <= OUT_MEAN_ABS, f"output error {err.max():.3e} {where}"
+    assert err.max() <= 2 ** -7 * np.abs(ref).max() + 1e-4, f"output error {err.max():.3e} (tight) {where}"
+    return float(err.max())
+
+
+def _select_and_adopt(o, sq, se, T, Q_gpu, E_gpu, k_q, k_e, ties, where):
+    """The oracle's picks at context length T; a differing pick must be a near tie, then the GPU's is adopted."""
+    _, C, _ = O.partition(T, o.nw, o.sink, o.block)
+    Q = O.select_query_aware(sq, C, k_q)
+    if Q != Q_gpu:
+        assert _near_tie_ok(np.asarray(sq).astype(np.float32), Q_gpu, Q, C, k_q), f"query-aware pick {where}"
+        ties.append(("q", where))
+        Q = Q_gpu
+    E = O.select_query_agnostic(se, C, Q, o.evicted, k_e)
+    if E != E_gpu:
+        pool = [b for b in C if b not in set(Q) and b not in o.evicted]
+        assert _near_tie_ok(np.asarray(se).astype(np.float32), E_gpu, E, pool, k_e), f"query-agnostic pick {where}"
+        ties.append(("e", where))
+        E = E_gpu
+    return Q, E
+
+
+def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3):
+    """Prefill n tokens into an empty layer, check against the oracle, then decode_steps steps."""
+    B, Hq, Hkv, d, G = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.group
+    U = B * Hkv
+    assert n + decode_steps <= wl.steps and wl.context == 0
+    cfg = N.make_config(num_layers=1, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
+                        window_tokens=wl.window_tokens, max_context=n + decode_steps, sink_blocks=wl.sink_blocks,
+                        evict_hidden=wl.evict_hidden, flags=flags)
+    stream = torch.cuda.current_stream()
+    ctx = N.nosa_create(cfg, stream.cuda_stream)
+    ties, max_err = [], 0.0
+    try:
+        sz = N.nosa_query_sizes(cfg)
+        cap = sz.cache_slots
+        xs = {(b, g): wl.unit_inputs(0, b, g) for b in range(B) for g in range(Hkv)}
+        W1 = np.stack([xs[(0, g)]["W1"] for g in range(Hkv)]).astype(np.float32)
+        W2 = np.stack([xs[(0, g)]["W2"] for g in range(Hkv)]).astype(np.float32)
+        N.nosa_set_eviction_head(ctx, 0, W1, W2)
+        q = np.zeros((B, Hq, n, d), np.uint16)
+        k = np.zeros((B, Hkv, n, d), np.uint16)
+        v = np.zeros((B, Hkv, n, d), np.uint16)
+        for (b, g), x in xs.items():
+            q[b, g * G:(g + 1) * G] = x["Q"][:n].transpose(1, 0, 2)
+            k[b, g] = x["K"][:n]
+            v[b, g] = x["V"][:n]
+        qd, kd, vd = _dev(q), _dev(k), _dev(v)
+        out = torch.full((B, Hq, n, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        nbytes = N.nosa_prefill_scratch_bytes(ctx, n)
+        assert nbytes == U * n * cap * 2
+        scratch = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda")
+        N.nosa_prefill(ctx, 0, qd, kd, vd, n, out.view(torch.int16), scratch, nbytes)
+        assert N.nosa_sync(ctx) == N.NOSA_OK
+        assert N.nosa_context_length(ctx, 0) == n
+        hist = scratch.cpu().numpy().reshape(U, n, cap)
+        out_h = out.float().cpu().numpy()
+        st = dict(sel=np.zeros((U, cap), np.int32), n_sel=np.zeros(U, np.int32), fetch=np.zeros((U, cap, 2), np.int32),
+                  n_fetch=np.zeros(U, np.int32), slot_blk=np.zeros((U, cap), np.int32),
+                  evicted=np.zeros((U, sz.evict_words), np.uint32),
+                  kt=np.zeros((U, max(sz.max_windows, 1), d), np.uint16))
+        N.nosa_export_state(ctx, 0, **st)
+        stats = N.nosa_get_stats(ctx)
+        assert stats.selections == U * n
+
+        oracles = {}
+        for (b, g) in check_units:
+            u = b * Hkv + g
+            x = xs[(b, g)]
+            o = O.UnitOracle(head_dim=d, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
+                             window_tokens=wl.window_tokens, max_context=n + decode_steps, W1=x["W1"], W2=x["W2"],
+                             dma_bias=bool(flags & N.NOSA_F_DMA_BIAS))
+            r = None
+            for t in range(n):
+                o.append(x["K"][t:t + 1], x["V"][t:t + 1])
+                sq, se = o.scores(x["Q"][t])
+                row = [int(h) for h in hist[u, t] if h >= 0]
+                blocks, kinds = [h & 0xFFF for h in row], [h >> 12 for h in row]
+                Qg = sorted(bb for bb, kk in zip(blocks, kinds) if kk == 2)
+                Eg = sorted(bb for bb, kk in zip(blocks, kinds) if kk == 3)
+                Q, E = _select_and_adopt(o, sq, se, o.T, Qg, Eg, wl.k_q, wl.k_e, ties, (u, t))
+                r = o.commit(Q, E)
+                assert blocks == r["S"], f"selection of position {t} unit {u}: {blocks} vs {r['S']}"
+                if t in out_positions:
+                    ref = o.attend(x["Q"][t], r["S"])
+                    max_err = max(max_err, _check_out(out_h[b, g * G:(g + 1) * G, t], ref, f"unit {u} position {t}"))
+            # the state after the prompt
+            assert np.array_equal(st["kt"][u, :o.nc], O.f64_to_bf16_bits(o.compressed_keys())), "K~"
+            assert list(st["sel"][u, :st["n_sel"][u]]) == r["S"]
+            assert list(st["slot_blk"][u]) == o.slot_blk, "slot map"
+            assert [tuple(f) for f in st["fetch"][u, :st["n_fetch"][u]]] == [tuple(f) for f in r["fetch"]]
+            ev = st["evicted"][u]
+            assert {bb for bb in range(o.nb) if (ev[bb >> 5] >> (bb & 31)) & 1} == o.evicted, "eviction bitmap"
+            oracles[(b, g)] = o
+
+        # decode continues from the prefill's state (cache slots refreshed from the prompt)
+        for j in range(decode_steps):
+            t = n + j
+            qs = np.zeros((B, Hq, d), np.uint16)
+            ks = np.zeros((B, Hkv, d), np.uint16)
+            vs = np.zeros((B, Hkv, d), np.uint16)
+            for (b, g), x in xs.items():
+                qs[b, g * G:(g + 1) * G] = x["Q"][t]
+                ks[b, g] = x["K"][t]
+                vs[b, g] = x["V"][t]
+            od = torch.empty((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+            N.nosa_step(ctx, 0, _dev(qs), _dev(ks), _dev(vs), od.view(torch.int16))
+            assert N.nosa_sync(ctx) == N.NOSA_OK
+            kinds = np.zeros((U, cap), np.int32)
+            sel = np.zeros((U, cap), np.int32)
+            nsel = np.zeros(U, np.int32)
+            N.nosa_export_state(ctx, 0, sel=sel, sel_kind=kinds, n_sel=nsel)
+            oh = od.float().cpu().numpy()
+            for (b, g), o in oracles.items():
+                u = b * Hkv + g
+                x = xs[(b, g)]
+                o.append(x["K"][t:t + 1], x["V"][t:t + 1])
+                sq, se = o.scores(x["Q"][t])
+                S_gpu = list(sel[u, :nsel[u]])
+                Qg = sorted(int(bb) for bb, kk in zip(S_gpu, kinds[u, :nsel[u]]) if kk == 2)
+                Eg = sorted(int(bb) for bb, kk in zip(S_gpu, kinds[u, :nsel[u]]) if kk == 3)
+                Q, E = _select_and_adopt(o, sq, se, o.T, Qg, Eg, wl.k_q, wl.k_e, ties, (u, t))
+                r = o.commit(Q, E)
+                assert S_gpu == r["S"], f"decode step {j} after the prefill, unit {u}"
+                max_err = max(max_err, _check_out(oh[b, g * G:(g + 1) * G], o.attend(x["Q"][t], r["S"]),
+                                                  f"decode step {j} unit {u}"))
+    finally:
+        N.nosa_destroy(ctx)
+    print(f"[prefill n={n}] units={len(check_units)} near_ties={len(ties)} max_out_abs={max_err:.2e}")
+    return ties
+
+
+@pytest.mark.parametrize("mode", [FUSED, UNFUSED], ids=["fused-decode", "three-kernel-decode"])
+def test_prefill_640_every_position(mode):
+    # k = 3 with a 2-block window: the selection turns sparse once the prompt passes 6 blocks, so
+    # evictions and the window sliding over the budget all happen inside the prompt
+    wl = syn.Workload("pf640", layers=1, batch=2, q_heads=16, kv_heads=2, context=0, k_q=1, k_e=2,
+                      window_tokens=128, steps=644, sigma=0.3)
+    units = [(b, g) for b in range(2) for g in range(2)]
+    run_prefill(wl, 640, units, set(range(640)), flags=mode, decode_steps=4)
+
+
+def test_prefill_ragged_group4_dma_bias():
+    # a prompt that ends mid-block and mid-window, 8 q heads over 2 kv heads, with the attention bias
+    wl = syn.Workload("pf_ragged", layers=1, batch=3, q_heads=8, kv_heads=2, context=0, k_q=3, k_e=5,
+                      window_tokens=128, steps=1004, sigma=1.0)
+    units = [(b, g) for b in range(3) for g in range(2)]
+    run_prefill(wl, 1001, units, set(range(1001)), flags=N.NOSA_F_DMA_BIAS, decode_steps=3)
+
+
+def test_prefill_16k_prompt_sampled_positions():
+    # the 1B-shaped layer (16/2 heads, k_q 16, k_e 48, 1024-token window) over a 16K prompt: one
+    # unit's selection checked at every position, its outputs at sampled positions
+    n = 16384
+    wl = syn.Workload("pf16k", layers=1, batch=1, q_heads=16, kv_heads=2, context=0, k_q=16, k_e=48,
+                      window_tokens=1024, steps=n + 2, sigma=0.3)
+    pos = set(range(0, n, 61)) | set(range(n - 8, n)) | {63, 64, 65, 1023, 1024, 1025}
+    run_prefill(wl, n, [(0, 1)], pos, decode_steps=2)
+
+
+def test_prefill_argument_checks():
+    cfg = N.make_config(num_layers=2, batch=1, num_q_heads=16, num_kv_heads=2, k_q=2, k_e=2, window_tokens=128,
+                        max_context=300)
+    ctx = N.nosa_create(cfg, torch.cuda.current_stream().cuda_stream)
+    try:
+        n = 200
+        q = torch.zeros((1, 16, n, 128), dtype=torch.int16, device="cuda")
+        kv = torch.zeros((1, 2, n, 128), dtype=torch.int16, device="cuda")
+        nb = N.nosa_prefill_scratch_bytes(ctx, n)
+        scratch = torch.zeros(nb // 2 + 8, dtype=torch.int16, device="cuda")
+        with pytest.raises(N.NosaError) as e:      # scratch too small
+            N.nosa_prefill(ctx, 0, q, kv, kv, n, q, scratch, nb - 2)
+        assert e.value.status == N.NOSA_ERR_CAPACITY
+        with pytest.raises(N.NosaError) as e:      # longer than the context's capacity
+            N.nosa_prefill(ctx, 0, q, kv, kv, 301, q, scratch, nb)
+        assert e.value.status == N.NOSA_ERR_CAPACITY
+        N.nosa_prefill(ctx, 0, q, kv, kv, n, q, scratch, nb)
+        with pytest.raises(N.NosaError) as e:      # the layer is no longer empty
+            N.nosa_prefill(ctx, 0, q, kv, kv, n, q, scratch, nb)
+        assert e.value.status == N.NOSA_ERR_STATE
+        N.nosa_prefill(ctx, 1, q, kv, kv, 1, q, scratch, nb)   # a one-token prompt
+        assert N.nosa_sync(ctx) == N.NOSA_OK
+        assert N.nosa_context_length(ctx, 0) == n and N.nosa_context_length(ctx, 1) == 1
+    finally:
+        N.nosa_destroy(ctx)
