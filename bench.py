@@ -281,7 +281,7 @@ def run_native(args, rank, world, local_rank):
     B, Hq, Hkv, d = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
     U = B * Hkv
     K, W = args.steps, args.warmup
-    n_time_leg = 0 if args.quick else 2 * min(K, 8)
+    n_time_leg = 0 if args.quick else 3 * min(K, 6)
     n_e2e = 0 if args.quick else min(K, 64)
     n_e2e_warm = 6 if n_e2e else 0  # two untimed replays of each e2e graph (the first uploads it)
     total_steps = 1 + W + K + n_time_leg + n_e2e_warm + n_e2e
@@ -427,20 +427,23 @@ def run_native(args, rank, world, local_rank):
         return result
 
     # ---------------- per-kernel leg: one event pair around each launch, on the launching stream.
-    # Plain mode: even steps time nosa_step per layer (the fused decode kernel, or its three
-    # kernels); odd steps time the separate calls: append, select and attend (which fetches the
-    # new blocks itself), then the standalone gather kernel (nosa_fetch) re-run on the same fetch
-    # list.  Forecast mode: every step times the forecast path's kernels as separate calls on the
-    # step stream: forecast selection, the gather of its new blocks, append, attention.
-    ev = {k: [] for k in ("decode", "append", "select", "attend", "gather", "fselect")}
-    fetched_split, split_steps = 0, 0
+    # Plain mode cycles three kinds of step: (0) nosa_step per layer (the fused decode kernel, or
+    # the chain); (1) the separate calls append, select and attend, the attention copying the new
+    # blocks from host memory itself, as in the timed step ("attend_fetch"); (2) append, select,
+    # the standalone gather (nosa_fetch) on that fresh fetch list, then the attention over blocks
+    # that are all resident ("attend": HBM only).  Forecast mode: every step times the forecast
+    # path's kernels as separate calls on the step stream: forecast selection, the gather of its
+    # new blocks, append, attention.
+    ev = {k: [] for k in ("decode", "append", "select", "attend_fetch", "attend", "gather", "fselect")}
+    fetched = {"fetch": 0, "gather": 0}
+    steps_of = {"fetch": 0, "gather": 0}
     for it in range(n_time_leg):
         t = step_i[0]
         step_i[0] += 1
-        split = fc or it % 2 == 1
-        if split:
+        kind = "gather" if fc else ("decode", "fetch", "gather")[it % 3]
+        if kind != "decode":
             s0 = N.nosa_get_stats(ctx).blocks_fetched
-            split_steps += 1
+            steps_of[kind] += 1
         for l in range(L):
             pairs = []
             # hold the stream while the launches and their events are queued, so that the
@@ -454,15 +457,19 @@ def run_native(args, rank, world, local_rank):
                           ("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16),
                                                               KVall[t, 1, l].view(i16), 1)),
                           ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16)))]
-            elif not split:
+            elif kind == "decode":
                 calls = [("decode", lambda: N.nosa_step(ctx, l, Qall[t, l].view(i16), KVall[t, 0, l].view(i16),
                                                         KVall[t, 1, l].view(i16), out[l].view(i16)))]
             else:
                 calls = [("append", lambda: N.nosa_append_kv(ctx, l, KVall[t, 0, l].view(i16),
                                                              KVall[t, 1, l].view(i16), 1)),
-                         ("select", lambda: N.nosa_select(ctx, l, Qall[t, l].view(i16))),
-                         ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16))),
-                         ("gather", lambda: N.nosa_fetch(ctx, l))]
+                         ("select", lambda: N.nosa_select(ctx, l, Qall[t, l].view(i16)))]
+                if kind == "gather":
+                    calls += [("gather", lambda: N.nosa_fetch(ctx, l)),
+                              ("attend", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16), out[l].view(i16)))]
+                else:
+                    calls += [("attend_fetch", lambda: N.nosa_attend(ctx, l, Qall[t, l].view(i16),
+                                                                     out[l].view(i16)))]
             for name, fn in calls:
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
@@ -472,8 +479,8 @@ def run_native(args, rank, world, local_rank):
             torch.cuda.synchronize()
             for name, a, b in pairs:
                 ev[name].append(a.elapsed_time(b) * 1e3)
-        if split:
-            fetched_split += N.nosa_get_stats(ctx).blocks_fetched - s0
+        if kind != "decode":
+            fetched[kind] += N.nosa_get_stats(ctx).blocks_fetched - s0
     us = {k: statistics.mean(v) for k, v in ev.items() if v}
     G = Hq // Hkv
     T_now = N.nosa_context_length(ctx, 0)
@@ -488,7 +495,8 @@ def run_native(args, rank, world, local_rank):
                              + 2 * U * G * d * 2)
     attend_bytes = statistics.mean(attend_layers)
     select_bytes = U * (nc * d * 2 + nb * 4 + G * d * 2)
-    fetch_bytes_launch = fetched_split / max(split_steps * L, 1) * BLOCK_BYTES
+    fetch_bytes_launch = fetched["gather"] / max(steps_of["gather"] * L, 1) * BLOCK_BYTES
+    fetch_bytes_attend = fetched["fetch"] / max(steps_of["fetch"] * L, 1) * BLOCK_BYTES
     hbm, src = measured_peaks()
     peak_src = f"{src} hbm_gbs (MEASURED_PEAKS.json)" if src == "measured" else "fallback"
     if step_kernels == 1 and not fc:
@@ -497,14 +505,18 @@ def run_native(args, rank, world, local_rank):
                 "pooled scores and q read by the scorer plus K+V of every selected token read by the attention "
                 "and its output; the newly selected blocks among them arrive over the host link inside the kernel")
     else:
-        hbm_kernels = {"attend": attend_bytes, "fselect" if fc else "select": select_bytes}
+        # the attention as the timed step runs it: with its own host copies in plain mode, over
+        # prefetched blocks in forecast mode
+        att = "attend" if fc else "attend_fetch"
+        hbm_kernels = {att: attend_bytes, "fselect" if fc else "select": select_bytes}
         dominant = max(hbm_kernels, key=lambda k: us[k])
         dom_bytes = hbm_kernels[dominant]
         note = ("attend bytes = K+V of every selected token and the output; in plain mode the newly selected "
                 "blocks among them arrive over the host link inside the same kernel, in forecast mode the "
                 "gather copied them before")
     ach = dom_bytes / (us[dominant] * 1e-6) / 1e9
-    kname = "score_select_kernel" if dominant in ("select", "fselect") else f"{dominant}_kernel"
+    kname = ("score_select_kernel" if dominant in ("select", "fselect") else
+             "attend_kernel" if dominant.startswith("attend") else f"{dominant}_kernel")
     traffic, traffic_src = captured_traffic(kname, f"{wl.name}|sigma{wl.sigma}|kq{wl.k_q}|dma{int(args.dma_bias)}")
     step_bytes = float(sum(attend_layers)) + L * select_bytes
     in_step = step_bytes / (ms * 1e-3) / 1e9
@@ -518,8 +530,14 @@ def run_native(args, rank, world, local_rank):
                                       "how": "score + select + attend bytes of every layer / ms_per_step of the "
                                              "timed graph leg"},
                           "note": note}
+    if "attend" in us:  # the same attention over blocks already resident: its HBM rate alone
+        a_hbm = attend_bytes / (us["attend"] * 1e-6) / 1e9
+        result["roofline"]["attend_resident"] = {
+            "achieved": a_hbm, "frac": a_hbm / hbm, "avg_launch_us": us["attend"],
+            "how": "attend_kernel after nosa_fetch copied the step's new blocks: every block read from HBM"}
     result["stages_us_per_layer"] = us
-    sel_att_us = us["decode"] if (step_kernels == 1 and not fc) else us["attend"] + us.get("select", us.get("fselect", 0))
+    att_us = us["decode"] if (step_kernels == 1 and not fc) else us["attend" if fc else "attend_fetch"]
+    sel_att_us = att_us if (step_kernels == 1 and not fc) else att_us + us.get("select", us.get("fselect", 0))
     result["hbm_frac_score_select_attend"] = (attend_bytes + select_bytes) / (sel_att_us * 1e-6) / 1e9 / hbm
 
     # ---------------- e2e through the public API, copies inside the timed region.  Plain mode:
@@ -645,10 +663,11 @@ def run_native(args, rank, world, local_rank):
     if fc:
         fr["note"] = "the forecast path's gather (nosa_fetch after nosa_forecast_select), the kernel the timed step runs"
     else:
-        attend_link = fetch_bytes_launch / (us["attend"] * 1e-6) / 1e9
-        fr["note"] = ("standalone nosa_fetch on the step's fetch list; in the timed step the attention kernel "
-                      "copies the new blocks itself")
+        attend_link = fetch_bytes_attend / (us["attend_fetch"] * 1e-6) / 1e9
+        fr["note"] = ("standalone nosa_fetch on a fresh fetch list (blocks not read since they were evicted); in "
+                      "the timed step the attention kernel copies the new blocks itself")
         fr["in_attend"] = {"achieved": attend_link, "frac": attend_link / h2d,
+                           "bytes_per_launch": fetch_bytes_attend, "avg_launch_us": us["attend_fetch"],
                            "how": "new blocks' bytes / the attention launch that copies them (a lower bound on "
                                   "the link's rate during that launch, which also reads the cached blocks)"}
     result["fetch_roofline"] = fr

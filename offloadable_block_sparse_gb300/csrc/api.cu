@@ -476,11 +476,18 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     for (;;) {
       const int ncp = std::max(c->pf_max_tokens < kCmpKernel ? 0 : (c->pf_max_tokens - kCmpKernel) / kCmpStride + 1, 1);
       sp.score_wpc = cdiv(ncp, 16 * kScoreWarps) * 16 * kScoreWarps;
-      if (prefill_select_smem(sp) + 8 * 1024 <= (size_t)optin || c->pf_max_tokens <= kBlock) break;
+      if (prefill_select_smem(sp, 1) + 8 * 1024 <= (size_t)optin || c->pf_max_tokens <= kBlock) break;
       c->pf_max_tokens -= 16 * kScoreWarps * kCmpStride;  // one tile row of windows less
     }
     c->pf_wpc = sp.score_wpc;
-    if (init_prefill(sp) != cudaSuccess) {
+    // positions scored per pass over the compressed keys: as many (4, 2, 1) as shared memory holds
+    c->pf_positions = 1;
+    for (int P : {4, 2})
+      if (prefill_select_smem(sp, P) + 8 * 1024 <= (size_t)optin) {
+        c->pf_positions = P;
+        break;
+      }
+    if (init_prefill(sp, c->pf_positions) != cudaSuccess) {
       (void)cudaGetLastError();
       c->pf_max_tokens = 0;
     }
@@ -814,7 +821,8 @@ nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16
   CK(launch_append_bulk(s, k, v, 0, n_tokens, c->stream));
   s.score_chunks = 1;
   s.score_wpc = c->pf_wpc;
-  CK(launch_prefill(s, &tk, &tv, q, k, v, out, static_cast<int16_t*>(scratch), n_tokens, c->stream));
+  CK(launch_prefill(s, c->pf_positions, &tk, &tv, q, k, v, out, static_cast<int16_t*>(scratch), n_tokens,
+                    c->stream));
   c->T_host[layer] = n_tokens;
   c->sel_T[layer] = n_tokens;
   c->fetch_T[layer] = n_tokens;  // every cache slot holds its block

@@ -5,7 +5,7 @@
 // handles all copy work, CTA count traded against compute SMs).
 //
 // One work item is one block: its K and V chunks (2 x 16 KiB) are contiguous in
-// both the host store and the slot.  Each thread moves 8 x 16 bytes per item; the
+// both the host store and the slot.  Each thread moves 4 x 16 bytes per item; the
 // CTA walks items item = blockIdx.x, += gridDim.x and keeps two items in flight: the
 // loads of the next item are issued before the stores of the current one, so every
 // CTA always has a host round trip under way.  Rows past the end of the partial tail
@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s, in
   if (tid == 0) pref[s.U] = carry;
   __syncthreads();
   const int total = carry;
-  constexpr int kVec = kBlockBytes / 16 / kGatherThreads;  // 16-byte vectors per thread per block (8)
+  constexpr int kVec = kBlockBytes / 16 / kGatherThreads;  // 16-byte vectors per thread per block (4)
   struct Job {
     const uint4* src;
     uint4* dst;

@@ -31,7 +31,7 @@ struct nosa_ctx {
   int dec_cs, dec_wpc, dec_nst, dec_teams;
   // sparse prefill: windows per selector CTA for the longest prompt whose selector state fits
   // shared memory, and that prompt length (0: the prefill kernels could not be set up)
-  int pf_wpc, pf_max_tokens;
+  int pf_wpc, pf_max_tokens, pf_positions;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   uint16_t *step_q, *step_k, *step_v, *step_out;  // every layer's inputs and outputs (nosa_step_host_all)
@@ -91,10 +91,11 @@ cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const ui
 // sparse prefill of an empty layer (after the bulk append of the prompt): selections of every
 // position in order into hist [U][n][cap], cache slots refreshed from the prompt, attention of
 // every position.  s.score_chunks = 1 and s.score_wpc covers the prompt's windows.
-size_t prefill_select_smem(const LayerState& s);
-cudaError_t init_prefill(const LayerState& s);
+// P: prompt positions scored per pass over the compressed keys (1, 2 or 4)
+size_t prefill_select_smem(const LayerState& s, int P);
+cudaError_t init_prefill(const LayerState& s, int P);
 int prefill_max_tokens();
-cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
-                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, int n,
-                           cudaStream_t st);
+cudaError_t launch_prefill(const LayerState& s, int P, const CUtensorMap* tk, const CUtensorMap* tv,
+                           const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist,
+                           int n, cudaStream_t st);
 }  // namespace nosa

@@ -40,7 +40,7 @@ constexpr int kMaxBlocksPerCta = 64;       // split-K chunk: selected blocks per
 constexpr int kMaxCacheSlots = 256;        // cache slots per unit (sink + window + k_q + k_e)
 constexpr int kPartStride = 2 + kHeadDim;  // (m, l, o[128]) per head in a split-K partial
 
-constexpr int kGatherThreads = 256;  // with 8 x 16 bytes per thread per item: fits beside two attention CTAs on an SM
+constexpr int kGatherThreads = 512;
 constexpr long long kWaitCycles = 2000000000LL;  // bounded device waits: about a second of SM clocks
 
 // Per-layer derived quantities from the context length T (same formulas on host and device).

@@ -7,8 +7,9 @@
 // attention then runs in one launch.
 //
 //   1. bulk append (append.cu): host store, eviction scores, compressed keys.
-//   2. prefill_select_kernel: one CTA per unit walks the positions.  Each position
-//      runs the scorer and the two-part selector of the decode step (select_core.cuh)
+//   2. prefill_select_kernel: one CTA per unit walks the positions.  Positions are
+//      scored P at a time (one load of every compressed-key tile for P queries); each
+//      position then runs the two-part selector of the decode step (select_core.cuh)
 //      with the geometry of T = t + 1: query-aware scores over the windows complete
 //      at T, pooled eviction scores of the blocks whose windows are complete at T
 //      (only the last two blocks can differ from the whole prompt's), the sticky
@@ -51,53 +52,173 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 }
 
 // ---------------------------------------------------------------- 2. selections, in order
+// Window logits of positions t0 .. t0 + np - 1 (np <= P), one CTA per unit: each 16-window tile
+// of compressed keys is loaded once and multiplied with every position's q on the tensor cores
+// (mma.sync m16n8k16, the group's heads as N = 8), so a tile's load serves P positions.  zp[p]
+// [h][i] = z_{h,i} of position p, -inf for windows not complete at that position's T (nc[p]
+// windows are).  Mst / Sst receive each position's per-head maximum and sum of exp.
+template <int P>
+__device__ __forceinline__ void score_positions(const LayerState& s, int u, const int (&nc)[P], int np,
+                                                float* const (&zp)[P], const uint4 (&qf)[P][4],
+                                                float (*Mst)[kMaxGroup], float (*Sst)[kMaxGroup],
+                                                float (*cmax)[P][kMaxGroup]) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gr = lane >> 2, t4 = lane & 3;
+  const int G = s.G, wpc = s.score_wpc;
+  const int nwarps = blockDim.x >> 5;
+  const int tiles = wpc / (16 * nwarps);
+  const int ncmax = nc[np - 1];  // the last position has the most windows
+  const float scale = s.scale;
+  float mx[P][2];
+#pragma unroll
+  for (int p = 0; p < P; ++p) mx[p][0] = mx[p][1] = -INFINITY;
+  for (int t0 = 0; t0 < tiles; t0 += 2) {  // the loads of two tiles in flight together
+    if ((warp * tiles + t0) * 16 >= ncmax) break;  // this warp's remaining tiles hold no complete window
+    uint4 a[2][2][4];
+#pragma unroll
+    for (int tl = 0; tl < 2; ++tl)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int r = (warp * tiles + t0 + tl) * 16 + gr + 8 * hr;
+        const bool ok = t0 + tl < tiles && r < ncmax;
+        const uint16_t* kr = s.kt + ((size_t)u * s.nc_max + (ok ? r : 0)) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          a[tl][hr][c] = ok ? *reinterpret_cast<const uint4*>(kr + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+    for (int tl = 0; tl < 2; ++tl) {
+      if (t0 + tl >= tiles) break;
+      const int wl0 = (warp * tiles + t0 + tl) * 16 + gr;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        if (p >= np) break;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t* r0 = reinterpret_cast<const uint32_t*>(&a[tl][0][c]);
+          const uint32_t* r1 = reinterpret_cast<const uint32_t*>(&a[tl][1][c]);
+          const uint32_t* qq = reinterpret_cast<const uint32_t*>(&qf[p][c]);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t af[4] = {r0[2 * hh], r1[2 * hh], r0[2 * hh + 1], r1[2 * hh + 1]};
+            mma_16816(acc, af, qq[2 * hh], qq[2 * hh + 1]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int wl = wl0 + 8 * (j >> 1), h = 2 * t4 + (j & 1);
+          const float z = wl < nc[p] ? acc[j] * scale : -INFINITY;
+          zp[p][h * wpc + wl] = z;
+          mx[p][j & 1] = fmaxf(mx[p][j & 1], z);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < P; ++p)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      mx[p][j] = fmaxf(mx[p][j], __shfl_xor_sync(0xffffffffu, mx[p][j], 4));
+      mx[p][j] = fmaxf(mx[p][j], __shfl_xor_sync(0xffffffffu, mx[p][j], 8));
+      mx[p][j] = fmaxf(mx[p][j], __shfl_xor_sync(0xffffffffu, mx[p][j], 16));
+    }
+  if (gr == 0)
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      cmax[warp][p][2 * t4] = mx[p][0];
+      cmax[warp][p][2 * t4 + 1] = mx[p][1];
+    }
+  __syncthreads();
+  if (tid < P * kMaxGroup) {
+    const int p = tid / kMaxGroup, h = tid % kMaxGroup;
+    float mm = -INFINITY;
+    for (int w = 0; w < nwarps; ++w) mm = fmaxf(mm, cmax[w][p][h]);
+    Mst[p][h] = mm;
+  }
+  __syncthreads();
+  for (int ph = warp; ph < np * G; ph += nwarps) {  // sums of exp, one (position, head) per warp
+    const int p = ph / G, h = ph % G;
+    const float M = Mst[p][h];
+    float e = 0.f;
+    if (M > -INFINITY)
+      for (int wl = lane; wl < nc[p]; wl += 32) e += expf(zp[p][h * wpc + wl] - M);
+    e = warp_sum(e);
+    if (lane == 0) Sst[p][h] = e;
+  }
+  __syncthreads();
+}
+
 // grid (1, U) in clusters of one CTA (the selector phases use the cluster API); 256 threads.
-// q: [B][Hq][n][d]; hist: [U][n][cap] block ids, -1 padded.
+// q: [B][Hq][n][d]; hist: [U][n][cap] selection entries, -1 padded.  Positions are scored P at
+// a time (score_positions), then selected one after the other: each position's selection needs
+// the eviction state and slot map the previous one left.  Dynamic shared memory: the selector's
+// region (whose logits array serves position 0) and P - 1 more logits arrays.
+template <int P>
 __global__ void __launch_bounds__(kScoreThreads, 1)
     prefill_select_kernel(LayerState s, const uint16_t* __restrict__ q, int16_t* __restrict__ hist, int n) {
   extern __shared__ __align__(16) unsigned char dsm[];
   __shared__ SelShared sh;
+  __shared__ float cmax[kScoreWarps][P][kMaxGroup];
+  __shared__ float Mst[P][kMaxGroup], Sst[P][kMaxGroup];
   cg::cluster_group cluster = cg::this_cluster();
   const int u = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
   const Smem m = layout(dsm, s);
-  const int G = s.G;
+  const int G = s.G, wpc = s.score_wpc;
+  float* zextra = reinterpret_cast<float*>(dsm + ((region_bytes(s) + 15) & ~size_t(15)));
+  float* zp[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) zp[p] = p == 0 ? m.zs : zextra + (size_t)(p - 1) * kMaxGroup * wpc;
   pdl_wait();  // the bulk append before this kernel wrote the keys, scores and host store
-  for (int t = 0; t < n; ++t) {
-    const int T = t + 1;
-    const Geometry geo = geometry(T, s.nw, s.sink);
-    const int my_slot_blk = leader_prefetch(s, u, geo.nb, geo.nb, m);
-    uint4 qf[4];
-    {  // q of this position: head j of unit u is row (u * G + j) * n + t
+  for (int t0 = 0; t0 < n; t0 += P) {
+    const int np = min(P, n - t0);
+    int nc[P];
+    uint4 qf[P][4];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int t = min(t0 + p, n - 1);
+      nc[p] = geometry(t + 1, s.nw, s.sink).nc;
+      // q of position t: head j of unit u is row (u * G + j) * n + t
       const int gr = lane >> 2, t4 = lane & 3;
       const uint16_t* qh = q + (((size_t)u * G + min(gr, G - 1)) * n + t) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        qf[c] = gr < G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
+        qf[p][c] = gr < G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
     }
-    score_windows<2>(s, u, geo.nc, 0, m, sh, qf);
-    cluster.sync();
-    pool_blocks(s, u, geo, 0, 1, m, sh);
-    rank_local(s, geo, 0, 1, m, sh);
-    cluster.sync();
-    cp_async_wait_all();
-    // The context's pooled eviction scores cover the whole prompt.  At T a block pools only the
-    // windows complete at T; for every block but the last two those are all its windows already.
-    if (tid < 2) {
-      const int b = geo.nb - 2 + tid;
-      if (b >= 0) {
-        const int lo = max(4 * b - 1, 0), hi = min(4 * b + 3, geo.nc - 1);
-        float mx = -INFINITY;
-        for (int i = lo; i <= hi; ++i) mx = fmaxf(mx, s.se_win[(size_t)u * s.nc_max + i]);
-        m.sek[b] = mx;
+    score_positions<P>(s, u, nc, np, zp, qf, Mst, Sst, cmax);
+    for (int p = 0; p < np; ++p) {
+      const int t = t0 + p, T = t + 1;
+      const Geometry geo = geometry(T, s.nw, s.sink);
+      const int my_slot_blk = leader_prefetch(s, u, geo.nb, geo.nb, m);
+      if (tid < G) {
+        sh.Mloc[tid] = Mst[p][tid];
+        sh.Sloc[tid] = Sst[p][tid];
       }
+      Smem mp = m;
+      mp.zs = zp[p];
+      pool_blocks(s, u, geo, 0, 1, mp, sh);  // opens with a barrier after the statistics above
+      rank_local(s, geo, 0, 1, mp, sh);
+      cluster.sync();
+      cp_async_wait_all();
+      // The context's pooled eviction scores cover the whole prompt.  At T a block pools only the
+      // windows complete at T; for every block but the last two those are all its windows already.
+      if (tid < 2) {
+        const int b = geo.nb - 2 + tid;
+        if (b >= 0) {
+          const int lo = max(4 * b - 1, 0), hi = min(4 * b + 3, geo.nc - 1);
+          float mx = -INFINITY;
+          for (int i = lo; i <= hi; ++i) mx = fmaxf(mx, s.se_win[(size_t)u * s.nc_max + i]);
+          m.sek[b] = mx;
+        }
+      }
+      __syncthreads();
+      int16_t* row = hist + ((size_t)u * n + t) * s.cap;
+      const int nS = leader_select(s, u, geo, 1, mp, sh, my_slot_blk, true, [&](int pos, int b, int, bool, int, int kd) {
+        row[pos] = (int16_t)(b | (kd << kPfKindShift));
+      });
+      for (int i = max(nS, 0) + tid; i < s.cap; i += blockDim.x) row[i] = -1;
+      __syncthreads();  // this position's state (slots, eviction words) is read by the next one
     }
-    __syncthreads();
-    int16_t* row = hist + ((size_t)u * n + t) * s.cap;
-    const int nS = leader_select(s, u, geo, 1, m, sh, my_slot_blk, true, [&](int pos, int b, int, bool, int, int kd) {
-      row[pos] = (int16_t)(b | (kd << kPfKindShift));
-    });
-    for (int i = max(nS, 0) + tid; i < s.cap; i += blockDim.x) row[i] = -1;
-    __syncthreads();  // this position's state (slots, eviction words) is read by the next one
   }
 }
 
@@ -324,26 +445,33 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-size_t prefill_select_smem(const LayerState& s) { return region_bytes(s); }
+size_t prefill_select_smem(const LayerState& s, int P) {
+  return ((region_bytes(s) + 15) & ~size_t(15)) + (size_t)(P - 1) * kMaxGroup * s.score_wpc * sizeof(float);
+}
 
 static size_t prefill_attend_smem() { return 1024 + (size_t)kPfStages * kStageBytes; }
 
-cudaError_t init_prefill(const LayerState& s) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)prefill_select_smem(s));
+cudaError_t init_prefill(const LayerState& s, int P) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_attend_kernel<kPfPositions>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prefill_attend_smem());
+  const int sm = (int)prefill_select_smem(s, P);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(prefill_attend_kernel<kPfPositions>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)prefill_attend_smem());
+    e = P == 4   ? cudaFuncSetAttribute(prefill_select_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm)
+        : P == 2 ? cudaFuncSetAttribute(prefill_select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm)
+                 : cudaFuncSetAttribute(prefill_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
   return e;
 }
 
 int prefill_max_tokens() { return kPfMaxWords * 32 * kBlock; }
 
-cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
-                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, int n,
-                           cudaStream_t st) {
-  cudaError_t e = launch_ex(prefill_select_kernel, dim3(1, s.U), dim3(kScoreThreads), prefill_select_smem(s), st,
-                            true, 1, s, q, hist, n);
+cudaError_t launch_prefill(const LayerState& s, int P, const CUtensorMap* tk, const CUtensorMap* tv,
+                           const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist,
+                           int n, cudaStream_t st) {
+  const dim3 grid(1, s.U), block(kScoreThreads);
+  const size_t sm = prefill_select_smem(s, P);
+  cudaError_t e = P == 4   ? launch_ex(prefill_select_kernel<4>, grid, block, sm, st, true, 1, s, q, hist, n)
+                  : P == 2 ? launch_ex(prefill_select_kernel<2>, grid, block, sm, st, true, 1, s, q, hist, n)
+                           : launch_ex(prefill_select_kernel<1>, grid, block, sm, st, true, 1, s, q, hist, n);
   if (e != cudaSuccess) return e;
   e = launch_ex(prefill_refresh_kernel, dim3(s.cap, s.U), dim3(256), 0, st, true, 0, s, k, v, n);
   if (e != cudaSuccess) return e;
