@@ -40,7 +40,7 @@ namespace cg = cooperative_groups;
 
 constexpr uint8_t F_CAND = 1, F_ELIG = 2, F_Q = 4, F_E = 8, F_S = 16, F_NEW = 32;
 constexpr int kMaxScoreCluster = 8;
-constexpr int kCtaTopkMin = 128;  // owned candidates above which the local ranking takes cta_topk
+constexpr int kSortRankMin = 64;  // owned candidates above which the local ranking sorts (k_q <= 32)
 
 struct SelShared {
   int cand_n[kMaxScoreCluster];  // leader: local winners per cluster CTA
@@ -54,9 +54,6 @@ struct SelShared {
   int cofs[kMaxScoreCluster + 1];
   float zx[kMaxGroup];  // logits of the window just before this CTA's range (pooled here too)
   float sqx;            // its query-aware score
-  uint32_t rmin[kScoreWarps], rmax[kScoreWarps];  // cta_topk: per-warp key range
-  int rcnt[kScoreWarps];
-  int dsel[2];          // cta_topk: the digit of this pass and the keys above it
 };
 
 // Composite ranking key: higher score first, then lower block.  Distinct blocks give
@@ -165,117 +162,36 @@ static __device__ void warp_topk(const uint32_t* keys, uint8_t* flags, int n, in
 }
 
 
-// Top-k over the blocks whose flag has `valid` set, run by every thread of the CTA: sets
-// `mark` on the k largest keys, ties to the lower block index.  The same radix select as
-// warp_topk (8-bit digits of the offsets from the smallest valid key, from the top of their
-// range), with the histogram built by all threads over contiguous per-thread ranges of blocks
-// and scanned by warp 0; the keys equal to the k-th largest are then taken in ascending block
-// order by one block-wide scan.  About 3 barriers per digit, so it pays over the branch-free
-// rank count (one pass over every key per key) from a few hundred blocks on.
-static __device__ __noinline__ void cta_topk(const uint32_t* keys, uint8_t* flags, int n, int k, uint8_t valid, uint8_t mark,
-                                      SelShared& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  if (k <= 0) return;
-  const int per = (n + blockDim.x - 1) / blockDim.x;
-  const int lo = min(tid * per, n), hi = min(lo + per, n);
-  int cnt = 0;
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int b = lo; b < hi; ++b)
-    if (flags[b] & valid) {
-      ++cnt;
-      kmin = min(kmin, keys[b]);
-      kmax = max(kmax, keys[b]);
-    }
+// Bitonic sort of one 64-bit key per lane, descending across the warp (15 compare-exchange
+// stages through warp shuffles).
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long x) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-  }
-  if (lane == 0) {
-    sh.rcnt[warp] = cnt;
-    sh.rmin[warp] = kmin;
-    sh.rmax[warp] = kmax;
-  }
-  __syncthreads();
-  cnt = 0;
-  kmin = 0xFFFFFFFFu;
-  kmax = 0u;
-  for (int w = 0; w < nwarps; ++w) {
-    cnt += sh.rcnt[w];
-    kmin = min(kmin, sh.rmin[w]);
-    kmax = max(kmax, sh.rmax[w]);
-  }
-  if (cnt <= k) {
-    for (int b = lo; b < hi; ++b)
-      if (flags[b] & valid) flags[b] |= mark;
-    __syncthreads();
-    return;
-  }
-  const int bits = 32 - __clz(kmax - kmin);  // offsets lie in [0, 2^bits)
-  uint32_t prefix = 0, pmask = 0;            // over offsets
-  int need = k;
-  for (int top = bits; top > 0; top -= 8) {
-    const int shift = max(top - 8, 0);
-    const uint32_t dmask = (1u << (top - shift)) - 1u;
-    for (int i = tid; i < 256; i += blockDim.x) sh.hist[i] = 0;
-    __syncthreads();
-    for (int b = lo; b < hi; ++b) {
-      const uint32_t off = keys[b] - kmin;
-      if ((flags[b] & valid) && (off & pmask) == prefix) atomicAdd(&sh.hist[(off >> shift) & dmask], 1);
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int c[8], tot = 0;
+  for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {  // lane owns 8 bins counted down from the top digit
-        c[j] = sh.hist[255 - (8 * lane + j)];
-        tot += c[j];
-      }
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int run = incl - tot, fd = -1, fa = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (fd < 0 && run < need && run + c[j] >= need) {
-          fd = 255 - (8 * lane + j);
-          fa = run;
-        }
-        run += c[j];
-      }
-      const unsigned int msk = __ballot_sync(0xffffffffu, fd >= 0);
-      const int src = __ffs(msk) - 1;
-      if (lane == src) {
-        sh.dsel[0] = fd;
-        sh.dsel[1] = fa;
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)sh.dsel[0] << shift;
-    pmask |= dmask << shift;
-    need -= sh.dsel[1];
-  }
-  // kmin + prefix is the k-th largest key; `need` keys equal to it are taken, lowest blocks first
-  const uint32_t thr = kmin + prefix;
-  int nt = 0;
-  for (int b = lo; b < hi; ++b) nt += ((flags[b] & valid) && keys[b] == thr) ? 1 : 0;
-  int tot_t;
-  int before = block_scan_excl(nt, sh.scan, &tot_t);
-  for (int b = lo; b < hi; ++b) {
-    if (!(flags[b] & valid)) continue;
-    const uint32_t key = keys[b];
-    if (key > thr) {
-      flags[b] |= mark;
-    } else if (key == thr) {
-      if (before < need) flags[b] |= mark;
-      ++before;
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+      // runs of length k alternate direction; the last run (k = 32) is descending
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
     }
   }
-  __syncthreads();
+  return x;
+}
+
+// The 32 largest keys of two descending warp lists, descending: the elementwise maximum of one
+// list and the other reversed is a bitonic sequence holding them, which five half-cleaner stages
+// sort.
+__device__ __forceinline__ unsigned long long warp_merge_top(unsigned long long a, unsigned long long b) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long br = __shfl_sync(0xffffffffu, b, 31 - lane);
+  unsigned long long x = a > br ? a : br;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) == 0 ? (x > y ? x : y) : (x < y ? x : y);
+  }
+  return x;
 }
 
 
@@ -564,26 +480,28 @@ __device__ __forceinline__ void rank_local(const LayerState& s, const Geometry& 
     const int cb0 = max(ob0, s.sink), cb1 = min(ob1, ws);
     const int nown = max(cb1 - cb0, 0);
     const int ndst = to_all ? CS : 1;
-    if (nown > kCtaTopkMin && kq > 0) {
-      // many owned candidates: radix select marks the k_q best (flags as scratch), then one scan
-      // gives each winner its place in the list
-      uint8_t* fl = m.flags;
-      const int per = (nown + blockDim.x - 1) / blockDim.x;
-      const int lo = min(tid * per, nown), hi = min(lo + per, nown);
-      for (int i = lo; i < hi; ++i) fl[i] = F_CAND;
+    if (nown > kSortRankMin && kq > 0 && kq <= 32) {
+      // many owned candidates: every warp sorts chunks of 32 composite keys and keeps the best 32
+      // (bitonic sort and merge in registers), then warp 0 merges the warps' lists; its first
+      // k_q lanes hold the winners in order
+      const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+      unsigned long long best = 0ull;  // below every real key (whose block field, all ones minus b, is never 0)
+      for (int base = warp * 32; base < nown; base += nwarps * 32) {
+        const int i = base + lane;
+        const unsigned long long x = i < nown ? rank_key(keys[cb0 + i], cb0 + i) : 0ull;
+        best = warp_merge_top(best, warp_sort_desc(x));
+      }
+      unsigned long long* wbest = reinterpret_cast<unsigned long long*>(zs);  // z is no longer needed
+      wbest[warp * 32 + lane] = best;
       __syncthreads();
-      cta_topk(keys + cb0, fl, nown, kq, F_CAND, F_Q, sh);
-      int nw = 0;
-      for (int i = lo; i < hi; ++i) nw += (fl[i] & F_Q) ? 1 : 0;
-      int tot;
-      int r = block_scan_excl(nw, sh.scan, &tot);
-      for (int i = lo; i < hi; ++i) {
-        if (!(fl[i] & F_Q)) continue;
-        for (int d = 0; d < ndst; ++d) {
-          cluster.map_shared_rank(cand_key, d)[rank * kq + r] = keys[cb0 + i];
-          cluster.map_shared_rank(cand_blk, d)[rank * kq + r] = cb0 + i;
-        }
-        ++r;
+      if (warp == 0) {
+        unsigned long long a = wbest[lane];
+        for (int w = 1; w < nwarps; ++w) a = warp_merge_top(a, wbest[w * 32 + lane]);
+        if (lane < min(kq, nown))
+          for (int d = 0; d < ndst; ++d) {
+            cluster.map_shared_rank(cand_key, d)[rank * kq + lane] = (uint32_t)(a >> 32);
+            cluster.map_shared_rank(cand_blk, d)[rank * kq + lane] = (int32_t)(0xFFFFFFFFu - (uint32_t)a);
+          }
       }
     } else {
       unsigned long long* lk = reinterpret_cast<unsigned long long*>(zs);  // z is no longer needed
