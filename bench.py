@@ -153,6 +153,7 @@ KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "append_core.cuh", "select_core.cuh", "attend_core.cuh", "ptx.cuh",
                       "nosa_internal.cuh"],
     "attend_kernel": ["attend.cu", "attend_core.cuh", "ptx.cuh", "nosa_internal.cuh"],
+    "score_select_kernel": ["select.cu", "select_core.cuh", "append_core.cuh", "ptx.cuh", "nosa_internal.cuh"],
 }
 
 
