@@ -137,6 +137,10 @@ typedef struct {
   int32_t forecast_streams;      /* forecast pipeline: 2 = selections and gathers on two streams
                                     (a layer's selection overlaps the previous layer's gather),
                                     1 = both in order on one stream */
+  int32_t prefill_ctas;          /* sparse prefill: CTAs per unit walking the prompt positions, 1..8
+                                    (1: one CTA scoring up to four positions per pass; more: one
+                                    cluster sharing each position's scoring); rule: about one SM
+                                    per CTA over a layer's units, at most 8, else 1 */
 } nosa_config;
 
 /* Values of nosa_config.attend_merge. */

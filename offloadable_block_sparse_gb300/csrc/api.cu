@@ -207,6 +207,7 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->decode_teams < 0 || c->decode_teams > 2) return NOSA_ERR_INVALID_ARG;
   if (c->decode_stages != 0 && (c->decode_stages < 2 || c->decode_stages > 6)) return NOSA_ERR_INVALID_ARG;
   if (c->forecast_streams < 0 || c->forecast_streams > 2) return NOSA_ERR_INVALID_ARG;
+  if (c->prefill_ctas < 0 || c->prefill_ctas > 8) return NOSA_ERR_INVALID_ARG;
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
   const long long cap = (long long)c->sink_blocks + c->window_tokens / kBlock + c->k_q + c->k_e;
@@ -490,6 +491,29 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     if (init_prefill(sp, c->pf_positions) != cudaSuccess) {
       (void)cudaGetLastError();
       c->pf_max_tokens = 0;
+    }
+    // few units per layer: a cluster of CTAs per unit shares each position's scoring, pooling and
+    // ranking, about one SM per CTA in total (8 CTAs per unit at 16 units)
+    c->pf_cs = 0;
+    const int want_cs = cfg->prefill_ctas > 0 ? cfg->prefill_ctas
+                                              : std::min(8, std::max(c->num_sms, 1) / std::max(c->U, 1));
+    if (c->pf_max_tokens > 0 && want_cs >= 2) {
+      LayerState sc = s0;
+      const int ncp = std::max(c->pf_max_tokens < kCmpKernel ? 0 : (c->pf_max_tokens - kCmpKernel) / kCmpStride + 1, 1);
+      for (int cs = want_cs; cs >= 2; --cs) {
+        sc.score_chunks = cs;
+        sc.score_wpc = cdiv(cdiv(ncp, cs), 16 * kScoreWarps) * 16 * kScoreWarps;
+        if (score_select_smem(sc) + 8 * 1024 > (size_t)optin) continue;
+        if (init_prefill_cluster(sc) != cudaSuccess) {
+          (void)cudaGetLastError();
+          break;
+        }
+        if (prefill_cluster_active(sc, cs) >= 1) {
+          c->pf_cs = cs;
+          c->pf_cs_wpc = sc.score_wpc;
+          break;
+        }
+      }
     }
   }
   // forecast pipeline: a selection and a prefetch stream and their events.  Both streams take the
@@ -819,8 +843,8 @@ nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16
       return NOSA_ERR_INVALID_ARG;
   LayerState s = layer_state(c, layer);
   CK(launch_append_bulk(s, k, v, 0, n_tokens, c->stream));
-  s.score_chunks = 1;
-  s.score_wpc = c->pf_wpc;
+  s.score_chunks = c->pf_cs > 1 ? c->pf_cs : 1;
+  s.score_wpc = c->pf_cs > 1 ? c->pf_cs_wpc : c->pf_wpc;
   CK(launch_prefill(s, c->pf_positions, &tk, &tv, q, k, v, out, static_cast<int16_t*>(scratch), n_tokens,
                     c->stream));
   c->T_host[layer] = n_tokens;

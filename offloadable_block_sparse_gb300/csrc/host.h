@@ -32,6 +32,7 @@ struct nosa_ctx {
   // sparse prefill: windows per selector CTA for the longest prompt whose selector state fits
   // shared memory, and that prompt length (0: the prefill kernels could not be set up)
   int pf_wpc, pf_max_tokens, pf_positions;
+  int pf_cs, pf_cs_wpc;  // selection walk with a cluster of pf_cs CTAs per unit (0: one CTA per unit)
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   uint16_t *step_q, *step_k, *step_v, *step_out;  // every layer's inputs and outputs (nosa_step_host_all)
@@ -94,6 +95,9 @@ cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const ui
 // P: prompt positions scored per pass over the compressed keys (1, 2 or 4)
 size_t prefill_select_smem(const LayerState& s, int P);
 cudaError_t init_prefill(const LayerState& s, int P);
+// the walk with one cluster of s.score_chunks CTAs per unit (s.score_wpc windows each)
+cudaError_t init_prefill_cluster(const LayerState& s);
+int prefill_cluster_active(const LayerState& s, int cs);
 int prefill_max_tokens();
 cudaError_t launch_prefill(const LayerState& s, int P, const CUtensorMap* tk, const CUtensorMap* tv,
                            const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist,

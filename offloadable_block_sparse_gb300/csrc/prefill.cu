@@ -222,6 +222,62 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   }
 }
 
+// The same walk with one thread-block cluster of CS CTAs per unit, for layers with few units:
+// CTA r scores windows [r * wpc, (r + 1) * wpc) of every position and pools and ranks the blocks
+// it owns (the decode selector's phases, statistics and local winners through distributed
+// shared memory between two cluster barriers); rank 0 then makes the selection on the state the
+// previous position left while the other CTAs go on to score the next position.  Every
+// cross-CTA read of a position happens between that position's two barriers, and no CTA writes
+// the next position's statistics or winners before all have passed its first barrier.
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    prefill_select_cluster_kernel(LayerState s, const uint16_t* __restrict__ q, int16_t* __restrict__ hist, int n) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  __shared__ SelShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank(), CS = (int)cluster.num_blocks();
+  const int u = blockIdx.y, tid = threadIdx.x;
+  const Smem m = layout(dsm, s);
+  pdl_wait();  // the bulk append before this kernel wrote the keys, scores and host store
+  for (int t = 0; t < n; ++t) {
+    const int T = t + 1;
+    const Geometry geo = geometry(T, s.nw, s.sink);
+    int my_slot_blk = -1;
+    if (rank == 0) my_slot_blk = leader_prefetch(s, u, geo.nb, geo.nb, m);
+    uint4 qf[4];
+    {  // q of position t: head j of unit u is row (u * G + j) * n + t
+      const int lane = tid & 31, gr = lane >> 2, t4 = lane & 3;
+      const uint16_t* qh = q + (((size_t)u * s.G + min(gr, s.G - 1)) * n + t) * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        qf[c] = gr < s.G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
+    }
+    score_windows<2>(s, u, geo.nc, rank, m, sh, qf);
+    cluster.sync();  // every CTA's statistics of this position are visible
+    pool_blocks(s, u, geo, rank, CS, m, sh);
+    rank_local(s, geo, rank, CS, m, sh);
+    cluster.sync();  // the local winners have landed in rank 0; the statistics reads are done
+    if (rank != 0) continue;
+    cp_async_wait_all();
+    // pooled eviction scores of the last two blocks as of T (windows complete at T only)
+    if (tid < 2) {
+      const int b = geo.nb - 2 + tid;
+      if (b >= 0) {
+        const int lo = max(4 * b - 1, 0), hi = min(4 * b + 3, geo.nc - 1);
+        float mx = -INFINITY;
+        for (int i = lo; i <= hi; ++i) mx = fmaxf(mx, s.se_win[(size_t)u * s.nc_max + i]);
+        m.sek[b] = mx;
+      }
+    }
+    __syncthreads();
+    int16_t* row = hist + ((size_t)u * n + t) * s.cap;
+    const int nS = leader_select(s, u, geo, CS, m, sh, my_slot_blk, true, [&](int pos, int b, int, bool, int, int kd) {
+      row[pos] = (int16_t)(b | (kd << kPfKindShift));
+    });
+    for (int i = max(nS, 0) + tid; i < s.cap; i += blockDim.x) row[i] = -1;
+    __syncthreads();  // this position's state (slots, eviction words) is read by the next one
+  }
+}
+
 // ---------------------------------------------------------------- 3. cache refresh
 // grid (cap, U), 256 threads: slot `slot` of unit u receives its block from the prompt's K/V
 // (rows past the prompt zero), as the fetches of the decode steps would have left it.
@@ -451,6 +507,34 @@ size_t prefill_select_smem(const LayerState& s, int P) {
 
 static size_t prefill_attend_smem() { return 1024 + (size_t)kPfStages * kStageBytes; }
 
+cudaError_t init_prefill_cluster(const LayerState& s) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)region_bytes(s));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_select_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+int prefill_cluster_active(const LayerState& s, int cs) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.gridDim = dim3(cs, 1);
+  cfg.dynamicSmemBytes = region_bytes(s);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nc = 0;
+  if (cudaOccupancyMaxActiveClusters(&nc, prefill_select_cluster_kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return nc;
+}
+
 cudaError_t init_prefill(const LayerState& s, int P) {
   cudaError_t e = cudaFuncSetAttribute(prefill_attend_kernel<kPfPositions>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prefill_attend_smem());
@@ -467,11 +551,18 @@ int prefill_max_tokens() { return kPfMaxWords * 32 * kBlock; }
 cudaError_t launch_prefill(const LayerState& s, int P, const CUtensorMap* tk, const CUtensorMap* tv,
                            const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist,
                            int n, cudaStream_t st) {
-  const dim3 grid(1, s.U), block(kScoreThreads);
-  const size_t sm = prefill_select_smem(s, P);
-  cudaError_t e = P == 4   ? launch_ex(prefill_select_kernel<4>, grid, block, sm, st, true, 1, s, q, hist, n)
-                  : P == 2 ? launch_ex(prefill_select_kernel<2>, grid, block, sm, st, true, 1, s, q, hist, n)
-                           : launch_ex(prefill_select_kernel<1>, grid, block, sm, st, true, 1, s, q, hist, n);
+  const dim3 block(kScoreThreads);
+  cudaError_t e;
+  if (s.score_chunks > 1) {  // a cluster per unit
+    e = launch_ex(prefill_select_cluster_kernel, dim3(s.score_chunks, s.U), block, region_bytes(s), st, true,
+                  s.score_chunks, s, q, hist, n);
+  } else {
+    const dim3 grid(1, s.U);
+    const size_t sm = prefill_select_smem(s, P);
+    e = P == 4   ? launch_ex(prefill_select_kernel<4>, grid, block, sm, st, true, 1, s, q, hist, n)
+        : P == 2 ? launch_ex(prefill_select_kernel<2>, grid, block, sm, st, true, 1, s, q, hist, n)
+                 : launch_ex(prefill_select_kernel<1>, grid, block, sm, st, true, 1, s, q, hist, n);
+  }
   if (e != cudaSuccess) return e;
   e = launch_ex(prefill_refresh_kernel, dim3(s.cap, s.U), dim3(256), 0, st, true, 0, s, k, v, n);
   if (e != cudaSuccess) return e;

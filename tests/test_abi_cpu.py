@@ -49,7 +49,7 @@ def test_validate_config():
            dict(k_q=200, k_e=100), dict(batch=4097, num_kv_heads=1, num_q_heads=8), dict(softmax_scale=-1.0),
            dict(score_ctas=9), dict(score_ctas=-1), dict(attend_blocks_per_cta=65), dict(attend_merge=4),
            dict(decode_cluster=9), dict(decode_teams=3), dict(decode_stages=1), dict(decode_stages=7),
-           dict(forecast_streams=3)]
+           dict(forecast_streams=3), dict(prefill_ctas=9)]
     for b in bad:
         assert N.nosa_validate_config(_cfg(**b)) == N.NOSA_ERR_INVALID_ARG, b
     c = _cfg()
@@ -60,7 +60,8 @@ def test_validate_config():
 def test_sizing_overrides_are_accepted():
     good = [dict(score_ctas=1), dict(score_ctas=8), dict(attend_blocks_per_cta=1), dict(attend_blocks_per_cta=64),
             dict(attend_merge=N.NOSA_MERGE_TICKET), dict(attend_merge=N.NOSA_MERGE_CLUSTER),
-            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1)]
+            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1),
+            dict(prefill_ctas=1), dict(prefill_ctas=8)]
     for g in good:
         assert N.nosa_validate_config(_cfg(**g)) == N.NOSA_OK, g
 

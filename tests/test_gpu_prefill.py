@@ -59,14 +59,14 @@ def _select_and_adopt(o, sq, se, T, Q_gpu, E_gpu, k_q, k_e, ties, where):
     return Q, E
 
 
-def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3):
+def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, prefill_ctas=0):
     """Prefill n tokens into an empty layer, check against the oracle, then decode_steps steps."""
     B, Hq, Hkv, d, G = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.group
     U = B * Hkv
     assert n + decode_steps <= wl.steps and wl.context == 0
     cfg = N.make_config(num_layers=1, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=n + decode_steps, sink_blocks=wl.sink_blocks,
-                        evict_hidden=wl.evict_hidden, flags=flags)
+                        evict_hidden=wl.evict_hidden, flags=flags, prefill_ctas=prefill_ctas)
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     ties, max_err = [], 0.0
@@ -169,32 +169,37 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3):
     return ties
 
 
+# prefill_ctas 0 takes the rule (few units here: a cluster of 8 CTAs per unit walks the positions),
+# 1 the one-CTA walk that scores four positions per pass
+@pytest.mark.parametrize("ctas", [0, 1, 3], ids=["cluster-rule", "one-cta", "cluster-3"])
 @pytest.mark.parametrize("mode", [FUSED, UNFUSED], ids=["fused-decode", "three-kernel-decode"])
-def test_prefill_640_every_position(mode):
+def test_prefill_640_every_position(mode, ctas):
     # k = 3 with a 2-block window: the selection turns sparse once the prompt passes 6 blocks, so
     # evictions and the window sliding over the budget all happen inside the prompt
     wl = syn.Workload("pf640", layers=1, batch=2, q_heads=16, kv_heads=2, context=0, k_q=1, k_e=2,
                       window_tokens=128, steps=644, sigma=0.3)
     units = [(b, g) for b in range(2) for g in range(2)]
-    run_prefill(wl, 640, units, set(range(640)), flags=mode, decode_steps=4)
+    run_prefill(wl, 640, units, set(range(640)), flags=mode, decode_steps=4, prefill_ctas=ctas)
 
 
-def test_prefill_ragged_group4_dma_bias():
+@pytest.mark.parametrize("ctas", [0, 1], ids=["cluster-rule", "one-cta"])
+def test_prefill_ragged_group4_dma_bias(ctas):
     # a prompt that ends mid-block and mid-window, 8 q heads over 2 kv heads, with the attention bias
     wl = syn.Workload("pf_ragged", layers=1, batch=3, q_heads=8, kv_heads=2, context=0, k_q=3, k_e=5,
                       window_tokens=128, steps=1004, sigma=1.0)
     units = [(b, g) for b in range(3) for g in range(2)]
-    run_prefill(wl, 1001, units, set(range(1001)), flags=N.NOSA_F_DMA_BIAS, decode_steps=3)
+    run_prefill(wl, 1001, units, set(range(1001)), flags=N.NOSA_F_DMA_BIAS, decode_steps=3, prefill_ctas=ctas)
 
 
-def test_prefill_16k_prompt_sampled_positions():
+@pytest.mark.parametrize("ctas", [0, 1], ids=["cluster-rule", "one-cta"])
+def test_prefill_16k_prompt_sampled_positions(ctas):
     # the 1B-shaped layer (16/2 heads, k_q 16, k_e 48, 1024-token window) over a 16K prompt: one
     # unit's selection checked at every position, its outputs at sampled positions
     n = 16384
     wl = syn.Workload("pf16k", layers=1, batch=1, q_heads=16, kv_heads=2, context=0, k_q=16, k_e=48,
                       window_tokens=1024, steps=n + 2, sigma=0.3)
     pos = set(range(0, n, 61)) | set(range(n - 8, n)) | {63, 64, 65, 1023, 1024, 1025}
-    run_prefill(wl, n, [(0, 1)], pos, decode_steps=2)
+    run_prefill(wl, n, [(0, 1)], pos, decode_steps=2, prefill_ctas=ctas)
 
 
 def test_prefill_argument_checks():
