@@ -139,8 +139,9 @@ typedef struct {
                                     1 = both in order on one stream */
   int32_t prefill_ctas;          /* sparse prefill: CTAs per unit walking the prompt positions, 1..8
                                     (1: one CTA scoring up to four positions per pass; more: one
-                                    cluster sharing each position's scoring); rule: about one SM
-                                    per CTA over a layer's units, at most 8, else 1 */
+                                    cluster sharing each position's scoring); rule: 4 when a layer
+                                    has at most a quarter as many units as the device has SMs,
+                                    fewer down to 1 beyond */
 } nosa_config;
 
 /* Values of nosa_config.attend_merge. */

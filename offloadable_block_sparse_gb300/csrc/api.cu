@@ -493,10 +493,11 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
       c->pf_max_tokens = 0;
     }
     // few units per layer: a cluster of CTAs per unit shares each position's scoring, pooling and
-    // ranking, about one SM per CTA in total (8 CTAs per unit at 16 units)
+    // ranking.  Measured at 16 units and a 16K prompt: 4 CTAs per unit 26.7K tok/s, one 22.7K, 8
+    // only 15.4K (the two cluster barriers per position cost more than the split scoring saves)
     c->pf_cs = 0;
     const int want_cs = cfg->prefill_ctas > 0 ? cfg->prefill_ctas
-                                              : std::min(8, std::max(c->num_sms, 1) / std::max(c->U, 1));
+                                              : std::min(4, std::max(c->num_sms, 1) / std::max(c->U, 1));
     if (c->pf_max_tokens > 0 && want_cs >= 2) {
       LayerState sc = s0;
       const int ncp = std::max(c->pf_max_tokens < kCmpKernel ? 0 : (c->pf_max_tokens - kCmpKernel) / kCmpStride + 1, 1);

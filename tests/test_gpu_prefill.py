@@ -169,8 +169,8 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, pref
     return ties
 
 
-# prefill_ctas 0 takes the rule (few units here: a cluster of 8 CTAs per unit walks the positions),
-# 1 the one-CTA walk that scores four positions per pass
+# prefill_ctas 0 takes the rule (few units here: a cluster of 4 CTAs per unit walks the positions),
+# 1 the one-CTA walk that scores four positions per pass, 3 a cluster of 3
 @pytest.mark.parametrize("ctas", [0, 1, 3], ids=["cluster-rule", "one-cta", "cluster-3"])
 @pytest.mark.parametrize("mode", [FUSED, UNFUSED], ids=["fused-decode", "three-kernel-decode"])
 def test_prefill_640_every_position(mode, ctas):
