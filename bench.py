@@ -81,7 +81,7 @@ def parse():
     ap.add_argument("--quick", action="store_true", help="timed graph leg only (profiling runs)")
     # kernel sizing overrides (nosa_config fields; 0 = the library's rule)
     for f in ("score-ctas", "attend-blocks-per-cta", "attend-merge", "decode-cluster", "decode-teams",
-              "decode-stages", "forecast-streams", "prefill-ctas"):
+              "decode-stages", "forecast-streams"):
         ap.add_argument(f"--{f}", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="three-kernel step even where the fused kernel fits")
     ap.add_argument("--prefill", action="store_true",
@@ -232,7 +232,7 @@ def oracle_baseline(wl, seconds, total_units):
 def sizing_overrides(args):
     """nosa_config sizing fields set on the command line (0 = the library's rule)."""
     return {k: getattr(args, k) for k in ("score_ctas", "attend_blocks_per_cta", "attend_merge", "decode_cluster",
-                                          "decode_teams", "decode_stages", "forecast_streams", "prefill_ctas")}
+                                          "decode_teams", "decode_stages", "forecast_streams")}
 
 
 def workload_config(wl, args, layers, world):

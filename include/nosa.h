@@ -99,6 +99,10 @@ typedef enum {
  * select, which otherwise runs only when more than 1024 blocks are eligible (the first
  * selection over a context of more than about 66K tokens).  Same selections either way. */
 #define NOSA_F_TEST_RADIX_TOPK 16u
+/* NOSA_F_TEST_PREFILL_WIDE (test hook): nosa_prefill takes the kernel forms it otherwise takes only
+ * for prompts of more than 65,536 tokens (two positions per warp for the query-aware picks instead
+ * of four, two bitmap words per lane in the walk instead of one).  Same selections either way. */
+#define NOSA_F_TEST_PREFILL_WIDE 32u
 
 typedef struct {
   uint32_t struct_size;   /* sizeof(nosa_config) */
@@ -137,11 +141,6 @@ typedef struct {
   int32_t forecast_streams;      /* forecast pipeline: 2 = selections and gathers on two streams
                                     (a layer's selection overlaps the previous layer's gather),
                                     1 = both in order on one stream */
-  int32_t prefill_ctas;          /* sparse prefill: CTAs per unit walking the prompt positions, 1..8
-                                    (1: one CTA scoring up to four positions per pass; more: one
-                                    cluster sharing each position's scoring); rule: 4 when a layer
-                                    has at most a quarter as many units as the device has SMs,
-                                    fewer down to 1 beyond */
 } nosa_config;
 
 /* Values of nosa_config.attend_merge. */
@@ -346,21 +345,24 @@ size_t nosa_dense_scratch_bytes(int units, int context_len);
  * decoding) and "How NOSA works" (a block the query-agnostic part drops at one step is never
  * re-selected by it, so a position's selection depends on the earlier positions').  The
  * selection for prompt position t is the one the decode step at T = t + 1 makes, with the
- * eviction state carried from position t - 1: the positions are selected in order (one CTA per
- * unit), then the attention of all positions runs in one launch, reading the prompt's K/V from
- * k and v.  Afterwards the layer's state (host store, compressed keys, scores, eviction bitmap,
+ * eviction state carried from position t - 1.  The query-aware picks of all positions are made
+ * at once (they do not depend on that state); one warp per unit then walks the positions in
+ * order for the query-agnostic picks, the eviction update and the slot pairing; the attention
+ * of all positions runs in one launch, reading the prompt's K/V from k and v.  Afterwards the
+ * layer's state (host store, compressed keys, scores, eviction bitmap,
  * cache slots and their contents, last selection, counters) is the state n_tokens calls of
  * nosa_step with the same tokens would leave, and decoding continues with nosa_step.
  *   q, out   device bf16 [B][Hq][n_tokens][d] (out[b][h][t] is position t's attention output)
- *   k, v     device bf16 [B][Hkv][n_tokens][d], 16-byte aligned
- *   scratch  device memory of at least nosa_prefill_scratch_bytes(ctx, n_tokens) bytes, 4-byte
- *            aligned.  Afterwards it holds every position's selection: int16 [B][Hkv][n_tokens]
- *            [cache_slots], ascending, -1 padded; entry bits 0-11 are the block, bits 12-13
- *            its kind (0 sink, 1 window, 2 query-aware, 3 query-agnostic)
- * NOSA_ERR_STATE if the layer is not empty; NOSA_ERR_CAPACITY if n_tokens exceeds max_context or
- * the prompt length one selector CTA holds (nosa_prefill_scratch_bytes returns the scratch size
- * for any length; 131,072 tokens at most, fewer when the selector state of the context's
- * max_context would not fit one CTA's shared memory), or if the scratch is too small. */
+ *   k, v     device bf16 [B][Hkv][n_tokens][d]; q, k and v 16-byte aligned
+ *   scratch  device memory of at least nosa_prefill_scratch_bytes(ctx, n_tokens) bytes, 16-byte
+ *            aligned.  Afterwards it begins with every position's selection: int16 [B][Hkv]
+ *            [n_tokens][R] with R = cache_slots rounded up to a multiple of 8, ascending, -1
+ *            padded; entry bits 0-11 are the block, bits 12-13 its kind (0 sink, 1 window,
+ *            2 query-aware, 3 query-agnostic).  The rest is working space (each position's
+ *            query-aware picks as bitmap words over the prompt's blocks).
+ * NOSA_ERR_INVALID_ARG on a misaligned pointer; NOSA_ERR_STATE if the layer is not empty;
+ * NOSA_ERR_CAPACITY if n_tokens exceeds max_context or 131,072 (the longest prompt the kernels'
+ * block bitmaps cover), or if the scratch is too small. */
 nosa_status nosa_prefill(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                          int n_tokens, uint16_t* out, void* scratch, size_t scratch_bytes);
 

@@ -198,7 +198,7 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->evict_hidden < 32 || c->evict_hidden > 256 || c->evict_hidden % 32) return NOSA_ERR_INVALID_ARG;
   if (c->gather_ctas < 0 || c->gather_ctas > 4096) return NOSA_ERR_INVALID_ARG;
   if (!(c->softmax_scale >= 0.f) || (c->flags & ~(NOSA_F_TEST_ZERO_WAIT | NOSA_F_TEST_BAD_SLOT | NOSA_F_UNFUSED_STEP | NOSA_F_DMA_BIAS |
-                                               NOSA_F_TEST_RADIX_TOPK)))
+                                               NOSA_F_TEST_RADIX_TOPK | NOSA_F_TEST_PREFILL_WIDE)))
     return NOSA_ERR_INVALID_ARG;
   if (c->score_ctas < 0 || c->score_ctas > 8) return NOSA_ERR_INVALID_ARG;
   if (c->attend_blocks_per_cta < 0 || c->attend_blocks_per_cta > kMaxBlocksPerCta) return NOSA_ERR_INVALID_ARG;
@@ -207,7 +207,6 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (c->decode_teams < 0 || c->decode_teams > 2) return NOSA_ERR_INVALID_ARG;
   if (c->decode_stages != 0 && (c->decode_stages < 2 || c->decode_stages > 6)) return NOSA_ERR_INVALID_ARG;
   if (c->forecast_streams < 0 || c->forecast_streams > 2) return NOSA_ERR_INVALID_ARG;
-  if (c->prefill_ctas < 0 || c->prefill_ctas > 8) return NOSA_ERR_INVALID_ARG;
   const long long U = (long long)c->batch * c->num_kv_heads;
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
   const long long cap = (long long)c->sink_blocks + c->window_tokens / kBlock + c->k_q + c->k_e;
@@ -467,54 +466,11 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
       free_ctx(c);
       return NOSA_ERR_CUDA;
     }
-    // sparse prefill: one selector CTA per unit holds the logits of every window of the prompt;
-    // the longest prompt (up to max_context) whose selector state fits the shared memory
-    int optin = 0;
-    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    LayerState sp = s0;
-    sp.score_chunks = 1;
+    // sparse prefill: prompts up to max_context, at most the length the walk's block bitmaps cover
     c->pf_max_tokens = std::min(cfg->max_context, prefill_max_tokens());
-    for (;;) {
-      const int ncp = std::max(c->pf_max_tokens < kCmpKernel ? 0 : (c->pf_max_tokens - kCmpKernel) / kCmpStride + 1, 1);
-      sp.score_wpc = cdiv(ncp, 16 * kScoreWarps) * 16 * kScoreWarps;
-      if (prefill_select_smem(sp, 1) + 8 * 1024 <= (size_t)optin || c->pf_max_tokens <= kBlock) break;
-      c->pf_max_tokens -= 16 * kScoreWarps * kCmpStride;  // one tile row of windows less
-    }
-    c->pf_wpc = sp.score_wpc;
-    // positions scored per pass over the compressed keys: as many (4, 2, 1) as shared memory holds
-    c->pf_positions = 1;
-    for (int P : {4, 2})
-      if (prefill_select_smem(sp, P) + 8 * 1024 <= (size_t)optin) {
-        c->pf_positions = P;
-        break;
-      }
-    if (init_prefill(sp, c->pf_positions) != cudaSuccess) {
+    if (init_prefill() != cudaSuccess) {
       (void)cudaGetLastError();
       c->pf_max_tokens = 0;
-    }
-    // few units per layer: a cluster of CTAs per unit shares each position's scoring, pooling and
-    // ranking.  Measured at 16 units and a 16K prompt: 4 CTAs per unit 26.7K tok/s, one 22.7K, 8
-    // only 15.4K (the two cluster barriers per position cost more than the split scoring saves)
-    c->pf_cs = 0;
-    const int want_cs = cfg->prefill_ctas > 0 ? cfg->prefill_ctas
-                                              : std::min(4, std::max(c->num_sms, 1) / std::max(c->U, 1));
-    if (c->pf_max_tokens > 0 && want_cs >= 2) {
-      LayerState sc = s0;
-      const int ncp = std::max(c->pf_max_tokens < kCmpKernel ? 0 : (c->pf_max_tokens - kCmpKernel) / kCmpStride + 1, 1);
-      for (int cs = want_cs; cs >= 2; --cs) {
-        sc.score_chunks = cs;
-        sc.score_wpc = cdiv(cdiv(ncp, cs), 16 * kScoreWarps) * 16 * kScoreWarps;
-        if (score_select_smem(sc) + 8 * 1024 > (size_t)optin) continue;
-        if (init_prefill_cluster(sc) != cudaSuccess) {
-          (void)cudaGetLastError();
-          break;
-        }
-        if (prefill_cluster_active(sc, cs) >= 1) {
-          c->pf_cs = cs;
-          c->pf_cs_wpc = sc.score_wpc;
-          break;
-        }
-      }
     }
   }
   // forecast pipeline: a selection and a prefetch stream and their events.  Both streams take the
@@ -812,9 +768,16 @@ nosa_status nosa_step_host_all(nosa_ctx* c, const uint16_t* q, const uint16_t* k
   return NOSA_OK;
 }
 
+// [U][n][cap rounded up to 8] int16 selection rows, then [U][n][ceil(nb / 32)] bitmap words of
+// the query-aware picks (nb: the prompt's blocks)
+static size_t prefill_hist_bytes(const nosa_ctx* c, int n_tokens) {
+  return (size_t)c->U * (size_t)n_tokens * (size_t)((c->cap + 7) & ~7) * sizeof(int16_t);
+}
+
 size_t nosa_prefill_scratch_bytes(nosa_ctx* c, int n_tokens) {
   if (!c || n_tokens < 1) return 0;
-  return (size_t)c->U * (size_t)n_tokens * (size_t)c->cap * sizeof(int16_t);
+  const size_t words = (size_t)cdiv(cdiv(n_tokens, kBlock), 32);
+  return prefill_hist_bytes(c, n_tokens) + (size_t)c->U * (size_t)n_tokens * words * sizeof(uint32_t);
 }
 
 nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -823,7 +786,7 @@ nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16
   if (st != NOSA_OK) return st;
   if (!q || !k || !v || !out || !scratch || n_tokens < 1) return NOSA_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) % 16) return NOSA_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(scratch) % 4) return NOSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(scratch) % 16) return NOSA_ERR_INVALID_ARG;
   if (c->T_host[layer] != 0) return NOSA_ERR_STATE;  // a prefill starts an empty layer
   if (n_tokens > c->cfg.max_context || n_tokens > c->pf_max_tokens) return NOSA_ERR_CAPACITY;
   if (scratch_bytes < nosa_prefill_scratch_bytes(c, n_tokens)) return NOSA_ERR_CAPACITY;
@@ -842,11 +805,11 @@ nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return NOSA_ERR_INVALID_ARG;
-  LayerState s = layer_state(c, layer);
+  const LayerState s = layer_state(c, layer);
   CK(launch_append_bulk(s, k, v, 0, n_tokens, c->stream));
-  s.score_chunks = c->pf_cs > 1 ? c->pf_cs : 1;
-  s.score_wpc = c->pf_cs > 1 ? c->pf_cs_wpc : c->pf_wpc;
-  CK(launch_prefill(s, c->pf_positions, &tk, &tv, q, k, v, out, static_cast<int16_t*>(scratch), n_tokens,
+  int16_t* hist = static_cast<int16_t*>(scratch);
+  uint32_t* qsel = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(scratch) + prefill_hist_bytes(c, n_tokens));
+  CK(launch_prefill(s, &tk, &tv, q, k, v, out, hist, qsel, n_tokens, (c->cfg.flags & NOSA_F_TEST_PREFILL_WIDE) != 0,
                     c->stream));
   c->T_host[layer] = n_tokens;
   c->sel_T[layer] = n_tokens;

@@ -29,10 +29,8 @@ struct nosa_ctx {
   // fused decode kernel (nosa_step): cluster size (0: off, three kernels instead), windows per
   // scoring CTA, attention stages per team
   int dec_cs, dec_wpc, dec_nst, dec_teams;
-  // sparse prefill: windows per selector CTA for the longest prompt whose selector state fits
-  // shared memory, and that prompt length (0: the prefill kernels could not be set up)
-  int pf_wpc, pf_max_tokens, pf_positions;
-  int pf_cs, pf_cs_wpc;  // selection walk with a cluster of pf_cs CTAs per unit (0: one CTA per unit)
+  // sparse prefill: the longest prompt (0: the prefill kernels could not be set up)
+  int pf_max_tokens;
   // staging buffers for host-pointer calls
   uint16_t *stage_q, *stage_k, *stage_v, *stage_out;
   uint16_t *step_q, *step_k, *step_v, *step_out;  // every layer's inputs and outputs (nosa_step_host_all)
@@ -89,17 +87,13 @@ cudaError_t init_decode(const LayerState& s, int teams, int nst);
 int decode_active_clusters(const LayerState& s, int teams, int nst, int cs);
 cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, uint16_t* out, int teams, int nst, bool pdl, cudaStream_t st);
-// sparse prefill of an empty layer (after the bulk append of the prompt): selections of every
-// position in order into hist [U][n][cap], cache slots refreshed from the prompt, attention of
-// every position.  s.score_chunks = 1 and s.score_wpc covers the prompt's windows.
-// P: prompt positions scored per pass over the compressed keys (1, 2 or 4)
-size_t prefill_select_smem(const LayerState& s, int P);
-cudaError_t init_prefill(const LayerState& s, int P);
-// the walk with one cluster of s.score_chunks CTAs per unit (s.score_wpc windows each)
-cudaError_t init_prefill_cluster(const LayerState& s);
-int prefill_cluster_active(const LayerState& s, int cs);
+// sparse prefill of an empty layer (after the bulk append of the prompt): every position's
+// query-aware picks into qsel [U][n][ceil(nb / 32)] (bitmap words over the prompt's nb blocks),
+// the positions' selections in order into hist [U][n][cap rounded up to 8], cache slots refreshed
+// from the prompt, attention of every position
+cudaError_t init_prefill();
 int prefill_max_tokens();
-cudaError_t launch_prefill(const LayerState& s, int P, const CUtensorMap* tk, const CUtensorMap* tv,
-                           const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist,
-                           int n, cudaStream_t st);
+cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
+                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, uint32_t* qsel, int n,
+                           bool wide, cudaStream_t st);  // wide: the long-prompt forms at any length
 }  // namespace nosa

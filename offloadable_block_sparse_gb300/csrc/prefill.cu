@@ -7,14 +7,16 @@
 // attention then runs in one launch.
 //
 //   1. bulk append (append.cu): host store, eviction scores, compressed keys.
-//   2. prefill_select_kernel: one CTA per unit walks the positions.  Positions are
-//      scored P at a time (one load of every compressed-key tile for P queries); each
-//      position then runs the two-part selector of the decode step (select_core.cuh)
-//      with the geometry of T = t + 1: query-aware scores over the windows complete
-//      at T, pooled eviction scores of the blocks whose windows are complete at T
-//      (only the last two blocks can differ from the whole prompt's), the sticky
-//      eviction update and the slot pairing.  The selection is written to the
-//      caller's scratch, one row of block ids (with their kinds) per position.
+//   2a. prefill_query_kernel: the query-aware part of every position's selection at once
+//      (it reads only the position's q and the windows complete at its T): scores over
+//      those windows, the group softmax summed over heads, max-pooled onto the blocks, the
+//      top-k_q candidates.  Each warp takes a few positions and walks the compressed keys.
+//   2b. prefill_walk_kernel: one warp per unit makes the rest of every position's
+//      selection in order: the k_e query-agnostic picks among the candidates never
+//      dropped before (a short list ordered by pooled s^e), the sticky eviction update,
+//      the set difference against the previous selection and the ascending free-slot
+//      pairing, with bitmaps over the blocks.  The selection is written to the caller's
+//      scratch, one row of block ids (with their kinds) per position.
 //   3. prefill_refresh_kernel: every cache slot gets its block's K/V from the prompt
 //      (the state after the prompt is the one the decode steps would have left).
 //   4. prefill_attend_kernel: a CTA takes P consecutive positions of one unit, forms
@@ -24,8 +26,6 @@
 //      of a position up to the position itself), with the decode attention's
 //      tensor-core math per position.  Positions share every block they have in
 //      common, so the K/V reads are shared P ways.
-#include <cooperative_groups.h>
-
 #include "attend_core.cuh"
 #include "host.h"
 #include "select_core.cuh"
@@ -41,6 +41,7 @@ constexpr int kPfMaxWords = 2048 / 32;  // block bitmap words per position (prom
 // 3 query-agnostic) above; -1 pads
 constexpr int kPfKindShift = 12;
 constexpr int kPfBlockMask = (1 << kPfKindShift) - 1;
+// selection rows are cache_slots entries rounded up to 8 (16 bytes), so a row is one vector store
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
@@ -51,230 +52,527 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// ---------------------------------------------------------------- 2. selections, in order
-// Window logits of positions t0 .. t0 + np - 1 (np <= P), one CTA per unit: each 16-window tile
-// of compressed keys is loaded once and multiplied with every position's q on the tensor cores
-// (mma.sync m16n8k16, the group's heads as N = 8), so a tile's load serves P positions.  zp[p]
-// [h][i] = z_{h,i} of position p, -inf for windows not complete at that position's T (nc[p]
-// windows are).  Mst / Sst receive each position's per-head maximum and sum of exp.
-template <int P>
-__device__ __forceinline__ void score_positions(const LayerState& s, int u, const int (&nc)[P], int np,
-                                                float* const (&zp)[P], const uint4 (&qf)[P][4],
-                                                float (*Mst)[kMaxGroup], float (*Sst)[kMaxGroup],
-                                                float (*cmax)[P][kMaxGroup]) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// ---------------------------------------------------------------- 2a. query-aware picks, all positions
+// The query-aware part of a position's selection depends only on its q and the windows complete
+// at its T, not on the eviction state, so every position's k_q picks are made at once.
+constexpr int kPqWarps = 8;
+
+// grid (ceil(n / (8 PW)), U), 256 threads; dynamic shared memory [8 PW][nbn] pooled scores.
+// Warp w takes positions tw .. tw + PW - 1 (tw = (8 blockIdx.x + w) PW), their q fragments in
+// registers, and walks the unit's compressed keys in 16-window tiles twice (through L1, which the
+// CTA's warps share): the first pass forms, per position and head, the maximum and the sum of exp
+// of z_{h,i} = q_h . K~_i * scale over the windows complete at the position's T (online); the
+// second forms the group softmax summed over the heads per window and max-pools it onto the
+// blocks each window overlaps.  Each position's k_q best candidate blocks (score, then lower
+// block) go to qsel [U][n][nbw] as a bitmap over the blocks (nbw = ceil(nbn / 32) words).  The
+// last position's pooled scores are also the layer's debug scores (sq_blk).
+template <int PW>
+__global__ void __launch_bounds__(kPqWarps * 32, 1)
+    prefill_query_kernel(LayerState s, const uint16_t* __restrict__ q, uint32_t* __restrict__ qsel, int n, int nbn) {
+  extern __shared__ uint32_t pool_sm[];
+  __shared__ uint32_t qword_sm[kPqWarps][kPfMaxWords];
+  const int u = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gr = lane >> 2, t4 = lane & 3;
-  const int G = s.G, wpc = s.score_wpc;
-  const int nwarps = blockDim.x >> 5;
-  const int tiles = wpc / (16 * nwarps);
-  const int ncmax = nc[np - 1];  // the last position has the most windows
+  const int G = s.G, kq = s.k_q;
+  const int tw = (blockIdx.x * kPqWarps + warp) * PW;
+  uint32_t* pooled = pool_sm + (size_t)warp * PW * nbn;
+  pdl_wait();  // the bulk append wrote the compressed keys
+  if (tw >= n) return;  // no CTA-wide barrier follows
+  const int np = min(PW, n - tw);
+  uint4 qf[PW][4];
+  int nc[PW];
+#pragma unroll
+  for (int p = 0; p < PW; ++p) {
+    const int t = min(tw + p, n - 1);
+    nc[p] = geometry(t + 1, s.nw, s.sink).nc;
+    // q of position t: head j of unit u is row (u * G + j) * n + t
+    const uint16_t* qh = q + (((size_t)u * G + min(gr, G - 1)) * n + t) * kHeadDim;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      qf[p][c] = gr < G ? __ldg(reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4)) : make_uint4(0, 0, 0, 0);
+  }
+  for (int i = lane; i < PW * nbn; i += 32) pooled[i] = 0u;  // +0.0f: group scores are non-negative
+  const int ncw = nc[np - 1];  // the warp's last position has the most windows
+  const int ntiles = (ncw + 15) >> 4;
   const float scale = s.scale;
-  float mx[P][2];
+  const uint16_t* kt = s.kt + (size_t)u * s.nc_max * kHeadDim;
+  auto load_tile = [&](int tl, uint4 (&a)[2][4]) {
 #pragma unroll
-  for (int p = 0; p < P; ++p) mx[p][0] = mx[p][1] = -INFINITY;
-  for (int t0 = 0; t0 < tiles; t0 += 2) {  // the loads of two tiles in flight together
-    if ((warp * tiles + t0) * 16 >= ncmax) break;  // this warp's remaining tiles hold no complete window
-    uint4 a[2][2][4];
+    for (int hr = 0; hr < 2; ++hr) {
+      const int r = tl * 16 + gr + 8 * hr;
+      const uint16_t* kr = kt + (size_t)(r < ncw ? r : 0) * kHeadDim;
 #pragma unroll
-    for (int tl = 0; tl < 2; ++tl)
+      for (int c = 0; c < 4; ++c)
+        a[hr][c] = r < ncw ? __ldg(reinterpret_cast<const uint4*>(kr + 32 * c + 8 * t4)) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // rows: windows tl*16 + gr (acc 0, 1) and + 8 (acc 2, 3); columns: heads 2 t4 (acc 0, 2), 2 t4 + 1
+  auto logits = [&](const uint4 (&a)[2][4], const uint4 (&qq)[4], float (&acc)[4]) {
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int r = (warp * tiles + t0 + tl) * 16 + gr + 8 * hr;
-        const bool ok = t0 + tl < tiles && r < ncmax;
-        const uint16_t* kr = s.kt + ((size_t)u * s.nc_max + (ok ? r : 0)) * kHeadDim;
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t* r0 = reinterpret_cast<const uint32_t*>(&a[0][c]);
+      const uint32_t* r1 = reinterpret_cast<const uint32_t*>(&a[1][c]);
+      const uint32_t* qv = reinterpret_cast<const uint32_t*>(&qq[c]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          a[tl][hr][c] = ok ? *reinterpret_cast<const uint4*>(kr + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t af[4] = {r0[2 * hh], r1[2 * hh], r0[2 * hh + 1], r1[2 * hh + 1]};
+        mma_16816(acc, af, qv[2 * hh], qv[2 * hh + 1]);
       }
+    }
+  };
+  float M[PW][2], L[PW][2];
 #pragma unroll
-    for (int tl = 0; tl < 2; ++tl) {
-      if (t0 + tl >= tiles) break;
-      const int wl0 = (warp * tiles + t0 + tl) * 16 + gr;
+  for (int p = 0; p < PW; ++p) M[p][0] = M[p][1] = -INFINITY, L[p][0] = L[p][1] = 0.f;
+  for (int tl = 0; tl < ntiles; ++tl) {  // pass 1: per (position, head) maximum and sum of exp
+    uint4 a[2][4];
+    load_tile(tl, a);
+    const int w0 = tl * 16 + gr;
 #pragma unroll
-      for (int p = 0; p < P; ++p) {
-        if (p >= np) break;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int p = 0; p < PW; ++p) {
+      if (p >= np) break;
+      float acc[4];
+      logits(a, qf[p], acc);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t* r0 = reinterpret_cast<const uint32_t*>(&a[tl][0][c]);
-          const uint32_t* r1 = reinterpret_cast<const uint32_t*>(&a[tl][1][c]);
-          const uint32_t* qq = reinterpret_cast<const uint32_t*>(&qf[p][c]);
+      for (int j = 0; j < 2; ++j) {
+        const float z0 = w0 < nc[p] ? acc[j] * scale : -INFINITY;
+        const float z1 = w0 + 8 < nc[p] ? acc[2 + j] * scale : -INFINITY;
+        const float mn = fmaxf(M[p][j], fmaxf(z0, z1));
+        if (mn > -INFINITY) {
+          L[p][j] = L[p][j] * expf(M[p][j] - mn) + expf(z0 - mn) + expf(z1 - mn);
+          M[p][j] = mn;
+        }
+      }
+    }
+  }
+  float inv[PW][2];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const uint32_t af[4] = {r0[2 * hh], r1[2 * hh], r0[2 * hh + 1], r1[2 * hh + 1]};
-            mma_16816(acc, af, qq[2 * hh], qq[2 * hh + 1]);
+  for (int p = 0; p < PW; ++p)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // the lanes of one column hold different windows
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, M[p][j], o), lo = __shfl_xor_sync(0xffffffffu, L[p][j], o);
+        const float mn = fmaxf(M[p][j], mo);
+        if (mn > -INFINITY) {
+          L[p][j] = (M[p][j] > -INFINITY ? L[p][j] * expf(M[p][j] - mn) : 0.f) + (mo > -INFINITY ? lo * expf(mo - mn) : 0.f);
+          M[p][j] = mn;
+        }
+      }
+      inv[p][j] = L[p][j] > 0.f ? 1.f / L[p][j] : 0.f;
+    }
+  for (int tl = 0; tl < ntiles; ++tl) {  // pass 2: group scores per window, max-pooled onto blocks
+    uint4 a[2][4];
+    load_tile(tl, a);
+    const int w0 = tl * 16 + gr;
+#pragma unroll
+    for (int p = 0; p < PW; ++p) {
+      if (p >= np) break;
+      float acc[4];
+      logits(a, qf[p], acc);
+      float e0 = 0.f, e1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (2 * t4 + j >= G) continue;
+        if (w0 < nc[p]) e0 += expf(acc[j] * scale - M[p][j]) * inv[p][j];
+        if (w0 + 8 < nc[p]) e1 += expf(acc[2 + j] * scale - M[p][j]) * inv[p][j];
+      }
+      e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
+      e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
+      e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
+      e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
+      if (t4 == 0) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int w = w0 + 8 * hr;
+          if (w >= nc[p]) continue;
+          // window w overlaps blocks (w + 1) / 4 and, when w = 4 b + 3, also b = (w + 1) / 4 - 1
+          const uint32_t bits = __float_as_uint(hr ? e1 : e0);
+          const int b1 = (w + 1) >> 2;
+          if (b1 < nbn) atomicMax(&pooled[p * nbn + b1], bits);
+          if (((w + 1) & 3) == 0 && b1 >= 1) atomicMax(&pooled[p * nbn + b1 - 1], bits);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  // a block with no complete window scores -inf, as in the decode step
+  auto pooled_score = [&](int p, int b) {
+    return (nc[p] >= 1 && 4 * b <= nc[p]) ? __uint_as_float(pooled[p * nbn + b]) : -INFINITY;
+  };
+  const int nbw = (nbn + 31) >> 5;
+  uint32_t* qw = qword_sm[warp];
+#pragma unroll
+  for (int p = 0; p < PW; ++p) {
+    if (p >= np) break;
+    const int t = tw + p;
+    const Geometry geo = geometry(t + 1, s.nw, s.sink);
+    for (int w = lane; w < nbw; w += 32) qw[w] = 0u;
+    __syncwarp();
+    const int c0 = s.sink, c1 = geo.ws;  // candidates [c0, c1)
+    unsigned long long thr = ~0ull;      // keys at or above it were taken by an earlier round
+    for (int got = 0; got < kq; got += 32) {
+      unsigned long long best = 0ull;    // below every real key (its block field is never 0)
+      for (int bb = c0; bb < c1; bb += 32) {
+        const int b = bb + lane;
+        unsigned long long x = 0ull;
+        if (b < c1) {
+          x = rank_key(orderable(pooled_score(p, b)), b);
+          if (x >= thr) x = 0ull;
+        }
+        best = warp_merge_top(best, warp_sort_desc(x));
+      }
+      if (best && lane < kq - got) {
+        const int b = (int)(0xFFFFFFFFu - (uint32_t)best);
+        atomicOr(&qw[b >> 5], 1u << (b & 31));
+      }
+      thr = __shfl_sync(0xffffffffu, best, 31);
+      if (thr == 0ull) break;  // fewer candidates than k_q
+    }
+    __syncwarp();
+    uint32_t* row = qsel + ((size_t)u * n + t) * nbw;
+    for (int w = lane; w < nbw; w += 32) row[w] = qw[w];
+    __syncwarp();
+    if (t == n - 1)
+      for (int b = lane; b < geo.nb; b += 32) s.sq_blk[(size_t)u * s.nb_max + b] = pooled_score(p, b);
+  }
+}
+
+// ---------------------------------------------------------------- 2b. the walk over the positions
+// One warp per unit makes the stateful part of every position's selection, in order: the k_e
+// query-agnostic picks among the candidates never dropped before, the sticky eviction update,
+// the set difference against the previous selection and the ascending free-slot pairing.  Every
+// candidate a selection leaves out is dropped for good, so the candidates still eligible are the
+// last selection's never-dropped blocks plus the blocks that have just become candidates; the warp
+// keeps them in a list ordered by (pooled s^e, then lower block), and a position's picks are the
+// list's first k_e entries outside its query-aware picks.  Selections are bitmaps over the blocks.
+// A position's work is one dependent chain of a single warp, so the loops run over the list
+// entries and bitmap words the configuration needs (KS entries and NW words per lane).
+constexpr int kWalkWarps = 4;
+constexpr int kWalkMaxSlots = 9;  // list entries per lane: k_q + k_e + 1 <= 288
+
+__host__ __device__ inline size_t walk_warp_bytes(int nbn) {
+  const int nbw = (nbn + 31) / 32;
+  return (size_t)32 * kWalkMaxSlots * 8 + (size_t)kPfMaxWords * 16 + 4 * (size_t)nbw * 4 + 8 * 4 +
+         (size_t)((nbn + 7) & ~7) * 2 + 4 * 256 * 2;
+}
+
+__device__ __forceinline__ uint32_t range_bits(int w, int lo, int hi) {  // bits of [lo, hi) in word w
+  const int a = max(lo - 32 * w, 0), b = min(hi - 32 * w, 32);
+  if (a >= b) return 0u;
+  const uint32_t top = b == 32 ? 0xFFFFFFFFu : ((1u << b) - 1u);
+  return top & ~((1u << a) - 1u);
+}
+
+// grid ceil(U / 4), 128 threads; dynamic shared memory 4 x walk_warp_bytes(nbn).  hist: [U][n][capp]
+// selection entries (block | kind << 12, -1 padded; capp = cap rounded up to 8); qsel: the
+// query-aware picks of 2a as [U][n][nbw] bitmap words.
+// KS: list entries per lane (k_q + k_e + 1 <= 32 KS); NW: bitmap words per lane (nbn <= 1024 NW).
+template <int KS, int NW>
+__global__ void __launch_bounds__(kWalkWarps * 32)
+    prefill_walk_kernel(LayerState s, const uint32_t* __restrict__ qsel, int16_t* __restrict__ hist, int n, int nbn) {
+  extern __shared__ __align__(16) unsigned char wsm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x * kWalkWarps + warp;
+  pdl_wait();  // the query-aware picks, and the bulk append's pooled eviction scores
+  if (u >= s.U) return;  // no CTA-wide barrier follows
+  const int nbw = (nbn + 31) / 32;
+  unsigned char* base = wsm + (size_t)warp * walk_warp_bytes(nbn);
+  unsigned long long* Lk = reinterpret_cast<unsigned long long*>(base);  // the eligible list, descending keys
+  uint4* wrec = reinterpret_cast<uint4*>(base + 32 * kWalkMaxSlots * 8);  // per word: D, new, left, Q
+  uint32_t* ev = reinterpret_cast<uint32_t*>(wrec + kPfMaxWords);
+  uint32_t* sprev = ev + nbw;  // the previous selection
+  uint32_t* qbm = sprev + nbw;  // this position's query-aware picks
+  uint32_t* ebm = qbm + nbw;    // and query-agnostic ones
+  uint32_t* fbm = ebm + nbw;    // free cache slots (8 words)
+  int16_t* slot_of = reinterpret_cast<int16_t*>(fbm + 8);
+  int16_t* slot_blk = slot_of + ((nbn + 7) & ~7);
+  int16_t* newl = slot_blk + 256;
+  int16_t* freel = newl + 256;
+  int16_t* rowbuf = freel + 256;  // the position's row, stored to hist in one vector store
+  const int ke = s.k_e, cap = s.cap, sink = s.sink;
+  const int capp = (cap + 7) & ~7;
+  const unsigned int lt = (1u << lane) - 1u;
+  // an empty layer: nothing dropped, selected or cached
+  for (int w = lane; w < nbw; w += 32) ev[w] = sprev[w] = qbm[w] = ebm[w] = 0u;
+  if (lane < 8) fbm[lane] = range_bits(lane, 0, cap);
+  for (int b = lane; b < nbn; b += 32) slot_of[b] = -1;
+  for (int i = lane; i < 256; i += 32) slot_blk[i] = -1;
+  __syncwarp();
+  const float* se_blk = s.se_blk + (size_t)u * s.nb_max;
+  const float* se_win = s.se_win + (size_t)u * s.nc_max;
+  // list key of candidate b at T: its pooled s^e over the windows complete at T (only the last
+  // two blocks can still change), then the lower block
+  auto se_key = [&](int b, const Geometry& g) {
+    float v;
+    if (b >= g.nb - 2) {
+      v = -INFINITY;
+      for (int i = max(4 * b - 1, 0); i <= min(4 * b + 3, g.nc - 1); ++i) v = fmaxf(v, se_win[i]);
+    } else {
+      v = se_blk[b];
+    }
+    return rank_key(orderable(v), b);
+  };
+  int nL = 0;
+  auto l_insert = [&](unsigned long long key) {  // at its place in the descending list
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < KS; ++i) c += (lane + 32 * i < nL && Lk[lane + 32 * i] > key) ? 1 : 0;
+    c = warp_sum(c);
+    unsigned long long v[KS];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const int j = lane + 32 * i;
+      v[i] = (j >= c && j < nL) ? Lk[j] : 0ull;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const int j = lane + 32 * i;
+      if (j >= c && j < nL && j + 1 < 32 * KS) Lk[j + 1] = v[i];
+    }
+    if (lane == 0 && c < 32 * KS) Lk[c] = key;
+    __syncwarp();
+    nL = min(nL + 1, 32 * KS);
+  };
+  // removes the entries of blocks >= bmin (at most two: the last two blocks) and returns them
+  auto l_remove_from = [&](int bmin, unsigned long long& o0, unsigned long long& o1) {
+    int nout = 0, wpos = 0;
+    unsigned long long v[KS];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) v[i] = lane + 32 * i < nL ? Lk[lane + 32 * i] : 0ull;
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const bool in = lane + 32 * i < nL;
+      const bool late = in && (int)(0xFFFFFFFFu - (uint32_t)v[i]) >= bmin;
+      const unsigned int kb = __ballot_sync(0xffffffffu, in && !late), lb = __ballot_sync(0xffffffffu, late);
+      if (in && !late) Lk[wpos + __popc(kb & lt)] = v[i];
+      for (unsigned int m = lb; m; m &= m - 1u) {
+        const unsigned long long x = __shfl_sync(0xffffffffu, v[i], __ffs(m) - 1);
+        if (nout == 0) o0 = x;
+        else if (nout == 1) o1 = x;
+        ++nout;
+      }
+      wpos += __popc(kb);
+    }
+    __syncwarp();
+    nL = wpos;
+    return min(nout, 2);
+  };
+  uint32_t qn[NW];  // the next position's query-aware words, loaded a position ahead
+  auto load_q = [&](int t) {
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      const int w = lane + 32 * k;
+      qn[k] = (t < n && w < nbw) ? qsel[((size_t)u * n + t) * nbw + w] : 0u;
+    }
+  };
+  load_q(0);
+  unsigned long long st_fetch = 0, st_short = 0, st_gs = 0, st_gn = 0, st_gd = 0;
+  uint32_t st_gmin = 0x7F800000u;  // +inf
+  int ws_prev = sink;               // candidates so far: [sink, ws_prev)
+  int nS_prev = 0, nS = 0, nD = 0, nDnew = 0, nNew = 0;
+  for (int t = 0; t < n; ++t) {
+    const Geometry geo = geometry(t + 1, s.nw, s.sink);
+    const int nbwT = (geo.nb + 31) >> 5;
+    uint32_t qc[NW];
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      qc[k] = qn[k];
+      if (lane + 32 * k < nbw) qbm[lane + 32 * k] = qc[k];
+    }
+    load_q(t + 1);  // in flight during this position
+    // list keys that follow T (a window shorter than two blocks lets the last two blocks be
+    // candidates), then the blocks that have just become candidates
+    if (s.nw < 2 && nL > 0) {
+      unsigned long long l0 = 0ull, l1 = 0ull;
+      const int nlate = l_remove_from(geo.nb - 2, l0, l1);
+      if (nlate > 0) l_insert(se_key((int)(0xFFFFFFFFu - (uint32_t)l0), geo));
+      if (nlate > 1) l_insert(se_key((int)(0xFFFFFFFFu - (uint32_t)l1), geo));
+    }
+    for (int b = max(sink, ws_prev); b < geo.ws; ++b) l_insert(se_key(b, geo));
+    ws_prev = max(ws_prev, geo.ws);
+    __syncwarp();  // query-aware words visible to every lane
+    // E: the list's first k_e entries outside Q; the other entries outside Q are dropped for good
+    int nElig = 0, wpos = 0;
+    unsigned long long v[KS];
+    bool keep[KS];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      const bool in = lane + 32 * i < nL;
+      v[i] = in ? Lk[lane + 32 * i] : 0ull;
+      const int b = (int)(0xFFFFFFFFu - (uint32_t)v[i]);
+      const bool inQ = in && ((qbm[b >> 5] >> (b & 31)) & 1u);
+      const bool elig = in && !inQ;
+      const unsigned int eb = __ballot_sync(0xffffffffu, elig);
+      const bool inE = elig && nElig + __popc(eb & lt) < ke;
+      nElig += __popc(eb);
+      if (inE) atomicOr(&ebm[b >> 5], 1u << (b & 31));
+      if (elig && !inE) atomicOr(&ev[b >> 5], 1u << (b & 31));
+      keep[i] = inQ || inE;
+    }
+    const int nE = min(ke, nElig);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {  // the list keeps D's never-dropped blocks, in order
+      const unsigned int kb = __ballot_sync(0xffffffffu, keep[i]);
+      if (keep[i]) Lk[wpos + __popc(kb & lt)] = v[i];
+      wpos += __popc(kb);
+    }
+    nL = wpos;
+    // S = sink + D + window per word; the blocks new to it and the blocks that left it
+    uint32_t Sw[NW];
+    int cnt = 0;  // popc(D) | popc(new) << 10 | popc(D & new) << 20 (each at most 256)
+#pragma unroll
+    for (int k = 0; k < NW; ++k) {
+      const int w = lane + 32 * k;
+      Sw[k] = 0u;
+      if (w >= nbwT) continue;
+      const uint32_t D = qc[k] | ebm[w];
+      const uint32_t sw = D | range_bits(w, 0, geo.ns) | range_bits(w, geo.ws, geo.nb);
+      const uint32_t pv = sprev[w];
+      Sw[k] = sw;
+      wrec[w] = make_uint4(D, sw & ~pv, pv & ~sw, qc[k]);
+      cnt += __popc(D) | (__popc(sw & ~pv) << 10) | (__popc(D & sw & ~pv) << 20);
+    }
+    cnt = warp_sum(cnt);
+    nD = cnt & 1023;
+    const int nNewAll = (cnt >> 10) & 1023;
+    nDnew = (cnt >> 20) & 1023;
+    nS = geo.ns + nD + (geo.nb - geo.ws);
+    __syncwarp();
+    // one pass over the words, a lane per bit: D's row entries (ascending), the new blocks in
+    // order, and the slots of the blocks that left become free
+    {
+      int dpos = geo.ns, npos = 0;
+      const uint32_t bit = 1u << lane;
+      for (int w = 0; w < nbwT; ++w) {
+        const uint4 r = wrec[w];
+        if ((r.x | r.y | r.z) == 0u) continue;
+        const int b = 32 * w + lane;
+        if (r.x & bit) {
+          const int pos = dpos + __popc(r.x & lt);
+          if (pos < capp) rowbuf[pos] = (int16_t)(b | (((r.w & bit) ? 2 : 3) << kPfKindShift));
+        }
+        if (r.y & bit) {
+          const int i = npos + __popc(r.y & lt);
+          if (i < 256) newl[i] = (int16_t)b;
+        }
+        if (r.z & bit) {
+          const int sl = slot_of[b];
+          slot_of[b] = -1;
+          if (sl >= 0) {
+            slot_blk[sl] = -1;
+            atomicOr(&fbm[sl >> 5], 1u << (sl & 31));
           }
         }
+        dpos += __popc(r.x);
+        npos += __popc(r.y);
+      }
+    }
+    // the row's sink and window ranges and padding (kinds 0 and 1), then one vector store per lane
+    if (nS > cap && lane == 0) atomicOr(s.err, kErrBounds);  // cannot happen when cap = sink + window + k_q + k_e
+    for (int i = lane; i < geo.ns; i += 32) rowbuf[i] = (int16_t)i;
+    for (int i = lane; i < geo.nb - geo.ws; i += 32)
+      if (geo.ns + nD + i < capp) rowbuf[geo.ns + nD + i] = (int16_t)((geo.ws + i) | (1 << kPfKindShift));
+    for (int i = min(nS, capp) + lane; i < capp; i += 32) rowbuf[i] = -1;
+    __syncwarp();
+    if (lane < capp / 8)
+      reinterpret_cast<uint4*>(hist + ((size_t)u * n + t) * capp)[lane] = reinterpret_cast<const uint4*>(rowbuf)[lane];
+    // the i-th new block (ascending) takes the i-th free slot (ascending)
+    nNew = min(nNewAll, 256);
+    {
+      int fbase = 0;
+      for (int w = 0; w < 8 && fbase < nNew; ++w) {
+        const uint32_t fv = fbm[w];
+        if (!fv) continue;
+        const int i = fbase + __popc(fv & lt);
+        const bool take = ((fv >> lane) & 1u) && i < nNew;
+        if (take) {
+          const int sl = 32 * w + lane, b = newl[i];
+          slot_of[b] = (int16_t)sl;
+          slot_blk[sl] = (int16_t)b;
+          freel[i] = (int16_t)sl;
+        }
+        const unsigned int tk = __ballot_sync(0xffffffffu, take);
+        if (lane == 0) fbm[w] = fv & ~tk;
+        fbase += __popc(fv);
+      }
+      if (fbase < nNew) {  // cannot happen when cap >= |S|; keep the slot table in bounds anyway
+        if (lane == 0) atomicOr(s.err, kErrBounds);
+        nNew = fbase;
+      }
+    }
+    // the decode step's counters
+    st_fetch += nNew;
+    if (nE < ke) ++st_short;
+    if (nS_prev > 0 && nD > 0) {  // some block was cached before
+      ++st_gs;
+      st_gn += nD - nDnew;
+      st_gd += nD;
+      st_gmin = min(st_gmin, __float_as_uint((float)(nD - nDnew) / (float)nD));
+    }
+    nS_prev = nS;
+    // this selection is the next position's previous one; the E bitmap starts empty (the last
+    // position's previous selection and picks stay, for the state below)
+    if (t + 1 < n) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int wl = wl0 + 8 * (j >> 1), h = 2 * t4 + (j & 1);
-          const float z = wl < nc[p] ? acc[j] * scale : -INFINITY;
-          zp[p][h * wpc + wl] = z;
-          mx[p][j & 1] = fmaxf(mx[p][j & 1], z);
+      for (int k = 0; k < NW; ++k) {
+        const int w = lane + 32 * k;
+        if (w < nbwT) {
+          sprev[w] = Sw[k];
+          ebm[w] = 0u;
         }
       }
     }
+    __syncwarp();
   }
-#pragma unroll
-  for (int p = 0; p < P; ++p)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      mx[p][j] = fmaxf(mx[p][j], __shfl_xor_sync(0xffffffffu, mx[p][j], 4));
-      mx[p][j] = fmaxf(mx[p][j], __shfl_xor_sync(0xffffffffu, mx[p][j], 8));
-      mx[p][j] = fmaxf(mx[p][j], __shfl_xor_sync(0xffffffffu, mx[p][j], 16));
-    }
-  if (gr == 0)
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      cmax[warp][p][2 * t4] = mx[p][0];
-      cmax[warp][p][2 * t4 + 1] = mx[p][1];
-    }
-  __syncthreads();
-  if (tid < P * kMaxGroup) {
-    const int p = tid / kMaxGroup, h = tid % kMaxGroup;
-    float mm = -INFINITY;
-    for (int w = 0; w < nwarps; ++w) mm = fmaxf(mm, cmax[w][p][h]);
-    Mst[p][h] = mm;
-  }
-  __syncthreads();
-  for (int ph = warp; ph < np * G; ph += nwarps) {  // sums of exp, one (position, head) per warp
-    const int p = ph / G, h = ph % G;
-    const float M = Mst[p][h];
-    float e = 0.f;
-    if (M > -INFINITY)
-      for (int wl = lane; wl < nc[p]; wl += 32) e += expf(zp[p][h * wpc + wl] - M);
-    e = warp_sum(e);
-    if (lane == 0) Sst[p][h] = e;
-  }
-  __syncthreads();
-}
-
-// grid (1, U) in clusters of one CTA (the selector phases use the cluster API); 256 threads.
-// q: [B][Hq][n][d]; hist: [U][n][cap] selection entries, -1 padded.  Positions are scored P at
-// a time (score_positions), then selected one after the other: each position's selection needs
-// the eviction state and slot map the previous one left.  Dynamic shared memory: the selector's
-// region (whose logits array serves position 0) and P - 1 more logits arrays.
-template <int P>
-__global__ void __launch_bounds__(kScoreThreads, 1)
-    prefill_select_kernel(LayerState s, const uint16_t* __restrict__ q, int16_t* __restrict__ hist, int n) {
-  extern __shared__ __align__(16) unsigned char dsm[];
-  __shared__ SelShared sh;
-  __shared__ float cmax[kScoreWarps][P][kMaxGroup];
-  __shared__ float Mst[P][kMaxGroup], Sst[P][kMaxGroup];
-  cg::cluster_group cluster = cg::this_cluster();
-  const int u = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
-  const Smem m = layout(dsm, s);
-  const int G = s.G, wpc = s.score_wpc;
-  float* zextra = reinterpret_cast<float*>(dsm + ((region_bytes(s) + 15) & ~size_t(15)));
-  float* zp[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) zp[p] = p == 0 ? m.zs : zextra + (size_t)(p - 1) * kMaxGroup * wpc;
-  pdl_wait();  // the bulk append before this kernel wrote the keys, scores and host store
-  for (int t0 = 0; t0 < n; t0 += P) {
-    const int np = min(P, n - t0);
-    int nc[P];
-    uint4 qf[P][4];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      const int t = min(t0 + p, n - 1);
-      nc[p] = geometry(t + 1, s.nw, s.sink).nc;
-      // q of position t: head j of unit u is row (u * G + j) * n + t
-      const int gr = lane >> 2, t4 = lane & 3;
-      const uint16_t* qh = q + (((size_t)u * G + min(gr, G - 1)) * n + t) * kHeadDim;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        qf[p][c] = gr < G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
-    }
-    score_positions<P>(s, u, nc, np, zp, qf, Mst, Sst, cmax);
-    for (int p = 0; p < np; ++p) {
-      const int t = t0 + p, T = t + 1;
-      const Geometry geo = geometry(T, s.nw, s.sink);
-      const int my_slot_blk = leader_prefetch(s, u, geo.nb, geo.nb, m);
-      if (tid < G) {
-        sh.Mloc[tid] = Mst[p][tid];
-        sh.Sloc[tid] = Sst[p][tid];
-      }
-      Smem mp = m;
-      mp.zs = zp[p];
-      pool_blocks(s, u, geo, 0, 1, mp, sh);  // opens with a barrier after the statistics above
-      rank_local(s, geo, 0, 1, mp, sh);
-      cluster.sync();
-      cp_async_wait_all();
-      // The context's pooled eviction scores cover the whole prompt.  At T a block pools only the
-      // windows complete at T; for every block but the last two those are all its windows already.
-      if (tid < 2) {
-        const int b = geo.nb - 2 + tid;
-        if (b >= 0) {
-          const int lo = max(4 * b - 1, 0), hi = min(4 * b + 3, geo.nc - 1);
-          float mx = -INFINITY;
-          for (int i = lo; i <= hi; ++i) mx = fmaxf(mx, s.se_win[(size_t)u * s.nc_max + i]);
-          m.sek[b] = mx;
-        }
-      }
-      __syncthreads();
-      int16_t* row = hist + ((size_t)u * n + t) * s.cap;
-      const int nS = leader_select(s, u, geo, 1, mp, sh, my_slot_blk, true, [&](int pos, int b, int, bool, int, int kd) {
-        row[pos] = (int16_t)(b | (kd << kPfKindShift));
-      });
-      for (int i = max(nS, 0) + tid; i < s.cap; i += blockDim.x) row[i] = -1;
-      __syncthreads();  // this position's state (slots, eviction words) is read by the next one
+  // the unit's state after the prompt: the last selection (the row still in shared memory) with
+  // kinds, slots and fetched marks, its fetch list, the eviction bitmap and the slot tables
+  int32_t* sel = s.sel + (size_t)u * cap;
+  int32_t* kind = s.sel_kind + (size_t)u * cap;
+  int32_t* sslot = s.sel_slot + (size_t)u * cap;
+  int32_t* snew = s.sel_new + (size_t)u * cap;
+  const int nSw = min(nS, cap);
+  for (int i = lane; i < cap; i += 32) {
+    if (i < nSw) {
+      const int e = rowbuf[i], b = e & kPfBlockMask;
+      sel[i] = b;
+      kind[i] = e >> kPfKindShift;
+      sslot[i] = slot_of[b];
+      snew[i] = ((sprev[b >> 5] >> (b & 31)) & 1u) ? 0 : 1;  // sprev holds the position before the last
+    } else {
+      sel[i] = -1;
+      kind[i] = -1;
+      sslot[i] = -1;
+      snew[i] = 0;
     }
   }
-}
-
-// The same walk with one thread-block cluster of CS CTAs per unit, for layers with few units:
-// CTA r scores windows [r * wpc, (r + 1) * wpc) of every position and pools and ranks the blocks
-// it owns (the decode selector's phases, statistics and local winners through distributed
-// shared memory between two cluster barriers); rank 0 then makes the selection on the state the
-// previous position left while the other CTAs go on to score the next position.  Every
-// cross-CTA read of a position happens between that position's two barriers, and no CTA writes
-// the next position's statistics or winners before all have passed its first barrier.
-__global__ void __launch_bounds__(kScoreThreads, 1)
-    prefill_select_cluster_kernel(LayerState s, const uint16_t* __restrict__ q, int16_t* __restrict__ hist, int n) {
-  extern __shared__ __align__(16) unsigned char dsm[];
-  __shared__ SelShared sh;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank(), CS = (int)cluster.num_blocks();
-  const int u = blockIdx.y, tid = threadIdx.x;
-  const Smem m = layout(dsm, s);
-  pdl_wait();  // the bulk append before this kernel wrote the keys, scores and host store
-  for (int t = 0; t < n; ++t) {
-    const int T = t + 1;
-    const Geometry geo = geometry(T, s.nw, s.sink);
-    int my_slot_blk = -1;
-    if (rank == 0) my_slot_blk = leader_prefetch(s, u, geo.nb, geo.nb, m);
-    uint4 qf[4];
-    {  // q of position t: head j of unit u is row (u * G + j) * n + t
-      const int lane = tid & 31, gr = lane >> 2, t4 = lane & 3;
-      const uint16_t* qh = q + (((size_t)u * s.G + min(gr, s.G - 1)) * n + t) * kHeadDim;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        qf[c] = gr < s.G ? *reinterpret_cast<const uint4*>(qh + 32 * c + 8 * t4) : make_uint4(0, 0, 0, 0);
+  int32_t* fl = s.fetch + (size_t)u * cap * 2;
+  for (int j = lane; j < nNew; j += 32) {
+    fl[2 * j] = newl[j];
+    fl[2 * j + 1] = freel[j];
+  }
+  if (lane == 0) {
+    s.n_sel[u] = nSw;
+    s.n_fetch[u] = nNew;
+    s.gamma[2 * u] = nD - nDnew;
+    s.gamma[2 * u + 1] = nD;
+  }
+  for (int w = lane; w < s.ev_words; w += 32) s.evicted[(size_t)u * s.ev_words + w] = w < nbw ? ev[w] : 0u;
+  for (int i = lane; i < cap; i += 32) s.slot_blk[(size_t)u * cap + i] = slot_blk[i];
+  for (int b = lane; b < nbn; b += 32) s.blk2slot[(size_t)u * s.nb_max + b] = slot_of[b];
+  if (lane == 0) {
+    atomicAdd(&s.stats->selections, (unsigned long long)n);
+    atomicAdd(&s.stats->blocks_fetched, st_fetch);
+    atomicAdd(&s.stats->short_selections, st_short);
+    if (st_gs) {
+      atomicAdd(&s.stats->gamma_samples, st_gs);
+      atomicAdd(&s.stats->gamma_num, st_gn);
+      atomicAdd(&s.stats->gamma_den, st_gd);
+      atomicMin(&s.stats->gamma_min_bits, st_gmin);
     }
-    score_windows<2>(s, u, geo.nc, rank, m, sh, qf);
-    cluster.sync();  // every CTA's statistics of this position are visible
-    pool_blocks(s, u, geo, rank, CS, m, sh);
-    rank_local(s, geo, rank, CS, m, sh);
-    cluster.sync();  // the local winners have landed in rank 0; the statistics reads are done
-    if (rank != 0) continue;
-    cp_async_wait_all();
-    // pooled eviction scores of the last two blocks as of T (windows complete at T only)
-    if (tid < 2) {
-      const int b = geo.nb - 2 + tid;
-      if (b >= 0) {
-        const int lo = max(4 * b - 1, 0), hi = min(4 * b + 3, geo.nc - 1);
-        float mx = -INFINITY;
-        for (int i = lo; i <= hi; ++i) mx = fmaxf(mx, s.se_win[(size_t)u * s.nc_max + i]);
-        m.sek[b] = mx;
-      }
-    }
-    __syncthreads();
-    int16_t* row = hist + ((size_t)u * n + t) * s.cap;
-    const int nS = leader_select(s, u, geo, CS, m, sh, my_slot_blk, true, [&](int pos, int b, int, bool, int, int kd) {
-      row[pos] = (int16_t)(b | (kd << kPfKindShift));
-    });
-    for (int i = max(nS, 0) + tid; i < s.cap; i += blockDim.x) row[i] = -1;
-    __syncthreads();  // this position's state (slots, eviction words) is read by the next one
   }
 }
 
@@ -333,7 +631,7 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
   __syncthreads();
   for (int idx = tid; idx < np * cap; idx += blockDim.x) {
     const int p = idx / cap, e = idx % cap;
-    const int h = hist[((size_t)u * n + t0 + p) * cap + e];
+    const int h = hist[((size_t)u * n + t0 + p) * ((cap + 7) & ~7) + e];
     const int b = h & kPfBlockMask;
     if (h >= 0 && b < nb_last) atomicOr(&bm[p][b >> 5], 1u << (b & 31));
   }
@@ -501,68 +799,57 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-size_t prefill_select_smem(const LayerState& s, int P) {
-  return ((region_bytes(s) + 15) & ~size_t(15)) + (size_t)(P - 1) * kMaxGroup * s.score_wpc * sizeof(float);
-}
-
+// prompts of up to 65,536 tokens (1,024 blocks): four positions per query-aware warp and one
+// bitmap word per walk lane; longer ones two and two
+static bool prefill_wide(int nbn) { return nbn > 1024; }
+static size_t query_smem(int nbn, int pw) { return (size_t)kPqWarps * pw * nbn * sizeof(uint32_t); }
+static size_t walk_smem(int nbn) { return kWalkWarps * walk_warp_bytes(nbn); }
 static size_t prefill_attend_smem() { return 1024 + (size_t)kPfStages * kStageBytes; }
-
-cudaError_t init_prefill_cluster(const LayerState& s) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)region_bytes(s));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(prefill_select_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  return e;
-}
-
-int prefill_cluster_active(const LayerState& s, int cs) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kScoreThreads);
-  cfg.gridDim = dim3(cs, 1);
-  cfg.dynamicSmemBytes = region_bytes(s);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int nc = 0;
-  if (cudaOccupancyMaxActiveClusters(&nc, prefill_select_cluster_kernel, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  return nc;
-}
-
-cudaError_t init_prefill(const LayerState& s, int P) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_attend_kernel<kPfPositions>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prefill_attend_smem());
-  const int sm = (int)prefill_select_smem(s, P);
-  if (e == cudaSuccess)
-    e = P == 4   ? cudaFuncSetAttribute(prefill_select_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm)
-        : P == 2 ? cudaFuncSetAttribute(prefill_select_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm)
-                 : cudaFuncSetAttribute(prefill_select_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-  return e;
-}
 
 int prefill_max_tokens() { return kPfMaxWords * 32 * kBlock; }
 
-cudaError_t launch_prefill(const LayerState& s, int P, const CUtensorMap* tk, const CUtensorMap* tv,
-                           const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist,
-                           int n, cudaStream_t st) {
-  const dim3 block(kScoreThreads);
-  cudaError_t e;
-  if (s.score_chunks > 1) {  // a cluster per unit
-    e = launch_ex(prefill_select_cluster_kernel, dim3(s.score_chunks, s.U), block, region_bytes(s), st, true,
-                  s.score_chunks, s, q, hist, n);
-  } else {
-    const dim3 grid(1, s.U);
-    const size_t sm = prefill_select_smem(s, P);
-    e = P == 4   ? launch_ex(prefill_select_kernel<4>, grid, block, sm, st, true, 1, s, q, hist, n)
-        : P == 2 ? launch_ex(prefill_select_kernel<2>, grid, block, sm, st, true, 1, s, q, hist, n)
-                 : launch_ex(prefill_select_kernel<1>, grid, block, sm, st, true, 1, s, q, hist, n);
+cudaError_t init_prefill() {
+  const int nbn = kPfMaxWords * 32;
+  cudaError_t e = cudaFuncSetAttribute(prefill_attend_kernel<kPfPositions>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prefill_attend_smem());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_query_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)query_smem(1024, 4));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(prefill_query_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)query_smem(nbn, 2));
+  return e;  // the walk's shared memory (4 x walk_warp_bytes) stays under the default 48 KiB
+}
+
+cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
+                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, uint32_t* qsel, int n,
+                           bool wide, cudaStream_t st) {
+  const int nbn = (n + kBlock - 1) / kBlock;
+  wide = wide || prefill_wide(nbn);
+  const int pw = wide ? 2 : 4;
+  const dim3 qgrid((n + kPqWarps * pw - 1) / (kPqWarps * pw), s.U);
+  cudaError_t e =
+      pw == 4 ? launch_ex(prefill_query_kernel<4>, qgrid, dim3(kPqWarps * 32), query_smem(nbn, 4), st, true, 0, s, q,
+                          qsel, n, nbn)
+              : launch_ex(prefill_query_kernel<2>, qgrid, dim3(kPqWarps * 32), query_smem(nbn, 2), st, true, 0, s, q,
+                          qsel, n, nbn);
+  if (e != cudaSuccess) return e;
+  // list entries and bitmap words per lane: as few as the configuration allows
+  const int need = s.k_q + s.k_e + 1;
+  const int ks = need <= 32 ? 1 : need <= 64 ? 2 : need <= 96 ? 3 : need <= 128 ? 4 : kWalkMaxSlots;
+  const bool nw1 = !wide;
+  const dim3 wgrid((s.U + kWalkWarps - 1) / kWalkWarps), wblock(kWalkWarps * 32);
+  const size_t wsm = walk_smem(nbn);
+  const uint32_t* qs = qsel;
+#define NOSA_WALK(KS, NW) launch_ex(prefill_walk_kernel<KS, NW>, wgrid, wblock, wsm, st, true, 0, s, qs, hist, n, nbn)
+  switch (ks) {
+    case 1: e = nw1 ? NOSA_WALK(1, 1) : NOSA_WALK(1, 2); break;
+    case 2: e = nw1 ? NOSA_WALK(2, 1) : NOSA_WALK(2, 2); break;
+    case 3: e = nw1 ? NOSA_WALK(3, 1) : NOSA_WALK(3, 2); break;
+    case 4: e = nw1 ? NOSA_WALK(4, 1) : NOSA_WALK(4, 2); break;
+    default: e = nw1 ? NOSA_WALK(kWalkMaxSlots, 1) : NOSA_WALK(kWalkMaxSlots, 2); break;
   }
+#undef NOSA_WALK
   if (e != cudaSuccess) return e;
   e = launch_ex(prefill_refresh_kernel, dim3(s.cap, s.U), dim3(256), 0, st, true, 0, s, k, v, n);
   if (e != cudaSuccess) return e;

@@ -23,6 +23,7 @@ NOSA_F_TEST_BAD_SLOT = 2
 NOSA_F_UNFUSED_STEP = 4
 NOSA_F_DMA_BIAS = 8
 NOSA_F_TEST_RADIX_TOPK = 16
+NOSA_F_TEST_PREFILL_WIDE = 32
 NOSA_MERGE_AUTO, NOSA_MERGE_KERNEL, NOSA_MERGE_TICKET, NOSA_MERGE_CLUSTER = 0, 1, 2, 3
 
 # every entry point declared in include/nosa.h
@@ -46,7 +47,7 @@ class nosa_config(ctypes.Structure):
                 ("score_ctas", ctypes.c_int32), ("attend_blocks_per_cta", ctypes.c_int32),
                 ("attend_merge", ctypes.c_int32), ("decode_cluster", ctypes.c_int32),
                 ("decode_teams", ctypes.c_int32), ("decode_stages", ctypes.c_int32),
-                ("forecast_streams", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32)]
+                ("forecast_streams", ctypes.c_int32)]
 
 
 class nosa_sizes(ctypes.Structure):
@@ -155,11 +156,11 @@ def make_config(*, num_layers, batch, num_q_heads, num_kv_heads, k_q, k_e, windo
                 head_dim=128, block_size=64, cmp_kernel=32, cmp_stride=16, sink_blocks=1, evict_hidden=128,
                 gather_ctas=0, softmax_scale=0.0, flags=0, score_ctas=0, attend_blocks_per_cta=0,
                 attend_merge=0, decode_cluster=0, decode_teams=0, decode_stages=0,
-                forecast_streams=0, prefill_ctas=0) -> nosa_config:
+                forecast_streams=0) -> nosa_config:
     return nosa_config(ctypes.sizeof(nosa_config), num_layers, batch, num_q_heads, num_kv_heads, head_dim,
                        block_size, cmp_kernel, cmp_stride, k_q, k_e, sink_blocks, window_tokens, max_context,
                        evict_hidden, gather_ctas, softmax_scale, flags, score_ctas, attend_blocks_per_cta,
-                       attend_merge, decode_cluster, decode_teams, decode_stages, forecast_streams, prefill_ctas)
+                       attend_merge, decode_cluster, decode_teams, decode_stages, forecast_streams)
 
 
 # ------------------------------------------------------------------ entry points

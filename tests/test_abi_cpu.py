@@ -45,11 +45,11 @@ def test_validate_config():
     assert N.nosa_validate_config(_cfg()) == N.NOSA_OK
     bad = [dict(head_dim=64), dict(block_size=32), dict(cmp_kernel=16), dict(cmp_stride=8),
            dict(num_q_heads=15), dict(num_q_heads=32, num_kv_heads=2), dict(k_q=-1), dict(window_tokens=100),
-           dict(max_context=0), dict(max_context=1 << 20), dict(evict_hidden=100), dict(flags=32),
+           dict(max_context=0), dict(max_context=1 << 20), dict(evict_hidden=100), dict(flags=64),
            dict(k_q=200, k_e=100), dict(batch=4097, num_kv_heads=1, num_q_heads=8), dict(softmax_scale=-1.0),
            dict(score_ctas=9), dict(score_ctas=-1), dict(attend_blocks_per_cta=65), dict(attend_merge=4),
            dict(decode_cluster=9), dict(decode_teams=3), dict(decode_stages=1), dict(decode_stages=7),
-           dict(forecast_streams=3), dict(prefill_ctas=9)]
+           dict(forecast_streams=3)]
     for b in bad:
         assert N.nosa_validate_config(_cfg(**b)) == N.NOSA_ERR_INVALID_ARG, b
     c = _cfg()
@@ -60,8 +60,7 @@ def test_validate_config():
 def test_sizing_overrides_are_accepted():
     good = [dict(score_ctas=1), dict(score_ctas=8), dict(attend_blocks_per_cta=1), dict(attend_blocks_per_cta=64),
             dict(attend_merge=N.NOSA_MERGE_TICKET), dict(attend_merge=N.NOSA_MERGE_CLUSTER),
-            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1),
-            dict(prefill_ctas=1), dict(prefill_ctas=8)]
+            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1)]
     for g in good:
         assert N.nosa_validate_config(_cfg(**g)) == N.NOSA_OK, g
 
@@ -71,6 +70,7 @@ def test_test_hook_flags_are_accepted():
     assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_TEST_BAD_SLOT | N.NOSA_F_TEST_ZERO_WAIT)) == N.NOSA_OK
     assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_UNFUSED_STEP)) == N.NOSA_OK
     assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_DMA_BIAS | N.NOSA_F_UNFUSED_STEP)) == N.NOSA_OK
+    assert N.nosa_validate_config(_cfg(flags=N.NOSA_F_TEST_RADIX_TOPK | N.NOSA_F_TEST_PREFILL_WIDE)) == N.NOSA_OK
 
 
 def test_query_sizes_closed_forms():

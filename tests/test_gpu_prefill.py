@@ -59,14 +59,19 @@ def _select_and_adopt(o, sq, se, T, Q_gpu, E_gpu, k_q, k_e, ties, where):
     return Q, E
 
 
-def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, prefill_ctas=0):
-    """Prefill n tokens into an empty layer, check against the oracle, then decode_steps steps."""
+def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, score_positions=None):
+    """Prefill n tokens into an empty layer, check against the oracle, then decode_steps steps.
+
+    score_positions (long prompts): the positions where the oracle forms its own query-aware
+    scores; elsewhere it takes the GPU's query-aware picks and ranks the query-agnostic part by
+    the whole prompt's pooled eviction scores (a candidate block lies before the window, so its
+    windows are complete at every position where it is a candidate)."""
     B, Hq, Hkv, d, G = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.group
     U = B * Hkv
     assert n + decode_steps <= wl.steps and wl.context == 0
     cfg = N.make_config(num_layers=1, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=n + decode_steps, sink_blocks=wl.sink_blocks,
-                        evict_hidden=wl.evict_hidden, flags=flags, prefill_ctas=prefill_ctas)
+                        evict_hidden=wl.evict_hidden, flags=flags)
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     ties, max_err = [], 0.0
@@ -87,12 +92,13 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, pref
         qd, kd, vd = _dev(q), _dev(k), _dev(v)
         out = torch.full((B, Hq, n, d), float("nan"), dtype=torch.bfloat16, device="cuda")
         nbytes = N.nosa_prefill_scratch_bytes(ctx, n)
-        assert nbytes == U * n * cap * 2
+        capp = (cap + 7) // 8 * 8  # selection rows padded to 16 bytes
+        assert nbytes == U * n * capp * 2 + U * n * ((-(-n // 64) + 31) // 32) * 4  # selections, then the picks
         scratch = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda")
         N.nosa_prefill(ctx, 0, qd, kd, vd, n, out.view(torch.int16), scratch, nbytes)
         assert N.nosa_sync(ctx) == N.NOSA_OK
         assert N.nosa_context_length(ctx, 0) == n
-        hist = scratch.cpu().numpy().reshape(U, n, cap)
+        hist = scratch[:U * n * capp].cpu().numpy().reshape(U, n, capp)
         out_h = out.float().cpu().numpy()
         st = dict(sel=np.zeros((U, cap), np.int32), n_sel=np.zeros(U, np.int32), fetch=np.zeros((U, cap, 2), np.int32),
                   n_fetch=np.zeros(U, np.int32), slot_blk=np.zeros((U, cap), np.int32),
@@ -109,15 +115,34 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, pref
             o = O.UnitOracle(head_dim=d, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
                              window_tokens=wl.window_tokens, max_context=n + decode_steps, W1=x["W1"], W2=x["W2"],
                              dma_bias=bool(flags & N.NOSA_F_DMA_BIAS))
+            se_full = None
+            if score_positions is not None:
+                assert wl.window_tokens >= 2 * 64
+                of = O.UnitOracle(head_dim=d, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
+                                  window_tokens=wl.window_tokens, max_context=n, W1=x["W1"], W2=x["W2"])
+                of.append(x["K"][:n], x["V"][:n])
+                se_full = of.scores(x["Q"][n - 1])[1]
             r = None
             for t in range(n):
                 o.append(x["K"][t:t + 1], x["V"][t:t + 1])
-                sq, se = o.scores(x["Q"][t])
                 row = [int(h) for h in hist[u, t] if h >= 0]
                 blocks, kinds = [h & 0xFFF for h in row], [h >> 12 for h in row]
                 Qg = sorted(bb for bb, kk in zip(blocks, kinds) if kk == 2)
                 Eg = sorted(bb for bb, kk in zip(blocks, kinds) if kk == 3)
-                Q, E = _select_and_adopt(o, sq, se, o.T, Qg, Eg, wl.k_q, wl.k_e, ties, (u, t))
+                if score_positions is None or t in score_positions:
+                    sq, se = o.scores(x["Q"][t])
+                    Q, E = _select_and_adopt(o, sq, se, o.T, Qg, Eg, wl.k_q, wl.k_e, ties, (u, t))
+                else:
+                    _, C, _ = O.partition(o.T, o.nw, o.sink, o.block)
+                    Q = Qg
+                    assert len(Q) == min(wl.k_q, len(C)) and set(Q) <= set(C), f"query-aware picks {(u, t)}"
+                    E = O.select_query_agnostic(se_full, C, Q, o.evicted, wl.k_e)
+                    if E != Eg:
+                        pool = [bb for bb in C if bb not in set(Q) and bb not in o.evicted]
+                        assert _near_tie_ok(np.asarray(se_full).astype(np.float32), Eg, E, pool, wl.k_e), \
+                            f"query-agnostic pick {(u, t)}"
+                        ties.append(("e", (u, t)))
+                        E = Eg
                 r = o.commit(Q, E)
                 assert blocks == r["S"], f"selection of position {t} unit {u}: {blocks} vs {r['S']}"
                 if t in out_positions:
@@ -169,37 +194,73 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, pref
     return ties
 
 
-# prefill_ctas 0 takes the rule (few units here: a cluster of 4 CTAs per unit walks the positions),
-# 1 the one-CTA walk that scores four positions per pass, 3 a cluster of 3
-@pytest.mark.parametrize("ctas", [0, 1, 3], ids=["cluster-rule", "one-cta", "cluster-3"])
+# NOSA_F_TEST_PREFILL_WIDE: the kernel forms prompts of more than 65,536 tokens take (two positions
+# per query-aware warp, two bitmap words per walk lane), here on short prompts
+TILE = pytest.mark.parametrize("tile", [0, N.NOSA_F_TEST_PREFILL_WIDE], ids=["short-form", "wide-form"])
+
+
+@TILE
 @pytest.mark.parametrize("mode", [FUSED, UNFUSED], ids=["fused-decode", "three-kernel-decode"])
-def test_prefill_640_every_position(mode, ctas):
+def test_prefill_640_every_position(mode, tile):
     # k = 3 with a 2-block window: the selection turns sparse once the prompt passes 6 blocks, so
     # evictions and the window sliding over the budget all happen inside the prompt
     wl = syn.Workload("pf640", layers=1, batch=2, q_heads=16, kv_heads=2, context=0, k_q=1, k_e=2,
                       window_tokens=128, steps=644, sigma=0.3)
     units = [(b, g) for b in range(2) for g in range(2)]
-    run_prefill(wl, 640, units, set(range(640)), flags=mode, decode_steps=4, prefill_ctas=ctas)
+    run_prefill(wl, 640, units, set(range(640)), flags=mode | tile, decode_steps=4)
 
 
-@pytest.mark.parametrize("ctas", [0, 1], ids=["cluster-rule", "one-cta"])
-def test_prefill_ragged_group4_dma_bias(ctas):
-    # a prompt that ends mid-block and mid-window, 8 q heads over 2 kv heads, with the attention bias
+@TILE
+def test_prefill_ragged_group4_dma_bias(tile):
+    # a prompt that ends mid-block and mid-window, 4 q heads per kv head, 6 units (two walk CTAs),
+    # with the attention bias
     wl = syn.Workload("pf_ragged", layers=1, batch=3, q_heads=8, kv_heads=2, context=0, k_q=3, k_e=5,
                       window_tokens=128, steps=1004, sigma=1.0)
     units = [(b, g) for b in range(3) for g in range(2)]
-    run_prefill(wl, 1001, units, set(range(1001)), flags=N.NOSA_F_DMA_BIAS, decode_steps=3, prefill_ctas=ctas)
+    run_prefill(wl, 1001, units, set(range(1001)), flags=N.NOSA_F_DMA_BIAS | tile, decode_steps=3)
 
 
-@pytest.mark.parametrize("ctas", [0, 1], ids=["cluster-rule", "one-cta"])
-def test_prefill_16k_prompt_sampled_positions(ctas):
+@pytest.mark.parametrize("window", [0, 64], ids=["no-window", "one-block-window"])
+def test_prefill_short_window(window):
+    # with a window of fewer than two blocks the last two blocks are candidates, whose pooled
+    # eviction scores still change as the prompt grows: the walk re-ranks them at every position
+    wl = syn.Workload(f"pf_w{window}", layers=1, batch=1, q_heads=16, kv_heads=2, context=0, k_q=2, k_e=3,
+                      window_tokens=window, steps=803, sigma=1.0)
+    units = [(0, 0), (0, 1)]
+    run_prefill(wl, 800, units, set(range(0, 800, 7)) | {799}, decode_steps=3)
+
+
+@pytest.mark.parametrize("kq,ke", [(40, 8), (0, 6), (5, 0)], ids=["kq40", "kq0", "ke0"])
+def test_prefill_pick_counts(kq, ke):
+    # more query-aware picks than a warp ranks in one round (40: two rounds), and either part empty
+    n = 3500 if kq == 40 else 900
+    wl = syn.Workload(f"pf_k{kq}_{ke}", layers=1, batch=1, q_heads=16, kv_heads=2, context=0, k_q=kq, k_e=ke,
+                      window_tokens=128, steps=n + 3, sigma=1.0)
+    units = [(0, 0), (0, 1)]
+    run_prefill(wl, n, units, set(range(0, n, 13)) | {n - 1}, decode_steps=3)
+
+
+def test_prefill_16k_prompt_sampled_positions():
     # the 1B-shaped layer (16/2 heads, k_q 16, k_e 48, 1024-token window) over a 16K prompt: one
     # unit's selection checked at every position, its outputs at sampled positions
     n = 16384
     wl = syn.Workload("pf16k", layers=1, batch=1, q_heads=16, kv_heads=2, context=0, k_q=16, k_e=48,
                       window_tokens=1024, steps=n + 2, sigma=0.3)
     pos = set(range(0, n, 61)) | set(range(n - 8, n)) | {63, 64, 65, 1023, 1024, 1025}
-    run_prefill(wl, n, [(0, 1)], pos, decode_steps=2, prefill_ctas=ctas)
+    run_prefill(wl, n, [(0, 1)], pos, decode_steps=2)
+
+
+def test_prefill_70k_prompt_long_forms():
+    # 70,000 tokens (1,094 blocks): the long-prompt kernel forms for real, block ids past 1,024 in
+    # the bitmaps' second words.  Every position's query-agnostic picks, eviction state, selection
+    # and slots against the oracle; the query-aware picks against the oracle's own scores at
+    # sampled positions (elsewhere checked for count and range, then adopted)
+    n = 70000
+    wl = syn.Workload("pf70k", layers=1, batch=1, q_heads=16, kv_heads=2, context=0, k_q=16, k_e=48,
+                      window_tokens=1024, steps=n + 2, sigma=0.3)
+    scored = set(range(0, n, 4999)) | {65535, 65536, 65600, n - 1}
+    out = set(range(0, n, 997)) | {n - 1}
+    run_prefill(wl, n, [(0, 0)], out, decode_steps=2, score_positions=scored)
 
 
 def test_prefill_argument_checks():
