@@ -355,11 +355,11 @@ size_t nosa_dense_scratch_bytes(int units, int context_len);
  *   q, out   device bf16 [B][Hq][n_tokens][d] (out[b][h][t] is position t's attention output)
  *   k, v     device bf16 [B][Hkv][n_tokens][d]; q, k and v 16-byte aligned
  *   scratch  device memory of at least nosa_prefill_scratch_bytes(ctx, n_tokens) bytes, 16-byte
- *            aligned.  Afterwards it begins with every position's selection: int16 [B][Hkv]
- *            [n_tokens][R] with R = cache_slots rounded up to a multiple of 8, ascending, -1
- *            padded; entry bits 0-11 are the block, bits 12-13 its kind (0 sink, 1 window,
- *            2 query-aware, 3 query-agnostic).  The rest is working space (each position's
- *            query-aware picks as bitmap words over the prompt's blocks).
+ *            aligned.  Afterwards it holds every position's selection as two bitmaps over the
+ *            prompt's blocks: uint32 [2][B][Hkv][n_tokens][W], W = ceil(ceil(n_tokens / 64) / 32),
+ *            block b at bit b % 32 of word b / 32; [0] the query-aware picks, [1] the
+ *            query-agnostic ones.  Position t's selection is those blocks plus the sink blocks
+ *            and the window blocks of a context of t + 1 tokens.
  * NOSA_ERR_INVALID_ARG on a misaligned pointer; NOSA_ERR_STATE if the layer is not empty;
  * NOSA_ERR_CAPACITY if n_tokens exceeds max_context or 131,072 (the longest prompt the kernels'
  * block bitmaps cover), or if the scratch is too small. */

@@ -768,16 +768,15 @@ nosa_status nosa_step_host_all(nosa_ctx* c, const uint16_t* q, const uint16_t* k
   return NOSA_OK;
 }
 
-// [U][n][cap rounded up to 8] int16 selection rows, then [U][n][ceil(nb / 32)] bitmap words of
-// the query-aware picks (nb: the prompt's blocks)
-static size_t prefill_hist_bytes(const nosa_ctx* c, int n_tokens) {
-  return (size_t)c->U * (size_t)n_tokens * (size_t)((c->cap + 7) & ~7) * sizeof(int16_t);
+// [2][U][n][ceil(nb / 32)] bitmap words over the prompt's nb blocks: each position's query-aware,
+// then query-agnostic picks
+static size_t prefill_pick_bytes(const nosa_ctx* c, int n_tokens) {
+  return (size_t)c->U * (size_t)n_tokens * (size_t)cdiv(cdiv(n_tokens, kBlock), 32) * sizeof(uint32_t);
 }
 
 size_t nosa_prefill_scratch_bytes(nosa_ctx* c, int n_tokens) {
   if (!c || n_tokens < 1) return 0;
-  const size_t words = (size_t)cdiv(cdiv(n_tokens, kBlock), 32);
-  return prefill_hist_bytes(c, n_tokens) + (size_t)c->U * (size_t)n_tokens * words * sizeof(uint32_t);
+  return 2 * prefill_pick_bytes(c, n_tokens);
 }
 
 nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -807,9 +806,9 @@ nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16
       return NOSA_ERR_INVALID_ARG;
   const LayerState s = layer_state(c, layer);
   CK(launch_append_bulk(s, k, v, 0, n_tokens, c->stream));
-  int16_t* hist = static_cast<int16_t*>(scratch);
-  uint32_t* qsel = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(scratch) + prefill_hist_bytes(c, n_tokens));
-  CK(launch_prefill(s, &tk, &tv, q, k, v, out, hist, qsel, n_tokens, (c->cfg.flags & NOSA_F_TEST_PREFILL_WIDE) != 0,
+  uint32_t* qsel = static_cast<uint32_t*>(scratch);
+  uint32_t* esel = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(scratch) + prefill_pick_bytes(c, n_tokens));
+  CK(launch_prefill(s, &tk, &tv, q, k, v, out, qsel, esel, n_tokens, (c->cfg.flags & NOSA_F_TEST_PREFILL_WIDE) != 0,
                     c->stream));
   c->T_host[layer] = n_tokens;
   c->sel_T[layer] = n_tokens;

@@ -88,12 +88,12 @@ int decode_active_clusters(const LayerState& s, int teams, int nst, int cs);
 cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const uint16_t* q, const uint16_t* k,
                           const uint16_t* v, uint16_t* out, int teams, int nst, bool pdl, cudaStream_t st);
 // sparse prefill of an empty layer (after the bulk append of the prompt): every position's
-// query-aware picks into qsel [U][n][ceil(nb / 32)] (bitmap words over the prompt's nb blocks),
-// the positions' selections in order into hist [U][n][cap rounded up to 8], cache slots refreshed
-// from the prompt, attention of every position
+// query-aware picks into qsel, then its query-agnostic picks in order into esel (both [U][n]
+// [ceil(nb / 32)] bitmap words over the prompt's nb blocks), cache slots refreshed from the
+// prompt, attention of every position
 cudaError_t init_prefill();
 int prefill_max_tokens();
 cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
-                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, uint32_t* qsel, int n,
+                           const uint16_t* k, const uint16_t* v, uint16_t* out, uint32_t* qsel, uint32_t* esel, int n,
                            bool wide, cudaStream_t st);  // wide: the long-prompt forms at any length
 }  // namespace nosa

@@ -37,11 +37,6 @@ using namespace selcore;
 constexpr int kPfPositions = 4;        // positions per attention CTA
 constexpr int kPfStages = 3;           // 32 KiB stages
 constexpr int kPfMaxWords = 2048 / 32;  // block bitmap words per position (prompts of up to 131,072 tokens)
-// a selection entry: block id in the low 12 bits, its kind (0 sink, 1 window, 2 query-aware,
-// 3 query-agnostic) above; -1 pads
-constexpr int kPfKindShift = 12;
-constexpr int kPfBlockMask = (1 << kPfKindShift) - 1;
-// selection rows are cache_slots entries rounded up to 8 (16 bytes), so a row is one vector store
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
@@ -253,8 +248,7 @@ constexpr int kWalkMaxSlots = 9;  // list entries per lane: k_q + k_e + 1 <= 288
 
 __host__ __device__ inline size_t walk_warp_bytes(int nbn) {
   const int nbw = (nbn + 31) / 32;
-  return (size_t)32 * kWalkMaxSlots * 8 + (size_t)kPfMaxWords * 16 + 4 * (size_t)nbw * 4 + 8 * 4 +
-         (size_t)((nbn + 7) & ~7) * 2 + 4 * 256 * 2;
+  return (size_t)32 * kWalkMaxSlots * 8 + 4 * (size_t)nbw * 4 + 8 * 4 + (size_t)((nbn + 7) & ~7) * 2 + 3 * 256 * 2;
 }
 
 __device__ __forceinline__ uint32_t range_bits(int w, int lo, int hi) {  // bits of [lo, hi) in word w
@@ -264,13 +258,26 @@ __device__ __forceinline__ uint32_t range_bits(int w, int lo, int hi) {  // bits
   return top & ~((1u << a) - 1u);
 }
 
-// grid ceil(U / 4), 128 threads; dynamic shared memory 4 x walk_warp_bytes(nbn).  hist: [U][n][capp]
-// selection entries (block | kind << 12, -1 padded; capp = cap rounded up to 8); qsel: the
-// query-aware picks of 2a as [U][n][nbw] bitmap words.
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// grid ceil(U / 4), 128 threads; dynamic shared memory 4 x walk_warp_bytes(nbn).  qsel: the
+// query-aware picks of 2a, esel: the query-agnostic picks this kernel makes, both [U][n][nbw]
+// bitmap words.  The list's blocks are also kept as a bitmap (lb): after a position's step the
+// list holds exactly the never-dropped blocks of D, so D = Q | lb and E = lb & ~Q without
+// touching the picks one by one.
 // KS: list entries per lane (k_q + k_e + 1 <= 32 KS); NW: bitmap words per lane (nbn <= 1024 NW).
 template <int KS, int NW>
 __global__ void __launch_bounds__(kWalkWarps * 32)
-    prefill_walk_kernel(LayerState s, const uint32_t* __restrict__ qsel, int16_t* __restrict__ hist, int n, int nbn) {
+    prefill_walk_kernel(LayerState s, const uint32_t* __restrict__ qsel, uint32_t* __restrict__ esel, int n,
+                        int nbn) {
   extern __shared__ __align__(16) unsigned char wsm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x * kWalkWarps + warp;
@@ -279,22 +286,19 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   const int nbw = (nbn + 31) / 32;
   unsigned char* base = wsm + (size_t)warp * walk_warp_bytes(nbn);
   unsigned long long* Lk = reinterpret_cast<unsigned long long*>(base);  // the eligible list, descending keys
-  uint4* wrec = reinterpret_cast<uint4*>(base + 32 * kWalkMaxSlots * 8);  // per word: D, new, left, Q
-  uint32_t* ev = reinterpret_cast<uint32_t*>(wrec + kPfMaxWords);
+  uint32_t* ev = reinterpret_cast<uint32_t*>(base + 32 * kWalkMaxSlots * 8);
   uint32_t* sprev = ev + nbw;  // the previous selection
   uint32_t* qbm = sprev + nbw;  // this position's query-aware picks
-  uint32_t* ebm = qbm + nbw;    // and query-agnostic ones
-  uint32_t* fbm = ebm + nbw;    // free cache slots (8 words)
+  uint32_t* lb = qbm + nbw;     // the list's blocks
+  uint32_t* fbm = lb + nbw;     // free cache slots (8 words)
   int16_t* slot_of = reinterpret_cast<int16_t*>(fbm + 8);
   int16_t* slot_blk = slot_of + ((nbn + 7) & ~7);
   int16_t* newl = slot_blk + 256;
   int16_t* freel = newl + 256;
-  int16_t* rowbuf = freel + 256;  // the position's row, stored to hist in one vector store
   const int ke = s.k_e, cap = s.cap, sink = s.sink;
-  const int capp = (cap + 7) & ~7;
   const unsigned int lt = (1u << lane) - 1u;
   // an empty layer: nothing dropped, selected or cached
-  for (int w = lane; w < nbw; w += 32) ev[w] = sprev[w] = qbm[w] = ebm[w] = 0u;
+  for (int w = lane; w < nbw; w += 32) ev[w] = sprev[w] = qbm[w] = lb[w] = 0u;
   if (lane < 8) fbm[lane] = range_bits(lane, 0, cap);
   for (int b = lane; b < nbn; b += 32) slot_of[b] = -1;
   for (int i = lane; i < 256; i += 32) slot_blk[i] = -1;
@@ -331,7 +335,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
       const int j = lane + 32 * i;
       if (j >= c && j < nL && j + 1 < 32 * KS) Lk[j + 1] = v[i];
     }
-    if (lane == 0 && c < 32 * KS) Lk[c] = key;
+    if (lane == 0 && c < 32 * KS) {
+      Lk[c] = key;
+      const int b = (int)(0xFFFFFFFFu - (uint32_t)key);
+      lb[b >> 5] |= 1u << (b & 31);
+    }
     __syncwarp();
     nL = min(nL + 1, 32 * KS);
   };
@@ -346,9 +354,9 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     for (int i = 0; i < KS; ++i) {
       const bool in = lane + 32 * i < nL;
       const bool late = in && (int)(0xFFFFFFFFu - (uint32_t)v[i]) >= bmin;
-      const unsigned int kb = __ballot_sync(0xffffffffu, in && !late), lb = __ballot_sync(0xffffffffu, late);
+      const unsigned int kb = __ballot_sync(0xffffffffu, in && !late), lb_ = __ballot_sync(0xffffffffu, late);
       if (in && !late) Lk[wpos + __popc(kb & lt)] = v[i];
-      for (unsigned int m = lb; m; m &= m - 1u) {
+      for (unsigned int m = lb_; m; m &= m - 1u) {
         const unsigned long long x = __shfl_sync(0xffffffffu, v[i], __ffs(m) - 1);
         if (nout == 0) o0 = x;
         else if (nout == 1) o1 = x;
@@ -373,8 +381,10 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   uint32_t st_gmin = 0x7F800000u;  // +inf
   int ws_prev = sink;               // candidates so far: [sink, ws_prev)
   int nS_prev = 0, nS = 0, nD = 0, nDnew = 0, nNew = 0;
+  uint32_t Sw[NW];
+  Geometry geo = geometry(1, s.nw, s.sink);
   for (int t = 0; t < n; ++t) {
-    const Geometry geo = geometry(t + 1, s.nw, s.sink);
+    geo = geometry(t + 1, s.nw, s.sink);
     const int nbwT = (geo.nb + 31) >> 5;
     uint32_t qc[NW];
 #pragma unroll
@@ -395,9 +405,11 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     ws_prev = max(ws_prev, geo.ws);
     __syncwarp();  // query-aware words visible to every lane
     // E: the list's first k_e entries outside Q; the other entries outside Q are dropped for good
-    int nElig = 0, wpos = 0;
+    // (out of the list, its bitmap and the eligible set)
+    int nElig = 0;
     unsigned long long v[KS];
-    bool keep[KS];
+    bool drop[KS];
+    unsigned int anyd = 0u;
 #pragma unroll
     for (int i = 0; i < KS; ++i) {
       const bool in = lane + 32 * i < nL;
@@ -406,80 +418,80 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
       const bool inQ = in && ((qbm[b >> 5] >> (b & 31)) & 1u);
       const bool elig = in && !inQ;
       const unsigned int eb = __ballot_sync(0xffffffffu, elig);
-      const bool inE = elig && nElig + __popc(eb & lt) < ke;
+      drop[i] = elig && nElig + __popc(eb & lt) >= ke;
       nElig += __popc(eb);
-      if (inE) atomicOr(&ebm[b >> 5], 1u << (b & 31));
-      if (elig && !inE) atomicOr(&ev[b >> 5], 1u << (b & 31));
-      keep[i] = inQ || inE;
+      if (drop[i]) {
+        atomicOr(&ev[b >> 5], 1u << (b & 31));
+        atomicAnd(&lb[b >> 5], ~(1u << (b & 31)));
+      }
+      anyd |= __ballot_sync(0xffffffffu, drop[i]);
     }
     const int nE = min(ke, nElig);
-    __syncwarp();
+    if (anyd) {  // the list keeps D's never-dropped blocks, in order
+      __syncwarp();
+      int wpos = 0;
 #pragma unroll
-    for (int i = 0; i < KS; ++i) {  // the list keeps D's never-dropped blocks, in order
-      const unsigned int kb = __ballot_sync(0xffffffffu, keep[i]);
-      if (keep[i]) Lk[wpos + __popc(kb & lt)] = v[i];
-      wpos += __popc(kb);
+      for (int i = 0; i < KS; ++i) {
+        const bool keep = lane + 32 * i < nL && !drop[i];
+        const unsigned int kb = __ballot_sync(0xffffffffu, keep);
+        if (keep) Lk[wpos + __popc(kb & lt)] = v[i];
+        wpos += __popc(kb);
+      }
+      nL = wpos;
     }
-    nL = wpos;
-    // S = sink + D + window per word; the blocks new to it and the blocks that left it
-    uint32_t Sw[NW];
+    __syncwarp();
+    // S = sink + D + window per word, D = Q | the list's blocks; the blocks new to S and the
+    // blocks that left it; this position's query-agnostic words to the caller
+    uint32_t Nw[NW], Fw[NW];
     int cnt = 0;  // popc(D) | popc(new) << 10 | popc(D & new) << 20 (each at most 256)
+    uint32_t* erow = esel + ((size_t)u * n + t) * nbw;
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
       const int w = lane + 32 * k;
-      Sw[k] = 0u;
+      Sw[k] = Nw[k] = Fw[k] = 0u;
+      if (w >= nbw) continue;
+      const uint32_t L = lb[w];
+      erow[w] = L & ~qc[k];
       if (w >= nbwT) continue;
-      const uint32_t D = qc[k] | ebm[w];
+      const uint32_t D = qc[k] | L;
       const uint32_t sw = D | range_bits(w, 0, geo.ns) | range_bits(w, geo.ws, geo.nb);
       const uint32_t pv = sprev[w];
       Sw[k] = sw;
-      wrec[w] = make_uint4(D, sw & ~pv, pv & ~sw, qc[k]);
-      cnt += __popc(D) | (__popc(sw & ~pv) << 10) | (__popc(D & sw & ~pv) << 20);
+      Nw[k] = sw & ~pv;
+      Fw[k] = pv & ~sw;
+      cnt += __popc(D) | (__popc(Nw[k]) << 10) | (__popc(D & Nw[k]) << 20);
     }
     cnt = warp_sum(cnt);
     nD = cnt & 1023;
     const int nNewAll = (cnt >> 10) & 1023;
     nDnew = (cnt >> 20) & 1023;
     nS = geo.ns + nD + (geo.nb - geo.ws);
-    __syncwarp();
-    // one pass over the words, a lane per bit: D's row entries (ascending), the new blocks in
-    // order, and the slots of the blocks that left become free
-    {
-      int dpos = geo.ns, npos = 0;
-      const uint32_t bit = 1u << lane;
-      for (int w = 0; w < nbwT; ++w) {
-        const uint4 r = wrec[w];
-        if ((r.x | r.y | r.z) == 0u) continue;
-        const int b = 32 * w + lane;
-        if (r.x & bit) {
-          const int pos = dpos + __popc(r.x & lt);
-          if (pos < capp) rowbuf[pos] = (int16_t)(b | (((r.w & bit) ? 2 : 3) << kPfKindShift));
-        }
-        if (r.y & bit) {
-          const int i = npos + __popc(r.y & lt);
-          if (i < 256) newl[i] = (int16_t)b;
-        }
-        if (r.z & bit) {
-          const int sl = slot_of[b];
-          slot_of[b] = -1;
-          if (sl >= 0) {
-            slot_blk[sl] = -1;
-            atomicOr(&fbm[sl >> 5], 1u << (sl & 31));
-          }
-        }
-        dpos += __popc(r.x);
-        npos += __popc(r.y);
+    if (nS > cap && lane == 0) atomicOr(s.err, kErrBounds);  // cannot happen when cap = sink + window + k_q + k_e
+    // the new blocks in ascending order; the slots of the blocks that left become free
+    if (nNewAll) {
+      int carry = 0;
+#pragma unroll
+      for (int k = 0; k < NW; ++k) {
+        const int c = __popc(Nw[k]);
+        const int incl = warp_incl_scan(c);
+        int pos = carry + incl - c;
+        for (uint32_t m = Nw[k]; m; m &= m - 1u, ++pos)
+          if (pos < 256) newl[pos] = (int16_t)(32 * (lane + 32 * k) + __ffs(m) - 1);
+        carry += __shfl_sync(0xffffffffu, incl, 31);
       }
     }
-    // the row's sink and window ranges and padding (kinds 0 and 1), then one vector store per lane
-    if (nS > cap && lane == 0) atomicOr(s.err, kErrBounds);  // cannot happen when cap = sink + window + k_q + k_e
-    for (int i = lane; i < geo.ns; i += 32) rowbuf[i] = (int16_t)i;
-    for (int i = lane; i < geo.nb - geo.ws; i += 32)
-      if (geo.ns + nD + i < capp) rowbuf[geo.ns + nD + i] = (int16_t)((geo.ws + i) | (1 << kPfKindShift));
-    for (int i = min(nS, capp) + lane; i < capp; i += 32) rowbuf[i] = -1;
+#pragma unroll
+    for (int k = 0; k < NW; ++k)
+      for (uint32_t m = Fw[k]; m; m &= m - 1u) {
+        const int b = 32 * (lane + 32 * k) + __ffs(m) - 1;
+        const int sl = slot_of[b];
+        slot_of[b] = -1;
+        if (sl >= 0) {
+          slot_blk[sl] = -1;
+          atomicOr(&fbm[sl >> 5], 1u << (sl & 31));
+        }
+      }
     __syncwarp();
-    if (lane < capp / 8)
-      reinterpret_cast<uint4*>(hist + ((size_t)u * n + t) * capp)[lane] = reinterpret_cast<const uint4*>(rowbuf)[lane];
     // the i-th new block (ascending) takes the i-th free slot (ascending)
     nNew = min(nNewAll, 256);
     {
@@ -514,40 +526,45 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
       st_gmin = min(st_gmin, __float_as_uint((float)(nD - nDnew) / (float)nD));
     }
     nS_prev = nS;
-    // this selection is the next position's previous one; the E bitmap starts empty (the last
-    // position's previous selection and picks stay, for the state below)
+    // this selection is the next position's previous one (the last position's previous one
+    // stays, for the fetched marks below)
     if (t + 1 < n) {
 #pragma unroll
-      for (int k = 0; k < NW; ++k) {
-        const int w = lane + 32 * k;
-        if (w < nbwT) {
-          sprev[w] = Sw[k];
-          ebm[w] = 0u;
-        }
-      }
+      for (int k = 0; k < NW; ++k)
+        if (lane + 32 * k < nbwT) sprev[lane + 32 * k] = Sw[k];
     }
     __syncwarp();
   }
-  // the unit's state after the prompt: the last selection (the row still in shared memory) with
-  // kinds, slots and fetched marks, its fetch list, the eviction bitmap and the slot tables
+  // the unit's state after the prompt: the last selection with kinds, slots and fetched marks,
+  // its fetch list, the eviction bitmap and the slot tables
   int32_t* sel = s.sel + (size_t)u * cap;
   int32_t* kind = s.sel_kind + (size_t)u * cap;
   int32_t* sslot = s.sel_slot + (size_t)u * cap;
   int32_t* snew = s.sel_new + (size_t)u * cap;
   const int nSw = min(nS, cap);
-  for (int i = lane; i < cap; i += 32) {
-    if (i < nSw) {
-      const int e = rowbuf[i], b = e & kPfBlockMask;
-      sel[i] = b;
-      kind[i] = e >> kPfKindShift;
-      sslot[i] = slot_of[b];
-      snew[i] = ((sprev[b >> 5] >> (b & 31)) & 1u) ? 0 : 1;  // sprev holds the position before the last
-    } else {
-      sel[i] = -1;
-      kind[i] = -1;
-      sslot[i] = -1;
-      snew[i] = 0;
+  {
+    int pos = 0;
+    const int nbwT = (geo.nb + 31) >> 5;
+    for (int w = 0; w < nbwT; ++w) {
+      const uint32_t mine = (NW > 1 && (w >> 5) == 1) ? Sw[NW - 1] : Sw[0];
+      const uint32_t sw = __shfl_sync(0xffffffffu, mine, w & 31);
+      if ((sw >> lane) & 1u) {
+        const int p = pos + __popc(sw & lt), b = 32 * w + lane;
+        if (p < nSw) {
+          sel[p] = b;
+          kind[p] = b < geo.ns ? 0 : b >= geo.ws ? 1 : ((qbm[w] >> lane) & 1u) ? 2 : 3;
+          sslot[p] = slot_of[b];
+          snew[p] = ((sprev[w] >> lane) & 1u) ? 0 : 1;  // sprev holds the position before the last
+        }
+      }
+      pos += __popc(sw);
     }
+  }
+  for (int i = nSw + lane; i < cap; i += 32) {
+    sel[i] = -1;
+    kind[i] = -1;
+    sslot[i] = -1;
+    snew[i] = 0;
   }
   int32_t* fl = s.fetch + (size_t)u * cap * 2;
   for (int j = lane; j < nNew; j += 32) {
@@ -596,12 +613,14 @@ __global__ void __launch_bounds__(256) prefill_refresh_kernel(LayerState s, cons
 }
 
 // ---------------------------------------------------------------- 4. attention of every position
-// grid (U, ceil(n / P)), 128 threads (four warps, 16 tokens of every block each).
+// grid (U, ceil(n / P)), 128 threads (four warps, 16 tokens of every block each).  A position's
+// selection: its query-aware and query-agnostic bitmap words (qsel, esel: [U][n][ceil(nbn / 32)])
+// plus its sink and window blocks.
 template <int P>
 __global__ void __launch_bounds__(kTeamThreads, 1)
     prefill_attend_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                           LayerState s, const uint16_t* __restrict__ q, uint16_t* __restrict__ out,
-                          const int16_t* __restrict__ hist, int n) {
+                          const uint32_t* __restrict__ qsel, const uint32_t* __restrict__ esel, int n) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bars[kPfStages];
   __shared__ uint32_t bm[P][kPfMaxWords];
@@ -629,11 +648,12 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
   pdl_wait();  // the selections, the prompt's K/V and (with the bias) the eviction scores
   for (int i = tid; i < P * kPfMaxWords; i += blockDim.x) bm[i / kPfMaxWords][i % kPfMaxWords] = 0u;
   __syncthreads();
-  for (int idx = tid; idx < np * cap; idx += blockDim.x) {
-    const int p = idx / cap, e = idx % cap;
-    const int h = hist[((size_t)u * n + t0 + p) * ((cap + 7) & ~7) + e];
-    const int b = h & kPfBlockMask;
-    if (h >= 0 && b < nb_last) atomicOr(&bm[p][b >> 5], 1u << (b & 31));
+  const int nbws = ((n + kBlock - 1) / kBlock + 31) / 32;  // words per position in qsel and esel
+  for (int idx = tid; idx < np * nbw; idx += blockDim.x) {
+    const int p = idx / nbw, w = idx % nbw;
+    const Geometry g = geometry(t0 + p + 1, s.nw, s.sink);
+    const size_t o = ((size_t)u * n + t0 + p) * nbws + w;
+    bm[p][w] = qsel[o] | esel[o] | range_bits(w, 0, g.ns) | range_bits(w, g.ws, g.nb);
   }
   __syncthreads();
   if (warp == 0) {  // the union of the positions' selections, ascending, with a position mask each
@@ -822,7 +842,7 @@ cudaError_t init_prefill() {
 }
 
 cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
-                           const uint16_t* k, const uint16_t* v, uint16_t* out, int16_t* hist, uint32_t* qsel, int n,
+                           const uint16_t* k, const uint16_t* v, uint16_t* out, uint32_t* qsel, uint32_t* esel, int n,
                            bool wide, cudaStream_t st) {
   const int nbn = (n + kBlock - 1) / kBlock;
   wide = wide || prefill_wide(nbn);
@@ -841,7 +861,7 @@ cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUt
   const dim3 wgrid((s.U + kWalkWarps - 1) / kWalkWarps), wblock(kWalkWarps * 32);
   const size_t wsm = walk_smem(nbn);
   const uint32_t* qs = qsel;
-#define NOSA_WALK(KS, NW) launch_ex(prefill_walk_kernel<KS, NW>, wgrid, wblock, wsm, st, true, 0, s, qs, hist, n, nbn)
+#define NOSA_WALK(KS, NW) launch_ex(prefill_walk_kernel<KS, NW>, wgrid, wblock, wsm, st, true, 0, s, qs, esel, n, nbn)
   switch (ks) {
     case 1: e = nw1 ? NOSA_WALK(1, 1) : NOSA_WALK(1, 2); break;
     case 2: e = nw1 ? NOSA_WALK(2, 1) : NOSA_WALK(2, 2); break;
@@ -855,7 +875,7 @@ cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUt
   if (e != cudaSuccess) return e;
   return launch_ex(prefill_attend_kernel<kPfPositions>, dim3(s.U, (n + kPfPositions - 1) / kPfPositions),
                    dim3(kTeamThreads), prefill_attend_smem(), st, true, 0, *tk, *tv, s, q, out,
-                   static_cast<const int16_t*>(hist), n);
+                   qs, static_cast<const uint32_t*>(esel), n);
 }
 
 }  // namespace nosa

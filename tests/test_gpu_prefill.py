@@ -4,7 +4,8 @@ The oracle runs its decode step over the prompt, one position at a time from an
 empty context (the reading of sparse prefill taken here: position t gets the
 selection the decode step at T = t + 1 makes, the eviction state carried from
 t - 1).  The GPU selects every position in order and attends all positions in
-one launch.  Compared: every checked position's selection (blocks and kinds)
+one launch.  Compared: every checked position's selection (its query-aware and
+query-agnostic picks, returned as bitmaps, with the sink and window blocks)
 bit-exact, near ties logged and adopted as in the decode tests; outputs within
 max-abs 2e-2 / mean-abs 2e-3 and the tighter relative bound; the layer's state
 after the prompt (compressed keys, eviction bitmap, slot map, last selection and
@@ -92,13 +93,14 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
         qd, kd, vd = _dev(q), _dev(k), _dev(v)
         out = torch.full((B, Hq, n, d), float("nan"), dtype=torch.bfloat16, device="cuda")
         nbytes = N.nosa_prefill_scratch_bytes(ctx, n)
-        capp = (cap + 7) // 8 * 8  # selection rows padded to 16 bytes
-        assert nbytes == U * n * capp * 2 + U * n * ((-(-n // 64) + 31) // 32) * 4  # selections, then the picks
+        W = (-(-n // 64) + 31) // 32  # bitmap words per position
+        assert nbytes == 2 * U * n * W * 4  # query-aware, then query-agnostic picks
         scratch = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda")
         N.nosa_prefill(ctx, 0, qd, kd, vd, n, out.view(torch.int16), scratch, nbytes)
         assert N.nosa_sync(ctx) == N.NOSA_OK
         assert N.nosa_context_length(ctx, 0) == n
-        hist = scratch[:U * n * capp].cpu().numpy().reshape(U, n, capp)
+        picks = scratch.view(torch.int32)[:2 * U * n * W].cpu().numpy().view(np.uint32).reshape(2, U, n, W)
+        picks = np.unpackbits(picks.view(np.uint8), axis=-1, bitorder="little").astype(bool)  # [2][U][n][32 W]
         out_h = out.float().cpu().numpy()
         st = dict(sel=np.zeros((U, cap), np.int32), n_sel=np.zeros(U, np.int32), fetch=np.zeros((U, cap, 2), np.int32),
                   n_fetch=np.zeros(U, np.int32), slot_blk=np.zeros((U, cap), np.int32),
@@ -125,10 +127,11 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
             r = None
             for t in range(n):
                 o.append(x["K"][t:t + 1], x["V"][t:t + 1])
-                row = [int(h) for h in hist[u, t] if h >= 0]
-                blocks, kinds = [h & 0xFFF for h in row], [h >> 12 for h in row]
-                Qg = sorted(bb for bb, kk in zip(blocks, kinds) if kk == 2)
-                Eg = sorted(bb for bb, kk in zip(blocks, kinds) if kk == 3)
+                Qg = np.flatnonzero(picks[0, u, t]).tolist()
+                Eg = np.flatnonzero(picks[1, u, t]).tolist()
+                sink_b, C_t, win_b = O.partition(o.T, o.nw, o.sink, o.block)
+                assert not set(Qg) & set(Eg) and set(Qg) | set(Eg) <= set(C_t), f"picks of position {t} unit {u}"
+                blocks = sorted(set(sink_b) | set(Qg) | set(Eg) | set(win_b))
                 if score_positions is None or t in score_positions:
                     sq, se = o.scores(x["Q"][t])
                     Q, E = _select_and_adopt(o, sq, se, o.T, Qg, Eg, wl.k_q, wl.k_e, ties, (u, t))
