@@ -742,33 +742,43 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
       break;
     }
     const uint32_t stg = sbase + st * kStageBytes;
+    // the positions whose selection holds this block and for which this warp's 16 tokens exist
+    // (the block's tail up to the position itself); warp-uniform
+    bool act[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) act[p] = ((mk >> p) & 1) && tok0 < min(t0 + p + 1 - kBlock * b, kBlock);
+    // S^T = K q^T for every active position, each K fragment loaded once for all of them
+    float acc[P][4];
+#pragma unroll
+    for (int p = 0; p < P; ++p) acc[p][0] = acc[p][1] = acc[p][2] = acc[p][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int dch = 2 * ks + ch_k;
+      uint32_t a[4];
+      ldsm_x4(a, swz(stg, dch >> 3, 0, tk_k, dch & 7));
+#pragma unroll
+      for (int p = 0; p < P; ++p)
+        if (act[p]) mma_16816(acc[p], a, qb[p][ks][0], qb[p][ks][1]);
+    }
+    uint32_t pb[P][2];
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-      if (!((mk >> p) & 1)) continue;
-      const int Tp = t0 + p + 1;  // tokens in position p's context
-      const int valid = min(Tp - kBlock * b, kBlock);
-      if (tok0 >= valid) continue;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      pb[p][0] = pb[p][1] = 0u;
+      if (!act[p]) continue;
+      const int valid = min(t0 + p + 1 - kBlock * b, kBlock);  // tokens of the block in position p's context
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int dch = 2 * ks + ch_k;
-        uint32_t a[4];
-        ldsm_x4(a, swz(stg, dch >> 3, 0, tk_k, dch & 7));
-        mma_16816(acc, a, qb[p][ks][0], qb[p][ks][1]);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[j] *= sl2;
+      for (int j = 0; j < 4; ++j) acc[p][j] *= sl2;
       if (dma) {
         const float b0 = sebuf[st][tok0 + gr] * 1.4426950408889634f;
         const float b1 = sebuf[st][tok0 + gr + 8] * 1.4426950408889634f;
-        acc[0] += b0;
-        acc[1] += b0;
-        acc[2] += b1;
-        acc[3] += b1;
+        acc[p][0] += b0;
+        acc[p][1] += b0;
+        acc[p][2] += b1;
+        acc[p][3] += b1;
       }
-      if (tok0 + gr >= valid) acc[0] = acc[1] = -INFINITY;
-      if (tok0 + gr + 8 >= valid) acc[2] = acc[3] = -INFINITY;
-      float mx0 = fmaxf(acc[0], acc[2]), mx1 = fmaxf(acc[1], acc[3]);
+      if (tok0 + gr >= valid) acc[p][0] = acc[p][1] = -INFINITY;
+      if (tok0 + gr + 8 >= valid) acc[p][2] = acc[p][3] = -INFINITY;
+      float mx0 = fmaxf(acc[p][0], acc[p][2]), mx1 = fmaxf(acc[p][1], acc[p][3]);
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
@@ -777,8 +787,8 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
       WarpAcc& a_ = A[p];
       const float mn0 = fmaxf(a_.m0, mx0), mn1 = fmaxf(a_.m1, mx1);  // finite: token tok0 is valid
       const float al0 = exp2f(a_.m0 - mn0), al1 = exp2f(a_.m1 - mn1);
-      const float p0 = exp2f(acc[0] - mn0), p1 = exp2f(acc[1] - mn1);
-      const float p2 = exp2f(acc[2] - mn0), p3 = exp2f(acc[3] - mn1);
+      const float p0 = exp2f(acc[p][0] - mn0), p1 = exp2f(acc[p][1] - mn1);
+      const float p2 = exp2f(acc[p][2] - mn0), p3 = exp2f(acc[p][3] - mn1);
       a_.l0 = a_.l0 * al0 + p0 + p2;
       a_.l1 = a_.l1 * al1 + p1 + p3;
       a_.m0 = mn0;
@@ -790,15 +800,18 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
         a_.o[mt][2] *= al0;
         a_.o[mt][3] *= al1;
       }
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      pb[p][0] = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0-7 of the tile
+      pb[p][1] = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8-15
+    }
+    // O^T += V^T P^T for every active position, each V fragment loaded once for all of them
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int dch = 2 * mt + ch_v;
-        uint32_t a[4];
-        ldsm_x4_trans(a, swz(stg, dch >> 3, 1, tk_v, dch & 7));
-        mma_16816(a_.o[mt], a, pb0, pb1);
-      }
+    for (int mt = 0; mt < 8; ++mt) {
+      const int dch = 2 * mt + ch_v;
+      uint32_t a[4];
+      ldsm_x4_trans(a, swz(stg, dch >> 3, 1, tk_v, dch & 7));
+#pragma unroll
+      for (int p = 0; p < P; ++p)
+        if (act[p]) mma_16816(A[p].o[mt], a, pb[p][0], pb[p][1]);
     }
     __syncthreads();  // every warp is done with this stage
     issue(i + kPfStages);
