@@ -15,27 +15,25 @@
 //      selection in order: the k_e query-agnostic picks among the candidates never
 //      dropped before (a short list ordered by pooled s^e), the sticky eviction update,
 //      the set difference against the previous selection and the ascending free-slot
-//      pairing, with bitmaps over the blocks.  The selection is written to the caller's
-//      scratch, one row of block ids (with their kinds) per position.
+//      pairing, with bitmaps over the blocks.  Each position's picks go to the caller's
+//      scratch as two bitmaps (query-aware, query-agnostic).
 //   3. prefill_refresh_kernel: every cache slot gets its block's K/V from the prompt
 //      (the state after the prompt is the one the decode steps would have left).
-//   4. prefill_attend_kernel: a CTA takes P consecutive positions of one unit, forms
-//      the union of their selections and streams those blocks from the prompt's K and
-//      V (TMA, 128-byte swizzle) through a ring of stages; every staged block is
-//      attended by each of the P positions whose selection holds it (the tail block
-//      of a position up to the position itself), with the decode attention's
-//      tensor-core math per position.  Positions share every block they have in
-//      common, so the K/V reads are shared P ways.
-#include "attend_core.cuh"
+//   4. prefill_attend_tc_kernel: a CTA takes 128 / G consecutive positions of one unit (128
+//      rows of position x q head), forms the union of their selections and streams those
+//      blocks from the prompt's K and V (TMA, 128-byte swizzle); each block's scores and
+//      its product with V run on the fifth-generation tensor cores (tcgen05, accumulators
+//      in tensor memory), one thread per row does that row's masking and online softmax.
+//      Positions share every block they have in common.
+#include "attend_core.cuh"  // kStageBytes, the TMA and mbarrier helpers
 #include "host.h"
 #include "select_core.cuh"
+#include "tc.cuh"
 
 namespace nosa {
 
 using namespace selcore;
 
-constexpr int kPfPositions = 4;        // positions per attention CTA
-constexpr int kPfStages = 3;           // 32 KiB stages
 constexpr int kPfMaxWords = 2048 / 32;  // block bitmap words per position (prompts of up to 131,072 tokens)
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
@@ -612,223 +610,285 @@ __global__ void __launch_bounds__(256) prefill_refresh_kernel(LayerState s, cons
   }
 }
 
-// ---------------------------------------------------------------- 4. attention of every position
-// grid (U, ceil(n / P)), 128 threads (four warps, 16 tokens of every block each).  A position's
-// selection: its query-aware and query-agnostic bitmap words (qsel, esel: [U][n][ceil(nbn / 32)])
-// plus its sink and window blocks.
-template <int P>
-__global__ void __launch_bounds__(kTeamThreads, 1)
-    prefill_attend_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                          LayerState s, const uint16_t* __restrict__ q, uint16_t* __restrict__ out,
-                          const uint32_t* __restrict__ qsel, const uint32_t* __restrict__ esel, int n) {
-  extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kPfStages];
-  __shared__ uint32_t bm[P][kPfMaxWords];
-  __shared__ int ublk[P * kMaxCacheSlots];
-  __shared__ uint8_t umask[P * kMaxCacheSlots];
-  __shared__ int n_union;
-  __shared__ float wm[4][kMaxGroup], wl[4][kMaxGroup];
-  __shared__ __align__(16) float sebuf[kPfStages][kBlock];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int u = blockIdx.x, t0 = blockIdx.y * P;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gr = lane >> 2, t4 = lane & 3;
-  const int G = s.G, cap = s.cap;
-  const int np = min(P, n - t0);
+// ---------------------------------------------------------------- 4. attention of every position (tcgen05)
+// A CTA takes PT = 128 / G consecutive positions of one unit: its M = 128 rows are (position, q
+// head) pairs, row r = p G + h (rows past PT G or past the prompt are padding).  It streams the
+// union of the positions' selections block by block (TMA ring of K and V, 128-byte swizzle):
+//   S = Q K^T (M 128, N 64 tokens, K 128 dims) into tensor memory (two buffers), by one thread;
+//   each softmax thread owns one row: it reads its 64 scores, masks the block if the row's
+//   position did not select it (and the tail tokens past the position), updates its running
+//   maximum and sum (base 2), and writes its probabilities as bf16 to shared memory;
+//   O_b = P V (M 128, N 2 x 64 dims, K 64 tokens; V as an MN-major operand) into tensor memory;
+//   the row's thread adds O_b into its register accumulator with the running rescale.
+// Roles: warp 0 lane 0 issues the MMAs, warp 1 lane 0 the TMA loads, warps 4-7 own the rows
+// (tensor-memory lanes 0-127); warp 0 allocates and frees 256 tensor-memory columns.  Every
+// wait is bounded; a CTA whose wait gives up flags a timeout, drains and writes NaN outputs.
+constexpr int kTcRows = 128;
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 256;
+constexpr uint32_t kTcCols = 256;  // S buffers at columns 0 and 64, O at 128
+
+__host__ __device__ inline int tc_positions(int G) { return kTcRows / G; }
+__host__ __device__ inline size_t tc_smem_bytes(int G) {
+  // 1024 alignment slack, Q 32 KiB, stages, P 16 KiB, per-position block bitmaps, union list,
+  // per-stage eviction scores
+  return 1024 + 32768 + (size_t)kTcStages * kStageBytes + 16384 + (size_t)tc_positions(G) * kPfMaxWords * 4 +
+         (size_t)kPfMaxWords * 32 * 2 + (size_t)kTcStages * kBlock * 4;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_attend_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                             LayerState s, const uint16_t* __restrict__ q, uint16_t* __restrict__ out,
+                             const uint32_t* __restrict__ qsel, const uint32_t* __restrict__ esel, int n) {
+  extern __shared__ unsigned char tsm_raw[];
+  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], s_full[2], s_free[2], p_full, o_full, o_free,
+      drain;
+  __shared__ uint32_t tbase;
+  __shared__ int n_union, bad_flag;
+  unsigned char* sm =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tsm_raw) + 1023) & ~uintptr_t(1023));
+  const int G = s.G, PT = tc_positions(G);
+  unsigned char* sQ = sm;                                   // [2 dim halves][128 rows][128 B]
+  unsigned char* sStage = sQ + 32768;                       // [stage][dim half][K, V][64 tokens][128 B]
+  unsigned char* sP = sStage + kTcStages * kStageBytes;     // [128 rows][64 tokens] bf16
+  uint32_t* bm = reinterpret_cast<uint32_t*>(sP + 16384);   // [PT][kPfMaxWords]
+  int16_t* ublk = reinterpret_cast<int16_t*>(bm + PT * kPfMaxWords);  // union, ascending
+  float* sebuf = reinterpret_cast<float*>(ublk + kPfMaxWords * 32);   // [stage][64]
+  const int u = blockIdx.x, t0 = blockIdx.y * PT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int np = min(PT, n - t0);
   const int nb_last = (t0 + np + kBlock - 1) / kBlock;  // blocks of the last position's context
   const int nbw = (nb_last + 31) / 32;
+  const int nbws = ((n + kBlock - 1) / kBlock + 31) / 32;  // words per position in qsel and esel
   const bool dma = s.dma_bias != 0;
+  const long long lim = s.wait_limit;
   if (tid == 0) {
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
-    for (int i = 0; i < kPfStages; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(&p_full, 128);
+    mbar_init(&o_full, 1);
+    mbar_init(&o_free, 128);
+    mbar_init(&drain, 1);
     fence_mbar_init();
+    bad_flag = 0;
   }
-  pdl_wait();  // the selections, the prompt's K/V and (with the bias) the eviction scores
-  for (int i = tid; i < P * kPfMaxWords; i += blockDim.x) bm[i / kPfMaxWords][i % kPfMaxWords] = 0u;
-  __syncthreads();
-  const int nbws = ((n + kBlock - 1) / kBlock + 31) / 32;  // words per position in qsel and esel
-  for (int idx = tid; idx < np * nbw; idx += blockDim.x) {
-    const int p = idx / nbw, w = idx % nbw;
-    const Geometry g = geometry(t0 + p + 1, s.nw, s.sink);
-    const size_t o = ((size_t)u * n + t0 + p) * nbws + w;
-    bm[p][w] = qsel[o] | esel[o] | range_bits(w, 0, g.ns) | range_bits(w, g.ws, g.nb);
+  if (warp == 0) tc::alloc(&tbase, kTcCols);
+  pdl_wait();  // the selections, the prompt's q, K and V and (with the bias) the eviction scores
+  // per-position selections: query-aware | query-agnostic | sink | window
+  for (int idx = tid; idx < PT * kPfMaxWords; idx += kTcThreads) {
+    const int p = idx / kPfMaxWords, w = idx % kPfMaxWords;
+    uint32_t v = 0u;
+    if (p < np && w < nbw) {
+      const Geometry g = geometry(t0 + p + 1, s.nw, s.sink);
+      const size_t o = ((size_t)u * n + t0 + p) * nbws + w;
+      v = qsel[o] | esel[o] | range_bits(w, 0, g.ns) | range_bits(w, g.ws, g.nb);
+    }
+    bm[idx] = v;
+  }
+  // Q rows (position p, head h) in the 128-byte swizzle: row r, 16-byte chunk c of its dim half
+  for (int idx = tid; idx < kTcRows * 16; idx += kTcThreads) {
+    const int r = idx >> 4, c = idx & 15, p = r / G, h = r % G;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (p < np) v = *reinterpret_cast<const uint4*>(q + (((size_t)u * G + h) * n + t0 + p) * kHeadDim + 8 * c);
+    *reinterpret_cast<uint4*>(sQ + (c >> 3) * 16384 + r * 128 + ((((c & 7) ^ (r & 7)) & 7) << 4)) = v;
   }
   __syncthreads();
-  if (warp == 0) {  // the union of the positions' selections, ascending, with a position mask each
+  if (warp == 2) {  // the union of the positions' selections, ascending
     int base = 0;
     for (int w0 = 0; w0 < nbw; w0 += 32) {
       const int w = w0 + lane;
-      uint32_t bits[P], uni = 0u;
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        bits[p] = w < nbw ? bm[p][w] : 0u;
-        uni |= bits[p];
-      }
+      uint32_t uni = 0u;
+      if (w < nbw)
+        for (int p = 0; p < np; ++p) uni |= bm[p * kPfMaxWords + w];
       const int c = __popc(uni);
-      int incl = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
+      const int incl = warp_incl_scan(c);
       int pos = base + incl - c;
-      while (uni) {
-        const int j = __ffs(uni) - 1;
-        uni &= uni - 1u;
-        uint8_t mk = 0;
-#pragma unroll
-        for (int p = 0; p < P; ++p) mk |= (uint8_t)(((bits[p] >> j) & 1u) << p);
-        ublk[pos] = 32 * w + j;
-        umask[pos] = mk;
-        ++pos;
-      }
+      for (; uni; uni &= uni - 1u) ublk[pos++] = (int16_t)(32 * w + __ffs(uni) - 1);
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) n_union = base;
   }
-  // q fragments of every position (head gr of the group, 16 dims per k-step)
-  uint32_t qb[P][8][2];
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    const int t = min(t0 + p, n - 1);
-    const uint16_t* qh = q + (((size_t)u * G + min(gr, G - 1)) * n + t) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qb[p][ks][0] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4) : 0u;
-      qb[p][ks][1] = gr < G ? *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * t4 + 8) : 0u;
-    }
-  }
+  fence_proxy_async_smem();  // Q (generic stores) is read by the tensor core
+  tc::fence_before();
   __syncthreads();
+  tc::fence_after();
   const int nu = n_union;
-  const uint32_t sbase = smem_u32(smem);
-  auto issue = [&](int i) {  // union entry i into stage i % kPfStages
-    if (i >= nu || tid != 0) return;
-    const int st = i % kPfStages, b = ublk[i];
-    const uint32_t dst = sbase + st * kStageBytes;
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&bars[st], kStageBytes + (dma ? kBlock * 4 : 0));
-    // stage layout [d half][K, V][64 tokens][64 dims]: four 8 KiB boxes
-    tma_load_3d(dst, &tk, 0, kBlock * b, u, &bars[st]);
-    tma_load_3d(dst + 8192, &tv, 0, kBlock * b, u, &bars[st]);
-    tma_load_3d(dst + 16384, &tk, 64, kBlock * b, u, &bars[st]);
-    tma_load_3d(dst + 24576, &tv, 64, kBlock * b, u, &bars[st]);
-    if (dma) bulk_copy_g2s(smem_u32(sebuf[st]), s.se_tok + (size_t)u * s.se_stride + (size_t)kBlock * b, kBlock * 4,
-                           &bars[st]);
-  };
-  for (int i = 0; i < kPfStages; ++i) issue(i);
+  const uint32_t tm = tbase;
+  const uint32_t sQa = smem_u32(sQ), sSa = smem_u32(sStage), sPa = smem_u32(sP);
+  constexpr uint32_t idS = tc::f16_idesc(128, 64, 0), idO = tc::f16_idesc(128, 64, 1);
 
-  WarpAcc A[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) A[p].init();
-  const float sl2 = s.scale * 1.4426950408889634f;
-  const int tok0 = warp * 16;
-  const int tk_k = tok0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-  const int ch_k = lane >> 4;
-  const int tk_v = tok0 + (lane & 7) + ((lane >> 4) << 3);
-  const int ch_v = (lane >> 3) & 1;
-  bool bad = false;
-  for (int i = 0; i < nu; ++i) {
-    const int st = i % kPfStages, b = ublk[i];
-    const uint8_t mk = umask[i];
-    const bool okw = s.wait_limit >= 0 && mbar_wait_bounded(&bars[st], (uint32_t)((i / kPfStages) & 1), s.wait_limit);
-    if (__syncthreads_or(!okw)) {
-      if (tid == 0) atomicOr(s.err, kErrTimeout);
-      bad = true;
-      if (tid == 0)  // drain the copies still in flight before the shared memory goes away
-        for (int j = i; j < min(i + kPfStages, nu); ++j)
-          mbar_wait_bounded(&bars[j % kPfStages], (uint32_t)((j / kPfStages) & 1), kWaitCycles);
-      break;
-    }
-    const uint32_t stg = sbase + st * kStageBytes;
-    // the positions whose selection holds this block and for which this warp's 16 tokens exist
-    // (the block's tail up to the position itself); warp-uniform
-    bool act[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) act[p] = ((mk >> p) & 1) && tok0 < min(t0 + p + 1 - kBlock * b, kBlock);
-    // S^T = K q^T for every active position, each K fragment loaded once for all of them
-    float acc[P][4];
-#pragma unroll
-    for (int p = 0; p < P; ++p) acc[p][0] = acc[p][1] = acc[p][2] = acc[p][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int dch = 2 * ks + ch_k;
-      uint32_t a[4];
-      ldsm_x4(a, swz(stg, dch >> 3, 0, tk_k, dch & 7));
-#pragma unroll
-      for (int p = 0; p < P; ++p)
-        if (act[p]) mma_16816(acc[p], a, qb[p][ks][0], qb[p][ks][1]);
-    }
-    uint32_t pb[P][2];
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      pb[p][0] = pb[p][1] = 0u;
-      if (!act[p]) continue;
-      const int valid = min(t0 + p + 1 - kBlock * b, kBlock);  // tokens of the block in position p's context
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[p][j] *= sl2;
-      if (dma) {
-        const float b0 = sebuf[st][tok0 + gr] * 1.4426950408889634f;
-        const float b1 = sebuf[st][tok0 + gr + 8] * 1.4426950408889634f;
-        acc[p][0] += b0;
-        acc[p][1] += b0;
-        acc[p][2] += b1;
-        acc[p][3] += b1;
+  if (warp == 1 && lane == 0) {  // TMA producer
+    int issued = 0;
+    for (int j = 0; j < nu; ++j) {
+      const int st = j % kTcStages;
+      if (j >= kTcStages && !mbar_wait_bounded(&empty[st], (uint32_t)(((j / kTcStages) - 1) & 1), lim)) {
+        atomicOr(&bad_flag, 1);
+        break;
       }
-      if (tok0 + gr >= valid) acc[p][0] = acc[p][1] = -INFINITY;
-      if (tok0 + gr + 8 >= valid) acc[p][2] = acc[p][3] = -INFINITY;
-      float mx0 = fmaxf(acc[p][0], acc[p][2]), mx1 = fmaxf(acc[p][1], acc[p][3]);
-#pragma unroll
-      for (int o2 = 4; o2 < 32; o2 <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
-      }
-      WarpAcc& a_ = A[p];
-      const float mn0 = fmaxf(a_.m0, mx0), mn1 = fmaxf(a_.m1, mx1);  // finite: token tok0 is valid
-      const float al0 = exp2f(a_.m0 - mn0), al1 = exp2f(a_.m1 - mn1);
-      const float p0 = exp2f(acc[p][0] - mn0), p1 = exp2f(acc[p][1] - mn1);
-      const float p2 = exp2f(acc[p][2] - mn0), p3 = exp2f(acc[p][3] - mn1);
-      a_.l0 = a_.l0 * al0 + p0 + p2;
-      a_.l1 = a_.l1 * al1 + p1 + p3;
-      a_.m0 = mn0;
-      a_.m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        a_.o[mt][0] *= al0;
-        a_.o[mt][1] *= al1;
-        a_.o[mt][2] *= al0;
-        a_.o[mt][3] *= al1;
-      }
-      pb[p][0] = movmatrix_trans(pack_bf16x2(p0, p1));  // tokens 0-7 of the tile
-      pb[p][1] = movmatrix_trans(pack_bf16x2(p2, p3));  // tokens 8-15
+      if (*(volatile int*)&bad_flag) break;
+      const int b = ublk[j];
+      const uint32_t dst = sSa + st * kStageBytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&full[st], kStageBytes + (dma ? kBlock * 4 : 0));
+      tma_load_3d(dst, &tk, 0, kBlock * b, u, &full[st]);
+      tma_load_3d(dst + 8192, &tv, 0, kBlock * b, u, &full[st]);
+      tma_load_3d(dst + 16384, &tk, 64, kBlock * b, u, &full[st]);
+      tma_load_3d(dst + 24576, &tv, 64, kBlock * b, u, &full[st]);
+      if (dma)
+        bulk_copy_g2s(smem_u32(sebuf + st * kBlock), s.se_tok + (size_t)u * s.se_stride + (size_t)kBlock * b,
+                      kBlock * 4, &full[st]);
+      issued = j + 1;
     }
-    // O^T += V^T P^T for every active position, each V fragment loaded once for all of them
+    // the last loads have landed before the shared memory goes away (on the normal path the MMA
+    // issuer has already waited for every one of them)
+    for (int j = max(issued - kTcStages, 0); j < issued; ++j)
+      mbar_wait_bounded(&full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kWaitCycles);
+  } else if (warp == 0 && lane == 0) {  // MMA issuer
+    auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j & 1
+      const int st = j % kTcStages, sb = j & 1;
+      if (!mbar_wait_bounded(&full[st], (uint32_t)((j / kTcStages) & 1), lim)) return false;
+      if (j >= 2 && !mbar_wait_bounded(&s_free[sb], (uint32_t)(((j >> 1) - 1) & 1), lim)) return false;
+      tc::fence_after();
+      const uint32_t kb = sSa + st * kStageBytes;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int dch = 2 * mt + ch_v;
-      uint32_t a[4];
-      ldsm_x4_trans(a, swz(stg, dch >> 3, 1, tk_v, dch & 7));
+      for (int kk = 0; kk < 8; ++kk) {  // dims 16 kk .. 16 kk + 15: K halves at +0 and +16384
+        const uint32_t off = (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32;
+        tc::mma_bf16(tm + 64 * sb, tc::sw128_desc(sQa + off), tc::sw128_desc(kb + off), idS, kk > 0);
+      }
+      tc::commit(&s_full[sb]);
+      return true;
+    };
+    bool ok = nu == 0 || issue_s(0);
+    for (int j = 0; ok && j < nu; ++j) {
+      if (j + 1 < nu && !issue_s(j + 1)) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait_bounded(&p_full, (uint32_t)(j & 1), lim) ||
+          (j >= 1 && !mbar_wait_bounded(&o_free, (uint32_t)((j - 1) & 1), lim))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      const uint32_t vb = sSa + (j % kTcStages) * kStageBytes + 8192;  // V halves at +8192 and +24576
 #pragma unroll
-      for (int p = 0; p < P; ++p)
-        if (act[p]) mma_16816(A[p].o[mt], a, pb[p][0], pb[p][1]);
+      for (int half = 0; half < 2; ++half)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // tokens 16 kk .. 16 kk + 15: 16 rows of V per step
+          tc::mma_bf16(tm + 128 + 64 * half, tc::sw128_desc(sPa + 32 * kk),
+                       tc::sw128_desc(vb + half * 16384 + 2048 * kk), idO, kk > 0);
+      tc::commit(&o_full);
+      tc::commit(&empty[j % kTcStages]);
     }
-    __syncthreads();  // every warp is done with this stage
-    issue(i + kPfStages);
-  }
-  __syncthreads();
-  float* wo = reinterpret_cast<float*>(smem);  // [4 warps][8 heads][128], over the stages
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    if (bad) A[p].l0 = A[p].l1 = __int_as_float(0x7fc00000);  // a wait gave up: NaN outputs
+    if (!ok) atomicOr(&bad_flag, 1);
+    tc::commit(&drain);  // arrives once every MMA issued above has completed
+    mbar_wait_bounded(&drain, 0u, kWaitCycles);
+  } else if (warp >= 4) {  // one row per thread
+    const int r = tid - 128, p = r / G, h = r % G;
+    const bool row_ok = p < np;
     const int t = t0 + p;
-    cta_partial<4>(A[p], wm, wl, wo, G, [&](int h, int x, float M, float L, float O) {
-      if (t < n)
-        out[(((size_t)u * G + h) * n + t) * kHeadDim + x] =
-            __bfloat16_as_ushort(__float2bfloat16_rn(L > 0.f ? O / L : 0.f));
-    });
-    __syncthreads();  // wo, wm and wl are reused by the next position
+    const uint32_t trow = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's tensor-memory lanes
+    const float sl2 = s.scale * 1.4426950408889634f;
+    float m = -INFINITY, l = 0.f;
+    float O[kHeadDim];
+#pragma unroll
+    for (int x = 0; x < kHeadDim; ++x) O[x] = 0.f;
+    for (int j = 0; j < nu; ++j) {
+      const int sb = j & 1, st = j % kTcStages, b = ublk[j];
+      if (!mbar_wait_bounded(&s_full[sb], (uint32_t)((j >> 1) & 1), lim)) {
+        atomicOr(&bad_flag, 1);
+        break;
+      }
+      tc::fence_after();
+      uint32_t sv[2][32];
+      tc::ld32(trow + 64 * sb, sv[0]);
+      tc::ld32(trow + 64 * sb + 32, sv[1]);
+      tc::wait_ld();
+      tc::fence_before();
+      mbar_arrive(&s_free[sb]);
+      const bool act = row_ok && ((bm[p * kPfMaxWords + (b >> 5)] >> (b & 31)) & 1u);
+      const int valid = min(t + 1 - kBlock * b, kBlock);  // tokens of the block in the position's context
+      float alpha = 1.f;
+      uint32_t pk[32];  // bf16 pairs of the row's 64 probabilities
+      if (act) {
+        float z[64];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float v = __uint_as_float(sv[i >> 5][i & 31]) * sl2;
+          if (dma) v += sebuf[st * kBlock + i] * 1.4426950408889634f;
+          z[i] = i < valid ? v : -INFINITY;
+          mx = fmaxf(mx, z[i]);
+        }
+        const float mn = fmaxf(m, mx);  // finite: token 0 of the block is in the context
+        alpha = exp2f(m - mn);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = exp2f(z[i] - mn), e1 = exp2f(z[i + 1] - mn);
+          sum += e0 + e1;
+          pk[i >> 1] = pack_bf16x2(e0, e1);
+        }
+        l = l * alpha + sum;
+        m = mn;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+      }
+      // the row's P in the 128-byte swizzle (eight 16-byte chunks of 8 tokens)
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sP + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(&p_full);
+      if (!mbar_wait_bounded(&o_full, (uint32_t)(j & 1), lim)) {
+        atomicOr(&bad_flag, 1);
+        break;
+      }
+      tc::fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        tc::ld32(trow + 128 + 32 * c, ov);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) O[32 * c + i] = O[32 * c + i] * alpha + __uint_as_float(ov[i]);
+      }
+      tc::fence_before();
+      mbar_arrive(&o_free);
+    }
+    const bool bad = *(volatile int*)&bad_flag != 0;
+    if (row_ok) {
+      uint16_t* orow = out + (((size_t)u * G + h) * n + t) * kHeadDim;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = bad ? __int_as_float(0x7fc00000) : O[8 * c + 2 * e] * inv;
+          const float a1 = bad ? __int_as_float(0x7fc00000) : O[8 * c + 2 * e + 1] * inv;
+          w4[e] = pack_bf16x2(a0, a1);
+        }
+        reinterpret_cast<uint4*>(orow)[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+    }
   }
+  // every MMA and every load has completed (the issuers waited for them above)
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (tid == 0 && bad_flag) atomicOr(s.err, kErrTimeout);
+  if (warp == 0) tc::dealloc(tm, kTcCols);
 }
 
 // ---------------------------------------------------------------- host side
@@ -837,14 +897,13 @@ __global__ void __launch_bounds__(kTeamThreads, 1)
 static bool prefill_wide(int nbn) { return nbn > 1024; }
 static size_t query_smem(int nbn, int pw) { return (size_t)kPqWarps * pw * nbn * sizeof(uint32_t); }
 static size_t walk_smem(int nbn) { return kWalkWarps * walk_warp_bytes(nbn); }
-static size_t prefill_attend_smem() { return 1024 + (size_t)kPfStages * kStageBytes; }
 
 int prefill_max_tokens() { return kPfMaxWords * 32 * kBlock; }
 
 cudaError_t init_prefill() {
   const int nbn = kPfMaxWords * 32;
-  cudaError_t e = cudaFuncSetAttribute(prefill_attend_kernel<kPfPositions>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prefill_attend_smem());
+  cudaError_t e = cudaFuncSetAttribute(prefill_attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tc_smem_bytes(1));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(prefill_query_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)query_smem(1024, 4));
@@ -886,9 +945,9 @@ cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUt
   if (e != cudaSuccess) return e;
   e = launch_ex(prefill_refresh_kernel, dim3(s.cap, s.U), dim3(256), 0, st, true, 0, s, k, v, n);
   if (e != cudaSuccess) return e;
-  return launch_ex(prefill_attend_kernel<kPfPositions>, dim3(s.U, (n + kPfPositions - 1) / kPfPositions),
-                   dim3(kTeamThreads), prefill_attend_smem(), st, true, 0, *tk, *tv, s, q, out,
-                   qs, static_cast<const uint32_t*>(esel), n);
+  const int pt = tc_positions(s.G);
+  return launch_ex(prefill_attend_tc_kernel, dim3(s.U, (n + pt - 1) / pt), dim3(kTcThreads), tc_smem_bytes(s.G), st,
+                   true, 0, *tk, *tv, s, q, out, qs, static_cast<const uint32_t*>(esel), n);
 }
 
 }  // namespace nosa

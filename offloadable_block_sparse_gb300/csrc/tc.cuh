@@ -1,0 +1,81 @@
+// Fifth-generation tensor core (tcgen05) wrappers: tensor-memory allocation, the kind::f16 MMA
+// with shared-memory operand descriptors, completion through an mbarrier, and loads of the
+// accumulator from tensor memory.  One-instruction inline-PTX wrappers.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace nosa {
+namespace tc {
+
+// Shared-memory operand descriptor for a tile in the canonical 128-byte swizzle: rows of 128 bytes
+// (64 bf16), 8-row atoms of 1024 bytes stacked along the strided dimension.  addr: shared-memory
+// byte address of the first element the instruction reads (a 16-byte multiple inside a
+// 1024-byte-aligned tile).  Fields: start address >> 4 (bits 0-13), leading byte offset >> 4
+// (bits 16-29; unused by this swizzle), stride byte offset >> 4 (bits 32-45: 1024 bytes between
+// atoms), descriptor version 1 (bits 46-47), swizzle mode 2 = 128 bytes (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, f32 accumulation: M rows, N columns; B
+// K-major (b_mn = 0: its rows are N, contiguous along K) or MN-major (b_mn = 1: rows are K,
+// contiguous along N).  Fields: accumulator format f32 (bits 4-5 = 1), A and B format bf16 (bits
+// 7-9, 10-12 = 1), B major-ness (bit 16), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+__host__ __device__ constexpr uint32_t f16_idesc(int M, int N, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// Allocates ncols (a power of two, 32..512) tensor-memory columns; the base address is written
+// to *dst (shared memory).  One full warp executes it; the same warp frees them with dealloc.
+__device__ __forceinline__ void alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A . B for one K = 16 slice; accumulate = false overwrites D.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
+// The mbarrier receives one arrival when every MMA this thread issued before has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Ordering of tensor-core operations around thread synchronisation (barriers, mbarrier waits).
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// 32 consecutive 32-bit columns of one tensor-memory lane per thread: warp w (mod 4) of the
+// warpgroup reads lanes 32 (w mod 4) .. + 31, thread lane l its lane 32 (w mod 4) + l.
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+}  // namespace tc
+}  // namespace nosa
