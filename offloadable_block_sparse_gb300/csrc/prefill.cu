@@ -614,12 +614,16 @@ __global__ void __launch_bounds__(256) prefill_refresh_kernel(LayerState s, cons
 // A CTA takes PT = 128 / G consecutive positions of one unit: its M = 128 rows are (position, q
 // head) pairs, row r = p G + h (rows past PT G or past the prompt are padding).  It streams the
 // union of the positions' selections block by block (TMA ring of K and V, 128-byte swizzle):
-//   S = Q K^T (M 128, N 64 tokens, K 128 dims) into tensor memory (two buffers), by one thread;
+//   S_b = Q K_b^T (M 128, N 64 tokens, K 128 dims) into tensor memory (two buffers);
 //   each softmax thread owns one row: it reads its 64 scores, masks the block if the row's
-//   position did not select it (and the tail tokens past the position), updates its running
-//   maximum and sum (base 2), and writes its probabilities as bf16 to shared memory;
-//   O_b = P V (M 128, N 2 x 64 dims, K 64 tokens; V as an MN-major operand) into tensor memory;
-//   the row's thread adds O_b into its register accumulator with the running rescale.
+//   position did not select it (and the tail tokens past the position), and writes its
+//   probabilities exp2(z - m_ref) as bf16 to shared memory (two buffers), adding them to its sum;
+//   O += P_b V_b (M 128, N 2 x 64 dims, K 64 tokens; V as an MN-major operand) accumulates in
+//   tensor memory across blocks.
+// m_ref, the reference maximum of a row, is raised only when a block's maximum exceeds it by more
+// than 8 (base 2): then the row's sum and its accumulated O (read and written back by the row's
+// thread, once the previous product has completed) are scaled by exp2(old - new).  Probabilities
+// stay below 2^8, and the output is O / sum with the same reference for both.
 // Roles: warp 0 lane 0 issues the MMAs, warp 1 lane 0 the TMA loads, warps 4-7 own the rows
 // (tensor-memory lanes 0-127); warp 0 allocates and frees 256 tensor-memory columns.  Every
 // wait is bounded; a CTA whose wait gives up flags a timeout, drains and writes NaN outputs.
@@ -627,12 +631,21 @@ constexpr int kTcRows = 128;
 constexpr int kTcStages = 3;
 constexpr int kTcThreads = 256;
 constexpr uint32_t kTcCols = 256;  // S buffers at columns 0 and 64, O at 128
+constexpr float kTcRescale = 8.f;  // base-2 growth of a row maximum that forces a rescale
+
+// 2^x by the special-function unit (relative error far below bf16's rounding of the probabilities;
+// -inf gives 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __host__ __device__ inline int tc_positions(int G) { return kTcRows / G; }
 __host__ __device__ inline size_t tc_smem_bytes(int G) {
-  // 1024 alignment slack, Q 32 KiB, stages, P 16 KiB, per-position block bitmaps, union list,
-  // per-stage eviction scores
-  return 1024 + 32768 + (size_t)kTcStages * kStageBytes + 16384 + (size_t)tc_positions(G) * kPfMaxWords * 4 +
+  // 1024 alignment slack, Q 32 KiB, stages, two P buffers of 16 KiB, per-position block bitmaps,
+  // union list, per-stage eviction scores
+  return 1024 + 32768 + (size_t)kTcStages * kStageBytes + 2 * 16384 + (size_t)tc_positions(G) * kPfMaxWords * 4 +
          (size_t)kPfMaxWords * 32 * 2 + (size_t)kTcStages * kBlock * 4;
 }
 
@@ -641,7 +654,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              LayerState s, const uint16_t* __restrict__ q, uint16_t* __restrict__ out,
                              const uint32_t* __restrict__ qsel, const uint32_t* __restrict__ esel, int n) {
   extern __shared__ unsigned char tsm_raw[];
-  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], s_full[2], s_free[2], p_full, o_full, o_free,
+  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], s_full[2], s_free[2], p_full[2], o_done[2],
       drain;
   __shared__ uint32_t tbase;
   __shared__ int n_union, bad_flag;
@@ -650,8 +663,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int G = s.G, PT = tc_positions(G);
   unsigned char* sQ = sm;                                   // [2 dim halves][128 rows][128 B]
   unsigned char* sStage = sQ + 32768;                       // [stage][dim half][K, V][64 tokens][128 B]
-  unsigned char* sP = sStage + kTcStages * kStageBytes;     // [128 rows][64 tokens] bf16
-  uint32_t* bm = reinterpret_cast<uint32_t*>(sP + 16384);   // [PT][kPfMaxWords]
+  unsigned char* sP = sStage + kTcStages * kStageBytes;     // [2][128 rows][64 tokens] bf16
+  uint32_t* bm = reinterpret_cast<uint32_t*>(sP + 2 * 16384);  // [PT][kPfMaxWords]
   int16_t* ublk = reinterpret_cast<int16_t*>(bm + PT * kPfMaxWords);  // union, ascending
   float* sebuf = reinterpret_cast<float*>(ublk + kPfMaxWords * 32);   // [stage][64]
   const int u = blockIdx.x, t0 = blockIdx.y * PT;
@@ -672,10 +685,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(&p_full, 128);
-    mbar_init(&o_full, 1);
-    mbar_init(&o_free, 128);
     mbar_init(&drain, 1);
     fence_mbar_init();
     bad_flag = 0;
@@ -772,20 +784,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = false;
         break;
       }
-      if (!mbar_wait_bounded(&p_full, (uint32_t)(j & 1), lim) ||
-          (j >= 1 && !mbar_wait_bounded(&o_free, (uint32_t)((j - 1) & 1), lim))) {
+      const int pb = j & 1;
+      if (!mbar_wait_bounded(&p_full[pb], (uint32_t)((j >> 1) & 1), lim)) {
         ok = false;
         break;
       }
       tc::fence_after();
       const uint32_t vb = sSa + (j % kTcStages) * kStageBytes + 8192;  // V halves at +8192 and +24576
+      const uint32_t pa = sPa + pb * 16384;
 #pragma unroll
       for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // tokens 16 kk .. 16 kk + 15: 16 rows of V per step
-          tc::mma_bf16(tm + 128 + 64 * half, tc::sw128_desc(sPa + 32 * kk),
-                       tc::sw128_desc(vb + half * 16384 + 2048 * kk), idO, kk > 0);
-      tc::commit(&o_full);
+          tc::mma_bf16(tm + 128 + 64 * half, tc::sw128_desc(pa + 32 * kk),
+                       tc::sw128_desc(vb + half * 16384 + 2048 * kk), idO, j > 0 || kk > 0);
+      tc::commit(&o_done[pb]);
       tc::commit(&empty[j % kTcStages]);
     }
     if (!ok) atomicOr(&bad_flag, 1);
@@ -797,14 +810,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int t = t0 + p;
     const uint32_t trow = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's tensor-memory lanes
     const float sl2 = s.scale * 1.4426950408889634f;
-    float m = -INFINITY, l = 0.f;
-    float O[kHeadDim];
-#pragma unroll
-    for (int x = 0; x < kHeadDim; ++x) O[x] = 0.f;
+    float mref = -INFINITY, l = 0.f;
+    bool good = true;
     for (int j = 0; j < nu; ++j) {
       const int sb = j & 1, st = j % kTcStages, b = ublk[j];
-      if (!mbar_wait_bounded(&s_full[sb], (uint32_t)((j >> 1) & 1), lim)) {
-        atomicOr(&bad_flag, 1);
+      // waits are decided for the whole warp: the tensor-memory accesses below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (uint32_t)((j >> 1) & 1), lim))) {
+        good = false;
         break;
       }
       tc::fence_after();
@@ -816,57 +828,101 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive(&s_free[sb]);
       const bool act = row_ok && ((bm[p * kPfMaxWords + (b >> 5)] >> (b & 31)) & 1u);
       const int valid = min(t + 1 - kBlock * b, kBlock);  // tokens of the block in the position's context
-      float alpha = 1.f;
-      uint32_t pk[32];  // bf16 pairs of the row's 64 probabilities
-      if (act) {
-        float z[64];
-        float mx = -INFINITY;
+      // scores in base 2 with the tail masked; eight independent partial maxima (one warp per
+      // scheduler: the row's chain of dependent operations is the cost)
+      float z[64];
+      float mxp[8];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float v = __uint_as_float(sv[i >> 5][i & 31]) * sl2;
-          if (dma) v += sebuf[st * kBlock + i] * 1.4426950408889634f;
-          z[i] = i < valid ? v : -INFINITY;
-          mx = fmaxf(mx, z[i]);
+      for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        float v = __uint_as_float(sv[i >> 5][i & 31]) * sl2;
+        if (dma) v = fmaf(sebuf[st * kBlock + i], 1.4426950408889634f, v);
+        z[i] = i < valid ? v : -INFINITY;
+        mxp[i & 7] = fmaxf(mxp[i & 7], z[i]);
+      }
+      const float mx = act ? fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])))
+                           : -INFINITY;
+      // raise the reference maximum: at once for a row with nothing accumulated yet, else when it
+      // grew by more than the threshold (the row's O scaled in tensor memory, warp by warp)
+      float alpha = 1.f;
+      if (act && mx > mref) {
+        if (l == 0.f) {
+          mref = mx;
+        } else if (mx > mref + kTcRescale) {
+          alpha = ex2(mref - mx);
+          mref = mx;
         }
-        const float mn = fmaxf(m, mx);  // finite: token 0 of the block is in the context
-        alpha = exp2f(m - mn);
-        float sum = 0.f;
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j >= 1 &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), lim))) {
+          good = false;
+          break;
+        }
+        tc::fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          tc::ld32(trow + 128 + 32 * c, ov);
+          tc::wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tc::st32(trow + 128 + 32 * c, ov);
+        }
+        tc::wait_st();
+        tc::fence_before();
+        l *= alpha;
+      }
+      uint32_t pk[32];  // bf16 pairs of the row's 64 probabilities (0 for a block it did not select)
+      if (act) {
+        float sp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sp[k] = 0.f;
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float e0 = exp2f(z[i] - mn), e1 = exp2f(z[i + 1] - mn);
-          sum += e0 + e1;
+          const float e0 = ex2(z[i] - mref), e1 = ex2(z[i + 1] - mref);  // 0 for masked tokens
+          sp[(i >> 1) & 7] += e0 + e1;
           pk[i >> 1] = pack_bf16x2(e0, e1);
         }
-        l = l * alpha + sum;
-        m = mn;
+        l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) pk[i] = 0u;
       }
-      // the row's P in the 128-byte swizzle (eight 16-byte chunks of 8 tokens)
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(sP + r * 128 + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      mbar_arrive(&p_full);
-      if (!mbar_wait_bounded(&o_full, (uint32_t)(j & 1), lim)) {
-        atomicOr(&bad_flag, 1);
+      // the row's P into buffer j & 1 once the product two blocks back has read it
+      const int pb = j & 1;
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[pb], (uint32_t)(((j >> 1) - 1) & 1), lim))) {
+        good = false;
         break;
       }
-      tc::fence_after();
+      unsigned char* prow = sP + pb * 16384 + r * 128;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        tc::ld32(trow + 128 + 32 * c, ov);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) O[32 * c + i] = O[32 * c + i] * alpha + __uint_as_float(ov[i]);
-      }
-      tc::fence_before();
-      mbar_arrive(&o_free);
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(&p_full[pb]);
     }
-    const bool bad = *(volatile int*)&bad_flag != 0;
+    if (!good) atomicOr(&bad_flag, 1);
+    // the last product has completed: O / sum for the row
+    if (__all_sync(0xffffffffu, good) && nu > 0 &&
+        !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[(nu - 1) & 1], (uint32_t)(((nu - 1) >> 1) & 1), lim))) {
+      good = false;
+      atomicOr(&bad_flag, 1);
+    }
+    tc::fence_after();
+    float O[kHeadDim];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ov[32];
+      tc::ld32(trow + 128 + 32 * c, ov);
+      tc::wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) O[32 * c + i] = __uint_as_float(ov[i]);
+    }
+    const bool bad = *(volatile int*)&bad_flag != 0 || !good;
     if (row_ok) {
       uint16_t* orow = out + (((size_t)u * G + h) * n + t) * kHeadDim;
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -875,8 +931,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a0 = bad ? __int_as_float(0x7fc00000) : O[8 * c + 2 * e] * inv;
-          const float a1 = bad ? __int_as_float(0x7fc00000) : O[8 * c + 2 * e + 1] * inv;
+          const float a0 = bad ? __int_as_float(0x7fc00000) : (nu > 0 ? O[8 * c + 2 * e] * inv : 0.f);
+          const float a1 = bad ? __int_as_float(0x7fc00000) : (nu > 0 ? O[8 * c + 2 * e + 1] * inv : 0.f);
           w4[e] = pack_bf16x2(a0, a1);
         }
         reinterpret_cast<uint4*>(orow)[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
