@@ -615,21 +615,24 @@ __global__ void __launch_bounds__(256) prefill_refresh_kernel(LayerState s, cons
 // head) pairs, row r = p G + h (rows past PT G or past the prompt are padding).  It streams the
 // union of the positions' selections block by block (TMA ring of K and V, 128-byte swizzle):
 //   S_b = Q K_b^T (M 128, N 64 tokens, K 128 dims) into tensor memory (two buffers);
-//   each softmax thread owns one row: it reads its 64 scores, masks the block if the row's
-//   position did not select it (and the tail tokens past the position), and writes its
-//   probabilities exp2(z - m_ref) as bf16 to shared memory (two buffers), adding them to its sum;
-//   O += P_b V_b (M 128, N 2 x 64 dims, K 64 tokens; V as an MN-major operand) accumulates in
-//   tensor memory across blocks.
+//   two threads per row (32 scores each) mask the block if the row's position did not select it
+//   (and the tail tokens past the position), agree on the block maximum, and write the
+//   probabilities exp2(z - m_ref) as bf16 to shared memory (two buffers), each adding its half to
+//   its part of the row's sum;
+//   O += P_b V_b (M 128, N 128 dims, K 64 tokens; V as an MN-major operand whose two 64-dim halves
+//   are 16 KiB apart) accumulates in tensor memory across blocks.
 // m_ref, the reference maximum of a row, is raised only when a block's maximum exceeds it by more
 // than 8 (base 2): then the row's sum and its accumulated O (read and written back by the row's
-// thread, once the previous product has completed) are scaled by exp2(old - new).  Probabilities
+// threads, once the previous product has completed) are scaled by exp2(old - new).  Probabilities
 // stay below 2^8, and the output is O / sum with the same reference for both.
-// Roles: warp 0 lane 0 issues the MMAs, warp 1 lane 0 the TMA loads, warps 4-7 own the rows
-// (tensor-memory lanes 0-127); warp 0 allocates and frees 256 tensor-memory columns.  Every
+// Roles: warp 0 lane 0 issues the MMAs, warp 1 lane 0 the TMA loads, warps 4-11 own the rows, two
+// threads per row (warps 4-7 columns 0-31, warps 8-11 columns 32-63 of a block, on the same
+// tensor-memory lanes), exchanging their partial maxima through shared memory (an mbarrier per row
+// quarter and block parity); warp 0 allocates and frees 256 tensor-memory columns.  Every
 // wait is bounded; a CTA whose wait gives up flags a timeout, drains and writes NaN outputs.
 constexpr int kTcRows = 128;
 constexpr int kTcStages = 3;
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 384;
 constexpr uint32_t kTcCols = 256;  // S buffers at columns 0 and 64, O at 128
 constexpr float kTcRescale = 8.f;  // base-2 growth of a row maximum that forces a rescale
 
@@ -655,7 +658,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                              const uint32_t* __restrict__ qsel, const uint32_t* __restrict__ esel, int n) {
   extern __shared__ unsigned char tsm_raw[];
   __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], s_full[2], s_free[2], p_full[2], o_done[2],
-      drain;
+      drain, xbar[4][2];
+  __shared__ float xchg[2][2][kTcRows];  // [block parity][column half][row]: the partner's partial maximum
   __shared__ uint32_t tbase;
   __shared__ int n_union, bad_flag;
   unsigned char* sm =
@@ -684,8 +688,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&s_free[i], 256);
+      mbar_init(&p_full[i], 256);
+      for (int qq = 0; qq < 4; ++qq) mbar_init(&xbar[qq][i], 64);
       mbar_init(&o_done[i], 1);
     }
     mbar_init(&drain, 1);
@@ -735,7 +740,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int nu = n_union;
   const uint32_t tm = tbase;
   const uint32_t sQa = smem_u32(sQ), sSa = smem_u32(sStage), sPa = smem_u32(sP);
-  constexpr uint32_t idS = tc::f16_idesc(128, 64, 0), idO = tc::f16_idesc(128, 64, 1);
+  constexpr uint32_t idS = tc::f16_idesc(128, 64, 0), idO = tc::f16_idesc(128, 128, 1);
 
   if (warp == 1 && lane == 0) {  // TMA producer
     int issued = 0;
@@ -793,25 +798,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t vb = sSa + (j % kTcStages) * kStageBytes + 8192;  // V halves at +8192 and +24576
       const uint32_t pa = sPa + pb * 16384;
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // tokens 16 kk .. 16 kk + 15: 16 rows of V per step
-          tc::mma_bf16(tm + 128 + 64 * half, tc::sw128_desc(pa + 32 * kk),
-                       tc::sw128_desc(vb + half * 16384 + 2048 * kk), idO, j > 0 || kk > 0);
+      for (int kk = 0; kk < 4; ++kk)  // tokens 16 kk .. 16 kk + 15: 16 rows of V per step, all 128 dims
+        tc::mma_bf16(tm + 128, tc::sw128_desc(pa + 32 * kk), tc::sw128_desc_mn(vb + 2048 * kk, 16384), idO,
+                     j > 0 || kk > 0);
       tc::commit(&o_done[pb]);
       tc::commit(&empty[j % kTcStages]);
     }
     if (!ok) atomicOr(&bad_flag, 1);
     tc::commit(&drain);  // arrives once every MMA issued above has completed
     mbar_wait_bounded(&drain, 0u, kWaitCycles);
-  } else if (warp >= 4) {  // one row per thread
-    const int r = tid - 128, p = r / G, h = r % G;
+  } else if (warp >= 4) {  // two threads per row: warps 4-7 columns 0-31, warps 8-11 columns 32-63
+    const int hf = (warp - 4) >> 2, qr = warp & 3;
+    const int r = 32 * qr + lane, p = r / G, h = r % G, col0 = 32 * hf;
     const bool row_ok = p < np;
     const int t = t0 + p;
-    const uint32_t trow = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's tensor-memory lanes
+    const uint32_t trow = tm + ((uint32_t)(32 * qr) << 16);  // this warp's tensor-memory lanes
     const float sl2 = s.scale * 1.4426950408889634f;
-    float mref = -INFINITY, l = 0.f;
-    bool good = true;
+    float mref = -INFINITY, l = 0.f;  // l: this thread's half of the row's sum
+    bool started = false, good = true;
+    // the partner thread (same row, other half) exchanges one value per block through shared
+    // memory; an mbarrier per row quarter and block parity (bounded wait) orders the exchange
+    auto exchange = [&](int j, float v, float& other) -> bool {
+      xchg[j & 1][hf][r] = v;
+      mbar_arrive(&xbar[qr][j & 1]);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&xbar[qr][j & 1], (uint32_t)((j >> 1) & 1), lim))) return false;
+      other = xchg[j & 1][1 - hf][r];
+      return true;
+    };
     for (int j = 0; j < nu; ++j) {
       const int sb = j & 1, st = j % kTcStages, b = ublk[j];
       // waits are decided for the whole warp: the tensor-memory accesses below are warp-collective
@@ -820,41 +833,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc::fence_after();
-      uint32_t sv[2][32];
-      tc::ld32(trow + 64 * sb, sv[0]);
-      tc::ld32(trow + 64 * sb + 32, sv[1]);
+      uint32_t sv[32];
+      tc::ld32(trow + 64 * sb + col0, sv);
       tc::wait_ld();
       tc::fence_before();
       mbar_arrive(&s_free[sb]);
       const bool act = row_ok && ((bm[p * kPfMaxWords + (b >> 5)] >> (b & 31)) & 1u);
-      const int valid = min(t + 1 - kBlock * b, kBlock);  // tokens of the block in the position's context
-      // scores in base 2 with the tail masked; eight independent partial maxima (one warp per
-      // scheduler: the row's chain of dependent operations is the cost)
-      float z[64];
+      const int valid = min(t + 1 - kBlock * b, kBlock) - col0;  // tokens of this half in the position's context
+      // scores in base 2 with the tail masked; eight independent partial maxima
+      float z[32];
       float mxp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float v = __uint_as_float(sv[i >> 5][i & 31]) * sl2;
-        if (dma) v = fmaf(sebuf[st * kBlock + i], 1.4426950408889634f, v);
+      for (int i = 0; i < 32; ++i) {
+        float v = __uint_as_float(sv[i]) * sl2;
+        if (dma) v = fmaf(sebuf[st * kBlock + col0 + i], 1.4426950408889634f, v);
         z[i] = i < valid ? v : -INFINITY;
         mxp[i & 7] = fmaxf(mxp[i & 7], z[i]);
       }
-      const float mx = act ? fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])))
-                           : -INFINITY;
+      const float mh = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      float mo;
+      if (!exchange(j, mh, mo)) {
+        good = false;
+        break;
+      }
+      const float mx = act ? fmaxf(mh, mo) : -INFINITY;  // the same in both threads of the row
       // raise the reference maximum: at once for a row with nothing accumulated yet, else when it
       // grew by more than the threshold (the row's O scaled in tensor memory, warp by warp)
       float alpha = 1.f;
       if (act && mx > mref) {
-        if (l == 0.f) {
+        if (!started) {
           mref = mx;
         } else if (mx > mref + kTcRescale) {
           alpha = ex2(mref - mx);
           mref = mx;
         }
       }
+      started = started || act;
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
         if (j >= 1 &&
             !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), lim))) {
@@ -863,25 +880,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc::fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {  // this thread's 64 of the row's 128 output columns
           uint32_t ov[32];
-          tc::ld32(trow + 128 + 32 * c, ov);
+          tc::ld32(trow + 128 + 64 * hf + 32 * c, ov);
           tc::wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tc::st32(trow + 128 + 32 * c, ov);
+          tc::st32(trow + 128 + 64 * hf + 32 * c, ov);
         }
         tc::wait_st();
         tc::fence_before();
         l *= alpha;
       }
-      uint32_t pk[32];  // bf16 pairs of the row's 64 probabilities (0 for a block it did not select)
+      uint32_t pk[16];  // bf16 pairs of this half's 32 probabilities (0 for a block the row did not select)
       if (act) {
         float sp[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) sp[k] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
+        for (int i = 0; i < 32; i += 2) {
           const float e0 = ex2(z[i] - mref), e1 = ex2(z[i + 1] - mref);  // 0 for masked tokens
           sp[(i >> 1) & 7] += e0 + e1;
           pk[i >> 1] = pack_bf16x2(e0, e1);
@@ -889,9 +906,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = 0u;
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
       }
-      // the row's P into buffer j & 1 once the product two blocks back has read it
+      // this half of the row's P into buffer j & 1 once the product two blocks back has read it
       const int pb = j & 1;
       if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[pb], (uint32_t)(((j >> 1) - 1) & 1), lim))) {
         good = false;
@@ -899,35 +916,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       unsigned char* prow = sP + pb * 16384 + r * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(prow + ((((col0 >> 3) + c) ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       mbar_arrive(&p_full[pb]);
     }
     if (!good) atomicOr(&bad_flag, 1);
-    // the last product has completed: O / sum for the row
+    // the row's sum from both halves; the last product has completed: O / sum for this half
+    float lo = 0.f;
+    if (!exchange(nu, l, lo)) {
+      good = false;
+      atomicOr(&bad_flag, 1);
+    }
+    const float lrow = l + lo;
     if (__all_sync(0xffffffffu, good) && nu > 0 &&
         !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[(nu - 1) & 1], (uint32_t)(((nu - 1) >> 1) & 1), lim))) {
       good = false;
       atomicOr(&bad_flag, 1);
     }
     tc::fence_after();
-    float O[kHeadDim];
+    float O[64];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t ov[32];
-      tc::ld32(trow + 128 + 32 * c, ov);
+      tc::ld32(trow + 128 + 64 * hf + 32 * c, ov);
       tc::wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; ++i) O[32 * c + i] = __uint_as_float(ov[i]);
     }
     const bool bad = *(volatile int*)&bad_flag != 0 || !good;
     if (row_ok) {
-      uint16_t* orow = out + (((size_t)u * G + h) * n + t) * kHeadDim;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint16_t* orow = out + (((size_t)u * G + h) * n + t) * kHeadDim + 64 * hf;
+      const float inv = lrow > 0.f ? 1.f / lrow : 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

@@ -21,6 +21,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// The same for an MN-major operand wider than one 64-element atom column: lbo = bytes between
+// consecutive 64-element columns along MN (a 16-byte multiple).
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t addr, uint32_t lbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, f32 accumulation: M rows, N columns; B
 // K-major (b_mn = 0: its rows are N, contiguous along K) or MN-major (b_mn = 1: rows are K,
 // contiguous along N).  Fields: accumulator format f32 (bits 4-5 = 1), A and B format bf16 (bits
