@@ -36,6 +36,13 @@ using namespace selcore;
 
 constexpr int kPfMaxWords = 2048 / 32;  // block bitmap words per position (prompts of up to 131,072 tokens)
 
+// 2^x by the special-function unit (relative error about 2^-22; -inf gives 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint64_t* bar) {
   asm volatile(
@@ -53,9 +60,9 @@ constexpr int kPqWarps = 8;
 // grid (ceil(n / (8 PW)), U), 256 threads; dynamic shared memory [8 PW][nbn] pooled scores.
 // Warp w takes positions tw .. tw + PW - 1 (tw = (8 blockIdx.x + w) PW), their q fragments in
 // registers, and walks the unit's compressed keys in 16-window tiles twice (through L1, which the
-// CTA's warps share): the first pass forms, per position and head, the maximum and the sum of exp
-// of z_{h,i} = q_h . K~_i * scale over the windows complete at the position's T (online); the
-// second forms the group softmax summed over the heads per window and max-pools it onto the
+// CTA's warps share): the first pass forms, per position and head, the maximum and the sum of
+// exp of z_{h,i} = q_h . K~_i * scale (base 2) over the windows complete at the position's T
+// (online); the second forms the group softmax summed over the heads per window and max-pools it onto the
 // blocks each window overlaps.  Each position's k_q best candidate blocks (score, then lower
 // block) go to qsel [U][n][nbw] as a bitmap over the blocks (nbw = ceil(nbn / 32) words).  The
 // last position's pooled scores are also the layer's debug scores (sq_blk).
@@ -87,7 +94,7 @@ __global__ void __launch_bounds__(kPqWarps * 32, 1)
   for (int i = lane; i < PW * nbn; i += 32) pooled[i] = 0u;  // +0.0f: group scores are non-negative
   const int ncw = nc[np - 1];  // the warp's last position has the most windows
   const int ntiles = (ncw + 15) >> 4;
-  const float scale = s.scale;
+  const float scale2 = s.scale * 1.4426950408889634f;  // logits in base 2
   const uint16_t* kt = s.kt + (size_t)u * s.nc_max * kHeadDim;
   auto load_tile = [&](int tl, uint4 (&a)[2][4]) {
 #pragma unroll
@@ -128,11 +135,11 @@ __global__ void __launch_bounds__(kPqWarps * 32, 1)
       logits(a, qf[p], acc);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float z0 = w0 < nc[p] ? acc[j] * scale : -INFINITY;
-        const float z1 = w0 + 8 < nc[p] ? acc[2 + j] * scale : -INFINITY;
+        const float z0 = w0 < nc[p] ? acc[j] * scale2 : -INFINITY;
+        const float z1 = w0 + 8 < nc[p] ? acc[2 + j] * scale2 : -INFINITY;
         const float mn = fmaxf(M[p][j], fmaxf(z0, z1));
         if (mn > -INFINITY) {
-          L[p][j] = L[p][j] * expf(M[p][j] - mn) + expf(z0 - mn) + expf(z1 - mn);
+          L[p][j] = (mn > M[p][j] ? L[p][j] * ex2(M[p][j] - mn) : L[p][j]) + ex2(z0 - mn) + ex2(z1 - mn);
           M[p][j] = mn;
         }
       }
@@ -148,7 +155,7 @@ __global__ void __launch_bounds__(kPqWarps * 32, 1)
         const float mo = __shfl_xor_sync(0xffffffffu, M[p][j], o), lo = __shfl_xor_sync(0xffffffffu, L[p][j], o);
         const float mn = fmaxf(M[p][j], mo);
         if (mn > -INFINITY) {
-          L[p][j] = (M[p][j] > -INFINITY ? L[p][j] * expf(M[p][j] - mn) : 0.f) + (mo > -INFINITY ? lo * expf(mo - mn) : 0.f);
+          L[p][j] = (M[p][j] > -INFINITY ? L[p][j] * ex2(M[p][j] - mn) : 0.f) + (mo > -INFINITY ? lo * ex2(mo - mn) : 0.f);
           M[p][j] = mn;
         }
       }
@@ -167,8 +174,8 @@ __global__ void __launch_bounds__(kPqWarps * 32, 1)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         if (2 * t4 + j >= G) continue;
-        if (w0 < nc[p]) e0 += expf(acc[j] * scale - M[p][j]) * inv[p][j];
-        if (w0 + 8 < nc[p]) e1 += expf(acc[2 + j] * scale - M[p][j]) * inv[p][j];
+        if (w0 < nc[p]) e0 += ex2(acc[j] * scale2 - M[p][j]) * inv[p][j];
+        if (w0 + 8 < nc[p]) e1 += ex2(acc[2 + j] * scale2 - M[p][j]) * inv[p][j];
       }
       e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
       e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
@@ -636,13 +643,6 @@ constexpr int kTcThreads = 384;
 constexpr uint32_t kTcCols = 256;  // S buffers at columns 0 and 64, O at 128
 constexpr float kTcRescale = 8.f;  // base-2 growth of a row maximum that forces a rescale
 
-// 2^x by the special-function unit (relative error far below bf16's rounding of the probabilities;
-// -inf gives 0)
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __host__ __device__ inline int tc_positions(int G) { return kTcRows / G; }
 __host__ __device__ inline size_t tc_smem_bytes(int G) {
