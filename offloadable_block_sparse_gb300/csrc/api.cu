@@ -805,11 +805,22 @@ nosa_status nosa_prefill(nosa_ctx* c, int layer, const uint16_t* q, const uint16
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return NOSA_ERR_INVALID_ARG;
   const LayerState s = layer_state(c, layer);
+  // the layer's compressed keys [U][nc_max][d]: boxes of 64 dims x 128 windows
+  CUtensorMap tkt;
+  {
+    cuuint64_t kdims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)s.nc_max, (cuuint64_t)c->U};
+    cuuint64_t kstr[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)s.nc_max * kHeadDim * 2};
+    cuuint32_t kbox[3] = {64, 128, 1};
+    if (enc(&tkt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, s.kt, kdims, kstr, kbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return NOSA_ERR_INVALID_ARG;
+  }
   CK(launch_append_bulk(s, k, v, 0, n_tokens, c->stream));
   uint32_t* qsel = static_cast<uint32_t*>(scratch);
   uint32_t* esel = reinterpret_cast<uint32_t*>(static_cast<unsigned char*>(scratch) + prefill_pick_bytes(c, n_tokens));
-  CK(launch_prefill(s, &tk, &tv, q, k, v, out, qsel, esel, n_tokens, (c->cfg.flags & NOSA_F_TEST_PREFILL_WIDE) != 0,
-                    c->stream));
+  CK(launch_prefill(s, &tk, &tv, &tkt, q, k, v, out, qsel, esel, n_tokens,
+                    (c->cfg.flags & NOSA_F_TEST_PREFILL_WIDE) != 0, c->stream));
   c->T_host[layer] = n_tokens;
   c->sel_T[layer] = n_tokens;
   c->fetch_T[layer] = n_tokens;  // every cache slot holds its block

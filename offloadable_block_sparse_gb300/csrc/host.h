@@ -93,7 +93,9 @@ cudaError_t launch_decode(const LayerState& s, const CUtensorMap* tmap, const ui
 // prompt, attention of every position
 cudaError_t init_prefill();
 int prefill_max_tokens();
-cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
-                           const uint16_t* k, const uint16_t* v, uint16_t* out, uint32_t* qsel, uint32_t* esel, int n,
-                           bool wide, cudaStream_t st);  // wide: the long-prompt forms at any length
+// tk, tv: the prompt's K and V; tkt: the layer's compressed keys [U][nc_max][d] (boxes of 64 dims x
+// 128 windows, 128-byte swizzle)
+cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tkt,
+                           const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, uint32_t* qsel,
+                           uint32_t* esel, int n, bool wide, cudaStream_t st);  // wide: the long-prompt walk at any length
 }  // namespace nosa

@@ -35,6 +35,7 @@ namespace nosa {
 using namespace selcore;
 
 constexpr int kPfMaxWords = 2048 / 32;  // block bitmap words per position (prompts of up to 131,072 tokens)
+constexpr int kTcRowsQ = 128;           // rows of a query-aware tcgen05 tile: positions x q heads
 
 // 2^x by the special-function unit (relative error about 2^-22; -inf gives 0)
 __device__ __forceinline__ float ex2(float x) {
@@ -236,6 +237,264 @@ __global__ void __launch_bounds__(kPqWarps * 32, 1)
     if (t == n - 1)
       for (int b = lane; b < geo.nb; b += 32) s.sq_blk[(size_t)u * s.nb_max + b] = pooled_score(p, b);
   }
+}
+
+// ---------------------------------------------------------------- 2a'. the same on tcgen05
+// A CTA takes PT consecutive positions of one unit (PT <= 128 / G, at most 32, fewer for long
+// prompts: their pooled scores live in shared memory); Q holds their (position, head) rows as an
+// M = 128 operand.  The unit's compressed keys stream through a TMA ring in tiles of 128 windows,
+// twice.  Pass 1: S = Q K~^T (rows (position, head), columns windows) into tensor memory; one
+// thread per row keeps its maximum and sum of exp over the windows complete at its position's T.
+// Pass 2: S^T = K~ Q^T (rows windows, columns (position, head)); one thread per window forms, for
+// each position, the group softmax summed over its heads (maxima and sums of pass 1 from shared
+// memory) and max-pools it onto the blocks the window overlaps (shared-memory atomics).  Then each
+// position's top k_q candidates, as in 2a.  Roles: warp 0 lane 0 issues the MMAs, warp 1 lane 0
+// the loads, warps 4-7 the rows and windows; 256 tensor-memory columns (two 128-column buffers).
+// Used for groups of up to four q heads per kv head, where its 128 rows hold 32 positions; with
+// eight heads a CTA holds only 16 and the per-window pooling (one thread per window, every
+// position) outweighs the MMAs it saves, so those groups take 2a.
+constexpr int kQtMaxGroup = 4;
+constexpr int kQtStages = 3;
+constexpr int kQtThreads = 256;
+constexpr int kQtTileBytes = 128 * 256;  // 128 windows x 128 dims bf16
+
+__host__ __device__ inline int qt_positions(int G, int nbn) {
+  const int by_rows = kTcRowsQ / G < 32 ? kTcRowsQ / G : 32;
+  const int by_smem = 16384 / nbn;  // pooled scores: PT x nbn floats <= 64 KiB
+  return by_rows < by_smem ? by_rows : (by_smem > 0 ? by_smem : 1);
+}
+__host__ __device__ inline size_t qt_smem_bytes(int PT, int nbn) {
+  return 1024 + 32768 + (size_t)kQtStages * kQtTileBytes + (size_t)PT * nbn * 4 + 2 * 128 * 4 + 4 * kPfMaxWords * 4 + 32 * 4;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kQtThreads, 1)
+    prefill_query_tc_kernel(const __grid_constant__ CUtensorMap tkt, LayerState s, const uint16_t* __restrict__ q,
+                            uint32_t* __restrict__ qsel, int n, int nbn, int PT) {
+  extern __shared__ unsigned char qsm_raw[];
+  __shared__ __align__(8) uint64_t full[kQtStages], empty[kQtStages], s_full[2], s_free[2], stats_bar, pool_bar,
+      drain;
+  __shared__ uint32_t tbase;
+  __shared__ int bad_flag;
+  unsigned char* sm =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(qsm_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = sm;                                     // [2 dim halves][128 rows][128 B]
+  unsigned char* sT = sQ + 32768;                             // [stage][2 dim halves][128 windows][128 B]
+  uint32_t* pooled = reinterpret_cast<uint32_t*>(sT + kQtStages * kQtTileBytes);  // [PT][nbn] float bits
+  float* colM = reinterpret_cast<float*>(pooled + (size_t)PT * nbn);  // per (position, head) row
+  float* colI = colM + 128;
+  uint32_t* qw_all = reinterpret_cast<uint32_t*>(colI + 128);  // [4 warps][kPfMaxWords]
+  int* ncp = reinterpret_cast<int*>(qw_all + 4 * kPfMaxWords); // windows complete at each position
+  const int u = blockIdx.x, t0 = blockIdx.y * PT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int np = min(PT, n - t0);
+  const int kq = s.k_q;
+  const long long lim = s.wait_limit;
+  const float scale2 = s.scale * 1.4426950408889634f;  // logits in base 2
+  if (tid == 0) {
+    prefetch_tmap(&tkt);
+    for (int i = 0; i < kQtStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 128);
+    }
+    mbar_init(&stats_bar, 128);
+    mbar_init(&pool_bar, 128);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+    bad_flag = 0;
+  }
+  if (warp == 0) tc::alloc(&tbase, 256);
+  pdl_wait();  // the bulk append wrote the compressed keys
+  for (int i = tid; i < PT * nbn; i += kQtThreads) pooled[i] = 0u;  // +0.0f: group scores are non-negative
+  if (tid < 32) ncp[tid] = tid < np ? geometry(t0 + tid + 1, s.nw, s.sink).nc : 0;
+  // Q rows (position p, head h) in the 128-byte swizzle; rows past PT G are zero
+  for (int idx = tid; idx < 128 * 16; idx += kQtThreads) {
+    const int r = idx >> 4, c = idx & 15, p = r / G, h = r % G;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (p < np) v = *reinterpret_cast<const uint4*>(q + (((size_t)u * G + h) * n + t0 + p) * kHeadDim + 8 * c);
+    *reinterpret_cast<uint4*>(sQ + (c >> 3) * 16384 + r * 128 + ((((c & 7) ^ (r & 7)) & 7) << 4)) = v;
+  }
+  fence_proxy_async_smem();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tm = tbase;
+  const int ncmax = geometry(t0 + np, s.nw, s.sink).nc;  // the last position's windows
+  const int ntile = (ncmax + 127) / 128, nitem = 2 * ntile;  // pass 1 over the tiles, then pass 2
+  const uint32_t sQa = smem_u32(sQ), sTa = smem_u32(sT);
+  constexpr uint32_t idS = tc::f16_idesc(128, 128, 0);
+
+  if (warp == 1 && lane == 0) {  // TMA producer
+    int issued = 0;
+    for (int i = 0; i < nitem; ++i) {
+      const int st = i % kQtStages, tile = i % ntile;
+      if (i >= kQtStages && !mbar_wait_bounded(&empty[st], (uint32_t)(((i / kQtStages) - 1) & 1), lim)) {
+        atomicOr(&bad_flag, 1);
+        break;
+      }
+      if (*(volatile int*)&bad_flag) break;
+      const uint32_t dst = sTa + st * kQtTileBytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&full[st], kQtTileBytes);
+      tma_load_3d(dst, &tkt, 0, 128 * tile, u, &full[st]);
+      tma_load_3d(dst + 16384, &tkt, 64, 128 * tile, u, &full[st]);
+      issued = i + 1;
+    }
+    for (int i = max(issued - kQtStages, 0); i < issued; ++i)
+      mbar_wait_bounded(&full[i % kQtStages], (uint32_t)((i / kQtStages) & 1), kWaitCycles);
+  } else if (warp == 0 && lane == 0) {  // MMA issuer
+    bool ok = true;
+    for (int i = 0; i < nitem && ok; ++i) {
+      const int st = i % kQtStages, sb = i & 1;
+      if (!mbar_wait_bounded(&full[st], (uint32_t)((i / kQtStages) & 1), lim) ||
+          (i >= 2 && !mbar_wait_bounded(&s_free[sb], (uint32_t)(((i >> 1) - 1) & 1), lim))) {
+        ok = false;
+        break;
+      }
+      tc::fence_after();
+      const uint32_t kb = sTa + st * kQtTileBytes;
+      const bool pass1 = i < ntile;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {  // dims 16 kk .. 16 kk + 15: halves at +0 and +16384
+        const uint32_t off = (uint32_t)(kk >> 2) * 16384 + (uint32_t)(kk & 3) * 32;
+        const uint64_t dq = tc::sw128_desc(sQa + off), dk = tc::sw128_desc(kb + off);
+        tc::mma_bf16(tm + 128 * sb, pass1 ? dq : dk, pass1 ? dk : dq, idS, kk > 0);
+      }
+      tc::commit(&s_full[sb]);
+      tc::commit(&empty[st]);
+    }
+    if (!ok) atomicOr(&bad_flag, 1);
+    tc::commit(&drain);
+    mbar_wait_bounded(&drain, 0u, kWaitCycles);
+  } else if (warp >= 4) {  // rows (pass 1) and windows (pass 2)
+    const int r = tid - 128;
+    const uint32_t trow = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int pr = r / G;                      // pass 1: this row's position
+    const bool row_ok = pr < np;
+    const int ncr = row_ok ? ncp[pr] : 0;
+    float m = -INFINITY, l = 0.f;
+    bool good = true;
+    for (int i = 0; i < nitem; ++i) {
+      const int sb = i & 1, tile = i % ntile;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[sb], (uint32_t)((i >> 1) & 1), lim))) {
+        good = false;
+        break;
+      }
+      tc::fence_after();
+      uint32_t v[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::ld32(trow + 128 * sb + 32 * c, v[c]);
+      tc::wait_ld();
+      tc::fence_before();
+      mbar_arrive(&s_free[sb]);
+      if (i < ntile) {  // pass 1: row (position, head) over this tile's 128 windows
+        if (row_ok) {
+          float mxp[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            const float z = 128 * tile + c < ncr ? __uint_as_float(v[c >> 5][c & 31]) * scale2 : -INFINITY;
+            mxp[c & 7] = fmaxf(mxp[c & 7], z);
+          }
+          const float mt = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+          if (mt > -INFINITY) {
+            const float mn = fmaxf(m, mt);
+            float sp[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (128 * tile + c < ncr) sp[c & 7] += ex2(__uint_as_float(v[c >> 5][c & 31]) * scale2 - mn);
+            const float st = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            l = (mn > m ? l * ex2(m - mn) : l) + st;
+            m = mn;
+          }
+        }
+        if (i == ntile - 1) {  // the row's statistics for pass 2
+          colM[r] = m;
+          colI[r] = l > 0.f ? 1.f / l : 0.f;
+          mbar_arrive(&stats_bar);
+          if (!__all_sync(0xffffffffu, mbar_wait_bounded(&stats_bar, 0u, lim))) {
+            good = false;
+            break;
+          }
+        }
+      } else {  // pass 2: window w of the tile, columns (position, head)
+        const int w = 128 * tile + r;
+        float gs[128 / G < 32 ? 128 / G : 32];
+#pragma unroll
+        for (int pp = 0; pp < (128 / G < 32 ? 128 / G : 32); ++pp) gs[pp] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int pp = c / G;
+          if (pp < (128 / G < 32 ? 128 / G : 32) && pp < np && w < ncp[pp])
+            gs[pp] += ex2(__uint_as_float(v[c >> 5][c & 31]) * scale2 - colM[c]) * colI[c];
+        }
+        // window w overlaps blocks (w + 1) / 4 and, when w = 4 b + 3, also b = (w + 1) / 4 - 1
+        const int b1 = (w + 1) >> 2;
+#pragma unroll
+        for (int pp = 0; pp < (128 / G < 32 ? 128 / G : 32); ++pp) {
+          if (pp >= np || w >= ncp[pp]) continue;
+          const uint32_t bits = __float_as_uint(gs[pp]);
+          if (b1 < nbn) atomicMax(&pooled[pp * nbn + b1], bits);
+          if (((w + 1) & 3) == 0 && b1 >= 1) atomicMax(&pooled[pp * nbn + b1 - 1], bits);
+        }
+      }
+    }
+    if (!good) atomicOr(&bad_flag, 1);
+    // every window's contribution pooled: each position's top k_q candidates (warps 4-7 in turn)
+    mbar_arrive(&pool_bar);
+    const bool pooled_ok = __all_sync(0xffffffffu, mbar_wait_bounded(&pool_bar, 0u, lim));
+    if (!pooled_ok) atomicOr(&bad_flag, 1);
+    const int nbw = (nbn + 31) >> 5;
+    uint32_t* qw = qw_all + (warp - 4) * kPfMaxWords;
+    for (int pp = warp - 4; pp < np; pp += 4) {
+      const int t = t0 + pp;
+      const Geometry geo = geometry(t + 1, s.nw, s.sink);
+      auto score = [&](int b) {
+        return (geo.nc >= 1 && 4 * b <= geo.nc) ? __uint_as_float(pooled[pp * nbn + b]) : -INFINITY;
+      };
+      for (int w = lane; w < nbw; w += 32) qw[w] = 0u;
+      __syncwarp();
+      const int c0 = s.sink, c1 = geo.ws;  // candidates [c0, c1)
+      unsigned long long thr = ~0ull;
+      for (int got = 0; got < kq; got += 32) {
+        unsigned long long best = 0ull;
+        for (int bb = c0; bb < c1; bb += 32) {
+          const int b = bb + lane;
+          unsigned long long x = 0ull;
+          if (b < c1) {
+            x = rank_key(orderable(score(b)), b);
+            if (x >= thr) x = 0ull;
+          }
+          best = warp_merge_top(best, warp_sort_desc(x));
+        }
+        if (best && lane < kq - got) {
+          const int b = (int)(0xFFFFFFFFu - (uint32_t)best);
+          atomicOr(&qw[b >> 5], 1u << (b & 31));
+        }
+        thr = __shfl_sync(0xffffffffu, best, 31);
+        if (thr == 0ull) break;
+      }
+      __syncwarp();
+      uint32_t* row = qsel + ((size_t)u * n + t) * nbw;
+      for (int w = lane; w < nbw; w += 32) row[w] = (*(volatile int*)&bad_flag) ? 0u : qw[w];
+      __syncwarp();
+      if (t == n - 1)
+        for (int b = lane; b < geo.nb; b += 32) s.sq_blk[(size_t)u * s.nb_max + b] = score(b);
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (tid == 0 && bad_flag) atomicOr(s.err, kErrTimeout);
+  if (warp == 0) tc::dealloc(tm, 256);
 }
 
 // ---------------------------------------------------------------- 2b. the walk over the positions
@@ -983,6 +1242,12 @@ cudaError_t init_prefill() {
   const int nbn = kPfMaxWords * 32;
   cudaError_t e = cudaFuncSetAttribute(prefill_attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)tc_smem_bytes(1));
+  const int qt_max = (int)qt_smem_bytes(32, 512);  // the largest PT x nbn (16384 floats)
+#define NOSA_QT_ATTR(GG)                                                                                      \
+  if (e == cudaSuccess)                                                                                       \
+    e = cudaFuncSetAttribute(prefill_query_tc_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, qt_max);
+  NOSA_QT_ATTR(1) NOSA_QT_ATTR(2) NOSA_QT_ATTR(3) NOSA_QT_ATTR(4)
+#undef NOSA_QT_ATTR
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(prefill_query_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)query_smem(1024, 4));
@@ -992,18 +1257,33 @@ cudaError_t init_prefill() {
   return e;  // the walk's shared memory (4 x walk_warp_bytes) stays under the default 48 KiB
 }
 
-cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const uint16_t* q,
-                           const uint16_t* k, const uint16_t* v, uint16_t* out, uint32_t* qsel, uint32_t* esel, int n,
-                           bool wide, cudaStream_t st) {
+cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tkt,
+                           const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* out, uint32_t* qsel,
+                           uint32_t* esel, int n, bool wide, cudaStream_t st) {
   const int nbn = (n + kBlock - 1) / kBlock;
   wide = wide || prefill_wide(nbn);
-  const int pw = wide ? 2 : 4;
-  const dim3 qgrid((n + kPqWarps * pw - 1) / (kPqWarps * pw), s.U);
-  cudaError_t e =
-      pw == 4 ? launch_ex(prefill_query_kernel<4>, qgrid, dim3(kPqWarps * 32), query_smem(nbn, 4), st, true, 0, s, q,
-                          qsel, n, nbn)
-              : launch_ex(prefill_query_kernel<2>, qgrid, dim3(kPqWarps * 32), query_smem(nbn, 2), st, true, 0, s, q,
-                          qsel, n, nbn);
+  cudaError_t e;
+  if (s.G <= kQtMaxGroup) {  // tensor-core scores: 128 rows of (position, q head) per CTA
+    const int qpt = qt_positions(s.G, nbn);
+    const dim3 qgrid(s.U, (n + qpt - 1) / qpt);
+    const size_t qsm = qt_smem_bytes(qpt, nbn);
+#define NOSA_QT(GG) \
+  launch_ex(prefill_query_tc_kernel<GG>, qgrid, dim3(kQtThreads), qsm, st, true, 0, *tkt, s, q, qsel, n, nbn, qpt)
+    switch (s.G) {
+      case 1: e = NOSA_QT(1); break;
+      case 2: e = NOSA_QT(2); break;
+      case 3: e = NOSA_QT(3); break;
+      default: e = NOSA_QT(4); break;
+    }
+#undef NOSA_QT
+  } else {  // larger groups: one warp's positions with all their heads on mma.sync
+    const int pw = wide ? 2 : 4;
+    const dim3 qgrid((n + kPqWarps * pw - 1) / (kPqWarps * pw), s.U);
+    e = pw == 4 ? launch_ex(prefill_query_kernel<4>, qgrid, dim3(kPqWarps * 32), query_smem(nbn, 4), st, true, 0, s,
+                            q, qsel, n, nbn)
+                : launch_ex(prefill_query_kernel<2>, qgrid, dim3(kPqWarps * 32), query_smem(nbn, 2), st, true, 0, s,
+                            q, qsel, n, nbn);
+  }
   if (e != cudaSuccess) return e;
   // list entries and bitmap words per lane: as few as the configuration allows
   const int need = s.k_q + s.k_e + 1;

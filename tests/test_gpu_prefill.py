@@ -223,6 +223,16 @@ def test_prefill_ragged_group4_dma_bias(tile):
     run_prefill(wl, 1001, units, set(range(1001)), flags=N.NOSA_F_DMA_BIAS | tile, decode_steps=3)
 
 
+@pytest.mark.parametrize("hq", [2, 4, 6], ids=["group1", "group2", "group3"])
+def test_prefill_small_groups(hq):
+    # 1, 2 and 3 q heads per kv head: the tensor-core query-aware scores with 32, 64 and 96 of
+    # their 128 rows in use, and the attention's last rows idle when 128 is not a multiple of G
+    wl = syn.Workload(f"pf_g{hq // 2}", layers=1, batch=2, q_heads=hq, kv_heads=2, context=0, k_q=4, k_e=6,
+                      window_tokens=128, steps=1203, sigma=1.0)
+    units = [(b, g) for b in range(2) for g in range(2)]
+    run_prefill(wl, 1200, units, set(range(0, 1200, 3)) | {1199}, decode_steps=2)
+
+
 @pytest.mark.parametrize("window", [0, 64], ids=["no-window", "one-block-window"])
 def test_prefill_short_window(window):
     # with a window of fewer than two blocks the last two blocks are candidates, whose pooled
@@ -264,6 +274,18 @@ def test_prefill_70k_prompt_long_forms():
     scored = set(range(0, n, 4999)) | {65535, 65536, 65600, n - 1}
     out = set(range(0, n, 997)) | {n - 1}
     run_prefill(wl, n, [(0, 0)], out, decode_steps=2, score_positions=scored)
+
+
+def test_prefill_40k_prompt_group4():
+    # the 8B-shaped group (32/8 heads: 4 per kv head) over 40,000 tokens (625 blocks): the
+    # tensor-core query-aware scores keep fewer positions per CTA (26) so that their pooled
+    # scores fit in shared memory, the last CTA ragged
+    n = 40000
+    wl = syn.Workload("pf40k_g4", layers=1, batch=1, q_heads=8, kv_heads=2, context=0, k_q=16, k_e=48,
+                      window_tokens=1024, steps=n + 2, sigma=0.3)
+    scored = set(range(0, n, 3001)) | {25, 26, 27, 51, 52, n - 1}
+    out = set(range(0, n, 499)) | {n - 1}
+    run_prefill(wl, n, [(0, 1)], out, decode_steps=2, score_positions=scored)
 
 
 def test_prefill_argument_checks():
