@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--k-q", type=int, default=None)
     ap.add_argument("--gather-ctas", type=int, default=0)
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (only for host-memory limits)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="fewer sequences than the workload's batch (--prefill only: small cases for profiling)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--dma-bias", action="store_true", help="attention adds each token's eviction score (DMA bias)")
     ap.add_argument("--dense", action="store_true",
@@ -778,6 +780,8 @@ def run_prefill(args, rank, world, local_rank):
     from synth import inputs as syn
     torch.cuda.set_device(local_rank)
     over = {"sigma": args.sigma} if args.sigma is not None else {}
+    if args.batch:
+        over["batch"] = args.batch
     wl = syn.workload(args.workload, **over)
     L = args.layers or wl.layers
     B, Hq, Hkv, d, n = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.context
@@ -860,6 +864,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.batch and not args.prefill:
+        raise SystemExit("--batch applies to --prefill only")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kQtThreads, 1)
   float* colI = colM + 128;
   uint32_t* qw_all = reinterpret_cast<uint32_t*>(colI + 128);  // [4 warps][kPfMaxWords]
   int* ncp = reinterpret_cast<int*>(qw_all + 4 * kPfMaxWords); // windows complete at each position
-  const int u = blockIdx.x, t0 = blockIdx.y * PT;
+  const int u = blockIdx.y, t0 = blockIdx.x * PT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int np = min(PT, n - t0);
   const int kq = s.k_q;
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* bm = reinterpret_cast<uint32_t*>(sP + 2 * 16384);  // [PT][kPfMaxWords]
   int16_t* ublk = reinterpret_cast<int16_t*>(bm + PT * kPfMaxWords);  // union, ascending
   float* sebuf = reinterpret_cast<float*>(ublk + kPfMaxWords * 32);   // [stage][64]
-  const int u = blockIdx.x, t0 = blockIdx.y * PT;
+  const int u = blockIdx.y, t0 = blockIdx.x * PT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int np = min(PT, n - t0);
   const int nb_last = (t0 + np + kBlock - 1) / kBlock;  // blocks of the last position's context
@@ -1265,7 +1265,9 @@ cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUt
   cudaError_t e;
   if (s.G <= kQtMaxGroup) {  // tensor-core scores: 128 rows of (position, q head) per CTA
     const int qpt = qt_positions(s.G, nbn);
-    const dim3 qgrid(s.U, (n + qpt - 1) / qpt);
+    // positions along x: the CTAs resident at once take consecutive positions of one unit and
+    // share its compressed keys in L2
+    const dim3 qgrid((n + qpt - 1) / qpt, s.U);
     const size_t qsm = qt_smem_bytes(qpt, nbn);
 #define NOSA_QT(GG) \
   launch_ex(prefill_query_tc_kernel<GG>, qgrid, dim3(kQtThreads), qsm, st, true, 0, *tkt, s, q, qsel, n, nbn, qpt)
@@ -1305,7 +1307,9 @@ cudaError_t launch_prefill(const LayerState& s, const CUtensorMap* tk, const CUt
   e = launch_ex(prefill_refresh_kernel, dim3(s.cap, s.U), dim3(256), 0, st, true, 0, s, k, v, n);
   if (e != cudaSuccess) return e;
   const int pt = tc_positions(s.G);
-  return launch_ex(prefill_attend_tc_kernel, dim3(s.U, (n + pt - 1) / pt), dim3(kTcThreads), tc_smem_bytes(s.G), st,
+  // positions along x, as above: neighbouring positions' selections overlap, so the CTAs resident at
+  // once read the same unit's blocks and most of them come from L2
+  return launch_ex(prefill_attend_tc_kernel, dim3((n + pt - 1) / pt, s.U), dim3(kTcThreads), tc_smem_bytes(s.G), st,
                    true, 0, *tk, *tv, s, q, out, qs, static_cast<const uint32_t*>(esel), n);
 }
 
