@@ -33,10 +33,18 @@ Readings taken where the pages leave a step open:
     never again eligible for the query-agnostic part; the query-aware part may
     still recall it.  With fewer than k_e eligible blocks the query-agnostic part
     comes up short.
-  * the cache holds exactly the blocks of the last selection; a selected block
-    without a slot is fetched (this includes a newly started tail block and, on
-    the first step after a bulk context load, every selected block); freed and
-    free slots are handed out in ascending order to new blocks in ascending order.
+  * the block cache has at least as many slots as a selection has blocks (as many
+    is the pages' cache: exactly the last selection).  A selected block without a
+    slot is fetched (this includes a newly started tail block and, on the first
+    step after a bulk context load, every selected block).  The new blocks, in
+    ascending order, take the slots that hold no selected block, least recently
+    selected first (an empty slot counts as never selected; ties to the lower
+    slot), those slots in ascending order; blocks in the other slots stay cached
+    for later steps.  With exactly as many slots as the selection, the slots taken
+    are those whose block left the selection.
+  * after a sparse prefill the cache holds exactly the prompt's last selection,
+    its i-th block (ascending) in slot i (every block of it was just written from
+    the prompt, so nothing earlier is worth keeping).
   * by default no DMA attention bias in the attention step (eq. 8 prints none);
     as an option (UnitOracle(dma_bias=True)) each token's eviction score s^e_j
     is added to its scaled logit q.k_j / sqrt(d), the additive bias of DMA that
@@ -174,25 +182,34 @@ def select_query_agnostic(se_blk, candidates, Q, evicted, k_e):
     return top_k(np.asarray(se_blk, np.float64).astype(np.float32), eligible, k_e)
 
 
-def assign_slots(S, slot_blk):
-    """Set difference of the new selection against the cached blocks.
+def assign_slots(S, slot_blk, last_used=None, T=0):
+    """Set difference of the selection S, made at context length T, against the block cache.
 
-    Slots whose block left the selection are freed; selected blocks with no slot
-    are new and get the free slots, both taken in ascending order.  Returns the
-    fetch list [(block, slot)], the new slot map and the slot of every block of S.
+    slot_blk: the block in each slot (-1: empty); last_used: the context length of the last
+    selection that held each slot's block (-1: never; None: all -1).  Selected blocks with no
+    slot are new.  In ascending order they take the slots that hold no selected block, least
+    recently selected first (ties to the lower slot), those slots in ascending order; the
+    other slots keep their blocks.  Every slot holding a block of S is marked selected at T.
+    Returns the fetch list [(block, slot)], the new slot map, the new marks and the slot of
+    every block of S.
     """
     keep = set(S)
+    n = len(slot_blk)
+    lu = [-1] * n if last_used is None else list(last_used)
     resident = {b for b in slot_blk if b >= 0}
-    new_map = [b if (b >= 0 and b in keep) else -1 for b in slot_blk]
-    free = [s for s, b in enumerate(new_map) if b < 0]
     new_blocks = [b for b in S if b not in resident]
-    if len(new_blocks) > len(free):
+    open_slots = [s for s in range(n) if not (slot_blk[s] >= 0 and slot_blk[s] in keep)]
+    if len(new_blocks) > len(open_slots):
         raise ValueError("block cache too small for the selection")
-    fetch = list(zip(new_blocks, free[:len(new_blocks)]))
+    taken = sorted(sorted(open_slots, key=lambda s: (lu[s], s))[:len(new_blocks)])
+    new_map = list(slot_blk)
+    fetch = list(zip(new_blocks, taken))
     for b, s in fetch:
         new_map[s] = b
     where = {b: s for s, b in enumerate(new_map) if b >= 0}
-    return fetch, new_map, [where[b] for b in S]
+    for b in S:
+        lu[where[b]] = T
+    return fetch, new_map, lu, [where[b] for b in S]
 
 
 def sparse_attention(Qg, K, V, S, T, scale, block=64, bias=None):
@@ -227,11 +244,15 @@ class UnitOracle:
     """State and steps of one (layer, batch, kv-head) unit, computed from its raw inputs."""
 
     def __init__(self, *, head_dim=128, block=64, kernel=32, stride=16, k_q, k_e,
-                 sink_blocks=1, window_tokens, max_context, W1, W2, scale=None, dma_bias=False):
+                 sink_blocks=1, window_tokens, max_context, W1, W2, scale=None, dma_bias=False,
+                 cache_slots=None):
         self.d, self.block, self.kernel, self.stride = head_dim, block, kernel, stride
         self.k_q, self.k_e, self.sink = k_q, k_e, sink_blocks
         self.nw = window_tokens // block
         self.cap = sink_blocks + self.nw + k_q + k_e
+        self.cslots = self.cap if not cache_slots else cache_slots
+        if self.cslots < self.cap:
+            raise ValueError("the block cache must hold a whole selection")
         self.scale = 1.0 / math.sqrt(head_dim) if not scale else scale
         self.dma_bias = dma_bias  # attention logits get each token's eviction score added
         self.W1 = np.asarray(W1, np.float64)
@@ -242,7 +263,8 @@ class UnitOracle:
         self.Kt = np.zeros((num_windows(max_context, kernel, stride), head_dim))
         self.T = 0
         self.evicted: set[int] = set()
-        self.slot_blk = [-1] * self.cap
+        self.slot_blk = [-1] * self.cslots
+        self.last_used = [-1] * self.cslots
         self.S_prev: list[int] | None = None
         self.steps = 0
 
@@ -295,17 +317,24 @@ class UnitOracle:
     # -- a3/a4: commit a selection: eviction update, set difference, slots (for a context of T tokens,
     # by default the current one)
     def commit(self, Q, E, T=None):
-        sink, C, win = partition(self.T if T is None else T, self.nw, self.sink, self.block)
+        T = self.T if T is None else T
+        sink, C, win = partition(T, self.nw, self.sink, self.block)
         D = sorted(set(Q) | set(E))
         S = sorted(set(sink) | set(D) | set(win))
         Dset = set(D)
         self.evicted |= {b for b in C if b not in Dset}
-        fetch, self.slot_blk, slot_of = assign_slots(S, self.slot_blk)
+        fetch, self.slot_blk, self.last_used, slot_of = assign_slots(S, self.slot_blk, self.last_used, T)
         gamma = None if self.S_prev is None else locality(D, self.S_prev)
         self.S_prev = S
         self.steps += 1
         return dict(S=S, D=D, fetch=fetch, slot_of=slot_of, gamma=gamma,
                     short=max(0, self.k_e - len(E)))
+
+    # -- the cache after a sparse prefill: the last selection, block i of it in slot i
+    def settle_cache(self):
+        S = self.S_prev or []
+        self.slot_blk = list(S) + [-1] * (self.cslots - len(S))
+        self.last_used = [self.T] * len(S) + [-1] * (self.cslots - len(S))
 
     # -- a6: attention over the selection
     def attend(self, q_bits, S):

@@ -235,12 +235,12 @@ def test_partition_sink_window_candidates():
 
 
 # ----------------------------------------------------------------------------- a unit over many steps
-def _run_unit(T0, steps, k_q, k_e, window, sigma, seed, G=2, d=32, kernel=32):
+def _run_unit(T0, steps, k_q, k_e, window, sigma, seed, G=2, d=32, kernel=32, cache_slots=None):
     w = syn.Workload("t", 1, 1, G, 1, T0, k_q, k_e, window, steps, sigma=sigma, head_dim=d,
                      evict_hidden=16, seed=seed)
     x = w.unit_inputs(0, 0, 0)
     u = O.UnitOracle(head_dim=d, k_q=k_q, k_e=k_e, window_tokens=window,
-                     max_context=T0 + steps, W1=x["W1"], W2=x["W2"])
+                     max_context=T0 + steps, W1=x["W1"], W2=x["W2"], cache_slots=cache_slots)
     u.append(x["K"][:T0], x["V"][:T0])
     res = []
     for t in range(steps):
@@ -288,10 +288,14 @@ def test_eviction_is_sticky_and_fetches_follow_the_set_difference():
     u, x, res = _run_unit(1500, 90, k_q, k_e, 128, 1.0, 5)
     dropped = set()
     S_prev = []
+    cached = [-1] * u.cslots  # the slot map, replayed from the fetch lists
     for t, r in enumerate(res):
         assert not (set(r["E"]) & dropped)                       # never re-selected by E
         fetched = [b for b, _ in r["fetch"]]
-        assert fetched == sorted(set(r["S"]) - set(S_prev))      # exactly the new blocks
+        assert fetched == sorted(set(r["S"]) - set(cached))      # exactly the selected blocks not cached
+        assert set(fetched) <= set(r["S"]) - set(S_prev)
+        for b, sl in r["fetch"]:
+            cached[sl] = b
         if t > 0:
             assert len(set(r["D"]) - set(S_prev)) <= k_q         # only Q can bring new dynamic blocks
         slots = r["slot_of"]
@@ -300,6 +304,26 @@ def test_eviction_is_sticky_and_fetches_follow_the_set_difference():
         dropped |= {b for b in C if b not in set(r["D"])}
         S_prev = r["S"]
     assert len(res[0]["fetch"]) == len(res[0]["S"])              # cold first step fetches all of S_1
+
+
+def test_a_larger_cache_changes_only_the_transfers():
+    # twice the selection's slots: the same selections, eviction and outputs, fewer fetches; a
+    # selected block is fetched exactly when it holds no slot, and every slot holds a distinct block
+    k_q, k_e = 4, 12
+    u1, _, r1 = _run_unit(2048, 60, k_q, k_e, 256, 1.0, 4)
+    u2, _, r2 = _run_unit(2048, 60, k_q, k_e, 256, 1.0, 4, cache_slots=2 * (1 + 4 + k_q + k_e))
+    assert u2.cslots == 2 * u1.cap
+    cached = [-1] * u2.cslots
+    for a, b in zip(r1, r2):
+        assert a["S"] == b["S"] and a["D"] == b["D"] and a["gamma"] == b["gamma"]
+        assert np.array_equal(a["out"], b["out"])
+        assert [x for x, _ in b["fetch"]] == [x for x in b["S"] if x not in set(cached)]
+        for x, sl in b["fetch"]:
+            cached[sl] = x
+        assert sorted(cached[sl] for sl in b["slot_of"]) == b["S"]
+    assert u1.evicted == u2.evicted
+    n1, n2 = sum(len(r["fetch"]) for r in r1), sum(len(r["fetch"]) for r in r2)
+    assert n2 < n1
 
 
 def test_budget_accounting_and_transfer_unit():
@@ -469,9 +493,44 @@ def test_unit_dma_bias_is_the_eviction_score_of_each_token():
 
 
 def test_assign_slots_pairs_ascending():
-    fetch, m, where = O.assign_slots([0, 3, 4, 9], [3, -1, 7, 0, 8])
-    # slot 2 (block 7) and 4 (block 8) are freed; free slots 1, 2, 4; new blocks 4, 9
-    assert fetch == [(4, 1), (9, 2)] and m == [3, 4, 9, 0, -1] and where == [3, 0, 1, 2]
+    fetch, m, lu, where = O.assign_slots([0, 3, 4, 9], [3, -1, 7, 0, 8], T=5)
+    # open slots 1 (empty), 2 (block 7) and 4 (block 8), none selected before: the two lowest
+    # go to the new blocks 4 and 9; block 8 stays cached in slot 4
+    assert fetch == [(4, 1), (9, 2)] and m == [3, 4, 9, 0, 8] and where == [3, 0, 1, 2]
+    assert lu == [5, 5, 5, 5, -1]
+
+
+def test_assign_slots_replaces_the_least_recently_selected():
+    # four slots, worked by hand: a block that left the selection stays cached while slots
+    # selected longer ago (or never) are free to take, and comes back without a fetch
+    m, lu = [-1] * 4, None
+    fetch, m, lu, where = O.assign_slots([0, 1], m, lu, T=10)
+    assert fetch == [(0, 0), (1, 1)] and m == [0, 1, -1, -1] and lu == [10, 10, -1, -1]
+    fetch, m, lu, where = O.assign_slots([0, 2], m, lu, T=11)   # empty slots before block 1's
+    assert fetch == [(2, 2)] and m == [0, 1, 2, -1] and lu == [11, 10, 11, -1]
+    fetch, m, lu, where = O.assign_slots([0, 3, 4], m, lu, T=12)  # slot 3 (never), slot 1 (T 10)
+    assert fetch == [(3, 1), (4, 3)] and m == [0, 3, 2, 4] and lu == [12, 12, 11, 12] and where == [0, 1, 3]
+    fetch, m, lu, where = O.assign_slots([0, 1, 2], m, lu, T=13)  # block 2 still cached
+    assert fetch == [(1, 1)] and m == [0, 1, 2, 4] and lu == [13, 13, 13, 12] and where == [0, 1, 2]
+
+
+def test_assign_slots_with_a_selection_sized_cache_frees_exactly_the_blocks_that_left():
+    # the pages' cache (as many slots as a full selection): written out directly, freed slots
+    # (ascending) paired with new blocks (ascending) -- the same fetch lists and slot maps
+    rng = np.random.default_rng(3)
+    cap, m, lu, ref = 6, [-1] * 6, None, [-1] * 6
+    for T in range(40):
+        S = sorted(rng.choice(20, size=cap, replace=False).tolist())
+        fetch, m, lu, where = O.assign_slots(S, m, lu, T)
+        keep = set(S)
+        resident = {b for b in ref if b >= 0}
+        ref = [b if b in keep else -1 for b in ref]
+        free = [s for s, b in enumerate(ref) if b < 0]
+        new = [b for b in S if b not in resident]
+        want = list(zip(new, free))
+        for b, s in want:
+            ref[s] = b
+        assert fetch == want and m == ref
 
 
 # ----------------------------------------------------------------------------- inputs
