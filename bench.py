@@ -83,7 +83,7 @@ def parse():
     ap.add_argument("--quick", action="store_true", help="timed graph leg only (profiling runs)")
     # kernel sizing overrides (nosa_config fields; 0 = the library's rule)
     for f in ("score-ctas", "attend-blocks-per-cta", "attend-merge", "decode-cluster", "decode-teams",
-              "decode-stages", "forecast-streams"):
+              "decode-stages", "forecast-streams", "cache-slots"):
         ap.add_argument(f"--{f}", type=int, default=0)
     ap.add_argument("--unfused", action="store_true", help="three-kernel step even where the fused kernel fits")
     ap.add_argument("--prefill", action="store_true",
@@ -234,7 +234,7 @@ def oracle_baseline(wl, seconds, total_units):
 def sizing_overrides(args):
     """nosa_config sizing fields set on the command line (0 = the library's rule)."""
     return {k: getattr(args, k) for k in ("score_ctas", "attend_blocks_per_cta", "attend_merge", "decode_cluster",
-                                          "decode_teams", "decode_stages", "forecast_streams")}
+                                          "decode_teams", "decode_stages", "forecast_streams", "cache_slots")}
 
 
 def workload_config(wl, args, layers, world):
@@ -418,7 +418,8 @@ def run_native(args, rank, world, local_rank):
               "dtype": "bf16", "data": "synthetic",
               "config": workload_config(wl, args, L, world),
               "plan": {"cuda_graph": use_graph, "gather_ctas": args.gather_ctas or (16 if B < 32 else 32),
-                       "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster},
+                       "step_kernels_per_layer": step_kernels, "decode_cluster": decode_cluster,
+                       "cache_slots": sizes.cache_slots, "select_slots": sizes.select_slots},
               # forecast: forecast select and gather (prefetch stream), append, attention, merge
               "gpu_launches": (5 if fc else step_kernels) * L * K,
               "clocks": ck,
@@ -787,8 +788,28 @@ def run_prefill(args, rank, world, local_rank):
     B, Hq, Hkv, d, n = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.context
     U = B * Hkv
     gen = torch.Generator(device="cuda").manual_seed(1000 * rank + 23)
-    q = torch.randn((B, Hq, n, d), generator=gen, device="cuda")
-    q = (q / q.norm(dim=-1, keepdim=True) * math.sqrt(d)).to(torch.bfloat16)
+    # the prompt's queries are correlated along the positions as the decode steps' random walk
+    # q_t = normalize(q_{t-1} + sigma N(0, I)) sqrt(d) is (neighbours at cosine 1 / sqrt(1 + sigma^2)):
+    # a stationary Gaussian sequence p_t = rho p_{t-1} + sqrt(1 - rho^2) e_t, rho = 1 / sqrt(1 + sigma^2),
+    # each p_t scaled to norm sqrt(d); stepped in closed form 256 positions at a time (one matrix
+    # product per chunk, no launch per position)
+    rho = 1.0 / math.sqrt(1.0 + wl.sigma ** 2)
+    c = 256
+    i_ = torch.arange(c, device="cuda", dtype=torch.float32)
+    lag = i_[:, None] - i_[None, :]
+    A = torch.where(lag >= 0, math.sqrt(1.0 - rho * rho) * torch.pow(rho, lag.clamp(min=0)), torch.zeros_like(lag))
+    r = torch.pow(rho, i_ + 1)
+    q = torch.empty((B, Hq, n, d), dtype=torch.bfloat16, device="cuda")
+    pt = torch.randn((B * Hq * d,), generator=gen, device="cuda")
+    for t0 in range(0, n, c):
+        m = min(c, n - t0)
+        E = torch.randn((m, B * Hq * d), generator=gen, device="cuda")
+        P = A[:m, :m] @ E + r[:m, None] * pt[None, :]
+        pt = P[m - 1].clone()
+        Qc = P.view(m, B, Hq, d)
+        Qc = Qc / Qc.norm(dim=-1, keepdim=True) * math.sqrt(d)
+        q[:, :, t0:t0 + m] = Qc.permute(1, 2, 0, 3).to(torch.bfloat16)
+    del A, E, P, Qc
     k = torch.randn((B, Hkv, n, d), generator=gen, device="cuda").to(torch.bfloat16)
     v = torch.randn((B, Hkv, n, d), generator=gen, device="cuda").to(torch.bfloat16)
     out = torch.empty_like(q)
@@ -835,7 +856,8 @@ def run_prefill(args, rank, world, local_rank):
             "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(workload_config(wl, args, L, world), prompt_tokens=n,
-                           selection="NOSA_S: every prompt position selected as the decode step would, in order"),
+                           selection="NOSA_S: every prompt position selected as the decode step would, in order",
+                           prompt_queries=f"correlated along the positions as the decode walk with sigma {wl.sigma}"),
             "gpu_launches": 6 * L * K, "clocks": ck,
             "step": "one prompt of context tokens per sequence through every layer (nosa_prefill per layer)",
             "gamma": {"mean": stats.gamma_mean, "min": stats.gamma_min},

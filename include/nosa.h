@@ -141,6 +141,13 @@ typedef struct {
   int32_t forecast_streams;      /* forecast pipeline: 2 = selections and gathers on two streams
                                     (a layer's selection overlaps the previous layer's gather),
                                     1 = both in order on one stream */
+  int32_t cache_slots;           /* GPU block cache slots per unit, from one selection's blocks
+                                    (sink + window/64 + k_q + k_e) up to 256; 0 = rule: twice a
+                                    selection, at most 256.
+                                    Slots beyond a selection keep blocks that left it, so a block
+                                    selected again later is not fetched again (the least recently
+                                    selected are replaced first).  Selections and outputs do not
+                                    depend on it; fetch lists, slots and transfers do. */
 } nosa_config;
 
 /* Values of nosa_config.attend_merge. */
@@ -153,12 +160,14 @@ typedef struct {
 typedef struct {
   int32_t units_per_layer; /* B * Hkv */
   int32_t group;           /* Hq / Hkv */
-  int32_t cache_slots;     /* blocks per unit in the GPU cache = sink + window/64 + k_q + k_e */
+  int32_t cache_slots;     /* slots per unit in the GPU block cache (nosa_config.cache_slots) */
   int32_t max_blocks;      /* ceil(max_context / 64) */
   int32_t max_windows;     /* complete CompressK windows at max_context */
   int32_t evict_words;     /* 32-bit words of the per-unit eviction bitmap */
   uint64_t host_store_bytes;   /* pinned K/V store: L*U*max_blocks*2*64*d*2 */
   uint64_t device_state_bytes; /* everything nosa_create allocates on the device */
+  int32_t select_slots;    /* blocks of one selection at most: sink + window/64 + k_q + k_e */
+  int32_t pad_;
 } nosa_sizes;
 
 typedef struct nosa_ctx nosa_ctx;
@@ -175,7 +184,8 @@ typedef struct {
 } nosa_stats;
 
 /* Host-side view for nosa_export_state: every pointer is host memory or NULL
- * (skipped).  Shapes are per layer; U = units_per_layer, cap = cache_slots. */
+ * (skipped).  Shapes are per layer; U = units_per_layer, cap = select_slots,
+ * cs = cache_slots. */
 typedef struct {
   int32_t* sel;       /* [U][cap] selected blocks S, ascending, -1 padded */
   int32_t* sel_kind;  /* [U][cap] 0 sink, 1 window, 2 query-aware, 3 query-agnostic, -1 pad */
@@ -183,12 +193,14 @@ typedef struct {
   int32_t* n_sel;     /* [U] */
   int32_t* fetch;     /* [U][cap][2] (block, slot) fetched by the last selection, ascending */
   int32_t* n_fetch;   /* [U] */
-  int32_t* slot_blk;  /* [U][cap] block held by each slot, -1 free */
+  int32_t* slot_blk;  /* [U][cs] block held by each cache slot, -1 empty */
   uint32_t* evicted;  /* [U][evict_words] sticky eviction bitmap, bit b%32 of word b/32 */
   uint16_t* kt;       /* [U][max_windows][d] compressed keys (bf16 bits) */
   float* se_win;      /* [U][max_windows] window means of the eviction score */
   float* se_blk;      /* [U][max_blocks] pooled eviction score (-inf before any window) */
   int32_t* gamma;     /* [U][2] |D_t & S_{t-1}| and |D_t| of the last selection */
+  int32_t* last_used; /* [U][cs] context length of the last selection holding each slot's
+                         block, -1 for a slot no selection has used */
 } nosa_state_view;
 
 /* Validate a config without touching the GPU.  NOSA_OK or NOSA_ERR_INVALID_ARG. */
@@ -234,8 +246,9 @@ nosa_status nosa_append_kv(nosa_ctx* ctx, int layer, const uint16_t* k, const ui
  * by that part never re-selected by it) and "Main-experiment configuration" (sink block,
  * sliding-window blocks, 64-token blocks); NOSA explainer, section 2.1, eq. 5-6 (pooled block
  * scores, the selection); SparDA summary, "lightweight design" (softmax aggregation over a GQA
- * group); NOSA wiki, "NOSI" (set difference against the cached blocks).  Optional device outputs: sel_out [B][Hkv][cache_slots]
- * (S ascending, -1 padded) and nfetch_out [B][Hkv] (blocks to fetch). */
+ * group); NOSA wiki, "NOSI" (set difference against the cached blocks: a selected block is
+ * fetched only when no cache slot holds it).  Optional device outputs: sel_out
+ * [B][Hkv][select_slots] (S ascending, -1 padded) and nfetch_out [B][Hkv] (blocks to fetch). */
 nosa_status nosa_select(nosa_ctx* ctx, int layer, const uint16_t* q, int32_t* sel_out,
                         int32_t* nfetch_out);
 

@@ -34,7 +34,7 @@ __global__ void copy_i32(int32_t* dst, const int32_t* src, size_t n) {
 }
 
 struct Derived {
-  int U, G, nw, cap, nb_max, nc_max, ev_words, h;
+  int U, G, nw, cap, cs, nb_max, nc_max, ev_words, h;
 };
 
 Derived derive(const nosa_config* c) {
@@ -43,6 +43,9 @@ Derived derive(const nosa_config* c) {
   d.G = c->num_q_heads / c->num_kv_heads;
   d.nw = c->window_tokens / c->block_size;
   d.cap = c->sink_blocks + d.nw + c->k_q + c->k_e;
+  // the block cache: twice a selection by default, so that blocks leaving the selection stay
+  // cached for a while (a block the query-aware part picks again is then not fetched again)
+  d.cs = c->cache_slots > 0 ? c->cache_slots : std::min(2 * d.cap, kMaxCacheSlots);
   d.nb_max = cdiv(c->max_context, kBlock);
   d.nc_max = c->max_context < kCmpKernel ? 0 : (c->max_context - kCmpKernel) / kCmpStride + 1;
   d.ev_words = cdiv(d.nb_max, 32);
@@ -78,7 +81,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 void free_ctx(nosa_ctx* c) {
-  void* dev[] = {c->cache, c->kt, c->kring, c->se_tok, c->se_win, c->se_blk, c->W1, c->W2, c->slot_blk,
+  void* dev[] = {c->cache, c->kt, c->kring, c->se_tok, c->se_win, c->se_blk, c->W1, c->W2, c->slot_blk, c->last_used,
                  c->blk2slot, c->sel, c->sel_kind, c->sel_slot, c->sel_new, c->n_sel, c->fetch, c->n_fetch, c->gamma,
                  c->evicted, c->T, c->err, c->stats, c->sq_blk, c->apart, c->tickets,
                  c->stage_q, c->stage_k, c->stage_v, c->stage_out, c->bulk_k, c->bulk_v,
@@ -108,6 +111,7 @@ LayerState layer_state(nosa_ctx* c, int l) {
   s.G = d.G;
   s.Hkv = c->Hkv;
   s.cap = d.cap;
+  s.cslots = d.cs;
   s.nb_max = d.nb_max;
   s.nc_max = std::max(d.nc_max, 1);
   s.T_max = c->cfg.max_context;
@@ -122,14 +126,15 @@ LayerState layer_state(nosa_ctx* c, int l) {
   const size_t lu = (size_t)l * U;
   s.T = c->T + l;
   s.host_kv = c->host_kv_dev + lu * d.nb_max * 2 * kBlockElems;
-  s.cache = c->cache + lu * d.cap * 2 * kBlockElems;
+  s.cache = c->cache + lu * d.cs * 2 * kBlockElems;
   s.kt = c->kt + lu * s.nc_max * kHeadDim;
   s.kring = c->kring + lu * 32 * kHeadDim;
   s.se_stride = d.nb_max * kBlock;
   s.se_tok = c->se_tok + lu * s.se_stride;
   s.se_win = c->se_win + lu * s.nc_max;
   s.se_blk = c->se_blk + lu * d.nb_max;
-  s.slot_blk = c->slot_blk + lu * d.cap;
+  s.slot_blk = c->slot_blk + lu * d.cs;
+  s.last_used = c->last_used + lu * d.cs;
   s.blk2slot = c->blk2slot + lu * d.nb_max;
   s.evicted = c->evicted + lu * d.ev_words;
   s.sel = c->sel + lu * d.cap;
@@ -211,6 +216,7 @@ nosa_status nosa_validate_config(const nosa_config* c) {
   if (U > 4096) return NOSA_ERR_INVALID_ARG;
   const long long cap = (long long)c->sink_blocks + c->window_tokens / kBlock + c->k_q + c->k_e;
   if (cap < 1 || cap > kMaxCacheSlots) return NOSA_ERR_INVALID_ARG;
+  if (c->cache_slots != 0 && (c->cache_slots < cap || c->cache_slots > kMaxCacheSlots)) return NOSA_ERR_INVALID_ARG;
   if ((long long)c->num_layers * U * cap >= (1ll << 31)) return NOSA_ERR_INVALID_ARG;
   return NOSA_OK;
 }
@@ -223,14 +229,16 @@ nosa_status nosa_query_sizes(const nosa_config* c, nosa_sizes* out) {
   const uint64_t L = c->num_layers, U = d.U, nc = std::max(d.nc_max, 1);
   out->units_per_layer = d.U;
   out->group = d.G;
-  out->cache_slots = d.cap;
+  out->cache_slots = d.cs;
+  out->select_slots = d.cap;
+  out->pad_ = 0;
   out->max_blocks = d.nb_max;
   out->max_windows = d.nc_max;
   out->evict_words = d.ev_words;
   out->host_store_bytes = L * U * d.nb_max * (uint64_t)kBlockBytes;
-  const uint64_t per_unit = (uint64_t)d.cap * kBlockBytes + nc * kHeadDim * 2 + 32 * kHeadDim * 2 +
+  const uint64_t per_unit = (uint64_t)d.cs * kBlockBytes + nc * kHeadDim * 2 + 32 * kHeadDim * 2 +
                             (uint64_t)d.nb_max * kBlock * 4 + nc * 4 + (uint64_t)d.nb_max * 12 + d.ev_words * 4ull +
-                            (uint64_t)d.cap * 4 * 5 + 4 * 4;
+                            (uint64_t)d.cap * 4 * 6 + (uint64_t)d.cs * 4 * 2 + 4 * 4;
   const int score_chunks = cdiv(nc, kWindowsPerCta);
   const uint64_t scratch = U * d.G * nc * 4 + U * score_chunks * kMaxGroup * 8 +
                            U * (uint64_t)d.cap * kMaxGroup * kPartStride * 4 + (3 * U + 1) * 4;
@@ -263,6 +271,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->h = d.h;
   c->nw = d.nw;
   c->cap = d.cap;
+  c->cs = d.cs;
   c->stream = (cudaStream_t)stream;
   c->device = dev;
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -324,7 +333,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   c->dec_cs = 0;
   c->dec_teams = cfg->decode_teams > 0 ? cfg->decode_teams : 2;
   c->dec_nst = cfg->decode_stages > 0 ? cfg->decode_stages : 3;
-  if (!(cfg->flags & NOSA_F_UNFUSED_STEP) && d.cap <= 128 * c->dec_teams) {
+  if (!(cfg->flags & NOSA_F_UNFUSED_STEP) && d.cs <= 128 * c->dec_teams) {  // a thread per cache slot
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     std::vector<int> sizes = {8, 4};  // with clusters of 2 the selector and attention are too narrow
@@ -366,7 +375,7 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
       oom = true;
     }
   };
-  dalloc(&c->cache, LU * d.cap * (size_t)kBlockBytes);
+  dalloc(&c->cache, LU * d.cs * (size_t)kBlockBytes);
   dalloc(&c->kt, LU * nc * kHeadDim * 2);
   dalloc(&c->kring, LU * 32 * kHeadDim * 2);
   dalloc(&c->se_tok, LU * (size_t)d.nb_max * kBlock * 4);
@@ -374,7 +383,8 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
   dalloc(&c->se_blk, LU * d.nb_max * 4);
   dalloc(&c->W1, (size_t)c->L * c->Hkv * kHeadDim * d.h * 4);
   dalloc(&c->W2, (size_t)c->L * c->Hkv * d.h * 4);
-  dalloc(&c->slot_blk, LU * d.cap * 4);
+  dalloc(&c->slot_blk, LU * d.cs * 4);
+  dalloc(&c->last_used, LU * d.cs * 4);
   dalloc(&c->blk2slot, LU * d.nb_max * 4);
   dalloc(&c->sel, LU * d.cap * 4);
   dalloc(&c->sel_kind, LU * d.cap * 4);
@@ -406,14 +416,15 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     return NOSA_ERR_OOM;
   }
   // initial state: empty cache, nothing evicted, pooled eviction scores at -inf
-  bool ok = cudaMemset(c->cache, 0, LU * d.cap * (size_t)kBlockBytes) == cudaSuccess;
+  bool ok = cudaMemset(c->cache, 0, LU * d.cs * (size_t)kBlockBytes) == cudaSuccess;
   ok = ok && cudaMemset(c->kt, 0, LU * nc * kHeadDim * 2) == cudaSuccess;
   ok = ok && cudaMemset(c->kring, 0, LU * 32 * kHeadDim * 2) == cudaSuccess;
   ok = ok && cudaMemset(c->se_tok, 0, LU * (size_t)d.nb_max * kBlock * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->se_win, 0, LU * nc * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->W1, 0, (size_t)c->L * c->Hkv * kHeadDim * d.h * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->W2, 0, (size_t)c->L * c->Hkv * d.h * 4) == cudaSuccess;
-  ok = ok && cudaMemset(c->slot_blk, 0xFF, LU * d.cap * 4) == cudaSuccess;
+  ok = ok && cudaMemset(c->slot_blk, 0xFF, LU * d.cs * 4) == cudaSuccess;
+  ok = ok && cudaMemset(c->last_used, 0xFF, LU * d.cs * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->blk2slot, 0xFF, LU * d.nb_max * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->sel, 0xFF, LU * d.cap * 4) == cudaSuccess;
   ok = ok && cudaMemset(c->sel_kind, 0xFF, LU * d.cap * 4) == cudaSuccess;
@@ -441,14 +452,14 @@ nosa_status nosa_create(const nosa_config* cfg, void* stream, nosa_ctx** out) {
     free_ctx(c);
     return NOSA_ERR_CUDA;
   }
-  // TMA descriptor over the block cache: (d 128, token 64, K/V 2, flat slot L*U*cap), bf16,
+  // TMA descriptor over the block cache: (d 128, token 64, K/V 2, flat slot L*U*cs), bf16,
   // boxes of 64 dims x 64 tokens x K+V with the 128-byte swizzle
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) {
     free_ctx(c);
     return NOSA_ERR_CUDA;
   }
-  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kBlock, 2, (cuuint64_t)LU * d.cap};
+  cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kBlock, 2, (cuuint64_t)LU * d.cs};
   cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)kBlockElems * 2, (cuuint64_t)kBlockBytes};
   cuuint32_t box[4] = {64, (cuuint32_t)kBlock, 2, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -915,7 +926,7 @@ nosa_status nosa_export_state(nosa_ctx* c, int layer, const nosa_state_view* v) 
   const nosa_status ss = sync_all(c);
   if (ss != NOSA_OK) return ss;
   const LayerState s = layer_state(c, layer);
-  const size_t U = c->U, cap = c->cap;
+  const size_t U = c->U, cap = c->cap, cs = c->cs;
   auto cp = [&](void* dst, const void* src, size_t bytes) {
     return dst ? cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost) : cudaSuccess;
   };
@@ -925,7 +936,8 @@ nosa_status nosa_export_state(nosa_ctx* c, int layer, const nosa_state_view* v) 
   CK(cp(v->n_sel, s.n_sel, U * 4));
   CK(cp(v->fetch, s.fetch, U * cap * 8));
   CK(cp(v->n_fetch, s.n_fetch, U * 4));
-  CK(cp(v->slot_blk, s.slot_blk, U * cap * 4));
+  CK(cp(v->slot_blk, s.slot_blk, U * cs * 4));
+  CK(cp(v->last_used, s.last_used, U * cs * 4));
   CK(cp(v->evicted, s.evicted, U * s.ev_words * 4));
   CK(cp(v->kt, s.kt, U * s.nc_max * kHeadDim * 2));
   CK(cp(v->se_win, s.se_win, U * s.nc_max * 4));

@@ -57,10 +57,10 @@ __global__ void __launch_bounds__(256) append_bulk_tokens_kernel(LayerState s, c
     const size_t hoff = (((size_t)u * s.nb_max + blk) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
     *reinterpret_cast<uint4*>(s.host_kv + hoff) = val;
     const int slot = s.blk2slot[(size_t)u * s.nb_max + blk];
-    if (slot >= s.cap) {
+    if (slot >= s.cslots) {
       atomicOr(s.err, kErrBounds);
     } else if (slot >= 0) {
-      const size_t coff = (((size_t)u * s.cap + slot) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
+      const size_t coff = (((size_t)u * s.cslots + slot) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
       *reinterpret_cast<uint4*>(s.cache + coff) = val;
     }
   }

@@ -90,10 +90,10 @@ __device__ __forceinline__ void append_token(const LayerState& s, int u, int p, 
     const int half = tid >> 4, c8 = (tid & 15) * 8;
     const size_t hoff = (((size_t)u * s.nb_max + blk) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
     *reinterpret_cast<uint4*>(s.host_kv + hoff) = rowv;  // store through the UVA alias of pinned memory
-    if (slot >= s.cap) {
+    if (slot >= s.cslots) {
       atomicOr(s.err, kErrBounds);
     } else if (slot >= 0) {
-      const size_t coff = (((size_t)u * s.cap + slot) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
+      const size_t coff = (((size_t)u * s.cslots + slot) * 2 + half) * kBlockElems + (size_t)row * kHeadDim + c8;
       *reinterpret_cast<uint4*>(s.cache + coff) = rowv;
     }
   }

@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kAttendThreads, 1)
       if (in && pos % CS == c0) {
         const int i = pos / CS;
         int slot = ev[it][1];
-        if (slot < 0 || slot >= s.cap) {
+        if (slot < 0 || slot >= s.cslots) {
           atomicOr(s.err, kErrBounds);
           slot = 0;  // keep the copy in bounds; the result is flagged as invalid
         }

@@ -124,7 +124,7 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
       if (ttid == 0) mbar_arrive(&bars[st]);
       host_copy(e, st);
     } else if (ttid == 0) {
-      const int flat = (s.unit_base + u) * s.cap + slot[e];
+      const int flat = (s.unit_base + u) * s.cslots + slot[e];
       fence_proxy_async_smem();
       mbar_arrive_expect_tx(&bars[st], kStageBytes + (dma ? kBlock * 4 : 0));
       tma_load_4d(sbase + st * kStageBytes, tmap, 0, 0, 0, flat, &bars[st]);
@@ -200,7 +200,7 @@ __device__ __forceinline__ bool attend_worker(const CUtensorMap* tmap, const Lay
       }
     }
     if (isnew[e]) {
-      uint16_t* dst = s.cache + ((size_t)u * s.cap + slot[e]) * 2 * kBlockElems;
+      uint16_t* dst = s.cache + ((size_t)u * s.cslots + slot[e]) * 2 * kBlockElems;
 #pragma unroll 4
       for (int j = 0; j < kStageBytes / 16 / kTeamThreads; ++j) {
         const int idx = ttid + j * kTeamThreads;

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kTeamThreads * kTeams, 1)
                                     [&](int pos, int b, int slot, bool isnew, int dp, int) {
                                       const int w = dp % NW;
                                       if (w / kTeams != rank || dp >= s.cap) return;
-                                      if (slot < 0 || slot >= s.cap) {
+                                      if (slot < 0 || slot >= s.cslots) {
                                         atomicOr(s.err, kErrBounds);
                                         slot = 0;  // keep the copy in bounds; the result is flagged
                                       }

@@ -146,6 +146,7 @@ extern "C" nosa_status nosa_dense_attend(const uint16_t* q, const uint16_t* kv, 
   s.G = group;
   s.Hkv = 1;
   s.cap = max_blocks;
+  s.cslots = max_blocks;
   s.nb_max = max_blocks;
   s.unit_base = 0;
   s.scale = softmax_scale > 0.f ? softmax_scale : 1.f / sqrtf((float)kHeadDim);

@@ -55,13 +55,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(LayerState s, in
     }
     const int u = lo, e = item - pref[u];
     const int b = s.fetch[((size_t)u * s.cap + e) * 2], slot = s.fetch[((size_t)u * s.cap + e) * 2 + 1];
-    if (b < 0 || b >= nb_sel || slot < 0 || slot >= s.cap) {
+    if (b < 0 || b >= nb_sel || slot < 0 || slot >= s.cslots) {
       if (tid == 0) atomicOr(s.err, kErrBounds);
       return j;
     }
     j.rows = b < geo.nb - 1 ? kBlock : (b == geo.nb - 1 ? geo.valid_tail : 0);
     j.src = reinterpret_cast<const uint4*>(s.host_kv + ((size_t)u * s.nb_max + b) * 2 * kBlockElems);
-    j.dst = reinterpret_cast<uint4*>(s.cache + ((size_t)u * s.cap + slot) * 2 * kBlockElems);
+    j.dst = reinterpret_cast<uint4*>(s.cache + ((size_t)u * s.cslots + slot) * 2 * kBlockElems);
     return j;
   };
   auto load = [&](const Job& j, uint4 (&v)[kVec]) {

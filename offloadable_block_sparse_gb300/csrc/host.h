@@ -7,7 +7,7 @@
 struct nosa_ctx {
   nosa_config cfg;
   nosa_sizes sz;
-  int L, B, Hq, Hkv, G, d, U, h, nw, cap;
+  int L, B, Hq, Hkv, G, d, U, h, nw, cap, cs;  // cap: blocks of a selection; cs: cache slots per unit
   cudaStream_t stream;
   int device;
   int num_sms;
@@ -18,7 +18,7 @@ struct nosa_ctx {
   // device state (all layers, one allocation each)
   uint16_t *cache, *kt, *kring;
   float *se_tok, *se_win, *se_blk, *W1, *W2;
-  int32_t *slot_blk, *blk2slot, *sel, *sel_kind, *sel_slot, *sel_new, *n_sel, *fetch, *n_fetch, *gamma;
+  int32_t *slot_blk, *last_used, *blk2slot, *sel, *sel_kind, *sel_slot, *sel_new, *n_sel, *fetch, *n_fetch, *gamma;
   uint32_t* evicted;
   int *T, *err;
   nosa::DevStats* stats;

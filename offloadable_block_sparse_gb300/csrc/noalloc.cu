@@ -130,6 +130,7 @@ extern "C" nosa_status nosa_attend_noalloc(const uint16_t* q, const uint16_t* ca
   s.G = group;
   s.Hkv = 1;
   s.cap = cache_slots;
+  s.cslots = cache_slots;
   s.nw = 0;
   s.sink = 0;
   s.unit_base = 0;

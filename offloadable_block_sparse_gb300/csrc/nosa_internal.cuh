@@ -78,20 +78,23 @@ struct LayerState {
   int U;            // units of this layer
   int G;            // q heads per kv head
   int Hkv;
-  int cap, nb_max, nc_max, T_max, ev_words, nw, sink, k_q, k_e, h;
+  int cap;          // blocks of one selection at most (sink + window + k_q + k_e): selection arrays
+  int cslots;       // block cache slots per unit (cap or more)
+  int nb_max, nc_max, T_max, ev_words, nw, sink, k_q, k_e, h;
   int se_stride;          // row stride of se_tok: nb_max * 64, so each block's scores start 256-byte aligned
   int dma_bias;           // attention logits get each token's eviction score added
   int unit_base;    // layer * U: first unit of this layer in context-wide arrays
   float scale;
   int* T;                 // device context length of this layer
   uint16_t* host_kv;      // device alias of the pinned store [U][nb_max][2][64][d]
-  uint16_t* cache;        // [U][cap][2][64][d]
+  uint16_t* cache;        // [U][cslots][2][64][d]
   uint16_t* kt;           // [U][nc_max][d]
   uint16_t* kring;        // [U][32][d]
   float* se_tok;          // [U][se_stride]
   float* se_win;          // [U][nc_max]
   float* se_blk;          // [U][nb_max]
-  int32_t* slot_blk;      // [U][cap]
+  int32_t* slot_blk;      // [U][cslots] block in each cache slot, -1 empty
+  int32_t* last_used;     // [U][cslots] context length of the last selection holding the slot's block, -1 never
   int32_t* blk2slot;      // [U][nb_max]
   uint32_t* evicted;      // [U][ev_words]
   int32_t* sel;           // [U][cap]

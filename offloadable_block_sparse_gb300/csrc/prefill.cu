@@ -13,12 +13,12 @@
 //      top-k_q candidates.  Each warp takes a few positions and walks the compressed keys.
 //   2b. prefill_walk_kernel: one warp per unit makes the rest of every position's
 //      selection in order: the k_e query-agnostic picks among the candidates never
-//      dropped before (a short list ordered by pooled s^e), the sticky eviction update,
-//      the set difference against the previous selection and the ascending free-slot
-//      pairing, with bitmaps over the blocks.  Each position's picks go to the caller's
-//      scratch as two bitmaps (query-aware, query-agnostic).
-//   3. prefill_refresh_kernel: every cache slot gets its block's K/V from the prompt
-//      (the state after the prompt is the one the decode steps would have left).
+//      dropped before (a short list ordered by pooled s^e) and the sticky eviction
+//      update, with bitmaps over the blocks.  Each position's picks go to the caller's
+//      scratch as two bitmaps (query-aware, query-agnostic).  The selection and eviction
+//      state after the prompt are the ones the decode steps would have left; the cache
+//      then holds exactly the last selection, its i-th block in slot i.
+//   3. prefill_refresh_kernel: every cache slot gets its block's K/V from the prompt.
 //   4. prefill_attend_tc_kernel: a CTA takes 128 / G consecutive positions of one unit (128
 //      rows of position x q head), forms the union of their selections and streams those
 //      blocks from the prompt's K and V (TMA, 128-byte swizzle); each block's scores and
@@ -499,8 +499,8 @@ __global__ void __launch_bounds__(kQtThreads, 1)
 
 // ---------------------------------------------------------------- 2b. the walk over the positions
 // One warp per unit makes the stateful part of every position's selection, in order: the k_e
-// query-agnostic picks among the candidates never dropped before, the sticky eviction update,
-// the set difference against the previous selection and the ascending free-slot pairing.  Every
+// query-agnostic picks among the candidates never dropped before and the sticky eviction
+// update (with the locality counters against the previous selection).  Every
 // candidate a selection leaves out is dropped for good, so the candidates still eligible are the
 // last selection's never-dropped blocks plus the blocks that have just become candidates; the warp
 // keeps them in a list ordered by (pooled s^e, then lower block), and a position's picks are the
@@ -512,7 +512,7 @@ constexpr int kWalkMaxSlots = 9;  // list entries per lane: k_q + k_e + 1 <= 288
 
 __host__ __device__ inline size_t walk_warp_bytes(int nbn) {
   const int nbw = (nbn + 31) / 32;
-  return (size_t)32 * kWalkMaxSlots * 8 + 4 * (size_t)nbw * 4 + 8 * 4 + (size_t)((nbn + 7) & ~7) * 2 + 3 * 256 * 2;
+  return (size_t)32 * kWalkMaxSlots * 8 + 4 * (size_t)nbw * 4;
 }
 
 __device__ __forceinline__ uint32_t range_bits(int w, int lo, int hi) {  // bits of [lo, hi) in word w
@@ -554,18 +554,10 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
   uint32_t* sprev = ev + nbw;  // the previous selection
   uint32_t* qbm = sprev + nbw;  // this position's query-aware picks
   uint32_t* lb = qbm + nbw;     // the list's blocks
-  uint32_t* fbm = lb + nbw;     // free cache slots (8 words)
-  int16_t* slot_of = reinterpret_cast<int16_t*>(fbm + 8);
-  int16_t* slot_blk = slot_of + ((nbn + 7) & ~7);
-  int16_t* newl = slot_blk + 256;
-  int16_t* freel = newl + 256;
   const int ke = s.k_e, cap = s.cap, sink = s.sink;
   const unsigned int lt = (1u << lane) - 1u;
-  // an empty layer: nothing dropped, selected or cached
+  // an empty layer: nothing dropped or selected
   for (int w = lane; w < nbw; w += 32) ev[w] = sprev[w] = qbm[w] = lb[w] = 0u;
-  if (lane < 8) fbm[lane] = range_bits(lane, 0, cap);
-  for (int b = lane; b < nbn; b += 32) slot_of[b] = -1;
-  for (int i = lane; i < 256; i += 32) slot_blk[i] = -1;
   __syncwarp();
   const float* se_blk = s.se_blk + (size_t)u * s.nb_max;
   const float* se_win = s.se_win + (size_t)u * s.nc_max;
@@ -641,10 +633,10 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     }
   };
   load_q(0);
-  unsigned long long st_fetch = 0, st_short = 0, st_gs = 0, st_gn = 0, st_gd = 0;
+  unsigned long long st_short = 0, st_gs = 0, st_gn = 0, st_gd = 0;
   uint32_t st_gmin = 0x7F800000u;  // +inf
   int ws_prev = sink;               // candidates so far: [sink, ws_prev)
-  int nS_prev = 0, nS = 0, nD = 0, nDnew = 0, nNew = 0;
+  int nS_prev = 0, nS = 0, nD = 0, nDnew = 0;
   uint32_t Sw[NW];
   Geometry geo = geometry(1, s.nw, s.sink);
   for (int t = 0; t < n; ++t) {
@@ -704,84 +696,29 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
       nL = wpos;
     }
     __syncwarp();
-    // S = sink + D + window per word, D = Q | the list's blocks; the blocks new to S and the
-    // blocks that left it; this position's query-agnostic words to the caller
-    uint32_t Nw[NW], Fw[NW];
-    int cnt = 0;  // popc(D) | popc(new) << 10 | popc(D & new) << 20 (each at most 256)
+    // S = sink + D + window per word, D = Q | the list's blocks; the blocks of D new to S (for the
+    // locality counters); this position's query-agnostic words to the caller
+    int cnt = 0;  // popc(D) | popc(D & new) << 10 (each at most 256)
     uint32_t* erow = esel + ((size_t)u * n + t) * nbw;
 #pragma unroll
     for (int k = 0; k < NW; ++k) {
       const int w = lane + 32 * k;
-      Sw[k] = Nw[k] = Fw[k] = 0u;
+      Sw[k] = 0u;
       if (w >= nbw) continue;
       const uint32_t L = lb[w];
       erow[w] = L & ~qc[k];
       if (w >= nbwT) continue;
       const uint32_t D = qc[k] | L;
       const uint32_t sw = D | range_bits(w, 0, geo.ns) | range_bits(w, geo.ws, geo.nb);
-      const uint32_t pv = sprev[w];
       Sw[k] = sw;
-      Nw[k] = sw & ~pv;
-      Fw[k] = pv & ~sw;
-      cnt += __popc(D) | (__popc(Nw[k]) << 10) | (__popc(D & Nw[k]) << 20);
+      cnt += __popc(D) | (__popc(D & ~sprev[w]) << 10);
     }
     cnt = warp_sum(cnt);
     nD = cnt & 1023;
-    const int nNewAll = (cnt >> 10) & 1023;
-    nDnew = (cnt >> 20) & 1023;
+    nDnew = (cnt >> 10) & 1023;
     nS = geo.ns + nD + (geo.nb - geo.ws);
     if (nS > cap && lane == 0) atomicOr(s.err, kErrBounds);  // cannot happen when cap = sink + window + k_q + k_e
-    // the new blocks in ascending order; the slots of the blocks that left become free
-    if (nNewAll) {
-      int carry = 0;
-#pragma unroll
-      for (int k = 0; k < NW; ++k) {
-        const int c = __popc(Nw[k]);
-        const int incl = warp_incl_scan(c);
-        int pos = carry + incl - c;
-        for (uint32_t m = Nw[k]; m; m &= m - 1u, ++pos)
-          if (pos < 256) newl[pos] = (int16_t)(32 * (lane + 32 * k) + __ffs(m) - 1);
-        carry += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < NW; ++k)
-      for (uint32_t m = Fw[k]; m; m &= m - 1u) {
-        const int b = 32 * (lane + 32 * k) + __ffs(m) - 1;
-        const int sl = slot_of[b];
-        slot_of[b] = -1;
-        if (sl >= 0) {
-          slot_blk[sl] = -1;
-          atomicOr(&fbm[sl >> 5], 1u << (sl & 31));
-        }
-      }
-    __syncwarp();
-    // the i-th new block (ascending) takes the i-th free slot (ascending)
-    nNew = min(nNewAll, 256);
-    {
-      int fbase = 0;
-      for (int w = 0; w < 8 && fbase < nNew; ++w) {
-        const uint32_t fv = fbm[w];
-        if (!fv) continue;
-        const int i = fbase + __popc(fv & lt);
-        const bool take = ((fv >> lane) & 1u) && i < nNew;
-        if (take) {
-          const int sl = 32 * w + lane, b = newl[i];
-          slot_of[b] = (int16_t)sl;
-          slot_blk[sl] = (int16_t)b;
-          freel[i] = (int16_t)sl;
-        }
-        const unsigned int tk = __ballot_sync(0xffffffffu, take);
-        if (lane == 0) fbm[w] = fv & ~tk;
-        fbase += __popc(fv);
-      }
-      if (fbase < nNew) {  // cannot happen when cap >= |S|; keep the slot table in bounds anyway
-        if (lane == 0) atomicOr(s.err, kErrBounds);
-        nNew = fbase;
-      }
-    }
     // the decode step's counters
-    st_fetch += nNew;
     if (nE < ke) ++st_short;
     if (nS_prev > 0 && nD > 0) {  // some block was cached before
       ++st_gs;
@@ -799,13 +736,18 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     }
     __syncwarp();
   }
-  // the unit's state after the prompt: the last selection with kinds, slots and fetched marks,
-  // its fetch list, the eviction bitmap and the slot tables
+  // the unit's state after the prompt: the last selection with its kinds; the cache holds exactly
+  // that selection, its i-th block in slot i (every block of it is written from the prompt next,
+  // so nothing else is worth keeping), each slot marked as serving the selection at T = n; nothing
+  // is left to fetch; the eviction bitmap
   int32_t* sel = s.sel + (size_t)u * cap;
   int32_t* kind = s.sel_kind + (size_t)u * cap;
   int32_t* sslot = s.sel_slot + (size_t)u * cap;
   int32_t* snew = s.sel_new + (size_t)u * cap;
+  int32_t* b2s = s.blk2slot + (size_t)u * s.nb_max;
   const int nSw = min(nS, cap);
+  for (int b = lane; b < nbn; b += 32) b2s[b] = -1;
+  __syncwarp();
   {
     int pos = 0;
     const int nbwT = (geo.nb + 31) >> 5;
@@ -817,8 +759,9 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
         if (p < nSw) {
           sel[p] = b;
           kind[p] = b < geo.ns ? 0 : b >= geo.ws ? 1 : ((qbm[w] >> lane) & 1u) ? 2 : 3;
-          sslot[p] = slot_of[b];
-          snew[p] = ((sprev[w] >> lane) & 1u) ? 0 : 1;  // sprev holds the position before the last
+          sslot[p] = p;
+          snew[p] = 0;
+          b2s[b] = p;
         }
       }
       pos += __popc(sw);
@@ -830,23 +773,20 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
     sslot[i] = -1;
     snew[i] = 0;
   }
-  int32_t* fl = s.fetch + (size_t)u * cap * 2;
-  for (int j = lane; j < nNew; j += 32) {
-    fl[2 * j] = newl[j];
-    fl[2 * j + 1] = freel[j];
+  __syncwarp();  // the selection list above, read back by other lanes
+  for (int i = lane; i < s.cslots; i += 32) {
+    s.slot_blk[(size_t)u * s.cslots + i] = i < nSw ? sel[i] : -1;
+    s.last_used[(size_t)u * s.cslots + i] = i < nSw ? n : -1;
   }
   if (lane == 0) {
     s.n_sel[u] = nSw;
-    s.n_fetch[u] = nNew;
+    s.n_fetch[u] = 0;
     s.gamma[2 * u] = nD - nDnew;
     s.gamma[2 * u + 1] = nD;
   }
   for (int w = lane; w < s.ev_words; w += 32) s.evicted[(size_t)u * s.ev_words + w] = w < nbw ? ev[w] : 0u;
-  for (int i = lane; i < cap; i += 32) s.slot_blk[(size_t)u * cap + i] = slot_blk[i];
-  for (int b = lane; b < nbn; b += 32) s.blk2slot[(size_t)u * s.nb_max + b] = slot_of[b];
   if (lane == 0) {
     atomicAdd(&s.stats->selections, (unsigned long long)n);
-    atomicAdd(&s.stats->blocks_fetched, st_fetch);
     atomicAdd(&s.stats->short_selections, st_short);
     if (st_gs) {
       atomicAdd(&s.stats->gamma_samples, st_gs);
@@ -859,14 +799,14 @@ __global__ void __launch_bounds__(kWalkWarps * 32)
 
 // ---------------------------------------------------------------- 3. cache refresh
 // grid (cap, U), 256 threads: slot `slot` of unit u receives its block from the prompt's K/V
-// (rows past the prompt zero), as the fetches of the decode steps would have left it.
+// (rows past the prompt zero); after the prompt only the first |S| <= cap slots hold blocks.
 __global__ void __launch_bounds__(256) prefill_refresh_kernel(LayerState s, const uint16_t* __restrict__ k,
                                                               const uint16_t* __restrict__ v, int n) {
   const int slot = blockIdx.x, u = blockIdx.y;
   pdl_wait();
-  const int b = s.slot_blk[(size_t)u * s.cap + slot];
+  const int b = s.slot_blk[(size_t)u * s.cslots + slot];
   if (b < 0 || b * kBlock >= n) return;
-  uint16_t* dst = s.cache + ((size_t)u * s.cap + slot) * 2 * kBlockElems;
+  uint16_t* dst = s.cache + ((size_t)u * s.cslots + slot) * 2 * kBlockElems;
   for (int idx = threadIdx.x; idx < 2 * kBlock * 16; idx += blockDim.x) {
     const int kv = idx >> 10, r = (idx >> 4) & (kBlock - 1), c = idx & 15;
     const int tok = kBlock * b + r;

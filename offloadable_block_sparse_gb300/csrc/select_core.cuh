@@ -54,6 +54,8 @@ struct SelShared {
   int cofs[kMaxScoreCluster + 1];
   float zx[kMaxGroup];  // logits of the window just before this CTA's range (pooled here too)
   float sqx;            // its query-aware score
+  int lumax[kMaxCacheSlots / 32];     // per warp: the latest selection any cache slot served
+  uint32_t okey[kMaxCacheSlots];      // cache slots open to new blocks: (last selected + 1, slot)
 };
 
 // Composite ranking key: higher score first, then lower block.  Distinct blocks give
@@ -205,10 +207,12 @@ __host__ __device__ inline int zs_floats(const LayerState& s) {
 // Bytes of dynamic shared memory the phases use: z[kMaxGroup][wpc] and sq[wpc] floats
 // (every CTA), then for the leader keys, pooled s^e and the block -> slot map
 // [nb_max] each, eviction words, the gathered local winners [8][k_q] (keys and
-// blocks), eligible blocks [nb_max] and flags [nb_max].
+// blocks), eligible blocks [nb_max], the cache slots' last selections [cslots] and
+// flags [nb_max].
 __host__ __device__ inline size_t region_bytes(const LayerState& s) {
   return sizeof(float) * ((size_t)zs_floats(s) + s.score_wpc) + 4 * sizeof(uint32_t) * s.nb_max +
-         sizeof(uint32_t) * s.ev_words + 2 * sizeof(uint32_t) * kMaxScoreCluster * s.k_q + s.nb_max + 16;
+         sizeof(uint32_t) * s.ev_words + 2 * sizeof(uint32_t) * kMaxScoreCluster * s.k_q +
+         sizeof(int32_t) * s.cslots + s.nb_max + 16;
 }
 
 struct Smem {
@@ -220,6 +224,7 @@ struct Smem {
   uint32_t* evw;       // leader: [ev_words]
   uint32_t* cand_key;  // leader: [8][k_q] local winners' keys
   int32_t* cand_blk;   // leader: [8][k_q]
+  int32_t* lu;         // leader: [cslots] context length of the last selection each slot served
   uint8_t* flags;      // leader: [nb_max]
 };
 
@@ -234,7 +239,8 @@ __device__ __forceinline__ Smem layout(unsigned char* dsm, const LayerState& s) 
   m.cand_key = m.evw + s.ev_words;
   m.cand_blk = reinterpret_cast<int32_t*>(m.cand_key + kMaxScoreCluster * s.k_q);
   int32_t* eblk = m.cand_blk + kMaxScoreCluster * s.k_q;  // [nb_max] (reserved)
-  m.flags = reinterpret_cast<uint8_t*>(eblk + s.nb_max);
+  m.lu = eblk + s.nb_max;
+  m.flags = reinterpret_cast<uint8_t*>(m.lu + s.cslots);
   return m;
 }
 
@@ -257,7 +263,7 @@ __device__ __forceinline__ void load_q(uint4 (&qf)[4], const uint16_t* q, int u,
 // Leader only, before phase 1: request the selection's inputs as asynchronous copies
 // into shared memory (waited for with cp_async_wait_all before leader_select).
 // Pooled s^e is read for blocks below nb_se only.
-// Returns this thread's cache slot's block (thread index < cap), or -1.
+// Returns this thread's cache slot's block (thread index < cslots), or -1.
 __device__ __forceinline__ int leader_prefetch(const LayerState& s, int u, int nb, int nb_se, const Smem& m) {
   const int tid = threadIdx.x;
   float* sek = m.sek;
@@ -277,8 +283,10 @@ __device__ __forceinline__ int leader_prefetch(const LayerState& s, int u, int n
     cp_async_4(smem_u32(b2s + b), b2g + b);
   }
   for (int w = tid; w < (nb + 31) / 32; w += blockDim.x) cp_async_4(smem_u32(evw + w), evg + w);
+  const int32_t* lug = s.last_used + (size_t)u * s.cslots;
+  for (int sl = tid; sl < s.cslots; sl += blockDim.x) cp_async_4(smem_u32(m.lu + sl), lug + sl);
   cp_async_commit();
-  return tid < s.cap ? s.slot_blk[(size_t)u * s.cap + tid] : -1;
+  return tid < s.cslots ? s.slot_blk[(size_t)u * s.cslots + tid] : -1;
 }
 
 // Phase 1: this CTA's window logits z (shared memory) and per-head statistics.  Each
@@ -588,8 +596,21 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
       ++nel;
     }
   }
+  // the previous selection's context length: the latest one any cache slot served (-1: none)
+  const int my_lu = tid < s.cslots ? m.lu[tid] : -1;
+  {
+    const int v = warp_max(my_lu);
+    if (lane == 0) sh.lumax[warp] = v;
+  }
   int n_elig;
-  int epos = block_scan_excl(nel, sh.scan, &n_elig);
+  int epos = block_scan_excl(nel, sh.scan, &n_elig);  // its barriers also publish lumax
+  int T_prev = -1;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) T_prev = max(T_prev, sh.lumax[w]);
+  // a block of the previous selection holds a slot that served it then
+  auto in_prev = [&](int b) {
+    const int sl = b2s[b];
+    return T_prev >= 0 && sl >= 0 && sl < s.cslots && m.lu[sl] == T_prev;
+  };
   if (n_elig <= s.k_e) {
     for (int b = lo; b < hi; ++b)
       if (flags[b] & F_ELIG) flags[b] |= F_E;
@@ -624,7 +645,7 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
     }
     if (f & (F_Q | F_E)) {
       ++nD;
-      if (f & F_NEW) ++nDnew;
+      if (!in_prev(b)) ++nDnew;
     }
     if (f & F_E) ++nE;
     flags[b] = f;
@@ -637,24 +658,44 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
         __ballot_sync(0xffffffffu, b < nb && (flags[b] & F_CAND) && !(flags[b] & (F_Q | F_E)));
     if (writer && lane == 0 && (bits & ~evw[w])) s.evicted[(size_t)u * s.ev_words + w] = evw[w] | bits;
   }
-  // one scan of three counts (each at most 256, 10 bits apiece): free slots (empty, or holding a
-  // block that left the selection; ascending), blocks without a slot, and selected blocks
-  int32_t* sblk = s.slot_blk + (size_t)u * s.cap;
-  const int is_free = tid < s.cap && !(my_slot_blk >= 0 && my_slot_blk < nb && (flags[my_slot_blk] & F_S));
+  // one scan of three counts (each at most 256, 10 bits apiece): cache slots open to new blocks
+  // (empty, or holding a block outside the selection), blocks without a slot, selected blocks
+  int32_t* sblk = s.slot_blk + (size_t)u * s.cslots;
+  const bool own = tid < s.cslots;
+  const bool holds_sel = own && my_slot_blk >= 0 && my_slot_blk < nb && (flags[my_slot_blk] & F_S);
+  const int is_open = (own && !holds_sel) ? 1 : 0;
   int packed_total;
-  const int packed = block_scan_excl(is_free | (nNew << 10) | (nS << 20), sh.scan, &packed_total);
-  const int free_rank = packed & 1023, n_free = packed_total & 1023;
+  const int packed = block_scan_excl(is_open | (nNew << 10) | (nS << 20), sh.scan, &packed_total);
+  const int n_open = packed_total & 1023;
   const int new_before = (packed >> 10) & 1023, n_new_all = (packed_total >> 10) & 1023;
   int new_rank = new_before, n_new = n_new_all;
   int pos = packed >> 20;
   const int total_S = packed_total >> 20;
-  if (is_free) sh.free_by_rank[free_rank] = tid;
-  if (n_new > n_free) {  // cannot happen when cap >= |S|; guard the slot table anyway
+  if (n_new > n_open) {  // cannot happen when the cache holds a whole selection; guard the tables anyway
     if (writer && tid == 0) atomicOr(s.err, kErrBounds);
-    n_new = n_free;
+    n_new = n_open;
   }
+  // the open slots the new blocks take: every one when there are as many, else the n_new least
+  // recently selected (an empty slot counts as never selected; ties to the lower slot); the
+  // others keep their blocks for later steps.  They are taken in ascending slot order.
+  bool take = is_open && n_new > 0;
+  int take_rank = packed & 1023;  // this slot's rank among the open ones
+  if (n_new > 0 && n_new < n_open) {
+    const uint32_t key = ((uint32_t)(my_lu + 1) << 9) | (uint32_t)tid;
+    if (own) sh.okey[tid] = is_open ? key : 0xFFFFFFFFu;
+    __syncthreads();
+    if (is_open) {
+      int r = 0;
+#pragma unroll 8
+      for (int j = 0; j < s.cslots; ++j) r += sh.okey[j] < key ? 1 : 0;
+      take = r < n_new;
+    }
+    int n_take;
+    take_rank = block_scan_excl(take ? 1 : 0, sh.scan, &n_take);
+  }
+  if (take) sh.free_by_rank[take_rank] = tid;
   int32_t* b2s_g = s.blk2slot + (size_t)u * s.nb_max;
-  if (writer && is_free && my_slot_blk >= 0) {
+  if (writer && take && my_slot_blk >= 0) {  // the block replaced in this slot is no longer cached
     if (my_slot_blk < s.nb_max) b2s_g[my_slot_blk] = -1;
     else atomicOr(s.err, kErrBounds);
   }
@@ -674,7 +715,8 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
     }
     ++new_rank;
   }
-  if (writer && is_free && free_rank >= n_new) sblk[tid] = -1;
+  // every slot that now holds a selected block served this selection
+  if (writer && (holds_sel || take)) s.last_used[(size_t)u * s.cslots + tid] = geo.T;
   // ascending selection list with kinds, slots and the fetched marks (a thread's own blocks:
   // their slots were assigned just above by the same thread)
   int32_t* sel = s.sel + (size_t)u * s.cap;
@@ -687,7 +729,7 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
     if (!(f & F_S)) continue;
     const bool isnew = f & F_NEW;
     if (pos < s.cap) {
-      const int slot = (s.test_bad_slot && u == 0 && pos == 0) ? s.cap : b2s[b];  // test hook
+      const int slot = (s.test_bad_slot && u == 0 && pos == 0) ? s.cslots : b2s[b];  // test hook
       const int kd = (f & F_Q) ? 2 : (f & F_E) ? 3 : (b < geo.ns ? 0 : 1);
       if (writer) {
         sel[pos] = b;
@@ -709,8 +751,8 @@ __device__ __forceinline__ int leader_rest(const LayerState& s, int u, const Geo
     sslot[i] = -1;
     snew[i] = 0;
   }
-  // unit totals: |D|, |D \ S_prev|, |E|, whether any block was resident before
-  int4 v = make_int4(nD, nDnew, nE, (tid < s.cap && my_slot_blk >= 0) ? 1 : 0);
+  // unit totals: |D|, |D \ S_prev|, |E|, whether there was a previous selection
+  int4 v = make_int4(nD, nDnew, nE, T_prev >= 0 ? 1 : 0);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     v.x += __shfl_xor_sync(0xffffffffu, v.x, o);

@@ -47,13 +47,14 @@ class nosa_config(ctypes.Structure):
                 ("score_ctas", ctypes.c_int32), ("attend_blocks_per_cta", ctypes.c_int32),
                 ("attend_merge", ctypes.c_int32), ("decode_cluster", ctypes.c_int32),
                 ("decode_teams", ctypes.c_int32), ("decode_stages", ctypes.c_int32),
-                ("forecast_streams", ctypes.c_int32)]
+                ("forecast_streams", ctypes.c_int32), ("cache_slots", ctypes.c_int32)]
 
 
 class nosa_sizes(ctypes.Structure):
     _fields_ = [("units_per_layer", ctypes.c_int32), ("group", ctypes.c_int32), ("cache_slots", ctypes.c_int32),
                 ("max_blocks", ctypes.c_int32), ("max_windows", ctypes.c_int32), ("evict_words", ctypes.c_int32),
-                ("host_store_bytes", ctypes.c_uint64), ("device_state_bytes", ctypes.c_uint64)]
+                ("host_store_bytes", ctypes.c_uint64), ("device_state_bytes", ctypes.c_uint64),
+                ("select_slots", ctypes.c_int32), ("pad_", ctypes.c_int32)]
 
 
 class nosa_stats(ctypes.Structure):
@@ -65,7 +66,8 @@ class nosa_stats(ctypes.Structure):
 
 class nosa_state_view(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("sel", "sel_kind", "sel_slot", "n_sel", "fetch", "n_fetch",
-                                               "slot_blk", "evicted", "kt", "se_win", "se_blk", "gamma")]
+                                               "slot_blk", "evicted", "kt", "se_win", "se_blk", "gamma",
+                                               "last_used")]
 
 
 class NosaError(RuntimeError):
@@ -156,11 +158,11 @@ def make_config(*, num_layers, batch, num_q_heads, num_kv_heads, k_q, k_e, windo
                 head_dim=128, block_size=64, cmp_kernel=32, cmp_stride=16, sink_blocks=1, evict_hidden=128,
                 gather_ctas=0, softmax_scale=0.0, flags=0, score_ctas=0, attend_blocks_per_cta=0,
                 attend_merge=0, decode_cluster=0, decode_teams=0, decode_stages=0,
-                forecast_streams=0) -> nosa_config:
+                forecast_streams=0, cache_slots=0) -> nosa_config:
     return nosa_config(ctypes.sizeof(nosa_config), num_layers, batch, num_q_heads, num_kv_heads, head_dim,
                        block_size, cmp_kernel, cmp_stride, k_q, k_e, sink_blocks, window_tokens, max_context,
                        evict_hidden, gather_ctas, softmax_scale, flags, score_ctas, attend_blocks_per_cta,
-                       attend_merge, decode_cluster, decode_teams, decode_stages, forecast_streams)
+                       attend_merge, decode_cluster, decode_teams, decode_stages, forecast_streams, cache_slots)
 
 
 # ------------------------------------------------------------------ entry points

@@ -122,7 +122,8 @@ class Parity:
                 V[b, g] = torch.from_numpy(x["V"][:T0].view(np.int16)).view(torch.bfloat16).to(self.dev)
                 o = O.UnitOracle(head_dim=d, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
                                  window_tokens=wl.window_tokens, max_context=wl.max_context,
-                                 W1=W1[g], W2=W2[g], dma_bias=bool(self.flags & N.NOSA_F_DMA_BIAS))
+                                 W1=W1[g], W2=W2[g], dma_bias=bool(self.flags & N.NOSA_F_DMA_BIAS),
+                                 cache_slots=self.sizes.cache_slots)
                 o.append(x["K"][:T0], x["V"][:T0])
                 self.oracles[(l, b, g)] = o
             N.nosa_append_kv(self.ctx, l, K.view(torch.int16), V.view(torch.int16), T0)
@@ -246,12 +247,13 @@ class Parity:
 
     # ------------------------------------------------------------------ comparison
     def _export(self, l):
-        U, cap, sz = self.U, self.sizes.cache_slots, self.sizes
+        U, cap, cs, sz = self.U, self.sizes.select_slots, self.sizes.cache_slots, self.sizes
         nc = max(sz.max_windows, 1)
         st = dict(sel=np.zeros((U, cap), np.int32), sel_kind=np.zeros((U, cap), np.int32),
                   sel_slot=np.zeros((U, cap), np.int32), n_sel=np.zeros(U, np.int32),
                   fetch=np.zeros((U, cap, 2), np.int32), n_fetch=np.zeros(U, np.int32),
-                  slot_blk=np.zeros((U, cap), np.int32), evicted=np.zeros((U, sz.evict_words), np.uint32),
+                  slot_blk=np.zeros((U, cs), np.int32), last_used=np.zeros((U, cs), np.int32),
+                  evicted=np.zeros((U, sz.evict_words), np.uint32),
                   kt=np.zeros((U, nc, self.d), np.uint16), se_blk=np.zeros((U, sz.max_blocks), np.float32),
                   gamma=np.zeros((U, 2), np.int32))
         self.N.nosa_export_state(self.ctx, l, **st)
@@ -326,6 +328,7 @@ class Parity:
             nf = st["n_fetch"][u]
             assert [tuple(x) for x in st["fetch"][u, :nf]] == [tuple(x) for x in r["fetch"]], "fetch list mismatch"
             assert list(st["slot_blk"][u]) == o.slot_blk, "slot map mismatch"
+            assert list(st["last_used"][u]) == o.last_used, "slot recency mismatch"
             ev = st["evicted"][u]
             ev_gpu = {bb for bb in range(nb) if (ev[bb >> 5] >> (bb & 31)) & 1}
             assert ev_gpu == o.evicted, "eviction bitmap mismatch"

@@ -49,7 +49,7 @@ def test_validate_config():
            dict(k_q=200, k_e=100), dict(batch=4097, num_kv_heads=1, num_q_heads=8), dict(softmax_scale=-1.0),
            dict(score_ctas=9), dict(score_ctas=-1), dict(attend_blocks_per_cta=65), dict(attend_merge=4),
            dict(decode_cluster=9), dict(decode_teams=3), dict(decode_stages=1), dict(decode_stages=7),
-           dict(forecast_streams=3)]
+           dict(forecast_streams=3), dict(cache_slots=20), dict(cache_slots=257)]
     for b in bad:
         assert N.nosa_validate_config(_cfg(**b)) == N.NOSA_ERR_INVALID_ARG, b
     c = _cfg()
@@ -60,7 +60,8 @@ def test_validate_config():
 def test_sizing_overrides_are_accepted():
     good = [dict(score_ctas=1), dict(score_ctas=8), dict(attend_blocks_per_cta=1), dict(attend_blocks_per_cta=64),
             dict(attend_merge=N.NOSA_MERGE_TICKET), dict(attend_merge=N.NOSA_MERGE_CLUSTER),
-            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1)]
+            dict(decode_cluster=2), dict(decode_teams=1), dict(decode_stages=6), dict(forecast_streams=1),
+            dict(cache_slots=21), dict(cache_slots=256)]
     for g in good:
         assert N.nosa_validate_config(_cfg(**g)) == N.NOSA_OK, g
 
@@ -76,7 +77,9 @@ def test_test_hook_flags_are_accepted():
 def test_query_sizes_closed_forms():
     s = N.nosa_query_sizes(_cfg())
     assert s.units_per_layer == 6 and s.group == 8
-    assert s.cache_slots == 1 + 4 + 4 + 12
+    assert s.select_slots == 1 + 4 + 4 + 12
+    assert s.cache_slots == 2 * s.select_slots  # the rule: twice a selection
+    assert N.nosa_query_sizes(_cfg(cache_slots=21)).cache_slots == 21
     assert s.max_blocks == -(-5000 // 64) and s.max_windows == (5000 - 32) // 16 + 1
     assert s.evict_words == -(-s.max_blocks // 32)
     # one block of K plus V is 2 x 16 KiB (the transfer unit on the NOSA wiki)

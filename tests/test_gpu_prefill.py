@@ -8,8 +8,8 @@ one launch.  Compared: every checked position's selection (its query-aware and
 query-agnostic picks, returned as bitmaps, with the sink and window blocks)
 bit-exact, near ties logged and adopted as in the decode tests; outputs within
 max-abs 2e-2 / mean-abs 2e-3 and the tighter relative bound; the layer's state
-after the prompt (compressed keys, eviction bitmap, slot map, last selection and
-fetch list) bit-exact; then a few decode steps continue from that state, which
+after the prompt (compressed keys, eviction bitmap, last selection; the cache holding
+exactly that selection, block i in slot i) bit-exact; then a few decode steps continue from that state, which
 checks the cache the prefill leaves behind.
 """
 import math
@@ -78,7 +78,7 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
     ties, max_err = [], 0.0
     try:
         sz = N.nosa_query_sizes(cfg)
-        cap = sz.cache_slots
+        cap, cs = sz.select_slots, sz.cache_slots
         xs = {(b, g): wl.unit_inputs(0, b, g) for b in range(B) for g in range(Hkv)}
         W1 = np.stack([xs[(0, g)]["W1"] for g in range(Hkv)]).astype(np.float32)
         W2 = np.stack([xs[(0, g)]["W2"] for g in range(Hkv)]).astype(np.float32)
@@ -103,7 +103,8 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
         picks = np.unpackbits(picks.view(np.uint8), axis=-1, bitorder="little").astype(bool)  # [2][U][n][32 W]
         out_h = out.float().cpu().numpy()
         st = dict(sel=np.zeros((U, cap), np.int32), n_sel=np.zeros(U, np.int32), fetch=np.zeros((U, cap, 2), np.int32),
-                  n_fetch=np.zeros(U, np.int32), slot_blk=np.zeros((U, cap), np.int32),
+                  n_fetch=np.zeros(U, np.int32), slot_blk=np.zeros((U, cs), np.int32),
+                  last_used=np.zeros((U, cs), np.int32),
                   evicted=np.zeros((U, sz.evict_words), np.uint32),
                   kt=np.zeros((U, max(sz.max_windows, 1), d), np.uint16))
         N.nosa_export_state(ctx, 0, **st)
@@ -116,7 +117,7 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
             x = xs[(b, g)]
             o = O.UnitOracle(head_dim=d, k_q=wl.k_q, k_e=wl.k_e, sink_blocks=wl.sink_blocks,
                              window_tokens=wl.window_tokens, max_context=n + decode_steps, W1=x["W1"], W2=x["W2"],
-                             dma_bias=bool(flags & N.NOSA_F_DMA_BIAS))
+                             dma_bias=bool(flags & N.NOSA_F_DMA_BIAS), cache_slots=cs)
             se_full = None
             if score_positions is not None:
                 assert wl.window_tokens >= 2 * 64
@@ -151,11 +152,14 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
                 if t in out_positions:
                     ref = o.attend(x["Q"][t], r["S"])
                     max_err = max(max_err, _check_out(out_h[b, g * G:(g + 1) * G, t], ref, f"unit {u} position {t}"))
-            # the state after the prompt
+            # the state after the prompt: the cache holds the last selection, block i in slot i,
+            # nothing left to fetch
+            o.settle_cache()
             assert np.array_equal(st["kt"][u, :o.nc], O.f64_to_bf16_bits(o.compressed_keys())), "K~"
             assert list(st["sel"][u, :st["n_sel"][u]]) == r["S"]
             assert list(st["slot_blk"][u]) == o.slot_blk, "slot map"
-            assert [tuple(f) for f in st["fetch"][u, :st["n_fetch"][u]]] == [tuple(f) for f in r["fetch"]]
+            assert list(st["last_used"][u]) == o.last_used, "slot recency"
+            assert st["n_fetch"][u] == 0
             ev = st["evicted"][u]
             assert {bb for bb in range(o.nb) if (ev[bb >> 5] >> (bb & 31)) & 1} == o.evicted, "eviction bitmap"
             oracles[(b, g)] = o

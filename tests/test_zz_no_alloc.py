@@ -40,6 +40,7 @@ def test_noalloc_attend_matches_the_oracle_twice():
     G, U = Hq // Hkv, B * Hkv
     cfg = N.make_config(num_layers=1, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=4, k_e=12,
                         window_tokens=256, max_context=T0 + steps)
+    cfg.cache_slots = N.nosa_query_sizes(cfg).select_slots  # a cache of one selection: the entry point's layout
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     try:
