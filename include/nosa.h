@@ -365,11 +365,13 @@ size_t nosa_dense_scratch_bytes(int units, int context_len);
  * selection for prompt position t is the one the decode step at T = t + 1 makes, with the
  * eviction state carried from position t - 1.  The query-aware picks of all positions are made
  * at once (they do not depend on that state); one warp per unit then walks the positions in
- * order for the query-agnostic picks, the eviction update and the slot pairing; the attention
- * of all positions runs in one launch, reading the prompt's K/V from k and v.  Afterwards the
- * layer's state (host store, compressed keys, scores, eviction bitmap,
- * cache slots and their contents, last selection, counters) is the state n_tokens calls of
- * nosa_step with the same tokens would leave, and decoding continues with nosa_step.
+ * order for the query-agnostic picks and the eviction update; the attention of all positions
+ * runs in one launch, reading the prompt's K/V from k and v.  Afterwards the layer's selection
+ * state (host store, compressed keys, scores, eviction bitmap, last selection, the selection
+ * and locality counters) is the state n_tokens calls of nosa_step with the same tokens would
+ * leave; the block cache holds exactly the last selection, its i-th block (ascending) in slot i,
+ * each marked as selected at T = n_tokens, with nothing left to fetch (the prompt's blocks never
+ * cross the host link, so blocks_fetched does not grow).  Decoding continues with nosa_step.
  *   q, out   device bf16 [B][Hq][n_tokens][d] (out[b][h][t] is position t's attention output)
  *   k, v     device bf16 [B][Hkv][n_tokens][d]; q, k and v 16-byte aligned
  *   scratch  device memory of at least nosa_prefill_scratch_bytes(ctx, n_tokens) bytes, 16-byte

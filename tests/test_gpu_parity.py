@@ -162,6 +162,10 @@ SIZING = [
     (dict(decode_teams=1), FUSED, None),
     (dict(decode_stages=2), FUSED, None),
     (dict(decode_teams=1, decode_stages=6), FUSED, None),
+    (dict(cache_slots=21), FUSED, None),      # a cache of one selection (the pages' cache)
+    (dict(cache_slots=21), UNFUSED, (3, 0)),
+    (dict(cache_slots=64), FUSED, None),      # three selections' worth: fewer fetches still
+    (dict(cache_slots=256), UNFUSED, (3, 0)),
 ]
 
 
