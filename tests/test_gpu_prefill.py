@@ -60,7 +60,7 @@ def _select_and_adopt(o, sq, se, T, Q_gpu, E_gpu, k_q, k_e, ties, where):
     return Q, E
 
 
-def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, score_positions=None):
+def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, score_positions=None, cache_slots=0):
     """Prefill n tokens into an empty layer, check against the oracle, then decode_steps steps.
 
     score_positions (long prompts): the positions where the oracle forms its own query-aware
@@ -72,7 +72,7 @@ def run_prefill(wl, n, check_units, out_positions, flags=0, decode_steps=3, scor
     assert n + decode_steps <= wl.steps and wl.context == 0
     cfg = N.make_config(num_layers=1, batch=B, num_q_heads=Hq, num_kv_heads=Hkv, k_q=wl.k_q, k_e=wl.k_e,
                         window_tokens=wl.window_tokens, max_context=n + decode_steps, sink_blocks=wl.sink_blocks,
-                        evict_hidden=wl.evict_hidden, flags=flags)
+                        evict_hidden=wl.evict_hidden, flags=flags, cache_slots=cache_slots)
     stream = torch.cuda.current_stream()
     ctx = N.nosa_create(cfg, stream.cuda_stream)
     ties, max_err = [], 0.0
@@ -215,6 +215,15 @@ def test_prefill_640_every_position(mode, tile):
                       window_tokens=128, steps=644, sigma=0.3)
     units = [(b, g) for b in range(2) for g in range(2)]
     run_prefill(wl, 640, units, set(range(640)), flags=mode | tile, decode_steps=4)
+
+
+def test_prefill_with_a_cache_of_one_selection():
+    # the pages' cache size (sink + window + k_q + k_e slots): the same state after the prompt,
+    # and the decode steps after it replace exactly the slots whose blocks left the selection
+    wl = syn.Workload("pf640c", layers=1, batch=2, q_heads=16, kv_heads=2, context=0, k_q=1, k_e=2,
+                      window_tokens=128, steps=650, sigma=0.3)
+    units = [(b, g) for b in range(2) for g in range(2)]
+    run_prefill(wl, 640, units, set(range(0, 640, 7)), decode_steps=8, cache_slots=1 + 2 + 1 + 2)
 
 
 @TILE
