@@ -877,7 +877,8 @@ def run_reference(args):
     per_step = max(2.0, min(8.0, 150.0 / max(args.steps + args.warmup, 1)))
     base = oracle_baseline(wl, per_step * (args.steps + args.warmup), U)
     return {"impl": "reference", "metric": METRIC, "value": base["value"], "unit": "tok/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.batch / base["value"],
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl, args, args.layers or wl.layers, 1),
             "cpu_baseline": base,
