@@ -773,6 +773,32 @@ def run_dense(args, rank, world, local_rank):
             "kv_resident_gb": kv.numel() * 2 / 1e9}
 
 
+def prompt_queries(B, Hq, n, d, sigma, gen, device):
+    """bf16 [B][Hq][n][d] prompt queries, correlated along the positions as the decode steps'
+    random walk q_t = normalize(q_{t-1} + sigma N(0, I)) sqrt(d) is (neighbours at cosine
+    1 / sqrt(1 + sigma^2)): a stationary Gaussian sequence p_t = rho p_{t-1} + sqrt(1 - rho^2) e_t,
+    rho = 1 / sqrt(1 + sigma^2), each p_t scaled to norm sqrt(d); stepped in closed form 256
+    positions at a time (one matrix product per chunk, no launch per position)."""
+    import torch
+    rho = 1.0 / math.sqrt(1.0 + sigma ** 2)
+    c = 256
+    i_ = torch.arange(c, device=device, dtype=torch.float32)
+    lag = i_[:, None] - i_[None, :]
+    A = torch.where(lag >= 0, math.sqrt(1.0 - rho * rho) * torch.pow(rho, lag.clamp(min=0)), torch.zeros_like(lag))
+    r = torch.pow(rho, i_ + 1)
+    q = torch.empty((B, Hq, n, d), dtype=torch.bfloat16, device=device)
+    pt = torch.randn((B * Hq * d,), generator=gen, device=device)
+    for t0 in range(0, n, c):
+        m = min(c, n - t0)
+        E = torch.randn((m, B * Hq * d), generator=gen, device=device)
+        P = A[:m, :m] @ E + r[:m, None] * pt[None, :]
+        pt = P[m - 1].clone()
+        Qc = P.view(m, B, Hq, d)
+        Qc = Qc / Qc.norm(dim=-1, keepdim=True) * math.sqrt(d)
+        q[:, :, t0:t0 + m] = Qc.permute(1, 2, 0, 3).to(torch.bfloat16)
+    return q
+
+
 def run_prefill(args, rank, world, local_rank):
     """NOSA_S sparse prefill: a prompt of the workload's context length through every layer (nosa_prefill),
     each timed repetition on a fresh context (a prefill starts from empty layers)."""
@@ -788,28 +814,7 @@ def run_prefill(args, rank, world, local_rank):
     B, Hq, Hkv, d, n = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, wl.context
     U = B * Hkv
     gen = torch.Generator(device="cuda").manual_seed(1000 * rank + 23)
-    # the prompt's queries are correlated along the positions as the decode steps' random walk
-    # q_t = normalize(q_{t-1} + sigma N(0, I)) sqrt(d) is (neighbours at cosine 1 / sqrt(1 + sigma^2)):
-    # a stationary Gaussian sequence p_t = rho p_{t-1} + sqrt(1 - rho^2) e_t, rho = 1 / sqrt(1 + sigma^2),
-    # each p_t scaled to norm sqrt(d); stepped in closed form 256 positions at a time (one matrix
-    # product per chunk, no launch per position)
-    rho = 1.0 / math.sqrt(1.0 + wl.sigma ** 2)
-    c = 256
-    i_ = torch.arange(c, device="cuda", dtype=torch.float32)
-    lag = i_[:, None] - i_[None, :]
-    A = torch.where(lag >= 0, math.sqrt(1.0 - rho * rho) * torch.pow(rho, lag.clamp(min=0)), torch.zeros_like(lag))
-    r = torch.pow(rho, i_ + 1)
-    q = torch.empty((B, Hq, n, d), dtype=torch.bfloat16, device="cuda")
-    pt = torch.randn((B * Hq * d,), generator=gen, device="cuda")
-    for t0 in range(0, n, c):
-        m = min(c, n - t0)
-        E = torch.randn((m, B * Hq * d), generator=gen, device="cuda")
-        P = A[:m, :m] @ E + r[:m, None] * pt[None, :]
-        pt = P[m - 1].clone()
-        Qc = P.view(m, B, Hq, d)
-        Qc = Qc / Qc.norm(dim=-1, keepdim=True) * math.sqrt(d)
-        q[:, :, t0:t0 + m] = Qc.permute(1, 2, 0, 3).to(torch.bfloat16)
-    del A, E, P, Qc
+    q = prompt_queries(B, Hq, n, d, wl.sigma, gen, "cuda")
     k = torch.randn((B, Hkv, n, d), generator=gen, device="cuda").to(torch.bfloat16)
     v = torch.randn((B, Hkv, n, d), generator=gen, device="cuda").to(torch.bfloat16)
     out = torch.empty_like(q)
