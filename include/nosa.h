@@ -323,11 +323,12 @@ nosa_status nosa_forecast_select(nosa_ctx* ctx, int layer, const uint16_t* f);
  * events, so a CUDA graph capture of a sequence of calls stays one graph; call
  * nosa_forecast_join before ending a capture.  Pointers as in nosa_step; f_next:
  * device bf16 [B][Hkv][d].
- * When it pays (measured on GB300 against nosa_step per layer): at small batch, where the
- * step is a latency chain (1B shape, batch 8: +23 %), and where the host link sets the pace
- * (8B shape 32K batch 32: +2-5 %; 1B 64K batch 32: +5 %); not at large batch over a short
- * context (1B 16K batch 128: -7 %), where the next layer's selection reads its compressed
- * keys from HBM beside the attention and costs more than the overlap saves. */
+ * When it pays (measured on GB300 against nosa_step per layer, block cache of twice a
+ * selection): at small batch, where the step is a latency chain (1B shape, 16K, batch 8:
+ * 12.1K against 8.6K tok/s, +40 %); not once the step is bound by HBM (8B shape, 32K, batch 32:
+ * 4.66K against 5.02K, -7 %), where the next layer's selection reads its compressed keys from
+ * HBM beside the attention and costs more than the overlap saves.  (With a cache of one
+ * selection, when the host link set the pace, it also paid at the 8B shape: +2-5 %.) */
 nosa_status nosa_step_forecast(nosa_ctx* ctx, int layer, const uint16_t* q, const uint16_t* k_new,
                                const uint16_t* v_new, uint16_t* out, const uint16_t* f_next, int next_layer);
 
