@@ -79,7 +79,10 @@ def test_query_sizes_closed_forms():
     assert s.units_per_layer == 6 and s.group == 8
     assert s.select_slots == 1 + 4 + 4 + 12
     assert s.cache_slots == 2 * s.select_slots  # the rule: twice a selection
-    assert N.nosa_query_sizes(_cfg(cache_slots=21)).cache_slots == 21
+    one = N.nosa_query_sizes(_cfg(cache_slots=21))
+    assert one.cache_slots == 21 and one.select_slots == 21
+    # each extra cache slot of every (layer, unit): one 32 KiB block, its block id and its last-selection mark
+    assert s.device_state_bytes - one.device_state_bytes == 2 * 6 * (42 - 21) * (32768 + 4 + 4)
     assert s.max_blocks == -(-5000 // 64) and s.max_windows == (5000 - 32) // 16 + 1
     assert s.evict_words == -(-s.max_blocks // 32)
     # one block of K plus V is 2 x 16 KiB (the transfer unit on the NOSA wiki)
